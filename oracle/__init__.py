@@ -1,0 +1,173 @@
+"""CPU oracle (float64) for the state-passing mixer forward and decode update.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, by
+``__graft_entry__.smoke()`` and by the benchmark's CPU-baseline leg, never by
+the product package.  It shares no code with the CUDA path; the only common
+module is ``synth`` (seeded input draws, no method arithmetic).
+
+The arithmetic lives in ``oracle.c`` (plain C, float64, literal loops; see the
+header there for what each function follows).  This module compiles it with
+gcc on first use and marshals numpy arrays.
+
+Functions
+---------
+conv_state_fwd(x, w, bias, S, apply_silu=True) -> (u, F)
+    Causal depthwise conv with an explicit (K-1)-sample state in the
+    extended-sequence form ("Chapter 7: state, chunking and incremental
+    inference", section on defining the state through the extended sequence).
+ssm_scan(u, dt, A, B, C, h0) -> (y, hT)
+    Scalar-decay recurrence h_t = exp(dt_t A_h) h_{t-1} + x_t B_t^T,
+    y_t = h_t C_t ("Understanding and Improving Length Generalization in
+    Recurrent Models", Eq. (1), from a non-zero h_{-1} as in Eq. (4)).
+mixer_update(...) -> (y, conv_pool', ssm_pool', n_skipped)
+    Single/multi-token update over a circular conv-state pool (same chapter,
+    sections on the single-token update, circular mode and continuous
+    batching), followed by the recurrence on the pool's SSM state.
+mixer_fwd(...) -> (y, F, hT)
+    conv_state_fwd then ssm_scan (a segment of the streaming forward).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_dp = ctypes.POINTER(ctypes.c_double)
+_ip = ctypes.POINTER(ctypes.c_int32)
+_L = ctypes.c_long
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c -> _build/liboracle.so (gcc, -O2, no fast-math)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off",
+                               "-std=c11", "-fPIC", "-shared", "-pthread", _SRC,
+                               "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            l = ctypes.CDLL(build())
+            l.orc_conv_state_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _L, _L, _L,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int]
+            l.orc_ssm_scan.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _L, _L, _L,
+                                       _L, _L, _L, ctypes.c_int]
+            l.orc_mixer_update.argtypes = [_dp, _dp, _dp, _dp, _L, _L, _ip, _ip, _dp, _dp,
+                                           _dp, _dp, _dp, _dp, _L, _L, _L, _L, _L, _L,
+                                           ctypes.c_int, ctypes.c_int]
+            l.orc_num_threads.argtypes = [ctypes.c_int]
+            for f in (l.orc_conv_state_fwd, l.orc_ssm_scan, l.orc_mixer_update,
+                      l.orc_num_threads):
+                f.restype = ctypes.c_int
+            _lib = l
+    return _lib
+
+
+def num_threads(nthreads: int = 0) -> int:
+    return int(lib().orc_num_threads(nthreads))
+
+
+def _f64(a) -> np.ndarray:
+    if a is None:
+        return None
+    if hasattr(a, "f64"):
+        a = a.f64()
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _ptr(a):
+    if a is None:
+        return ctypes.cast(None, _dp)
+    return a.ctypes.data_as(_dp)
+
+
+def conv_state_fwd(x, w, bias=None, S=None, apply_silu: bool = True, nthreads: int = 0):
+    """x [Bz, L, D], w [D, K], bias [D] | None, S [Bz, D, K-1] | None.
+
+    Returns u [Bz, L, D] and the final state F [Bz, D, K-1] (float64)."""
+    x, w, bias, S = _f64(x), _f64(w), _f64(bias), _f64(S)
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    u = np.empty((Bz, L, D))
+    F = np.empty((Bz, D, K - 1))
+    rc = lib().orc_conv_state_fwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(S), _ptr(u), _ptr(F),
+                                  Bz, L, D, K, int(bool(apply_silu)), nthreads)
+    if rc != 0:
+        raise ValueError("orc_conv_state_fwd: bad sizes")
+    return u, F
+
+
+def ssm_scan(u, dt, A, B, C, h0=None, nthreads: int = 0):
+    """u [Bz, L, H, P] (or [Bz, L, D]), dt [Bz, L, H], A [H], B/C [Bz, L, G, N],
+    h0 [Bz, H, P, N] | None.  Returns y [Bz, L, H, P] and hT [Bz, H, P, N]."""
+    dt, A, B, C, h0 = _f64(dt), _f64(A), _f64(B), _f64(C), _f64(h0)
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    u = _f64(u).reshape(Bz, L, H, -1)
+    P = u.shape[3]
+    y = np.empty((Bz, L, H, P))
+    hT = np.empty((Bz, H, P, N))
+    rc = lib().orc_ssm_scan(_ptr(u), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0),
+                            _ptr(y), _ptr(hT), Bz, L, H, P, N, G, nthreads)
+    if rc != 0:
+        raise ValueError("orc_ssm_scan: bad sizes")
+    return y, hT
+
+
+def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, nthreads: int = 0):
+    """One segment of the streaming forward: conv (with state) + SiLU, then
+    the scan from h0.  Returns y [Bz, L, H, P], F [Bz, D, K-1], hT."""
+    u, F = conv_state_fwd(x, w, bias, conv_state, True, nthreads)
+    y, hT = ssm_scan(u, dt, A, B, C, h0, nthreads)
+    return y, F, hT
+
+
+def mixer_update(x, w, bias, conv_pool, cache_seqlens, conv_state_indices, dt, A, B, C,
+                 ssm_pool, nthreads: int = 0):
+    """x [Bz, L_new, D]; conv_pool [pool, D, S_len]; cache_seqlens [Bz] int;
+    conv_state_indices [Bz] int | None (identity); dt [Bz, L_new, H]; A [H];
+    B/C [Bz, L_new, G, N]; ssm_pool [pool, H, P, N].
+
+    Returns (y [Bz, L_new, H, P], new conv pool, new SSM pool, n_skipped).
+    The input pools are not modified."""
+    x, w, bias = _f64(x), _f64(w), _f64(bias)
+    dt, A, B, C = _f64(dt), _f64(A), _f64(B), _f64(C)
+    cp = _f64(conv_pool).copy()
+    sp = _f64(ssm_pool).copy()
+    Bz, Lnew, D = x.shape
+    H = dt.shape[2]
+    pool, _, S_len = cp.shape
+    P = D // H
+    G, N = B.shape[2], B.shape[3]
+    K = w.shape[1]
+    sl = np.ascontiguousarray(getattr(cache_seqlens, "data", cache_seqlens), dtype=np.int32)
+    ix = None
+    if conv_state_indices is not None:
+        ix = np.ascontiguousarray(getattr(conv_state_indices, "data", conv_state_indices),
+                                  dtype=np.int32)
+    y = np.empty((Bz, Lnew, H, P))
+    rc = lib().orc_mixer_update(_ptr(x), _ptr(w), _ptr(bias), _ptr(cp), pool, S_len,
+                                sl.ctypes.data_as(_ip),
+                                ix.ctypes.data_as(_ip) if ix is not None else ctypes.cast(None, _ip),
+                                _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(sp), _ptr(y),
+                                Bz, Lnew, H, P, N, G, K, nthreads)
+    if rc < 0:
+        raise ValueError("orc_mixer_update: bad sizes")
+    return y, cp, sp, rc

@@ -1,0 +1,294 @@
+/*
+ * CPU oracle for the state-passing mixer forward and the decode update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the package's smoke check
+ * and the benchmark's CPU-baseline leg may load this library.  The product
+ * path never calls it and shares no code with it.
+ *
+ * Everything is float64, computed literally in the order the method states,
+ * from the exact values of the (bf16 or fp32) inputs, with no intermediate
+ * rounding and no blocking, chunking or reordering:
+ *
+ *   orc_conv_state_fwd  causal depthwise conv with an explicit (K-1)-sample
+ *                       state, in the extended-sequence form of
+ *                       "Chapter 7: state, chunking and incremental inference"
+ *                       (section "define the state with the extended
+ *                       sequence"):  u = [S_0..S_{K-2}, x_0..x_{L-1}],
+ *                       z_t = beta + sum_k w_k u_{t+k},  F = u[L : L+K-1],
+ *                       output SiLU(z) = z / (1 + exp(-z)).
+ *   orc_ssm_scan        the linear recurrence of "Understanding and Improving
+ *                       Length Generalization in Recurrent Models" section 2
+ *                       Eq. (1), h_t = A_t h_{t-1} + B_t x_t, y_t = C_t^T h_t,
+ *                       specialised to one scalar decay per head,
+ *                       A_t = exp(dt_t * A_h), run from the initial state
+ *                       h_{-1} (Eq. (4)'s non-zero initial state), one token
+ *                       at a time.
+ *   orc_mixer_update    the single- and multi-token update of the same
+ *                       chapter (sections "single-token update", "the
+ *                       physical cache can be longer", "circular mode",
+ *                       "continuous batching"): history j of a request at
+ *                       length p is read from slot (p - j) mod S_len, token i
+ *                       is written to slot (p + i) mod S_len after every
+ *                       read, the stored value is the input x (not the
+ *                       output), rows are addressed through
+ *                       conv_state_indices, cache_seqlens is not advanced;
+ *                       then the same recurrence on the pool's SSM state.
+ *
+ * Threads split only independent (batch, channel) / (batch, head) / request
+ * work; each item is computed by one thread in sequential order, so the
+ * result does not depend on the thread count.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+typedef void (*item_fn)(void* ctx, long item);
+
+typedef struct {
+  item_fn fn;
+  void* ctx;
+  long n_items;
+  long tid;
+  long nthreads;
+} worker_arg;
+
+static void* worker_main(void* p) {
+  worker_arg* a = (worker_arg*)p;
+  for (long i = a->tid; i < a->n_items; i += a->nthreads) a->fn(a->ctx, i);
+  return NULL;
+}
+
+static long resolve_threads(int nthreads, long n_items) {
+  long t = nthreads;
+  if (t <= 0) t = sysconf(_SC_NPROCESSORS_ONLN);
+  if (t < 1) t = 1;
+  if (t > n_items) t = n_items;
+  if (t > 256) t = 256;
+  return t < 1 ? 1 : t;
+}
+
+/* run fn(ctx, i) for i in [0, n_items), items interleaved over threads */
+static void parallel_for(long n_items, int nthreads, item_fn fn, void* ctx) {
+  if (n_items <= 0) return;
+  long T = resolve_threads(nthreads, n_items);
+  if (T == 1) {
+    for (long i = 0; i < n_items; ++i) fn(ctx, i);
+    return;
+  }
+  pthread_t th[256];
+  worker_arg args[256];
+  for (long t = 0; t < T; ++t) {
+    args[t].fn = fn;
+    args[t].ctx = ctx;
+    args[t].n_items = n_items;
+    args[t].tid = t;
+    args[t].nthreads = T;
+    pthread_create(&th[t], NULL, worker_main, &args[t]);
+  }
+  for (long t = 0; t < T; ++t) pthread_join(th[t], NULL);
+}
+
+int orc_num_threads(int nthreads) { return (int)resolve_threads(nthreads, 1L << 30); }
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+/* ------------------------------------------------------------------------ */
+/* causal conv with state                                                   */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const double *x, *w, *bias, *S;
+  double *u, *F;
+  long Bz, L, D;
+  int K, act;
+} conv_ctx;
+
+static void conv_item(void* p, long item) {
+  conv_ctx* c = (conv_ctx*)p;
+  const long b = item / c->D, d = item % c->D;
+  const int K = c->K;
+  const long L = c->L, D = c->D, E = L + K - 1;
+  /* the extended sequence u = [S, x] for this (batch, channel) */
+  double* ext = (double*)malloc(sizeof(double) * (size_t)(E > 0 ? E : 1));
+  for (int j = 0; j < K - 1; ++j)
+    ext[j] = c->S ? c->S[(b * D + d) * (K - 1) + j] : 0.0;
+  for (long t = 0; t < L; ++t) ext[K - 1 + t] = c->x[(b * L + t) * D + d];
+  const double beta = c->bias ? c->bias[d] : 0.0;
+  for (long t = 0; t < L; ++t) {
+    double z = beta;
+    for (int k = 0; k < K; ++k) z += c->w[d * K + k] * ext[t + k];
+    c->u[(b * L + t) * D + d] = c->act ? silu(z) : z;
+  }
+  /* final state: the K-1 newest entries of the extended sequence */
+  for (int j = 0; j < K - 1; ++j) c->F[(b * D + d) * (K - 1) + j] = ext[L + j];
+  free(ext);
+}
+
+int orc_conv_state_fwd(const double* x, const double* w, const double* bias,
+                       const double* S, double* u, double* F, long Bz, long L,
+                       long D, int K, int apply_silu, int nthreads) {
+  if (Bz < 0 || L < 0 || D < 0 || K < 1) return -1;
+  conv_ctx c = {x, w, bias, S, u, F, Bz, L, D, K, apply_silu};
+  parallel_for(Bz * D, nthreads, conv_item, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* scalar-decay selective scan from an initial state                        */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const double *u, *dt, *A, *B, *C, *h0;
+  double *y, *hT;
+  long Bz, L, H, P, N, G;
+} scan_ctx;
+
+static void scan_item(void* p, long item) {
+  scan_ctx* c = (scan_ctx*)p;
+  const long H = c->H, P = c->P, N = c->N, G = c->G, L = c->L;
+  const long b = item / H, hd = item % H;
+  const long g = hd / (H / G);
+  double* h = (double*)malloc(sizeof(double) * (size_t)(P * N > 0 ? P * N : 1));
+  for (long i = 0; i < P * N; ++i)
+    h[i] = c->h0 ? c->h0[(b * H + hd) * P * N + i] : 0.0;
+  for (long t = 0; t < L; ++t) {
+    const double a = exp(c->dt[(b * L + t) * H + hd] * c->A[hd]);
+    const double* Bt = c->B + ((b * L + t) * G + g) * N;
+    const double* Ct = c->C + ((b * L + t) * G + g) * N;
+    const double* xt = c->u + ((b * L + t) * H + hd) * P;
+    double* yt = c->y + ((b * L + t) * H + hd) * P;
+    for (long pp = 0; pp < P; ++pp) {
+      double acc = 0.0;
+      for (long n = 0; n < N; ++n) {
+        double v = a * h[pp * N + n] + xt[pp] * Bt[n];
+        h[pp * N + n] = v;
+        acc += v * Ct[n];
+      }
+      yt[pp] = acc;
+    }
+  }
+  if (c->hT)
+    for (long i = 0; i < P * N; ++i) c->hT[(b * H + hd) * P * N + i] = h[i];
+  free(h);
+}
+
+int orc_ssm_scan(const double* u, const double* dt, const double* A,
+                 const double* B, const double* C, const double* h0, double* y,
+                 double* hT, long Bz, long L, long H, long P, long N, long G,
+                 int nthreads) {
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return -1;
+  scan_ctx c = {u, dt, A, B, C, h0, y, hT, Bz, L, H, P, N, G};
+  parallel_for(Bz * H, nthreads, scan_item, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* decode update over a circular conv-state pool                            */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const double *x, *w, *bias, *dt, *A, *B, *C;
+  double *conv_pool, *ssm_pool, *y;
+  const int32_t *seqlens, *idx;
+  long Bz, Lnew, H, P, N, G, pool, S_len;
+  int K;
+  int* bad; /* per row: 1 if the row was skipped */
+} upd_ctx;
+
+static long pos_mod(long a, long m) {
+  long r = a % m;
+  return r < 0 ? r + m : r;
+}
+
+static void upd_item(void* p, long b) {
+  upd_ctx* c = (upd_ctx*)p;
+  const long H = c->H, P = c->P, N = c->N, G = c->G, D = H * P;
+  const long Lnew = c->Lnew, S_len = c->S_len;
+  const int K = c->K;
+  const long r = c->idx ? (long)c->idx[b] : b;
+  const long pl = (long)c->seqlens[b];
+  if (r < 0 || r >= c->pool || pl < 0) {
+    c->bad[b] = 1;
+    for (long i = 0; i < Lnew * D; ++i) c->y[b * Lnew * D + i] = 0.0;
+    return;
+  }
+  double* u = (double*)malloc(sizeof(double) * (size_t)(Lnew * D > 0 ? Lnew * D : 1));
+  double* ext = (double*)malloc(sizeof(double) * (size_t)(K - 1 + Lnew));
+  double* row = c->conv_pool + r * D * S_len;
+  for (long d = 0; d < D; ++d) {
+    /* read every history value this call needs before any slot is written:
+       logical position p - (K-1) + j lives in slot (p - (K-1) + j) mod S_len */
+    for (int j = 0; j < K - 1; ++j)
+      ext[j] = row[d * S_len + pos_mod(pl - (K - 1) + j, S_len)];
+    for (long i = 0; i < Lnew; ++i) ext[K - 1 + i] = c->x[(b * Lnew + i) * D + d];
+    const double beta = c->bias ? c->bias[d] : 0.0;
+    for (long i = 0; i < Lnew; ++i) {
+      double z = beta;
+      for (int k = 0; k < K; ++k) z += c->w[d * K + k] * ext[i + k];
+      u[i * D + d] = silu(z);
+    }
+    /* store the inputs (not the outputs) at the write pointer */
+    for (long i = 0; i < Lnew; ++i)
+      row[d * S_len + pos_mod(pl + i, S_len)] = c->x[(b * Lnew + i) * D + d];
+  }
+  for (long hd = 0; hd < H; ++hd) {
+    const long g = hd / (H / G);
+    double* h = c->ssm_pool + (r * H + hd) * P * N;
+    for (long i = 0; i < Lnew; ++i) {
+      const double a = exp(c->dt[(b * Lnew + i) * H + hd] * c->A[hd]);
+      const double* Bt = c->B + ((b * Lnew + i) * G + g) * N;
+      const double* Ct = c->C + ((b * Lnew + i) * G + g) * N;
+      for (long pp = 0; pp < P; ++pp) {
+        const double xv = u[i * D + hd * P + pp];
+        double acc = 0.0;
+        for (long n = 0; n < N; ++n) {
+          double v = a * h[pp * N + n] + xv * Bt[n];
+          h[pp * N + n] = v;
+          acc += v * Ct[n];
+        }
+        c->y[((b * Lnew + i) * H + hd) * P + pp] = acc;
+      }
+    }
+  }
+  free(ext);
+  free(u);
+}
+
+/* Returns the number of skipped rows (row index outside [0, pool) or a
+   negative length: pools untouched, y row set to zero), or -1 on bad sizes.
+   Rows whose slot appears twice are a caller contract violation; the oracle
+   then applies rows one after another in batch order (single thread). */
+int orc_mixer_update(const double* x, const double* w, const double* bias,
+                     double* conv_pool, long pool, long S_len,
+                     const int32_t* cache_seqlens, const int32_t* idx,
+                     const double* dt, const double* A, const double* B,
+                     const double* C, double* ssm_pool, double* y, long Bz,
+                     long Lnew, long H, long P, long N, long G, int K,
+                     int nthreads) {
+  if (Bz < 0 || Lnew < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G ||
+      K < 1 || S_len < K - 1 || S_len < 1 || pool < 0)
+    return -1;
+  int* bad = (int*)calloc((size_t)(Bz > 0 ? Bz : 1), sizeof(int));
+  int dup = 0;
+  if (idx) {
+    char* seen = (char*)calloc((size_t)(pool > 0 ? pool : 1), 1);
+    for (long b = 0; b < Bz; ++b) {
+      long r = idx[b];
+      if (r >= 0 && r < pool) {
+        if (seen[r]) dup = 1;
+        seen[r] = 1;
+      }
+    }
+    free(seen);
+  }
+  upd_ctx c = {x, w, bias, dt, A, B, C, conv_pool, ssm_pool, y, cache_seqlens, idx,
+               Bz, Lnew, H, P, N, G, pool, S_len, K, bad};
+  parallel_for(Bz, dup ? 1 : nthreads, upd_item, &c);
+  int nbad = 0;
+  for (long b = 0; b < Bz; ++b) nbad += bad[b];
+  free(bad);
+  return nbad;
+}

@@ -1,0 +1,367 @@
+"""Pins of the CPU oracle to facts fixed by the pages and by mathematics.
+
+Each test checks the oracle against something other than itself: a worked
+example printed on a page (fixtures under tests/golden/, each with its
+source), a closed form, a textbook routine (numpy convolve / cumsum), the
+unrolled form of the recurrence (Eq. (4) of "Understanding and Improving
+Length Generalization in Recurrent Models"), or an invariant the pages state
+(segment equivalence under state passing, superposition of the initial
+state).  No GPU is used.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+def silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+def _load(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------------------
+# conv with state
+# ---------------------------------------------------------------------------
+
+def test_conv_worked_example_k4(golden_dir):
+    """K=4, S=[a,b,c], x=[d]: the window is [a,b,c,d] and F=[b,c,d]."""
+    ex = _load(golden_dir, "conv_state_examples.json")["examples"][0]
+    K = ex["K"]
+    S = np.array(ex["S"]).reshape(1, 1, K - 1)
+    x = np.array(ex["x"]).reshape(1, 1, 1)
+    w = np.array(ex["w"]).reshape(1, K)
+    bias = np.array([ex["bias"]])
+    u, F = oracle.conv_state_fwd(x, w, bias, S, apply_silu=False)
+    np.testing.assert_array_equal(F.reshape(-1), ex["F"])
+    assert not np.array_equal(F.reshape(-1), ex["wrong_F_zero_padded"])
+    z = ex["bias"] + float(np.dot(ex["w"], ex["window"]))
+    assert u.reshape(-1)[0] == z
+    # with the activation: SiLU of the same pre-activation
+    u2, _ = oracle.conv_state_fwd(x, w, bias, S, apply_silu=True)
+    assert u2.reshape(-1)[0] == pytest.approx(silu(z), rel=1e-15)
+
+
+def test_conv_worked_example_k3(golden_dir):
+    """K=3, S=[a,b], x=[c]: z = beta + w0 a + w1 b + w2 c and F = [b, c]."""
+    ex = _load(golden_dir, "conv_state_examples.json")["examples"][1]
+    K = ex["K"]
+    u, F = oracle.conv_state_fwd(np.array(ex["x"]).reshape(1, 1, 1),
+                                 np.array(ex["w"]).reshape(1, K),
+                                 np.array([ex["bias"]]),
+                                 np.array(ex["S"]).reshape(1, 1, K - 1), apply_silu=False)
+    assert u.reshape(-1)[0] == ex["z"]
+    np.testing.assert_array_equal(F.reshape(-1), ex["F"])
+
+
+@pytest.mark.parametrize("K,L", [(4, 37), (4, 1), (4, 2), (4, 3), (3, 9), (2, 5), (6, 4)])
+def test_conv_matches_numpy_convolve(K, L):
+    """Brute force: numpy's textbook convolution over the extended sequence."""
+    g = np.random.default_rng(7 + K * 100 + L)
+    Bz, D = 2, 5
+    x = g.standard_normal((Bz, L, D))
+    S = g.standard_normal((Bz, D, K - 1))
+    w = g.standard_normal((D, K))
+    bias = g.standard_normal(D)
+    u, F = oracle.conv_state_fwd(x, w, bias, S)
+    for b in range(Bz):
+        for d in range(D):
+            ext = np.concatenate([S[b, d], x[b, :, d]])
+            z = bias[d] + np.convolve(ext, w[d][::-1], mode="valid")
+            np.testing.assert_allclose(u[b, :, d], silu(z), rtol=1e-13, atol=1e-15)
+            np.testing.assert_array_equal(F[b, d], ext[len(ext) - (K - 1):])
+
+
+def test_conv_without_state_is_zero_padding():
+    """No initial state means S = 0."""
+    g = np.random.default_rng(3)
+    x = g.standard_normal((1, 6, 3))
+    w = g.standard_normal((3, 4))
+    u0, F0 = oracle.conv_state_fwd(x, w, None, None)
+    u1, F1 = oracle.conv_state_fwd(x, w, np.zeros(3), np.zeros((1, 3, 3)))
+    np.testing.assert_array_equal(u0, u1)
+    np.testing.assert_array_equal(F0, F1)
+
+
+def test_conv_k1_is_pointwise_affine():
+    g = np.random.default_rng(4)
+    x = g.standard_normal((2, 7, 3))
+    w = g.standard_normal((3, 1))
+    bias = g.standard_normal(3)
+    u, F = oracle.conv_state_fwd(x, w, bias, None)
+    np.testing.assert_allclose(u, silu(bias + x * w[:, 0]), rtol=1e-14)
+    assert F.shape == (2, 3, 0)
+
+
+def test_conv_empty_sequence_keeps_state():
+    g = np.random.default_rng(5)
+    S = g.standard_normal((2, 3, 3))
+    u, F = oracle.conv_state_fwd(np.zeros((2, 0, 3)), g.standard_normal((3, 4)), None, S)
+    assert u.shape == (2, 0, 3)
+    np.testing.assert_array_equal(F, S)
+
+
+# ---------------------------------------------------------------------------
+# the recurrence
+# ---------------------------------------------------------------------------
+
+def _scan_case(g, Bz=2, L=11, H=4, P=3, N=5, G=2, h0=True):
+    u = g.standard_normal((Bz, L, H, P))
+    dt = np.log1p(np.exp(g.standard_normal((Bz, L, H)) - 1.0))
+    A = -g.uniform(0.05, 1.0, H)
+    B = g.standard_normal((Bz, L, G, N))
+    C = g.standard_normal((Bz, L, G, N))
+    hh = g.standard_normal((Bz, H, P, N)) if h0 else None
+    return u, dt, A, B, C, hh
+
+
+def test_scan_matches_unrolled_eq4():
+    """Eq. (4): h_t = sum_s (prod_{r=s+1..t} a_r) B_s x_s + (prod_{r=0..t} a_r) h_{-1},
+    y_t = C_t^T h_t, written out as an explicit double sum."""
+    g = np.random.default_rng(11)
+    Bz, L, H, P, N, G = 2, 9, 4, 3, 5, 2
+    u, dt, A, B, C, h0 = _scan_case(g, Bz, L, H, P, N, G)
+    y, hT = oracle.ssm_scan(u, dt, A, B, C, h0)
+    for b in range(Bz):
+        for h in range(H):
+            gi = h // (H // G)
+            a = np.exp(dt[b, :, h] * A[h])
+            for t in range(L):
+                ht = np.prod(a[0:t + 1]) * h0[b, h]
+                for s in range(t + 1):
+                    ht = ht + np.prod(a[s + 1:t + 1]) * np.outer(u[b, s, h], B[b, s, gi])
+                np.testing.assert_allclose(y[b, t, h], ht @ C[b, t, gi], rtol=1e-12, atol=1e-12)
+                if t == L - 1:
+                    np.testing.assert_allclose(hT[b, h], ht, rtol=1e-12, atol=1e-12)
+
+
+def test_scan_impulse_response_is_product_of_later_decays():
+    """An input at s=0 only reaches h_t through a_1 ... a_t (not a_0)."""
+    g = np.random.default_rng(12)
+    L, H = 8, 1
+    dt = g.uniform(0.1, 0.9, (1, L, H))
+    A = np.array([-0.7])
+    u = np.zeros((1, L, H, 1))
+    u[0, 0, 0, 0] = 1.0
+    B = np.ones((1, L, 1, 1))
+    C = np.ones((1, L, 1, 1))
+    y, _ = oracle.ssm_scan(u, dt, A, B, C, None)
+    a = np.exp(dt[0, :, 0] * A[0])
+    expect = [np.prod(a[1:t + 1]) for t in range(L)]
+    np.testing.assert_allclose(y[0, :, 0, 0], expect, rtol=1e-14)
+
+
+def test_scan_no_decay_is_prefix_sum():
+    """A_h = 0 gives a_t = 1: h_t = h0 + cumsum_s x_s B_s^T."""
+    g = np.random.default_rng(13)
+    u, dt, A, B, C, h0 = _scan_case(g, G=1)
+    A = np.zeros_like(A)
+    y, hT = oracle.ssm_scan(u, dt, A, B, C, h0)
+    upd = np.einsum("blhp,bln->blhpn", u, B[:, :, 0, :])
+    h = h0[:, None] + np.cumsum(upd, axis=1)
+    np.testing.assert_allclose(hT, h[:, -1], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(y, np.einsum("blhpn,bln->blhp", h, C[:, :, 0, :]),
+                               rtol=1e-11, atol=1e-11)
+
+
+def test_scan_full_decay_forgets_everything():
+    """exp(dt*A) underflows to 0: h_t = x_t B_t^T, so y_t = x_t (B_t . C_t)."""
+    g = np.random.default_rng(14)
+    u, dt, A, B, C, h0 = _scan_case(g, G=1)
+    A = np.full_like(A, -1e5)
+    y, hT = oracle.ssm_scan(u, dt, A, B, C, h0)
+    bc = np.einsum("bln,bln->bl", B[:, :, 0], C[:, :, 0])
+    np.testing.assert_allclose(y, u * bc[:, :, None, None], rtol=1e-13)
+
+
+def test_scan_initial_state_superposition():
+    """Eq. (4): y(x, h0) = y(x, 0) + C_t^T (prod_{r<=t} a_r) h0."""
+    g = np.random.default_rng(15)
+    u, dt, A, B, C, h0 = _scan_case(g, Bz=2, L=23, H=4, P=3, N=6, G=2)
+    y1, hT1 = oracle.ssm_scan(u, dt, A, B, C, h0)
+    y0, hT0 = oracle.ssm_scan(u, dt, A, B, C, None)
+    H, G = 4, 2
+    for h in range(H):
+        gi = h // (H // G)
+        decay = np.exp(np.cumsum(dt[:, :, h] * A[h], axis=1))  # [Bz, L]
+        corr = np.einsum("bl,bpn,bln->blp", decay, h0[:, h], C[:, :, gi])
+        np.testing.assert_allclose(y1[:, :, h], y0[:, :, h] + corr, rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(hT1[:, h], hT0[:, h] + decay[:, -1, None, None] * h0[:, h],
+                                   rtol=1e-11, atol=1e-11)
+
+
+def test_state_variance_closed_form(golden_dir):
+    """Section 2.4 teaching example: Var(h_t) = (1 - a^{2(t+1)}) / (1 - a^2); at
+    a = 0.99 the state reaches ~47.4% of its stationary variance after 32 tokens
+    and is near-stationary by 512.  Monte-Carlo over independent heads."""
+    ex = _load(golden_dir, "state_variance.json")
+    a = ex["a"]
+    T = ex["tokens"]
+    closed = lambda t: (1 - a ** (2 * (t + 1))) / (1 - a ** 2)
+    stat = 1 / (1 - a ** 2)
+    # the closed form reproduces the printed fraction
+    assert abs(closed(T - 1) / stat - ex["fraction_of_stationary_printed"]) <= ex["printed_precision"]
+    assert closed(ex["tokens_near_stationary"] - 1) / stat > 0.999
+    n = 1 << 16
+    L = ex["tokens_near_stationary"]
+    g = np.random.default_rng(16)
+    u = g.standard_normal((1, L, n, 1))
+    dt = np.ones((1, L, n))
+    A = np.full(n, np.log(a))
+    one = np.ones((1, L, 1, 1))
+    y, _ = oracle.ssm_scan(u, dt, A, one, one, None)
+    for t in (T - 1, L - 1):
+        v = np.mean(y[0, t, :, 0] ** 2)
+        sig = np.sqrt(2.0 / n) * closed(t)
+        assert abs(v - closed(t)) < 4 * sig, (t, v, closed(t))
+
+
+# ---------------------------------------------------------------------------
+# state passing
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("split", [1, 2, 3, 17, 31])
+def test_segment_equivalence(split):
+    """Whole sequence == segment A then segment B started from A's final conv
+    and SSM states (S_B = F_A, h0_B = hT_A)."""
+    g = np.random.default_rng(20 + split)
+    Bz, L, H, P, N, K = 2, 32, 2, 4, 8, 4
+    D = H * P
+    x = g.standard_normal((Bz, L, D))
+    dt = np.log1p(np.exp(g.standard_normal((Bz, L, H)) - 2.0))
+    A = -g.uniform(0.01, 1, H)
+    B = g.standard_normal((Bz, L, 1, N))
+    C = g.standard_normal((Bz, L, 1, N))
+    w = g.normal(0, np.sqrt(0.5), (D, K))
+    bias = np.full(D, 0.1)
+    S0 = g.standard_normal((Bz, D, K - 1))
+    h0 = g.normal(0, 0.1, (Bz, H, P, N))
+    y, F, hT = oracle.mixer_fwd(x, dt, A, B, C, w, bias, S0, h0)
+    sa, sb = slice(0, split), slice(split, L)
+    ya, Fa, ha = oracle.mixer_fwd(x[:, sa], dt[:, sa], A, B[:, sa], C[:, sa], w, bias, S0, h0)
+    yb, Fb, hb = oracle.mixer_fwd(x[:, sb], dt[:, sb], A, B[:, sb], C[:, sb], w, bias, Fa, ha)
+    np.testing.assert_allclose(np.concatenate([ya, yb], axis=1), y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(Fb, F)
+    np.testing.assert_allclose(hb, hT, rtol=1e-12, atol=1e-12)
+
+
+def test_tiny_workload_split_equals_unsplit():
+    """The tiny fp32 workload: 64 tokens as two 32-token segments == unsplit."""
+    s = synth.WORKLOADS["tiny_f32"]
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    segs = [synth.mixer_segment(s, i) for i in range(len(s.segments))]
+    cat = {k: np.concatenate([sg[k].f64() for sg in segs], axis=1) for k in segs[0]}
+    y, F, hT = oracle.mixer_fwd(cat["x"], cat["dt"], p["A"], cat["B"], cat["C"], p["w"],
+                                p["bias"], st["conv_state"], st["h0"])
+    S, h = st["conv_state"].f64(), st["h0"].f64()
+    ys = []
+    for sg in segs:
+        yi, S, h = oracle.mixer_fwd(sg["x"], sg["dt"], p["A"], sg["B"], sg["C"], p["w"],
+                                    p["bias"], S, h)
+        ys.append(yi)
+    np.testing.assert_allclose(np.concatenate(ys, axis=1), y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(S, F)
+    np.testing.assert_allclose(h, hT, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# decode update
+# ---------------------------------------------------------------------------
+
+def test_circular_slot_example(golden_dir):
+    """K=3, S_len=4, p=5: history = logical 3, 4 = slots 3, 0; the new input
+    goes to slot 1.  One channel, one-hot weights pick each history value."""
+    ex = _load(golden_dir, "circular_slots.json")
+    K, S_len, p = ex["K"], ex["S_len"], ex["p"]
+    slots = np.array([1.0, 10.0, 100.0, 1000.0])
+    pool = slots.reshape(1, 1, S_len)
+    xnew = np.array([7.0]).reshape(1, 1, 1)
+    one = np.ones((1, 1, 1, 1))
+    ssm = np.zeros((1, 1, 1, 1))
+    seen = []
+    for k in range(K - 1):  # weight k picks the k-th oldest history value
+        w = np.zeros((1, K))
+        w[0, k] = 1.0
+        # a = exp(-1e5) = 0 and B = C = 1: y equals the conv output
+        y, cp, sp, nbad = oracle.mixer_update(xnew, w, np.zeros(1), pool, np.array([p]),
+                                              np.array([0]), np.ones((1, 1, 1)),
+                                              np.array([-1e5]), one, one, ssm)
+        assert nbad == 0
+        # invert SiLU by matching against the candidate slot values
+        cand = [silu(v) for v in slots]
+        seen.append(int(np.argmin([abs(c - y[0, 0, 0, 0]) for c in cand])))
+        expect_new = slots.copy()
+        expect_new[ex["write_slot"]] = 7.0
+        np.testing.assert_array_equal(cp.reshape(-1), expect_new)
+    assert seen == ex["history_slots"]
+
+
+def _decode_case(g, Bz=3, pool=5, Lnew=2, H=2, P=3, N=4, K=4, S_len=4, G=1):
+    D = H * P
+    return dict(
+        x=g.standard_normal((Bz, Lnew, D)), w=g.standard_normal((D, K)),
+        bias=g.standard_normal(D), conv_pool=g.standard_normal((pool, D, S_len)),
+        cache_seqlens=g.integers(0, 50, Bz).astype(np.int32),
+        conv_state_indices=g.permutation(pool)[:Bz].astype(np.int32),
+        dt=np.log1p(np.exp(g.standard_normal((Bz, Lnew, H)))), A=-g.uniform(0.01, 1, H),
+        B=g.standard_normal((Bz, Lnew, G, N)), C=g.standard_normal((Bz, Lnew, G, N)),
+        ssm_pool=g.standard_normal((pool, H, P, N)))
+
+
+@pytest.mark.parametrize("Lnew,S_len,K", [(1, 3, 4), (1, 4, 4), (4, 4, 4), (6, 4, 4),
+                                          (3, 7, 4), (2, 2, 3), (5, 1, 2)])
+def test_update_equals_forward_from_gathered_state(Lnew, S_len, K):
+    """The update on L_new tokens equals the conv-with-state forward plus the
+    scan, started from the history read out of the circular slots; the slots
+    then hold the newest inputs (x, not y), rows not addressed are untouched."""
+    g = np.random.default_rng(30 + Lnew * 10 + S_len)
+    c = _decode_case(g, Lnew=Lnew, S_len=S_len, K=K)
+    y, cp, sp, nbad = oracle.mixer_update(**c)
+    assert nbad == 0
+    pool = c["conv_pool"]
+    for b, r in enumerate(c["conv_state_indices"]):
+        p = int(c["cache_seqlens"][b])
+        hist = np.stack([pool[r, :, (p - (K - 1) + j) % S_len] for j in range(K - 1)], axis=-1)
+        yb, Fb, hb = oracle.mixer_fwd(c["x"][b:b + 1], c["dt"][b:b + 1], c["A"],
+                                      c["B"][b:b + 1], c["C"][b:b + 1], c["w"], c["bias"],
+                                      hist[None], c["ssm_pool"][r:r + 1])
+        np.testing.assert_allclose(y[b], yb[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(sp[r], hb[0], rtol=1e-12, atol=1e-12)
+        expect = pool[r].copy()
+        for i in range(Lnew):
+            expect[:, (p + i) % S_len] = c["x"][b, i]
+        np.testing.assert_array_equal(cp[r], expect)
+    untouched = np.setdiff1d(np.arange(pool.shape[0]), c["conv_state_indices"])
+    np.testing.assert_array_equal(cp[untouched], pool[untouched])
+    np.testing.assert_array_equal(sp[untouched], c["ssm_pool"][untouched])
+
+
+def test_update_skips_bad_rows():
+    g = np.random.default_rng(40)
+    c = _decode_case(g)
+    c["conv_state_indices"] = np.array([0, 99, 2], np.int32)
+    c["cache_seqlens"] = np.array([3, 4, -1], np.int32)
+    y, cp, sp, nbad = oracle.mixer_update(**c)
+    assert nbad == 2
+    assert np.all(y[1] == 0) and np.all(y[2] == 0)
+    np.testing.assert_array_equal(cp[2], c["conv_pool"][2])
+    assert not np.array_equal(cp[0], c["conv_pool"][0])
+
+
+def test_update_does_not_depend_on_thread_count():
+    g = np.random.default_rng(41)
+    c = _decode_case(g, Bz=4, pool=6)
+    r1 = oracle.mixer_update(nthreads=1, **c)
+    r8 = oracle.mixer_update(nthreads=8, **c)
+    for a, b in zip(r1[:3], r8[:3]):
+        np.testing.assert_array_equal(a, b)
