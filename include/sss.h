@@ -1,0 +1,185 @@
+/*
+ * sss.h -- C ABI of libsss: the state-passing forward of a Mamba-2-style
+ * recurrent mixer (causal depthwise conv with an explicit conv state, then a
+ * scalar-decay selective scan from a non-zero initial state) and its
+ * single/multi-token decode update over a circular conv-state pool, as
+ * hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every tensor pointer is a DEVICE pointer owned by the caller; the library
+ *    keeps no pointer after a call returns and allocates nothing.
+ *  - Tensors are dense and row-major (last index fastest), with the layouts
+ *    given per argument.  Every pointer must be aligned to its element size;
+ *    16-byte alignment of every tensor (and row strides that are multiples of
+ *    16 bytes) selects the vectorised and tensor-core paths.
+ *  - All work is enqueued asynchronously on `stream` (NULL = the legacy
+ *    default stream).  Host-detectable problems (null pointers, sizes,
+ *    dtypes) return a status before anything is launched and leave every
+ *    output untouched.  Problems only the device can see (an out-of-range
+ *    pool row, a negative length, a wait that ran out) are OR-ed into a
+ *    device status word that sss_device_status() reads.
+ *  - Names follow the pages: x input, u conv output, dt step size, A per-head
+ *    decay rate, B/C input/output projections, h SSM state, S/F conv state,
+ *    K conv width, cache_seqlens, conv_state_indices.
+ *
+ * Symbols: Bz batch, L tokens in the call, D = H*P channels, H heads, P head
+ * dimension, N state size, G groups of B/C (H % G == 0, head h uses group
+ * h / (H/G)), K conv width.
+ */
+#ifndef SSS_H_
+#define SSS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime and driver stream handle types are the same). */
+typedef struct CUstream_st* sss_stream_t;
+
+typedef enum {
+  SSS_OK = 0,
+  SSS_ERR_INVALID_ARG = 1, /* null pointer, bad size or dtype; nothing launched */
+  SSS_ERR_UNSUPPORTED = 2, /* valid request this build cannot run             */
+  SSS_ERR_INDEX = 4,       /* device: pool row outside [0,pool) or length < 0  */
+  SSS_ERR_TIMEOUT = 8,     /* device: a bounded wait inside a kernel ran out   */
+  SSS_ERR_CUDA = 16        /* a CUDA runtime call failed (launch, no device)   */
+} sss_status;
+
+typedef enum { SSS_F32 = 0, SSS_BF16 = 1 } sss_dtype;
+
+/* Library version, major*10000 + minor*100 + patch. */
+int sss_version(void);
+
+/* Static string for a status value (bits may be OR-ed together). */
+const char* sss_status_string(int status);
+
+/*
+ * sss_conv_state_fwd -- causal depthwise conv1d with an explicit conv state.
+ *
+ * Source: "Chapter 7: state, chunking and incremental inference" (causal-conv1d
+ * tutorial), section "define the state with the extended sequence": with the
+ * state S holding the K-1 inputs before this call, oldest first, the call
+ * computes over u = [S_0..S_{K-2}, x_0..x_{L-1}]
+ *     z_t = bias + sum_{k<K} w_k u_{t+k},   F = u[L : L+K-1],
+ * and returns SiLU(z) (z / (1 + exp(-z))) when apply_silu != 0, else z.
+ * The form holds for L < K-1 (F then keeps part of S) and L == 0 (F = S).
+ *
+ *  x          [Bz, L, D]   x_dtype
+ *  w          [D, K]       float32
+ *  bias       [D]          float32, NULL = 0
+ *  state_in   [Bz, D, K-1] x_dtype, NULL = zeros (no history)
+ *  state_out  [Bz, D, K-1] x_dtype, receives F; may equal state_in (the
+ *                          streaming case); NULL = do not write F
+ *  u          [Bz, L, D]   u_dtype (SSS_F32 keeps the conv output exact
+ *                          enough for the scan's state; SSS_BF16 halves
+ *                          the bytes)
+ * Returns SSS_ERR_INVALID_ARG for null x/w/u (when L > 0), K < 1, negative
+ * sizes, or an unknown dtype.
+ */
+sss_status sss_conv_state_fwd(const void* x, sss_dtype x_dtype, const float* w,
+                              const float* bias, const void* state_in,
+                              void* state_out, void* u, sss_dtype u_dtype,
+                              int64_t Bz, int64_t L, int64_t D, int K,
+                              int apply_silu, sss_stream_t stream);
+
+/*
+ * sss_ssm_scan_fwd -- scalar-decay selective scan from an initial state.
+ *
+ * Source: "Understanding and Improving Length Generalization in Recurrent
+ * Models", section 2 Eq. (1) h_t = A_t h_{t-1} + B_t x_t, y_t = C_t^T h_t,
+ * with one scalar decay per head A_t = exp(dt_t * A_h), started from a
+ * non-zero initial state h_{-1} as in Eq. (4) (section 4.1), and returning
+ * the final state so a later call can continue (state passing, TBTT).
+ * Per (batch b, head h, channel p, state n):
+ *     h[p,n] <- exp(dt[b,t,h] A[h]) h[p,n] + x[b,t,h,p] B[b,t,g,n]
+ *     y[b,t,h,p] = sum_n h[p,n] C[b,t,g,n]
+ *
+ *  x       [Bz, L, H, P]  x_dtype (the conv output u)
+ *  dt      [Bz, L, H]     act_dtype, already positive (post-softplus)
+ *  A       [H]            float32 (negative for a decaying state)
+ *  B, C    [Bz, L, G, N]  act_dtype
+ *  h0_in   [Bz, H, P, N]  float32, NULL = zeros
+ *  hT_out  [Bz, H, P, N]  float32, may equal h0_in; NULL = do not write
+ *  y       [Bz, L, H, P]  y_dtype
+ *  workspace / workspace_bytes: scratch of at least
+ *          sss_ssm_scan_workspace_size() bytes (may be NULL when that is 0).
+ * bf16 activations with P == 64, N == 128 run on the tcgen05 tensor-core
+ * chunked scan; every other case runs on the fp32 CUDA-core scan.  The
+ * state is kept in fp32 in both.
+ */
+size_t sss_ssm_scan_workspace_size(int64_t Bz, int64_t L, int H, int P, int N,
+                                   int G, sss_dtype x_dtype, sss_dtype act_dtype);
+
+/* Which kernel sss_ssm_scan_fwd picks for these sizes and dtypes (given
+ * 16-byte aligned tensors): 1 = tcgen05 tensor-core chunked scan,
+ * 0 = fp32 CUDA-core scan, -1 = unsupported. */
+int sss_ssm_scan_path(int64_t Bz, int64_t L, int H, int P, int N, int G,
+                      sss_dtype x_dtype, sss_dtype act_dtype, sss_dtype y_dtype);
+
+sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt,
+                            const float* A, const void* B, const void* C,
+                            sss_dtype act_dtype, const float* h0_in,
+                            float* hT_out, void* y, sss_dtype y_dtype,
+                            int64_t Bz, int64_t L, int H, int P, int N, int G,
+                            void* workspace, size_t workspace_bytes,
+                            sss_stream_t stream);
+
+/*
+ * sss_mixer_update -- single/multi-token decode update over a circular
+ * conv-state pool, then the same scan on the pool's SSM state.
+ *
+ * Source: "Chapter 7: state, chunking and incremental inference", sections
+ * "single-token update", "the physical cache may be longer than the minimum
+ * history", "circular mode" and "continuous batching".  For request row b:
+ * r = conv_state_indices[b] (b when NULL), p = cache_seqlens[b].  History j
+ * (j = 1..K-1) of channel d is read from conv_pool[r, d, (p-j) mod S_len]
+ * before anything is written; token i (logical position p+i) uses the
+ * register window, then its INPUT x_i (not the output) is stored at slot
+ * (p+i) mod S_len.  u_i = SiLU(bias + sum_k w_k window_k).  Then for every
+ * head the recurrence above runs over the L_new tokens on
+ * ssm_pool[r, h] (fp32, updated in place) and writes y.
+ * cache_seqlens is NOT advanced: the caller adds L_new after the call.
+ * A slot reused for a new request must be cleared by the caller (p < K-1
+ * reads the wrapped slots as they are).  Two rows naming the same pool row
+ * is a contract violation (undefined result).  A row with r outside
+ * [0, pool) or p < 0 is skipped: its pool rows are untouched, its y rows are
+ * set to zero and SSS_ERR_INDEX is raised in the device status.
+ *
+ *  x_new              [Bz, L_new, D]      act_dtype
+ *  w, bias            [D, K], [D]         float32 (bias NULL = 0)
+ *  conv_pool          [pool, D, S_len]    act_dtype, S_len >= K-1, in/out
+ *  cache_seqlens      [Bz]                int32 (device)
+ *  conv_state_indices [Bz]                int32 (device), NULL = identity
+ *  dt                 [Bz, L_new, H]      act_dtype
+ *  A                  [H]                 float32
+ *  B, C               [Bz, L_new, G, N]   act_dtype
+ *  ssm_pool           [pool, H, P, N]     float32, in/out
+ *  y                  [Bz, L_new, H, P]   act_dtype
+ * L_new <= 64.
+ */
+sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
+                            const float* w, const float* bias, void* conv_pool,
+                            int64_t pool, int S_len,
+                            const int32_t* cache_seqlens,
+                            const int32_t* conv_state_indices, const void* dt,
+                            const float* A, const void* B, const void* C,
+                            float* ssm_pool, void* y, int64_t Bz, int L_new,
+                            int H, int P, int N, int G, int K,
+                            sss_stream_t stream);
+
+/*
+ * sss_device_status -- read the device status word (OR of SSS_ERR_INDEX /
+ * SSS_ERR_TIMEOUT raised by kernels of this library on the current device)
+ * after the work on `stream` has finished; clear it when `clear` != 0.
+ * Synchronises `stream`.
+ */
+sss_status sss_device_status(int* status_out, int clear, sss_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSS_H_ */

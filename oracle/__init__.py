@@ -120,8 +120,9 @@ def ssm_scan(u, dt, A, B, C, h0=None, nthreads: int = 0):
     dt, A, B, C, h0 = _f64(dt), _f64(A), _f64(B), _f64(C), _f64(h0)
     Bz, L, H = dt.shape
     G, N = B.shape[2], B.shape[3]
-    u = _f64(u).reshape(Bz, L, H, -1)
-    P = u.shape[3]
+    u = _f64(u)
+    P = u.shape[3] if u.ndim == 4 else u.shape[2] // H
+    u = u.reshape(Bz, L, H, P)
     y = np.empty((Bz, L, H, P))
     hT = np.empty((Bz, H, P, N))
     rc = lib().orc_ssm_scan(_ptr(u), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0),

@@ -1,0 +1,209 @@
+"""Python binding of libsss (ctypes): the state-passing mixer forward and the
+decode update on GB300.
+
+Argument marshalling only: every step runs in the CUDA kernels of libsss.
+Tensors are torch CUDA tensors (torch supplies device memory and streams);
+calls are enqueued on torch's current stream.  Importing this module loads
+``_build/libsss.so`` and raises if it is missing (build it with
+``python selective_ssm_scan_gb300/build.py``); there is no fallback.
+
+Functions (same names as the C ABI in include/sss.h, minus the prefix):
+    conv_state_fwd, ssm_scan_fwd, ssm_scan_path, ssm_scan_workspace_size,
+    mixer_update, device_status, version, status_string
+plus ``mixer_fwd`` (conv_state_fwd then ssm_scan_fwd: one segment of the
+streaming forward with both states passed) and ``library_path``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "_build", "libsss.so")
+
+SSS_OK = 0
+SSS_ERR_INVALID_ARG = 1
+SSS_ERR_UNSUPPORTED = 2
+SSS_ERR_INDEX = 4
+SSS_ERR_TIMEOUT = 8
+SSS_ERR_CUDA = 16
+SSS_F32 = 0
+SSS_BF16 = 1
+
+if not os.path.exists(library_path):
+    raise ImportError(
+        f"libsss.so not found at {library_path}; build it with "
+        "`python selective_ssm_scan_gb300/build.py` (needs nvcc)")
+
+_lib = ctypes.CDLL(library_path)
+_p = ctypes.c_void_p
+_i64 = ctypes.c_int64
+_i = ctypes.c_int
+
+_lib.sss_version.restype = _i
+_lib.sss_status_string.restype = ctypes.c_char_p
+_lib.sss_status_string.argtypes = [_i]
+_lib.sss_conv_state_fwd.restype = _i
+_lib.sss_conv_state_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _i, _i64, _i64, _i64, _i, _i, _p]
+_lib.sss_ssm_scan_workspace_size.restype = ctypes.c_size_t
+_lib.sss_ssm_scan_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i]
+_lib.sss_ssm_scan_path.restype = _i
+_lib.sss_ssm_scan_path.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
+_lib.sss_ssm_scan_fwd.restype = _i
+_lib.sss_ssm_scan_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i64, _i64, _i, _i,
+                                  _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_mixer_update.restype = _i
+_lib.sss_mixer_update.argtypes = [_p, _i, _p, _p, _p, _i64, _i, _p, _p, _p, _p, _p, _p, _p, _p,
+                                  _i64, _i, _i, _i, _i, _i, _i, _p]
+_lib.sss_device_status.restype = _i
+_lib.sss_device_status.argtypes = [ctypes.POINTER(_i), _i, _p]
+
+
+class SSSError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def version() -> int:
+    return int(_lib.sss_version())
+
+
+def status_string(s: int) -> str:
+    return _lib.sss_status_string(int(s)).decode()
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SSS_F32
+    if t.dtype == torch.bfloat16:
+        return SSS_BF16
+    raise TypeError(f"unsupported dtype {t.dtype} (float32 or bfloat16)")
+
+
+def _dtype_code(d) -> int:
+    return _dt(torch.empty(0, dtype=d)) if isinstance(d, torch.dtype) else int(d)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr() if t.numel() else None
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream if hasattr(s, "cuda_stream") else int(s)
+
+
+def _check(fn: str, rc: int):
+    if rc != SSS_OK:
+        raise SSSError(fn, rc)
+
+
+def conv_state_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                   state_in: Optional[torch.Tensor] = None,
+                   state_out: Optional[torch.Tensor] = None, u: Optional[torch.Tensor] = None,
+                   u_dtype=torch.float32, apply_silu: bool = True, stream=None) -> torch.Tensor:
+    """x [Bz, L, D]; w [D, K] fp32; bias [D] fp32; state_in/state_out [Bz, D, K-1]
+    (x's dtype, may be the same tensor).  Returns u [Bz, L, D]."""
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    if u is None:
+        u = torch.empty((Bz, L, D), dtype=u_dtype, device=x.device)
+    rc = _lib.sss_conv_state_fwd(_ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(state_in),
+                                 _ptr(state_out), _ptr(u), _dt(u), Bz, L, D, K,
+                                 int(bool(apply_silu)), _stream(stream))
+    _check("sss_conv_state_fwd", rc)
+    return u
+
+
+def ssm_scan_workspace_size(Bz, L, H, P, N, G, x_dtype, act_dtype) -> int:
+    return int(_lib.sss_ssm_scan_workspace_size(Bz, L, H, P, N, G, _dtype_code(x_dtype),
+                                                _dtype_code(act_dtype)))
+
+
+def ssm_scan_path(Bz, L, H, P, N, G, x_dtype, act_dtype, y_dtype) -> int:
+    """1 = tcgen05 chunked scan, 0 = fp32 CUDA-core scan, -1 = unsupported."""
+    return int(_lib.sss_ssm_scan_path(Bz, L, H, P, N, G, _dtype_code(x_dtype),
+                                      _dtype_code(act_dtype), _dtype_code(y_dtype)))
+
+
+def ssm_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                 C: torch.Tensor, h0: Optional[torch.Tensor] = None,
+                 hT: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
+                 y_dtype=None, workspace: Optional[torch.Tensor] = None, stream=None):
+    """x [Bz, L, H, P] (or [Bz, L, D] with H taken from dt); dt [Bz, L, H];
+    A [H] fp32; B, C [Bz, L, G, N]; h0/hT [Bz, H, P, N] fp32 (may be the same
+    tensor).  Returns (y, hT)."""
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    P = x.shape[-1] if x.dim() == 4 else x.shape[-1] // H
+    dev = x.device
+    if y is None:
+        y = torch.empty((Bz, L, H, P), dtype=y_dtype or dt.dtype, device=dev)
+    if hT is None:
+        hT = torch.empty((Bz, H, P, N), dtype=torch.float32, device=dev)
+    ws = ssm_scan_workspace_size(Bz, L, H, P, N, G, x.dtype, dt.dtype)
+    if ws and (workspace is None or workspace.numel() * workspace.element_size() < ws):
+        workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+    wsb = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib.sss_ssm_scan_fwd(_ptr(x), _dt(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _dt(dt),
+                               _ptr(h0), _ptr(hT), _ptr(y), _dt(y), Bz, L, H, P, N, G,
+                               _ptr(workspace), wsb, _stream(stream))
+    _check("sss_ssm_scan_fwd", rc)
+    return y, hT
+
+
+def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, conv_state_out=None,
+              hT=None, u_dtype=torch.float32, y_dtype=None, stream=None):
+    """One segment of the streaming forward: conv (with state) + SiLU, then the
+    scan from h0.  Returns (y, conv_state_out, hT)."""
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    if conv_state_out is None:
+        conv_state_out = torch.empty((Bz, D, K - 1), dtype=x.dtype, device=x.device)
+    u = conv_state_fwd(x, w, bias, conv_state, conv_state_out, u_dtype=u_dtype, stream=stream)
+    y, hT = ssm_scan_fwd(u, dt, A, B, C, h0, hT, y_dtype=y_dtype or x.dtype, stream=stream)
+    return y, conv_state_out, hT
+
+
+def mixer_update(x_new: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                 conv_pool: torch.Tensor, cache_seqlens: torch.Tensor,
+                 conv_state_indices: Optional[torch.Tensor], dt: torch.Tensor, A: torch.Tensor,
+                 B: torch.Tensor, C: torch.Tensor, ssm_pool: torch.Tensor,
+                 y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """x_new [Bz, L_new, D]; conv_pool [pool, D, S_len] (updated in place);
+    cache_seqlens, conv_state_indices [Bz] int32; dt [Bz, L_new, H]; A [H];
+    B, C [Bz, L_new, G, N]; ssm_pool [pool, H, P, N] fp32 (updated in place).
+    Returns y [Bz, L_new, H, P].  cache_seqlens is not advanced."""
+    Bz, L_new, D = x_new.shape
+    H = dt.shape[2]
+    P = D // H
+    pool, _, S_len = conv_pool.shape
+    G, N = B.shape[2], B.shape[3]
+    K = w.shape[1]
+    if cache_seqlens.dtype != torch.int32 or (conv_state_indices is not None and
+                                              conv_state_indices.dtype != torch.int32):
+        raise TypeError("cache_seqlens and conv_state_indices must be int32")
+    if y is None:
+        y = torch.empty((Bz, L_new, H, P), dtype=x_new.dtype, device=x_new.device)
+    rc = _lib.sss_mixer_update(_ptr(x_new), _dt(x_new), _ptr(w), _ptr(bias), _ptr(conv_pool),
+                               pool, S_len, _ptr(cache_seqlens), _ptr(conv_state_indices),
+                               _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(ssm_pool), _ptr(y), Bz,
+                               L_new, H, P, N, G, K, _stream(stream))
+    _check("sss_mixer_update", rc)
+    return y
+
+
+def device_status(clear: bool = True, stream=None) -> int:
+    """OR of device-raised status bits since the last clear (synchronises)."""
+    v = ctypes.c_int(0)
+    _check("sss_device_status", _lib.sss_device_status(ctypes.byref(v), int(bool(clear)),
+                                                       _stream(stream)))
+    return int(v.value)

@@ -1,0 +1,205 @@
+// C ABI of libsss: argument validation, path selection and launch.  All
+// arithmetic runs in the kernels of the other files.
+#include <mutex>
+
+#include "common.cuh"
+
+namespace sss {
+
+__device__ int g_status_word;
+
+cudaError_t conv_state_fwd_launch(const void* x, sss_dtype xt, const float* w,
+                                  const float* bias, const void* s_in, void* s_out,
+                                  void* u, sss_dtype ut, int64_t Bz, int64_t L,
+                                  int64_t D, int K, int silu_on, cudaStream_t st);
+bool ssm_scan_simt_supports(int P, int N);
+cudaError_t ssm_scan_simt_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
+                                 const void* B, const void* C, sss_dtype at,
+                                 const float* h0, float* hT, void* y, sss_dtype yt,
+                                 int64_t Bz, int64_t L, int H, int P, int N, int G,
+                                 cudaStream_t st);
+bool ssm_scan_tc_supports(sss_dtype xt, sss_dtype at, sss_dtype yt, int64_t L, int H, int P,
+                          int N, int G);
+cudaError_t ssm_scan_tc_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
+                               const void* B, const void* C, const float* h0, float* hT,
+                               void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int P,
+                               int N, int G, int* status, cudaStream_t st);
+bool mixer_update_supports(int P, int N, int K, int L_new);
+cudaError_t mixer_update_launch(const void* x, sss_dtype at, const float* w, const float* bias,
+                                void* cp, int64_t pool, int S_len, const int32_t* sl,
+                                const int32_t* ix, const void* dt, const float* A,
+                                const void* B, const void* C, float* sp, void* y, int64_t Bz,
+                                int L_new, int H, int P, int N, int G, int K, int* status,
+                                cudaStream_t st);
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int g_sms[kMaxDevices];
+int* g_status_ptr[kMaxDevices];
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+}  // namespace
+
+int sm_count() {
+  const int dev = current_device();
+  if (dev < 0) return 1;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[dev]) {
+    int v = 0;
+    cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+    g_sms[dev] = v > 0 ? v : 1;
+  }
+  return g_sms[dev];
+}
+
+int* status_word() {
+  const int dev = current_device();
+  if (dev < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+static bool aligned(const void* p, size_t a) {
+  return (reinterpret_cast<uintptr_t>(p) % a) == 0;
+}
+
+static sss_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return SSS_OK;
+  if (e == cudaErrorNotSupported) {
+    cudaGetLastError();
+    return SSS_ERR_UNSUPPORTED;
+  }
+  return SSS_ERR_CUDA;
+}
+
+}  // namespace sss
+
+using namespace sss;
+
+extern "C" {
+
+int sss_version(void) { return 100; }
+
+const char* sss_status_string(int s) {
+  switch (s) {
+    case SSS_OK: return "ok";
+    case SSS_ERR_INVALID_ARG: return "invalid argument";
+    case SSS_ERR_UNSUPPORTED: return "unsupported configuration";
+    case SSS_ERR_INDEX: return "pool index or length out of range (device)";
+    case SSS_ERR_TIMEOUT: return "bounded device wait ran out";
+    case SSS_ERR_CUDA: return "CUDA runtime error";
+    default: return "several errors (bitwise OR of sss_status values)";
+  }
+}
+
+sss_status sss_conv_state_fwd(const void* x, sss_dtype x_dtype, const float* w,
+                              const float* bias, const void* state_in, void* state_out,
+                              void* u, sss_dtype u_dtype, int64_t Bz, int64_t L, int64_t D,
+                              int K, int apply_silu, sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(u_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || D < 0 || K < 1) return SSS_ERR_INVALID_ARG;
+  if (K > 8) return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0 || D == 0) return SSS_OK;
+  const size_t xs = dtype_size(x_dtype), us = dtype_size(u_dtype);
+  if (!w || !aligned(w, 4) || (bias && !aligned(bias, 4))) return SSS_ERR_INVALID_ARG;
+  if (L > 0 && (!x || !u || !aligned(x, xs) || !aligned(u, us))) return SSS_ERR_INVALID_ARG;
+  if ((state_in && !aligned(state_in, xs)) || (state_out && !aligned(state_out, xs)))
+    return SSS_ERR_INVALID_ARG;
+  if (L == 0 && !state_out) return SSS_OK;
+  return from_cuda(conv_state_fwd_launch(x, x_dtype, w, bias, state_in, state_out, u, u_dtype,
+                                         Bz, L, D, K, apply_silu != 0,
+                                         reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t sss_ssm_scan_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G,
+                                   sss_dtype x_dtype, sss_dtype act_dtype) {
+  (void)Bz; (void)L; (void)H; (void)P; (void)N; (void)G; (void)x_dtype; (void)act_dtype;
+  return 0;
+}
+
+int sss_ssm_scan_path(int64_t Bz, int64_t L, int H, int P, int N, int G, sss_dtype x_dtype,
+                      sss_dtype act_dtype, sss_dtype y_dtype) {
+  (void)Bz;
+  if (ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, L, H, P, N, G)) return 1;
+  if (ssm_scan_simt_supports(P, N)) return 0;
+  return -1;
+}
+
+sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
+                            const void* B, const void* C, sss_dtype act_dtype,
+                            const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
+                            int64_t Bz, int64_t L, int H, int P, int N, int G, void* workspace,
+                            size_t workspace_bytes, sss_stream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  if (!dtype_ok(x_dtype) || !dtype_ok(act_dtype) || !dtype_ok(y_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return SSS_ERR_INVALID_ARG;
+  if (Bz == 0) return SSS_OK;
+  const size_t xs = dtype_size(x_dtype), as = dtype_size(act_dtype), ys = dtype_size(y_dtype);
+  if (!A || !aligned(A, 4)) return SSS_ERR_INVALID_ARG;
+  if (L > 0 && (!x || !dt || !B || !C || !y)) return SSS_ERR_INVALID_ARG;
+  if (L > 0 && (!aligned(x, xs) || !aligned(dt, as) || !aligned(B, as) || !aligned(C, as) ||
+                !aligned(y, ys)))
+    return SSS_ERR_INVALID_ARG;
+  if ((h0_in && !aligned(h0_in, 4)) || (hT_out && !aligned(hT_out, 4))) return SSS_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (L > 0 && ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, L, H, P, N, G) &&
+      aligned(x, 16) && aligned(B, 16) && aligned(C, 16) && aligned(y, 16) &&
+      (!h0_in || aligned(h0_in, 16)) && (!hT_out || aligned(hT_out, 16)))
+    return from_cuda(ssm_scan_tc_launch(x, x_dtype, dt, A, B, C, h0_in, hT_out, y, y_dtype, Bz,
+                                        L, H, P, N, G, status_word(), st));
+  if (!ssm_scan_simt_supports(P, N)) return SSS_ERR_UNSUPPORTED;
+  return from_cuda(ssm_scan_simt_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y,
+                                        y_dtype, Bz, L, H, P, N, G, st));
+}
+
+sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype, const float* w,
+                            const float* bias, void* conv_pool, int64_t pool, int S_len,
+                            const int32_t* cache_seqlens, const int32_t* conv_state_indices,
+                            const void* dt, const float* A, const void* B, const void* C,
+                            float* ssm_pool, void* y, int64_t Bz, int L_new, int H, int P,
+                            int N, int G, int K, sss_stream_t stream) {
+  if (!dtype_ok(act_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || pool < 0 || L_new < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || K < 1 ||
+      S_len < 1 || S_len < K - 1)
+    return SSS_ERR_INVALID_ARG;
+  if (!mixer_update_supports(P, N, K, L_new)) return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0 || L_new == 0) return SSS_OK;
+  const size_t as = dtype_size(act_dtype);
+  if (!x_new || !w || !conv_pool || !cache_seqlens || !dt || !A || !B || !C || !ssm_pool || !y)
+    return SSS_ERR_INVALID_ARG;
+  if (!aligned(x_new, as) || !aligned(conv_pool, as) || !aligned(dt, as) || !aligned(B, as) ||
+      !aligned(C, as) || !aligned(y, as) || !aligned(w, 4) || (bias && !aligned(bias, 4)) ||
+      !aligned(A, 4) || !aligned(ssm_pool, 16) || !aligned(cache_seqlens, 4) ||
+      (conv_state_indices && !aligned(conv_state_indices, 4)))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(mixer_update_launch(x_new, act_dtype, w, bias, conv_pool, pool, S_len,
+                                       cache_seqlens, conv_state_indices, dt, A, B, C,
+                                       ssm_pool, y, Bz, L_new, H, P, N, G, K, status_word(),
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_device_status(int* status_out, int clear, sss_stream_t stream) {
+  if (!status_out) return SSS_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int* p = status_word();
+  if (!p) return SSS_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SSS_ERR_CUDA;
+  if (clear && cudaMemsetAsync(p, 0, sizeof(int), st) != cudaSuccess) return SSS_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SSS_ERR_CUDA;
+  *status_out = v;
+  return SSS_OK;
+}
+
+}  // extern "C"

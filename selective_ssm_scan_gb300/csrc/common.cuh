@@ -1,0 +1,96 @@
+// Shared device helpers of libsss: storage-type conversion, SiLU, the
+// device status word.  Arithmetic of the method lives in the kernel files.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sss.h"
+
+namespace sss {
+
+// Kernels OR status bits into a device status word (they never trap).  The
+// word lives in api.cu; its device address is passed to every kernel.
+__device__ __forceinline__ void raise_status(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)); the exp is CUDA's expf.
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// Host helpers implemented in api.cu.
+int sm_count();        // SMs of the current device (cached per device)
+int* status_word();    // device address of the status word (current device)
+
+inline size_t dtype_size(sss_dtype t) { return t == SSS_BF16 ? 2 : 4; }
+inline bool dtype_ok(int t) { return t == SSS_F32 || t == SSS_BF16; }
+
+}  // namespace sss
+
+namespace sss {
+
+// ---- vector load / store of VEC elements as floats -------------------------
+template <typename T, int VEC>
+__device__ __forceinline__ void ld_vec(const T* __restrict__ p, float* v) {
+  constexpr int BYTES = int(sizeof(T)) * VEC;
+  if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < BYTES / 16; ++c) {
+      union { uint4 r; T e[16 / sizeof(T)]; } u;
+      u.r = __ldg(reinterpret_cast<const uint4*>(p) + c);
+#pragma unroll
+      for (int i = 0; i < int(16 / sizeof(T)); ++i) v[c * int(16 / sizeof(T)) + i] = to_f32(u.e[i]);
+    }
+  } else if constexpr (BYTES == 8) {
+    union { uint2 r; T e[8 / sizeof(T)]; } u;
+    u.r = __ldg(reinterpret_cast<const uint2*>(p));
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) v[i] = to_f32(u.e[i]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) v[i] = to_f32(p[i]);
+  }
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ void st_vec(T* __restrict__ p, const float* v) {
+  constexpr int BYTES = int(sizeof(T)) * VEC;
+  if constexpr (BYTES % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < BYTES / 16; ++c) {
+      union { uint4 r; T e[16 / sizeof(T)]; } u;
+#pragma unroll
+      for (int i = 0; i < int(16 / sizeof(T)); ++i) u.e[i] = from_f32<T>(v[c * int(16 / sizeof(T)) + i]);
+      reinterpret_cast<uint4*>(p)[c] = u.r;
+    }
+  } else if constexpr (BYTES == 8) {
+    union { uint2 r; T e[8 / sizeof(T)]; } u;
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) u.e[i] = from_f32<T>(v[i]);
+    *reinterpret_cast<uint2*>(p) = u.r;
+  } else {
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) p[i] = from_f32<T>(v[i]);
+  }
+}
+
+}  // namespace sss

@@ -1,0 +1,88 @@
+"""The C-ABI library loads and exports every entry point its header declares;
+host-side argument checks answer without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sss.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._build_module().build()
+    return ctypes.CDLL(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sss_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("sss_conv_state_fwd", "sss_ssm_scan_fwd", "sss_mixer_update",
+                     "sss_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_version_and_status_strings(lib):
+    lib.sss_version.restype = ctypes.c_int
+    assert lib.sss_version() >= 100
+    lib.sss_status_string.restype = ctypes.c_char_p
+    assert lib.sss_status_string(0) == b"ok"
+    assert b"index" in lib.sss_status_string(4)
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    i64 = ctypes.c_int64
+    f = lib.sss_conv_state_fwd
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, i64, i64, i64,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    assert f(None, 0, None, None, None, None, None, 0, 1, 4, 8, 0, 1, None) == 1   # K < 1
+    assert f(None, 0, None, None, None, None, None, 0, 1, 4, 8, 4, 1, None) == 1   # null w/x/u
+    assert f(None, 7, None, None, None, None, None, 0, 1, 4, 8, 4, 1, None) == 1   # bad dtype
+    assert f(None, 0, None, None, None, None, None, 0, 1, 4, 8, 9, 1, None) == 2   # K > 8
+    assert f(None, 0, None, None, None, None, None, 0, 0, 4, 8, 4, 1, None) == 0   # empty batch
+    g = lib.sss_ssm_scan_fwd
+    g.restype = ctypes.c_int
+    g.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, i64, i64, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t,
+                  ctypes.c_void_p]
+    assert g(None, 0, None, None, None, None, 0, None, None, None, 0, 1, 8, 3, 4, 8, 2, None, 0,
+             None) == 1  # H % G != 0
+    assert g(None, 0, None, None, None, None, 0, None, None, None, 0, 1, 8, 2, 4, 8, 1, None, 0,
+             None) == 1  # null A
+    h = lib.sss_mixer_update
+    h.restype = ctypes.c_int
+    h.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, i64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                  ctypes.c_void_p, ctypes.c_void_p, i64, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p]
+    # S_len < K-1
+    assert h(None, 1, None, None, None, 4, 2, None, None, None, None, None, None, None, None, 2,
+             1, 2, 4, 8, 1, 4, None) == 1
+    # L_new above the supported maximum
+    assert h(None, 1, None, None, None, 4, 4, None, None, None, None, None, None, None, None, 2,
+             65, 2, 4, 8, 1, 4, None) == 2
+
+
+def test_scan_path_selection(lib):
+    lib.sss_ssm_scan_path.restype = ctypes.c_int
+    lib.sss_ssm_scan_path.argtypes = [ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int] * 7
+    assert lib.sss_ssm_scan_path(1, 64, 2, 4, 8, 1, 0, 0, 0) == 0      # fp32 -> CUDA cores
+    assert lib.sss_ssm_scan_path(1, 64, 2, 4, 1000, 1, 0, 0, 0) == -1  # N too large

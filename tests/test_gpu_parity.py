@@ -1,0 +1,317 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Every case draws its inputs from ``synth`` (seeded), runs the kernels of
+libsss on cuda:0, and compares with the oracle element by element on the same
+input bits (tolerances in tests/helpers.py).  Full-size workloads run in the
+launch configuration the benchmark times and are checked on sampled
+(batch, head) slices that the oracle recomputes alone.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import F32_REL, STATE_REL, assert_rel, assert_y_close, f64, max_rel, to_torch
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover - CPU container
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import selective_ssm_scan_gb300 as sss  # noqa: E402  (raises if libsss is missing)
+
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _clean_status():
+    sss.device_status(clear=True)
+    yield
+
+
+def T(a):
+    return to_torch(a, DEV)
+
+
+# ---------------------------------------------------------------------------
+# conv with state
+# ---------------------------------------------------------------------------
+
+def _conv_case(seed, Bz, L, D, K, dtype, state=True):
+    g = np.random.default_rng(seed)
+    x = synth.store(g.standard_normal((Bz, L, D)), dtype)
+    w = synth.f32(g.normal(0, np.sqrt(0.5), (D, K)))
+    bias = synth.f32(np.full(D, 0.1))
+    S = synth.store(g.standard_normal((Bz, D, K - 1)), dtype) if state else None
+    return x, w, bias, S
+
+
+@pytest.mark.parametrize("dtype,udtype", [("bf16", "f32"), ("bf16", "bf16"), ("f32", "f32")])
+@pytest.mark.parametrize("L", [0, 1, 2, 3, 8, 9, 100, 1027])
+@pytest.mark.parametrize("D", [2048, 24, 7])
+def test_conv_parity(dtype, udtype, L, D):
+    K = 4
+    x, w, bias, S = _conv_case(100 + L + D, 3, L, D, K, dtype)
+    u_ref, F_ref = oracle.conv_state_fwd(x, w, bias, S)
+    St = T(S)
+    Fo = torch.empty_like(St)
+    u = sss.conv_state_fwd(T(x), T(w), T(bias), St, Fo,
+                           u_dtype=torch.float32 if udtype == "f32" else torch.bfloat16)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(Fo), F_ref)  # copies of inputs: bit-exact
+    if udtype == "f32":
+        assert_rel(f64(u), u_ref, F32_REL, "u")
+    else:
+        assert_y_close(f64(u), u_ref, "u(bf16)")
+
+
+@pytest.mark.parametrize("K", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("L", [1, 2, 6, 33])
+def test_conv_other_widths(K, L):
+    x, w, bias, S = _conv_case(7 * K + L, 2, L, 16, K, "bf16")
+    u_ref, F_ref = oracle.conv_state_fwd(x, w, bias, S)
+    St = T(S)
+    Fo = torch.empty_like(St)
+    u = sss.conv_state_fwd(T(x), T(w), T(bias), St, Fo)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(Fo), F_ref)
+    assert_rel(f64(u), u_ref, F32_REL, "u")
+
+
+def test_conv_state_aliasing_and_no_state():
+    """state_out may be state_in (streaming in place); no state means zeros."""
+    x, w, bias, S = _conv_case(5, 2, 2, 64, 4, "bf16")  # L < K-1: F keeps part of S
+    u_ref, F_ref = oracle.conv_state_fwd(x, w, bias, S)
+    St = T(S)
+    sss.conv_state_fwd(T(x), T(w), T(bias), St, St)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(St), F_ref)
+    u0_ref, F0_ref = oracle.conv_state_fwd(x, w, bias, None)
+    Fo = torch.full((2, 64, 3), 7.0, dtype=torch.bfloat16, device=DEV)
+    u0 = sss.conv_state_fwd(T(x), T(w), T(bias), None, Fo)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(Fo), F0_ref)
+    assert_rel(f64(u0), u0_ref, F32_REL, "u")
+
+
+# ---------------------------------------------------------------------------
+# scan
+# ---------------------------------------------------------------------------
+
+def _scan_case(seed, Bz, L, H, P, N, G, dtype, h0=True):
+    g = np.random.default_rng(seed)
+    u = synth.store(g.standard_normal((Bz, L, H, P)), "f32")
+    dt = synth.store(np.logaddexp(0, g.standard_normal((Bz, L, H)) - 2.0), dtype)
+    A = synth.f32(-g.uniform(0.01, 1.0, H))
+    B = synth.store(g.standard_normal((Bz, L, G, N)), dtype)
+    C = synth.store(g.standard_normal((Bz, L, G, N)), dtype)
+    hh = synth.f32(g.normal(0, 0.1, (Bz, H, P, N))) if h0 else None
+    return u, dt, A, B, C, hh
+
+
+@pytest.mark.parametrize("Bz,L,H,P,N,G", [(1, 64, 2, 4, 8, 1), (2, 37, 4, 8, 16, 2),
+                                          (1, 1, 1, 1, 1, 1), (2, 0, 2, 4, 8, 1),
+                                          (1, 200, 3, 64, 128, 1), (1, 50, 2, 100, 200, 2)])
+def test_scan_fp32_parity(Bz, L, H, P, N, G):
+    u, dt, A, B, C, h0 = _scan_case(L + 10 * H, Bz, L, H, P, N, G, "f32")
+    y_ref, hT_ref = oracle.ssm_scan(u, dt, A, B, C, h0)
+    y, hT = sss.ssm_scan_fwd(T(u), T(dt), T(A), T(B), T(C), T(h0), y_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert_rel(f64(y), y_ref, F32_REL, "y")
+    assert_rel(f64(hT), hT_ref, F32_REL, "hT")
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 300, 1024])
+@pytest.mark.parametrize("h0", [True, False])
+def test_scan_bf16_parity(L, h0):
+    """bf16 activations at the Mamba-2 head shape (P=64, N=128): the path the
+    streaming forward takes; several chunks and a ragged tail."""
+    u, dt, A, B, C, hh = _scan_case(L, 2, L, 3, 64, 128, 1, "bf16", h0)
+    y_ref, hT_ref = oracle.ssm_scan(u, dt, A, B, C, hh)
+    h0t = T(hh) if h0 else None
+    y, hT = sss.ssm_scan_fwd(T(u), T(dt), T(A), T(B), T(C), h0t, y_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert_y_close(f64(y), y_ref)
+    assert_rel(f64(hT), hT_ref, STATE_REL, "hT")
+
+
+def test_scan_state_aliasing():
+    u, dt, A, B, C, hh = _scan_case(3, 1, 96, 2, 64, 128, 1, "bf16")
+    y_ref, hT_ref = oracle.ssm_scan(u, dt, A, B, C, hh)
+    h = T(hh)
+    y, hT = sss.ssm_scan_fwd(T(u), T(dt), T(A), T(B), T(C), h, h)
+    torch.cuda.synchronize()
+    assert hT.data_ptr() == h.data_ptr()
+    assert_rel(f64(h), hT_ref, STATE_REL, "hT in place")
+    assert_y_close(f64(y), y_ref)
+
+
+# ---------------------------------------------------------------------------
+# streaming forward: conv + scan with both states passed
+# ---------------------------------------------------------------------------
+
+def _run_stream(s, heads=None, batches=None):
+    """Run every segment of workload ``s`` on the GPU with the states passed in
+    place; return the y of each segment (sliced to the sampled heads/batches),
+    the final states, and the oracle's results for the same slices."""
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
+    S, h = T(st["conv_state"]), T(st["h0"])
+    heads = list(range(s.H)) if heads is None else heads
+    batches = list(range(s.Bz)) if batches is None else batches
+    chan = np.concatenate([np.arange(hh * s.P, (hh + 1) * s.P) for hh in heads])
+    gid = [hh // (s.H // s.G) for hh in heads]
+    # oracle on the sliced problem: H' = len(heads), one group per sampled head
+    S_ref = st["conv_state"].f64()[batches][:, chan]
+    h_ref = st["h0"].f64()[batches][:, heads]
+    A_ref = p["A"].f64()[heads]
+    w_ref, b_ref = p["w"].f64()[chan], p["bias"].f64()[chan]
+    for i in range(len(s.segments)):
+        seg = synth.mixer_segment(s, i)
+        y, S, h = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), A, T(seg["B"]), T(seg["C"]), w, bias,
+                                S, h, conv_state_out=S, hT=h)
+        x_r = seg["x"].f64()[batches][:, :, chan]
+        dt_r = seg["dt"].f64()[batches][:, :, heads]
+        B_r = seg["B"].f64()[batches][:, :, gid]
+        C_r = seg["C"].f64()[batches][:, :, gid]
+        y_ref, S_ref, h_ref = oracle.mixer_fwd(x_r, dt_r, A_ref, B_r, C_r, w_ref, b_ref,
+                                               S_ref, h_ref)
+        yg = f64(y[batches][:, :, heads])
+        assert_y_close(yg, y_ref, f"{s.name} segment {i} y")
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(S)[batches][:, chan], S_ref)
+    return f64(h)[batches][:, heads], h_ref
+
+
+def test_tiny_fp32_workload_split_equals_unsplit():
+    """The tiny fp32 workload: two 32-token segments with state passing equal
+    the oracle's unsplit 64-token sequence within 1e-5."""
+    s = synth.WORKLOADS["tiny_f32"]
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    segs = [synth.mixer_segment(s, i) for i in range(2)]
+    cat = {k: np.concatenate([sg[k].f64() for sg in segs], axis=1) for k in segs[0]}
+    y_ref, F_ref, hT_ref = oracle.mixer_fwd(cat["x"], cat["dt"], p["A"], cat["B"], cat["C"],
+                                            p["w"], p["bias"], st["conv_state"], st["h0"])
+    S, h = T(st["conv_state"]), T(st["h0"])
+    ys = []
+    for sg in segs:
+        y, S, h = sss.mixer_fwd(T(sg["x"]), T(sg["dt"]), T(p["A"]), T(sg["B"]), T(sg["C"]),
+                                T(p["w"]), T(p["bias"]), S, h, conv_state_out=S, hT=h,
+                                y_dtype=torch.float32)
+        ys.append(f64(y).reshape(1, 32, -1))
+    torch.cuda.synchronize()
+    assert_rel(np.concatenate(ys, axis=1), y_ref.reshape(1, 64, -1), F32_REL, "y")
+    np.testing.assert_array_equal(f64(S), F_ref)
+    assert_rel(f64(h), hT_ref, F32_REL, "hT")
+
+
+@pytest.mark.parametrize("name,heads,batches", [
+    ("m370m_2k", [0, 17, 31], [0, 7]),
+    ("m1p3b_8k", [0, 63], [0, 3]),
+])
+def test_workload_full_size_sampled(name, heads, batches):
+    s = synth.WORKLOADS[name]
+    hg, h_ref = _run_stream(s, heads, batches)
+    assert_rel(hg, h_ref, STATE_REL, f"{name} final SSM state")
+
+
+@pytest.mark.slow
+def test_long_context_streaming_sampled():
+    """64 consecutive 2048-token segments (131072 tokens), states passed."""
+    s = synth.WORKLOADS["m780m_128k"]
+    hg, h_ref = _run_stream(s, [0, 47], [0])
+    assert_rel(hg, h_ref, STATE_REL, "final SSM state")
+
+
+def test_reduced_workload_all_heads():
+    """370M-like recipe at a size the oracle finishes in a second, every
+    output element compared; L not a multiple of any chunk length."""
+    s = synth.WORKLOADS["m370m_2k"].with_(Bz=2, segments=(333, 700), H=4,
+                                          gaussian_init=True)
+    hg, h_ref = _run_stream(s)
+    assert_rel(hg, h_ref, STATE_REL, "final SSM state")
+
+
+# ---------------------------------------------------------------------------
+# decode update
+# ---------------------------------------------------------------------------
+
+def _decode_gpu(d, inp):
+    g = {k: T(v) for k, v in inp.items()}
+    y = sss.mixer_update(g["x"], g["w"], g["bias"], g["conv_pool"], g["cache_seqlens"],
+                         g["conv_state_indices"], g["dt"], g["A"], g["B"], g["C"], g["ssm_pool"])
+    torch.cuda.synchronize()
+    return y, g
+
+
+@pytest.mark.parametrize("L_new,S_len,K", [(1, 4, 4), (4, 4, 4), (6, 4, 4), (2, 3, 4),
+                                           (3, 9, 4), (1, 2, 3), (2, 1, 2), (5, 8, 8)])
+@pytest.mark.parametrize("H,P,N", [(2, 64, 128), (3, 4, 8)])
+def test_decode_parity(L_new, S_len, K, H, P, N):
+    d = synth.DECODE["decode_256x1"].with_(Bz=5, pool=9, L_new=L_new, S_len=S_len, K=K, H=H,
+                                           P=P, N=N, max_seqlen=30)
+    inp = synth.decode_inputs(d)
+    y, g = _decode_gpu(d, inp)
+    y_ref, cp_ref, sp_ref, nbad = oracle.mixer_update(
+        inp["x"], inp["w"], inp["bias"], inp["conv_pool"], inp["cache_seqlens"],
+        inp["conv_state_indices"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["ssm_pool"])
+    assert nbad == 0 and sss.device_status() == 0
+    assert_y_close(f64(y), y_ref)
+    np.testing.assert_array_equal(f64(g["conv_pool"]), cp_ref)      # slots: bit-exact
+    assert_rel(f64(g["ssm_pool"]), sp_ref, 1e-5, "ssm pool")
+    untouched = np.setdiff1d(np.arange(d.pool), inp["conv_state_indices"].data)
+    np.testing.assert_array_equal(g["ssm_pool"].cpu().numpy()[untouched],
+                                  inp["ssm_pool"].data[untouched])   # bytes unchanged
+    np.testing.assert_array_equal(g["conv_pool"].view(torch.int16).cpu().numpy()[untouched],
+                                  inp["conv_pool"].data.view(np.int16)[untouched])
+
+
+def test_decode_bad_rows_are_skipped_and_reported():
+    d = synth.DECODE["decode_256x1"].with_(Bz=3, pool=5, H=2, P=4, N=8)
+    inp = synth.decode_inputs(d)
+    inp["conv_state_indices"].data[:] = [0, 9, 2]
+    inp["cache_seqlens"].data[:] = [3, 4, -1]
+    y, g = _decode_gpu(d, inp)
+    st = sss.device_status()
+    assert st & sss.SSS_ERR_INDEX
+    y_ref, cp_ref, sp_ref, nbad = oracle.mixer_update(
+        inp["x"], inp["w"], inp["bias"], inp["conv_pool"], inp["cache_seqlens"],
+        inp["conv_state_indices"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["ssm_pool"])
+    assert nbad == 2
+    assert_y_close(f64(y), y_ref)
+    np.testing.assert_array_equal(f64(g["conv_pool"]), cp_ref)
+
+
+@pytest.mark.parametrize("name", ["decode_256x1", "decode_256x4"])
+def test_decode_full_size_sampled(name):
+    """The full continuous-batching call (256 of 512 pool rows); sampled
+    requests recomputed by the oracle, untouched pool rows bit-identical."""
+    d = synth.DECODE[name]
+    inp = synth.decode_inputs(d)
+    y, g = _decode_gpu(d, inp)
+    assert sss.device_status() == 0
+    idx = inp["conv_state_indices"].data
+    rows = [0, 1, 128, 255]
+    sub = {k: v for k, v in inp.items()}
+    pick = lambda a: synth.Arr(np.ascontiguousarray(a.data[rows]), a.dtype)
+    for k in ("x", "dt", "B", "C", "cache_seqlens"):
+        sub[k] = pick(inp[k])
+    pool_rows = idx[rows]
+    sub["conv_pool"] = synth.Arr(np.ascontiguousarray(inp["conv_pool"].data[pool_rows]), "bf16")
+    sub["ssm_pool"] = synth.Arr(np.ascontiguousarray(inp["ssm_pool"].data[pool_rows]), "f32")
+    sub["conv_state_indices"] = synth.Arr(np.arange(len(rows), dtype=np.int32), "i32")
+    y_ref, cp_ref, sp_ref, nbad = oracle.mixer_update(
+        sub["x"], sub["w"], sub["bias"], sub["conv_pool"], sub["cache_seqlens"],
+        sub["conv_state_indices"], sub["dt"], sub["A"], sub["B"], sub["C"], sub["ssm_pool"])
+    assert nbad == 0
+    assert_y_close(f64(y[rows]), y_ref)
+    pr = torch.as_tensor(pool_rows, device=DEV, dtype=torch.long)
+    np.testing.assert_array_equal(f64(g["conv_pool"][pr]), cp_ref)
+    assert_rel(f64(g["ssm_pool"][pr]), sp_ref, 1e-5, "ssm pool rows")
+    untouched = torch.as_tensor(np.setdiff1d(np.arange(d.pool), idx), device=DEV)
+    assert torch.equal(g["ssm_pool"][untouched], T(inp["ssm_pool"])[untouched])
+    assert torch.equal(g["conv_pool"][untouched].view(torch.int16),
+                       T(inp["conv_pool"])[untouched].view(torch.int16))
