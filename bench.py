@@ -1,0 +1,439 @@
+#!/usr/bin/env python3
+"""Benchmark: state-passing conv + scan forward of a Mamba-2 370M-like mixer
+layer on GB300, tokens/s, with the roofline of the dominant kernel.
+
+A step is one pass of the hot path over one batch: batch 8, L = 2048 tokens
+run as two 1024-token segments, each segment = conv with state (+SiLU) then
+the scan from the previous segment's final SSM state (H=32, P=64, N=128, K=4,
+bf16 activations, fp32 state).  Inputs are resident in HBM when the timed
+region starts; L2 is flushed (a 256 MiB write) before every timed step,
+outside the events.  The same line also reports the decode update of a
+continuous-batching call (256 of 512 pool rows, L_new = 1) measured the same
+way.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the workload (the
+work shards by batch with no exchange); ``value`` is the tokens of all ranks
+divided by the slowest rank's time.  ``--impl reference`` times the float64
+CPU oracle on this machine's host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = "m370m_2k"
+METRIC = "tokens/s per GB300 (conv+scan fwd w/ state passing) and % of HBM/tensor roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def workload_desc(s) -> str:
+    return (f"{s.name}: Mamba-2 370M-like mixer layer, batch {s.Bz}, L={s.L} as "
+            f"{len(s.segments)}x{s.segments[0]}-token segments with conv and SSM state passed, "
+            f"H={s.H}, P={s.P}, N={s.N}, K={s.K}, bf16 x/dt/B/C, fp32 state")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def traffic_from_profile(kernel: str):
+    """dram bytes per launch from the committed ncu summary, if it covers the
+    current build of the kernel (the summary states the source hash)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    import hashlib
+    src = None
+    val = None
+    for line in text.splitlines():
+        if line.startswith("source_sha256:"):
+            src = line.split(":", 1)[1].strip()
+        if line.startswith("traffic_bytes_per_launch:"):
+            val = int(float(line.split(":", 1)[1].strip()))
+    try:
+        fn = os.path.join(ROOT, "selective_ssm_scan_gb300", "csrc", f"{kernel}.cu")
+        cur = hashlib.sha256(open(fn, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if src != cur:
+        return None
+    return val
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.out = out
+        else:
+            self.out = ""
+
+    def summary(self):
+        rows = [r.split(",") for r in self.out.strip().splitlines() if r.count(",") >= 8]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if r[5 + i].strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def cpu_step_sample(s, nthreads: int = 0, rows: int = 0):
+    """The oracle on one step of the workload (or its first ``rows`` batch
+    rows): conv + scan over both segments with the states passed."""
+    import oracle
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    rows = slice(0, rows or s.Bz)
+    segs = [synth.mixer_segment(s, i, Bz=rows) for i in range(len(s.segments))]
+    S = st["conv_state"].f64()[rows]
+    h = st["h0"].f64()[rows]
+    t0 = time.perf_counter()
+    for sg in segs:
+        _, S, h = oracle.mixer_fwd(sg["x"], sg["dt"], p["A"], sg["B"], sg["C"], p["w"],
+                                   p["bias"], S, h, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    tokens = sum(s.segments) * (rows.stop - rows.start)
+    return tokens / dt, dt, tokens, oracle.num_threads(nthreads)
+
+
+def run_reference(args, s):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_step_sample(s)
+    times = []
+    tokens = 0
+    cores = None
+    for _ in range(args.steps):
+        _, dt, tokens, cores = cpu_step_sample(s)
+        times.append(dt)
+    total = sum(times)
+    value = tokens * len(times) / total
+    sample = (f"one full step of {s.name} per step ({tokens} tokens: batch {s.Bz}, "
+              f"{len(s.segments)} segments of {s.segments[0]}, all {s.H} heads)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(s), "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    s = synth.WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        run_reference(args, s)
+        return
+
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import selective_ssm_scan_gb300 as sss
+
+    def T(a):
+        if a.dtype == "bf16":
+            return torch.from_numpy(a.data.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a.data).to(dev)
+
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    segs = [synth.mixer_segment(s, i) for i in range(len(s.segments))]
+    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
+    S0, h00 = T(st["conv_state"]), T(st["h0"])
+    dseg = [{k: T(v) for k, v in sg.items()} for sg in segs]
+    S = torch.empty_like(S0)
+    h = torch.empty_like(h00)
+    us = [torch.empty((s.Bz, L, s.D), dtype=torch.float32, device=dev) for L in s.segments]
+    ys = [torch.empty((s.Bz, L, s.H, s.P), dtype=torch.bfloat16, device=dev)
+          for L in s.segments]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def reset():
+        S.copy_(S0)
+        h.copy_(h00)
+
+    def step(evs=None):
+        for i, sg in enumerate(dseg):
+            if evs is not None:
+                evs[2 * i].record(stream)
+            sss.conv_state_fwd(sg["x"], w, bias, S, S, u=us[i])
+            if evs is not None:
+                evs[2 * i + 1].record(stream)
+            sss.ssm_scan_fwd(us[i], sg["dt"], A, sg["B"], sg["C"], h, h, y=ys[i])
+        if evs is not None:
+            evs[2 * len(dseg)].record(stream)
+
+    n_seg = len(dseg)
+    launches_per_step = 2 * n_seg
+    for _ in range(args.warmup):
+        reset()
+        step()
+    torch.cuda.synchronize()
+
+    # ---- timed: device-resident inputs -----------------------------------
+    step_ms, conv_ms, scan_ms = [], [], []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            reset()
+            flush.zero_()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_seg + 1)]
+            step(evs)
+            stream.synchronize()
+            for i in range(n_seg):
+                conv_ms.append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
+                scan_ms.append(evs[2 * i + 1].elapsed_time(evs[2 * i + 2]))
+            step_ms.append(evs[0].elapsed_time(evs[-1]))
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens_per_step = s.Bz * s.L
+    value = world * tokens_per_step * args.steps / (total_ms * 1e-3)
+
+    # ---- roofline of the dominant kernel (the scan) ------------------------
+    hbm, hbm_kind = peaks()
+    Lseg = s.segments[0]
+    scan_bytes = (s.Bz * Lseg * s.D * 4          # u (fp32) read
+                  + s.Bz * Lseg * s.H * 2        # dt
+                  + 2 * s.Bz * Lseg * s.G * s.N * 2  # B, C
+                  + s.Bz * Lseg * s.D * 2        # y (bf16) write
+                  + 2 * s.Bz * s.H * s.P * s.N * 4)  # h0 read + hT write
+    conv_bytes = (s.Bz * Lseg * s.D * (2 + 4) + 2 * s.Bz * s.D * (s.K - 1) * 2)
+    scan_avg = statistics.mean(scan_ms)
+    conv_avg = statistics.mean(conv_ms)
+    dom, dom_bytes, dom_ms = ("ssm_scan", scan_bytes, scan_avg)
+    if conv_avg > scan_avg:
+        dom, dom_bytes, dom_ms = ("conv_state_fwd", conv_bytes, conv_avg)
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    path = sss.ssm_scan_path(s.Bz, Lseg, s.H, s.P, s.N, s.G, torch.float32, torch.bfloat16,
+                             torch.bfloat16)
+    kernel_file = "ssm_scan_tc" if path == 1 else "ssm_scan_simt"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm,
+                "traffic": traffic_from_profile(kernel_file if dom == "ssm_scan" else "conv_state_fwd"),
+                "kernel": kernel_file if dom == "ssm_scan" else "conv_state_fwd",
+                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured"
+                else "fallback 6.8 TB/s",
+                "other": {"conv_state_fwd": {"avg_launch_ms": conv_avg,
+                                             "achieved_gbs": conv_bytes / conv_avg / 1e6,
+                                             "frac": conv_bytes / conv_avg / 1e6 / hbm},
+                          "ssm_scan": {"avg_launch_ms": scan_avg,
+                                       "achieved_gbs": scan_bytes / scan_avg / 1e6,
+                                       "frac": scan_bytes / scan_avg / 1e6 / hbm}}}
+
+    # ---- end to end through the API with host buffers ----------------------
+    host = {}
+    for i, sg in enumerate(dseg):
+        for k, v in sg.items():
+            host[(i, k)] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
+    hS0 = torch.empty(S0.shape, dtype=S0.dtype, pin_memory=True).copy_(S0)
+    hh0 = torch.empty(h00.shape, dtype=h00.dtype, pin_memory=True).copy_(h00)
+    hy = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys]
+    hS = torch.empty(S0.shape, dtype=S0.dtype, pin_memory=True)
+    hh = torch.empty(h00.shape, dtype=h00.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
+        hS0.numel() * hS0.element_size() + hh0.numel() * hh0.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in hy) + hS.numel() * hS.element_size() + \
+        hh.numel() * hh.element_size()
+
+    def e2e_step():
+        for (i, k), t in host.items():
+            dseg[i][k].copy_(t, non_blocking=True)
+        S.copy_(hS0, non_blocking=True)
+        h.copy_(hh0, non_blocking=True)
+        for i, sg in enumerate(dseg):
+            sss.conv_state_fwd(sg["x"], w, bias, S, S, u=us[i])
+            sss.ssm_scan_fwd(us[i], sg["dt"], A, sg["B"], sg["C"], h, h, y=ys[i])
+            hy[i].copy_(ys[i], non_blocking=True)
+        hS.copy_(S, non_blocking=True)
+        hh.copy_(h, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = sum(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_total = float(t.item())
+    e2e_value = world * tokens_per_step * args.steps / (e2e_total * 1e-3)
+
+    # ---- decode update (continuous batching), same rules -------------------
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(torch, sss, dev, stream, flush, args, hbm)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_desc(s), "tokens_per_step": tokens_per_step,
+                   "scan_path": "tcgen05" if path == 1 else "cuda-core fp32",
+                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if decode is not None:
+        out["decode"] = decode
+    if rank == 0 and not args.no_cpu_baseline:
+        v, dt, tokens, cores = cpu_step_sample(s)
+        out["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                               "sample": f"one full step ({tokens} tokens, {dt:.1f} s wall)"}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def bench_decode(torch, sss, dev, stream, flush, args, hbm):
+    d = synth.DECODE["decode_256x1"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(d.seed)
+    bf = torch.bfloat16
+    conv_pool = torch.randn((d.pool, d.D, d.S_len), generator=g, device=dev).to(bf)
+    ssm_pool = torch.randn((d.pool, d.H, d.P, d.N), generator=g, device=dev) * 0.1
+    idx = torch.randperm(d.pool, generator=g, device=dev)[: d.Bz].to(torch.int32)
+    seqlens = torch.randint(0, d.max_seqlen, (d.Bz,), generator=g, device=dev,
+                            dtype=torch.int32)
+    x = torch.randn((d.Bz, d.L_new, d.D), generator=g, device=dev).to(bf)
+    dt = torch.nn.functional.softplus(
+        torch.randn((d.Bz, d.L_new, d.H), generator=g, device=dev) - 2.0).to(bf)
+    B = torch.randn((d.Bz, d.L_new, d.G, d.N), generator=g, device=dev).to(bf)
+    C = torch.randn((d.Bz, d.L_new, d.G, d.N), generator=g, device=dev).to(bf)
+    A = -(torch.rand((d.H,), generator=g, device=dev) * 0.99 + 0.01)
+    w = torch.randn((d.D, d.K), generator=g, device=dev) * (0.5 ** 0.5)
+    bias = torch.full((d.D,), 0.1, device=dev)
+    y = torch.empty((d.Bz, d.L_new, d.H, d.P), dtype=bf, device=dev)
+
+    def call():
+        sss.mixer_update(x, w, bias, conv_pool, seqlens, idx, dt, A, B, C, ssm_pool, y)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        stream.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    avg = statistics.mean(ms)
+    byts = (2 * d.Bz * d.H * d.P * d.N * 4
+            + d.Bz * d.D * (d.K - 1) * 2 + d.Bz * d.L_new * d.D * 2
+            + d.Bz * d.L_new * (2 * d.D * 2 + 2 * d.G * d.N * 2 + d.H * 2))
+    gbs = byts / (avg * 1e-3) / 1e9
+    return {"workload": "decode_256x1: 256 of 512 pool rows by a random permutation, circular "
+                        "conv pool [512,4096,4], cache_seqlens ~ U[0,10000), SSM pool "
+                        "[512,64,64,128] fp32, L_new=1, H=64, P=64, N=128, K=4, bf16",
+            "tokens_per_s": d.Bz * d.L_new / (avg * 1e-3), "avg_launch_ms": avg,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "algorithmic_bytes_per_launch": byts,
+                         "kernel": "mixer_update"}}
+
+
+if __name__ == "__main__":
+    main()

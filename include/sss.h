@@ -172,6 +172,18 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
                             sss_stream_t stream);
 
 /*
+ * sss_tcgen05_selftest -- diagnostic of the tensor-core operand layouts the
+ * chunked scan uses (no counterpart on the pages).  With A and B two
+ * [128][128] bf16 row-major matrices (device), writes four fp32 [128][128]
+ * blocks to `out` (device, 4*128*128 floats), each = A B^T computed through
+ * one descriptor form: [0] both operands K-major (all 128 columns valid);
+ * [1] A MN-major; [2] B MN-major; [3] A read from tensor memory ([1]..[3]:
+ * columns 0..63 valid).
+ */
+sss_status sss_tcgen05_selftest(const void* A, const void* B, float* out,
+                                sss_stream_t stream);
+
+/*
  * sss_device_status -- read the device status word (OR of SSS_ERR_INDEX /
  * SSS_ERR_TIMEOUT raised by kernels of this library on the current device)
  * after the work on `stream` has finished; clear it when `clear` != 0.

@@ -58,6 +58,8 @@ _lib.sss_ssm_scan_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i
 _lib.sss_mixer_update.restype = _i
 _lib.sss_mixer_update.argtypes = [_p, _i, _p, _p, _p, _i64, _i, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i, _i, _i, _i, _i, _i, _p]
+_lib.sss_tcgen05_selftest.restype = _i
+_lib.sss_tcgen05_selftest.argtypes = [_p, _p, _p, _p]
 _lib.sss_device_status.restype = _i
 _lib.sss_device_status.argtypes = [ctypes.POINTER(_i), _i, _p]
 
@@ -199,6 +201,16 @@ def mixer_update(x_new: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tens
                                L_new, H, P, N, G, K, _stream(stream))
     _check("sss_mixer_update", rc)
     return y
+
+
+def tcgen05_selftest(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
+    """A, B [128, 128] bf16 (cuda).  Returns [4, 128, 128] fp32: A @ B.T through
+    the four tensor-core operand forms of the chunked scan (blocks 1..3 valid
+    in columns 0..63)."""
+    out = torch.zeros((4, 128, 128), dtype=torch.float32, device=A.device)
+    _check("sss_tcgen05_selftest", _lib.sss_tcgen05_selftest(_ptr(A), _ptr(B), _ptr(out),
+                                                             _stream(stream)))
+    return out
 
 
 def device_status(clear: bool = True, stream=None) -> int:

@@ -24,6 +24,8 @@ cudaError_t ssm_scan_tc_launch(const void* x, sss_dtype xt, const void* dt, cons
                                const void* B, const void* C, const float* h0, float* hT,
                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int P,
                                int N, int G, int* status, cudaStream_t st);
+cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
+                               cudaStream_t st);
 bool mixer_update_supports(int P, int N, int K, int L_new);
 cudaError_t mixer_update_launch(const void* x, sss_dtype at, const float* w, const float* bias,
                                 void* cp, int64_t pool, int S_len, const int32_t* sl,
@@ -186,6 +188,14 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype, const float*
                                        cache_seqlens, conv_state_indices, dt, A, B, C,
                                        ssm_pool, y, Bz, L_new, H, P, N, G, K, status_word(),
                                        reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_tcgen05_selftest(const void* A, const void* B, float* out,
+                                sss_stream_t stream) {
+  if (!A || !B || !out || !aligned(A, 16) || !aligned(B, 16) || !aligned(out, 4))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(tc_selftest_launch(A, B, out, status_word(),
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sss_status sss_device_status(int* status_out, int clear, sss_stream_t stream) {

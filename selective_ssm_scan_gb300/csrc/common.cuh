@@ -34,8 +34,12 @@ __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
   return __float2bfloat16_rn(v);
 }
 
-// SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)); the exp is CUDA's expf.
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU(z) = z * sigmoid(z) = z / (1 + exp(-z)), with CUDA's fast __expf and
+// __fdividef (a few ulp; the argument of the exp is capped at 80 so that the
+// divisor stays finite: for z < -80 the result is ~1e-33 either way).
+__device__ __forceinline__ float silu(float z) {
+  return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f)));
+}
 
 // Host helpers implemented in api.cu.
 int sm_count();        // SMs of the current device (cached per device)

@@ -29,7 +29,7 @@ struct __align__((sizeof(T) * VEC) >= 16 ? 16 : (sizeof(T) * VEC)) Pack {
 };
 
 template <typename TX, typename TU, int VEC, int TILE, int KT>
-__global__ void __launch_bounds__(256, 2)
+__global__ void __launch_bounds__(256, 3)
 conv_state_fwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
                       const float* __restrict__ bias, const TX* s_in, TX* s_out,
                       TU* __restrict__ u, int64_t L, int64_t D, int K_rt,

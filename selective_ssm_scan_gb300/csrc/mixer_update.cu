@@ -61,7 +61,7 @@ __device__ __forceinline__ int64_t pos_mod(int64_t a, int64_t m) {
 }
 
 template <typename T, int RP, int CV>
-__global__ void __launch_bounds__(kUpdWarps * 32)
+__global__ void __launch_bounds__(kUpdWarps * 32, RP * CV <= 8 ? 3 : 1)
 mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
                     const float* __restrict__ bias, T* conv_pool, int64_t pool, int S_len,
                     const int32_t* __restrict__ seqlens, const int32_t* __restrict__ idx,
