@@ -98,7 +98,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -183,7 +183,7 @@ def run_reference(args, s):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -225,12 +225,28 @@ def main():
           for L in s.segments]
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
+    n_seg = len(dseg)
+    fused_ok = sss.mixer_fwd_supported(s.Bz, s.segments[0], s.H, s.P, s.N, s.G, s.K,
+                                       torch.bfloat16, torch.bfloat16)
+    if not fused_ok:
+        raise SystemExit("the fused forward does not support this workload")
 
     def reset():
         S.copy_(S0)
         h.copy_(h00)
 
     def step(evs=None):
+        """The default path: one kernel per segment (conv + SiLU + scan)."""
+        for i, sg in enumerate(dseg):
+            if evs is not None:
+                evs[i].record(stream)
+            sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
+                          conv_state_out=S, hT=h, y=ys[i], fused=True)
+        if evs is not None:
+            evs[n_seg].record(stream)
+
+    def step_two_calls(evs=None):
+        """The same forward as two calls per segment, u kept in fp32 in HBM."""
         for i, sg in enumerate(dseg):
             if evs is not None:
                 evs[2 * i].record(stream)
@@ -239,34 +255,38 @@ def main():
                 evs[2 * i + 1].record(stream)
             sss.ssm_scan_fwd(us[i], sg["dt"], A, sg["B"], sg["C"], h, h, y=ys[i])
         if evs is not None:
-            evs[2 * len(dseg)].record(stream)
+            evs[2 * n_seg].record(stream)
 
-    n_seg = len(dseg)
-    launches_per_step = 2 * n_seg
+    def timed(fn, n_events, steps):
+        all_evs = []
+        for _ in range(steps):
+            reset()
+            flush.zero_()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
+            fn(evs)
+            all_evs.append(evs)
+        stream.synchronize()
+        return all_evs
+
+    launches_per_step = n_seg
     for _ in range(args.warmup):
         reset()
         step()
+        reset()
+        step_two_calls()
     torch.cuda.synchronize()
 
     # ---- timed: device-resident inputs -----------------------------------
-    step_ms, conv_ms, scan_ms = [], [], []
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        for _ in range(args.steps):
-            reset()
-            flush.zero_()
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_seg + 1)]
-            step(evs)
-            stream.synchronize()
-            for i in range(n_seg):
-                conv_ms.append(evs[2 * i].elapsed_time(evs[2 * i + 1]))
-                scan_ms.append(evs[2 * i + 1].elapsed_time(evs[2 * i + 2]))
-            step_ms.append(evs[0].elapsed_time(evs[-1]))
+        evs_all = timed(step, n_seg + 1, args.steps)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
+    step_ms = [e[0].elapsed_time(e[-1]) for e in evs_all]
+    seg_ms = [e[i].elapsed_time(e[i + 1]) for e in evs_all for i in range(n_seg)]
     total_ms = sum(step_ms)
     if dist:
         t = torch.tensor([total_ms], device=dev)
@@ -275,37 +295,51 @@ def main():
     tokens_per_step = s.Bz * s.L
     value = world * tokens_per_step * args.steps / (total_ms * 1e-3)
 
-    # ---- roofline of the dominant kernel (the scan) ------------------------
+    # the two-call composition, same rules (reported beside the default path)
+    evs2 = timed(step_two_calls, 2 * n_seg + 1, max(3, args.steps // 4))
+    conv_ms = [e[2 * i].elapsed_time(e[2 * i + 1]) for e in evs2 for i in range(n_seg)]
+    scan_ms = [e[2 * i + 1].elapsed_time(e[2 * i + 2]) for e in evs2 for i in range(n_seg)]
+    two_call_step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs2)
+
+    # ---- roofline of the dominant kernel -----------------------------------
     hbm, hbm_kind = peaks()
     Lseg = s.segments[0]
-    scan_bytes = (s.Bz * Lseg * s.D * 4          # u (fp32) read
-                  + s.Bz * Lseg * s.H * 2        # dt
-                  + 2 * s.Bz * Lseg * s.G * s.N * 2  # B, C
-                  + s.Bz * Lseg * s.D * 2        # y (bf16) write
-                  + 2 * s.Bz * s.H * s.P * s.N * 4)  # h0 read + hT write
-    conv_bytes = (s.Bz * Lseg * s.D * (2 + 4) + 2 * s.Bz * s.D * (s.K - 1) * 2)
+    state_bytes = 2 * s.Bz * s.H * s.P * s.N * 4                 # h0 read + hT write
+    cstate_bytes = 2 * s.Bz * s.D * (s.K - 1) * 2                # conv state read + write
+    io_bytes = (s.Bz * Lseg * s.H * 2 + 2 * s.Bz * Lseg * s.G * s.N * 2   # dt, B, C
+                + s.Bz * Lseg * s.D * 2)                          # y (bf16) write
+    fused_bytes = s.Bz * Lseg * s.D * 2 + io_bytes + state_bytes + cstate_bytes
+    scan_bytes = s.Bz * Lseg * s.D * 4 + io_bytes + state_bytes   # u (fp32) read
+    conv_bytes = s.Bz * Lseg * s.D * (2 + 4) + cstate_bytes
+    fused_avg = statistics.mean(seg_ms)
     scan_avg = statistics.mean(scan_ms)
     conv_avg = statistics.mean(conv_ms)
-    dom, dom_bytes, dom_ms = ("ssm_scan", scan_bytes, scan_avg)
-    if conv_avg > scan_avg:
-        dom, dom_bytes, dom_ms = ("conv_state_fwd", conv_bytes, conv_avg)
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    path = sss.ssm_scan_path(s.Bz, Lseg, s.H, s.P, s.N, s.G, torch.float32, torch.bfloat16,
-                             torch.bfloat16)
-    kernel_file = "ssm_scan_tc" if path == 1 else "ssm_scan_simt"
+    achieved = fused_bytes / (fused_avg * 1e-3) / 1e9
+    # useful (unsplit) contraction flops of the chunked form, for the tensor pipe
+    Q = 128
+    chunks = -(-Lseg // Q)
+    tc_flops = s.Bz * s.H * chunks * 2 * Q * (Q * s.N + Q * s.P + 2 * s.P * s.N)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm,
-                "traffic": traffic_from_profile(kernel_file if dom == "ssm_scan" else "conv_state_fwd"),
-                "kernel": kernel_file if dom == "ssm_scan" else "conv_state_fwd",
-                "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
-                "peak_source": f"{hbm_kind} (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured"
+                "traffic": traffic_from_profile("ssm_scan_tc"),
+                "kernel": "ssm_scan_tc_kernel<bf16,bf16,fused> (conv+SiLU+scan, one launch "
+                          "per segment)",
+                "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_ms": fused_avg,
+                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured"
                 else "fallback 6.8 TB/s",
-                "other": {"conv_state_fwd": {"avg_launch_ms": conv_avg,
-                                             "achieved_gbs": conv_bytes / conv_avg / 1e6,
-                                             "frac": conv_bytes / conv_avg / 1e6 / hbm},
-                          "ssm_scan": {"avg_launch_ms": scan_avg,
-                                       "achieved_gbs": scan_bytes / scan_avg / 1e6,
-                                       "frac": scan_bytes / scan_avg / 1e6 / hbm}}}
+                "tensor_useful_tflops": tc_flops / (fused_avg * 1e-3) / 1e12,
+                "two_call_path": {
+                    "ms_per_step": two_call_step_ms,
+                    "conv_state_fwd": {"avg_launch_ms": conv_avg,
+                                       "algorithmic_bytes_per_launch": conv_bytes,
+                                       "achieved_gbs": conv_bytes / conv_avg / 1e6,
+                                       "frac": conv_bytes / conv_avg / 1e6 / hbm},
+                    "ssm_scan_fwd": {"avg_launch_ms": scan_avg,
+                                     "algorithmic_bytes_per_launch": scan_bytes,
+                                     "achieved_gbs": scan_bytes / scan_avg / 1e6,
+                                     "frac": scan_bytes / scan_avg / 1e6 / hbm}}}
+    path = sss.ssm_scan_path(s.Bz, Lseg, s.H, s.P, s.N, s.G, torch.float32, torch.bfloat16,
+                             torch.bfloat16)
 
     # ---- end to end through the API with host buffers ----------------------
     host = {}
@@ -328,8 +362,8 @@ def main():
         S.copy_(hS0, non_blocking=True)
         h.copy_(hh0, non_blocking=True)
         for i, sg in enumerate(dseg):
-            sss.conv_state_fwd(sg["x"], w, bias, S, S, u=us[i])
-            sss.ssm_scan_fwd(us[i], sg["dt"], A, sg["B"], sg["C"], h, h, y=ys[i])
+            sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
+                          conv_state_out=S, hT=h, y=ys[i], fused=True)
             hy[i].copy_(ys[i], non_blocking=True)
         hS.copy_(S, non_blocking=True)
         hh.copy_(h, non_blocking=True)
@@ -338,7 +372,8 @@ def main():
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = []
-    for _ in range(args.steps):
+    e2e_steps = max(3, args.steps // 10)
+    for _ in range(e2e_steps):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -352,7 +387,7 @@ def main():
         t = torch.tensor([e2e_total], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_total = float(t.item())
-    e2e_value = world * tokens_per_step * args.steps / (e2e_total * 1e-3)
+    e2e_value = world * tokens_per_step * e2e_steps / (e2e_total * 1e-3)
 
     # ---- decode update (continuous batching), same rules -------------------
     decode = None
@@ -364,7 +399,8 @@ def main():
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(s), "tokens_per_step": tokens_per_step,
-                   "scan_path": "tcgen05" if path == 1 else "cuda-core fp32",
+                   "path": "sss_mixer_fwd: one tcgen05 kernel per segment (conv+SiLU+scan)",
+                   "scan_path_two_call": "tcgen05" if path == 1 else "cuda-core fp32",
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
@@ -411,16 +447,17 @@ def bench_decode(torch, sss, dev, stream, flush, args, hbm):
     for _ in range(args.warmup):
         call()
     torch.cuda.synchronize()
-    ms = []
-    for _ in range(args.steps):
+    evs = []
+    for _ in range(max(3, args.steps // 10)):
         flush.zero_()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         call()
         e1.record(stream)
-        stream.synchronize()
-        ms.append(e0.elapsed_time(e1))
+        evs.append((e0, e1))
+    stream.synchronize()
+    ms = [a.elapsed_time(b) for a, b in evs]
     avg = statistics.mean(ms)
     byts = (2 * d.Bz * d.H * d.P * d.N * 4
             + d.Bz * d.D * (d.K - 1) * 2 + d.Bz * d.L_new * d.D * 2

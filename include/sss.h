@@ -129,6 +129,40 @@ sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt,
                             sss_stream_t stream);
 
 /*
+ * sss_mixer_fwd -- one segment of the streaming forward in a single kernel:
+ * the conv with state of sss_conv_state_fwd (SiLU applied) feeding the scan
+ * of sss_ssm_scan_fwd, so the conv output never goes to memory.  Sources:
+ * both of the above, and "Chapter 7: state, chunking and incremental
+ * inference", section "chunked training and truncated backpropagation"
+ * (segment B starts from segment A's final conv state, S_B = F_A) together
+ * with section 2.6 / Eq. (4) of "Understanding and Improving Length
+ * Generalization in Recurrent Models" (state passing of h).
+ *
+ *  x                   [Bz, L, H*P]  x_dtype (bf16 on this path)
+ *  w, bias             [H*P, K], [H*P]  float32 (bias NULL = 0)
+ *  conv_state_in/out   [Bz, H*P, K-1] x_dtype; may be the same buffer;
+ *                      NULL in = zeros, NULL out = not written
+ *  dt                  [Bz, L, H]    x_dtype, positive
+ *  A                   [H]           float32
+ *  B, C                [Bz, L, G, N] x_dtype
+ *  h0_in / hT_out      [Bz, H, P, N] float32; may be the same buffer
+ *  y                   [Bz, L, H, P] y_dtype
+ * Supported (sss_mixer_fwd_supported() == 1): bf16 x/dt/B/C, P == 64,
+ * N == 128, K <= 4; otherwise SSS_ERR_UNSUPPORTED (compose
+ * sss_conv_state_fwd and sss_ssm_scan_fwd instead).
+ */
+int sss_mixer_fwd_supported(int64_t Bz, int64_t L, int H, int P, int N, int G,
+                            int K, sss_dtype x_dtype, sss_dtype y_dtype);
+
+sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w,
+                         const float* bias, const void* conv_state_in,
+                         void* conv_state_out, const void* dt, const float* A,
+                         const void* B, const void* C, const float* h0_in,
+                         float* hT_out, void* y, sss_dtype y_dtype, int64_t Bz,
+                         int64_t L, int H, int P, int N, int G, int K,
+                         sss_stream_t stream);
+
+/*
  * sss_mixer_update -- single/multi-token decode update over a circular
  * conv-state pool, then the same scan on the pool's SSM state.
  *
@@ -174,11 +208,12 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
 /*
  * sss_tcgen05_selftest -- diagnostic of the tensor-core operand layouts the
  * chunked scan uses (no counterpart on the pages).  With A and B two
- * [128][128] bf16 row-major matrices (device), writes four fp32 [128][128]
- * blocks to `out` (device, 4*128*128 floats), each = A B^T computed through
+ * [128][128] bf16 row-major matrices (device), writes six fp32 [128][128]
+ * blocks to `out` (device, 6*128*128 floats), each = A B^T computed through
  * one descriptor form: [0] both operands K-major (all 128 columns valid);
- * [1] A MN-major; [2] B MN-major; [3] A read from tensor memory ([1]..[3]:
- * columns 0..63 valid).
+ * [1] A MN-major; [2] B MN-major; [3] A read from tensor memory; [4] A from
+ * tensor memory with B MN-major; [5] A and B MN-major ([1]..[5]: columns
+ * 0..63 valid).
  */
 sss_status sss_tcgen05_selftest(const void* A, const void* B, float* out,
                                 sss_stream_t stream);

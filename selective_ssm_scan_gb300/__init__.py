@@ -58,6 +58,11 @@ _lib.sss_ssm_scan_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i
 _lib.sss_mixer_update.restype = _i
 _lib.sss_mixer_update.argtypes = [_p, _i, _p, _p, _p, _i64, _i, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i, _i, _i, _i, _i, _i, _p]
+_lib.sss_mixer_fwd_supported.restype = _i
+_lib.sss_mixer_fwd_supported.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
+_lib.sss_mixer_fwd.restype = _i
+_lib.sss_mixer_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i64, _i64,
+                               _i, _i, _i, _i, _i, _p]
 _lib.sss_tcgen05_selftest.restype = _i
 _lib.sss_tcgen05_selftest.argtypes = [_p, _p, _p, _p]
 _lib.sss_device_status.restype = _i
@@ -162,16 +167,42 @@ def ssm_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
     return y, hT
 
 
+def mixer_fwd_supported(Bz, L, H, P, N, G, K, x_dtype, y_dtype) -> bool:
+    return bool(_lib.sss_mixer_fwd_supported(Bz, L, H, P, N, G, K, _dtype_code(x_dtype),
+                                             _dtype_code(y_dtype)))
+
+
 def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, conv_state_out=None,
-              hT=None, u_dtype=torch.float32, y_dtype=None, stream=None):
+              hT=None, y=None, u_dtype=torch.float32, y_dtype=None, fused=None, stream=None):
     """One segment of the streaming forward: conv (with state) + SiLU, then the
-    scan from h0.  Returns (y, conv_state_out, hT)."""
+    scan from h0.  Returns (y, conv_state_out, hT).
+
+    fused=None picks the single-kernel sss_mixer_fwd when the library supports
+    the shapes, else the two calls conv_state_fwd + ssm_scan_fwd (u kept in
+    u_dtype between them); fused=True / False forces one or the other."""
     Bz, L, D = x.shape
+    H = dt.shape[2]
+    P = D // H
+    G, N = B.shape[2], B.shape[3]
     K = w.shape[1]
+    y_dtype = y_dtype or x.dtype
     if conv_state_out is None:
         conv_state_out = torch.empty((Bz, D, K - 1), dtype=x.dtype, device=x.device)
+    if hT is None:
+        hT = torch.empty((Bz, H, P, N), dtype=torch.float32, device=x.device)
+    if y is None:
+        y = torch.empty((Bz, L, H, P), dtype=y_dtype, device=x.device)
+    if fused is None:
+        fused = mixer_fwd_supported(Bz, L, H, P, N, G, K, x.dtype, y.dtype)
+    if fused:
+        rc = _lib.sss_mixer_fwd(_ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(conv_state),
+                                _ptr(conv_state_out), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                _ptr(h0), _ptr(hT), _ptr(y), _dt(y), Bz, L, H, P, N, G, K,
+                                _stream(stream))
+        _check("sss_mixer_fwd", rc)
+        return y, conv_state_out, hT
     u = conv_state_fwd(x, w, bias, conv_state, conv_state_out, u_dtype=u_dtype, stream=stream)
-    y, hT = ssm_scan_fwd(u, dt, A, B, C, h0, hT, y_dtype=y_dtype or x.dtype, stream=stream)
+    ssm_scan_fwd(u, dt, A, B, C, h0, hT, y=y, stream=stream)
     return y, conv_state_out, hT
 
 
@@ -204,10 +235,10 @@ def mixer_update(x_new: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tens
 
 
 def tcgen05_selftest(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
-    """A, B [128, 128] bf16 (cuda).  Returns [4, 128, 128] fp32: A @ B.T through
-    the four tensor-core operand forms of the chunked scan (blocks 1..3 valid
-    in columns 0..63)."""
-    out = torch.zeros((4, 128, 128), dtype=torch.float32, device=A.device)
+    """A, B [128, 128] bf16 (cuda).  Returns [6, 128, 128] fp32: A @ B.T through
+    the tensor-core operand forms of the chunked scan (blocks 1..5 valid in
+    columns 0..63)."""
+    out = torch.zeros((6, 128, 128), dtype=torch.float32, device=A.device)
     _check("sss_tcgen05_selftest", _lib.sss_tcgen05_selftest(_ptr(A), _ptr(B), _ptr(out),
                                                              _stream(stream)))
     return out

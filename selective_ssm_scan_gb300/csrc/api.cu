@@ -24,6 +24,13 @@ cudaError_t ssm_scan_tc_launch(const void* x, sss_dtype xt, const void* dt, cons
                                const void* B, const void* C, const float* h0, float* hT,
                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int P,
                                int N, int G, int* status, cudaStream_t st);
+bool mixer_fwd_tc_supports(sss_dtype xt, sss_dtype at, int K, int64_t L, int H, int P, int N,
+                           int G);
+cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias,
+                                const void* s_in, void* s_out, const void* dt, const float* A,
+                                const void* B, const void* C, const float* h0, float* hT,
+                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G, int K,
+                                int* status, cudaStream_t st);
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
                                cudaStream_t st);
 bool mixer_update_supports(int P, int N, int K, int L_new);
@@ -162,6 +169,44 @@ sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, co
   if (!ssm_scan_simt_supports(P, N)) return SSS_ERR_UNSUPPORTED;
   return from_cuda(ssm_scan_simt_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y,
                                         y_dtype, Bz, L, H, P, N, G, st));
+}
+
+int sss_mixer_fwd_supported(int64_t Bz, int64_t L, int H, int P, int N, int G, int K,
+                            sss_dtype x_dtype, sss_dtype y_dtype) {
+  (void)Bz; (void)y_dtype;
+  return (L == 0 || mixer_fwd_tc_supports(x_dtype, x_dtype, K, L > 0 ? L : 1, H, P, N, G)) ? 1 : 0;
+}
+
+sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const float* bias,
+                         const void* conv_state_in, void* conv_state_out, const void* dt,
+                         const float* A, const void* B, const void* C, const float* h0_in,
+                         float* hT_out, void* y, sss_dtype y_dtype, int64_t Bz, int64_t L, int H,
+                         int P, int N, int G, int K, sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(y_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || K < 1)
+    return SSS_ERR_INVALID_ARG;
+  if (!sss_mixer_fwd_supported(Bz, L, H, P, N, G, K, x_dtype, y_dtype)) return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0) return SSS_OK;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (!w || !A || !aligned(w, 4) || !aligned(A, 4) || (bias && !aligned(bias, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if ((conv_state_in && !aligned(conv_state_in, 2)) || (conv_state_out && !aligned(conv_state_out, 2)) ||
+      (h0_in && !aligned(h0_in, 4)) || (hT_out && !aligned(hT_out, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if (L == 0) {  // no tokens: F = S and hT = h0, through the general kernels
+    sss_status r = sss_conv_state_fwd(nullptr, x_dtype, w, bias, conv_state_in, conv_state_out,
+                                      nullptr, SSS_F32, Bz, 0, int64_t(H) * P, K, 1, stream);
+    if (r != SSS_OK) return r;
+    return from_cuda(ssm_scan_simt_launch(nullptr, SSS_F32, nullptr, A, nullptr, nullptr,
+                                          x_dtype, h0_in, hT_out, nullptr, y_dtype, Bz, 0, H, P,
+                                          N, G, st));
+  }
+  if (!x || !dt || !B || !C || !y || !aligned(x, 16) || !aligned(dt, 2) || !aligned(B, 16) ||
+      !aligned(C, 16) || !aligned(y, 16))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(mixer_fwd_tc_launch(x, w, bias, conv_state_in, conv_state_out, dt, A, B, C,
+                                       h0_in, hT_out, y, y_dtype, Bz, L, H, G, K, status_word(),
+                                       st));
 }
 
 sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype, const float* w,

@@ -1,5 +1,6 @@
 // Tensor-core (tcgen05) chunked selective scan, one scalar decay per head,
-// from an initial state.
+// from an initial state; optionally fused with the causal conv + SiLU that
+// produces its input.
 //
 // The recurrence is Eq. (1) of "Understanding and Improving Length
 // Generalization in Recurrent Models" with A_t = exp(dt_t A_h).  Its unrolled
@@ -14,25 +15,32 @@
 //   h_new = exp(Lam_end) h_prev + sum_s exp(Lam_end - Lam_s) x_s B_s^T
 //
 // Per chunk and head that is four products on the tensor cores (bf16 in,
-// fp32 accumulate in tensor memory), M = Q = 128 rows each:
+// fp32 accumulate in tensor memory), M = 128 rows each:
 //   G   = C B^T                     [t][s]  (K = N)
 //   Yd  = (G o M) X                 [t][p]  (K = Q, A operand from TMEM)
 //   Yo  = C h_prev^T                [t][p]  (K = N)
 //   S^T = B^T X~                    [n][p]  (K = Q), X~_s = exp(Lam_end - Lam_s) x_s
-// The fp32 operands the pages' tolerance cannot afford to round once to bf16
-// (x, G o M, h_prev, X~; B and C are bf16 inputs and stay exact) are split
-// into hi + lo bf16 parts; each product takes the hi*hi, hi*lo and lo*hi terms
-// it needs (the state path keeps ~2^-16 relative precision).  The state h
-// itself stays in fp32 registers, one TMEM lane (= one state row n) per
-// thread, across all chunks of the sequence: it never goes to HBM between
-// chunks.
+// The fp32 operands that a single bf16 rounding would push past the
+// tolerance (x, G o M, h_prev, X~; B and C are bf16 inputs and stay exact)
+// are split into hi + lo bf16 parts and each product takes the hi*hi, hi*lo
+// and lo*hi terms.  The state stays in fp32 registers (one TMEM lane = one
+// state row n per consumer thread) for the whole sequence.
 //
-// One CTA (128 threads = the 128 TMEM lanes) owns one (batch, head) and walks
-// its chunks in order; B and C chunks arrive by TMA (128-byte swizzle, OOB rows
-// zero-filled so a ragged tail needs no special case), x is read by the
-// threads and written into the swizzled K-major operand tiles, thread 0
-// issues the MMAs.  Every wait on an mbarrier is bounded (2 s): on expiry the
-// kernel raises SSS_ERR_TIMEOUT, frees its tensor memory and returns.
+// Warp roles in one CTA = one (batch, head), 288 threads:
+//   warps 0-3  producers: per chunk, Lam, the input rows (or the conv of the
+//              raw input, fused), the hi/lo operand tiles of x and x~
+//              (token-major rows = MN-major operands, 16-byte stores),
+//              double-buffered so chunk c+1 is prepared during chunk c;
+//   warps 4-7  consumers: the decay mask G -> G o M (into TMEM), the state
+//              carry h_c = exp(Lam_end) h_{c-1} + S_c and its hi/lo tiles,
+//              the y epilogue;
+//   warp 8     issuer: TMA of the B and C chunks and every tcgen05.mma, one
+//              thread; TMA for chunk c+1 starts as soon as chunk c's products
+//              that read B and C are done.
+// Stages hand over through mbarriers.  Every wait is bounded (2 s): on expiry
+// the waiter raises SSS_ERR_TIMEOUT and sets an abort flag that makes every
+// other role stop at its next wait; the issuer drains its MMAs, the CTA frees
+// its tensor memory and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -47,31 +55,44 @@ namespace {
 constexpr int kQ = 128;  // chunk length = MMA M
 constexpr int kP = 64;   // head dimension
 constexpr int kN = 128;  // state size
-constexpr int kThreads = 128;
+constexpr int kMaxK = 4; // conv width handled by the fused producer
+constexpr int kThreads = 288;
 constexpr uint32_t kTmemCols = 512;
 // tensor memory columns (fp32 accumulators unless noted)
-constexpr uint32_t kColG = 0;     // C B^T          [t][s]  128
-constexpr uint32_t kColYd = 128;  // (G o M) x      [t][p]   64
-constexpr uint32_t kColYo = 192;  // C h^T          [t][p]   64
-constexpr uint32_t kColS = 256;   // B^T x~         [n][p]   64
-constexpr uint32_t kColGh = 320;  // hi(G o M), bf16 pairs   64
-constexpr uint32_t kColGl = 384;  // lo(G o M), bf16 pairs   64
+constexpr uint32_t kColG = 0;     // C B^T            [t][s] 128
+constexpr uint32_t kColGh = 128;  // hi(G o M), bf16 pairs    64
+constexpr uint32_t kColGl = 192;  // lo(G o M), bf16 pairs    64
+constexpr uint32_t kColYd = 256;  // (G o M) x        [t][p]  64
+constexpr uint32_t kColYo = 320;  // C h^T            [t][p]  64
+constexpr uint32_t kColS = 384;   // B^T x~, 2 buffers [n][p] 2 x 64
 // shared memory (bytes from a 1024-byte aligned base)
-constexpr uint32_t kOffC = 0;         // C chunk  [t][n] K-major, two 64-wide n blocks
-constexpr uint32_t kOffB = 32768;     // B chunk  [s][n]
-constexpr uint32_t kOffUh = 65536;    // hi(x)    [p][s] K-major, two 64-wide s blocks
-constexpr uint32_t kOffUl = 81920;    // lo(x)
-constexpr uint32_t kOffXh = 98304;    // hi(x~)
-constexpr uint32_t kOffXl = 114688;   // lo(x~)
-constexpr uint32_t kOffHh = 131072;   // hi(h)    [n][p] MN-major (rows = K = n)
-constexpr uint32_t kOffHl = 147456;   // lo(h)
-constexpr uint32_t kOffMisc = 163840;
-constexpr uint32_t kSmemBytes = kOffMisc + 2048 + 1024;
+constexpr uint32_t kOffC = 0;         // C chunk [t][n], K-major, two 64-wide n blocks
+constexpr uint32_t kOffB = 32768;     // B chunk [s][n]
+constexpr uint32_t kOffU = 65536;     // x hi/lo, 2 stages x (hi 16 KB, lo 16 KB), rows s
+constexpr uint32_t kOffX = 131072;    // x~ hi (16 KB), lo (16 KB), rows s
+constexpr uint32_t kOffH = 163840;    // h hi (16 KB), lo (16 KB), rows n
+constexpr uint32_t kOffMisc = 196608;
+constexpr uint32_t kMiscLam = 0;       // [2][128] consumer Lam
+constexpr uint32_t kMiscRedP = 1024;   // [2][4]  producer scan scratch
+constexpr uint32_t kMiscRedE = 1056;   // [2][4]  consumer scan scratch
+constexpr uint32_t kMiscW = 1088;      // [64][4] conv weights of the head
+constexpr uint32_t kMiscBias = 2112;   // [64]
+constexpr uint32_t kMiscBars = 2368;   // 18 mbarriers
+constexpr uint32_t kMiscTmem = 2528;
+constexpr uint32_t kMiscAbort = 2532;
+constexpr uint32_t kSmemBytes = kOffMisc + 2560 + 1024;
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint32_t kIdG = idesc_bf16(128, 128, 0, 0);
-constexpr uint32_t kIdS = idesc_bf16(128, 64, 1, 0);
-constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);
-constexpr uint32_t kIdYd = idesc_bf16(128, 64, 0, 0);
+// barriers
+enum {
+  BAR_FULL_CB = 0, BAR_TILES = 1 /*2*/, BAR_U_FREE = 3 /*2*/, BAR_X_FREE = 5, BAR_G_FULL = 6,
+  BAR_GM_FULL = 7, BAR_S_FULL = 8 /*2*/, BAR_S_FREE = 10 /*2*/, BAR_YO_DONE = 12,
+  BAR_H_FULL = 13, BAR_Y_FULL = 14, BAR_ACC_FREE = 15, BAR_CB_FREE = 16, BAR_DRAIN = 17,
+  NUM_BARS = 18
+};
+constexpr uint32_t kIdG = idesc_bf16(128, 128, 0, 0);   // C (K-major) x B (K-major)
+constexpr uint32_t kIdS = idesc_bf16(128, 64, 1, 1);    // B^T (MN-major) x x~ (MN-major)
+constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);   // C (K-major) x h (MN-major)
+constexpr uint32_t kIdYd = idesc_bf16(128, 64, 0, 1);   // G o M (TMEM) x x (MN-major)
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -79,13 +100,14 @@ __device__ __forceinline__ uint16_t bf16_bits(float v) {
 __device__ __forceinline__ float bf16_val(uint16_t b) {
   return __bfloat162float(__ushort_as_bfloat16(b));
 }
-// hi = bf16(v), lo = bf16(v - hi): v == hi + lo to ~2^-16 relative
-__device__ __forceinline__ void split(float v, uint16_t& hi, uint16_t& lo) {
-  hi = bf16_bits(v);
-  lo = bf16_bits(v - bf16_val(hi));
-}
 __device__ __forceinline__ uint32_t pack2(uint16_t lo_elem, uint16_t hi_elem) {
   return uint32_t(lo_elem) | (uint32_t(hi_elem) << 16);
+}
+// (a, b) -> packed hi pair and lo pair: v == hi + lo to ~2^-16 relative
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const uint16_t ha = bf16_bits(a), hb = bf16_bits(b);
+  hi = pack2(ha, hb);
+  lo = pack2(bf16_bits(a - bf16_val(ha)), bf16_bits(b - bf16_val(hb)));
 }
 
 // K-major descriptor of a [rows][128-element K] tile stored as two 64-wide K
@@ -93,23 +115,22 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo_elem, uint16_t hi_elem) {
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, uint32_t blk) {
   return sdesc_sw128(base + uint32_t(kk >> 2) * blk + uint32_t(kk & 3) * 32u, 16, 1024);
 }
+// MN-major descriptor of a [K rows][64 MN] tile (128-byte rows): K step kk
+// starts 16 rows further.
+__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
+  return sdesc_sw128(base + uint32_t(kk) * 2048u, 8192, 1024);
+}
 
-// h (fp32, this thread's state row n) -> hi/lo bf16 rows of the MN-major
-// B operand of C h^T.
-__device__ __forceinline__ void write_h_rows(uint8_t* sm, int n, const float* hreg) {
+// Row `r` (64 fp32 values) -> hi and lo bf16 rows of two MN-major tiles.
+__device__ __forceinline__ void write_split_row(uint8_t* hi_tile, uint8_t* lo_tile, int r,
+                                                const float* v) {
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint32_t hw[4], lw[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      uint16_t h0, l0, h1, l1;
-      split(hreg[8 * c + 2 * k], h0, l0);
-      split(hreg[8 * c + 2 * k + 1], h1, l1);
-      hw[k] = pack2(h0, h1);
-      lw[k] = pack2(l0, l1);
-    }
-    *reinterpret_cast<uint4*>(sm + kOffHh + sw128(n, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(sm + kOffHl + sw128(n, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    for (int k = 0; k < 4; ++k) split2(v[8 * c + 2 * k], v[8 * c + 2 * k + 1], hw[k], lw[k]);
+    *reinterpret_cast<uint4*>(hi_tile + sw128(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(lo_tile + sw128(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 }
 
@@ -131,8 +152,8 @@ __device__ __forceinline__ void load_row64<__nv_bfloat16>(const __nv_bfloat16* r
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      u[8 * q + 2 * k] = bf16_val(uint16_t(w[k] & 0xFFFFu));
-      u[8 * q + 2 * k + 1] = bf16_val(uint16_t(w[k] >> 16));
+      u[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
+      u[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
     }
   }
 }
@@ -156,280 +177,394 @@ __device__ __forceinline__ void store_row64<__nv_bfloat16>(__nv_bfloat16* row, c
   }
 }
 
+// Named barrier among the 128 threads of one role (ids 1, 2; 0 is __syncthreads).
+__device__ __forceinline__ void role_sync(int id) {
+  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+struct Ctl {
+  uint32_t bars;              // smem address of barrier 0
+  volatile int* abort;
+  int* status;
+  __device__ uint32_t bar(int i) const { return bars + 8u * uint32_t(i); }
+  // bounded wait; false when the CTA is aborting
+  __device__ bool wait(int i, uint32_t parity) const {
+    const uint32_t b = bar(i);
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(b, parity)) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        raise_status(status, SSS_ERR_TIMEOUT);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+// inclusive prefix of `v` over the 128 threads of a role (4 warps)
+__device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* red, int bar_id,
+                                             float* total) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float nb = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += nb;
+  }
+  if (lane == 31) red[wq] = v;
+  role_sync(bar_id);
+  float off = 0.0f, tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float r = red[w];
+    if (w < wq) off += r;
+    tot += r;
+  }
+  *total = tot;
+  return v + off;
+}
+
 }  // namespace
 
-template <typename TX, typename TY>
-__global__ void __launch_bounds__(kThreads, 1)
+// x: the scan input u [Bz, L, H, 64] (TX = float or bf16), or with FUSED the
+// raw input [Bz, L, H*64] (bf16) that the producers convolve (K <= 4, SiLU).
+template <typename TX, typename TY, bool FUSED>
+__global__ void __maxnreg__(224)
 ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                    const TX* __restrict__ x, const __nv_bfloat16* __restrict__ dt,
                    const float* __restrict__ A, const float* h0, float* hT,
-                   TY* __restrict__ y, int L, int H, int G, int* status) {
+                   TY* __restrict__ y, const float* __restrict__ conv_w,
+                   const float* __restrict__ conv_b, const TX* conv_s_in, TX* conv_s_out,
+                   int K, int L, int H, int G, int* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~uintptr_t(1023));
   const uint32_t sb = smem_u32(sm);
-  float* lam = reinterpret_cast<float*>(sm + kOffMisc);  // [128] Lam_t
-  float* gfac = lam + 128;                                 // [128] exp(R - Lam_s)
-  float* red = gfac + 128;                                 // [16]  block reductions
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffMisc + 1152);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffMisc + 1152 + 16);
-  const uint32_t bar_tma = smem_u32(&bars[0]);
-  const uint32_t bar_mma = smem_u32(&bars[1]);
+  uint8_t* misc = sm + kOffMisc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + kMiscTmem);
+  Ctl ctl{smem_u32(misc + kMiscBars), reinterpret_cast<volatile int*>(misc + kMiscAbort), status};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x / H, h = blockIdx.x % H, g = h / (H / G);
   const float Ah = A[h];
   const int64_t D = int64_t(H) * kP;
+  const int nC = (L + kQ - 1) / kQ;
 
-  if (warp == 0) {
+  if (warp == 8) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    mbar_init(bar_tma, 1);
-    mbar_init(bar_mma, 1);
+    const int counts[NUM_BARS] = {1, 128, 128, 1, 1, 1, 1, 128, 1, 1, 128, 128, 1, 128, 1, 128, 1, 1};
+    for (int i = 0; i < NUM_BARS; ++i) mbar_init(ctl.bar(i), counts[i]);
+    *ctl.abort = 0;
     fence_mbar_init();
-    prefetch_tmap(&tmB);
-    prefetch_tmap(&tmC);
+  }
+  if (FUSED && tid < kP) {
+    const int64_t d = int64_t(h) * kP + tid;
+    float* sw = reinterpret_cast<float*>(misc + kMiscW);
+#pragma unroll
+    for (int k = 0; k < kMaxK; ++k) sw[tid * kMaxK + k] = k < K ? conv_w[d * K + k] : 0.0f;
+    reinterpret_cast<float*>(misc + kMiscBias)[tid] = conv_b ? conv_b[d] : 0.0f;
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
-  const uint32_t tl = tm + (uint32_t(warp * 32) << 16);  // this warp's TMEM lanes
 
-  // the state row n = tid, fp32, for the whole sequence
-  float hreg[kP];
-  const int64_t hoff = (int64_t(b) * H + h) * kP * kN;
-#pragma unroll
-  for (int p = 0; p < kP; ++p) hreg[p] = h0 ? h0[hoff + int64_t(p) * kN + tid] : 0.0f;
-  write_h_rows(sm, tid, hreg);
-
-  uint32_t tma_phase = 0, mma_phase = 0;
-  bool failed = false;
-  const int nC = (L + kQ - 1) / kQ;
-  for (int c = 0; c < nC; ++c) {
-    const int t0 = c * kQ;
-    const int valid = min(kQ, L - t0);
-    if (tid == 0) {
-      mbar_arrive_expect_tx(bar_tma, 4u * 16384u);
-      tma_load_3d(sb + kOffC, &tmC, g * kN, t0, b, bar_tma);
-      tma_load_3d(sb + kOffC + 16384, &tmC, g * kN + 64, t0, b, bar_tma);
-      tma_load_3d(sb + kOffB, &tmB, g * kN, t0, b, bar_tma);
-      tma_load_3d(sb + kOffB + 16384, &tmB, g * kN + 64, t0, b, bar_tma);
-    }
-
-    // ---- log-decay prefix Lam_t over the chunk (padding tokens add 0) ----------
-    const float ell =
-        tid < valid ? __bfloat162float(dt[(int64_t(b) * L + t0 + tid) * H + h]) * Ah : 0.0f;
-    float v = ell;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float nb = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += nb;
-    }
-    if (lane == 31) red[warp] = v;
-    __syncthreads();
-    float lam_t = v;
-    for (int w = 0; w < warp; ++w) lam_t += red[w];
-    lam[tid] = lam_t;
-    float mn = lam_t, mx = lam_t;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (lane == 0) {
-      red[4 + warp] = mn;
-      red[8 + warp] = mx;
-    }
-    __syncthreads();
-    const float lam_min = fminf(fminf(red[4], red[5]), fminf(red[6], red[7]));
-    const float lam_max = fmaxf(fmaxf(red[8], red[9]), fmaxf(red[10], red[11]));
-    const float lam_end = lam[kQ - 1];
-    // exp(Lam_t - Lam_s) = f_t * g_s with a mid-range reference R keeps both
-    // factors inside fp32 while the chunk's decay range is below 160
-    const float R = 0.5f * (lam_min + lam_max);
-    const bool factored = (lam_max - lam_min) <= 160.0f;
-    gfac[tid] = expf(R - lam_t);
-    const float f_t = expf(lam_t - R);
-    const float dec_t = expf(lam_t);             // h_prev reaches token t as exp(Lam_t)
-    const float xdec = expf(lam_end - lam_t);    // token s reaches the chunk end
-    const float dec_end = expf(lam_end);
-
-    // ---- x row of token s = tid -> hi/lo of x and of x~ in [p][s] tiles ------
-    {
+  if (warp < 4) {
+    // ======================= producers: token s = tid =======================
+    const int s = tid;
+    float* red = reinterpret_cast<float*>(misc + kMiscRedP);
+    const float* sw = reinterpret_cast<const float*>(misc + kMiscW);
+    const float* sbias = reinterpret_cast<const float*>(misc + kMiscBias);
+    // on abort every loop below keeps running its named barriers with the
+    // work skipped, so no thread is ever left waiting at one
+    bool ok = true;
+    for (int c = 0; c < nC; ++c) {
+      const int t0 = c * kQ;
+      const int valid = min(kQ, L - t0);
+      const int tok = t0 + s;
+      const bool live = ok && s < valid;
+      const float ell = live ? __bfloat162float(dt[(int64_t(b) * L + tok) * H + h]) * Ah : 0.0f;
       float u[kP];
-      if (tid < valid) {
-        load_row64<TX>(x + (int64_t(b) * L + t0 + tid) * D + int64_t(h) * kP, u);
-      } else {
+      if (!live) {
 #pragma unroll
         for (int p = 0; p < kP; ++p) u[p] = 0.0f;
-      }
-      const uint32_t sblk = uint32_t(tid >> 6) * 8192u;
-      const uint32_t ins = uint32_t(tid & 63);
-      const uint32_t cc = ins >> 3, bo = (ins & 7u) * 2u;
+      } else if constexpr (!FUSED) {
+        load_row64<TX>(x + (int64_t(b) * L + tok) * D + int64_t(h) * kP, u);
+      } else {
+        // causal conv over the extended sequence [S, x]: token tok reads
+        // positions tok-(K-1) .. tok; positions < 0 come from the conv state.
+        // Eight channels (one 16-byte load per tap) at a time.
 #pragma unroll
-      for (int p = 0; p < kP; ++p) {
-        const uint32_t off = sblk + sw128(uint32_t(p), cc) + bo;
-        uint16_t uh, ul, xh, xl;
-        split(u[p], uh, ul);
-        split(u[p] * xdec, xh, xl);
-        *reinterpret_cast<uint16_t*>(sm + kOffUh + off) = uh;
-        *reinterpret_cast<uint16_t*>(sm + kOffUl + off) = ul;
-        *reinterpret_cast<uint16_t*>(sm + kOffXh + off) = xh;
-        *reinterpret_cast<uint16_t*>(sm + kOffXl + off) = xl;
+        for (int q = 0; q < 8; ++q) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[8 * q + e] = sbias[8 * q + e];
+#pragma unroll
+          for (int k = 0; k < kMaxK; ++k) {
+            if (k < K) {
+              const int pos = tok - (K - 1) + k;
+              float xv[8];
+              if (pos >= 0) {
+                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+                                            x + (int64_t(b) * L + pos) * D + int64_t(h) * kP) + q);
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  xv[2 * i] = __uint_as_float(w4[i] << 16);
+                  xv[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+                }
+              } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  xv[e] = conv_s_in ? to_f32(conv_s_in[(int64_t(b) * D + int64_t(h) * kP + 8 * q + e) *
+                                                           (K - 1) + (K - 1) + pos])
+                                    : 0.0f;
+              }
+#pragma unroll
+              for (int e = 0; e < 8; ++e) u[8 * q + e] = fmaf(sw[(8 * q + e) * kMaxK + k], xv[e], u[8 * q + e]);
+            }
+          }
+        }
+#pragma unroll
+        for (int p = 0; p < kP; ++p) u[p] = silu(u[p]);
+      }
+      float lam_end;
+      const float lam_s = role_prefix(ell, lane, warp, red + 4 * (c & 1), 1, &lam_end);
+      const float xdec = expf(lam_end - lam_s);
+      const int st = c & 1;
+      if (ok && c >= 2) ok = ctl.wait(BAR_U_FREE + st, uint32_t(((c >> 1) + 1) & 1));
+      if (ok) write_split_row(sm + kOffU + st * 32768, sm + kOffU + st * 32768 + 16384, s, u);
+#pragma unroll
+      for (int p = 0; p < kP; ++p) u[p] *= xdec;
+      if (ok && c >= 1) ok = ctl.wait(BAR_X_FREE, uint32_t((c - 1) & 1));
+      if (ok) {
+        write_split_row(sm + kOffX, sm + kOffX + 16384, s, u);
+        fence_proxy_async_smem();
+        mbar_arrive(ctl.bar(BAR_TILES + st));
       }
     }
-    fence_proxy_async_smem();
-    __syncthreads();
-
-    // ---- products that need only the inputs: G, S, Yo ---------------------------
-    bool ok = mbar_wait(bar_tma, tma_phase, kWaitNs);
-    tma_phase ^= 1u;
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
+    if constexpr (FUSED) {
+      // final conv state F_j = ext[L + j]; every read of S happened in chunk 0
+      role_sync(1);
+      if (conv_s_out && s < kP && !*ctl.abort) {
+        const int64_t d = int64_t(h) * kP + s;
+        TX f[kMaxK - 1];
+        for (int j = 0; j < K - 1; ++j) {
+          const int e = L + j;  // extended-sequence index
+          f[j] = e < K - 1 ? (conv_s_in ? conv_s_in[(int64_t(b) * D + d) * (K - 1) + e]
+                                        : from_f32<TX>(0.0f))
+                           : x[(int64_t(b) * L + (e - (K - 1))) * D + d];
+        }
+        for (int j = 0; j < K - 1; ++j) conv_s_out[(int64_t(b) * D + d) * (K - 1) + j] = f[j];
+      }
     }
-    if (tid == 0) {
+  } else if (warp < 8) {
+    // ===== consumers: TMEM lane r = row t (mask, y) = state row n (S, h) =====
+    const int r = tid - 128, wq = warp - 4;
+    const uint32_t tl = tm + (uint32_t(wq * 32) << 16);
+    float* red = reinterpret_cast<float*>(misc + kMiscRedE);
+    float* lamE = reinterpret_cast<float*>(misc + kMiscLam);
+    float hreg[kP];
+    const int64_t hoff = (int64_t(b) * H + h) * kP * kN;
+#pragma unroll
+    for (int p = 0; p < kP; ++p) hreg[p] = h0 ? h0[hoff + int64_t(p) * kN + r] : 0.0f;
+    write_split_row(sm + kOffH, sm + kOffH + 16384, r, hreg);
+    fence_proxy_async_smem();
+    mbar_arrive(ctl.bar(BAR_H_FULL));
+    {  // blocks of G o M above the diagonal of this warp's rows stay zero
+      uint32_t z[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) z[i] = 0u;
+      for (int j = wq + 1; j < 4; ++j) {
+        tmem_st_x16(tl + kColGh + 16u * j, z);
+        tmem_st_x16(tl + kColGl + 16u * j, z);
+      }
+      tmem_st_wait();
+    }
+    bool ok = true;
+    for (int c = 0; c < nC; ++c) {
+      const int t0 = c * kQ;
+      const int valid = min(kQ, L - t0);
+      const float ell =
+          ok && r < valid ? __bfloat162float(dt[(int64_t(b) * L + t0 + r) * H + h]) * Ah : 0.0f;
+      float lam_end;
+      const float lam_t = role_prefix(ell, lane, wq, red + 4 * (c & 1), 2, &lam_end);
+      float* lam = lamE + 128 * (c & 1);
+      lam[r] = lam_t;
+      role_sync(2);
+      // ---- decay mask: row t = r, columns s <= t --------------------------
+      // (ok is made warp-uniform before every warp-collective TMEM access)
+      if (ok) ok = ctl.wait(BAR_G_FULL, uint32_t(c & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        for (int j = 0; j <= wq; ++j) {
+          uint32_t graw[32], ph[16], pl[16];
+          tmem_ld_x32(tl + kColG + 32u * j, graw);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float m[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int s = 32 * j + 2 * i + e;
+              m[e] = s <= r ? __uint_as_float(graw[2 * i + e]) * __expf(lam_t - lam[s]) : 0.0f;
+            }
+            split2(m[0], m[1], ph[i], pl[i]);
+          }
+          tmem_st_x16(tl + kColGh + 16u * j, ph);
+          tmem_st_x16(tl + kColGl + 16u * j, pl);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(ctl.bar(BAR_GM_FULL));
+      }
+      // ---- state carry: row n = r ------------------------------------------
+      const int st = c & 1;
+      if (ok) ok = ctl.wait(BAR_S_FULL + st, uint32_t((c >> 1) & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float dec_end = expf(lam_end);
+        uint32_t r0[32], r1[32];
+        tmem_ld_x32(tl + kColS + 64u * st, r0);
+        tmem_ld_x32(tl + kColS + 64u * st + 32u, r1);
+#pragma unroll
+        for (int p = 0; p < 32; ++p) {
+          hreg[p] = fmaf(dec_end, hreg[p], __uint_as_float(r0[p]));
+          hreg[p + 32] = fmaf(dec_end, hreg[p + 32], __uint_as_float(r1[p]));
+        }
+        tc_fence_before();
+        mbar_arrive(ctl.bar(BAR_S_FREE + st));
+      }
+      if (ok) ok = ctl.wait(BAR_YO_DONE, uint32_t(c & 1));  // Yo(c) has read h_{c-1}
+      if (ok) {
+        write_split_row(sm + kOffH, sm + kOffH + 16384, r, hreg);
+        fence_proxy_async_smem();
+        mbar_arrive(ctl.bar(BAR_H_FULL));
+      }
+      // ---- y rows ------------------------------------------------------------
+      if (ok) ok = ctl.wait(BAR_Y_FULL, uint32_t(c & 1));
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        const float dec_t = expf(lam_t);
+        float yv[kP];
+        uint32_t r0[32], r1[32];
+        tmem_ld_x32(tl + kColYd, r0);
+        tmem_ld_x32(tl + kColYd + 32u, r1);
+#pragma unroll
+        for (int p = 0; p < 32; ++p) {
+          yv[p] = __uint_as_float(r0[p]);
+          yv[p + 32] = __uint_as_float(r1[p]);
+        }
+        tmem_ld_x32(tl + kColYo, r0);
+        tmem_ld_x32(tl + kColYo + 32u, r1);
+        tc_fence_before();
+        mbar_arrive(ctl.bar(BAR_ACC_FREE));
+#pragma unroll
+        for (int p = 0; p < 32; ++p) {
+          yv[p] = fmaf(dec_t, __uint_as_float(r0[p]), yv[p]);
+          yv[p + 32] = fmaf(dec_t, __uint_as_float(r1[p]), yv[p + 32]);
+        }
+        if (r < valid) store_row64<TY>(y + (int64_t(b) * L + t0 + r) * D + int64_t(h) * kP, yv);
+      }
+    }
+    if (ok && hT) {
+#pragma unroll
+      for (int p = 0; p < kP; ++p) hT[hoff + int64_t(p) * kN + r] = hreg[p];
+    }
+  } else {
+   if (lane == 0) {
+    // ========================= issuer (one thread) =========================
+    auto tma_chunk = [&](int c) {
+      mbar_arrive_expect_tx(ctl.bar(BAR_FULL_CB), 4u * 16384u);
+      const int t0 = c * kQ;
+      tma_load_3d(sb + kOffC, &tmC, g * kN, t0, b, ctl.bar(BAR_FULL_CB));
+      tma_load_3d(sb + kOffC + 16384, &tmC, g * kN + 64, t0, b, ctl.bar(BAR_FULL_CB));
+      tma_load_3d(sb + kOffB, &tmB, g * kN, t0, b, ctl.bar(BAR_FULL_CB));
+      tma_load_3d(sb + kOffB + 16384, &tmB, g * kN + 64, t0, b, ctl.bar(BAR_FULL_CB));
+    };
+    prefetch_tmap(&tmB);
+    prefetch_tmap(&tmC);
+    tma_chunk(0);
+    int tma_issued = 1, tma_landed = 0;
+    for (int c = 0; c < nC; ++c) {
+      const int st = c & 1;
+      if (!ctl.wait(BAR_FULL_CB, uint32_t(c & 1))) break;
+      tma_landed = c + 1;
+      if (!ctl.wait(BAR_TILES + st, uint32_t((c >> 1) & 1))) break;
+      if (c >= 2 && !ctl.wait(BAR_S_FREE + st, uint32_t(((c >> 1) + 1) & 1))) break;
       tc_fence_after();
+      // G = C B^T
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ss(tm + kColG, kdesc(sb + kOffC, kk, 16384), kdesc(sb + kOffB, kk, 16384), kIdG, kk);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // B^T as an MN-major A operand: rows s, n blocks 16 KB apart
-        mma_ss(tm + kColS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024),
-               kdesc(sb + kOffXh, kk, 8192), kIdS, kk);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024),
-               kdesc(sb + kOffXl, kk, 8192), kIdS, 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // h^T as an MN-major B operand: rows n
-        mma_ss(tm + kColYo, kdesc(sb + kOffC, kk, 16384),
-               sdesc_sw128(sb + kOffHh + kk * 2048, 8192, 1024), kIdYo, kk);
+      mma_commit(ctl.bar(BAR_G_FULL));
+      // S^T = B^T (x~hi + x~lo); B^T is the MN-major view of the B chunk
+      const uint32_t dS = tm + kColS + 64u * st;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColYo, kdesc(sb + kOffC, kk, 16384),
-               sdesc_sw128(sb + kOffHl + kk * 2048, 8192, 1024), kIdYo, 1);
-      mma_commit(bar_mma);
-    }
-    ok = mbar_wait(bar_mma, mma_phase, kWaitNs);
-    mma_phase ^= 1u;
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-
-    // ---- decay mask on G (row t = tid) -> hi/lo bf16 pairs in TMEM ------------
+        mma_ss(dS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(sb + kOffX, kk), kIdS, kk);
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {  // s in [32 j, 32 j + 32)
-      uint32_t ph[16], pl[16];
-      if (j <= warp) {
-        uint32_t graw[32];
-        tmem_ld_x32(tl + kColG + 32u * j, graw);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          uint16_t hh[2], ll[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int s = 32 * j + 2 * i + e;
-            float m = 0.0f;
-            if (s <= tid) {
-              const float wgt = factored ? f_t * gfac[s] : expf(lam_t - lam[s]);
-              m = __uint_as_float(graw[2 * i + e]) * wgt;
-            }
-            split(m, hh[e], ll[e]);
-          }
-          ph[i] = pack2(hh[0], hh[1]);
-          pl[i] = pack2(ll[0], ll[1]);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) ph[i] = pl[i] = 0u;
-      }
-      tmem_st_x16(tl + kColGh + 16u * j, ph);
-      tmem_st_x16(tl + kColGl + 16u * j, pl);
-    }
-    tmem_st_wait();
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- Yd = (G o M) x: hi*hi + hi*lo + lo*hi --------------------------------
-    if (tid == 0) {
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(dS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(sb + kOffX + 16384, kk),
+               kIdS, 1);
+      mma_commit(ctl.bar(BAR_X_FREE));
+      mma_commit(ctl.bar(BAR_S_FULL + st));
+      // Yo = C (h_hi + h_lo)^T, once h_{c-1} is in place and Yo is free
+      if (!ctl.wait(BAR_H_FULL, uint32_t(c & 1))) break;
+      if (c >= 1 && !ctl.wait(BAR_ACC_FREE, uint32_t((c - 1) & 1))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tm + kColYd, tm + kColGh + 8u * kk, kdesc(sb + kOffUh, kk, 8192), kIdYd, kk);
+        mma_ss(tm + kColYo, kdesc(sb + kOffC, kk, 16384), mndesc(sb + kOffH, kk), kIdYo, kk);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tm + kColYd, tm + kColGh + 8u * kk, kdesc(sb + kOffUl, kk, 8192), kIdYd, 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tm + kColYd, tm + kColGl + 8u * kk, kdesc(sb + kOffUh, kk, 8192), kIdYd, 1);
-      mma_commit(bar_mma);
-    }
-    ok = mbar_wait(bar_mma, mma_phase, kWaitNs);
-    mma_phase ^= 1u;
-    if (__syncthreads_or(!ok)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-
-    // ---- epilogue: y row t = tid, state row n = tid ----------------------------
-    {
-      float yv[kP];
-      uint32_t r0[32], r1[32];
-      tmem_ld_x32(tl + kColYd, r0);
-      tmem_ld_x32(tl + kColYd + 32, r1);
-#pragma unroll
-      for (int p = 0; p < 32; ++p) {
-        yv[p] = __uint_as_float(r0[p]);
-        yv[p + 32] = __uint_as_float(r1[p]);
+        mma_ss(tm + kColYo, kdesc(sb + kOffC, kk, 16384), mndesc(sb + kOffH + 16384, kk), kIdYo, 1);
+      mma_commit(ctl.bar(BAR_YO_DONE));
+      mma_commit(ctl.bar(BAR_CB_FREE));
+      // the next chunk's B and C as soon as this chunk's readers are done
+      if (c + 1 < nC) {
+        if (!ctl.wait(BAR_CB_FREE, uint32_t(c & 1))) break;
+        tma_chunk(c + 1);
+        tma_issued = c + 2;
       }
-      tmem_ld_x32(tl + kColYo, r0);
-      tmem_ld_x32(tl + kColYo + 32, r1);
+      // Yd = (G o M)(x_hi + x_lo), hi*hi + hi*lo + lo*hi
+      if (!ctl.wait(BAR_GM_FULL, uint32_t(c & 1))) break;
+      tc_fence_after();
+      const uint32_t uh = sb + kOffU + st * 32768, ul = uh + 16384;
 #pragma unroll
-      for (int p = 0; p < 32; ++p) {
-        yv[p] = fmaf(dec_t, __uint_as_float(r0[p]), yv[p]);
-        yv[p + 32] = fmaf(dec_t, __uint_as_float(r1[p]), yv[p + 32]);
-      }
-      if (tid < valid) store_row64<TY>(y + (int64_t(b) * L + t0 + tid) * D + int64_t(h) * kP, yv);
-      tmem_ld_x32(tl + kColS, r0);
-      tmem_ld_x32(tl + kColS + 32, r1);
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(uh, kk), kIdYd, kk);
 #pragma unroll
-      for (int p = 0; p < 32; ++p) {
-        hreg[p] = fmaf(dec_end, hreg[p], __uint_as_float(r0[p]));
-        hreg[p + 32] = fmaf(dec_end, hreg[p + 32], __uint_as_float(r1[p]));
-      }
-      write_h_rows(sm, tid, hreg);
-      fence_proxy_async_smem();
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(ul, kk), kIdYd, 1);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, mndesc(uh, kk), kIdYd, 1);
+      mma_commit(ctl.bar(BAR_Y_FULL));
+      mma_commit(ctl.bar(BAR_U_FREE + st));
     }
-    tc_fence_before();
-    __syncthreads();
-  }
-
-  if (failed) {
-    // let whatever is still in flight land before the memory is released
-    if (tid == 0) {
-      raise_status(status, SSS_ERR_TIMEOUT);
-      mbar_wait(bar_mma, mma_phase ^ 1u, kWaitNs / 2);
-      mbar_wait(bar_tma, tma_phase ^ 1u, kWaitNs / 2);
-    }
-  } else if (hT) {
-#pragma unroll
-    for (int p = 0; p < kP; ++p) hT[hoff + int64_t(p) * kN + tid] = hreg[p];
+    // every MMA of this CTA (and a TMA still in flight) lands before the
+    // tensor memory and shared memory are released
+    mma_commit(ctl.bar(BAR_DRAIN));
+    mbar_wait(ctl.bar(BAR_DRAIN), 0, kWaitNs);
+    if (tma_issued > tma_landed)
+      mbar_wait(ctl.bar(BAR_FULL_CB), uint32_t(tma_landed & 1), kWaitNs / 2);
+   }
+   __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tm, kTmemCols);
+  if (warp == 8) tmem_dealloc(tm, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
-// operand-layout self-test: the four descriptor forms of the scan on one tile
+// operand-layout self-test: the descriptor forms of the scan on one tile
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(128, 1)
 tc_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -482,11 +617,11 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       w[e] = pack2(B16[(8 * c + 2 * e) * 128 + tid], B16[(8 * c + 2 * e + 1) * 128 + tid]);
     *reinterpret_cast<uint4*>(sm + oBt + sw128(tid, c)) = make_uint4(w[0], w[1], w[2], w[3]);
   }
-  // A row m = tid into TMEM as bf16 pairs (columns 320..383)
+  // A row m = tid into TMEM as bf16 pairs (columns 448..511)
   for (int j = 0; j < 4; ++j) {
     uint32_t w[16];
     for (int i = 0; i < 16; ++i) w[i] = pack2(A16[tid * 128 + 32 * j + 2 * i], A16[tid * 128 + 32 * j + 2 * i + 1]);
-    tmem_st_x16(tl + 320u + 16u * j, w);
+    tmem_st_x16(tl + 448u + 16u * j, w);
   }
   tmem_st_wait();
   fence_proxy_async_smem();
@@ -496,16 +631,19 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   if (!__syncthreads_or(!ok)) {
     if (tid == 0) {
       tc_fence_after();
-      for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < 8; ++kk)  // [0] K-major A, K-major B, N = 128
         mma_ss(tm + 0, kdesc(sb + oA, kk, 16384), kdesc(sb + oB, kk, 16384), kIdG, kk);
-      for (int kk = 0; kk < 8; ++kk)
+      for (int kk = 0; kk < 8; ++kk)  // [1] MN-major A, K-major B
         mma_ss(tm + 128, sdesc_sw128(sb + oAt + kk * 2048, 16384, 1024), kdesc(sb + oB, kk, 16384),
-               kIdS, kk);
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + 192, kdesc(sb + oA, kk, 16384), sdesc_sw128(sb + oBt + kk * 2048, 8192, 1024),
-               kIdYo, kk);
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tm + 256, tm + 320u + 8u * kk, kdesc(sb + oB, kk, 16384), kIdYd, kk);
+               idesc_bf16(128, 64, 1, 0), kk);
+      for (int kk = 0; kk < 8; ++kk)  // [2] K-major A, MN-major B
+        mma_ss(tm + 192, kdesc(sb + oA, kk, 16384), mndesc(sb + oBt, kk), kIdYo, kk);
+      for (int kk = 0; kk < 8; ++kk)  // [3] A from TMEM, K-major B
+        mma_ts(tm + 256, tm + 448u + 8u * kk, kdesc(sb + oB, kk, 16384), idesc_bf16(128, 64, 0, 0), kk);
+      for (int kk = 0; kk < 8; ++kk)  // [4] A from TMEM, MN-major B
+        mma_ts(tm + 320, tm + 448u + 8u * kk, mndesc(sb + oBt, kk), kIdYd, kk);
+      for (int kk = 0; kk < 8; ++kk)  // [5] MN-major A, MN-major B
+        mma_ss(tm + 384, sdesc_sw128(sb + oAt + kk * 2048, 16384, 1024), mndesc(sb + oBt, kk), kIdS, kk);
       mma_commit(bar_mma);
     }
     ok = mbar_wait(bar_mma, 0, kWaitNs);
@@ -514,9 +652,9 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
       uint32_t r[32];
       for (int j = 0; j < 4; ++j) {
         tmem_ld_x32(tl + 32u * j, r);
-        for (int i = 0; i < 32; ++i) out[0 * 16384 + tid * 128 + 32 * j + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 32; ++i) out[tid * 128 + 32 * j + i] = __uint_as_float(r[i]);
       }
-      for (int t = 1; t < 4; ++t)
+      for (int t = 1; t < 6; ++t)
         for (int j = 0; j < 2; ++j) {
           tmem_ld_x32(tl + 128u + 64u * (t - 1) + 32u * j, r);
           for (int i = 0; i < 32; ++i) out[t * 16384 + tid * 128 + 32 * j + i] = __uint_as_float(r[i]);
@@ -576,21 +714,22 @@ bool make_tile_map(CUtensorMap* m, const void* ptr) {  // [128][128] bf16
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename TX, typename TY>
+template <typename TX, typename TY, bool FUSED>
 cudaError_t launch_tc(const void* x, const void* dt, const float* A, const void* B, const void* C,
-                      const float* h0, float* hT, void* y, int64_t Bz, int64_t L, int H, int G,
+                      const float* h0, float* hT, void* y, const float* w, const float* bias,
+                      const void* s_in, void* s_out, int K, int64_t Bz, int64_t L, int H, int G,
                       int* status, cudaStream_t st) {
   CUtensorMap mB, mC;
   if (!make_bc_map(&mB, B, Bz, L, G, kN) || !make_bc_map(&mC, C, Bz, L, G, kN))
     return cudaErrorInvalidValue;
-  auto kern = ssm_scan_tc_kernel<TX, TY>;
+  auto kern = ssm_scan_tc_kernel<TX, TY, FUSED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
   if (e != cudaSuccess) return e;
-  const int64_t grid = Bz * H;
-  kern<<<unsigned(grid), kThreads, kSmemBytes, st>>>(
+  kern<<<unsigned(Bz * H), kThreads, kSmemBytes, st>>>(
       mB, mC, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, h0, hT,
-      static_cast<TY*>(y), int(L), H, G, status);
+      static_cast<TY*>(y), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out), K,
+      int(L), H, G, status);
   return cudaGetLastError();
 }
 }  // namespace
@@ -602,19 +741,38 @@ bool ssm_scan_tc_supports(sss_dtype xt, sss_dtype at, sss_dtype yt, int64_t L, i
          G >= 1 && H % G == 0 && encode_fn() != nullptr;
 }
 
+bool mixer_fwd_tc_supports(sss_dtype xt, sss_dtype at, int K, int64_t L, int H, int P, int N,
+                           int G) {
+  return xt == SSS_BF16 && K >= 1 && K <= kMaxK && ssm_scan_tc_supports(xt, at, at, L, H, P, N, G);
+}
+
 cudaError_t ssm_scan_tc_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                const void* B, const void* C, const float* h0, float* hT,
                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int P,
                                int N, int G, int* status, cudaStream_t st) {
   (void)P; (void)N;
   if (Bz * H > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  if (xt == SSS_F32 && yt == SSS_BF16)
-    return launch_tc<float, __nv_bfloat16>(x, dt, A, B, C, h0, hT, y, Bz, L, H, G, status, st);
-  if (xt == SSS_F32)
-    return launch_tc<float, float>(x, dt, A, B, C, h0, hT, y, Bz, L, H, G, status, st);
+#define SSS_TC(TXT, TYT)                                                                    \
+  return launch_tc<TXT, TYT, false>(x, dt, A, B, C, h0, hT, y, nullptr, nullptr, nullptr,  \
+                                    nullptr, 1, Bz, L, H, G, status, st);
+  if (xt == SSS_F32 && yt == SSS_BF16) SSS_TC(float, __nv_bfloat16)
+  if (xt == SSS_F32) SSS_TC(float, float)
+  if (yt == SSS_BF16) SSS_TC(__nv_bfloat16, __nv_bfloat16)
+  SSS_TC(__nv_bfloat16, float)
+#undef SSS_TC
+}
+
+cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias,
+                                const void* s_in, void* s_out, const void* dt, const float* A,
+                                const void* B, const void* C, const float* h0, float* hT,
+                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G, int K,
+                                int* status, cudaStream_t st) {
+  if (Bz * H > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (yt == SSS_BF16)
-    return launch_tc<__nv_bfloat16, __nv_bfloat16>(x, dt, A, B, C, h0, hT, y, Bz, L, H, G, status, st);
-  return launch_tc<__nv_bfloat16, float>(x, dt, A, B, C, h0, hT, y, Bz, L, H, G, status, st);
+    return launch_tc<__nv_bfloat16, __nv_bfloat16, true>(x, dt, A, B, C, h0, hT, y, w, bias, s_in,
+                                                         s_out, K, Bz, L, H, G, status, st);
+  return launch_tc<__nv_bfloat16, float, true>(x, dt, A, B, C, h0, hT, y, w, bias, s_in, s_out, K,
+                                               Bz, L, H, G, status, st);
 }
 
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,

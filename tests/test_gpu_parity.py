@@ -151,7 +151,7 @@ def test_scan_state_aliasing():
 # streaming forward: conv + scan with both states passed
 # ---------------------------------------------------------------------------
 
-def _run_stream(s, heads=None, batches=None):
+def _run_stream(s, heads=None, batches=None, fused=None):
     """Run every segment of workload ``s`` on the GPU with the states passed in
     place; return the y of each segment (sliced to the sampled heads/batches),
     the final states, and the oracle's results for the same slices."""
@@ -171,7 +171,7 @@ def _run_stream(s, heads=None, batches=None):
     for i in range(len(s.segments)):
         seg = synth.mixer_segment(s, i)
         y, S, h = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), A, T(seg["B"]), T(seg["C"]), w, bias,
-                                S, h, conv_state_out=S, hT=h)
+                                S, h, conv_state_out=S, hT=h, fused=fused)
         x_r = seg["x"].f64()[batches][:, :, chan]
         dt_r = seg["dt"].f64()[batches][:, :, heads]
         B_r = seg["B"].f64()[batches][:, :, gid]
@@ -226,13 +226,40 @@ def test_long_context_streaming_sampled():
     assert_rel(hg, h_ref, STATE_REL, "final SSM state")
 
 
-def test_reduced_workload_all_heads():
+@pytest.mark.parametrize("fused", [True, False])
+def test_reduced_workload_all_heads(fused):
     """370M-like recipe at a size the oracle finishes in a second, every
-    output element compared; L not a multiple of any chunk length."""
+    output element compared; L not a multiple of any chunk length; the
+    single-kernel forward and the two-call composition."""
     s = synth.WORKLOADS["m370m_2k"].with_(Bz=2, segments=(333, 700), H=4,
                                           gaussian_init=True)
-    hg, h_ref = _run_stream(s)
+    hg, h_ref = _run_stream(s, fused=fused)
     assert_rel(hg, h_ref, STATE_REL, "final SSM state")
+
+
+@pytest.mark.parametrize("segments", [(1, 2, 3, 5), (127, 1, 128), (129, 300), (2, 256)])
+def test_fused_forward_short_and_ragged_segments(segments):
+    """Segments shorter than the conv window (the final conv state then keeps
+    part of the passed state), exactly one chunk, one token past a chunk."""
+    s = synth.WORKLOADS["m370m_2k"].with_(Bz=2, segments=segments, H=2, gaussian_init=True)
+    hg, h_ref = _run_stream(s, fused=True)
+    assert_rel(hg, h_ref, STATE_REL, "final SSM state")
+
+
+def test_fused_forward_without_states_and_separate_outputs():
+    """NULL initial states mean zeros; outputs in fresh buffers (no aliasing)."""
+    s = synth.WORKLOADS["m370m_2k"].with_(Bz=1, segments=(200,), H=3)
+    p = synth.mixer_params(s)
+    seg = synth.mixer_segment(s, 0)
+    y_ref, F_ref, h_ref = oracle.mixer_fwd(seg["x"], seg["dt"], p["A"], seg["B"], seg["C"],
+                                           p["w"], p["bias"], None, None)
+    y, F, h = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), T(p["A"]), T(seg["B"]), T(seg["C"]),
+                            T(p["w"]), T(p["bias"]), None, None, fused=True)
+    torch.cuda.synchronize()
+    assert_y_close(f64(y), y_ref)
+    np.testing.assert_array_equal(f64(F), F_ref)
+    assert_rel(f64(h), h_ref, STATE_REL, "hT")
+    assert sss.device_status() == 0
 
 
 # ---------------------------------------------------------------------------

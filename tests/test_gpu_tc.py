@@ -27,7 +27,8 @@ def test_tcgen05_operand_layouts():
     torch.cuda.synchronize()
     assert sss.device_status() == 0
     ref = (A.double() @ B.double().T).float()
-    names = ["K-major A and B", "MN-major A", "MN-major B", "A from tensor memory"]
+    names = ["K-major A and B", "MN-major A", "MN-major B", "A from tensor memory",
+             "A from tensor memory, MN-major B", "MN-major A and B"]
     for i, name in enumerate(names):
         cols = 128 if i == 0 else 64
         err = (out[i, :, :cols] - ref[:, :cols]).abs().max().item()
