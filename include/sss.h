@@ -57,6 +57,10 @@ int sss_version(void);
 /* Static string for a status value (bits may be OR-ed together). */
 const char* sss_status_string(int status);
 
+/* Text of the last CUDA runtime error a call of this thread turned into
+ * SSS_ERR_CUDA (or SSS_ERR_UNSUPPORTED). */
+const char* sss_last_cuda_error(void);
+
 /*
  * sss_conv_state_fwd -- causal depthwise conv1d with an explicit conv state.
  *

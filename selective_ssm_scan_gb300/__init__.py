@@ -46,6 +46,7 @@ _i = ctypes.c_int
 _lib.sss_version.restype = _i
 _lib.sss_status_string.restype = ctypes.c_char_p
 _lib.sss_status_string.argtypes = [_i]
+_lib.sss_last_cuda_error.restype = ctypes.c_char_p
 _lib.sss_conv_state_fwd.restype = _i
 _lib.sss_conv_state_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _i, _i64, _i64, _i64, _i, _i, _p]
 _lib.sss_ssm_scan_workspace_size.restype = ctypes.c_size_t
@@ -71,7 +72,10 @@ _lib.sss_device_status.argtypes = [ctypes.POINTER(_i), _i, _p]
 
 class SSSError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        msg = f"{fn}: {status_string(status)} (status {status})"
+        if status & SSS_ERR_CUDA:
+            msg += f": {_lib.sss_last_cuda_error().decode()}"
+        super().__init__(msg)
         self.status = status
 
 

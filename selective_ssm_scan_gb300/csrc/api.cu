@@ -82,8 +82,11 @@ static bool aligned(const void* p, size_t a) {
   return (reinterpret_cast<uintptr_t>(p) % a) == 0;
 }
 
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
 static sss_status from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return SSS_OK;
+  g_last_cuda_error = e;
   if (e == cudaErrorNotSupported) {
     cudaGetLastError();
     return SSS_ERR_UNSUPPORTED;
@@ -98,6 +101,8 @@ using namespace sss;
 extern "C" {
 
 int sss_version(void) { return 100; }
+
+const char* sss_last_cuda_error(void) { return cudaGetErrorString(sss::g_last_cuda_error); }
 
 const char* sss_status_string(int s) {
   switch (s) {

@@ -72,15 +72,21 @@ constexpr uint32_t kOffU = 65536;     // x hi/lo, 2 stages x (hi 16 KB, lo 16 KB
 constexpr uint32_t kOffX = 131072;    // x~ hi (16 KB), lo (16 KB), rows s
 constexpr uint32_t kOffH = 163840;    // h hi (16 KB), lo (16 KB), rows n
 constexpr uint32_t kOffMisc = 196608;
-constexpr uint32_t kMiscLam = 0;       // [2][128] consumer Lam
-constexpr uint32_t kMiscRedP = 1024;   // [2][4]  producer scan scratch
-constexpr uint32_t kMiscRedE = 1056;   // [2][4]  consumer scan scratch
-constexpr uint32_t kMiscW = 1088;      // [64][4] conv weights of the head
-constexpr uint32_t kMiscBias = 2112;   // [64]
-constexpr uint32_t kMiscBars = 2368;   // 18 mbarriers
-constexpr uint32_t kMiscTmem = 2528;
-constexpr uint32_t kMiscAbort = 2532;
-constexpr uint32_t kSmemBytes = kOffMisc + 2560 + 1024;
+constexpr uint32_t kMiscLam = 0;       // [2][128] consumer Lam_t
+constexpr uint32_t kMiscGf = 1024;     // [2][128] consumer exp(R - Lam_s)
+constexpr uint32_t kMiscXd = 2048;     // [2][128] producer exp(Lam_end - Lam_s)
+constexpr uint32_t kMiscRedP = 3072;   // [2][12] producer scan scratch
+constexpr uint32_t kMiscRedE = 3168;   // [2][12] consumer scan scratch
+constexpr uint32_t kMiscW = 3264;      // [64][4] conv weights of the head
+constexpr uint32_t kMiscBias = 4288;   // [64]
+constexpr uint32_t kMiscBars = 4544;   // 18 mbarriers
+constexpr uint32_t kMiscTmem = 4688;
+constexpr uint32_t kMiscAbort = 4692;
+constexpr uint32_t kMiscBytes = 4800;
+constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
+// chunks whose log-decay range exceeds this use exp(Lam_t - Lam_s) per
+// element instead of the factored exp(Lam_t - R) exp(R - Lam_s)
+constexpr float kFactorRange = 160.0f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 // barriers
 enum {
@@ -104,10 +110,13 @@ __device__ __forceinline__ uint32_t pack2(uint16_t lo_elem, uint16_t hi_elem) {
   return uint32_t(lo_elem) | (uint32_t(hi_elem) << 16);
 }
 // (a, b) -> packed hi pair and lo pair: v == hi + lo to ~2^-16 relative
+// (one paired conversion for each half)
 __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const uint16_t ha = bf16_bits(a), hb = bf16_bits(b);
-  hi = pack2(ha, hb);
-  lo = pack2(bf16_bits(a - bf16_val(ha)), bf16_bits(b - bf16_val(hb)));
+  const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+  hi = *reinterpret_cast<const uint32_t*>(&h2);
+  const __nv_bfloat162 l2 =
+      __floats2bfloat162_rn(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
+  lo = *reinterpret_cast<const uint32_t*>(&l2);
 }
 
 // K-major descriptor of a [rows][128-element K] tile stored as two 64-wide K
@@ -159,17 +168,17 @@ __device__ __forceinline__ void load_row64<__nv_bfloat16>(const __nv_bfloat16* r
 }
 
 template <typename TY>
-__device__ __forceinline__ void store_row64(TY* row, const float* v);
+__device__ __forceinline__ void store_row32(TY* row, const float* v);
 template <>
-__device__ __forceinline__ void store_row64<float>(float* row, const float* v) {
+__device__ __forceinline__ void store_row32<float>(float* row, const float* v) {
 #pragma unroll
-  for (int q = 0; q < 16; ++q)
+  for (int q = 0; q < 8; ++q)
     reinterpret_cast<float4*>(row)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 template <>
-__device__ __forceinline__ void store_row64<__nv_bfloat16>(__nv_bfloat16* row, const float* v) {
+__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* row, const float* v) {
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     uint32_t w[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) w[k] = pack2(bf16_bits(v[8 * q + 2 * k]), bf16_bits(v[8 * q + 2 * k + 1]));
@@ -207,24 +216,38 @@ struct Ctl {
   }
 };
 
-// inclusive prefix of `v` over the 128 threads of a role (4 warps)
+// Inclusive prefix of `v` over the 128 threads of a role (4 warps); also the
+// total and the minimum / maximum of the prefix over the role.
 __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* red, int bar_id,
-                                             float* total) {
+                                             float* total, float* pmin, float* pmax) {
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const float nb = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += nb;
   }
+  float mn = v, mx = v;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  }
   if (lane == 31) red[wq] = v;
+  if (lane == 0) {
+    red[4 + wq] = mn;
+    red[8 + wq] = mx;
+  }
   role_sync(bar_id);
-  float off = 0.0f, tot = 0.0f;
+  float off = 0.0f, run = 0.0f, gmn = 3.0e38f, gmx = -3.0e38f;
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    const float r = red[w];
-    if (w < wq) off += r;
-    tot += r;
+    gmn = fminf(gmn, run + red[4 + w]);
+    gmx = fmaxf(gmx, run + red[8 + w]);
+    if (w < wq) off += red[w];
+    run += red[w];
   }
-  *total = tot;
+  *total = run;
+  *pmin = gmn;
+  *pmax = gmx;
   return v + off;
 }
 
@@ -233,7 +256,7 @@ __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* r
 // x: the scan input u [Bz, L, H, 64] (TX = float or bf16), or with FUSED the
 // raw input [Bz, L, H*64] (bf16) that the producers convolve (K <= 4, SiLU).
 template <typename TX, typename TY, bool FUSED>
-__global__ void __maxnreg__(224)
+__global__ void __launch_bounds__(kThreads, 1)
 ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                    const TX* __restrict__ x, const __nv_bfloat16* __restrict__ dt,
                    const float* __restrict__ A, const float* h0, float* hT,
@@ -267,8 +290,10 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
   if (FUSED && tid < kP) {
     const int64_t d = int64_t(h) * kP + tid;
     float* sw = reinterpret_cast<float*>(misc + kMiscW);
+    // taps right-aligned in a window of kMaxK (leading zero weights for K < kMaxK)
 #pragma unroll
-    for (int k = 0; k < kMaxK; ++k) sw[tid * kMaxK + k] = k < K ? conv_w[d * K + k] : 0.0f;
+    for (int k = 0; k < kMaxK; ++k)
+      sw[tid * kMaxK + k] = k >= kMaxK - K ? conv_w[d * K + k - (kMaxK - K)] : 0.0f;
     reinterpret_cast<float*>(misc + kMiscBias)[tid] = conv_b ? conv_b[d] : 0.0f;
   }
   tc_fence_before();
@@ -277,74 +302,136 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
   const uint32_t tm = *tmem_slot;
 
   if (warp < 4) {
-    // ======================= producers: token s = tid =======================
-    const int s = tid;
+    // ======================= producers =======================
+    // The prefix runs with one token per thread (s = tid); the inputs and the
+    // operand rows with thread (q, g) = 8 channels [8q, 8q+8) x 8 tokens
+    // [8g, 8g+8): every input element is loaded (and, fused, convolved in a
+    // register window) once, all loads of a chunk issued up front.
+    const int s = tid, q = tid & 7, g8 = tid >> 3;
     float* red = reinterpret_cast<float*>(misc + kMiscRedP);
-    const float* sw = reinterpret_cast<const float*>(misc + kMiscW);
-    const float* sbias = reinterpret_cast<const float*>(misc + kMiscBias);
+    float* xdP = reinterpret_cast<float*>(misc + kMiscXd);
+    float wk[kMaxK][8], bk[8];
+    if constexpr (FUSED) {
+      const float* sw = reinterpret_cast<const float*>(misc + kMiscW);
+      const float* sbias = reinterpret_cast<const float*>(misc + kMiscBias);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        bk[e] = sbias[8 * q + e];
+#pragma unroll
+        for (int k = 0; k < kMaxK; ++k) wk[k][e] = sw[(8 * q + e) * kMaxK + k];
+      }
+    }
     // on abort every loop below keeps running its named barriers with the
     // work skipped, so no thread is ever left waiting at one
     bool ok = true;
     for (int c = 0; c < nC; ++c) {
       const int t0 = c * kQ;
       const int valid = min(kQ, L - t0);
-      const int tok = t0 + s;
-      const bool live = ok && s < valid;
-      const float ell = live ? __bfloat162float(dt[(int64_t(b) * L + tok) * H + h]) * Ah : 0.0f;
-      float u[kP];
-      if (!live) {
+      const float ell =
+          ok && s < valid ? __bfloat162float(dt[(int64_t(b) * L + t0 + s) * H + h]) * Ah : 0.0f;
+      // ---- inputs of tokens [8 g8, 8 g8 + 8), channels [8 q, 8 q + 8) -------
+      float u[8][8];  // [token j][channel e]
+      const int tb = t0 + 8 * g8;          // first token of the group
+      const int nv = ok ? min(8, max(0, valid - 8 * g8)) : 0;  // live tokens
+      if constexpr (!FUSED) {
 #pragma unroll
-        for (int p = 0; p < kP; ++p) u[p] = 0.0f;
-      } else if constexpr (!FUSED) {
-        load_row64<TX>(x + (int64_t(b) * L + tok) * D + int64_t(h) * kP, u);
-      } else {
-        // causal conv over the extended sequence [S, x]: token tok reads
-        // positions tok-(K-1) .. tok; positions < 0 come from the conv state.
-        // Eight channels (one 16-byte load per tap) at a time.
+        for (int j = 0; j < 8; ++j) {
+          if (j < nv) {
+            const TX* row = x + (int64_t(b) * L + tb + j) * D + int64_t(h) * kP + 8 * q;
+            if constexpr (sizeof(TX) == 4) {
+              const float4 v0 = __ldg(reinterpret_cast<const float4*>(row));
+              const float4 v1 = __ldg(reinterpret_cast<const float4*>(row) + 1);
+              u[j][0] = v0.x; u[j][1] = v0.y; u[j][2] = v0.z; u[j][3] = v0.w;
+              u[j][4] = v1.x; u[j][5] = v1.y; u[j][6] = v1.z; u[j][7] = v1.w;
+            } else {
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(row));
+              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) u[8 * q + e] = sbias[8 * q + e];
-#pragma unroll
-          for (int k = 0; k < kMaxK; ++k) {
-            if (k < K) {
-              const int pos = tok - (K - 1) + k;
-              float xv[8];
-              if (pos >= 0) {
-                const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
-                                            x + (int64_t(b) * L + pos) * D + int64_t(h) * kP) + q);
-                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  xv[2 * i] = __uint_as_float(w4[i] << 16);
-                  xv[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-                }
-              } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  xv[e] = conv_s_in ? to_f32(conv_s_in[(int64_t(b) * D + int64_t(h) * kP + 8 * q + e) *
-                                                           (K - 1) + (K - 1) + pos])
-                                    : 0.0f;
+              for (int i = 0; i < 4; ++i) {
+                u[j][2 * i] = __uint_as_float(w4[i] << 16);
+                u[j][2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
               }
-#pragma unroll
-              for (int e = 0; e < 8; ++e) u[8 * q + e] = fmaf(sw[(8 * q + e) * kMaxK + k], xv[e], u[8 * q + e]);
             }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) u[j][e] = 0.0f;
           }
         }
+      } else {
+        // rows tb - (kMaxK-1) + i, i < 8 + kMaxK - 1; positions < 0 are the
+        // conv state (extended sequence [S, x]), positions >= L are unused
+        constexpr int NR = 8 + kMaxK - 1;
+        uint4 xr[NR];
 #pragma unroll
-        for (int p = 0; p < kP; ++p) u[p] = silu(u[p]);
+        for (int i = 0; i < NR; ++i) {
+          const int pos = tb - (kMaxK - 1) + i;
+          xr[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (nv > 0 && pos >= 0 && pos < tb + nv) {
+            xr[i] = __ldg(reinterpret_cast<const uint4*>(x + (int64_t(b) * L + pos) * D +
+                                                         int64_t(h) * kP + 8 * q));
+          } else if (nv > 0 && pos < 0 && pos >= -(K - 1) && conv_s_in) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2) {
+              const int64_t d0 = int64_t(b) * D + int64_t(h) * kP + 8 * q + 2 * i2;
+              const uint16_t lo = *reinterpret_cast<const uint16_t*>(&conv_s_in[d0 * (K - 1) + (K - 1) + pos]);
+              const uint16_t hi = *reinterpret_cast<const uint16_t*>(&conv_s_in[(d0 + 1) * (K - 1) + (K - 1) + pos]);
+              w4[i2] = pack2(lo, hi);
+            }
+            xr[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+        // window over the rows: token j uses rows j + k with the right-aligned
+        // taps (rows before the sequence are the state, zero-weighted for K < 4)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[j][e] = bk[e];
+#pragma unroll
+          for (int k = 0; k < kMaxK; ++k) {
+            const uint4 rv = xr[j + k];
+            const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              u[j][2 * i] = fmaf(wk[k][2 * i], __uint_as_float(w4[i] << 16), u[j][2 * i]);
+              u[j][2 * i + 1] =
+                  fmaf(wk[k][2 * i + 1], __uint_as_float(w4[i] & 0xFFFF0000u), u[j][2 * i + 1]);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[j][e] = j < nv ? silu(u[j][e]) : 0.0f;
+        }
       }
-      float lam_end;
-      const float lam_s = role_prefix(ell, lane, warp, red + 4 * (c & 1), 1, &lam_end);
-      const float xdec = expf(lam_end - lam_s);
+      // ---- Lam and the state-path decay of each token -----------------------
+      float lam_end, lmin, lmax;
+      const float lam_s = role_prefix(ell, lane, warp, red + 12 * (c & 1), 1, &lam_end, &lmin, &lmax);
+      float* xd = xdP + 128 * (c & 1);
+      xd[s] = expf(lam_end - lam_s);
+      role_sync(1);
       const int st = c & 1;
+      uint8_t* uh = sm + kOffU + st * 32768;
       if (ok && c >= 2) ok = ctl.wait(BAR_U_FREE + st, uint32_t(((c >> 1) + 1) & 1));
-      if (ok) write_split_row(sm + kOffU + st * 32768, sm + kOffU + st * 32768 + 16384, s, u);
+      if (ok) {
 #pragma unroll
-      for (int p = 0; p < kP; ++p) u[p] *= xdec;
+        for (int j = 0; j < 8; ++j) {
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) split2(u[j][2 * k], u[j][2 * k + 1], hw[k], lw[k]);
+          *reinterpret_cast<uint4*>(uh + sw128(8 * g8 + j, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(uh + 16384 + sw128(8 * g8 + j, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+      }
       if (ok && c >= 1) ok = ctl.wait(BAR_X_FREE, uint32_t((c - 1) & 1));
       if (ok) {
-        write_split_row(sm + kOffX, sm + kOffX + 16384, s, u);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float f = xd[8 * g8 + j];
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) split2(u[j][2 * k] * f, u[j][2 * k + 1] * f, hw[k], lw[k]);
+          *reinterpret_cast<uint4*>(sm + kOffX + sw128(8 * g8 + j, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(sm + kOffX + 16384 + sw128(8 * g8 + j, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
         fence_proxy_async_smem();
         mbar_arrive(ctl.bar(BAR_TILES + st));
       }
@@ -370,6 +457,7 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
     const uint32_t tl = tm + (uint32_t(wq * 32) << 16);
     float* red = reinterpret_cast<float*>(misc + kMiscRedE);
     float* lamE = reinterpret_cast<float*>(misc + kMiscLam);
+    float* gfE = reinterpret_cast<float*>(misc + kMiscGf);
     float hreg[kP];
     const int64_t hoff = (int64_t(b) * H + h) * kP * kN;
 #pragma unroll
@@ -393,10 +481,17 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       const int valid = min(kQ, L - t0);
       const float ell =
           ok && r < valid ? __bfloat162float(dt[(int64_t(b) * L + t0 + r) * H + h]) * Ah : 0.0f;
-      float lam_end;
-      const float lam_t = role_prefix(ell, lane, wq, red + 4 * (c & 1), 2, &lam_end);
+      float lam_end, lmin, lmax;
+      const float lam_t = role_prefix(ell, lane, wq, red + 12 * (c & 1), 2, &lam_end, &lmin, &lmax);
+      // exp(Lam_t - Lam_s) = f_t g_s with the mid-range reference R: both
+      // factors stay within exp(+-80) while the chunk's range is <= 160
+      const bool factored = (lmax - lmin) <= kFactorRange;
+      const float R = 0.5f * (lmin + lmax);
+      const float f_t = expf(lam_t - R);
       float* lam = lamE + 128 * (c & 1);
+      float* gf = gfE + 128 * (c & 1);
       lam[r] = lam_t;
+      gf[r] = expf(R - lam_t);
       role_sync(2);
       // ---- decay mask: row t = r, columns s <= t --------------------------
       // (ok is made warp-uniform before every warp-collective TMEM access)
@@ -407,15 +502,27 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         for (int j = 0; j <= wq; ++j) {
           uint32_t graw[32], ph[16], pl[16];
           tmem_ld_x32(tl + kColG + 32u * j, graw);
+          const bool diag = (j == wq);
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float m[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int s = 32 * j + 2 * i + e;
-              m[e] = s <= r ? __uint_as_float(graw[2 * i + e]) * __expf(lam_t - lam[s]) : 0.0f;
+            const int s0 = 32 * j + 2 * i;
+            float w0, w1;
+            if (factored) {
+              const float2 g2 = *reinterpret_cast<const float2*>(gf + s0);
+              w0 = f_t * g2.x;
+              w1 = f_t * g2.y;
+            } else {
+              const float2 l2 = *reinterpret_cast<const float2*>(lam + s0);
+              w0 = __expf(lam_t - l2.x);
+              w1 = __expf(lam_t - l2.y);
             }
-            split2(m[0], m[1], ph[i], pl[i]);
+            float m0 = __uint_as_float(graw[2 * i]) * w0;
+            float m1 = __uint_as_float(graw[2 * i + 1]) * w1;
+            if (diag) {
+              m0 = s0 <= r ? m0 : 0.0f;
+              m1 = s0 + 1 <= r ? m1 : 0.0f;
+            }
+            split2(m0, m1, ph[i], pl[i]);
           }
           tmem_st_x16(tl + kColGh + 16u * j, ph);
           tmem_st_x16(tl + kColGl + 16u * j, pl);
@@ -431,13 +538,13 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       if (ok) {
         tc_fence_after();
         const float dec_end = expf(lam_end);
-        uint32_t r0[32], r1[32];
-        tmem_ld_x32(tl + kColS + 64u * st, r0);
-        tmem_ld_x32(tl + kColS + 64u * st + 32u, r1);
 #pragma unroll
-        for (int p = 0; p < 32; ++p) {
-          hreg[p] = fmaf(dec_end, hreg[p], __uint_as_float(r0[p]));
-          hreg[p + 32] = fmaf(dec_end, hreg[p + 32], __uint_as_float(r1[p]));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r0[32];
+          tmem_ld_x32(tl + kColS + 64u * st + 32u * hf, r0);
+#pragma unroll
+          for (int p = 0; p < 32; ++p)
+            hreg[32 * hf + p] = fmaf(dec_end, hreg[32 * hf + p], __uint_as_float(r0[p]));
         }
         tc_fence_before();
         mbar_arrive(ctl.bar(BAR_S_FREE + st));
@@ -454,25 +561,21 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       if (ok) {
         tc_fence_after();
         const float dec_t = expf(lam_t);
-        float yv[kP];
-        uint32_t r0[32], r1[32];
-        tmem_ld_x32(tl + kColYd, r0);
-        tmem_ld_x32(tl + kColYd + 32u, r1);
+        TY* yrow = y + (int64_t(b) * L + t0 + r) * D + int64_t(h) * kP;
 #pragma unroll
-        for (int p = 0; p < 32; ++p) {
-          yv[p] = __uint_as_float(r0[p]);
-          yv[p + 32] = __uint_as_float(r1[p]);
-        }
-        tmem_ld_x32(tl + kColYo, r0);
-        tmem_ld_x32(tl + kColYo + 32u, r1);
-        tc_fence_before();
-        mbar_arrive(ctl.bar(BAR_ACC_FREE));
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t r0[32], r1[32];
+          tmem_ld_x32(tl + kColYd + 32u * hf, r0);
+          tmem_ld_x32(tl + kColYo + 32u * hf, r1);
+          if (hf == 1) {
+            tc_fence_before();
+            mbar_arrive(ctl.bar(BAR_ACC_FREE));
+          }
+          float yv[32];
 #pragma unroll
-        for (int p = 0; p < 32; ++p) {
-          yv[p] = fmaf(dec_t, __uint_as_float(r0[p]), yv[p]);
-          yv[p + 32] = fmaf(dec_t, __uint_as_float(r1[p]), yv[p + 32]);
+          for (int p = 0; p < 32; ++p) yv[p] = fmaf(dec_t, __uint_as_float(r1[p]), __uint_as_float(r0[p]));
+          if (r < valid) store_row32<TY>(yrow + 32 * hf, yv);
         }
-        if (r < valid) store_row64<TY>(y + (int64_t(b) * L + t0 + r) * D + int64_t(h) * kP, yv);
       }
     }
     if (ok && hT) {

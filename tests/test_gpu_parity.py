@@ -342,3 +342,30 @@ def test_decode_full_size_sampled(name):
     assert torch.equal(g["ssm_pool"][untouched], T(inp["ssm_pool"])[untouched])
     assert torch.equal(g["conv_pool"][untouched].view(torch.int16),
                        T(inp["conv_pool"])[untouched].view(torch.int16))
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("A_scale", [8.0, 0.0])
+def test_strong_and_no_decay(fused, A_scale):
+    """A chunk whose log-decay range is far beyond what the factored decay
+    weights cover (A_h ~ -8, dt ~ 1: the exact per-element path), and A_h = 0
+    (no decay: a running sum over 700 tokens)."""
+    s = synth.WORKLOADS["m370m_2k"].with_(Bz=1, segments=(300, 400), H=2, gaussian_init=True)
+    p = synth.mixer_params(s)
+    p["A"] = synth.f32(-A_scale * np.array([1.0, 0.5]))
+    st = synth.mixer_initial_states(s)
+    S, h = T(st["conv_state"]), T(st["h0"])
+    S_ref, h_ref = st["conv_state"].f64(), st["h0"].f64()
+    for i in range(len(s.segments)):
+        seg = synth.mixer_segment(s, i)
+        if A_scale > 0:  # dt around 1
+            seg["dt"] = synth.bf16(np.full(seg["dt"].shape, 1.0) + 0.5 * seg["dt"].f64())
+        y, S, h = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), T(p["A"]), T(seg["B"]), T(seg["C"]),
+                                T(p["w"]), T(p["bias"]), S, h, conv_state_out=S, hT=h,
+                                fused=fused)
+        y_ref, S_ref, h_ref = oracle.mixer_fwd(seg["x"], seg["dt"], p["A"], seg["B"], seg["C"],
+                                               p["w"], p["bias"], S_ref, h_ref)
+        assert_y_close(f64(y), y_ref, f"segment {i}")
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(S), S_ref)
+    assert_rel(f64(h), h_ref, STATE_REL, "hT")
