@@ -212,12 +212,13 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
 /*
  * sss_tcgen05_selftest -- diagnostic of the tensor-core operand layouts the
  * chunked scan uses (no counterpart on the pages).  With A and B two
- * [128][128] bf16 row-major matrices (device), writes six fp32 [128][128]
- * blocks to `out` (device, 6*128*128 floats), each = A B^T computed through
- * one descriptor form: [0] both operands K-major (all 128 columns valid);
- * [1] A MN-major; [2] B MN-major; [3] A read from tensor memory; [4] A from
- * tensor memory with B MN-major; [5] A and B MN-major ([1]..[5]: columns
- * 0..63 valid).
+ * [128][128] bf16 row-major matrices (device), writes nine fp32 [128][128]
+ * blocks to `out` (device, 9*128*128 floats), each = A B^T computed through
+ * one descriptor form: [0] both operands K-major; [1] A MN-major; [2] B
+ * MN-major; [3] A read from tensor memory; [4] A from tensor memory with B
+ * MN-major; [5] A and B MN-major ([1]..[5]: N = 64, columns 0..63 valid);
+ * [6] K-major A, [7] A from tensor memory, [8] MN-major A, each with an
+ * N = 128 MN-major B made of two 64-wide blocks 16 KB apart.
  */
 sss_status sss_tcgen05_selftest(const void* A, const void* B, float* out,
                                 sss_stream_t stream);

@@ -239,10 +239,10 @@ def mixer_update(x_new: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tens
 
 
 def tcgen05_selftest(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
-    """A, B [128, 128] bf16 (cuda).  Returns [6, 128, 128] fp32: A @ B.T through
+    """A, B [128, 128] bf16 (cuda).  Returns [9, 128, 128] fp32: A @ B.T through
     the tensor-core operand forms of the chunked scan (blocks 1..5 valid in
-    columns 0..63)."""
-    out = torch.zeros((6, 128, 128), dtype=torch.float32, device=A.device)
+    columns 0..63, the others in all columns)."""
+    out = torch.zeros((9, 128, 128), dtype=torch.float32, device=A.device)
     _check("sss_tcgen05_selftest", _lib.sss_tcgen05_selftest(_ptr(A), _ptr(B), _ptr(out),
                                                              _stream(stream)))
     return out

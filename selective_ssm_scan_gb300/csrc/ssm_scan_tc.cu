@@ -15,28 +15,35 @@
 //   h_new = exp(Lam_end) h_prev + sum_s exp(Lam_end - Lam_s) x_s B_s^T
 //
 // Per chunk and head that is four products on the tensor cores (bf16 in,
-// fp32 accumulate in tensor memory), M = 128 rows each:
+// fp32 accumulate in tensor memory), M = 128 rows each.  With a reference
+// R = the middle of the chunk's Lam range, g_s = exp(R - Lam_s) and
+// f_t = exp(Lam_t - R), the decay weight is exp(Lam_t - Lam_s) = f_t g_s, so
+// with x'_s = g_s x_s:
 //   G   = C B^T                     [t][s]  (K = N)
-//   Yd  = (G o M) X                 [t][p]  (K = Q, A operand from TMEM)
+//   Yd' = (G o causal) X'           [t][p]  (K = Q, A operand from TMEM)
 //   Yo  = C h_prev^T                [t][p]  (K = N)
-//   S^T = B^T X~                    [n][p]  (K = Q), X~_s = exp(Lam_end - Lam_s) x_s
+//   S'  = B^T X'                    [n][p]  (K = Q)
+//   y_t = f_t Yd'_t + exp(Lam_t) Yo_t,   h_new = exp(Lam_end) h_prev + exp(Lam_end - R) S'.
+// The factors stay inside exp(+-50) while the chunk's range is <= 100; a
+// chunk with a wider range uses the plain weights exp(Lam_t - Lam_s) in the
+// mask and a second operand tile X~_s = exp(Lam_end - Lam_s) x_s for S.
 // The fp32 operands that a single bf16 rounding would push past the
-// tolerance (x, G o M, h_prev, X~; B and C are bf16 inputs and stay exact)
+// tolerance (x', G o causal, h_prev; B and C are bf16 inputs and stay exact)
 // are split into hi + lo bf16 parts and each product takes the hi*hi, hi*lo
 // and lo*hi terms.  The state stays in fp32 registers (one TMEM lane = one
 // state row n per consumer thread) for the whole sequence.
 //
-// Warp roles in one CTA = one (batch, head), 288 threads:
-//   warps 0-3  producers: per chunk, Lam, the input rows (or the conv of the
-//              raw input, fused), the hi/lo operand tiles of x and x~
+// Warp roles in one CTA = one (batch, head), 416 threads:
+//   warps 0-7  producers: per chunk, Lam and the chunk's scalars (published in
+//              shared memory for the other roles), the input rows (or the
+//              conv of the raw input, fused), the hi/lo operand tiles of x'
 //              (token-major rows = MN-major operands, 16-byte stores),
 //              double-buffered so chunk c+1 is prepared during chunk c;
-//   warps 4-7  consumers: the decay mask G -> G o M (into TMEM), the state
-//              carry h_c = exp(Lam_end) h_{c-1} + S_c and its hi/lo tiles,
-//              the y epilogue;
-//   warp 8     issuer: TMA of the B and C chunks and every tcgen05.mma, one
+//   warps 8-11 consumers: the causal mask G -> G o causal (into TMEM), the
+//              state carry and its hi/lo tiles, the y epilogue;
+//   warp 12    issuer: TMA of the B and C chunks and every tcgen05.mma, one
 //              thread; TMA for chunk c+1 starts as soon as chunk c's products
-//              that read B and C are done.
+//              that read B and C are done, G(c+1) overlaps chunk c's epilogue.
 // Stages hand over through mbarriers.  Every wait is bounded (2 s): on expiry
 // the waiter raises SSS_ERR_TIMEOUT and sets an abort flag that makes every
 // other role stop at its next wait; the issuer drains its MMAs, the CTA frees
@@ -56,15 +63,18 @@ constexpr int kQ = 128;  // chunk length = MMA M
 constexpr int kP = 64;   // head dimension
 constexpr int kN = 128;  // state size
 constexpr int kMaxK = 4; // conv width handled by the fused producer
-constexpr int kThreads = 288;
+constexpr int kProdWarps = 8;                 // warps 0-7
+constexpr int kConsWarp0 = kProdWarps;        // warps 8-11 (TMEM lane quarters 0-3)
+constexpr int kIssuerWarp = kConsWarp0 + 4;   // warp 12
+constexpr int kThreads = (kIssuerWarp + 1) * 32;
 constexpr uint32_t kTmemCols = 512;
 // tensor memory columns (fp32 accumulators unless noted)
-constexpr uint32_t kColG = 0;     // C B^T            [t][s] 128
-constexpr uint32_t kColGh = 128;  // hi(G o M), bf16 pairs    64
-constexpr uint32_t kColGl = 192;  // lo(G o M), bf16 pairs    64
-constexpr uint32_t kColYd = 256;  // (G o M) x        [t][p]  64
-constexpr uint32_t kColYo = 320;  // C h^T            [t][p]  64
-constexpr uint32_t kColS = 384;   // B^T x~, 2 buffers [n][p] 2 x 64
+constexpr uint32_t kColG = 0;     // C B^T                          [t][s] 128
+constexpr uint32_t kColGh = 128;  // hi(G o mask), bf16 pairs              64
+constexpr uint32_t kColGl = 192;  // lo(G o mask), bf16 pairs              64
+constexpr uint32_t kColYd = 256;  // hi(G o mask)(x'hi | x'lo) + lo x'hi [t][128]
+constexpr uint32_t kColYo = 384;  // C (h_hi + h_lo)^T                [t][p]  64
+constexpr uint32_t kColS = 448;   // B^T (x'hi + x'lo)                [n][p]  64
 // shared memory (bytes from a 1024-byte aligned base)
 constexpr uint32_t kOffC = 0;         // C chunk [t][n], K-major, two 64-wide n blocks
 constexpr uint32_t kOffB = 32768;     // B chunk [s][n]
@@ -72,39 +82,41 @@ constexpr uint32_t kOffU = 65536;     // x hi/lo, 2 stages x (hi 16 KB, lo 16 KB
 constexpr uint32_t kOffX = 131072;    // x~ hi (16 KB), lo (16 KB), rows s
 constexpr uint32_t kOffH = 163840;    // h hi (16 KB), lo (16 KB), rows n
 constexpr uint32_t kOffMisc = 196608;
-constexpr uint32_t kMiscLam = 0;       // [2][128] consumer Lam_t
-constexpr uint32_t kMiscGf = 1024;     // [2][128] consumer exp(R - Lam_s)
-constexpr uint32_t kMiscXd = 2048;     // [2][128] producer exp(Lam_end - Lam_s)
-constexpr uint32_t kMiscRedP = 3072;   // [2][12] producer scan scratch
-constexpr uint32_t kMiscRedE = 3168;   // [2][12] consumer scan scratch
-constexpr uint32_t kMiscW = 3264;      // [64][4] conv weights of the head
-constexpr uint32_t kMiscBias = 4288;   // [64]
-constexpr uint32_t kMiscBars = 4544;   // 18 mbarriers
-constexpr uint32_t kMiscTmem = 4688;
-constexpr uint32_t kMiscAbort = 4692;
-constexpr uint32_t kMiscBytes = 4800;
-constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
+constexpr uint32_t kMiscLam = 0;       // [2][128] Lam_t of the chunk (published by producers)
+constexpr uint32_t kMiscGf = 1024;     // [2][128] exp(R - Lam_s), or 1 on the plain path
+constexpr uint32_t kMiscXd = 2048;     // [2][128] exp(Lam_end - Lam_s) (plain path)
+constexpr uint32_t kMiscRedP = 3072;   // [2][24] producer scan scratch
+constexpr uint32_t kMiscScal = 3264;   // [2][4] chunk scalars: factored flag, R, Lam_end
+constexpr uint32_t kMiscW = 3456;      // [64][4] conv weights of the head
+constexpr uint32_t kMiscBias = 4480;   // [64]
+constexpr uint32_t kMiscBars = 4736;   // 17 mbarriers
+constexpr uint32_t kMiscTmem = 4888;
+constexpr uint32_t kMiscAbort = 4892;
+// fused path: the raw-input rows of the next chunk, staged by TMA with the
+// K-1 halo rows in front (128 + 3 rows of 128 bytes, 128-byte swizzle)
+constexpr uint32_t kOffXs = 202752;
+constexpr uint32_t kXsRows = 128 + 3;
+constexpr uint32_t kXsBytes = kXsRows * 128;
+constexpr uint32_t kSmemBytes = kOffXs + kXsBytes + 1024;
 // chunks whose log-decay range exceeds this use exp(Lam_t - Lam_s) per
 // element instead of the factored exp(Lam_t - R) exp(R - Lam_s)
-constexpr float kFactorRange = 160.0f;
+constexpr float kFactorRange = 100.0f;
 constexpr uint64_t kWaitNs = 2000000000ull;
 // barriers
 enum {
   BAR_FULL_CB = 0, BAR_TILES = 1 /*2*/, BAR_U_FREE = 3 /*2*/, BAR_X_FREE = 5, BAR_G_FULL = 6,
-  BAR_GM_FULL = 7, BAR_S_FULL = 8 /*2*/, BAR_S_FREE = 10 /*2*/, BAR_YO_DONE = 12,
-  BAR_H_FULL = 13, BAR_Y_FULL = 14, BAR_ACC_FREE = 15, BAR_CB_FREE = 16, BAR_DRAIN = 17,
-  NUM_BARS = 18
+  BAR_GM_FULL = 7, BAR_S_FULL = 8, BAR_S_FREE = 9, BAR_YO_DONE = 10, BAR_H_FULL = 11,
+  BAR_Y_FULL = 12, BAR_ACC_FREE = 13, BAR_CB_FREE = 14, BAR_DRAIN = 15, BAR_XS_FULL = 16,
+  NUM_BARS = 17
 };
-constexpr uint32_t kIdG = idesc_bf16(128, 128, 0, 0);   // C (K-major) x B (K-major)
-constexpr uint32_t kIdS = idesc_bf16(128, 64, 1, 1);    // B^T (MN-major) x x~ (MN-major)
-constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);   // C (K-major) x h (MN-major)
-constexpr uint32_t kIdYd = idesc_bf16(128, 64, 0, 1);   // G o M (TMEM) x x (MN-major)
+constexpr uint32_t kIdG = idesc_bf16(128, 128, 0, 0);     // C (K-major) x B (K-major)
+constexpr uint32_t kIdS = idesc_bf16(128, 64, 1, 1);      // B^T (MN-major) x x' (MN-major)
+constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);     // C (K-major) x h (MN-major)
+constexpr uint32_t kIdYd = idesc_bf16(128, 128, 0, 1);    // hi(G o mask) (TMEM) x x'hi|lo (MN-major)
+constexpr uint32_t kIdYdLo = idesc_bf16(128, 64, 0, 1);   // lo(G o mask) (TMEM) x x'hi
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-__device__ __forceinline__ float bf16_val(uint16_t b) {
-  return __bfloat162float(__ushort_as_bfloat16(b));
 }
 __device__ __forceinline__ uint32_t pack2(uint16_t lo_elem, uint16_t hi_elem) {
   return uint32_t(lo_elem) | (uint32_t(hi_elem) << 16);
@@ -124,10 +136,11 @@ __device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t&
 __device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, uint32_t blk) {
   return sdesc_sw128(base + uint32_t(kk >> 2) * blk + uint32_t(kk & 3) * 32u, 16, 1024);
 }
-// MN-major descriptor of a [K rows][64 MN] tile (128-byte rows): K step kk
-// starts 16 rows further.
+// MN-major descriptor of [K rows][64 MN] tiles (128-byte rows), a second
+// 64-wide MN block 16 KB further (used when N = 128): K step kk starts 16
+// rows further.
 __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
-  return sdesc_sw128(base + uint32_t(kk) * 2048u, 8192, 1024);
+  return sdesc_sw128(base + uint32_t(kk) * 2048u, 16384, 1024);
 }
 
 // Row `r` (64 fp32 values) -> hi and lo bf16 rows of two MN-major tiles.
@@ -143,52 +156,9 @@ __device__ __forceinline__ void write_split_row(uint8_t* hi_tile, uint8_t* lo_ti
   }
 }
 
-template <typename TX>
-__device__ __forceinline__ void load_row64(const TX* row, float* u);
-template <>
-__device__ __forceinline__ void load_row64<float>(const float* row, float* u) {
-#pragma unroll
-  for (int q = 0; q < 16; ++q) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
-    u[4 * q] = v.x; u[4 * q + 1] = v.y; u[4 * q + 2] = v.z; u[4 * q + 3] = v.w;
-  }
-}
-template <>
-__device__ __forceinline__ void load_row64<__nv_bfloat16>(const __nv_bfloat16* row, float* u) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(row) + q);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      u[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
-      u[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
-  }
-}
-
-template <typename TY>
-__device__ __forceinline__ void store_row32(TY* row, const float* v);
-template <>
-__device__ __forceinline__ void store_row32<float>(float* row, const float* v) {
-#pragma unroll
-  for (int q = 0; q < 8; ++q)
-    reinterpret_cast<float4*>(row)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-template <>
-__device__ __forceinline__ void store_row32<__nv_bfloat16>(__nv_bfloat16* row, const float* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = pack2(bf16_bits(v[8 * q + 2 * k]), bf16_bits(v[8 * q + 2 * k + 1]));
-    reinterpret_cast<uint4*>(row)[q] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
-// Named barrier among the 128 threads of one role (ids 1, 2; 0 is __syncthreads).
-__device__ __forceinline__ void role_sync(int id) {
-  asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+// Named barrier among the threads of one role (ids 1, 2; 0 is __syncthreads).
+__device__ __forceinline__ void role_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -204,7 +174,8 @@ struct Ctl {
     const uint32_t b = bar(i);
     if (mbar_try_wait(b, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(b, parity)) {
+    // sleep in the wait (woken by the phase completing) rather than spin
+    while (!mbar_try_wait_sleep(b, parity, 20000u)) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > kWaitNs) {
         *abort = 1;
@@ -216,8 +187,9 @@ struct Ctl {
   }
 };
 
-// Inclusive prefix of `v` over the 128 threads of a role (4 warps); also the
-// total and the minimum / maximum of the prefix over the role.
+// Inclusive prefix of `v` over the NW warps of a role; also the total and the
+// minimum / maximum of the prefix over the role.  `red` holds 3 NW floats.
+template <int NW>
 __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* red, int bar_id,
                                              float* total, float* pmin, float* pmax) {
 #pragma unroll
@@ -233,15 +205,15 @@ __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* r
   }
   if (lane == 31) red[wq] = v;
   if (lane == 0) {
-    red[4 + wq] = mn;
-    red[8 + wq] = mx;
+    red[NW + wq] = mn;
+    red[2 * NW + wq] = mx;
   }
-  role_sync(bar_id);
+  role_sync(bar_id, NW * 32);
   float off = 0.0f, run = 0.0f, gmn = 3.0e38f, gmx = -3.0e38f;
 #pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    gmn = fminf(gmn, run + red[4 + w]);
-    gmx = fmaxf(gmx, run + red[8 + w]);
+  for (int w = 0; w < NW; ++w) {
+    gmn = fminf(gmn, run + red[NW + w]);
+    gmx = fmaxf(gmx, run + red[2 * NW + w]);
     if (w < wq) off += red[w];
     run += red[w];
   }
@@ -251,6 +223,25 @@ __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* r
   return v + off;
 }
 
+template <typename TY>
+__device__ __forceinline__ void store_row16(TY* row, const float* v);
+template <>
+__device__ __forceinline__ void store_row16<float>(float* row, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    reinterpret_cast<float4*>(row)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+template <>
+__device__ __forceinline__ void store_row16<__nv_bfloat16>(__nv_bfloat16* row, const float* v) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = pack2(bf16_bits(v[8 * q + 2 * k]), bf16_bits(v[8 * q + 2 * k + 1]));
+    reinterpret_cast<uint4*>(row)[q] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 }  // namespace
 
 // x: the scan input u [Bz, L, H, 64] (TX = float or bf16), or with FUSED the
@@ -258,14 +249,15 @@ __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* r
 template <typename TX, typename TY, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
 ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
-                   const TX* __restrict__ x, const __nv_bfloat16* __restrict__ dt,
-                   const float* __restrict__ A, const float* h0, float* hT,
-                   TY* __restrict__ y, const float* __restrict__ conv_w,
+                   const __grid_constant__ CUtensorMap tmX, const TX* __restrict__ x,
+                   const __nv_bfloat16* __restrict__ dt, const float* __restrict__ A,
+                   const float* h0, float* hT, TY* __restrict__ y, const float* __restrict__ conv_w,
                    const float* __restrict__ conv_b, const TX* conv_s_in, TX* conv_s_out,
                    int K, int L, int H, int G, int* status) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from the shared array itself so that the
+  // compiler keeps every access in the shared address space
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
   uint8_t* misc = sm + kOffMisc;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + kMiscTmem);
@@ -277,12 +269,16 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
   const int64_t D = int64_t(H) * kP;
   const int nC = (L + kQ - 1) / kQ;
 
-  if (warp == 8) {
+  if (warp == kIssuerWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    const int counts[NUM_BARS] = {1, 128, 128, 1, 1, 1, 1, 128, 1, 1, 128, 128, 1, 128, 1, 128, 1, 1};
+    int counts[NUM_BARS];
+    for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
+    counts[BAR_TILES] = counts[BAR_TILES + 1] = kProdWarps * 32;
+    counts[BAR_GM_FULL] = counts[BAR_S_FREE] = 128;
+    counts[BAR_H_FULL] = counts[BAR_ACC_FREE] = 128;
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(ctl.bar(i), counts[i]);
     *ctl.abort = 0;
     fence_mbar_init();
@@ -301,144 +297,196 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
   tc_fence_after();
   const uint32_t tm = *tmem_slot;
 
-  if (warp < 4) {
-    // ======================= producers =======================
-    // The prefix runs with one token per thread (s = tid); the inputs and the
-    // operand rows with thread (q, g) = 8 channels [8q, 8q+8) x 8 tokens
-    // [8g, 8g+8): every input element is loaded (and, fused, convolved in a
-    // register window) once, all loads of a chunk issued up front.
-    const int s = tid, q = tid & 7, g8 = tid >> 3;
+  if (warp < kProdWarps) {
+    // ============================ producers ============================
+    // The prefix runs with one token per thread (s = tid < 128); the inputs
+    // and operand rows with thread (q, g4) = channels [8q, 8q+8) x tokens
+    // [4 g4, 4 g4 + 4): every input element is read (and, fused, convolved in
+    // a register window) once.
+    constexpr int NT = 4;                        // tokens per thread
+    constexpr int PT = kProdWarps * 32;
+    const int s = tid, q = tid & 7, g4 = tid >> 3;
     float* red = reinterpret_cast<float*>(misc + kMiscRedP);
-    float* xdP = reinterpret_cast<float*>(misc + kMiscXd);
-    float wk[kMaxK][8], bk[8];
-    if constexpr (FUSED) {
-      const float* sw = reinterpret_cast<const float*>(misc + kMiscW);
-      const float* sbias = reinterpret_cast<const float*>(misc + kMiscBias);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        bk[e] = sbias[8 * q + e];
-#pragma unroll
-        for (int k = 0; k < kMaxK; ++k) wk[k][e] = sw[(8 * q + e) * kMaxK + k];
-      }
+    const float* swq = reinterpret_cast<const float*>(misc + kMiscW) + 8 * q * kMaxK;
+    const float* sbq = reinterpret_cast<const float*>(misc + kMiscBias) + 8 * q;
+    auto stage_x = [&](int c) {  // TMA of chunk c's raw rows [t0 - 3, t0 + 128)
+      mbar_arrive_expect_tx(ctl.bar(BAR_XS_FULL), kXsBytes);
+      tma_load_3d(sb + kOffXs, &tmX, h * kP, c * kQ - (kMaxK - 1), b, ctl.bar(BAR_XS_FULL));
+    };
+    if (FUSED && s == 0) {
+      prefetch_tmap(&tmX);
+      stage_x(0);
     }
+    int xs_issued = FUSED ? 1 : 0, xs_landed = 0;
     // on abort every loop below keeps running its named barriers with the
     // work skipped, so no thread is ever left waiting at one
     bool ok = true;
     for (int c = 0; c < nC; ++c) {
       const int t0 = c * kQ;
       const int valid = min(kQ, L - t0);
-      const float ell =
-          ok && s < valid ? __bfloat162float(dt[(int64_t(b) * L + t0 + s) * H + h]) * Ah : 0.0f;
-      // ---- inputs of tokens [8 g8, 8 g8 + 8), channels [8 q, 8 q + 8) -------
-      float u[8][8];  // [token j][channel e]
-      const int tb = t0 + 8 * g8;          // first token of the group
-      const int nv = ok ? min(8, max(0, valid - 8 * g8)) : 0;  // live tokens
+      const float ell = ok && s < valid && warp < 4
+                            ? __bfloat162float(dt[(int64_t(b) * L + t0 + s) * H + h]) * Ah
+                            : 0.0f;
+      float u[NT][8];  // [token j][channel e]
+      const int tb = t0 + NT * g4;  // first token of the group
+      const int nv = ok ? min(NT, max(0, valid - NT * g4)) : 0;  // live tokens
       if constexpr (!FUSED) {
+        // unconditional loads of clamped rows, dead tokens zeroed afterwards
+        const int64_t rowbase = int64_t(b) * L * D + int64_t(h) * kP + 8 * q;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j < nv) {
-            const TX* row = x + (int64_t(b) * L + tb + j) * D + int64_t(h) * kP + 8 * q;
-            if constexpr (sizeof(TX) == 4) {
-              const float4 v0 = __ldg(reinterpret_cast<const float4*>(row));
-              const float4 v1 = __ldg(reinterpret_cast<const float4*>(row) + 1);
-              u[j][0] = v0.x; u[j][1] = v0.y; u[j][2] = v0.z; u[j][3] = v0.w;
-              u[j][4] = v1.x; u[j][5] = v1.y; u[j][6] = v1.z; u[j][7] = v1.w;
-            } else {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(row));
-              const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                u[j][2 * i] = __uint_as_float(w4[i] << 16);
-                u[j][2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-              }
-            }
+        for (int j = 0; j < NT; ++j) {
+          const int pc = min(tb + j, L - 1);
+          const TX* row = x + rowbase + int64_t(pc) * D;
+          float v[8];
+          if constexpr (sizeof(TX) == 4) {
+            const float4 v0 = __ldg(reinterpret_cast<const float4*>(row));
+            const float4 v1 = __ldg(reinterpret_cast<const float4*>(row) + 1);
+            v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+            v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
           } else {
+            const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(row));
+            const uint32_t w4[4] = {r4.x, r4.y, r4.z, r4.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) u[j][e] = 0.0f;
+            for (int i = 0; i < 4; ++i) {
+              v[2 * i] = __uint_as_float(w4[i] << 16);
+              v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+            }
           }
+          const float live_j = j < nv ? 1.0f : 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[j][e] = v[e] * live_j;
         }
       } else {
-        // rows tb - (kMaxK-1) + i, i < 8 + kMaxK - 1; positions < 0 are the
-        // conv state (extended sequence [S, x]), positions >= L are unused
-        constexpr int NR = 8 + kMaxK - 1;
+        // rows tb - (kMaxK-1) + i, i < NT + kMaxK - 1, from the staged tile
+        // (rows outside [0, L) arrive zero-filled; rows past the last live
+        // token are zeroed; positions < 0 are then taken from the conv state)
+        constexpr int NR = NT + kMaxK - 1;
+        if (ok) ok = ctl.wait(BAR_XS_FULL, uint32_t(c & 1));
+        if (ok) xs_landed = c + 1;
         uint4 xr[NR];
 #pragma unroll
         for (int i = 0; i < NR; ++i) {
+          const int row = NT * g4 + i;  // staged row = position t0 - 3 + row
           const int pos = tb - (kMaxK - 1) + i;
-          xr[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (nv > 0 && pos >= 0 && pos < tb + nv) {
-            xr[i] = __ldg(reinterpret_cast<const uint4*>(x + (int64_t(b) * L + pos) * D +
-                                                         int64_t(h) * kP + 8 * q));
-          } else if (nv > 0 && pos < 0 && pos >= -(K - 1) && conv_s_in) {
-            uint32_t w4[4];
+          const uint4 v = *reinterpret_cast<const uint4*>(sm + kOffXs + sw128(row, q));
+          xr[i] = (ok && nv > 0 && pos < tb + nv) ? v : make_uint4(0u, 0u, 0u, 0u);
+        }
+        if (tb < kMaxK - 1 && nv > 0 && conv_s_in) {
 #pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) {
-              const int64_t d0 = int64_t(b) * D + int64_t(h) * kP + 8 * q + 2 * i2;
-              const uint16_t lo = *reinterpret_cast<const uint16_t*>(&conv_s_in[d0 * (K - 1) + (K - 1) + pos]);
-              const uint16_t hi = *reinterpret_cast<const uint16_t*>(&conv_s_in[(d0 + 1) * (K - 1) + (K - 1) + pos]);
-              w4[i2] = pack2(lo, hi);
+          for (int i = 0; i < kMaxK - 1; ++i) {
+            const int pos = tb - (kMaxK - 1) + i;
+            if (pos < 0 && pos >= -(K - 1)) {
+              uint32_t w4[4];
+#pragma unroll
+              for (int i2 = 0; i2 < 4; ++i2) {
+                const int64_t d0 = int64_t(b) * D + int64_t(h) * kP + 8 * q + 2 * i2;
+                const uint16_t lo = *reinterpret_cast<const uint16_t*>(&conv_s_in[d0 * (K - 1) + (K - 1) + pos]);
+                const uint16_t hi = *reinterpret_cast<const uint16_t*>(&conv_s_in[(d0 + 1) * (K - 1) + (K - 1) + pos]);
+                w4[i2] = pack2(lo, hi);
+              }
+              xr[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
             }
-            xr[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
           }
         }
-        // window over the rows: token j uses rows j + k with the right-aligned
-        // taps (rows before the sequence are the state, zero-weighted for K < 4)
+        // channel pair by channel pair (weights of two channels = two float4
+        // broadcast reads of the staged table), all tokens per pair; token j
+        // uses rows j + k with the right-aligned taps
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int e2 = 0; e2 < 4; ++e2) {
+          const float4 wa = *reinterpret_cast<const float4*>(swq + (2 * e2) * kMaxK);
+          const float4 wb = *reinterpret_cast<const float4*>(swq + (2 * e2 + 1) * kMaxK);
+          const float2 bb = *reinterpret_cast<const float2*>(sbq + 2 * e2);
+          const float wa_[4] = {wa.x, wa.y, wa.z, wa.w}, wb_[4] = {wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) u[j][e] = bk[e];
+          for (int j = 0; j < NT; ++j) {
+            float za = bb.x, zb = bb.y;
 #pragma unroll
-          for (int k = 0; k < kMaxK; ++k) {
-            const uint4 rv = xr[j + k];
-            const uint32_t w4[4] = {rv.x, rv.y, rv.z, rv.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              u[j][2 * i] = fmaf(wk[k][2 * i], __uint_as_float(w4[i] << 16), u[j][2 * i]);
-              u[j][2 * i + 1] =
-                  fmaf(wk[k][2 * i + 1], __uint_as_float(w4[i] & 0xFFFF0000u), u[j][2 * i + 1]);
+            for (int k = 0; k < kMaxK; ++k) {
+              const uint4 rv = xr[j + k];
+              const uint32_t wv = e2 == 0 ? rv.x : e2 == 1 ? rv.y : e2 == 2 ? rv.z : rv.w;
+              za = fmaf(wa_[k], __uint_as_float(wv << 16), za);
+              zb = fmaf(wb_[k], __uint_as_float(wv & 0xFFFF0000u), zb);
             }
+            u[j][2 * e2] = za;
+            u[j][2 * e2 + 1] = zb;
           }
+        }
+        // SiLU on every value (dead tokens hold finite conv outputs of zero
+        // rows), then zeroed by a multiply: no branch around the expensive part
 #pragma unroll
-          for (int e = 0; e < 8; ++e) u[j][e] = j < nv ? silu(u[j][e]) : 0.0f;
+        for (int j = 0; j < NT; ++j) {
+          const float live_j = j < nv ? 1.0f : 0.0f;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) u[j][e] = silu(u[j][e]) * live_j;
         }
       }
-      // ---- Lam and the state-path decay of each token -----------------------
-      float lam_end, lmin, lmax;
-      const float lam_s = role_prefix(ell, lane, warp, red + 12 * (c & 1), 1, &lam_end, &lmin, &lmax);
-      float* xd = xdP + 128 * (c & 1);
-      xd[s] = expf(lam_end - lam_s);
-      role_sync(1);
+      // ---- Lam over the chunk (warps 0-3, one token per thread) -------------
+      float lam_s = 0.0f, lam_end = 0.0f, lmin = 0.0f, lmax = 0.0f;
+      if (warp < 4)
+        lam_s = role_prefix<4>(ell, lane, warp, red + 12 * (c & 1), 3, &lam_end, &lmin, &lmax);
       const int st = c & 1;
-      uint8_t* uh = sm + kOffU + st * 32768;
+      // the stage's shared arrays and tiles are free once Yd(c-2) is done
       if (ok && c >= 2) ok = ctl.wait(BAR_U_FREE + st, uint32_t(((c >> 1) + 1) & 1));
-      if (ok) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) split2(u[j][2 * k], u[j][2 * k + 1], hw[k], lw[k]);
-          *reinterpret_cast<uint4*>(uh + sw128(8 * g8 + j, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(uh + 16384 + sw128(8 * g8 + j, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      float* lamP = reinterpret_cast<float*>(misc + kMiscLam) + 128 * st;
+      float* gP = reinterpret_cast<float*>(misc + kMiscGf) + 128 * st;
+      float* xdP = reinterpret_cast<float*>(misc + kMiscXd) + 128 * st;
+      float* scal = reinterpret_cast<float*>(misc + kMiscScal) + 4 * st;
+      if (warp < 4) {  // publish Lam and the scalars that every role uses
+        const bool fac = (lmax - lmin) <= kFactorRange;
+        const float R = 0.5f * (lmin + lmax);
+        lamP[s] = lam_s;
+        gP[s] = fac ? expf(R - lam_s) : 1.0f;
+        xdP[s] = expf(lam_end - lam_s);
+        if (s == 0) {
+          scal[0] = fac ? 1.0f : 0.0f;
+          scal[1] = R;
+          scal[2] = lam_end;
         }
       }
-      if (ok && c >= 1) ok = ctl.wait(BAR_X_FREE, uint32_t((c - 1) & 1));
-      if (ok) {
+      role_sync(1, PT);
+      // every producer has read the staged tile: stage the next chunk's rows
+      // while this chunk's operand tiles go out
+      if (FUSED && s == 0 && ok && c + 1 < nC) {
+        stage_x(c + 1);
+        xs_issued = c + 2;
+      }
+      const bool fac = scal[0] != 0.0f;
+      uint8_t* uh = sm + kOffU + st * 32768;
+      if (ok) {  // x' = g_s x (plain path: g_s = 1)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float f = xd[8 * g8 + j];
+        for (int j = 0; j < NT; ++j) {
+          const float f = gP[NT * g4 + j];
           uint32_t hw[4], lw[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) split2(u[j][2 * k] * f, u[j][2 * k + 1] * f, hw[k], lw[k]);
-          *reinterpret_cast<uint4*>(sm + kOffX + sw128(8 * g8 + j, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(sm + kOffX + 16384 + sw128(8 * g8 + j, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          *reinterpret_cast<uint4*>(uh + sw128(NT * g4 + j, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(uh + 16384 + sw128(NT * g4 + j, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
+      }
+      if (!fac) {  // plain path: X~_s = exp(Lam_end - Lam_s) x_s for the state product
+        if (ok && c >= 1) ok = ctl.wait(BAR_X_FREE, uint32_t((c - 1) & 1));
+        if (ok) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const float f = xdP[NT * g4 + j];
+            uint32_t hw[4], lw[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) split2(u[j][2 * k] * f, u[j][2 * k + 1] * f, hw[k], lw[k]);
+            *reinterpret_cast<uint4*>(sm + kOffX + sw128(NT * g4 + j, q)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(sm + kOffX + 16384 + sw128(NT * g4 + j, q)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+      }
+      if (ok) {
         fence_proxy_async_smem();
         mbar_arrive(ctl.bar(BAR_TILES + st));
       }
     }
+    if (FUSED && s == 0 && xs_issued > xs_landed)  // a staged tile still in flight
+      mbar_wait(ctl.bar(BAR_XS_FULL), uint32_t(xs_landed & 1), kWaitNs / 2);
     if constexpr (FUSED) {
       // final conv state F_j = ext[L + j]; every read of S happened in chunk 0
-      role_sync(1);
+      role_sync(1, PT);
       if (conv_s_out && s < kP && !*ctl.abort) {
         const int64_t d = int64_t(h) * kP + s;
         TX f[kMaxK - 1];
@@ -451,13 +499,11 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         for (int j = 0; j < K - 1; ++j) conv_s_out[(int64_t(b) * D + d) * (K - 1) + j] = f[j];
       }
     }
-  } else if (warp < 8) {
+  } else if (warp < kIssuerWarp) {
     // ===== consumers: TMEM lane r = row t (mask, y) = state row n (S, h) =====
-    const int r = tid - 128, wq = warp - 4;
+    const int wq = warp - kConsWarp0;  // == warp % 4, the TMEM lane quarter
+    const int r = 32 * wq + lane;
     const uint32_t tl = tm + (uint32_t(wq * 32) << 16);
-    float* red = reinterpret_cast<float*>(misc + kMiscRedE);
-    float* lamE = reinterpret_cast<float*>(misc + kMiscLam);
-    float* gfE = reinterpret_cast<float*>(misc + kMiscGf);
     float hreg[kP];
     const int64_t hoff = (int64_t(b) * H + h) * kP * kN;
 #pragma unroll
@@ -479,75 +525,73 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
     for (int c = 0; c < nC; ++c) {
       const int t0 = c * kQ;
       const int valid = min(kQ, L - t0);
-      const float ell =
-          ok && r < valid ? __bfloat162float(dt[(int64_t(b) * L + t0 + r) * H + h]) * Ah : 0.0f;
-      float lam_end, lmin, lmax;
-      const float lam_t = role_prefix(ell, lane, wq, red + 12 * (c & 1), 2, &lam_end, &lmin, &lmax);
-      // exp(Lam_t - Lam_s) = f_t g_s with the mid-range reference R: both
-      // factors stay within exp(+-80) while the chunk's range is <= 160
-      const bool factored = (lmax - lmin) <= kFactorRange;
-      const float R = 0.5f * (lmin + lmax);
-      const float f_t = expf(lam_t - R);
-      float* lam = lamE + 128 * (c & 1);
-      float* gf = gfE + 128 * (c & 1);
-      lam[r] = lam_t;
-      gf[r] = expf(R - lam_t);
-      role_sync(2);
-      // ---- decay mask: row t = r, columns s <= t --------------------------
+      const int st = c & 1;
+      // the chunk's Lam and scalars, published by the producers with the tiles
+      if (ok) ok = ctl.wait(BAR_TILES + st, uint32_t((c >> 1) & 1));
+      const float* lam = reinterpret_cast<const float*>(misc + kMiscLam) + 128 * st;
+      const float* scal = reinterpret_cast<const float*>(misc + kMiscScal) + 4 * st;
+      const bool fac = scal[0] != 0.0f;
+      const float R = scal[1], lam_end = scal[2];
+      const float lam_t = lam[r];
+      const float f_t = fac ? expf(lam_t - R) : 1.0f;       // row scale of Yd'
+      const float dec_t = expf(lam_t);                        // h_prev reaches row t
+      const float dec_end = expf(lam_end);                    // h_prev reaches the chunk end
+      const float s_scale = fac ? expf(lam_end - R) : 1.0f;  // scale of S'
+      // ---- mask: row t = r, columns s <= t, 16 columns at a time ------------
       // (ok is made warp-uniform before every warp-collective TMEM access)
       if (ok) ok = ctl.wait(BAR_G_FULL, uint32_t(c & 1));
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
         for (int j = 0; j <= wq; ++j) {
-          uint32_t graw[32], ph[16], pl[16];
-          tmem_ld_x32(tl + kColG + 32u * j, graw);
-          const bool diag = (j == wq);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int s0 = 32 * j + 2 * i;
-            float w0, w1;
-            if (factored) {
-              const float2 g2 = *reinterpret_cast<const float2*>(gf + s0);
-              w0 = f_t * g2.x;
-              w1 = f_t * g2.y;
+          for (int hf = 0; hf < 2; ++hf) {
+            const int s0 = 32 * j + 16 * hf;
+            uint32_t graw[16], ph[8], pl[8];
+            tmem_ld_x16(tl + kColG + uint32_t(s0), graw);
+            float m[16];
+            if (fac) {  // the decay lives in x' and the row scale f_t
+#pragma unroll
+              for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(graw[i]);
             } else {
-              const float2 l2 = *reinterpret_cast<const float2*>(lam + s0);
-              w0 = __expf(lam_t - l2.x);
-              w1 = __expf(lam_t - l2.y);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 l4 = *reinterpret_cast<const float4*>(lam + s0 + 4 * i);
+                m[4 * i] = __uint_as_float(graw[4 * i]) * __expf(lam_t - l4.x);
+                m[4 * i + 1] = __uint_as_float(graw[4 * i + 1]) * __expf(lam_t - l4.y);
+                m[4 * i + 2] = __uint_as_float(graw[4 * i + 2]) * __expf(lam_t - l4.z);
+                m[4 * i + 3] = __uint_as_float(graw[4 * i + 3]) * __expf(lam_t - l4.w);
+              }
             }
-            float m0 = __uint_as_float(graw[2 * i]) * w0;
-            float m1 = __uint_as_float(graw[2 * i + 1]) * w1;
-            if (diag) {
-              m0 = s0 <= r ? m0 : 0.0f;
-              m1 = s0 + 1 <= r ? m1 : 0.0f;
+            if (j == wq) {  // diagonal block: s = s0 + i <= t = 32 wq + lane
+#pragma unroll
+              for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
             }
-            split2(m0, m1, ph[i], pl[i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[i], pl[i]);
+            tmem_st_x8(tl + kColGh + uint32_t(s0 / 2), ph);
+            tmem_st_x8(tl + kColGl + uint32_t(s0 / 2), pl);
           }
-          tmem_st_x16(tl + kColGh + 16u * j, ph);
-          tmem_st_x16(tl + kColGl + 16u * j, pl);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(ctl.bar(BAR_GM_FULL));
       }
       // ---- state carry: row n = r ------------------------------------------
-      const int st = c & 1;
-      if (ok) ok = ctl.wait(BAR_S_FULL + st, uint32_t((c >> 1) & 1));
+      if (ok) ok = ctl.wait(BAR_S_FULL, uint32_t(c & 1));
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float dec_end = expf(lam_end);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t r0[32];
-          tmem_ld_x32(tl + kColS + 64u * st + 32u * hf, r0);
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t r0[16];
+          tmem_ld_x16(tl + kColS + 16u * qq, r0);
 #pragma unroll
-          for (int p = 0; p < 32; ++p)
-            hreg[32 * hf + p] = fmaf(dec_end, hreg[32 * hf + p], __uint_as_float(r0[p]));
+          for (int p = 0; p < 16; ++p)
+            hreg[16 * qq + p] = fmaf(dec_end, hreg[16 * qq + p], s_scale * __uint_as_float(r0[p]));
         }
         tc_fence_before();
-        mbar_arrive(ctl.bar(BAR_S_FREE + st));
+        mbar_arrive(ctl.bar(BAR_S_FREE));
       }
       if (ok) ok = ctl.wait(BAR_YO_DONE, uint32_t(c & 1));  // Yo(c) has read h_{c-1}
       if (ok) {
@@ -560,21 +604,28 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        const float dec_t = expf(lam_t);
         TY* yrow = y + (int64_t(b) * L + t0 + r) * D + int64_t(h) * kP;
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t r0[32], r1[32];
-          tmem_ld_x32(tl + kColYd + 32u * hf, r0);
-          tmem_ld_x32(tl + kColYo + 32u * hf, r1);
-          if (hf == 1) {
-            tc_fence_before();
-            mbar_arrive(ctl.bar(BAR_ACC_FREE));
-          }
-          float yv[32];
+        for (int qq = 0; qq < 4; ++qq) {
+          float yv[16];
+          {
+            uint32_t a0[16], a1[16];
+            tmem_ld_x16(tl + kColYd + 16u * qq, a0);
+            tmem_ld_x16(tl + kColYd + 64u + 16u * qq, a1);
 #pragma unroll
-          for (int p = 0; p < 32; ++p) yv[p] = fmaf(dec_t, __uint_as_float(r1[p]), __uint_as_float(r0[p]));
-          if (r < valid) store_row32<TY>(yrow + 32 * hf, yv);
+            for (int p = 0; p < 16; ++p) yv[p] = f_t * (__uint_as_float(a0[p]) + __uint_as_float(a1[p]));
+          }
+          {
+            uint32_t a0[16];
+            tmem_ld_x16(tl + kColYo + 16u * qq, a0);
+            if (qq == 3) {
+              tc_fence_before();
+              mbar_arrive(ctl.bar(BAR_ACC_FREE));
+            }
+#pragma unroll
+            for (int p = 0; p < 16; ++p) yv[p] = fmaf(dec_t, __uint_as_float(a0[p]), yv[p]);
+          }
+          if (r < valid) store_row16<TY>(yrow + 16 * qq, yv);
         }
       }
     }
@@ -602,25 +653,30 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       if (!ctl.wait(BAR_FULL_CB, uint32_t(c & 1))) break;
       tma_landed = c + 1;
       if (!ctl.wait(BAR_TILES + st, uint32_t((c >> 1) & 1))) break;
-      if (c >= 2 && !ctl.wait(BAR_S_FREE + st, uint32_t(((c >> 1) + 1) & 1))) break;
+      const bool fac = reinterpret_cast<const float*>(misc + kMiscScal)[4 * st] != 0.0f;
+      const uint32_t uh = sb + kOffU + st * 32768;          // x' hi | lo
+      const uint32_t xs = fac ? uh : sb + kOffX;             // operand of the state product
       tc_fence_after();
-      // G = C B^T
+      // G = C B^T (mask(c-1) has read G(c-1): Yd(c-1) was issued after it)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ss(tm + kColG, kdesc(sb + kOffC, kk, 16384), kdesc(sb + kOffB, kk, 16384), kIdG, kk);
       mma_commit(ctl.bar(BAR_G_FULL));
-      // S^T = B^T (x~hi + x~lo); B^T is the MN-major view of the B chunk
-      const uint32_t dS = tm + kColS + 64u * st;
+      // S' = B^T (x'hi + x'lo) into the single S buffer once state(c-1) read it;
+      // B^T is the MN-major view of the B chunk
+      if (c >= 1 && !ctl.wait(BAR_S_FREE, uint32_t((c - 1) & 1))) break;
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(dS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(sb + kOffX, kk), kIdS, kk);
+        mma_ss(tm + kColS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(xs, kk), kIdS, kk);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(dS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(sb + kOffX + 16384, kk),
+        mma_ss(tm + kColS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(xs + 16384, kk),
                kIdS, 1);
       mma_commit(ctl.bar(BAR_X_FREE));
-      mma_commit(ctl.bar(BAR_S_FULL + st));
-      // Yo = C (h_hi + h_lo)^T, once h_{c-1} is in place and Yo is free
+      mma_commit(ctl.bar(BAR_S_FULL));
+      // Yo = C (h_hi + h_lo)^T once h_{c-1} is in place and the epilogue of
+      // chunk c-1 has read Yo and Yd
       if (!ctl.wait(BAR_H_FULL, uint32_t(c & 1))) break;
       if (c >= 1 && !ctl.wait(BAR_ACC_FREE, uint32_t((c - 1) & 1))) break;
       tc_fence_after();
@@ -638,16 +694,13 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         tma_chunk(c + 1);
         tma_issued = c + 2;
       }
-      // Yd = (G o M)(x_hi + x_lo), hi*hi + hi*lo + lo*hi
+      // Yd' = hi(G o mask)(x'hi | x'lo) + lo(G o mask) x'hi
       if (!ctl.wait(BAR_GM_FULL, uint32_t(c & 1))) break;
       tc_fence_after();
-      const uint32_t uh = sb + kOffU + st * 32768, ul = uh + 16384;
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(uh, kk), kIdYd, kk);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(ul, kk), kIdYd, 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, mndesc(uh, kk), kIdYd, 1);
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, mndesc(uh, kk), kIdYdLo, 1);
       mma_commit(ctl.bar(BAR_Y_FULL));
       mma_commit(ctl.bar(BAR_U_FREE + st));
     }
@@ -663,7 +716,7 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tm, kTmemCols);
+  if (warp == kIssuerWarp) tmem_dealloc(tm, kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -674,10 +727,13 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                    const __nv_bfloat16* __restrict__ Am, const __nv_bfloat16* __restrict__ Bm,
                    float* __restrict__ out, int* status) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~uintptr_t(1023));
+  // 1024-byte aligned base, derived from the shared array itself so that the
+  // compiler keeps every access in the shared address space
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t sb = smem_u32(sm);
-  constexpr uint32_t oA = 0, oB = 32768, oAt = 65536, oBt = 98304, oMisc = 114688;
+  // every MN-major operand keeps valid memory one LBO (16 KB) past its start:
+  // the hardware may read there even when N = 64 needs a single 64-wide block
+  constexpr uint32_t oA = 0, oB = 32768, oAt = 65536, oBt = 98304, oMisc = 131072;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + oMisc + 16);
   const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
@@ -774,6 +830,96 @@ tc_selftest_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
   if (warp == 0) tmem_dealloc(tm, 512);
 }
 
+// The N = 128 forms: the B operand is two 64-wide MN-major blocks 16 KB
+// apart (as the hi and lo tiles of the scan are).  out[6..8]:
+// [6] K-major A, [7] A from tensor memory, [8] MN-major A.
+__global__ void __launch_bounds__(128, 1)
+tc_selftest2_kernel(const __grid_constant__ CUtensorMap tmA, const __nv_bfloat16* __restrict__ Am,
+                    const __nv_bfloat16* __restrict__ Bm, float* __restrict__ out, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sb = smem_u32(sm);
+  constexpr uint32_t oA = 0, oAt = 32768, oBt = 65536, oMisc = 98304;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + oMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + oMisc + 16);
+  const uint32_t bar_tma = smem_u32(&bars[0]), bar_mma = smem_u32(&bars[1]);
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(bar_tma, 1);
+    mbar_init(bar_mma, 1);
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tm = *tmem_slot;
+  const uint32_t tl = tm + (uint32_t(warp * 32) << 16);
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar_tma, 2u * 16384u);
+    tma_load_2d(sb + oA, &tmA, 0, 0, bar_tma);
+    tma_load_2d(sb + oA + 16384, &tmA, 64, 0, bar_tma);
+  }
+  const uint16_t* A16 = reinterpret_cast<const uint16_t*>(Am);
+  const uint16_t* B16 = reinterpret_cast<const uint16_t*>(Bm);
+  for (int j = 0; j < 2; ++j)
+    for (int c = 0; c < 8; ++c) {
+      uint32_t wa[4], wb[4];
+      for (int e = 0; e < 4; ++e) {
+        const int m = 64 * j + 8 * c + 2 * e;
+        wa[e] = pack2(A16[m * 128 + tid], A16[(m + 1) * 128 + tid]);
+        wb[e] = pack2(B16[m * 128 + tid], B16[(m + 1) * 128 + tid]);
+      }
+      *reinterpret_cast<uint4*>(sm + oAt + j * 16384 + sw128(tid, c)) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+      *reinterpret_cast<uint4*>(sm + oBt + j * 16384 + sw128(tid, c)) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+    }
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w[16];
+    for (int i = 0; i < 16; ++i) w[i] = pack2(A16[tid * 128 + 32 * j + 2 * i], A16[tid * 128 + 32 * j + 2 * i + 1]);
+    tmem_st_x16(tl + 384u + 16u * j, w);
+  }
+  tmem_st_wait();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  bool ok = mbar_wait(bar_tma, 0, kWaitNs);
+  if (!__syncthreads_or(!ok)) {
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t id_k = idesc_bf16(128, 128, 0, 1), id_mn = idesc_bf16(128, 128, 1, 1);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tm + 0, kdesc(sb + oA, kk, 16384), sdesc_sw128(sb + oBt + kk * 2048, 16384, 1024), id_k, kk);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ts(tm + 128, tm + 384u + 8u * kk, sdesc_sw128(sb + oBt + kk * 2048, 16384, 1024), id_k, kk);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tm + 256, sdesc_sw128(sb + oAt + kk * 2048, 16384, 1024),
+               sdesc_sw128(sb + oBt + kk * 2048, 16384, 1024), id_mn, kk);
+      mma_commit(bar_mma);
+    }
+    ok = mbar_wait(bar_mma, 0, kWaitNs);
+    if (!__syncthreads_or(!ok)) {
+      tc_fence_after();
+      uint32_t r[32];
+      for (int t = 0; t < 3; ++t)
+        for (int j = 0; j < 4; ++j) {
+          tmem_ld_x32(tl + 128u * t + 32u * j, r);
+          for (int i = 0; i < 32; ++i) out[(6 + t) * 16384 + tid * 128 + 32 * j + i] = __uint_as_float(r[i]);
+        }
+    } else if (tid == 0) {
+      raise_status(status, SSS_ERR_TIMEOUT);
+    }
+  } else if (tid == 0) {
+    raise_status(status, SSS_ERR_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tm, 512);
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -805,6 +951,19 @@ bool make_bc_map(CUtensorMap* m, const void* ptr, int64_t Bz, int64_t L, int G, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// raw input [Bz][L][D] bf16 as a 3-D tensor; boxes of 64 channels x 131 rows x 1
+bool make_x_map(CUtensorMap* m, const void* ptr, int64_t Bz, int64_t L, int64_t D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(L), cuuint64_t(Bz)};
+  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(L) * D * 2};
+  const cuuint32_t box[3] = {64, kXsRows, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_tile_map(CUtensorMap* m, const void* ptr) {  // [128][128] bf16
   auto fn = encode_fn();
   if (!fn) return false;
@@ -822,15 +981,20 @@ cudaError_t launch_tc(const void* x, const void* dt, const float* A, const void*
                       const float* h0, float* hT, void* y, const float* w, const float* bias,
                       const void* s_in, void* s_out, int K, int64_t Bz, int64_t L, int H, int G,
                       int* status, cudaStream_t st) {
-  CUtensorMap mB, mC;
+  CUtensorMap mB, mC, mX;
   if (!make_bc_map(&mB, B, Bz, L, G, kN) || !make_bc_map(&mC, C, Bz, L, G, kN))
     return cudaErrorInvalidValue;
+  if (FUSED) {
+    if (!make_x_map(&mX, x, Bz, L, int64_t(H) * kP)) return cudaErrorInvalidValue;
+  } else {
+    mX = mB;  // unused
+  }
   auto kern = ssm_scan_tc_kernel<TX, TY, FUSED>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
   if (e != cudaSuccess) return e;
   kern<<<unsigned(Bz * H), kThreads, kSmemBytes, st>>>(
-      mB, mC, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, h0, hT,
+      mB, mC, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, h0, hT,
       static_cast<TY*>(y), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out), K,
       int(L), H, G, status);
   return cudaGetLastError();
@@ -882,12 +1046,20 @@ cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* st
                                cudaStream_t st) {
   CUtensorMap mA, mB;
   if (!make_tile_map(&mA, A) || !make_tile_map(&mB, B)) return cudaErrorInvalidValue;
-  const uint32_t smem = 114688 + 64 + 1024;
+  const uint32_t smem = 131072 + 64 + 1024;
   cudaError_t e = cudaFuncSetAttribute(tc_selftest_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem));
   if (e != cudaSuccess) return e;
   tc_selftest_kernel<<<1, 128, smem, st>>>(mA, mB, static_cast<const __nv_bfloat16*>(A),
                                            static_cast<const __nv_bfloat16*>(B), out, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const uint32_t smem2 = 98304 + 64 + 1024;
+  e = cudaFuncSetAttribute(tc_selftest2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(smem2));
+  if (e != cudaSuccess) return e;
+  tc_selftest2_kernel<<<1, 128, smem2, st>>>(mA, static_cast<const __nv_bfloat16*>(A),
+                                             static_cast<const __nv_bfloat16*>(B), out, status);
   return cudaGetLastError();
 }
 
