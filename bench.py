@@ -57,10 +57,23 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def traffic_from_profile(kernel: str):
-    """dram bytes per launch from the committed ncu summary, if it covers the
-    current build of the kernel (the summary states the source hash)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}.md")
+def kernel_source_hash(kernel: str) -> str:
+    """sha256 (first 16 hex digits) of the kernel's .cu file followed by the
+    two shared headers it includes."""
+    import hashlib
+    d = os.path.join(ROOT, "selective_ssm_scan_gb300", "csrc")
+    h = hashlib.sha256()
+    for fn in (f"{kernel}.cu", "tc_ptx.cuh", "common.cuh"):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary of the kernel on
+    this workload, if it covers the current build of the kernel (the summary
+    states the source hash)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -74,8 +87,7 @@ def traffic_from_profile(kernel: str):
         if line.startswith("traffic_bytes_per_launch:"):
             val = int(float(line.split(":", 1)[1].strip()))
     try:
-        fn = os.path.join(ROOT, "selective_ssm_scan_gb300", "csrc", f"{kernel}.cu")
-        cur = hashlib.sha256(open(fn, "rb").read()).hexdigest()[:16]
+        cur = kernel_source_hash(kernel)
     except OSError:
         return None
     if src != cur:
@@ -321,7 +333,7 @@ def main():
     tc_flops = s.Bz * s.H * chunks * 2 * Q * (Q * s.N + Q * s.P + 2 * s.P * s.N)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm,
-                "traffic": traffic_from_profile("ssm_scan_tc"),
+                "traffic": traffic_from_profile("ssm_scan_tc", WORKLOAD),
                 "kernel": "ssm_scan_tc_kernel<bf16,bf16,fused> (conv+SiLU+scan, one launch "
                           "per segment)",
                 "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_ms": fused_avg,

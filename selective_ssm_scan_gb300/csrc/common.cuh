@@ -69,6 +69,11 @@ __device__ __forceinline__ void ld_vec(const T* __restrict__ p, float* v) {
     u.r = __ldg(reinterpret_cast<const uint2*>(p));
 #pragma unroll
     for (int i = 0; i < VEC; ++i) v[i] = to_f32(u.e[i]);
+  } else if constexpr (BYTES == 4 && VEC == 2) {
+    union { uint32_t r; T e[2]; } u;
+    u.r = __ldg(reinterpret_cast<const unsigned int*>(p));
+    v[0] = to_f32(u.e[0]);
+    v[1] = to_f32(u.e[1]);
   } else {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) v[i] = to_f32(p[i]);
@@ -91,6 +96,11 @@ __device__ __forceinline__ void st_vec(T* __restrict__ p, const float* v) {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) u.e[i] = from_f32<T>(v[i]);
     *reinterpret_cast<uint2*>(p) = u.r;
+  } else if constexpr (BYTES == 4 && VEC == 2) {
+    union { uint32_t r; T e[2]; } u;
+    u.e[0] = from_f32<T>(v[0]);
+    u.e[1] = from_f32<T>(v[1]);
+    *reinterpret_cast<uint32_t*>(p) = u.r;
   } else {
 #pragma unroll
     for (int i = 0; i < VEC; ++i) p[i] = from_f32<T>(v[i]);

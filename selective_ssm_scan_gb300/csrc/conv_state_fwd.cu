@@ -6,15 +6,19 @@
 // u = [S_0..S_{K-2}, x_0..x_{L-1}], z_t = bias + sum_k w_k u_{t+k},
 // F = u[L : L+K-1].
 //
-// GB300 mapping (HBM-bound: read x once, write u once):
-//  * a thread owns VEC adjacent channels (16 bytes of x: 8 bf16 or 4 fp32)
-//    and TILE consecutive tokens; a warp covers 32*VEC adjacent channels of
-//    one token, so every load and store instruction is a coalesced 128-bit
-//    access of a contiguous 512-byte run;
-//  * the whole TILE of x is loaded into registers before any arithmetic, so
-//    each thread keeps TILE independent 16-byte loads in flight;
-//  * the K-1 samples before the tile come from x (L2 hits: they are the
-//    previous tile's tail) or, for tile 0, from the conv state;
+// GB300 mapping (HBM-bound: read x once, write u once; the kernel is
+// latency-bound unless each SM keeps enough loads in flight):
+//  * a work item is VEC adjacent channels (4 bytes of x: a bf16 pair or one
+//    fp32) by TILE consecutive tokens of one sequence; a warp covers
+//    32*VEC adjacent channels of a token, so each load is one fully used
+//    128-byte line and the stores are 256 (fp32 u) or 128 (bf16 u) bytes;
+//  * the TILE inputs of an item are loaded, still packed, into TILE
+//    registers before any arithmetic: a thread holds ~40 registers, so an SM
+//    runs 1500+ threads with TILE independent loads each in flight;
+//  * the K-1 samples before the tile come from x (L2 hits: the previous
+//    tile's tail) or, for tile 0, from the conv state;
+//  * a grid-stride loop over items on a grid of (SMs x resident CTAs) keeps
+//    every SM busy to the end (no partial last wave);
 //  * the thread of tile 0 is the only one that reads S for its channels and
 //    the only one that writes F, so state_out may alias state_in.
 #include "common.cuh"
@@ -22,90 +26,99 @@
 namespace sss {
 
 constexpr int kConvMaxK = 8;
+constexpr int kConvThreads = 256;
 
 template <typename T, int VEC>
-struct __align__((sizeof(T) * VEC) >= 16 ? 16 : (sizeof(T) * VEC)) Pack {
+struct __align__(sizeof(T) * VEC) Pack {
   T e[VEC];
 };
 
-template <typename TX, typename TU, int VEC, int TILE, int KT>
-__global__ void __launch_bounds__(256, 3)
-conv_state_fwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
-                      const float* __restrict__ bias, const TX* s_in, TX* s_out,
-                      TU* __restrict__ u, int64_t L, int64_t D, int K_rt,
-                      int apply_silu, int64_t n_dvec, int64_t n_tiles, int64_t n_items) {
+// One work item: VEC channels from d0 by the tokens [t0, t0 + nt) of
+// sequence b (xp = &x[b][t0][d0], up = &u[b][t0][d0]).  FULL: nt == TILE,
+// no per-token predicates.
+template <typename TX, typename TU, int VEC, int TILE, int KT, bool SILU, bool FULL>
+__device__ __forceinline__ void conv_item(const TX* __restrict__ xp, const float* __restrict__ w,
+                                          const float* __restrict__ bias, const TX* s_in,
+                                          TU* __restrict__ up, int64_t b, int d0, int tile,
+                                          int nt, int D, int K) {
   constexpr int MK = KT > 0 ? KT : kConvMaxK;  // register window capacity
-  const int K = KT > 0 ? KT : K_rt;
+  constexpr int MW = MK - 1 > 0 ? MK - 1 : 1;
   using PX = Pack<TX, VEC>;
-  const int64_t item = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (item >= n_items) return;
-  const int64_t dvec = item % n_dvec;
-  const int64_t rest = item / n_dvec;
-  const int64_t tile = rest % n_tiles;
-  const int64_t b = rest / n_tiles;
-  const int64_t d0 = dvec * VEC;
-  const int64_t t0 = tile * TILE;
-  const int64_t nt = (L - t0) < TILE ? (L - t0) : TILE;
-
-  // the tile's inputs: all loads are issued before any arithmetic
+  // the tile's inputs, packed, all issued before any arithmetic
   PX xr[TILE];
+  {
+    const TX* q = xp;
 #pragma unroll
-  for (int i = 0; i < TILE; ++i)
-    if (i < nt) xr[i] = *reinterpret_cast<const PX*>(x + (b * L + t0 + i) * D + d0);
+    for (int i = 0; i < TILE; ++i) {
+      if (FULL || i < nt) xr[i] = *reinterpret_cast<const PX*>(q);
+      q += D;
+    }
+  }
 
-  // window: the K-1 extended-sequence samples before token t0, oldest first.
-  // Tile 0 reads them from the conv state S (t0 - (K-1) + j < 0 there);
-  // later tiles read the previous tile's tail of x (TILE >= K-1).
-  float win[MK - 1 > 0 ? MK - 1 : 1][VEC];
+  // window: the K-1 extended-sequence samples before token t0, oldest
+  // first.  Tile 0 reads them from the conv state S; later tiles read the
+  // previous tile's tail of x (TILE >= K-1).
+  float win[MW][VEC];
 #pragma unroll
-  for (int j = 0; j < MK - 1; ++j) {
+  for (int j = 0; j < MW; ++j) {
 #pragma unroll
-    for (int v = 0; v < VEC; ++v) win[j][v] = 0.0f;  // unused entries (j >= K-1) stay 0
+    for (int v = 0; v < VEC; ++v) win[j][v] = 0.0f;  // unused entries stay 0
     if (j < K - 1) {
       if (tile == 0) {
+        if (s_in) {
 #pragma unroll
-        for (int v = 0; v < VEC; ++v)
-          win[j][v] = s_in ? to_f32(s_in[(b * D + d0 + v) * (K - 1) + j]) : 0.0f;
+          for (int v = 0; v < VEC; ++v)
+            win[j][v] = to_f32(s_in[(int64_t(b) * D + d0 + v) * (K - 1) + j]);
+        }
       } else {
-        const PX p = *reinterpret_cast<const PX*>(x + (b * L + t0 - (K - 1) + j) * D + d0);
+        const PX q = *reinterpret_cast<const PX*>(xp - int64_t(K - 1 - j) * D);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) win[j][v] = to_f32(p.e[v]);
+        for (int v = 0; v < VEC; ++v) win[j][v] = to_f32(q.e[v]);
       }
     }
   }
 
   // weights: wk[k] multiplies window sample k, wx the current input
-  float wk[MK - 1 > 0 ? MK - 1 : 1][VEC];
+  float wk[MW][VEC];
   float wx[VEC], bs[VEC];
 #pragma unroll
   for (int v = 0; v < VEC; ++v) {
     bs[v] = bias ? bias[d0 + v] : 0.0f;
-    wx[v] = w[(d0 + v) * K + (K - 1)];
+    if constexpr (KT == 4) {
+      // one 16-byte load per channel (the host checks w's alignment)
+      const float4 q = __ldg(reinterpret_cast<const float4*>(w) + (d0 + v));
+      wk[0][v] = q.x;
+      wk[1][v] = q.y;
+      wk[2][v] = q.z;
+      wx[v] = q.w;
+    } else {
+      wx[v] = w[(d0 + v) * K + (K - 1)];
 #pragma unroll
-    for (int k = 0; k < MK - 1; ++k) wk[k][v] = (k < K - 1) ? w[(d0 + v) * K + k] : 0.0f;
+      for (int k = 0; k < MW; ++k) wk[k][v] = (k < K - 1) ? w[(d0 + v) * K + k] : 0.0f;
+    }
   }
 
 #pragma unroll
-  for (int i = 0; i < TILE; ++i) {
-    if (i < nt) {
+  for (int i = 0; i < TILE; ++i, up += D) {
+    if (FULL || i < nt) {
       float xv[VEC], z[VEC];
 #pragma unroll
       for (int v = 0; v < VEC; ++v) {
         xv[v] = to_f32(xr[i].e[v]);
         float acc = bs[v];
 #pragma unroll
-        for (int k = 0; k < MK - 1; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
+        for (int k = 0; k < MW; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
         acc = fmaf(wx[v], xv[v], acc);
-        z[v] = apply_silu ? silu(acc) : acc;
+        z[v] = SILU ? silu(acc) : acc;  // compile-time: no branch in the loop
       }
-      st_vec<TU, VEC>(u + (b * L + t0 + i) * D + d0, z);
+      st_vec<TU, VEC>(up, z);
       // slide the window by one sample (entries k >= K-1 stay unused: wk = 0)
 #pragma unroll
-      for (int k = 0; k < MK - 2; ++k)
+      for (int k = 0; k < MW - 1; ++k)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) win[k][v] = (k < K - 2) ? win[k + 1][v] : win[k][v];
 #pragma unroll
-      for (int k = 0; k < MK - 1; ++k)
+      for (int k = 0; k < MW; ++k)
         if (k == K - 2) {
 #pragma unroll
           for (int v = 0; v < VEC; ++v) win[k][v] = xv[v];
@@ -113,21 +126,51 @@ conv_state_fwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
     }
   }
 
-  // final state F_j = ext[L + j].  Only tile 0 reads S for these channels and
-  // it writes F last, in increasing j: when L + j < K-1 it reads S[L + j],
-  // an entry it has not written yet (L + j >= j), so state_out may alias
-  // state_in.
-  if (tile == 0 && s_out) {
-    for (int j = 0; j < K - 1; ++j) {
-      const int64_t e = L + j;
+}
+
+template <typename TX, typename TU, int VEC, int TILE, int KT, bool SILU>
+__global__ void __launch_bounds__(kConvThreads)
+conv_state_fwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
+                      const float* __restrict__ bias, const TX* s_in, TX* s_out,
+                      TU* __restrict__ u, int L, int D, int K_rt,
+                      int n_dvec, int n_tiles, int n_items) {
+  const int K = KT > 0 ? KT : K_rt;
+  // item = (b * n_tiles + tile) * n_dvec + dvec, 32-bit (the host splits
+  // the batch so that n_items fits)
+  for (int item = blockIdx.x * blockDim.x + threadIdx.x; item < n_items;
+       item += gridDim.x * blockDim.x) {
+    const int dvec = item % n_dvec;
+    const int rest = item / n_dvec;
+    const int tile = rest % n_tiles;
+    const int b = rest / n_tiles;
+    const int d0 = dvec * VEC;
+    const int t0 = tile * TILE;
+    const int nt = (L - t0) < TILE ? (L - t0) : TILE;
+    const int64_t off = (int64_t(b) * L + t0) * D + d0;
+    if (nt == TILE)
+      conv_item<TX, TU, VEC, TILE, KT, SILU, true>(x + off, w, bias, s_in, u + off, b, d0, tile,
+                                                   nt, D, K);
+    else
+      conv_item<TX, TU, VEC, TILE, KT, SILU, false>(x + off, w, bias, s_in, u + off, b, d0, tile,
+                                                    nt, D, K);
+
+    // final state F_j = ext[L + j].  Only tile 0 reads S for these channels
+    // and it writes F last, in increasing j: when L + j < K-1 it reads
+    // S[L + j], an entry it has not written yet (L + j >= j), so state_out
+    // may alias state_in.
+    if (tile == 0 && s_out) {
+      const int64_t sb = (int64_t(b) * D + d0) * (K - 1);
+      for (int j = 0; j < K - 1; ++j) {
+        const int e = L + j;
 #pragma unroll
-      for (int v = 0; v < VEC; ++v) {
-        TX fv;
-        if (e < K - 1)
-          fv = s_in ? s_in[(b * D + d0 + v) * (K - 1) + e] : from_f32<TX>(0.0f);
-        else
-          fv = x[(b * L + (e - (K - 1))) * D + d0 + v];
-        s_out[(b * D + d0 + v) * (K - 1) + j] = fv;
+        for (int v = 0; v < VEC; ++v) {
+          TX fv;
+          if (e < K - 1)
+            fv = s_in ? s_in[sb + v * (K - 1) + e] : from_f32<TX>(0.0f);
+          else
+            fv = x[(int64_t(b) * L + (e - (K - 1))) * D + d0 + v];
+          s_out[sb + v * (K - 1) + j] = fv;
+        }
       }
     }
   }
@@ -140,26 +183,39 @@ static cudaError_t launch_conv(const void* x, const float* w, const float* bias,
                                cudaStream_t st) {
   const int64_t n_dvec = D / VEC;
   const int64_t n_tiles = L > 0 ? (L + TILE - 1) / TILE : 1;
-  const int64_t n_items = Bz * n_tiles * n_dvec;
-  if (n_items == 0) return cudaSuccess;
-  const int threads = 256;
-  const int64_t blocks = (n_items + threads - 1) / threads;
-  if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto args = [&](auto kern) {
-    kern<<<unsigned(blocks), threads, 0, st>>>(
-        static_cast<const TX*>(x), w, bias, static_cast<const TX*>(s_in),
-        static_cast<TX*>(s_out), static_cast<TU*>(u), L, D, K, silu_on, n_dvec,
-        n_tiles, n_items);
+  const int64_t per_seq = n_tiles * n_dvec;  // items of one sequence
+  if (Bz == 0 || per_seq == 0) return cudaSuccess;
+  if (L > 0x7fffffffLL - TILE || D > 0x7fffffffLL || per_seq > 0x7fffffffLL)
+    return cudaErrorInvalidValue;
+  // sequences per launch so that the 32-bit item index cannot overflow
+  const int64_t seq_per_launch = 0x7fffffffLL / per_seq;
+  auto args = [&](auto kern) -> cudaError_t {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kConvThreads, 0);
+    if (e != cudaSuccess) return e;
+    const int64_t cap = int64_t(sm_count()) * (per_sm > 0 ? per_sm : 1);
+    for (int64_t b0 = 0; b0 < Bz; b0 += seq_per_launch) {
+      const int64_t nb = (Bz - b0) < seq_per_launch ? (Bz - b0) : seq_per_launch;
+      const int64_t n_items = nb * per_seq;
+      const int64_t need = (n_items + kConvThreads - 1) / kConvThreads;
+      const int64_t blocks = need < cap ? need : cap;
+      const TX* xb = static_cast<const TX*>(x) + b0 * L * D;
+      const TX* sib = s_in ? static_cast<const TX*>(s_in) + b0 * D * (K - 1) : nullptr;
+      TX* sob = s_out ? static_cast<TX*>(s_out) + b0 * D * (K - 1) : nullptr;
+      TU* ub = static_cast<TU*>(u) + b0 * L * D;
+      kern<<<unsigned(blocks), kConvThreads, 0, st>>>(xb, w, bias, sib, sob, ub, int(L), int(D),
+                                                      K, int(n_dvec), int(n_tiles), int(n_items));
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
   };
-  if (K == 4)
-    args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 4>);
-  else if (K == 3)
-    args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 3>);
-  else if (K == 2)
-    args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 2>);
-  else
-    args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 0>);
-  return cudaGetLastError();
+  if (!silu_on) return args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 0, false>);
+  if (K == 4 && reinterpret_cast<uintptr_t>(w) % 16 == 0)
+    return args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 4, true>);
+  if (K == 3) return args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 3, true>);
+  if (K == 2) return args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 2, true>);
+  return args(conv_state_fwd_kernel<TX, TU, VEC, TILE, 0, true>);
 }
 
 template <typename TX, typename TU>
@@ -167,9 +223,12 @@ static cudaError_t conv_dispatch_u(const void* x, const float* w, const float* b
                                    const void* s_in, void* s_out, void* u, int64_t Bz,
                                    int64_t L, int64_t D, int K, int silu_on,
                                    cudaStream_t st) {
-  constexpr int VEC = 16 / int(sizeof(TX));
-  const bool aligned = (D % VEC == 0) && (reinterpret_cast<uintptr_t>(x) % 16 == 0) &&
-                       (reinterpret_cast<uintptr_t>(u) % 16 == 0);
+  // a bf16 pair (4 bytes) per thread when the channel count and the
+  // pointers allow it; one channel otherwise
+  constexpr int VEC = sizeof(TX) == 2 ? 2 : 1;
+  const bool aligned = (D % VEC == 0) &&
+                       (reinterpret_cast<uintptr_t>(x) % (sizeof(TX) * VEC) == 0) &&
+                       (reinterpret_cast<uintptr_t>(u) % (sizeof(TU) * VEC) == 0);
   if (aligned)
     return launch_conv<TX, TU, VEC, 8>(x, w, bias, s_in, s_out, u, Bz, L, D, K, silu_on, st);
   return launch_conv<TX, TU, 1, 16>(x, w, bias, s_in, s_out, u, Bz, L, D, K, silu_on, st);

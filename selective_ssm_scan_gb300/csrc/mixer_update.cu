@@ -14,7 +14,8 @@
 // request, is read and written once and dominates the traffic):
 //  * one CTA per (request, head), 8 warps; warp w owns state rows
 //    p = w + 8 r, lane l owns the float4 column groups n4 = l + 32 c, so the
-//    state moves as fully coalesced 16-byte accesses;
+//    state moves as fully coalesced 16-byte accesses and three CTAs share an
+//    SM (the loads of the state are what keeps HBM busy);
 //  * threads p < P first run the conv of channel d = h*P + p: they read every
 //    history slot they need into registers, compute u for the L_new tokens
 //    and only then store the new inputs into the slots, so the kernel is
@@ -60,7 +61,7 @@ __device__ __forceinline__ int64_t pos_mod(int64_t a, int64_t m) {
   return r < 0 ? r + m : r;
 }
 
-template <typename T, int RP, int CV>
+template <typename T, int RP, int CV, int KT>
 __global__ void __launch_bounds__(kUpdWarps * 32, RP * CV <= 8 ? 3 : 1)
 mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
                     const float* __restrict__ bias, T* conv_pool, int64_t pool, int S_len,
@@ -91,7 +92,8 @@ mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
     return;
   }
 
-  // ---- SSM state (loads issued first, consumed after the conv): rows p = warp + 8 rr, float4 groups n4 = lane + 32 c ---
+  // ---- SSM state (loads issued first, consumed after the conv):
+  //      rows p = warp + kUpdWarps rr, float4 groups n4 = lane + 32 c ----
   float* hs = ssm_pool + (r * H + h) * int64_t(P) * N;
   const int N4 = N / 4;
   float4 st[RP][CV];
@@ -110,29 +112,29 @@ mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
     T* row = conv_pool + (r * D + d) * S_len;
     // every history value this call needs is read before any slot write:
     // logical position p0 - (K-1) + j sits in slot (p0 - (K-1) + j) mod S_len
-    float win[kUpdMaxK - 1];
+    float win[KT - 1];
 #pragma unroll
-    for (int j = 0; j < kUpdMaxK - 1; ++j)
+    for (int j = 0; j < KT - 1; ++j)
       win[j] = (j < K - 1) ? to_f32(row[pos_mod(p0 - (K - 1) + j, S_len)]) : 0.0f;
-    float wk[kUpdMaxK];
+    float wk[KT];
 #pragma unroll
-    for (int k = 0; k < kUpdMaxK; ++k) wk[k] = k < K ? w[d * K + k] : 0.0f;
+    for (int k = 0; k < KT; ++k) wk[k] = k < K ? w[d * K + k] : 0.0f;
     const float bsd = bias ? bias[d] : 0.0f;
     for (int i = 0; i < L_new; ++i) {
       const float xv = to_f32(x[(int64_t(b) * L_new + i) * D + d]);
       float z = bsd;
 #pragma unroll
-      for (int k = 0; k < kUpdMaxK - 1; ++k)
+      for (int k = 0; k < KT - 1; ++k)
         if (k < K - 1) z = fmaf(wk[k], win[k], z);
 #pragma unroll
-      for (int k = 0; k < kUpdMaxK; ++k)
+      for (int k = 0; k < KT; ++k)
         if (k == K - 1) z = fmaf(wk[k], xv, z);
       us[i * P + p] = silu(z);
 #pragma unroll
-      for (int k = 0; k < kUpdMaxK - 2; ++k)
+      for (int k = 0; k < KT - 2; ++k)
         if (k < K - 2) win[k] = win[k + 1];
 #pragma unroll
-      for (int k = 0; k < kUpdMaxK - 1; ++k)
+      for (int k = 0; k < KT - 1; ++k)
         if (k == K - 2) win[k] = xv;
     }
     // store the inputs (not the outputs) at the write pointer, in token
@@ -192,14 +194,14 @@ mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
     }
 }
 
-template <typename T, int RP, int CV>
+template <typename T, int RP, int CV, int KT>
 static cudaError_t launch_upd(const void* x, const float* w, const float* bias, void* cp,
                               int64_t pool, int S_len, const int32_t* sl, const int32_t* ix,
                               const void* dt, const float* A, const void* B, const void* C,
                               float* sp, void* y, int64_t Bz, int L_new, int H, int P, int N,
                               int G, int K, int* status, cudaStream_t st) {
   const size_t smem = size_t(((L_new * P + 3) & ~3) + 2 * L_new * N + L_new) * sizeof(float);
-  auto kern = mixer_update_kernel<T, RP, CV>;
+  auto kern = mixer_update_kernel<T, RP, CV, KT>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
@@ -221,10 +223,14 @@ static cudaError_t upd_shape(const void* x, const float* w, const float* bias, v
                              const void* dt, const float* A, const void* B, const void* C,
                              float* sp, void* y, int64_t Bz, int L_new, int H, int P, int N,
                              int G, int K, int* status, cudaStream_t st) {
-#define SSS_UPD(RP, CV)                                                                    \
-  if (P <= kUpdWarps * RP && N <= 128 * CV)                                                \
-    return launch_upd<T, RP, CV>(x, w, bias, cp, pool, S_len, sl, ix, dt, A, B, C, sp, y,   \
-                                 Bz, L_new, H, P, N, G, K, status, st);
+#define SSS_UPD(RP, CV)                                                                     \
+  if (P <= kUpdWarps * RP && N <= 128 * CV) {                                               \
+    if (K <= 4)                                                                             \
+      return launch_upd<T, RP, CV, 4>(x, w, bias, cp, pool, S_len, sl, ix, dt, A, B, C, sp, y, \
+                                      Bz, L_new, H, P, N, G, K, status, st);                 \
+    return launch_upd<T, RP, CV, 8>(x, w, bias, cp, pool, S_len, sl, ix, dt, A, B, C, sp, y,   \
+                                    Bz, L_new, H, P, N, G, K, status, st);                   \
+  }
   SSS_UPD(1, 1)
   SSS_UPD(8, 1)
   SSS_UPD(16, 2)
