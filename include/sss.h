@@ -197,7 +197,11 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w,
  *  B, C               [Bz, L_new, G, N]   act_dtype
  *  ssm_pool           [pool, H, P, N]     float32, in/out
  *  y                  [Bz, L_new, H, P]   act_dtype
- * L_new <= 64.
+ * L_new <= 64.  With N == 128, P a multiple of 8 (P <= 128), L_new <= 8
+ * and 16-byte aligned x_new, w, bias, conv_pool, B, C and ssm_pool the
+ * update streams each (request, head) state block through shared memory
+ * with bulk copies (persistent kernel); other shapes run one CTA per
+ * (request, head).  Both give the same result.
  */
 sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
                             const float* w, const float* bias, void* conv_pool,
@@ -208,6 +212,12 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
                             float* ssm_pool, void* y, int64_t Bz, int L_new,
                             int H, int P, int N, int G, int K,
                             sss_stream_t stream);
+
+/* Which kernel sss_mixer_update picks for these sizes (given 16-byte
+ * aligned tensors and a bias): 1 = bulk-copy pipelined kernel, 0 = one CTA
+ * per (request, head), -1 = unsupported. */
+int sss_mixer_update_path(int L_new, int P, int N, int K, int S_len,
+                          sss_dtype act_dtype);
 
 /*
  * sss_tcgen05_selftest -- diagnostic of the tensor-core operand layouts the

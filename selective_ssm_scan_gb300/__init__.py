@@ -8,7 +8,7 @@ calls are enqueued on torch's current stream.  Importing this module loads
 ``python selective_ssm_scan_gb300/build.py``); there is no fallback.
 
 Functions (same names as the C ABI in include/sss.h, minus the prefix):
-    conv_state_fwd, ssm_scan_fwd, ssm_scan_path, ssm_scan_workspace_size,
+    conv_state_fwd, ssm_scan_fwd, ssm_scan_path, ssm_scan_workspace_size, mixer_update_path,
     mixer_update, device_status, version, status_string
 plus ``mixer_fwd`` (conv_state_fwd then ssm_scan_fwd: one segment of the
 streaming forward with both states passed) and ``library_path``.
@@ -51,6 +51,8 @@ _lib.sss_conv_state_fwd.restype = _i
 _lib.sss_conv_state_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _i, _i64, _i64, _i64, _i, _i, _p]
 _lib.sss_ssm_scan_workspace_size.restype = ctypes.c_size_t
 _lib.sss_ssm_scan_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i]
+_lib.sss_mixer_update_path.restype = _i
+_lib.sss_mixer_update_path.argtypes = [_i, _i, _i, _i, _i, _i]
 _lib.sss_ssm_scan_path.restype = _i
 _lib.sss_ssm_scan_path.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
 _lib.sss_ssm_scan_fwd.restype = _i
@@ -236,6 +238,12 @@ def mixer_update(x_new: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tens
                                L_new, H, P, N, G, K, _stream(stream))
     _check("sss_mixer_update", rc)
     return y
+
+
+def mixer_update_path(L_new, P, N, K, S_len, act_dtype) -> int:
+    """1 = bulk-copy pipelined update kernel, 0 = one CTA per (request, head),
+    -1 = unsupported (for 16-byte aligned tensors with a bias)."""
+    return int(_lib.sss_mixer_update_path(L_new, P, N, K, S_len, _dtype_code(act_dtype)))
 
 
 def tcgen05_selftest(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:

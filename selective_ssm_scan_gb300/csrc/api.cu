@@ -34,6 +34,7 @@ cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
                                cudaStream_t st);
 bool mixer_update_supports(int P, int N, int K, int L_new);
+int mixer_update_path(sss_dtype at, int S_len, int L_new, int P, int N, int K);
 cudaError_t mixer_update_launch(const void* x, sss_dtype at, const float* w, const float* bias,
                                 void* cp, int64_t pool, int S_len, const int32_t* sl,
                                 const int32_t* ix, const void* dt, const float* A,
@@ -212,6 +213,13 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const
   return from_cuda(mixer_fwd_tc_launch(x, w, bias, conv_state_in, conv_state_out, dt, A, B, C,
                                        h0_in, hT_out, y, y_dtype, Bz, L, H, G, K, status_word(),
                                        st));
+}
+
+int sss_mixer_update_path(int L_new, int P, int N, int K, int S_len, sss_dtype act_dtype) {
+  if (!dtype_ok(act_dtype) || L_new < 0 || P < 1 || N < 1 || K < 1 || S_len < 1 ||
+      S_len < K - 1)
+    return -1;
+  return sss::mixer_update_path(act_dtype, S_len, L_new, P, N, K);
 }
 
 sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype, const float* w,

@@ -157,12 +157,6 @@ __device__ __forceinline__ void write_split_row(uint8_t* hi_tile, uint8_t* lo_ti
 }
 
 // Named barrier among the threads of one role (ids 1, 2; 0 is __syncthreads).
-__device__ __forceinline__ void role_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 
 struct Ctl {
   uint32_t bars;              // smem address of barrier 0

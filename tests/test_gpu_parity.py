@@ -275,12 +275,16 @@ def _decode_gpu(d, inp):
 
 
 @pytest.mark.parametrize("L_new,S_len,K", [(1, 4, 4), (4, 4, 4), (6, 4, 4), (2, 3, 4),
-                                           (3, 9, 4), (1, 2, 3), (2, 1, 2), (5, 8, 8)])
-@pytest.mark.parametrize("H,P,N", [(2, 64, 128), (3, 4, 8)])
+                                           (3, 9, 4), (1, 2, 3), (2, 1, 2), (5, 8, 8),
+                                           (8, 4, 4), (10, 4, 4)])
+@pytest.mark.parametrize("H,P,N", [(2, 64, 128), (3, 4, 8), (5, 128, 128), (3, 24, 128)])
 def test_decode_parity(L_new, S_len, K, H, P, N):
     d = synth.DECODE["decode_256x1"].with_(Bz=5, pool=9, L_new=L_new, S_len=S_len, K=K, H=H,
                                            P=P, N=N, max_seqlen=30)
     inp = synth.decode_inputs(d)
+    # N = 128, P % 8 == 0, L_new <= 8: the bulk-copy pipelined kernel
+    want = 1 if (N == 128 and P % 8 == 0 and L_new <= 8) else 0
+    assert sss.mixer_update_path(L_new, P, N, K, S_len, torch.bfloat16) == want
     y, g = _decode_gpu(d, inp)
     y_ref, cp_ref, sp_ref, nbad = oracle.mixer_update(
         inp["x"], inp["w"], inp["bias"], inp["conv_pool"], inp["cache_seqlens"],
@@ -296,8 +300,9 @@ def test_decode_parity(L_new, S_len, K, H, P, N):
                                   inp["conv_pool"].data.view(np.int16)[untouched])
 
 
-def test_decode_bad_rows_are_skipped_and_reported():
-    d = synth.DECODE["decode_256x1"].with_(Bz=3, pool=5, H=2, P=4, N=8)
+@pytest.mark.parametrize("H,P,N", [(2, 4, 8), (2, 64, 128)])
+def test_decode_bad_rows_are_skipped_and_reported(H, P, N):
+    d = synth.DECODE["decode_256x1"].with_(Bz=3, pool=5, H=H, P=P, N=N)
     inp = synth.decode_inputs(d)
     inp["conv_state_indices"].data[:] = [0, 9, 2]
     inp["cache_seqlens"].data[:] = [3, 4, -1]
@@ -310,6 +315,27 @@ def test_decode_bad_rows_are_skipped_and_reported():
     assert nbad == 2
     assert_y_close(f64(y), y_ref)
     np.testing.assert_array_equal(f64(g["conv_pool"]), cp_ref)
+
+
+@pytest.mark.parametrize("L_new", [1, 3])
+def test_decode_fp32_activations_and_no_bias(L_new):
+    """fp32 activations through the pipelined kernel (fp32 bound), bias absent."""
+    d = synth.DECODE["decode_256x1"].with_(dtype="f32", Bz=7, pool=11, L_new=L_new, H=3, P=64,
+                                           N=128, max_seqlen=40)
+    assert sss.mixer_update_path(L_new, 64, 128, 4, 4, torch.float32) == 1
+    inp = synth.decode_inputs(d)
+    inp["bias"] = None
+    g = {k: (T(v) if v is not None else None) for k, v in inp.items()}
+    y = sss.mixer_update(g["x"], g["w"], None, g["conv_pool"], g["cache_seqlens"],
+                         g["conv_state_indices"], g["dt"], g["A"], g["B"], g["C"], g["ssm_pool"])
+    torch.cuda.synchronize()
+    y_ref, cp_ref, sp_ref, nbad = oracle.mixer_update(
+        inp["x"], inp["w"], None, inp["conv_pool"], inp["cache_seqlens"],
+        inp["conv_state_indices"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["ssm_pool"])
+    assert nbad == 0 and sss.device_status() == 0
+    assert_rel(f64(y), y_ref, F32_REL, "y")
+    np.testing.assert_array_equal(f64(g["conv_pool"]), cp_ref)
+    assert_rel(f64(g["ssm_pool"]), sp_ref, F32_REL, "ssm pool")
 
 
 @pytest.mark.parametrize("name", ["decode_256x1", "decode_256x4"])
