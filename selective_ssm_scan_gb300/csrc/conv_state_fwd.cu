@@ -17,8 +17,9 @@
 //    runs 1500+ threads with TILE independent loads each in flight;
 //  * the K-1 samples before the tile come from x (L2 hits: the previous
 //    tile's tail) or, for tile 0, from the conv state;
-//  * a grid-stride loop over items on a grid of (SMs x resident CTAs) keeps
-//    every SM busy to the end (no partial last wave);
+//  * a 2-D grid (channel vectors x token tiles x sequences) gives every item
+//    its coordinates without any division; ~46 registers let five
+//    256-thread CTAs share an SM;
 //  * the thread of tile 0 is the only one that reads S for its channels and
 //    the only one that writes F, so state_out may alias state_in.
 #include "common.cuh"
@@ -132,45 +133,40 @@ template <typename TX, typename TU, int VEC, int TILE, int KT, bool SILU>
 __global__ void __launch_bounds__(kConvThreads)
 conv_state_fwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
                       const float* __restrict__ bias, const TX* s_in, TX* s_out,
-                      TU* __restrict__ u, int L, int D, int K_rt,
-                      int n_dvec, int n_tiles, int n_items) {
+                      TU* __restrict__ u, int L, int D, int K_rt, int n_dvec, int tile_base) {
   const int K = KT > 0 ? KT : K_rt;
-  // item = (b * n_tiles + tile) * n_dvec + dvec, 32-bit (the host splits
-  // the batch so that n_items fits)
-  for (int item = blockIdx.x * blockDim.x + threadIdx.x; item < n_items;
-       item += gridDim.x * blockDim.x) {
-    const int dvec = item % n_dvec;
-    const int rest = item / n_dvec;
-    const int tile = rest % n_tiles;
-    const int b = rest / n_tiles;
-    const int d0 = dvec * VEC;
-    const int t0 = tile * TILE;
-    const int nt = (L - t0) < TILE ? (L - t0) : TILE;
-    const int64_t off = (int64_t(b) * L + t0) * D + d0;
-    if (nt == TILE)
-      conv_item<TX, TU, VEC, TILE, KT, SILU, true>(x + off, w, bias, s_in, u + off, b, d0, tile,
-                                                   nt, D, K);
-    else
-      conv_item<TX, TU, VEC, TILE, KT, SILU, false>(x + off, w, bias, s_in, u + off, b, d0, tile,
-                                                    nt, D, K);
+  // grid: x = channel vectors, y = token tiles (from tile_base), z = sequences
+  const int dvec = blockIdx.x * blockDim.x + threadIdx.x;
+  if (dvec >= n_dvec) return;
+  const int tile = tile_base + int(blockIdx.y);
+  const int64_t b = blockIdx.z;
+  const int d0 = dvec * VEC;
+  const int t0 = tile * TILE;
+  const int nt = (L - t0) < TILE ? (L - t0) : TILE;
+  const int64_t off = (b * L + t0) * D + d0;
+  if (nt == TILE)
+    conv_item<TX, TU, VEC, TILE, KT, SILU, true>(x + off, w, bias, s_in, u + off, b, d0, tile,
+                                                 nt, D, K);
+  else
+    conv_item<TX, TU, VEC, TILE, KT, SILU, false>(x + off, w, bias, s_in, u + off, b, d0, tile,
+                                                  nt, D, K);
 
-    // final state F_j = ext[L + j].  Only tile 0 reads S for these channels
-    // and it writes F last, in increasing j: when L + j < K-1 it reads
-    // S[L + j], an entry it has not written yet (L + j >= j), so state_out
-    // may alias state_in.
-    if (tile == 0 && s_out) {
-      const int64_t sb = (int64_t(b) * D + d0) * (K - 1);
-      for (int j = 0; j < K - 1; ++j) {
-        const int e = L + j;
+  // final state F_j = ext[L + j].  Only tile 0 reads S for these channels
+  // and it writes F last, in increasing j: when L + j < K-1 it reads
+  // S[L + j], an entry it has not written yet (L + j >= j), so state_out
+  // may alias state_in.
+  if (tile == 0 && s_out) {
+    const int64_t sb = (b * D + d0) * (K - 1);
+    for (int j = 0; j < K - 1; ++j) {
+      const int e = L + j;
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-          TX fv;
-          if (e < K - 1)
-            fv = s_in ? s_in[sb + v * (K - 1) + e] : from_f32<TX>(0.0f);
-          else
-            fv = x[(int64_t(b) * L + (e - (K - 1))) * D + d0 + v];
-          s_out[sb + v * (K - 1) + j] = fv;
-        }
+      for (int v = 0; v < VEC; ++v) {
+        TX fv;
+        if (e < K - 1)
+          fv = s_in ? s_in[sb + v * (K - 1) + e] : from_f32<TX>(0.0f);
+        else
+          fv = x[(b * L + (e - (K - 1))) * D + d0 + v];
+        s_out[sb + v * (K - 1) + j] = fv;
       }
     }
   }
@@ -183,30 +179,24 @@ static cudaError_t launch_conv(const void* x, const float* w, const float* bias,
                                cudaStream_t st) {
   const int64_t n_dvec = D / VEC;
   const int64_t n_tiles = L > 0 ? (L + TILE - 1) / TILE : 1;
-  const int64_t per_seq = n_tiles * n_dvec;  // items of one sequence
-  if (Bz == 0 || per_seq == 0) return cudaSuccess;
-  if (L > 0x7fffffffLL - TILE || D > 0x7fffffffLL || per_seq > 0x7fffffffLL)
-    return cudaErrorInvalidValue;
-  // sequences per launch so that the 32-bit item index cannot overflow
-  const int64_t seq_per_launch = 0x7fffffffLL / per_seq;
+  if (Bz == 0 || n_dvec == 0) return cudaSuccess;
+  if (L > 0x7fffffffLL - TILE || D > 0x7fffffffLL) return cudaErrorInvalidValue;
+  constexpr int64_t kMaxYZ = 65535;  // grid y and z limits: larger shapes take several launches
   auto args = [&](auto kern) -> cudaError_t {
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kConvThreads, 0);
-    if (e != cudaSuccess) return e;
-    const int64_t cap = int64_t(sm_count()) * (per_sm > 0 ? per_sm : 1);
-    for (int64_t b0 = 0; b0 < Bz; b0 += seq_per_launch) {
-      const int64_t nb = (Bz - b0) < seq_per_launch ? (Bz - b0) : seq_per_launch;
-      const int64_t n_items = nb * per_seq;
-      const int64_t need = (n_items + kConvThreads - 1) / kConvThreads;
-      const int64_t blocks = need < cap ? need : cap;
+    const unsigned gx = unsigned((n_dvec + kConvThreads - 1) / kConvThreads);
+    for (int64_t b0 = 0; b0 < Bz; b0 += kMaxYZ) {
+      const int64_t nb = (Bz - b0) < kMaxYZ ? (Bz - b0) : kMaxYZ;
       const TX* xb = static_cast<const TX*>(x) + b0 * L * D;
       const TX* sib = s_in ? static_cast<const TX*>(s_in) + b0 * D * (K - 1) : nullptr;
       TX* sob = s_out ? static_cast<TX*>(s_out) + b0 * D * (K - 1) : nullptr;
       TU* ub = static_cast<TU*>(u) + b0 * L * D;
-      kern<<<unsigned(blocks), kConvThreads, 0, st>>>(xb, w, bias, sib, sob, ub, int(L), int(D),
-                                                      K, int(n_dvec), int(n_tiles), int(n_items));
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
+      for (int64_t tb = 0; tb < n_tiles; tb += kMaxYZ) {
+        const int64_t ny = (n_tiles - tb) < kMaxYZ ? (n_tiles - tb) : kMaxYZ;
+        kern<<<dim3(gx, unsigned(ny), unsigned(nb)), kConvThreads, 0, st>>>(
+            xb, w, bias, sib, sob, ub, int(L), int(D), K, int(n_dvec), int(tb));
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+      }
     }
     return cudaSuccess;
   };
