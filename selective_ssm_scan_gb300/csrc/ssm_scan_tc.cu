@@ -72,8 +72,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColG = 0;     // C B^T                          [t][s] 128
 constexpr uint32_t kColGh = 128;  // hi(G o mask), bf16 pairs              64
 constexpr uint32_t kColGl = 192;  // lo(G o mask), bf16 pairs              64
-constexpr uint32_t kColYd = 256;  // hi(G o mask)(x'hi + x'lo) + lo x'hi  [t][p]  64
-constexpr uint32_t kColH = 320;   // the state h (consumers), fp32      [n][p]  64
+constexpr uint32_t kColYd = 256;  // hi(G o mask)(x'hi | x'lo) + lo x'hi [t][128]
 constexpr uint32_t kColYo = 384;  // C (h_hi + h_lo)^T                [t][p]  64
 constexpr uint32_t kColS = 448;   // B^T (x'hi + x'lo)                [n][p]  64
 // shared memory (bytes from a 1024-byte aligned base)
@@ -113,7 +112,8 @@ enum {
 constexpr uint32_t kIdG = idesc_bf16(128, 128, 0, 0);     // C (K-major) x B (K-major)
 constexpr uint32_t kIdS = idesc_bf16(128, 64, 1, 1);      // B^T (MN-major) x x' (MN-major)
 constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);     // C (K-major) x h (MN-major)
-constexpr uint32_t kIdYd = idesc_bf16(128, 64, 0, 1);     // (G o mask) part (TMEM) x x' part (MN-major)
+constexpr uint32_t kIdYd = idesc_bf16(128, 128, 0, 1);    // hi(G o mask) (TMEM) x x'hi|lo (MN-major)
+constexpr uint32_t kIdYdLo = idesc_bf16(128, 64, 0, 1);   // lo(G o mask) (TMEM) x x'hi
 
 __device__ __forceinline__ uint16_t bf16_bits(float v) {
   return __bfloat16_as_ushort(__float2bfloat16_rn(v));
@@ -144,19 +144,6 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
 }
 
 // Row `r` (64 fp32 values) -> hi and lo bf16 rows of two MN-major tiles.
-// Columns [32 q2, 32 q2 + 32) of row r (v holds those 32 values).
-__device__ __forceinline__ void write_split_half(uint8_t* hi_tile, uint8_t* lo_tile, int r, int q2,
-                                                 const uint32_t (&v)[32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      split2(__uint_as_float(v[8 * c + 2 * k]), __uint_as_float(v[8 * c + 2 * k + 1]), hw[k], lw[k]);
-    *reinterpret_cast<uint4*>(hi_tile + sw128(r, 4 * q2 + c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(lo_tile + sw128(r, 4 * q2 + c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
-}
 __device__ __forceinline__ void write_split_row(uint8_t* hi_tile, uint8_t* lo_tile, int r,
                                                 const float* v) {
 #pragma unroll
@@ -328,17 +315,12 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
     // on abort every loop below keeps running its named barriers with the
     // work skipped, so no thread is ever left waiting at one
     bool ok = true;
-    // dt of token t0 + s (warps 0-3), loaded one chunk ahead and kept raw so
-    // that nothing waits for it until the prefix uses it
-    const __nv_bfloat16* dts = dt + (int64_t(b) * L + s) * H + h;
-    __nv_bfloat16 dt_next = __float2bfloat16_rn(0.0f);
-    if (warp < 4 && s < L) dt_next = dts[0];
     for (int c = 0; c < nC; ++c) {
       const int t0 = c * kQ;
       const int valid = min(kQ, L - t0);
-      const __nv_bfloat16 dt_cur = dt_next;
-      if (warp < 4 && t0 + kQ + s < L) dt_next = dts[int64_t(t0 + kQ) * H];
-      const float ell = ok && s < valid && warp < 4 ? __bfloat162float(dt_cur) * Ah : 0.0f;
+      const float ell = ok && s < valid && warp < 4
+                            ? __bfloat162float(dt[(int64_t(b) * L + t0 + s) * H + h]) * Ah
+                            : 0.0f;
       float u[NT][8];  // [token j][channel e]
       const int tb = t0 + NT * g4;  // first token of the group
       const int nv = ok ? min(NT, max(0, valid - NT * g4)) : 0;  // live tokens
@@ -516,17 +498,11 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
     const int wq = warp - kConsWarp0;  // == warp % 4, the TMEM lane quarter
     const int r = 32 * wq + lane;
     const uint32_t tl = tm + (uint32_t(wq * 32) << 16);
-    // the state row n = r lives in TMEM columns kColH.. (fp32) between chunks
+    float hreg[kP];
     const int64_t hoff = (int64_t(b) * H + h) * kP * kN;
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2) {
-      uint32_t hv[32];
-#pragma unroll
-      for (int p = 0; p < 32; ++p)
-        hv[p] = __float_as_uint(h0 ? h0[hoff + int64_t(32 * q2 + p) * kN + r] : 0.0f);
-      write_split_half(sm + kOffH, sm + kOffH + 16384, r, q2, hv);
-      tmem_st_x32(tl + kColH + 32u * q2, hv);
-    }
+    for (int p = 0; p < kP; ++p) hreg[p] = h0 ? h0[hoff + int64_t(p) * kN + r] : 0.0f;
+    write_split_row(sm + kOffH, sm + kOffH + 16384, r, hreg);
     fence_proxy_async_smem();
     mbar_arrive(ctl.bar(BAR_H_FULL));
     {  // blocks of G o M above the diagonal of this warp's rows stay zero
@@ -561,48 +537,34 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
         tc_fence_after();
-        // one 16-column piece: G -> G o mask -> hi, lo bf16 pairs
-        auto piece = [&](uint32_t (&graw)[16], int j, int hf) {
-          const int s0 = 32 * j + 16 * hf;
-          uint32_t ph[8], pl[8];
-          float m[16];
-          if (fac) {  // the decay lives in x' and the row scale f_t
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(graw[i]);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float4 l4 = *reinterpret_cast<const float4*>(lam + s0 + 4 * i);
-              m[4 * i] = __uint_as_float(graw[4 * i]) * __expf(lam_t - l4.x);
-              m[4 * i + 1] = __uint_as_float(graw[4 * i + 1]) * __expf(lam_t - l4.y);
-              m[4 * i + 2] = __uint_as_float(graw[4 * i + 2]) * __expf(lam_t - l4.z);
-              m[4 * i + 3] = __uint_as_float(graw[4 * i + 3]) * __expf(lam_t - l4.w);
-            }
-          }
-          if (j == wq) {  // diagonal block: s = s0 + i <= t = 32 wq + lane
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
-          }
-#pragma unroll
-          for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[i], pl[i]);
-          tmem_st_x8(tl + kColGh + uint32_t(s0 / 2), ph);
-          tmem_st_x8(tl + kColGl + uint32_t(s0 / 2), pl);
-        };
-        // the load of the next piece is in flight while this one is split
-        uint32_t ga[16], gb[16];
-        tmem_ld_x16_nowait(tl + kColG, ga);
-        tmem_ld_wait();
-        reg_fence16(ga);
         for (int j = 0; j <= wq; ++j) {
-          tmem_ld_x16_nowait(tl + kColG + uint32_t(32 * j + 16), gb);
-          piece(ga, j, 0);
-          tmem_ld_wait();
-          reg_fence16(gb);
-          if (j < wq) tmem_ld_x16_nowait(tl + kColG + uint32_t(32 * j + 32), ga);
-          piece(gb, j, 1);
-          if (j < wq) {
-            tmem_ld_wait();
-            reg_fence16(ga);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int s0 = 32 * j + 16 * hf;
+            uint32_t graw[16], ph[8], pl[8];
+            tmem_ld_x16(tl + kColG + uint32_t(s0), graw);
+            float m[16];
+            if (fac) {  // the decay lives in x' and the row scale f_t
+#pragma unroll
+              for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(graw[i]);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float4 l4 = *reinterpret_cast<const float4*>(lam + s0 + 4 * i);
+                m[4 * i] = __uint_as_float(graw[4 * i]) * __expf(lam_t - l4.x);
+                m[4 * i + 1] = __uint_as_float(graw[4 * i + 1]) * __expf(lam_t - l4.y);
+                m[4 * i + 2] = __uint_as_float(graw[4 * i + 2]) * __expf(lam_t - l4.z);
+                m[4 * i + 3] = __uint_as_float(graw[4 * i + 3]) * __expf(lam_t - l4.w);
+              }
+            }
+            if (j == wq) {  // diagonal block: s = s0 + i <= t = 32 wq + lane
+#pragma unroll
+              for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[i], pl[i]);
+            tmem_st_x8(tl + kColGh + uint32_t(s0 / 2), ph);
+            tmem_st_x8(tl + kColGl + uint32_t(s0 / 2), pl);
           }
         }
         tmem_st_wait();
@@ -615,49 +577,23 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       if (ok) {
         tc_fence_after();
 #pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {  // h = exp(Lam_end) h + scale S', in TMEM
-          uint32_t s0[16], s1[16], hv[32];
-          uint32_t (&h0v)[16] = *reinterpret_cast<uint32_t (*)[16]>(hv);
-          uint32_t (&h1v)[16] = *reinterpret_cast<uint32_t (*)[16]>(hv + 16);
-          tmem_ld_x16_nowait(tl + kColS + 32u * q2, s0);
-          tmem_ld_x16_nowait(tl + kColS + 32u * q2 + 16u, s1);
-          tmem_ld_x16_nowait(tl + kColH + 32u * q2, h0v);
-          tmem_ld_x16_nowait(tl + kColH + 32u * q2 + 16u, h1v);
-          tmem_ld_wait();
-          reg_fence16(s0);
-          reg_fence16(s1);
-          reg_fence16(h0v);
-          reg_fence16(h1v);
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t r0[16];
+          tmem_ld_x16(tl + kColS + 16u * qq, r0);
 #pragma unroll
-          for (int p = 0; p < 16; ++p) {
-            hv[p] = __float_as_uint(fmaf(dec_end, __uint_as_float(hv[p]), s_scale * __uint_as_float(s0[p])));
-            hv[16 + p] =
-                __float_as_uint(fmaf(dec_end, __uint_as_float(hv[16 + p]), s_scale * __uint_as_float(s1[p])));
-          }
-          tmem_st_x32(tl + kColH + 32u * q2, hv);
+          for (int p = 0; p < 16; ++p)
+            hreg[16 * qq + p] = fmaf(dec_end, hreg[16 * qq + p], s_scale * __uint_as_float(r0[p]));
         }
-        tmem_st_wait();
         tc_fence_before();
         mbar_arrive(ctl.bar(BAR_S_FREE));
       }
       if (ok) ok = ctl.wait(BAR_YO_DONE, uint32_t(c & 1));  // Yo(c) has read h_{c-1}
       if (ok) {
-#pragma unroll
-        for (int q2 = 0; q2 < 2; ++q2) {
-          uint32_t hv[32];
-          uint32_t (&h0v)[16] = *reinterpret_cast<uint32_t (*)[16]>(hv);
-          uint32_t (&h1v)[16] = *reinterpret_cast<uint32_t (*)[16]>(hv + 16);
-          tmem_ld_x16_nowait(tl + kColH + 32u * q2, h0v);
-          tmem_ld_x16_nowait(tl + kColH + 32u * q2 + 16u, h1v);
-          tmem_ld_wait();
-          reg_fence16(h0v);
-          reg_fence16(h1v);
-          write_split_half(sm + kOffH, sm + kOffH + 16384, r, q2, hv);
-        }
+        write_split_row(sm + kOffH, sm + kOffH + 16384, r, hreg);
         fence_proxy_async_smem();
         mbar_arrive(ctl.bar(BAR_H_FULL));
       }
-      // ---- y rows: y_t = f_t Yd'_t + exp(Lam_t) Yo_t ------------------------
+      // ---- y rows ------------------------------------------------------------
       if (ok) ok = ctl.wait(BAR_Y_FULL, uint32_t(c & 1));
       ok = __all_sync(0xffffffffu, ok);
       if (ok) {
@@ -665,39 +601,31 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         TY* yrow = y + (int64_t(b) * L + t0 + r) * D + int64_t(h) * kP;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-          uint32_t a[2][16];
-          tmem_ld_x16_nowait(tl + kColYd + 16u * qq, a[0]);
-          tmem_ld_x16_nowait(tl + kColYo + 16u * qq, a[1]);
-          tmem_ld_wait();
-          reg_fence16(a[0]);
-          reg_fence16(a[1]);
-          if (qq == 3) {
-            tc_fence_before();
-            mbar_arrive(ctl.bar(BAR_ACC_FREE));  // Yd and Yo are in registers
-          }
           float yv[16];
+          {
+            uint32_t a0[16], a1[16];
+            tmem_ld_x16(tl + kColYd + 16u * qq, a0);
+            tmem_ld_x16(tl + kColYd + 64u + 16u * qq, a1);
 #pragma unroll
-          for (int p = 0; p < 16; ++p)
-            yv[p] = fmaf(dec_t, __uint_as_float(a[1][p]), f_t * __uint_as_float(a[0][p]));
+            for (int p = 0; p < 16; ++p) yv[p] = f_t * (__uint_as_float(a0[p]) + __uint_as_float(a1[p]));
+          }
+          {
+            uint32_t a0[16];
+            tmem_ld_x16(tl + kColYo + 16u * qq, a0);
+            if (qq == 3) {
+              tc_fence_before();
+              mbar_arrive(ctl.bar(BAR_ACC_FREE));
+            }
+#pragma unroll
+            for (int p = 0; p < 16; ++p) yv[p] = fmaf(dec_t, __uint_as_float(a0[p]), yv[p]);
+          }
           if (r < valid) store_row16<TY>(yrow + 16 * qq, yv);
         }
       }
     }
     if (ok && hT) {
-      tc_fence_after();
 #pragma unroll
-      for (int q2 = 0; q2 < 2; ++q2) {
-        uint32_t hv[32];
-        uint32_t (&h0v)[16] = *reinterpret_cast<uint32_t (*)[16]>(hv);
-        uint32_t (&h1v)[16] = *reinterpret_cast<uint32_t (*)[16]>(hv + 16);
-        tmem_ld_x16_nowait(tl + kColH + 32u * q2, h0v);
-        tmem_ld_x16_nowait(tl + kColH + 32u * q2 + 16u, h1v);
-        tmem_ld_wait();
-        reg_fence16(h0v);
-        reg_fence16(h1v);
-#pragma unroll
-        for (int p = 0; p < 32; ++p) hT[hoff + int64_t(32 * q2 + p) * kN + r] = __uint_as_float(hv[p]);
-      }
+      for (int p = 0; p < kP; ++p) hT[hoff + int64_t(p) * kN + r] = hreg[p];
     }
   } else {
    if (lane == 0) {
@@ -760,17 +688,13 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
         tma_chunk(c + 1);
         tma_issued = c + 2;
       }
-      // Yd' = hi(G o mask) x'hi + hi(G o mask) x'lo + lo(G o mask) x'hi, all
-      // three accumulated in one 64-column accumulator
+      // Yd' = hi(G o mask)(x'hi | x'lo) + lo(G o mask) x'hi
       if (!ctl.wait(BAR_GM_FULL, uint32_t(c & 1))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(uh, kk), kIdYd, kk);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(uh + 16384, kk), kIdYd, 1);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, mndesc(uh, kk), kIdYd, 1);
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, mndesc(uh, kk), kIdYdLo, 1);
       mma_commit(ctl.bar(BAR_Y_FULL));
       mma_commit(ctl.bar(BAR_U_FREE + st));
     }
