@@ -274,6 +274,9 @@ def main():
         for _ in range(steps):
             reset()
             flush.zero_()
+            # keep the GPU busy ~100 us while the host enqueues the whole step,
+            # so that no launch in the timed region waits for the host
+            torch.cuda._sleep(200_000)
             evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
             fn(evs)
             all_evs.append(evs)
@@ -462,6 +465,7 @@ def bench_decode(torch, sss, dev, stream, flush, args, hbm):
     evs = []
     for _ in range(max(3, args.steps // 10)):
         flush.zero_()
+        torch.cuda._sleep(200_000)  # the host enqueues the call meanwhile
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
