@@ -371,17 +371,37 @@ def main():
     d2h = sum(t.numel() * t.element_size() for t in hy) + hS.numel() * hS.element_size() + \
         hh.numel() * hh.element_size()
 
-    def e2e_step():
-        for (i, k), t in host.items():
-            dseg[i][k].copy_(t, non_blocking=True)
-        S.copy_(hS0, non_blocking=True)
-        h.copy_(hh0, non_blocking=True)
+    # Copies in on one stream and out on another, compute on the main stream:
+    # segment i+1's inputs go up while segment i computes, and y(i) comes down
+    # while segment i+1 computes.  Events order each step's work after e0 and
+    # before e1, both recorded on the main stream.
+    s_in = torch.cuda.Stream(device=dev)
+    s_out = torch.cuda.Stream(device=dev)
+
+    def e2e_step(e0=None):
+        landed = [torch.cuda.Event() for _ in dseg]
+        done = [torch.cuda.Event() for _ in dseg]
+        if e0 is not None:
+            s_in.wait_event(e0)
+        with torch.cuda.stream(s_in):
+            S.copy_(hS0, non_blocking=True)
+            h.copy_(hh0, non_blocking=True)
+            for i in range(n_seg):
+                for k in dseg[i]:
+                    dseg[i][k].copy_(host[(i, k)], non_blocking=True)
+                landed[i].record(s_in)
         for i, sg in enumerate(dseg):
+            stream.wait_event(landed[i])
             sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
-                          conv_state_out=S, hT=h, y=ys[i], fused=True)
-            hy[i].copy_(ys[i], non_blocking=True)
-        hS.copy_(S, non_blocking=True)
-        hh.copy_(h, non_blocking=True)
+                          conv_state_out=S, hT=h, y=ys[i], fused=True, stream=stream)
+            done[i].record(stream)
+            s_out.wait_event(done[i])
+            with torch.cuda.stream(s_out):
+                hy[i].copy_(ys[i], non_blocking=True)
+        with torch.cuda.stream(s_out):
+            hS.copy_(S, non_blocking=True)
+            hh.copy_(h, non_blocking=True)
+        stream.wait_stream(s_out)
 
     for _ in range(3):
         e2e_step()
@@ -390,10 +410,11 @@ def main():
     e2e_steps = max(3, args.steps // 10)
     for _ in range(e2e_steps):
         flush.zero_()
+        torch.cuda._sleep(200_000)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        e2e_step()
+        e2e_step(e0)
         e1.record(stream)
         stream.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
