@@ -19,6 +19,9 @@ ssm_scan(u, dt, A, B, C, h0) -> (y, hT)
     Scalar-decay recurrence h_t = exp(dt_t A_h) h_{t-1} + x_t B_t^T,
     y_t = h_t C_t ("Understanding and Improving Length Generalization in
     Recurrent Models", Eq. (1), from a non-zero h_{-1} as in Eq. (4)).
+conv_state_bwd(x, w, bias, S, dy, dF, apply_silu=True) -> (dx, dS, dw, dbias)
+    Its gradient with state (same chapter, section on the backward pass
+    with state).
 mixer_update(...) -> (y, conv_pool', ssm_pool', n_skipped)
     Single/multi-token update over a circular conv-state pool (same chapter,
     sections on the single-token update, circular mode and continuous
@@ -67,14 +70,16 @@ def lib():
             l = ctypes.CDLL(build())
             l.orc_conv_state_fwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _L, _L, _L,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int]
+            l.orc_conv_state_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                             _L, _L, _L, ctypes.c_int, ctypes.c_int, ctypes.c_int]
             l.orc_ssm_scan.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _L, _L, _L,
                                        _L, _L, _L, ctypes.c_int]
             l.orc_mixer_update.argtypes = [_dp, _dp, _dp, _dp, _L, _L, _ip, _ip, _dp, _dp,
                                            _dp, _dp, _dp, _dp, _L, _L, _L, _L, _L, _L,
                                            ctypes.c_int, ctypes.c_int]
             l.orc_num_threads.argtypes = [ctypes.c_int]
-            for f in (l.orc_conv_state_fwd, l.orc_ssm_scan, l.orc_mixer_update,
-                      l.orc_num_threads):
+            for f in (l.orc_conv_state_fwd, l.orc_conv_state_bwd, l.orc_ssm_scan,
+                      l.orc_mixer_update, l.orc_num_threads):
                 f.restype = ctypes.c_int
             _lib = l
     return _lib
@@ -112,6 +117,26 @@ def conv_state_fwd(x, w, bias=None, S=None, apply_silu: bool = True, nthreads: i
     if rc != 0:
         raise ValueError("orc_conv_state_fwd: bad sizes")
     return u, F
+
+
+def conv_state_bwd(x, w, bias, S, dy, dF=None, apply_silu: bool = True, nthreads: int = 0):
+    """Gradient of conv_state_fwd: x [Bz, L, D], w [D, K], bias [D] | None,
+    S [Bz, D, K-1] | None, dy = dL/du [Bz, L, D], dF = dL/dF [Bz, D, K-1] | None.
+
+    Returns dx [Bz, L, D], dS [Bz, D, K-1], dw [D, K], dbias [D] (float64)."""
+    x, w, bias, S, dy, dF = (_f64(a) for a in (x, w, bias, S, dy, dF))
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    dx = np.empty((Bz, L, D))
+    dS = np.empty((Bz, D, K - 1))
+    dw = np.empty((D, K))
+    db = np.empty(D)
+    rc = lib().orc_conv_state_bwd(_ptr(x), _ptr(w), _ptr(bias), _ptr(S), _ptr(dy), _ptr(dF),
+                                  _ptr(dx), _ptr(dS), _ptr(dw), _ptr(db), Bz, L, D, K,
+                                  int(bool(apply_silu)), nthreads)
+    if rc != 0:
+        raise ValueError("orc_conv_state_bwd: bad sizes")
+    return dx, dS, dw, db
 
 
 def ssm_scan(u, dt, A, B, C, h0=None, nthreads: int = 0):

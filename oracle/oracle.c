@@ -16,6 +16,13 @@
  *                       sequence"):  u = [S_0..S_{K-2}, x_0..x_{L-1}],
  *                       z_t = beta + sum_k w_k u_{t+k},  F = u[L : L+K-1],
  *                       output SiLU(z) = z / (1 + exp(-z)).
+ *   orc_conv_state_bwd  its gradient with state, as derived in the same
+ *                       chapter (section "unified derivation of the backward
+ *                       pass with state"): with delta_t = dL/dz_t and
+ *                       q = dL/dF, dL/du_j = sum_{t,k: t+k=j} delta_t w_k
+ *                       + [L <= j < L+K-1] q_{j-L}, dS = du[0 : K-1],
+ *                       dx = du[K-1 : K-1+L], dw_k = sum_t delta_t u_{t+k},
+ *                       dbeta = sum_t delta_t (summed over the batch too).
  *   orc_ssm_scan        the linear recurrence of "Understanding and Improving
  *                       Length Generalization in Recurrent Models" section 2
  *                       Eq. (1), h_t = A_t h_{t-1} + B_t x_t, y_t = C_t^T h_t,
@@ -133,6 +140,77 @@ int orc_conv_state_fwd(const double* x, const double* w, const double* bias,
   if (Bz < 0 || L < 0 || D < 0 || K < 1) return -1;
   conv_ctx c = {x, w, bias, S, u, F, Bz, L, D, K, apply_silu};
   parallel_for(Bz * D, nthreads, conv_item, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* its gradient with state                                                  */
+/* ------------------------------------------------------------------------ */
+
+/* d/dz of z / (1 + exp(-z)) = s (1 + z (1 - s)) with s the logistic function */
+static double dsilu(double z) {
+  const double s = 1.0 / (1.0 + exp(-z));
+  return s * (1.0 + z * (1.0 - s));
+}
+
+typedef struct {
+  const double *x, *w, *bias, *S, *dy, *q;
+  double *dx, *dS, *dw, *dbias;
+  long Bz, L, D;
+  int K, act;
+} convb_ctx;
+
+/* one channel d, every sequence of the batch in order (dw and dbeta sum
+   over the batch, so one thread owns the channel) */
+static void convb_item(void* p, long d) {
+  convb_ctx* c = (convb_ctx*)p;
+  const int K = c->K;
+  const long L = c->L, D = c->D, E = L + K - 1;
+  double* ext = (double*)malloc(sizeof(double) * (size_t)(E > 0 ? E : 1));
+  double* du = (double*)malloc(sizeof(double) * (size_t)(E > 0 ? E : 1));
+  double* delta = (double*)malloc(sizeof(double) * (size_t)(L > 0 ? L : 1));
+  const double beta = c->bias ? c->bias[d] : 0.0;
+  double dbeta = 0.0;
+  for (int k = 0; k < K; ++k) c->dw[d * K + k] = 0.0;
+  for (long b = 0; b < c->Bz; ++b) {
+    /* forward again: the extended sequence and z_t */
+    for (int j = 0; j < K - 1; ++j)
+      ext[j] = c->S ? c->S[(b * D + d) * (K - 1) + j] : 0.0;
+    for (long t = 0; t < L; ++t) ext[K - 1 + t] = c->x[(b * L + t) * D + d];
+    for (long t = 0; t < L; ++t) {
+      double z = beta;
+      for (int k = 0; k < K; ++k) z += c->w[d * K + k] * ext[t + k];
+      const double g = c->dy[(b * L + t) * D + d];
+      delta[t] = c->act ? g * dsilu(z) : g;
+    }
+    /* dL/du: the convolution term, then the direct path of the tail slice */
+    for (long j = 0; j < E; ++j) du[j] = 0.0;
+    for (long t = 0; t < L; ++t)
+      for (int k = 0; k < K; ++k) du[t + k] += delta[t] * c->w[d * K + k];
+    for (int r = 0; r < K - 1; ++r)
+      du[L + r] += c->q ? c->q[(b * D + d) * (K - 1) + r] : 0.0;
+    for (int j = 0; j < K - 1; ++j) c->dS[(b * D + d) * (K - 1) + j] = du[j];
+    for (long t = 0; t < L; ++t) c->dx[(b * L + t) * D + d] = du[K - 1 + t];
+    for (int k = 0; k < K; ++k) {
+      double acc = 0.0;
+      for (long t = 0; t < L; ++t) acc += delta[t] * ext[t + k];
+      c->dw[d * K + k] += acc;
+    }
+    for (long t = 0; t < L; ++t) dbeta += delta[t];
+  }
+  if (c->dbias) c->dbias[d] = dbeta;
+  free(ext);
+  free(du);
+  free(delta);
+}
+
+int orc_conv_state_bwd(const double* x, const double* w, const double* bias,
+                       const double* S, const double* dy, const double* q, double* dx,
+                       double* dS, double* dw, double* dbias, long Bz, long L, long D, int K,
+                       int apply_silu, int nthreads) {
+  if (Bz < 0 || L < 0 || D < 0 || K < 1) return -1;
+  convb_ctx c = {x, w, bias, S, dy, q, dx, dS, dw, dbias, Bz, L, D, K, apply_silu};
+  parallel_for(D, nthreads, convb_item, &c);
   return 0;
 }
 

@@ -365,3 +365,88 @@ def test_update_does_not_depend_on_thread_count():
     r8 = oracle.mixer_update(nthreads=8, **c)
     for a, b in zip(r1[:3], r8[:3]):
         np.testing.assert_array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# conv backward with state
+# ---------------------------------------------------------------------------
+
+def test_conv_bwd_worked_example_k3(golden_dir):
+    """The page's single-token check: dS = [w0 d, w1 d + q0], dx = [w2 d + q1]."""
+    ex = json.load(open(os.path.join(golden_dir, "conv_state_examples.json")))["backward_examples"][0]
+    K = ex["K"]
+    x = np.array(ex["x"]).reshape(1, 1, 1)
+    S = np.array(ex["S"]).reshape(1, 1, K - 1)
+    w = np.array(ex["w"]).reshape(1, K)
+    dy = np.array([ex["delta"]]).reshape(1, 1, 1)
+    q = np.array(ex["q"]).reshape(1, 1, K - 1)
+    dx, dS, dw, db = oracle.conv_state_bwd(x, w, np.array([ex["bias"]]), S, dy, q, apply_silu=False)
+    assert dS.ravel().tolist() == ex["dS"]
+    assert dx.ravel().tolist() == ex["dx"]
+    assert dw.ravel().tolist() == ex["dw"]
+    assert db.ravel().tolist() == [ex["dbias"]]
+
+
+def _conv_loss(x, w, bias, S, dy, q, silu):
+    u, F = oracle.conv_state_fwd(x, w, bias, S, silu)
+    return float((u * dy).sum() + (F * q).sum())
+
+
+@pytest.mark.parametrize("K,L,silu", [(4, 6, True), (4, 2, True), (3, 5, False), (2, 1, True)])
+def test_conv_bwd_matches_finite_differences(K, L, silu):
+    """Central differences of the forward oracle (a loss linear in u and F)."""
+    r = np.random.default_rng(7 + K + L)
+    Bz, D = 2, 3
+    x = r.standard_normal((Bz, L, D))
+    w = r.standard_normal((D, K))
+    bias = r.standard_normal(D)
+    S = r.standard_normal((Bz, D, K - 1))
+    dy = r.standard_normal((Bz, L, D))
+    q = r.standard_normal((Bz, D, K - 1))
+    dx, dS, dw, db = oracle.conv_state_bwd(x, w, bias, S, dy, q, apply_silu=silu)
+    eps = 1e-6
+    for name, arr, grad in (("x", x, dx), ("S", S, dS), ("w", w, dw), ("bias", bias, db)):
+        num = np.empty_like(arr)
+        for idx in np.ndindex(arr.shape):
+            keep = arr[idx]
+            arr[idx] = keep + eps
+            lp = _conv_loss(x, w, bias, S, dy, q, silu)
+            arr[idx] = keep - eps
+            lm = _conv_loss(x, w, bias, S, dy, q, silu)
+            arr[idx] = keep
+            num[idx] = (lp - lm) / (2 * eps)
+        np.testing.assert_allclose(grad, num, rtol=1e-6, atol=1e-7, err_msg=name)
+
+
+@pytest.mark.parametrize("split", [1, 2, 5])
+def test_conv_bwd_chunked_equals_whole(split):
+    """Segments A then B with S_B = F_A: B's dS is A's dF (the chunked-training
+    section), and the pieces reassemble the whole sequence's gradient."""
+    r = np.random.default_rng(11 + split)
+    Bz, L, D, K = 2, 7, 3, 4
+    x = r.standard_normal((Bz, L, D))
+    w = r.standard_normal((D, K))
+    bias = r.standard_normal(D)
+    S = r.standard_normal((Bz, D, K - 1))
+    dy = r.standard_normal((Bz, L, D))
+    q = r.standard_normal((Bz, D, K - 1))
+    dx, dS, dw, db = oracle.conv_state_bwd(x, w, bias, S, dy, q)
+    xa, xb = x[:, :split], x[:, split:]
+    _, FA = oracle.conv_state_fwd(xa, w, bias, S, True)
+    dxb, dSb, dwb, dbb = oracle.conv_state_bwd(xb, w, bias, FA, dy[:, split:], q)
+    dxa, dSa, dwa, dba = oracle.conv_state_bwd(xa, w, bias, S, dy[:, :split], dSb)
+    np.testing.assert_allclose(np.concatenate([dxa, dxb], axis=1), dx, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dSa, dS, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dwa + dwb, dw, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dba + dbb, db, rtol=1e-12, atol=1e-12)
+
+
+def test_conv_bwd_empty_sequence_passes_the_state_gradient():
+    """L = 0: F = S, so dS = dF and no weight gradient."""
+    r = np.random.default_rng(3)
+    S = r.standard_normal((2, 3, 3))
+    q = r.standard_normal((2, 3, 3))
+    dx, dS, dw, db = oracle.conv_state_bwd(np.zeros((2, 0, 3)), r.standard_normal((3, 4)),
+                                           np.zeros(3), S, np.zeros((2, 0, 3)), q)
+    np.testing.assert_array_equal(dS, q)
+    assert not dw.any() and not db.any() and dx.shape == (2, 0, 3)
