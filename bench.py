@@ -425,6 +425,9 @@ def main():
         e2e_total = float(t.item())
     e2e_value = world * tokens_per_step * e2e_steps / (e2e_total * 1e-3)
 
+    # ---- conv backward with state on one segment, same rules ---------------
+    conv_bwd = bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
+
     # ---- decode update (continuous batching), same rules -------------------
     decode = None
     if not args.no_decode:
@@ -440,6 +443,7 @@ def main():
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
+        "conv_bwd": conv_bwd,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -455,6 +459,57 @@ def main():
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
+    """sss_conv_state_bwd on one segment of the workload: bf16 x and state,
+    fp32 dy and dF, bf16 dx and dS, fp32 dw and dbias (two kernels: the
+    gradient pass and the fixed-order reduction of the weight partials)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    bf = torch.bfloat16
+    Bz, D, K = s.Bz, s.D, s.K
+    x = torch.randn((Bz, Lseg, D), generator=g, device=dev).to(bf)
+    S = torch.randn((Bz, D, K - 1), generator=g, device=dev).to(bf)
+    dy = torch.randn((Bz, Lseg, D), generator=g, device=dev)
+    q = torch.randn((Bz, D, K - 1), generator=g, device=dev)
+    w = torch.randn((D, K), generator=g, device=dev) * (0.5 ** 0.5)
+    bias = torch.full((D,), 0.1, device=dev)
+    dx = torch.empty((Bz, Lseg, D), dtype=bf, device=dev)
+    dS = torch.empty((Bz, D, K - 1), dtype=bf, device=dev)
+    dw = torch.empty((D, K), device=dev)
+    db = torch.empty((D,), device=dev)
+    ws = torch.empty(max(1, sss.conv_state_bwd_workspace_size(Bz, Lseg, D, K)),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        sss.conv_state_bwd(x, w, bias, S, dy, q, dx, dS, dw, db, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(max(3, args.steps // 10)):
+        flush.zero_()
+        torch.cuda._sleep(200_000)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        evs.append((e0, e1))
+    stream.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    n_el = Bz * Lseg * D
+    part = sss.conv_state_bwd_workspace_size(Bz, Lseg, D, K)
+    byts = (n_el * (2 + 4 + 2)                       # x, dy in; dx out
+            + Bz * D * (K - 1) * (2 + 4 + 2)         # S, dF in; dS out
+            + 2 * part                               # partials written, read back
+            + D * (K + 1) * 4 * 2)                   # w, bias in; dw, dbias out
+    return {"workload": f"one {Lseg}-token segment, Bz={Bz}, D={D}, K={K}",
+            "avg_call_ms": ms, "launches_per_call": 2, "algorithmic_bytes_per_call": byts,
+            "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
+            "tokens_per_s": Bz * Lseg / (ms * 1e-3)}
 
 
 def bench_decode(torch, sss, dev, stream, flush, args, hbm):

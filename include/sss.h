@@ -91,6 +91,47 @@ sss_status sss_conv_state_fwd(const void* x, sss_dtype x_dtype, const float* w,
                               int apply_silu, sss_stream_t stream);
 
 /*
+ * sss_conv_state_bwd -- gradient of sss_conv_state_fwd, state included.
+ *
+ * Source: "Chapter 7: state, chunking and incremental inference", section
+ * "unified derivation of the backward pass with state": with
+ * delta_t = dL/dz_t = dy_t SiLU'(z_t) (dy_t when apply_silu == 0) and
+ * q = dL/dF,
+ *     dL/du_j = sum_{t,k: t+k=j} delta_t w_k + [L <= j < L+K-1] q_{j-L},
+ *     dS = du[0 : K-1],  dx = du[K-1 : K-1+L],
+ *     dw_k = sum_{b,t} delta_t u_{t+k},  dbias = sum_{b,t} delta_t.
+ * The forward is recomputed from x, w, bias and state_in.  Chunked training:
+ * the dstate_in of segment B is the dstate_out of segment A (the same
+ * chapter, section on chunked training and truncated backpropagation).
+ *
+ *  x, w, bias, state_in   as in sss_conv_state_fwd (state_in NULL = zeros)
+ *  dy          [Bz, L, D]     dy_dtype, dL/d(output)
+ *  dstate_out  [Bz, D, K-1]   dy_dtype, dL/dF, NULL = zeros
+ *  dx          [Bz, L, D]     dx_dtype, written
+ *  dstate_in   [Bz, D, K-1]   dx_dtype, dL/dS, written; must not overlap
+ *                             dstate_out
+ *  dw, dbias   [D, K], [D]    float32, written (not accumulated); dbias may
+ *                             be NULL
+ *  workspace   device scratch of at least sss_conv_state_bwd_workspace_size
+ *              bytes (per-block partial sums of dw and dbias, reduced in a
+ *              fixed order: the result is deterministic); may be NULL when
+ *              that size is 0
+ * Returns SSS_ERR_INVALID_ARG for null required pointers, misalignment,
+ * overlapping dstate_in / dstate_out, a short workspace, bad sizes or an
+ * unknown dtype; SSS_ERR_UNSUPPORTED for K > 8.
+ */
+size_t sss_conv_state_bwd_workspace_size(int64_t Bz, int64_t L, int64_t D, int K);
+
+sss_status sss_conv_state_bwd(const void* x, sss_dtype x_dtype, const float* w,
+                              const float* bias, const void* state_in,
+                              const void* dy, sss_dtype dy_dtype,
+                              const void* dstate_out, void* dx, sss_dtype dx_dtype,
+                              void* dstate_in, float* dw, float* dbias,
+                              int64_t Bz, int64_t L, int64_t D, int K,
+                              int apply_silu, void* workspace,
+                              size_t workspace_bytes, sss_stream_t stream);
+
+/*
  * sss_ssm_scan_fwd -- scalar-decay selective scan from an initial state.
  *
  * Source: "Understanding and Improving Length Generalization in Recurrent

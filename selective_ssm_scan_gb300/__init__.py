@@ -8,7 +8,8 @@ calls are enqueued on torch's current stream.  Importing this module loads
 ``python selective_ssm_scan_gb300/build.py``); there is no fallback.
 
 Functions (same names as the C ABI in include/sss.h, minus the prefix):
-    conv_state_fwd, ssm_scan_fwd, ssm_scan_path, ssm_scan_workspace_size, mixer_update_path,
+    conv_state_fwd, conv_state_bwd, conv_state_bwd_workspace_size, ssm_scan_fwd,
+    ssm_scan_path, ssm_scan_workspace_size, mixer_update_path,
     mixer_update, device_status, version, status_string
 plus ``mixer_fwd`` (conv_state_fwd then ssm_scan_fwd: one segment of the
 streaming forward with both states passed) and ``library_path``.
@@ -49,6 +50,11 @@ _lib.sss_status_string.argtypes = [_i]
 _lib.sss_last_cuda_error.restype = ctypes.c_char_p
 _lib.sss_conv_state_fwd.restype = _i
 _lib.sss_conv_state_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _i, _i64, _i64, _i64, _i, _i, _p]
+_lib.sss_conv_state_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.sss_conv_state_bwd_workspace_size.argtypes = [_i64, _i64, _i64, _i]
+_lib.sss_conv_state_bwd.restype = _i
+_lib.sss_conv_state_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p,
+                                    _i64, _i64, _i64, _i, _i, _p, ctypes.c_size_t, _p]
 _lib.sss_ssm_scan_workspace_size.restype = ctypes.c_size_t
 _lib.sss_ssm_scan_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i]
 _lib.sss_mixer_update_path.restype = _i
@@ -134,6 +140,43 @@ def conv_state_fwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
                                  int(bool(apply_silu)), _stream(stream))
     _check("sss_conv_state_fwd", rc)
     return u
+
+
+def conv_state_bwd_workspace_size(Bz, L, D, K) -> int:
+    return int(_lib.sss_conv_state_bwd_workspace_size(Bz, L, D, K))
+
+
+def conv_state_bwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                   state_in: Optional[torch.Tensor], dy: torch.Tensor,
+                   dstate_out: Optional[torch.Tensor] = None, dx: Optional[torch.Tensor] = None,
+                   dstate_in: Optional[torch.Tensor] = None, dw: Optional[torch.Tensor] = None,
+                   dbias: Optional[torch.Tensor] = None, dx_dtype=None, apply_silu: bool = True,
+                   workspace: Optional[torch.Tensor] = None, stream=None):
+    """Gradient of conv_state_fwd.  dy = dL/du [Bz, L, D]; dstate_out = dL/dF
+    [Bz, D, K-1] (dy's dtype) or None.  Returns (dx [Bz, L, D], dstate_in
+    [Bz, D, K-1] (dx's dtype), dw [D, K] fp32, dbias [D] fp32)."""
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    dev = x.device
+    dx_dtype = dx_dtype or x.dtype
+    if dx is None:
+        dx = torch.empty((Bz, L, D), dtype=dx_dtype, device=dev)
+    if dstate_in is None:
+        dstate_in = torch.empty((Bz, D, K - 1), dtype=dx.dtype, device=dev)
+    if dw is None:
+        dw = torch.empty((D, K), dtype=torch.float32, device=dev)
+    if dbias is None:
+        dbias = torch.empty((D,), dtype=torch.float32, device=dev)
+    need = conv_state_bwd_workspace_size(Bz, L, D, K)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = _lib.sss_conv_state_bwd(_ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(state_in), _ptr(dy),
+                                 _dt(dy), _ptr(dstate_out), _ptr(dx), _dt(dx), _ptr(dstate_in),
+                                 _ptr(dw), _ptr(dbias), Bz, L, D, K, int(bool(apply_silu)),
+                                 _ptr(workspace), ws_bytes, _stream(stream))
+    _check("sss_conv_state_bwd", rc)
+    return dx, dstate_in, dw, dbias
 
 
 def ssm_scan_workspace_size(Bz, L, H, P, N, G, x_dtype, act_dtype) -> int:

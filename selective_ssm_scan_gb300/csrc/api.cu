@@ -33,6 +33,13 @@ cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias
                                 int* status, cudaStream_t st);
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
                                cudaStream_t st);
+cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
+                                  const void* s_in, const void* dy, sss_dtype dyt, const void* q,
+                                  void* dx, sss_dtype dxt, void* dS, float* dw, float* dbias,
+                                  int64_t Bz, int64_t L, int64_t D, int K, int silu_on,
+                                  void* ws, cudaStream_t st);
+size_t conv_state_bwd_workspace(int64_t Bz, int64_t L, int64_t D, int K);
+bool conv_state_bwd_supports(int K);
 bool mixer_update_supports(int P, int N, int K, int L_new);
 int mixer_update_path(sss_dtype at, int S_len, int L_new, int P, int N, int K);
 cudaError_t mixer_update_launch(const void* x, sss_dtype at, const float* w, const float* bias,
@@ -148,6 +155,47 @@ int sss_ssm_scan_path(int64_t Bz, int64_t L, int H, int P, int N, int G, sss_dty
   if (ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, L, H, P, N, G)) return 1;
   if (ssm_scan_simt_supports(P, N)) return 0;
   return -1;
+}
+
+size_t sss_conv_state_bwd_workspace_size(int64_t Bz, int64_t L, int64_t D, int K) {
+  return sss::conv_state_bwd_workspace(Bz, L, D, K);
+}
+
+static bool ranges_overlap(const void* a, const void* b, size_t bytes) {
+  if (!a || !b || bytes == 0) return false;
+  const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+  return pa < pb + bytes && pb < pa + bytes;
+}
+
+sss_status sss_conv_state_bwd(const void* x, sss_dtype x_dtype, const float* w,
+                              const float* bias, const void* state_in, const void* dy,
+                              sss_dtype dy_dtype, const void* dstate_out, void* dx,
+                              sss_dtype dx_dtype, void* dstate_in, float* dw, float* dbias,
+                              int64_t Bz, int64_t L, int64_t D, int K, int apply_silu,
+                              void* workspace, size_t workspace_bytes, sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(dy_dtype) || !dtype_ok(dx_dtype))
+    return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || D < 0 || K < 1) return SSS_ERR_INVALID_ARG;
+  if (!sss::conv_state_bwd_supports(K)) return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0 || D == 0) return SSS_OK;
+  const size_t xs = dtype_size(x_dtype), ys = dtype_size(dy_dtype), os = dtype_size(dx_dtype);
+  if (!w || !dw || !aligned(w, 4) || !aligned(dw, 4) || (bias && !aligned(bias, 4)) ||
+      (dbias && !aligned(dbias, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if (K > 1 && (!dstate_in || !aligned(dstate_in, os))) return SSS_ERR_INVALID_ARG;
+  if ((state_in && !aligned(state_in, xs)) || (dstate_out && !aligned(dstate_out, ys)))
+    return SSS_ERR_INVALID_ARG;
+  if (L > 0 && (!x || !dy || !dx || !aligned(x, xs) || !aligned(dy, ys) || !aligned(dx, os)))
+    return SSS_ERR_INVALID_ARG;
+  const size_t state_bytes = size_t(Bz) * size_t(D) * size_t(K - 1);
+  if (ranges_overlap(dstate_in, dstate_out, state_bytes * (os > ys ? os : ys)))
+    return SSS_ERR_INVALID_ARG;
+  const size_t need = sss::conv_state_bwd_workspace(Bz, L, D, K);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::conv_state_bwd_launch(
+      x, x_dtype, w, bias, state_in, dy, dy_dtype, dstate_out, dx, dx_dtype, dstate_in, dw,
+      dbias, Bz, L, D, K, apply_silu != 0, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, const float* A,

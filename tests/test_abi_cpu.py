@@ -86,3 +86,34 @@ def test_scan_path_selection(lib):
     lib.sss_ssm_scan_path.argtypes = [ctypes.c_int64, ctypes.c_int64] + [ctypes.c_int] * 7
     assert lib.sss_ssm_scan_path(1, 64, 2, 4, 8, 1, 0, 0, 0) == 0      # fp32 -> CUDA cores
     assert lib.sss_ssm_scan_path(1, 64, 2, 4, 1000, 1, 0, 0, 0) == -1  # N too large
+
+
+def test_conv_backward_host_checks(lib):
+    """Workspace size and argument checks of the conv backward (each case
+    returns before any launch)."""
+    i64 = ctypes.c_int64
+    ws = lib.sss_conv_state_bwd_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i64, i64, i64, ctypes.c_int]
+    # one row of D * (K+1) fp32 partial sums per sequence and 64-token group
+    assert ws(8, 1024, 2048, 4) == 8 * 16 * 2048 * 5 * 4
+    assert ws(2, 65, 10, 3) == 2 * 2 * 10 * 4 * 4
+    assert ws(2, 0, 10, 3) == 0
+    f = lib.sss_conv_state_bwd
+    f.restype = ctypes.c_int
+    P = ctypes.c_void_p
+    f.argtypes = [P, ctypes.c_int, P, P, P, P, ctypes.c_int, P, P, ctypes.c_int, P, P, P,
+                  i64, i64, i64, ctypes.c_int, ctypes.c_int, P, ctypes.c_size_t, P]
+    a = lambda k: ctypes.c_void_p(0x10000000 * k)  # aligned stand-ins, never dereferenced
+    args = lambda **kw: dict(dict(x=a(1), xt=1, w=a(2), b=a(3), s=a(4), dy=a(5), dyt=0, q=a(6),
+                                  dx=a(7), dxt=1, ds=a(8), dw=a(9), db=a(10), Bz=2, L=100, D=64,
+                                  K=4, silu=1, ws=a(11), wsb=ws(2, 100, 64, 4), st=None), **kw)
+    call = lambda d: f(*d.values())
+    assert call(args(K=9)) == 2                      # K > 8
+    assert call(args(K=0)) == 1                      # K < 1
+    assert call(args(dyt=5)) == 1                    # unknown dtype
+    assert call(args(wsb=16)) == 1                   # workspace too small
+    assert call(args(ws=None)) == 1                  # no workspace
+    assert call(args(ds=a(6))) == 1                  # dS would overwrite dF
+    assert call(args(dw=None)) == 1                  # no weight gradient buffer
+    assert call(args(Bz=0)) == 0                     # empty batch: nothing to do
