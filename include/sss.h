@@ -132,6 +132,50 @@ sss_status sss_conv_state_bwd(const void* x, sss_dtype x_dtype, const float* w,
                               size_t workspace_bytes, sss_stream_t stream);
 
 /*
+ * sss_conv_state_bwd_noalloc -- sss_conv_state_bwd without a caller-provided
+ * workspace, for callers that cannot allocate device memory.  The pages have
+ * no counterpart: this is a library convenience, not part of the method.
+ *
+ * Some callers can't call cudaMalloc (or any allocator) at the point where
+ * they run the backward: a plugin inside an inference or training engine
+ * whose execute step is not allowed to allocate, code that runs with a fixed
+ * device-memory budget handed to it by a host framework it has no allocator
+ * handle for, or a latency-critical loop that must not pay for cudaMalloc's
+ * implicit synchronisation.  This entry point takes the same arguments as
+ * sss_conv_state_bwd minus the workspace, computes the same dx, dstate_in,
+ * dw and dbias, and keeps its partial sums in one static device array of
+ * SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES bytes that belongs to the library.  It
+ * calls no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *  - Size limit: it serves calls whose sss_conv_state_bwd_workspace_size()
+ *    is at most SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES (8 MiB: for example
+ *    Bz = 8 sequences of 1024 tokens at D = 2048, K = 4, which need 5 MiB)
+ *    and returns SSS_ERR_UNSUPPORTED, before anything is launched, for
+ *    larger ones.  Other errors are those of sss_conv_state_bwd.
+ *  - Memory: every GPU that loads the library holds the 8 MiB array until
+ *    the process exits.
+ *  - Set-up: the first call on a device, with that device current, looks up
+ *    the array's device address (cudaGetSymbolAddress) and caches it; make
+ *    that first call before any stream capture begins.  A failed lookup
+ *    returns SSS_ERR_CUDA.
+ *  - Sharing: all calls on a device use the same array, and it keeps the
+ *    last call's partial sums.  Each call writes every partial it reads
+ *    before reading it, so nothing needs clearing between calls; but two
+ *    calls that can run at the same time on the GPU (different streams, no
+ *    ordering between them) race on the array and give wrong dw and dbias.
+ *    Serialise them, e.g. by issuing them on one stream.
+ */
+#define SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+sss_status sss_conv_state_bwd_noalloc(const void* x, sss_dtype x_dtype, const float* w,
+                                      const float* bias, const void* state_in,
+                                      const void* dy, sss_dtype dy_dtype,
+                                      const void* dstate_out, void* dx,
+                                      sss_dtype dx_dtype, void* dstate_in, float* dw,
+                                      float* dbias, int64_t Bz, int64_t L, int64_t D,
+                                      int K, int apply_silu, sss_stream_t stream);
+
+/*
  * sss_ssm_scan_fwd -- scalar-decay selective scan from an initial state.
  *
  * Source: "Understanding and Improving Length Generalization in Recurrent

@@ -8,7 +8,8 @@ calls are enqueued on torch's current stream.  Importing this module loads
 ``python selective_ssm_scan_gb300/build.py``); there is no fallback.
 
 Functions (same names as the C ABI in include/sss.h, minus the prefix):
-    conv_state_fwd, conv_state_bwd, conv_state_bwd_workspace_size, ssm_scan_fwd,
+    conv_state_fwd, conv_state_bwd, conv_state_bwd_workspace_size,
+    conv_state_bwd_noalloc, ssm_scan_fwd,
     ssm_scan_path, ssm_scan_workspace_size, mixer_update_path,
     mixer_update, device_status, version, status_string
 plus ``mixer_fwd`` (conv_state_fwd then ssm_scan_fwd: one segment of the
@@ -55,6 +56,9 @@ _lib.sss_conv_state_bwd_workspace_size.argtypes = [_i64, _i64, _i64, _i]
 _lib.sss_conv_state_bwd.restype = _i
 _lib.sss_conv_state_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p,
                                     _i64, _i64, _i64, _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_conv_state_bwd_noalloc.restype = _i
+_lib.sss_conv_state_bwd_noalloc.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _i, _p, _p, _p,
+                                            _i64, _i64, _i64, _i, _i, _p]
 _lib.sss_ssm_scan_workspace_size.restype = ctypes.c_size_t
 _lib.sss_ssm_scan_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i]
 _lib.sss_mixer_update_path.restype = _i
@@ -176,6 +180,33 @@ def conv_state_bwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
                                  _ptr(dw), _ptr(dbias), Bz, L, D, K, int(bool(apply_silu)),
                                  _ptr(workspace), ws_bytes, _stream(stream))
     _check("sss_conv_state_bwd", rc)
+    return dx, dstate_in, dw, dbias
+
+
+# Size of the library's static scratch behind conv_state_bwd_noalloc (the
+# SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES of the C header).
+CONV_BWD_NOALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def conv_state_bwd_noalloc(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                           state_in: Optional[torch.Tensor], dy: torch.Tensor,
+                           dstate_out: Optional[torch.Tensor], dx: torch.Tensor,
+                           dstate_in: torch.Tensor, dw: torch.Tensor,
+                           dbias: Optional[torch.Tensor] = None, apply_silu: bool = True,
+                           stream=None):
+    """conv_state_bwd for callers that cannot allocate device memory: every
+    output is passed in, and the partial sums go to the library's static
+    scratch of CONV_BWD_NOALLOC_SCRATCH_BYTES bytes (calls needing more raise
+    with SSS_ERR_UNSUPPORTED).  Calls that may run at the same time on the
+    GPU share that scratch and race; issue them on one stream.  Returns
+    (dx, dstate_in, dw, dbias)."""
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    rc = _lib.sss_conv_state_bwd_noalloc(_ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(state_in),
+                                         _ptr(dy), _dt(dy), _ptr(dstate_out), _ptr(dx), _dt(dx),
+                                         _ptr(dstate_in), _ptr(dw), _ptr(dbias), Bz, L, D, K,
+                                         int(bool(apply_silu)), _stream(stream))
+    _check("sss_conv_state_bwd_noalloc", rc)
     return dx, dstate_in, dw, dbias
 
 
