@@ -501,10 +501,8 @@ def bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
     stream.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
     n_el = Bz * Lseg * D
-    part = sss.conv_state_bwd_workspace_size(Bz, Lseg, D, K)
     byts = (n_el * (2 + 4 + 2)                       # x, dy in; dx out
             + Bz * D * (K - 1) * (2 + 4 + 2)         # S, dF in; dS out
-            + 2 * part                               # partials written, read back
             + D * (K + 1) * 4 * 2)                   # w, bias in; dw, dbias out
     return {"workload": f"one {Lseg}-token segment, Bz={Bz}, D={D}, K={K}",
             "avg_call_ms": ms, "launches_per_call": 2, "algorithmic_bytes_per_call": byts,

@@ -10,16 +10,19 @@
 //   dw_k = sum_t delta_t u_{t+k},  dbias = sum_t delta_t   (and over the batch).
 //
 // GB300 mapping (HBM-bound: read x and dy once, write dx once):
-//  * a CTA is 8 warps; warp w takes the token tile tg * 8 + w of kTile tokens,
-//    lane l the channel vector d0 = (blockIdx.x * 32 + l) * VEC, so each load
-//    of a token row is one contiguous line per warp;
-//  * a thread recomputes z for the tokens [t0, t0 + kTile + K - 1) from the
-//    x window [t0 - (K-1), t0 + kTile + K - 1) (the conv state in front of
-//    token 0), turns dy into delta there, and forms dx_t for its kTile
-//    tokens from delta_{t..t+K-1} (the correlation runs forward in time);
-//  * the tile holding token 0 writes dS, the tiles holding the last K-1
-//    tokens add q;
-//  * dw and dbias: each thread sums its tile, the CTA sums its 8 tiles in
+//  * a CTA is 8 warps; lane l takes the channel vector d0 = (blockIdx.x * 32
+//    + l) * VEC (one 128-byte line of bf16 x per warp and token), warp w the
+//    tile of TT tokens t0 = (blockIdx.y * 8 + w) * TT;
+//  * a thread walks its tile forward in time, j = t0 .. t0 + TT + MK - 2,
+//    with two register windows: the last MK inputs x_{j-MK+1..j} and the
+//    last MK values of delta.  At step j it forms z_j and delta_j, adds
+//    delta_j u_{j+k} to its dw_k, and finishes du for the token MK - 1
+//    behind (dx, or dS for the steps before token 0 in tile 0).  The MK - 1
+//    tokens after the tile are read again by the next tile (L2 hits);
+//  * loads are clamped into the sequence and masked, so they are issued
+//    without branches, one batch of 6 tokens ahead of their use (two CTAs
+//    of <= 128 registers a thread share an SM);
+//  * dw and dbias: each thread sums its tile, the CTA sums its 8 warps in
 //    shared memory and writes one row of partials to the workspace; a second
 //    kernel adds the rows in a fixed order, so the result is deterministic.
 #include "common.cuh"
@@ -28,9 +31,15 @@ namespace sss {
 
 namespace {
 constexpr int kBwdWarps = 8;
-constexpr int kBwdTile = 8;         // tokens per warp
+constexpr int kBwdTile = 64;        // tokens per warp
 constexpr int kBwdMaxK = 8;
 constexpr int kBwdCtaTokens = kBwdWarps * kBwdTile;
+constexpr int kBwdBatch = 6;        // tokens loaded ahead of their use
+
+template <typename T, int VEC>
+struct __align__(sizeof(T) * VEC) BwdPack {
+  T e[VEC];
+};
 
 __device__ __forceinline__ float dsilu(float z) {
   // d/dz [z s(z)] = s (1 + z (1 - s)), s = 1 / (1 + exp(-z))
@@ -39,17 +48,17 @@ __device__ __forceinline__ float dsilu(float z) {
 }
 }  // namespace
 
-template <typename TX, typename TD, typename TO, int VEC, int KT, bool SILU>
-__global__ void __launch_bounds__(kBwdWarps * 32)
+// MK: window capacity (the conv width when it is a compile-time constant,
+// else kBwdMaxK with the real K <= MK at run time).
+template <typename TX, typename TD, typename TO, int VEC, int MK, bool SILU>
+__global__ void __launch_bounds__(kBwdWarps * 32, 2)
 conv_state_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
                       const float* __restrict__ bias, const TX* __restrict__ s_in,
                       const TD* __restrict__ dy, const TD* __restrict__ q, TO* __restrict__ dx,
-                      TO* __restrict__ dS, float* __restrict__ part, int L, int D, int K_rt,
+                      TO* __restrict__ dS, float* __restrict__ part, int L, int D, int K,
                       int n_dvec, int n_groups) {
-  constexpr int MK = KT > 0 ? KT : kBwdMaxK;
-  constexpr int NW = kBwdTile + 2 * (MK - 1);  // x window: u indices
-  constexpr int NZ = kBwdTile + MK - 1;        // tokens whose z (delta) is needed
-  const int K = KT > 0 ? KT : K_rt;
+  constexpr int NIT = kBwdTile + MK - 1;            // steps of the walk
+  constexpr int NB = (NIT + kBwdBatch - 1) / kBwdBatch;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int dvec = blockIdx.x * 32 + lane;
   const int tg = blockIdx.y;
@@ -57,6 +66,7 @@ conv_state_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
   const int t0 = (tg * kBwdWarps + warp) * kBwdTile;
   const bool live = dvec < n_dvec && t0 < L;
   const int d0 = dvec * VEC;
+  const int KM1 = K - 1;
 
   float dwp[MK][VEC], dbp[VEC];
 #pragma unroll
@@ -67,99 +77,118 @@ conv_state_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
   }
 
   if (live) {
-    float wk[MK][VEC], bs[VEC];
+    // wz[i]: weight of window slot i (slot MK-1 = newest) in z_j;
+    // wd[i]: weight of delta slot i in du_{j-MK+1+KM1}; bs: bias
+    float wz[MK][VEC], wd[MK][VEC], bs[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) {
       bs[v] = bias ? bias[d0 + v] : 0.0f;
 #pragma unroll
-      for (int k = 0; k < MK; ++k) wk[k][v] = k < K ? w[(d0 + v) * K + k] : 0.0f;
+      for (int i = 0; i < MK; ++i) {
+        const int kz = i - (MK - K);   // tap of slot i in z
+        const int kd = KM1 - i;        // tap of slot i in du
+        wz[i][v] = kz >= 0 ? w[(d0 + v) * K + kz] : 0.0f;
+        wd[i][v] = (kd >= 0 && kd < K) ? w[(d0 + v) * K + kd] : 0.0f;
+      }
     }
-    // ext[i] = u_{t0 + i} = x_{t0 + i - (K-1)}, i in [0, NW); S in front of
-    // token 0, zero past the end
-    float ext[NW][VEC];
+    // x window before step 0: slot i >= 1 holds x_{t0-MK+i} (the conv state
+    // before token 0, zero before that); each step shifts the window down
+    // one slot and puts x_j in slot MK-1
+    float xw[MK][VEC], dl[MK][VEC];
 #pragma unroll
-    for (int i = 0; i < NW; ++i) {
-      const int tx = t0 + i - (K - 1);
+    for (int i = 0; i < MK; ++i) {
+      const int tx = t0 - MK + i;
 #pragma unroll
       for (int v = 0; v < VEC; ++v) {
         float val = 0.0f;
-        if (i < kBwdTile + 2 * (K - 1)) {
-          if (tx >= 0 && tx < L)
+        if (i >= 1) {
+          if (tx >= 0)
             val = to_f32(x[(b * L + tx) * D + d0 + v]);
-          else if (tx < 0 && s_in)
-            val = to_f32(s_in[(b * D + d0 + v) * (K - 1) + (K - 1) + tx]);
+          else if (tx >= -KM1 && s_in)
+            val = to_f32(s_in[(b * D + d0 + v) * KM1 + KM1 + tx]);
         }
-        ext[i][v] = val;
+        xw[i][v] = val;
+        dl[i][v] = 0.0f;  // delta before token t0: unused except (zero) before token 0
       }
     }
-    // delta_t for t = t0 + i, i in [0, NZ), zero for t >= L
-    float dl[NZ][VEC];
+    const TX* xb = x + b * L * D + d0;
+    const TD* gb = dy + b * L * D + d0;
+    using PX = BwdPack<TX, VEC>;
+    using PG = BwdPack<TD, VEC>;
+    // batch nb + 1 is loaded (still packed) while batch nb is computed
+    PX xn[kBwdBatch];
+    PG gn[kBwdBatch];
+    auto load_batch = [&](int nb) {
 #pragma unroll
-    for (int i = 0; i < NZ; ++i) {
-      const int t = t0 + i;
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) {
-        float dv = 0.0f;
-        if (i < kBwdTile + K - 1 && t < L) {
-          float z = bs[v];
-#pragma unroll
-          for (int k = 0; k < MK; ++k)
-            if (k < K) z = fmaf(wk[k][v], ext[i + k][v], z);
-          const float g = to_f32(dy[(b * L + t) * D + d0 + v]);
-          dv = SILU ? g * dsilu(z) : g;
-        }
-        dl[i][v] = dv;
+      for (int i = 0; i < kBwdBatch; ++i) {
+        const int j = t0 + nb * kBwdBatch + i;
+        const int64_t jc = j < L ? j : L - 1;  // clamped into the sequence, masked below
+        xn[i] = *reinterpret_cast<const PX*>(xb + jc * D);
+        gn[i] = *reinterpret_cast<const PG*>(gb + jc * D);
       }
-    }
-    // dx_t = sum_k w_k delta_{t+K-1-k} (+ q for the last K-1 tokens)
+    };
+    load_batch(0);
+#pragma unroll 1
+    for (int nb = 0; nb < NB; ++nb) {
+      PX xc[kBwdBatch];
+      PG gc[kBwdBatch];
 #pragma unroll
-    for (int i = 0; i < kBwdTile; ++i) {
-      const int t = t0 + i;
-      if (t < L) {
-        float o[VEC];
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-          float acc = 0.0f;
-#pragma unroll
-          for (int k = 0; k < MK; ++k)
-            if (k < K) acc = fmaf(wk[k][v], dl[i + K - 1 - k][v], acc);
-          const int r = t + K - 1 - L;  // tail slot of F this input became
-          if (r >= 0 && q) acc += to_f32(q[(b * D + d0 + v) * (K - 1) + r]);
-          o[v] = acc;
-        }
-#pragma unroll
-        for (int v = 0; v < VEC; ++v) dx[(b * L + t) * D + d0 + v] = from_f32<TO>(o[v]);
+      for (int i = 0; i < kBwdBatch; ++i) {
+        xc[i] = xn[i];
+        gc[i] = gn[i];
       }
-    }
-    // dS_j = du_j = sum_k w_k delta_{j-k} (+ q_{j-L} when j >= L), j < K-1
-    if (t0 == 0) {
-      for (int j = 0; j < K - 1; ++j) {
+      if (nb + 1 < NB) load_batch(nb + 1);
 #pragma unroll
-        for (int v = 0; v < VEC; ++v) {
-          float acc = 0.0f;
+      for (int i = 0; i < kBwdBatch; ++i) {
+        const int s = nb * kBwdBatch + i;  // step index, j = t0 + s
+        if (s < NIT) {
+          const int j = t0 + s;
+          const float m = j < L ? 1.0f : 0.0f;
 #pragma unroll
-          for (int k = 0; k < MK; ++k) {
-            const int i = j - k;
-            if (k < K && i >= 0) {
-              // dl is indexed from t0 = 0; i < K-1 < NZ
+          for (int v = 0; v < VEC; ++v) {
 #pragma unroll
-              for (int ii = 0; ii < NZ; ++ii)
-                if (ii == i) acc = fmaf(wk[k][v], dl[ii][v], acc);
+            for (int k = 0; k < MK - 1; ++k) xw[k][v] = xw[k + 1][v];
+            xw[MK - 1][v] = to_f32(xc[i].e[v]) * m;
+#pragma unroll
+            for (int k = 0; k < MK - 1; ++k) dl[k][v] = dl[k + 1][v];
+            float z = bs[v];
+#pragma unroll
+            for (int k = 0; k < MK; ++k) z = fmaf(wz[k][v], xw[k][v], z);
+            const float g = to_f32(gc[i].e[v]) * m;
+            const float dv = SILU ? g * dsilu(z) : g;
+            dl[MK - 1][v] = dv;
+            if (s < kBwdTile) {  // delta_j belongs to this tile
+              dbp[v] += dv;
+#pragma unroll
+              for (int k = 0; k < MK; ++k) dwp[k][v] = fmaf(dv, xw[k][v], dwp[k][v]);
             }
           }
-          if (j >= L && q) acc += to_f32(q[(b * D + d0 + v) * (K - 1) + (j - L)]);
-          dS[(b * D + d0 + v) * (K - 1) + j] = from_f32<TO>(acc);
+          // du for u index ju = j - (MK-1) + KM1, i.e. x token t = j - (MK-1)
+          const int t = j - (MK - 1);
+          const int ju = t + KM1;
+          if (t >= t0 || (t0 == 0 && ju >= 0)) {
+            float o[VEC];
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) {
+              float acc = 0.0f;
+#pragma unroll
+              for (int k = 0; k < MK; ++k) acc = fmaf(wd[k][v], dl[k][v], acc);
+              o[v] = acc;
+            }
+            if (q && ju >= L && ju < L + KM1) {  // direct path from F = u[L : L+K-1]
+#pragma unroll
+              for (int v = 0; v < VEC; ++v)
+                o[v] += to_f32(q[(b * D + d0 + v) * KM1 + (ju - L)]);
+            }
+            if (t >= t0) {
+              if (t < L) st_vec<TO, VEC>(dx + (b * L + t) * D + d0, o);
+            } else {
+#pragma unroll
+              for (int v = 0; v < VEC; ++v)
+                dS[(b * D + d0 + v) * KM1 + ju] = from_f32<TO>(o[v]);
+            }
+          }
         }
-      }
-    }
-    // this tile's dw_k = sum_t delta_t u_{t+k}, dbias = sum_t delta_t
-#pragma unroll
-    for (int i = 0; i < kBwdTile; ++i) {
-#pragma unroll
-      for (int v = 0; v < VEC; ++v) {
-        dbp[v] += dl[i][v];
-#pragma unroll
-        for (int k = 0; k < MK; ++k) dwp[k][v] = fmaf(dl[i][v], ext[i + k][v], dwp[k][v]);
       }
     }
   }
@@ -173,13 +202,14 @@ conv_state_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
     red[warp][MK][lane * VEC + v] = dbp[v];
   }
   __syncthreads();
-  // row (b, tg) of the partials: [D][K+1] floats
+  // row (b, tg) of the partials: [D][K+1] floats; dwp[k] holds the tap of
+  // window slot k, i.e. tap k - (MK - K)
   float* row = part + (b * n_groups + tg) * int64_t(D) * (K + 1);
   for (int e = threadIdx.x; e < 32 * VEC * (K + 1); e += blockDim.x) {
     const int c = e / (K + 1), k = e % (K + 1);  // channel c of this CTA's 32*VEC
     const int d = blockIdx.x * 32 * VEC + c;
     if (d < n_dvec * VEC) {
-      const int kk = k < K ? k : MK;
+      const int kk = k < K ? k + (MK - K) : MK;
       float acc = 0.0f;
       for (int ww = 0; ww < kBwdWarps; ++ww) acc += red[ww][kk][c];
       row[int64_t(d) * (K + 1) + k] = acc;
@@ -187,19 +217,41 @@ conv_state_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
   }
 }
 
-// dw[d][k] = sum over rows of part[row][d][k] (k < K); dbias[d] = part[..][d][K]
-__global__ void conv_bwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
-                                       float* __restrict__ dbias, int64_t rows, int D, int K) {
-  const int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+// dw[d][k] = sum over rows of part[row][d][k] (k < K); dbias[d] = part[..][d][K].
+// A CTA takes 32 consecutive entries; warp w adds rows w, w+8, ... in order,
+// then the 8 warp sums are added in warp order (a fixed order for given sizes).
+__global__ void __launch_bounds__(256)
+conv_bwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
+                       float* __restrict__ dbias, int64_t rows, int D, int K) {
+  __shared__ float acc_s[8][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n = int64_t(D) * (K + 1);
-  if (e >= n) return;
+  const int64_t e = int64_t(blockIdx.x) * 32 + lane;
   float acc = 0.0f;
-  for (int64_t r = 0; r < rows; ++r) acc += part[r * n + e];
-  const int d = int(e / (K + 1)), k = int(e % (K + 1));
-  if (k < K)
-    dw[int64_t(d) * K + k] = acc;
-  else if (dbias)
-    dbias[d] = acc;
+  if (e < n) {
+    int64_t r = warp;
+    for (; r + 24 < rows; r += 32) {
+      const float a0 = part[r * n + e], a1 = part[(r + 8) * n + e];
+      const float a2 = part[(r + 16) * n + e], a3 = part[(r + 24) * n + e];
+      acc += a0;
+      acc += a1;
+      acc += a2;
+      acc += a3;
+    }
+    for (; r < rows; r += 8) acc += part[r * n + e];
+  }
+  acc_s[warp][lane] = acc;
+  __syncthreads();
+  if (warp == 0 && e < n) {
+    float s = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < 8; ++ww) s += acc_s[ww][lane];
+    const int d = int(e / (K + 1)), k = int(e % (K + 1));
+    if (k < K)
+      dw[int64_t(d) * K + k] = s;
+    else if (dbias)
+      dbias[d] = s;
+  }
 }
 
 // L = 0: F = S, so dS = q, and there is no weight or bias gradient
@@ -243,12 +295,12 @@ static cudaError_t launch_bwd(const void* x, const float* w, const float* bias, 
     e = silu_on ? args(conv_state_bwd_kernel<TX, TD, TO, VEC, 4, true>)
                 : args(conv_state_bwd_kernel<TX, TD, TO, VEC, 4, false>);
   else
-    e = silu_on ? args(conv_state_bwd_kernel<TX, TD, TO, VEC, 0, true>)
-                : args(conv_state_bwd_kernel<TX, TD, TO, VEC, 0, false>);
+    e = silu_on ? args(conv_state_bwd_kernel<TX, TD, TO, VEC, kBwdMaxK, true>)
+                : args(conv_state_bwd_kernel<TX, TD, TO, VEC, kBwdMaxK, false>);
   if (e != cudaSuccess) return e;
   const int64_t n = D * (K + 1);
-  conv_bwd_reduce_kernel<<<unsigned((n + 255) / 256), 256, 0, st>>>(part, dw, dbias,
-                                                                     Bz * groups, int(D), K);
+  conv_bwd_reduce_kernel<<<unsigned((n + 31) / 32), 256, 0, st>>>(part, dw, dbias, Bz * groups,
+                                                                  int(D), K);
   return cudaGetLastError();
 }
 
@@ -265,7 +317,12 @@ static cudaError_t bwd_vec(const void* x, const float* w, const float* bias, con
         static_cast<const TD*>(q), static_cast<TO*>(dS), dw, dbias, n_state, int(D), K);
     return cudaGetLastError();
   }
-  if (D % 2 == 0)
+  // channel pairs are loaded and stored as one vector each, which needs
+  // every tensor aligned to two elements
+  auto al2 = [](const void* p, size_t es) {
+    return (reinterpret_cast<uintptr_t>(p) % (2 * es)) == 0;
+  };
+  if (D % 2 == 0 && al2(x, sizeof(TX)) && al2(dy, sizeof(TD)) && al2(dx, sizeof(TO)))
     return launch_bwd<TX, TD, TO, 2>(x, w, bias, s_in, dy, q, dx, dS, dw, dbias, Bz, L, D, K,
                                      silu_on, ws, st);
   return launch_bwd<TX, TD, TO, 1>(x, w, bias, s_in, dy, q, dx, dS, dw, dbias, Bz, L, D, K,

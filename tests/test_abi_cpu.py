@@ -95,9 +95,9 @@ def test_conv_backward_host_checks(lib):
     ws = lib.sss_conv_state_bwd_workspace_size
     ws.restype = ctypes.c_size_t
     ws.argtypes = [i64, i64, i64, ctypes.c_int]
-    # one row of D * (K+1) fp32 partial sums per sequence and 64-token group
-    assert ws(8, 1024, 2048, 4) == 8 * 16 * 2048 * 5 * 4
-    assert ws(2, 65, 10, 3) == 2 * 2 * 10 * 4 * 4
+    # one row of D * (K+1) fp32 partial sums per sequence and 512-token group
+    assert ws(8, 1024, 2048, 4) == 8 * 2 * 2048 * 5 * 4
+    assert ws(2, 513, 10, 3) == 2 * 2 * 10 * 4 * 4
     assert ws(2, 0, 10, 3) == 0
     f = lib.sss_conv_state_bwd
     f.restype = ctypes.c_int

@@ -52,7 +52,8 @@ def _run(x, w, bias, S, dy, q, dxdt, silu=True):
 @pytest.mark.parametrize("Bz,L,D,K,silu", [
     (2, 37, 24, 4, True), (2, 37, 7, 4, False), (3, 1, 16, 4, True), (2, 2, 16, 4, True),
     (2, 70, 16, 3, True), (2, 65, 16, 2, True), (1, 130, 10, 5, True), (2, 9, 16, 8, True),
-    (2, 5, 6, 1, True), (1, 64, 32, 4, True), (1, 129, 32, 4, True)])
+    (2, 5, 6, 1, True), (1, 64, 32, 4, True), (1, 129, 32, 4, True), (2, 600, 18, 3, True),
+    (1, 520, 34, 8, False), (2, 769, 66, 4, True)])
 def test_conv_bwd_fp32_parity(Bz, L, D, K, silu):
     x, w, bias, S, dy, q = _case(31 * L + D + K, Bz, L, D, K, "f32", "f32")
     dx_r, dS_r, dw_r, db_r = oracle.conv_state_bwd(x, w, bias, S, dy, q, apply_silu=silu)

@@ -71,7 +71,7 @@ def _compare(got, ref, bf16_out):
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
     # first call: a full 1024-token segment of the Mamba-2 370M-like layer
-    # (5 MiB of partial sums); second call: a smaller ragged fp32 case that
+    # (0.6 MiB of partial sums); second call: a smaller ragged fp32 case that
     # reads only part of what the first call left in the scratch
     cases = [((1, 8, 1024, 2048, 4), "bf16", "f32", torch.bfloat16),
              ((2, 3, 301, 96, 4), "f32", "f32", torch.float32)]
@@ -86,9 +86,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # 16 sequences of 1024 tokens at D = 2048 need 10 MiB of partial sums: the
-    # call returns SSS_ERR_UNSUPPORTED before looking at any pointer
-    Bz, L, D, K = 16, 1024, 2048, 4
+    # 64 sequences of 4096 tokens at D = 2048 need 40 MiB of partial sums:
+    # the call returns SSS_ERR_UNSUPPORTED before looking at any pointer
+    Bz, L, D, K = 64, 4096, 2048, 4
     assert sss.conv_state_bwd_workspace_size(Bz, L, D, K) > sss.CONV_BWD_NOALLOC_SCRATCH_BYTES
     rc = sss._lib.sss_conv_state_bwd_noalloc(
         None, sss.SSS_BF16, None, None, None, None, sss.SSS_F32, None, None, sss.SSS_BF16,
