@@ -438,8 +438,10 @@ def main():
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(s), "tokens_per_step": tokens_per_step,
-                   "path": "sss_mixer_fwd: one tcgen05 kernel per segment (conv+SiLU+scan)",
-                   "scan_path_two_call": "tcgen05" if path == 1 else "cuda-core fp32",
+                   "path": "sss_mixer_fwd: one tcgen05 kernel per segment (conv+SiLU+scan), "
+                           "two heads per CTA",
+                   "scan_path_two_call": {2: "tcgen05, two heads per CTA", 1: "tcgen05",
+                                          0: "cuda-core fp32"}.get(path, "unsupported"),
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,

@@ -196,16 +196,18 @@ sss_status sss_conv_state_bwd_noalloc(const void* x, sss_dtype x_dtype, const fl
  *  y       [Bz, L, H, P]  y_dtype
  *  workspace / workspace_bytes: scratch of at least
  *          sss_ssm_scan_workspace_size() bytes (may be NULL when that is 0).
- * bf16 activations with P == 64, N == 128 run on the tcgen05 tensor-core
- * chunked scan; every other case runs on the fp32 CUDA-core scan.  The
- * state is kept in fp32 in both.
+ * bf16 activations with P == 64, N == 128 run on a tcgen05 tensor-core
+ * chunked scan (two heads per CTA when H / G is even, one otherwise); every
+ * other case runs on the fp32 CUDA-core scan.  The state is kept in fp32
+ * throughout.
  */
 size_t sss_ssm_scan_workspace_size(int64_t Bz, int64_t L, int H, int P, int N,
                                    int G, sss_dtype x_dtype, sss_dtype act_dtype);
 
 /* Which kernel sss_ssm_scan_fwd picks for these sizes and dtypes (given
- * 16-byte aligned tensors): 1 = tcgen05 tensor-core chunked scan,
- * 0 = fp32 CUDA-core scan, -1 = unsupported. */
+ * 16-byte aligned tensors): 2 = tcgen05 chunked scan over head pairs,
+ * 1 = tcgen05 chunked scan, one head per CTA, 0 = fp32 CUDA-core scan,
+ * -1 = unsupported. */
 int sss_ssm_scan_path(int64_t Bz, int64_t L, int H, int P, int N, int G,
                       sss_dtype x_dtype, sss_dtype act_dtype, sss_dtype y_dtype);
 

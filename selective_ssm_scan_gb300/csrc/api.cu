@@ -31,6 +31,16 @@ cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias
                                 const void* B, const void* C, const float* h0, float* hT,
                                 void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G, int K,
                                 int* status, cudaStream_t st);
+bool ssm_scan_pair_supports(sss_dtype at, int64_t L, int H, int P, int N, int G);
+cudaError_t ssm_scan_pair_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
+                                 const void* B, const void* C, const float* h0, float* hT,
+                                 void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
+                                 int* status, cudaStream_t st);
+cudaError_t mixer_fwd_pair_launch(const void* x, const float* w, const float* bias,
+                                  const void* s_in, void* s_out, const void* dt, const float* A,
+                                  const void* B, const void* C, const float* h0, float* hT,
+                                  void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
+                                  int K, int* status, cudaStream_t st);
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
                                cudaStream_t st);
 cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
@@ -152,7 +162,8 @@ size_t sss_ssm_scan_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, i
 int sss_ssm_scan_path(int64_t Bz, int64_t L, int H, int P, int N, int G, sss_dtype x_dtype,
                       sss_dtype act_dtype, sss_dtype y_dtype) {
   (void)Bz;
-  if (ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, L, H, P, N, G)) return 1;
+  if (ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, L, H, P, N, G))
+    return ssm_scan_pair_supports(act_dtype, L, H, P, N, G) ? 2 : 1;
   if (ssm_scan_simt_supports(P, N)) return 0;
   return -1;
 }
@@ -217,9 +228,13 @@ sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (L > 0 && ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, L, H, P, N, G) &&
       aligned(x, 16) && aligned(B, 16) && aligned(C, 16) && aligned(y, 16) &&
-      (!h0_in || aligned(h0_in, 16)) && (!hT_out || aligned(hT_out, 16)))
+      (!h0_in || aligned(h0_in, 16)) && (!hT_out || aligned(hT_out, 16))) {
+    if (ssm_scan_pair_supports(act_dtype, L, H, P, N, G))
+      return from_cuda(ssm_scan_pair_launch(x, x_dtype, dt, A, B, C, h0_in, hT_out, y, y_dtype,
+                                            Bz, L, H, G, status_word(), st));
     return from_cuda(ssm_scan_tc_launch(x, x_dtype, dt, A, B, C, h0_in, hT_out, y, y_dtype, Bz,
                                         L, H, P, N, G, status_word(), st));
+  }
   if (!ssm_scan_simt_supports(P, N)) return SSS_ERR_UNSUPPORTED;
   return from_cuda(ssm_scan_simt_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y,
                                         y_dtype, Bz, L, H, P, N, G, st));
@@ -258,6 +273,10 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const
   if (!x || !dt || !B || !C || !y || !aligned(x, 16) || !aligned(dt, 2) || !aligned(B, 16) ||
       !aligned(C, 16) || !aligned(y, 16))
     return SSS_ERR_INVALID_ARG;
+  if (ssm_scan_pair_supports(x_dtype, L, H, P, N, G))
+    return from_cuda(mixer_fwd_pair_launch(x, w, bias, conv_state_in, conv_state_out, dt, A, B,
+                                           C, h0_in, hT_out, y, y_dtype, Bz, L, H, G, K,
+                                           status_word(), st));
   return from_cuda(mixer_fwd_tc_launch(x, w, bias, conv_state_in, conv_state_out, dt, A, B, C,
                                        h0_in, hT_out, y, y_dtype, Bz, L, H, G, K, status_word(),
                                        st));

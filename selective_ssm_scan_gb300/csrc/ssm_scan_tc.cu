@@ -53,10 +53,12 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "scan_tc_util.cuh"
 #include "tc_ptx.cuh"
 
 namespace sss {
 using namespace tc;
+using namespace tcs;
 
 namespace {
 constexpr int kQ = 128;  // chunk length = MMA M
@@ -98,10 +100,6 @@ constexpr uint32_t kOffXs = 202752;
 constexpr uint32_t kXsRows = 128 + 3;
 constexpr uint32_t kXsBytes = kXsRows * 128;
 constexpr uint32_t kSmemBytes = kOffXs + kXsBytes + 1024;
-// chunks whose log-decay range exceeds this use exp(Lam_t - Lam_s) per
-// element instead of the factored exp(Lam_t - R) exp(R - Lam_s)
-constexpr float kFactorRange = 100.0f;
-constexpr uint64_t kWaitNs = 2000000000ull;
 // barriers
 enum {
   BAR_FULL_CB = 0, BAR_TILES = 1 /*2*/, BAR_U_FREE = 3 /*2*/, BAR_X_FREE = 5, BAR_G_FULL = 6,
@@ -115,71 +113,7 @@ constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);     // C (K-major) x h (MN
 constexpr uint32_t kIdYd = idesc_bf16(128, 128, 0, 1);    // hi(G o mask) (TMEM) x x'hi|lo (MN-major)
 constexpr uint32_t kIdYdLo = idesc_bf16(128, 64, 0, 1);   // lo(G o mask) (TMEM) x x'hi
 
-__device__ __forceinline__ uint16_t bf16_bits(float v) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(v));
-}
-__device__ __forceinline__ uint32_t pack2(uint16_t lo_elem, uint16_t hi_elem) {
-  return uint32_t(lo_elem) | (uint32_t(hi_elem) << 16);
-}
-// (a, b) -> packed hi pair and lo pair: v == hi + lo to ~2^-16 relative
-// (one paired conversion for each half)
-__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
-  hi = *reinterpret_cast<const uint32_t*>(&h2);
-  const __nv_bfloat162 l2 =
-      __floats2bfloat162_rn(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xFFFF0000u));
-  lo = *reinterpret_cast<const uint32_t*>(&l2);
-}
-
-// K-major descriptor of a [rows][128-element K] tile stored as two 64-wide K
-// blocks `blk` bytes apart; K step kk covers K elements [16 kk, 16 kk + 16).
-__device__ __forceinline__ uint64_t kdesc(uint32_t base, int kk, uint32_t blk) {
-  return sdesc_sw128(base + uint32_t(kk >> 2) * blk + uint32_t(kk & 3) * 32u, 16, 1024);
-}
-// MN-major descriptor of [K rows][64 MN] tiles (128-byte rows), a second
-// 64-wide MN block 16 KB further (used when N = 128): K step kk starts 16
-// rows further.
-__device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
-  return sdesc_sw128(base + uint32_t(kk) * 2048u, 16384, 1024);
-}
-
-// Row `r` (64 fp32 values) -> hi and lo bf16 rows of two MN-major tiles.
-__device__ __forceinline__ void write_split_row(uint8_t* hi_tile, uint8_t* lo_tile, int r,
-                                                const float* v) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint32_t hw[4], lw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) split2(v[8 * c + 2 * k], v[8 * c + 2 * k + 1], hw[k], lw[k]);
-    *reinterpret_cast<uint4*>(hi_tile + sw128(r, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(lo_tile + sw128(r, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  }
-}
-
 // Named barrier among the threads of one role (ids 1, 2; 0 is __syncthreads).
-
-struct Ctl {
-  uint32_t bars;              // smem address of barrier 0
-  volatile int* abort;
-  int* status;
-  __device__ uint32_t bar(int i) const { return bars + 8u * uint32_t(i); }
-  // bounded wait; false when the CTA is aborting
-  __device__ bool wait(int i, uint32_t parity) const {
-    const uint32_t b = bar(i);
-    if (mbar_try_wait(b, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    // sleep in the wait (woken by the phase completing) rather than spin
-    while (!mbar_try_wait_sleep(b, parity, 20000u)) {
-      if (*abort) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) {
-        *abort = 1;
-        raise_status(status, SSS_ERR_TIMEOUT);
-        return false;
-      }
-    }
-    return true;
-  }
-};
 
 // Inclusive prefix of `v` over the NW warps of a role; also the total and the
 // minimum / maximum of the prefix over the role.  `red` holds 3 NW floats.
@@ -215,25 +149,6 @@ __device__ __forceinline__ float role_prefix(float v, int lane, int wq, float* r
   *pmin = gmn;
   *pmax = gmx;
   return v + off;
-}
-
-template <typename TY>
-__device__ __forceinline__ void store_row16(TY* row, const float* v);
-template <>
-__device__ __forceinline__ void store_row16<float>(float* row, const float* v) {
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    reinterpret_cast<float4*>(row)[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-}
-template <>
-__device__ __forceinline__ void store_row16<__nv_bfloat16>(__nv_bfloat16* row, const float* v) {
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    uint32_t w[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) w[k] = pack2(bf16_bits(v[8 * q + 2 * k]), bf16_bits(v[8 * q + 2 * k + 1]));
-    reinterpret_cast<uint4*>(row)[q] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
 }
 
 }  // namespace
@@ -918,46 +833,6 @@ tc_selftest2_kernel(const __grid_constant__ CUtensorMap tmA, const __nv_bfloat16
 // host side
 // ---------------------------------------------------------------------------
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// [Bz][L][G*N] bf16 viewed as a 3-D tensor; boxes of 64 (n) x 128 (t) x 1.
-bool make_bc_map(CUtensorMap* m, const void* ptr, int64_t Bz, int64_t L, int G, int N) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {cuuint64_t(G) * N, cuuint64_t(L), cuuint64_t(Bz)};
-  const cuuint64_t strides[2] = {cuuint64_t(G) * N * 2, cuuint64_t(L) * G * N * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// raw input [Bz][L][D] bf16 as a 3-D tensor; boxes of 64 channels x 131 rows x 1
-bool make_x_map(CUtensorMap* m, const void* ptr, int64_t Bz, int64_t L, int64_t D) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(L), cuuint64_t(Bz)};
-  const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(L) * D * 2};
-  const cuuint32_t box[3] = {64, kXsRows, 1};
-  const cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool make_tile_map(CUtensorMap* m, const void* ptr) {  // [128][128] bf16
   auto fn = encode_fn();
   if (!fn) return false;
@@ -979,7 +854,7 @@ cudaError_t launch_tc(const void* x, const void* dt, const float* A, const void*
   if (!make_bc_map(&mB, B, Bz, L, G, kN) || !make_bc_map(&mC, C, Bz, L, G, kN))
     return cudaErrorInvalidValue;
   if (FUSED) {
-    if (!make_x_map(&mX, x, Bz, L, int64_t(H) * kP)) return cudaErrorInvalidValue;
+    if (!make_x_map(&mX, x, Bz, L, int64_t(H) * kP, kXsRows)) return cudaErrorInvalidValue;
   } else {
     mX = mB;  // unused
   }

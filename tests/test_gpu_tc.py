@@ -39,7 +39,12 @@ def test_tcgen05_operand_layouts():
 
 def test_scan_path_selection():
     bf, f32 = torch.bfloat16, torch.float32
-    assert sss.ssm_scan_path(8, 1024, 32, 64, 128, 1, f32, bf, bf) == 1
-    assert sss.ssm_scan_path(8, 1024, 32, 64, 128, 1, bf, bf, bf) == 1
+    # head pairs share a B/C group: the two-head kernel
+    assert sss.ssm_scan_path(8, 1024, 32, 64, 128, 1, f32, bf, bf) == 2
+    assert sss.ssm_scan_path(8, 1024, 32, 64, 128, 1, bf, bf, bf) == 2
+    assert sss.ssm_scan_path(2, 300, 8, 64, 128, 4, bf, bf, bf) == 2
+    # an odd number of heads per group: one head per CTA
+    assert sss.ssm_scan_path(2, 300, 3, 64, 128, 1, bf, bf, bf) == 1
+    assert sss.ssm_scan_path(2, 300, 6, 64, 128, 2, bf, bf, bf) == 1
     assert sss.ssm_scan_path(1, 64, 2, 4, 8, 1, f32, f32, f32) == 0
     assert sss.ssm_scan_path(1, 64, 2, 64, 128, 1, f32, f32, f32) == 0
