@@ -58,12 +58,23 @@ def peaks():
 
 
 def kernel_source_hash(kernel: str) -> str:
-    """sha256 (first 16 hex digits) of the kernel's .cu file followed by the
-    two shared headers it includes."""
+    """sha256 (first 16 hex digits) of the kernel's .cu file followed by every
+    local header it includes, directly or through another header, in the
+    order first met."""
     import hashlib
+    import re
     d = os.path.join(ROOT, "selective_ssm_scan_gb300", "csrc")
+    order, todo = [], [f"{kernel}.cu"]
+    while todo:
+        fn = todo.pop(0)
+        if fn in order:
+            continue
+        order.append(fn)
+        with open(os.path.join(d, fn)) as f:
+            todo += [m for m in re.findall(r'^#include "([^"]+)"', f.read(), re.M)
+                     if os.path.exists(os.path.join(d, m))]
     h = hashlib.sha256()
-    for fn in (f"{kernel}.cu", "tc_ptx.cuh", "common.cuh"):
+    for fn in order:
         with open(os.path.join(d, fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -336,9 +347,9 @@ def main():
     tc_flops = s.Bz * s.H * chunks * 2 * Q * (Q * s.N + Q * s.P + 2 * s.P * s.N)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm,
-                "traffic": traffic_from_profile("ssm_scan_tc", WORKLOAD),
-                "kernel": "ssm_scan_tc_kernel<bf16,bf16,fused> (conv+SiLU+scan, one launch "
-                          "per segment)",
+                "traffic": traffic_from_profile("ssm_scan_pair", WORKLOAD),
+                "kernel": "ssm_scan_pair_kernel<bf16,bf16,fused> (conv+SiLU+scan, two heads "
+                          "per CTA, one launch per segment)",
                 "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_ms": fused_avg,
                 "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured"
                 else "fallback 6.8 TB/s",

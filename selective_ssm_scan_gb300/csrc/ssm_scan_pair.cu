@@ -20,27 +20,34 @@
 // 128-token pieces; a head with a huge decay gives shorter ones (a single
 // token always qualifies: its range is 0).
 //
-// GB300 mapping, one CTA per (batch, head pair), 416 threads (13 warps: the
+// GB300 mapping, one CTA per (batch, head pair), 448 threads (14 warps: the
 // register file then allows 128 registers a thread):
-//   warps 0-3  producers: per piece, the decay prefix of both heads (one token
-//              per thread) and the piece length; then per head the conv + SiLU
-//              of the raw rows (TMA-staged) or the input rows and the
-//              x' = g x hi/lo tiles (16-byte stores, 128-byte swizzle), two
-//              items of 8 channels x 4 tokens per thread;
-//   warps 4-11 consumers: warp 4 + 4 hs + q owns head hs and TMEM lanes
-//              32q..32q+31: its share of the causal mask of G (32-column blocks
-//              2hs, 2hs+1), then the state carry of head hs (one state row n
-//              per thread, fp32 registers) and the y rows of head hs;
-//   warp 12    issuer: TMA of B and C (double-buffered, one piece ahead) and
-//              every tcgen05.mma, one thread.
-// Tensor memory (512 columns): G [t][s] 128, hi/lo(G o causal) 64 + 64,
-// Y of each head 64, S' of each head 64.  Shared memory: B/C stages 2 x 64 KB,
-// one x' tile pair and one h' tile pair shared by the two heads (each head's
-// tiles are written once the other head's products have read them), the
-// staged raw rows, and the piece descriptors.  Per piece the MMAs run
-//   G, Yo_a, S'_a, Yd_a, Yo_b, S'_b, Yd_b
-// so each tile hand-over hides behind products of the other head.  Every
-// wait is bounded (2 s); a timeout raises SSS_ERR_TIMEOUT and unwinds.
+//   warps 0-7  producers: per piece and head the conv + SiLU of the raw rows
+//              (TMA-staged) or the input rows and the x' = g x hi/lo values,
+//              8 channels x 4 tokens per thread (packed f32x2 arithmetic),
+//              stored for both heads at once;
+//   warps 8-11 consumers: warp 8 + q owns TMEM lanes 32q..32q+31 (rows t of
+//              G and Y, state rows n of S' and h) for both heads: the causal
+//              mask of its rows of G, the state carry, its rows of the h'
+//              tiles and its y rows;
+//   warp 12    issuer: TMA of B and C and every tcgen05.mma, one thread;
+//   warp 13    decay: per piece, the log-decay prefix of both heads (4 tokens
+//              per lane), the piece length and the chunk scalars, published
+//              in a ring of 4 piece descriptors up to 4 pieces ahead.
+// The two heads' x' tiles (and h' tiles) sit side by side as the two 64-wide
+// halves of one N = 128 operand, so every product covers both heads in one
+// M = 128, N = 128 MMA:
+//   G = C B^T,  S'_ab = B^T [x'_a | x'_b],  Y_ab = C [h'_a | h'_b]^T + (G o c) [x'_a | x'_b].
+// Tensor memory (512 columns): G [t][s] 128 (the masked hi/lo split of G is
+// written over G, block by block), Y, S' and the fp32 state h of both heads,
+// 128 each: the state never leaves the SM between pieces.  Shared memory:
+// the piece's C and B
+// (32 KB each), the x' tiles (hi and lo, 64 KB), the h' tiles (64 KB), the
+// staged raw rows and the piece descriptors.  Per piece the MMAs run
+//   G, S', Yo, Yd
+// and every hand-over (x', h', Y, S', the mask, the next piece's B and C) has
+// at least one product group of slack.  Every wait is bounded (2 s); a timeout
+// raises SSS_ERR_TIMEOUT and unwinds.
 #include "common.cuh"
 #include "scan_tc_util.cuh"
 #include "tc_ptx.cuh"
@@ -54,35 +61,41 @@ namespace pr {
 constexpr int kP = 64;    // head dimension
 constexpr int kN = 128;   // state size
 constexpr int kMaxK = 4;  // conv width handled by the fused producer
-constexpr int kProdWarps = 4;
-constexpr int kConsWarp0 = 4;
+constexpr int kProdWarps = 8;
 constexpr int kIssuerWarp = 12;
-constexpr int kThreads = (kIssuerWarp + 1) * 32;  // 416
-constexpr int kPT = kProdWarps * 32;              // 128 producer threads
+constexpr int kDecayWarp = 13;
+constexpr int kThreads = (kDecayWarp + 1) * 32;    // 448
+constexpr int kPT = kProdWarps * 32;               // 256 producer threads
+constexpr int kCT = 128;                           // consumer threads
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColG = 0, kColGh = 128, kColGl = 192;
-constexpr uint32_t kColY = 256;  // + 64 hs
-constexpr uint32_t kColS = 384;  // + 64 hs
+// tensor memory columns: G [t][s] fp32, overwritten block by block by the
+// masked split (32-column block j: hi pairs at 32j, lo pairs at 32j + 16);
+// Y [t][p], S' [n][p] and the fp32 state h [n][p], head b at + 64 in each
+constexpr uint32_t kColG = 0;
+constexpr uint32_t kColY = 128;
+constexpr uint32_t kColS = 256;
+constexpr uint32_t kColH = 384;
 // shared memory (bytes from a 1024-byte aligned base)
-constexpr uint32_t kOffBC = 0;        // stage k: C at 65536 k (two 64-wide n blocks), B at +32768
-constexpr uint32_t kOffX = 131072;    // x' hi; lo at +16384 (rows s)
-constexpr uint32_t kOffH = 163840;    // h' hi; lo at +16384 (rows n)
+constexpr uint32_t kOffC = 0;         // C of the piece [t][n] (two 64-wide n blocks)
+constexpr uint32_t kOffB = 32768;     // B of the piece [s][n]
+constexpr uint32_t kOffX = 65536;     // x' hi of head hs at + 16384 hs, lo at + 32768 + 16384 hs (rows s)
+constexpr uint32_t kOffH = 131072;    // h' hi of head hs at + 16384 hs, lo at + 32768 + 16384 hs (rows n)
 constexpr uint32_t kOffXs = 196608;   // staged raw rows [t0 - 3, t0 + 128) of one head
 constexpr uint32_t kXsRows = 128 + kMaxK - 1;
 constexpr uint32_t kXsBytes = kXsRows * 128;
 constexpr uint32_t kOffMisc = kOffXs + kXsBytes;  // 213376
 // misc (offsets from kOffMisc)
 constexpr uint32_t kMiInfo = 0;       // 4 piece descriptors
-constexpr uint32_t kMiRed = 4224;     // producer scan scratch [2][4][4] + piece lengths
+constexpr uint32_t kMiRed = 4224;     // (unused)
 // conv weights and bias, per (head hs, channel pair e2, channel group q) 12
 // floats: the taps of channels 8q + 2e2 and 8q + 2e2 + 1 interleaved (tap k of
 // the pair = floats 2k, 2k+1), the two biases, 2 pad.  The 48-byte stride puts
 // the 8 groups a warp reads on distinct banks.
 constexpr uint32_t kMiW = 4480;       // [2][4][8][12] floats
 constexpr uint32_t kMiBars = 7552;    // mbarriers
-constexpr uint32_t kMiTmem = 7808;
-constexpr uint32_t kMiAbort = 7812;
-constexpr uint32_t kMiscBytes = 7816;
+constexpr uint32_t kMiTmem = 7840;
+constexpr uint32_t kMiAbort = 7844;
+constexpr uint32_t kMiscBytes = 7848;
 constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
 constexpr int kSlots = 4;
 
@@ -94,72 +107,21 @@ struct PieceInfo {
 static_assert(sizeof(PieceInfo) * kSlots <= kMiRed, "piece ring");
 
 enum {
-  BAR_BC_FULL = 0 /*2*/, BAR_BC_FREE = 2 /*2*/, BAR_XS_FULL = 4, BAR_INFO_FULL = 5 /*4*/,
-  BAR_INFO_FREE = 9 /*4*/, BAR_X_FULL = 13, BAR_X_FREE = 14, BAR_G_FULL = 15, BAR_GM_FULL = 16,
-  BAR_GM_FREE = 17, BAR_H_FULL = 18 /*2*/, BAR_H_FREE = 20 /*2*/, BAR_S_FULL = 22 /*2*/,
-  BAR_S_FREE = 24 /*2*/, BAR_Y_FULL = 26 /*2*/, BAR_Y_FREE = 28 /*2*/, BAR_DRAIN = 30,
-  NUM_BARS = 31
+  BAR_C_FULL = 0, BAR_B_FULL = 1, BAR_C_FREE = 2, BAR_B_FREE = 3, BAR_XS_FULL = 4,
+  BAR_INFO_FULL = 5 /*4*/, BAR_INFO_FREE = 9 /*4*/, BAR_X_FULL = 13, BAR_X_FREE = 14,
+  BAR_G_FULL = 15, BAR_GM_FULL = 16, BAR_YD_DONE = 17, BAR_H_FULL = 18, BAR_H_FREE = 19,
+  BAR_S_FULL = 20, BAR_S_FREE = 21, BAR_Y_FULL = 22, BAR_Y_FREE = 23,
+  BAR_DRAIN = 24, NUM_BARS = 25
 };
-// Barrier discipline: each barrier's completions are awaited in order by one
-// role that sees every one of them, so the phase parity it waits on is never
-// two phases stale.  (The h' tile pair is handed between the heads through
-// two barriers, BAR_H_FREE + hs = "Yo of head hs has read the tiles", for
-// that reason: arrivals on different barriers are not ordered.)
+// Barrier discipline: each barrier's completions are awaited in order by
+// threads that see every one of them, so the phase parity they wait on is
+// never two phases stale (arrivals on different barriers are not ordered).
 static_assert(NUM_BARS * 8 <= kMiTmem - kMiBars, "barrier area");
 
 constexpr uint32_t kIdG = idesc_bf16(128, 128, 0, 0);   // C (K-major) x B (K-major)
-constexpr uint32_t kIdS = idesc_bf16(128, 64, 1, 1);    // B^T (MN-major) x x' (MN-major)
-constexpr uint32_t kIdYo = idesc_bf16(128, 64, 0, 1);   // C (K-major) x h' (MN-major)
-constexpr uint32_t kIdYd = idesc_bf16(128, 64, 0, 1);   // (G o causal) (TMEM) x x' (MN-major)
-
-// Inclusive prefix over 128 tokens held one per thread by 4 warps, for the
-// two heads at once (one named barrier): per head the prefix sum and the
-// prefix min / max of the prefix sum.  `red` holds 24 floats.
-__device__ __forceinline__ void piece_scan2(const float (&v0)[2], int lane, int w4, float* red,
-                                            int bar_id, float (&lam)[2], float (&pmin)[2],
-                                            float (&pmax)[2]) {
-  float v[2] = {v0[0], v0[1]}, mn[2], mx[2];
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float nb = __shfl_up_sync(0xffffffffu, v[h2], o);
-      if (lane >= o) v[h2] += nb;
-    }
-    mn[h2] = v[h2];
-    mx[h2] = v[h2];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float a = __shfl_up_sync(0xffffffffu, mn[h2], o);
-      const float c = __shfl_up_sync(0xffffffffu, mx[h2], o);
-      if (lane >= o) {
-        mn[h2] = fminf(mn[h2], a);
-        mx[h2] = fmaxf(mx[h2], c);
-      }
-    }
-    if (lane == 31) {
-      red[12 * h2 + 3 * w4] = v[h2];
-      red[12 * h2 + 3 * w4 + 1] = mn[h2];
-      red[12 * h2 + 3 * w4 + 2] = mx[h2];
-    }
-  }
-  role_sync(bar_id, 128);
-#pragma unroll
-  for (int h2 = 0; h2 < 2; ++h2) {
-    float off = 0.0f, gmn = 3.0e38f, gmx = -3.0e38f;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      if (w < w4) {
-        gmn = fminf(gmn, off + red[12 * h2 + 3 * w + 1]);
-        gmx = fmaxf(gmx, off + red[12 * h2 + 3 * w + 2]);
-        off += red[12 * h2 + 3 * w];
-      }
-    }
-    lam[h2] = off + v[h2];
-    pmin[h2] = fminf(gmn, off + mn[h2]);
-    pmax[h2] = fmaxf(gmx, off + mx[h2]);
-  }
-}
+constexpr uint32_t kIdS = idesc_bf16(128, 128, 1, 1);   // B^T (MN-major) x [x'_a | x'_b] (MN-major)
+constexpr uint32_t kIdYo = idesc_bf16(128, 128, 0, 1);  // C (K-major) x [h'_a | h'_b] (MN-major)
+constexpr uint32_t kIdYd = idesc_bf16(128, 128, 0, 1);  // (G o causal) (TMEM) x [x'_a | x'_b]
 
 // ---- packed fp32 pairs (two channels at once: f32x2 FMA / MUL / ADD) --------
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
@@ -257,16 +219,12 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     int counts[NUM_BARS];
     for (int i = 0; i < NUM_BARS; ++i) counts[i] = 1;
     for (int i = 0; i < kSlots; ++i) {
-      counts[BAR_INFO_FULL + i] = kPT;
-      counts[BAR_INFO_FREE + i] = 256 + 1;  // consumers + issuer
+      counts[BAR_INFO_FULL + i] = 32;             // the decay warp
+      counts[BAR_INFO_FREE + i] = kPT + kCT + 1;  // producers, consumers, issuer
     }
+    counts[BAR_GM_FULL] = counts[BAR_H_FULL] = counts[BAR_S_FREE] = kCT;
+    counts[BAR_Y_FREE] = kCT;
     counts[BAR_X_FULL] = kPT;
-    counts[BAR_GM_FULL] = 256;
-    for (int i = 0; i < 2; ++i) {
-      counts[BAR_H_FULL + i] = 128;
-      counts[BAR_S_FREE + i] = 128;
-      counts[BAR_Y_FREE + i] = 128;
-    }
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(ctl.bar(i), counts[i]);
     *ctl.abort = 0;
     fence_mbar_init();
@@ -290,16 +248,11 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
 
   if (warp < kProdWarps) {
     // ============================ producers ============================
-    // decay phase: thread = token tk of the piece, both heads; operand phase:
-    // item i = tid + 128 rd (rd = 0, 1) = channels [8q, 8q+8) x tokens
-    // [4 g4, 4 g4 + 4) of one head, q = i & 7, g4 = i >> 3
+    // decay phase: thread = (head hl, token tk); operand phase: thread
+    // (q, g4) = channels [8q, 8q+8) x tokens [4 g4, 4 g4 + 4) of one head
     constexpr int NT = 4;
-    constexpr int NR = NT + kMaxK - 1;  // staged rows an item reads
-    const int tk = tid;
-    const int q = tid & 7;
-    float* red = reinterpret_cast<float*>(misc + kMiRed);
-    int* nred = reinterpret_cast<int*>(misc + kMiRed + 24 * 4);
-    const float Aa = A[2 * pair], Ab = A[2 * pair + 1];
+    constexpr int NR = NT + kMaxK - 1;  // staged rows a thread reads
+    const int q = tid & 7, g4 = tid >> 3, tb = 4 * g4;
     auto stage_x = [&](int start, int hs) {  // TMA of raw rows [start - 3, start + 128)
       mbar_arrive_expect_tx(ctl.bar(BAR_XS_FULL), kXsBytes);
       tma_load_3d(sb + kOffXs, &tmX, (2 * pair + hs) * kP, start - (kMaxK - 1), b,
@@ -310,191 +263,141 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       stage_x(0, 0);
     }
     int xs_issued = FUSED ? 1 : 0, xs_landed = 0;
-    // dt of the next piece's token, loaded one piece ahead
-    auto load_dt = [&](int start, int hh) -> float {
-      const int t = start + tk;
-      return t < L ? __bfloat162float(dt[(int64_t(b) * L + t) * H + 2 * pair + hh]) : 0.0f;
-    };
-    float dt_next[2] = {load_dt(0, 0), load_dt(0, 1)};
     bool ok = true;
-    int p = 0;
     for (int c = 0;; ++c) {
       const int slot = c & (kSlots - 1);
-      PieceInfo* inf = info + slot;
-      // ---- decay prefix of both heads, piece length ----------------------
-      const float ell[2] = {ok ? dt_next[0] * Aa : 0.0f, ok ? dt_next[1] * Ab : 0.0f};
-      float lam[2], pmin[2], pmax[2];
-      piece_scan2(ell, lane, warp, red, 1, lam, pmin, pmax);
-      const bool live_tok = p + tk < L;
-      const unsigned bal0 = __ballot_sync(0xffffffffu, live_tok && (pmax[0] - pmin[0]) <= kFactorRange);
-      const unsigned bal1 = __ballot_sync(0xffffffffu, live_tok && (pmax[1] - pmin[1]) <= kFactorRange);
-      if (lane == 0) {
-        nred[warp] = __popc(bal0);
-        nred[4 + warp] = __popc(bal1);
-      }
-      role_sync(1, kPT);
-      int n = min(nred[0] + nred[1] + nred[2] + nred[3], nred[4] + nred[5] + nred[6] + nred[7]);
-      n = max(n, 1);  // token 0 always qualifies while p < L
-      const bool last = p + n >= L;
-      if (!last) {
-        dt_next[0] = load_dt(p + n, 0);
-        dt_next[1] = load_dt(p + n, 1);
-      }
-      // ---- publish the piece descriptor ----------------------------------
-      if (ok && c >= kSlots) ok = ctl.wait(BAR_INFO_FREE + slot, uint32_t(((c / kSlots) - 1) & 1));
-      inf->lam[0][tk] = lam[0];
-      inf->lam[1][tk] = lam[1];
-      if (tk == n - 1) {
+      const PieceInfo* inf = info + slot;
+      // ---- the piece descriptor (start, length, decay prefix) -------------
+      if (ok) ok = ctl.wait(BAR_INFO_FULL + slot, uint32_t((c / kSlots) & 1));
+      const int p = inf->start, n = ok ? inf->n : 1;
+      const bool last = !ok || inf->last != 0;
+      // ---- per head: inputs, x' = g x hi/lo values ------------------------
+      uint32_t hw2[2][NT][4], lw2[2][NT][4];  // both heads' values, stored together
 #pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          inf->R[h2] = 0.5f * (pmin[h2] + pmax[h2]);
-          inf->lend[h2] = lam[h2];
-        }
-      }
-      if (tid == 0) {
-        inf->start = p;
-        inf->n = n;
-        inf->last = last ? 1 : 0;
-      }
-      role_sync(1, kPT);
-      mbar_arrive(ctl.bar(BAR_INFO_FULL + slot));
-      // ---- per head: inputs, x' = g x hi/lo tiles ------------------------
-#pragma unroll 1
       for (int hs = 0; hs < 2; ++hs) {
         const int head = 2 * pair + hs;
+        const int nv = ok ? min(NT, max(0, n - tb)) : 0;  // live tokens of this thread
         const float R = inf->R[hs];
-        uint32_t hw[NT][4], lw[NT][4];
-        const int xu = 2 * c + hs;  // use of the x' tile pair
-        if (FUSED) {
+        // x' = g_s x with g_s = exp(R - Lam_s), 0 for dead tokens
+        float gv[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+          gv[j] = j < nv ? ex2f((R - inf->lam[hs][tb + j]) * kLog2e) : 0.0f;
+        uint32_t(&hw)[NT][4] = hw2[hs];
+        uint32_t(&lw)[NT][4] = lw2[hs];
+        if constexpr (!FUSED) {
+          const int64_t rowbase = int64_t(b) * L * D + int64_t(head) * kP + 8 * q;
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int pc = min(p + tb + j, L - 1);
+            const TX* row = x + rowbase + int64_t(pc) * D;
+            float v[8];
+            if constexpr (sizeof(TX) == 4) {
+              const float4 v0 = __ldg(reinterpret_cast<const float4*>(row));
+              const float4 v1 = __ldg(reinterpret_cast<const float4*>(row) + 1);
+              v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+              v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+            } else {
+              const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(row));
+              const uint32_t w4[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(w4[i] << 16);
+                v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              split_pair(mul2(pk2(v[2 * k], v[2 * k + 1]), pk2(gv[j], gv[j])), hw[j][k], lw[j][k]);
+          }
+        } else {
           const int su = 2 * c + hs;  // staging use
           if (ok) ok = ctl.wait(BAR_XS_FULL, uint32_t(su & 1));
           if (ok) xs_landed = su + 1;
-        }
-#pragma unroll 1
-        for (int rd = 0; rd < 2; ++rd) {
-          const int g4 = (tid >> 3) + 16 * rd;
-          const int tb = 4 * g4;                            // first token (in the piece)
-          const int nv = ok ? min(NT, max(0, n - tb)) : 0;  // live tokens
-          // x' = g_s x with g_s = exp(R - Lam_s), 0 for dead tokens
-          float gv[NT];
+          // staged rows tb + i = positions p + tb - 3 + i
+          uint4 xr[NR];
 #pragma unroll
-          for (int j = 0; j < NT; ++j)
-            gv[j] = j < nv ? ex2f((R - inf->lam[hs][tb + j]) * kLog2e) : 0.0f;
-          if constexpr (!FUSED) {
-            const int64_t rowbase = int64_t(b) * L * D + int64_t(head) * kP + 8 * q;
+          for (int i = 0; i < NR; ++i)
+            xr[i] = *reinterpret_cast<const uint4*>(sm + kOffXs + sw128(tb + i, q));
+          if (p == 0 && tb < kMaxK - 1 && nv > 0) {
+            // positions < 0: the conv state S (zeros without one)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              const int pc = min(p + tb + j, L - 1);
-              const TX* row = x + rowbase + int64_t(pc) * D;
-              float v[8];
-              if constexpr (sizeof(TX) == 4) {
-                const float4 v0 = __ldg(reinterpret_cast<const float4*>(row));
-                const float4 v1 = __ldg(reinterpret_cast<const float4*>(row) + 1);
-                v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
-                v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
-              } else {
-                const uint4 r4 = __ldg(reinterpret_cast<const uint4*>(row));
-                const uint32_t w4[4] = {r4.x, r4.y, r4.z, r4.w};
+            for (int i = 0; i < kMaxK - 1; ++i) {
+              const int pos = tb - (kMaxK - 1) + i;
+              if (pos < 0) {
+                uint32_t w4[4] = {0u, 0u, 0u, 0u};
+                if (conv_s_in && pos >= -(K - 1)) {
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  v[2 * i] = __uint_as_float(w4[i] << 16);
-                  v[2 * i + 1] = __uint_as_float(w4[i] & 0xFFFF0000u);
-                }
-              }
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                split_pair(mul2(pk2(v[2 * k], v[2 * k + 1]), pk2(gv[j], gv[j])), hw[j][k], lw[j][k]);
-            }
-          } else {
-            // staged rows tb + i = positions p + tb - 3 + i
-            uint4 xr[NR];
-#pragma unroll
-            for (int i = 0; i < NR; ++i)
-              xr[i] = *reinterpret_cast<const uint4*>(sm + kOffXs + sw128(tb + i, q));
-            if (p == 0 && tb < kMaxK - 1 && nv > 0) {
-              // positions < 0: the conv state S (zeros without one)
-#pragma unroll
-              for (int i = 0; i < kMaxK - 1; ++i) {
-                const int pos = tb - (kMaxK - 1) + i;
-                if (pos < 0) {
-                  uint32_t w4[4] = {0u, 0u, 0u, 0u};
-                  if (conv_s_in && pos >= -(K - 1)) {
-#pragma unroll
-                    for (int i2 = 0; i2 < 4; ++i2) {
-                      const int64_t d0 = int64_t(b) * D + int64_t(head) * kP + 8 * q + 2 * i2;
-                      const uint16_t lo = *reinterpret_cast<const uint16_t*>(&conv_s_in[d0 * (K - 1) + (K - 1) + pos]);
-                      const uint16_t hi = *reinterpret_cast<const uint16_t*>(&conv_s_in[(d0 + 1) * (K - 1) + (K - 1) + pos]);
-                      w4[i2] = pack2(lo, hi);
-                    }
+                  for (int i2 = 0; i2 < 4; ++i2) {
+                    const int64_t d0 = int64_t(b) * D + int64_t(head) * kP + 8 * q + 2 * i2;
+                    const uint16_t lo = *reinterpret_cast<const uint16_t*>(&conv_s_in[d0 * (K - 1) + (K - 1) + pos]);
+                    const uint16_t hi = *reinterpret_cast<const uint16_t*>(&conv_s_in[(d0 + 1) * (K - 1) + (K - 1) + pos]);
+                    w4[i2] = pack2(lo, hi);
                   }
-                  xr[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
                 }
-              }
-            }
-            if (rd == 1) {
-              // every producer has its rows in registers (the empty asm reads
-              // them, so each load has returned before the barrier): stage the
-              // next head's (or piece's) rows, the TMA write ordered after the
-              // generic-proxy reads by the proxy fence
-#pragma unroll
-              for (int i = 0; i < NR; ++i)
-                asm volatile("" ::"r"(xr[i].x), "r"(xr[i].y), "r"(xr[i].z), "r"(xr[i].w) : "memory");
-              role_sync(1, kPT);
-              if (tid == 0 && ok) {
-                fence_proxy_async_smem();
-                if (hs == 0) {
-                  stage_x(p, 1);
-                  xs_issued = 2 * c + 2;
-                } else if (!last) {
-                  stage_x(p + n, 0);
-                  xs_issued = 2 * c + 3;
-                }
-              }
-            }
-            // channel pair by channel pair: conv, SiLU, g, split, two channels
-            // per packed fp32 operation
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-              const float* sw = reinterpret_cast<const float*>(misc + kMiW) + ((hs * 4 + e2) * 8 + q) * 12;
-              const float4 w01 = *reinterpret_cast<const float4*>(sw);
-              const float4 w23 = *reinterpret_cast<const float4*>(sw + 4);
-              const float2 bb = *reinterpret_cast<const float2*>(sw + 8);
-              const uint64_t wk[4] = {pk2(w01.x, w01.y), pk2(w01.z, w01.w), pk2(w23.x, w23.y),
-                                      pk2(w23.z, w23.w)};
-              uint64_t xv[NR];
-#pragma unroll
-              for (int i = 0; i < NR; ++i) {
-                const uint32_t wv = e2 == 0 ? xr[i].x : e2 == 1 ? xr[i].y : e2 == 2 ? xr[i].z : xr[i].w;
-                xv[i] = bf2_to_f2(wv);
-              }
-#pragma unroll
-              for (int j = 0; j < NT; ++j) {
-                uint64_t z = pk2(bb.x, bb.y);
-#pragma unroll
-                for (int k = 0; k < kMaxK; ++k) z = fma2(wk[k], xv[j + k], z);
-                split_pair(silu_scaled2(z, gv[j]), hw[j][e2], lw[j][e2]);
+                xr[i] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
               }
             }
           }
-          // the tile pair is free once the previous use's products are done
-          if (rd == 0 && ok && xu >= 1) ok = ctl.wait(BAR_X_FREE, uint32_t((xu - 1) & 1));
-          if (ok) {
+          // channel pair by channel pair: conv, SiLU, g, split, two channels
+          // per packed fp32 operation
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            const float* sw = reinterpret_cast<const float*>(misc + kMiW) + ((hs * 4 + e2) * 8 + q) * 12;
+            const float4 w01 = *reinterpret_cast<const float4*>(sw);
+            const float4 w23 = *reinterpret_cast<const float4*>(sw + 4);
+            const float2 bb = *reinterpret_cast<const float2*>(sw + 8);
+            const uint64_t wk[4] = {pk2(w01.x, w01.y), pk2(w01.z, w01.w), pk2(w23.x, w23.y),
+                                    pk2(w23.z, w23.w)};
+            uint64_t xv[NR];
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+              const uint32_t wv = e2 == 0 ? xr[i].x : e2 == 1 ? xr[i].y : e2 == 2 ? xr[i].z : xr[i].w;
+              xv[i] = bf2_to_f2(wv);
+            }
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
-              *reinterpret_cast<uint4*>(sm + kOffX + sw128(tb + j, q)) =
-                  make_uint4(hw[j][0], hw[j][1], hw[j][2], hw[j][3]);
-              *reinterpret_cast<uint4*>(sm + kOffX + 16384 + sw128(tb + j, q)) =
-                  make_uint4(lw[j][0], lw[j][1], lw[j][2], lw[j][3]);
+              uint64_t z = pk2(bb.x, bb.y);
+#pragma unroll
+              for (int k = 0; k < kMaxK; ++k) z = fma2(wk[k], xv[j + k], z);
+              split_pair(silu_scaled2(z, gv[j]), hw[j][e2], lw[j][e2]);
             }
           }
-        }
-        if (ok) {
-          fence_proxy_async_smem();
-          mbar_arrive(ctl.bar(BAR_X_FULL));
+          // every staged row was used above, so each load has returned:
+          // release the buffer to the next head's (or piece's) rows, the TMA
+          // write ordered after the generic-proxy reads by the proxy fence
+          role_sync(3, kPT);
+          if (tid == 0 && ok) {
+            fence_proxy_async_smem();
+            if (hs == 0) {
+              stage_x(p, 1);
+              xs_issued = su + 2;
+            } else if (!last) {
+              stage_x(p + n, 0);
+              xs_issued = su + 2;
+            }
+          }
         }
       }
+      mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));  // done with the descriptor
+      // the x' tiles are free once the previous piece's S' and Yd are done
+      if (ok && c >= 1) ok = ctl.wait(BAR_X_FREE, uint32_t((c - 1) & 1));
+      if (ok) {
+#pragma unroll
+        for (int hs = 0; hs < 2; ++hs) {
+          uint8_t* xt = sm + kOffX + 16384u * hs;
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            *reinterpret_cast<uint4*>(xt + sw128(tb + j, q)) =
+                make_uint4(hw2[hs][j][0], hw2[hs][j][1], hw2[hs][j][2], hw2[hs][j][3]);
+            *reinterpret_cast<uint4*>(xt + 32768 + sw128(tb + j, q)) =
+                make_uint4(lw2[hs][j][0], lw2[hs][j][1], lw2[hs][j][2], lw2[hs][j][3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(ctl.bar(BAR_X_FULL));
+      }
       if (last) break;
-      p += n;
     }
     if (FUSED && tid == 0) {  // staged tiles still in flight
       for (int su = xs_landed; su < xs_issued; ++su)
@@ -503,8 +406,8 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     if constexpr (FUSED) {
       // final conv state F_j = ext[L + j] of both heads' channels; every read
       // of S happened in piece 0
-      role_sync(1, kPT);
-      if (conv_s_out && !*ctl.abort) {
+      role_sync(3, kPT);
+      if (conv_s_out && tid < 2 * kP && !*ctl.abort) {
         const int64_t d = int64_t(2 * pair) * kP + tid;
         TX f[kMaxK - 1];
         for (int j = 0; j < K - 1; ++j) {
@@ -517,44 +420,54 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       }
     }
   } else if (warp < kIssuerWarp) {
-    // ===== consumers: head hs, TMEM lanes of quarter q (row t = state row n = r) =====
-    const int cw = warp - kConsWarp0;
+    // ===== consumers: TMEM lanes of quarter q (row t = state row n = r), both heads =====
     const int q = warp & 3;  // == warp % 4: the TMEM lane quarter this warp may access
-    const int hs = cw >> 2;
     const int r = 32 * q + lane;
-    const int head = 2 * pair + hs;
     const uint32_t tl = tm + (uint32_t(q * 32) << 16);
-    const uint32_t colY = kColY + 64u * hs, colS = kColS + 64u * hs;
-    float hreg[kP];
-    const int64_t hoff = (int64_t(b) * H + head) * kP * kN;
-#pragma unroll
-    for (int pp = 0; pp < kP; ++pp) hreg[pp] = h0 ? h0[hoff + int64_t(pp) * kN + r] : 0.0f;
-    {  // blocks of G o causal above the diagonal of this quarter stay zero
-      uint32_t z[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) z[i] = 0u;
-      for (int j = 2 * hs; j < 2 * hs + 2; ++j) {
-        if (j > q) {
-          tmem_st_x16(tl + kColGh + 16u * j, z);
-          tmem_st_x16(tl + kColGl + 16u * j, z);
-        }
-      }
-      tmem_st_wait();
-    }
-    uint8_t* htile = sm + kOffH;
+    const int64_t hoff0 = (int64_t(b) * H + 2 * pair) * kP * kN;  // head a; head b + kP * kN
     // every wait is followed by a warp vote, so the warp leaves the loop
     // together (its TMEM accesses are warp-collective)
     auto wait_all = [&](int bar, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, ctl.wait(bar, parity));
     };
-    bool ok = true;
-    if (hs == 0) {  // h' for Yo_a of piece 0: e^{R_0} h0
-      ok = wait_all(BAR_INFO_FULL, 0u);
-      if (ok) {
-        write_split_row(htile, htile + 16384, r, hreg, expf(info[0].R[0]));
-        fence_proxy_async_smem();
-        mbar_arrive(ctl.bar(BAR_H_FULL));
+    // h' tiles of both heads for the next Yo: hi/lo split of e^{R} h, h read
+    // back from the state columns
+    auto write_h = [&](float e0, float e1) {
+#pragma unroll 1
+      for (int hs = 0; hs < 2; ++hs) {
+        float v[kP];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t w[16];
+          tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, w);
+#pragma unroll
+          for (int pp = 0; pp < 16; ++pp) v[16 * qq + pp] = __uint_as_float(w[pp]);
+        }
+        uint8_t* ht = sm + kOffH + 16384u * hs;
+        write_split_row(ht, ht + 32768, r, v, hs == 0 ? e0 : e1);
       }
+    };
+    // the initial state h0 into the state columns, e^{R_0} h0 into the h'
+    // tiles (the operand of Yo for piece 0)
+    bool ok = wait_all(BAR_INFO_FULL, 0u);
+    if (ok) {
+#pragma unroll 1
+      for (int hs = 0; hs < 2; ++hs) {
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t w[16];
+#pragma unroll
+          for (int pp = 0; pp < 16; ++pp) {
+            const int pc = 16 * qq + pp;
+            w[pp] = __float_as_uint(h0 ? h0[hoff0 + int64_t(hs) * kP * kN + int64_t(pc) * kN + r] : 0.0f);
+          }
+          tmem_st_x16(tl + kColH + 64u * hs + 16u * qq, w);
+        }
+      }
+      tmem_st_wait();
+      write_h(expf(info[0].R[0]), expf(info[0].R[1]));
+      fence_proxy_async_smem();
+      mbar_arrive(ctl.bar(BAR_H_FULL));
     }
     for (int c = 0; ok; ++c) {
       const int slot = c & (kSlots - 1);
@@ -562,69 +475,82 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       if (!(ok = wait_all(BAR_INFO_FULL + slot, uint32_t((c / kSlots) & 1)))) break;
       const int n = inf->n, start = inf->start;
       const bool last = inf->last != 0;
-      const float R = inf->R[hs], lend = inf->lend[hs], lam_t = inf->lam[hs][r];
-      // ---- mask share: rows of quarter q, 32-column blocks 2hs, 2hs+1 ----
-      if (c >= 1 && !(ok = wait_all(BAR_GM_FREE, uint32_t((c - 1) & 1)))) break;
+      // ---- causal mask of this quarter's rows of G, split in place --------
       if (!(ok = wait_all(BAR_G_FULL, uint32_t(c & 1)))) break;
       tc_fence_after();
-      for (int j = 2 * hs; j <= min(q, 2 * hs + 1); ++j) {
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
-          const int s0 = 32 * j + 16 * hf;
-          uint32_t graw[16], ph[8], pl[8];
-          tmem_ld_x16(tl + kColG + uint32_t(s0), graw);
-          float m[16];
+      for (int j = 0; j < 4; ++j) {
+        uint32_t ph[16], pl[16];
+        if (j <= q) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(graw[i]);
-          if (j == q) {  // diagonal block: s = s0 + i <= t = 32 q + lane
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t graw[16];
+            tmem_ld_x16(tl + kColG + uint32_t(32 * j + 16 * hf), graw);
+            float m[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
+            for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(graw[i]);
+            if (j == q) {  // diagonal block: s = 32 j + 16 hf + i <= t = 32 q + lane
+#pragma unroll
+              for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[8 * hf + i], pl[8 * hf + i]);
           }
+        } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[i], pl[i]);
-          tmem_st_x8(tl + kColGh + uint32_t(s0 / 2), ph);
-          tmem_st_x8(tl + kColGl + uint32_t(s0 / 2), pl);
+          for (int i = 0; i < 16; ++i) ph[i] = pl[i] = 0u;
         }
+        // the block's 32 fp32 columns were read above: write its hi pairs
+        // over the first 16 and its lo pairs over the last 16
+        tmem_st_x16(tl + kColG + uint32_t(32 * j), ph);
+        tmem_st_x16(tl + kColG + uint32_t(32 * j + 16), pl);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ctl.bar(BAR_GM_FULL));
-      // ---- head b: h' = e^{R_c} h_{c-1} for Yo_b(c), once Yo_a(c) has read the tiles
-      if (hs == 1) {
-        if (!(ok = wait_all(BAR_H_FREE + 0, uint32_t(c & 1)))) break;  // Yo_a(c) is done
-        write_split_row(htile, htile + 16384, r, hreg, expf(R));
-        fence_proxy_async_smem();
-        mbar_arrive(ctl.bar(BAR_H_FULL + 1));
-      }
-      // ---- state carry: row n = r ---------------------------------------
-      if (!(ok = wait_all(BAR_S_FULL + hs, uint32_t(c & 1)))) break;
+      // ---- state carry: h_end = e^{Lam_end} h + e^{Lam_end - R} S' ---------
+      if (!(ok = wait_all(BAR_S_FULL, uint32_t(c & 1)))) break;
       tc_fence_after();
-      {
-        const float dec_end = expf(lend), s_scale = expf(lend - R);
+#pragma unroll 1
+      for (int hs = 0; hs < 2; ++hs) {
+        const float dec_end = expf(inf->lend[hs]);
+        const float s_scale = expf(inf->lend[hs] - inf->R[hs]);
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
-          uint32_t r0[16];
-          tmem_ld_x16(tl + colS + 16u * qq, r0);
+          uint32_t sv[16], hv[16];
+          tmem_ld_x16(tl + kColS + 64u * hs + 16u * qq, sv);
+          tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, hv);
 #pragma unroll
           for (int pp = 0; pp < 16; ++pp)
-            hreg[16 * qq + pp] = fmaf(dec_end, hreg[16 * qq + pp], s_scale * __uint_as_float(r0[pp]));
+            hv[pp] = __float_as_uint(fmaf(dec_end, __uint_as_float(hv[pp]), s_scale * __uint_as_float(sv[pp])));
+          tmem_st_x16(tl + kColH + 64u * hs + 16u * qq, hv);
         }
       }
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ctl.bar(BAR_S_FREE + hs));
-      // ---- y rows: y_t = f_t Y_t ---------------------------------------------
-      if (!(ok = wait_all(BAR_Y_FULL + hs, uint32_t(c & 1)))) break;
+      mbar_arrive(ctl.bar(BAR_S_FREE));
+      if (!last) {  // h' tiles of the next piece, once Yo(c) has read these
+        const int slot1 = (c + 1) & (kSlots - 1);
+        if (!(ok = wait_all(BAR_INFO_FULL + slot1, uint32_t(((c + 1) / kSlots) & 1)))) break;
+        if (!(ok = wait_all(BAR_H_FREE, uint32_t(c & 1)))) break;
+        write_h(expf(info[slot1].R[0]), expf(info[slot1].R[1]));
+        fence_proxy_async_smem();
+        mbar_arrive(ctl.bar(BAR_H_FULL));
+      }
+      // ---- y rows of both heads: y_t = f_t Y_t --------------------------------
+      if (!(ok = wait_all(BAR_Y_FULL, uint32_t(c & 1)))) break;
       tc_fence_after();
-      {
-        const float f_t = expf(lam_t - R);
-        TY* yrow = y + (int64_t(b) * L + start + r) * D + int64_t(head) * kP;
+#pragma unroll 1
+      for (int hs = 0; hs < 2; ++hs) {
+        const float f_t = expf(inf->lam[hs][r] - inf->R[hs]);
+        TY* yrow = y + (int64_t(b) * L + start + r) * D + int64_t(2 * pair + hs) * kP;
 #pragma unroll
         for (int qq = 0; qq < 4; ++qq) {
           uint32_t a0[16];
-          tmem_ld_x16(tl + colY + 16u * qq, a0);
-          if (qq == 3) {  // Y is read: the next piece's products may start
+          tmem_ld_x16(tl + kColY + 64u * hs + 16u * qq, a0);
+          if (hs == 1 && qq == 3) {  // Y is read: the next piece's Yo may start
             tc_fence_before();
-            mbar_arrive(ctl.bar(BAR_Y_FREE + hs));
+            mbar_arrive(ctl.bar(BAR_Y_FREE));
           }
           float yv[16];
 #pragma unroll
@@ -634,115 +560,245 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       }
       mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
       if (last) break;
-      // ---- head a: h' = e^{R_{c+1}} h_c for Yo_a(c+1), once Yo_b(c) is done
-      if (hs == 0) {
-        const int slot1 = (c + 1) & (kSlots - 1);
-        if (!(ok = wait_all(BAR_INFO_FULL + slot1, uint32_t(((c + 1) / kSlots) & 1)))) break;
-        if (!(ok = wait_all(BAR_H_FREE + 1, uint32_t(c & 1)))) break;  // Yo_b(c) is done
-        write_split_row(htile, htile + 16384, r, hreg, expf(info[slot1].R[0]));
-        fence_proxy_async_smem();
-        mbar_arrive(ctl.bar(BAR_H_FULL));
-      }
     }
     if (ok && !*ctl.abort && hT) {
+#pragma unroll 1
+      for (int hs = 0; hs < 2; ++hs) {
 #pragma unroll
-      for (int pp = 0; pp < kP; ++pp) hT[hoff + int64_t(pp) * kN + r] = hreg[pp];
+        for (int qq = 0; qq < 4; ++qq) {
+          uint32_t a0[16];
+          tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, a0);
+#pragma unroll
+          for (int pp = 0; pp < 16; ++pp)
+            hT[hoff0 + int64_t(hs) * kP * kN + int64_t(16 * qq + pp) * kN + r] = __uint_as_float(a0[pp]);
+        }
+      }
     }
-  } else {
+  } else if (warp == kIssuerWarp) {
     if (lane == 0) {
       // ========================= issuer (one thread) =========================
-      auto tma_bc = [&](int start, int st) {
-        const uint32_t base = sb + kOffBC + uint32_t(st) * 65536u;
-        const uint32_t bar = ctl.bar(BAR_BC_FULL + st);
-        mbar_arrive_expect_tx(bar, 65536u);
-        tma_load_3d(base, &tmC, g * kN, start, b, bar);
-        tma_load_3d(base + 16384, &tmC, g * kN + 64, start, b, bar);
-        tma_load_3d(base + 32768, &tmB, g * kN, start, b, bar);
-        tma_load_3d(base + 49152, &tmB, g * kN + 64, start, b, bar);
+      const uint32_t cb = sb + kOffC, bb = sb + kOffB, xb = sb + kOffX, hb = sb + kOffH;
+      auto tma_c = [&](int start) {
+        const uint32_t bar = ctl.bar(BAR_C_FULL);
+        mbar_arrive_expect_tx(bar, 32768u);
+        tma_load_3d(cb, &tmC, g * kN, start, b, bar);
+        tma_load_3d(cb + 16384, &tmC, g * kN + 64, start, b, bar);
+      };
+      auto tma_b = [&](int start) {
+        const uint32_t bar = ctl.bar(BAR_B_FULL);
+        mbar_arrive_expect_tx(bar, 32768u);
+        tma_load_3d(bb, &tmB, g * kN, start, b, bar);
+        tma_load_3d(bb + 16384, &tmB, g * kN + 64, start, b, bar);
       };
       prefetch_tmap(&tmB);
       prefetch_tmap(&tmC);
-      tma_bc(0, 0);
-      int tma_issued = 1, tma_landed = 0;
+      tma_c(0);
+      tma_b(0);
+      int c_issued = 1, c_landed = 0, b_issued = 1, b_landed = 0;
       for (int c = 0;; ++c) {
-        const int st = c & 1, slot = c & (kSlots - 1);
+        const int slot = c & (kSlots - 1);
         if (!ctl.wait(BAR_INFO_FULL + slot, uint32_t((c / kSlots) & 1))) break;
         const int start = info[slot].start, n = info[slot].n;
         const bool last = info[slot].last != 0;
         mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
-        if (!last) {  // the next piece's B and C into the other stage
-          if (c >= 1 && !ctl.wait(BAR_BC_FREE + (st ^ 1), uint32_t(((c - 1) >> 1) & 1))) break;
-          tma_bc(start + n, st ^ 1);
-          tma_issued = c + 2;
-        }
-        if (!ctl.wait(BAR_BC_FULL + st, uint32_t((c >> 1) & 1))) break;
-        tma_landed = c + 1;
-        const uint32_t cb = sb + kOffBC + uint32_t(st) * 65536u, bb = cb + 32768u;
+        // G = C B^T once this piece's B and C are in and Yd(c-1) has read the
+        // masked split that G overwrites
+        if (!ctl.wait(BAR_C_FULL, uint32_t(c & 1))) break;
+        c_landed = c + 1;
+        if (!ctl.wait(BAR_B_FULL, uint32_t(c & 1))) break;
+        b_landed = c + 1;
+        if (c >= 1 && !ctl.wait(BAR_YD_DONE, uint32_t((c - 1) & 1))) break;
         tc_fence_after();
-        // G = C B^T (mask(c-1) has read G(c-1): Yd_a(c-1) waited for it)
-#pragma unroll
+#pragma unroll 1
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tm + kColG, kdesc(cb, kk, 16384), kdesc(bb, kk, 16384), kIdG, kk);
         mma_commit(ctl.bar(BAR_G_FULL));
-        bool good = true;
-#pragma unroll 1
-        for (int hs = 0; hs < 2 && good; ++hs) {
-          const uint32_t dY = tm + kColY + 64u * hs, dS = tm + kColS + 64u * hs;
-          // Yo = C (e^R h)^T starts the Y accumulator, once the h' tiles are
-          // written and the previous y rows are read
-          good = ctl.wait(BAR_H_FULL + hs, uint32_t(c & 1));
-          if (good && c >= 1) good = ctl.wait(BAR_Y_FREE + hs, uint32_t((c - 1) & 1));
-          if (!good) break;
-          tc_fence_after();
+        if (!last) {  // warm L2 with the next piece's B and C
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(dY, kdesc(cb, kk, 16384), mndesc(sb + kOffH, kk), kIdYo, kk);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(dY, kdesc(cb, kk, 16384), mndesc(sb + kOffH + 16384, kk), kIdYo, 1);
-          mma_commit(ctl.bar(BAR_H_FREE + hs));
-          // S' = B^T (x'hi + x'lo) once the x' tiles are in and the previous
-          // carry has read S'
-          good = ctl.wait(BAR_X_FULL, uint32_t(hs));  // completion 2c + hs
-          if (good && c >= 1) good = ctl.wait(BAR_S_FREE + hs, uint32_t((c - 1) & 1));
-          if (!good) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(dS, sdesc_sw128(bb + kk * 2048, 16384, 1024), mndesc(sb + kOffX, kk), kIdS, kk);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ss(dS, sdesc_sw128(bb + kk * 2048, 16384, 1024), mndesc(sb + kOffX + 16384, kk),
-                   kIdS, 1);
-          mma_commit(ctl.bar(BAR_S_FULL + hs));
-          if (hs == 1) mma_commit(ctl.bar(BAR_BC_FREE + st));
-          // Yd = hi(G o c) x'hi + hi(G o c) x'lo + lo(G o c) x'hi onto Y
-          if (hs == 0) good = ctl.wait(BAR_GM_FULL, uint32_t(c & 1));
-          if (!good) break;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(dY, tm + kColGh + 8u * kk, mndesc(sb + kOffX, kk), kIdYd, 1);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(dY, tm + kColGh + 8u * kk, mndesc(sb + kOffX + 16384, kk), kIdYd, 1);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(dY, tm + kColGl + 8u * kk, mndesc(sb + kOffX, kk), kIdYd, 1);
-          mma_commit(ctl.bar(BAR_Y_FULL + hs));
-          mma_commit(ctl.bar(BAR_X_FREE));
-          if (hs == 1) mma_commit(ctl.bar(BAR_GM_FREE));
+          for (int hh = 0; hh < 2; ++hh) {
+            tma_prefetch_3d(&tmC, g * kN + 64 * hh, start + n, b);
+            tma_prefetch_3d(&tmB, g * kN + 64 * hh, start + n, b);
+          }
         }
-        if (!good || last) break;
+        // S' = B^T [x'_a | x'_b] (hi + lo), once the x' tiles are in and the
+        // previous carry has read S'
+        if (!ctl.wait(BAR_X_FULL, uint32_t(c & 1))) break;
+        if (c >= 1 && !ctl.wait(BAR_S_FREE, uint32_t((c - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tm + kColS, sdesc_sw128(bb + kk * 2048, 16384, 1024), mndesc(xb, kk), kIdS, kk);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(tm + kColS, sdesc_sw128(bb + kk * 2048, 16384, 1024), mndesc(xb + 32768, kk), kIdS, 1);
+        mma_commit(ctl.bar(BAR_S_FULL));
+        mma_commit(ctl.bar(BAR_B_FREE));
+        // Y_ab = C [e^R h_a | e^R h_b]^T (hi + lo) starts Y, once the h' tiles
+        // are written and the previous piece's y rows are read
+        const uint32_t dY = tm + kColY;
+        if (!ctl.wait(BAR_H_FULL, uint32_t(c & 1))) break;
+        if (c >= 1 && !ctl.wait(BAR_Y_FREE, uint32_t((c - 1) & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(dY, kdesc(cb, kk, 16384), mndesc(hb, kk), kIdYo, kk);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ss(dY, kdesc(cb, kk, 16384), mndesc(hb + 32768, kk), kIdYo, 1);
+        mma_commit(ctl.bar(BAR_H_FREE));
+        mma_commit(ctl.bar(BAR_C_FREE));
+        // Y_ab += hi(G o c) x'hi + hi(G o c) x'lo + lo(G o c) x'hi; K step kk
+        // (tokens 16 kk ..) reads 32-column block kk / 2, half kk % 2
+        if (!ctl.wait(BAR_GM_FULL, uint32_t(c & 1))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(dY, tm + kColG + 32u * (kk >> 1) + 8u * (kk & 1), mndesc(xb, kk), kIdYd, 1);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(dY, tm + kColG + 32u * (kk >> 1) + 8u * (kk & 1), mndesc(xb + 32768, kk), kIdYd, 1);
+#pragma unroll 1
+        for (int kk = 0; kk < 8; ++kk)
+          mma_ts(dY, tm + kColG + 32u * (kk >> 1) + 16u + 8u * (kk & 1), mndesc(xb, kk), kIdYd, 1);
+        mma_commit(ctl.bar(BAR_Y_FULL));
+        mma_commit(ctl.bar(BAR_X_FREE));
+        mma_commit(ctl.bar(BAR_YD_DONE));
+        if (last) break;
+        // the next piece's B once S' has read this one, its C once Yo has
+        if (!ctl.wait(BAR_B_FREE, uint32_t(c & 1))) break;
+        tma_b(start + n);
+        b_issued = c + 2;
+        if (!ctl.wait(BAR_C_FREE, uint32_t(c & 1))) break;
+        tma_c(start + n);
+        c_issued = c + 2;
       }
-      // every MMA of this CTA (and TMA still in flight) lands before the
-      // tensor memory and shared memory are released
+      // every MMA (and a TMA still in flight) lands before the tensor memory
+      // and shared memory are released
       mma_commit(ctl.bar(BAR_DRAIN));
       mbar_wait(ctl.bar(BAR_DRAIN), 0, kWaitNs);
-      for (int i = tma_landed; i < tma_issued; ++i)
-        mbar_wait(ctl.bar(BAR_BC_FULL + (i & 1)), uint32_t((i >> 1) & 1), kWaitNs / 2);
+      for (int i = c_landed; i < c_issued; ++i)
+        mbar_wait(ctl.bar(BAR_C_FULL), uint32_t(i & 1), kWaitNs / 2);
+      for (int i = b_landed; i < b_issued; ++i)
+        mbar_wait(ctl.bar(BAR_B_FULL), uint32_t(i & 1), kWaitNs / 2);
     }
     __syncwarp();
+  } else {
+    // ============================ decay warp ============================
+    // lane l holds tokens 4l .. 4l+3 of the piece for both heads: the
+    // inclusive log-decay prefix Lam, its running min / max, the piece length
+    // (tokens while both heads' Lam range stays <= kFactorRange), and per head
+    // R = the middle of the range and Lam_end, published in the descriptor ring
+    const float Ah[2] = {A[2 * pair], A[2 * pair + 1]};
+    auto load_dt = [&](int start, float (&v)[2][4]) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = start + 4 * lane + i;
+          v[hh][i] = t < L ? __bfloat162float(dt[(int64_t(b) * L + t) * H + 2 * pair + hh]) : 0.0f;
+        }
+    };
+    float dtv[2][4];
+    load_dt(0, dtv);
+    bool ok = true;
+    int p = 0;
+    for (int c = 0;; ++c) {
+      const int slot = c & (kSlots - 1);
+      PieceInfo* inf = info + slot;
+      float lam[2][4], pmn[2][4], pmx[2][4];
+      int ngood[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float run = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          run += dtv[hh][i] * Ah[hh];
+          lam[hh][i] = run;
+        }
+        float incl = run;  // inclusive scan of the lanes' sums
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float nb = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += nb;
+        }
+        const float excl = incl - run;
+        float lmn = 3.0e38f, lmx = -3.0e38f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          lam[hh][i] += excl;
+          lmn = fminf(lmn, lam[hh][i]);
+          lmx = fmaxf(lmx, lam[hh][i]);
+          pmn[hh][i] = lmn;
+          pmx[hh][i] = lmx;
+        }
+        // min / max over the earlier lanes' tokens: exclusive warp scan
+        float smn = lmn, smx = lmx;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float a2 = __shfl_up_sync(0xffffffffu, smn, o);
+          const float c2 = __shfl_up_sync(0xffffffffu, smx, o);
+          if (lane >= o) {
+            smn = fminf(smn, a2);
+            smx = fmaxf(smx, c2);
+          }
+        }
+        float emn = __shfl_up_sync(0xffffffffu, smn, 1), emx = __shfl_up_sync(0xffffffffu, smx, 1);
+        if (lane == 0) {
+          emn = 3.0e38f;
+          emx = -3.0e38f;
+        }
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          pmn[hh][i] = fminf(pmn[hh][i], emn);
+          pmx[hh][i] = fmaxf(pmx[hh][i], emx);
+          const bool good = p + 4 * lane + i < L && (pmx[hh][i] - pmn[hh][i]) <= kFactorRange;
+          cnt += __popc(__ballot_sync(0xffffffffu, good));
+        }
+        ngood[hh] = cnt;
+      }
+      const int n = max(1, min(ngood[0], ngood[1]));  // token 0 always qualifies while p < L
+      const bool last = p + n >= L;
+      float dtn[2][4];
+      if (!last) load_dt(p + n, dtn);  // the next piece's dt, in flight during the publish
+      if (ok && c >= kSlots) ok = ctl.wait(BAR_INFO_FREE + slot, uint32_t(((c / kSlots) - 1) & 1));
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        *reinterpret_cast<float4*>(&inf->lam[hh][4 * lane]) =
+            make_float4(lam[hh][0], lam[hh][1], lam[hh][2], lam[hh][3]);
+      // token n-1: lane (n-1) / 4, slot (n-1) % 4
+      const int src = (n - 1) >> 2, idx = (n - 1) & 3;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        float mn = pmn[hh][0], mx = pmx[hh][0], le = lam[hh][0];
+#pragma unroll
+        for (int i = 1; i < 4; ++i)
+          if (idx == i) {
+            mn = pmn[hh][i];
+            mx = pmx[hh][i];
+            le = lam[hh][i];
+          }
+        const float R = __shfl_sync(0xffffffffu, 0.5f * (mn + mx), src);
+        const float lend = __shfl_sync(0xffffffffu, le, src);
+        if (lane == 0) {
+          inf->R[hh] = R;
+          inf->lend[hh] = lend;
+        }
+      }
+      if (lane == 0) {
+        inf->start = p;
+        inf->n = n;
+        inf->last = last ? 1 : 0;
+      }
+      __syncwarp();
+      mbar_arrive(ctl.bar(BAR_INFO_FULL + slot));
+      if (last) break;
+      p += n;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dtv[hh][i] = dtn[hh][i];
+    }
   }
   tc_fence_before();
   __syncthreads();
