@@ -49,6 +49,16 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t base, int kk) {
   return sdesc_sw128(base + uint32_t(kk) * 2048u, 16384, 1024);
 }
 
+// The same K steps as additions to a base descriptor (start address in
+// 16-byte units in the low 14 bits; shared addresses stay below 256 KB, so the
+// sum never carries into the next field).  With the step a compile-time
+// constant the issuing thread spends one 64-bit add per MMA instead of
+// rebuilding the descriptor, which otherwise costs more than the MMA itself.
+__host__ __device__ constexpr uint64_t kstep(int kk, uint32_t blk) {
+  return uint64_t((uint32_t(kk >> 2) * blk + uint32_t(kk & 3) * 32u) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnstep(int kk) { return uint64_t(kk) * 128u; }
+
 // Row `r` (64 fp32 values, times `scale`) -> hi and lo bf16 rows of two
 // MN-major tiles.
 __device__ __forceinline__ void write_split_row(uint8_t* hi_tile, uint8_t* lo_tile, int r,

@@ -578,6 +578,12 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     if (lane == 0) {
       // ========================= issuer (one thread) =========================
       const uint32_t cb = sb + kOffC, bb = sb + kOffB, xb = sb + kOffX, hb = sb + kOffH;
+      // base descriptors; every K step below adds a constant to them
+      const uint64_t dC = sdesc_sw128(cb, 16, 1024), dBk = sdesc_sw128(bb, 16, 1024);
+      const uint64_t dBm = sdesc_sw128(bb, 16384, 1024);
+      const uint64_t dXh = sdesc_sw128(xb, 16384, 1024), dXl = sdesc_sw128(xb + 32768, 16384, 1024);
+      const uint64_t dHh = sdesc_sw128(hb, 16384, 1024), dHl = sdesc_sw128(hb + 32768, 16384, 1024);
+      const uint32_t tG = tm + kColG, tS = tm + kColS, dY = tm + kColY;
       auto tma_c = [&](int start) {
         const uint32_t bar = ctl.bar(BAR_C_FULL);
         mbar_arrive_expect_tx(bar, 32768u);
@@ -609,9 +615,9 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         b_landed = c + 1;
         if (c >= 1 && !ctl.wait(BAR_YD_DONE, uint32_t((c - 1) & 1))) break;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tm + kColG, kdesc(cb, kk, 16384), kdesc(bb, kk, 16384), kIdG, kk);
+          mma_ss(tG, dC + kstep(kk, 16384), dBk + kstep(kk, 16384), kIdG, kk);
         mma_commit(ctl.bar(BAR_G_FULL));
         if (!last) {  // warm L2 with the next piece's B and C
 #pragma unroll
@@ -625,41 +631,36 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         if (!ctl.wait(BAR_X_FULL, uint32_t(c & 1))) break;
         if (c >= 1 && !ctl.wait(BAR_S_FREE, uint32_t((c - 1) & 1))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tm + kColS, sdesc_sw128(bb + kk * 2048, 16384, 1024), mndesc(xb, kk), kIdS, kk);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tm + kColS, sdesc_sw128(bb + kk * 2048, 16384, 1024), mndesc(xb + 32768, kk), kIdS, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS, dBm + mnstep(kk), dXh + mnstep(kk), kIdS, kk);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(tS, dBm + mnstep(kk), dXl + mnstep(kk), kIdS, 1);
         mma_commit(ctl.bar(BAR_S_FULL));
         mma_commit(ctl.bar(BAR_B_FREE));
         // Y_ab = C [e^R h_a | e^R h_b]^T (hi + lo) starts Y, once the h' tiles
         // are written and the previous piece's y rows are read
-        const uint32_t dY = tm + kColY;
         if (!ctl.wait(BAR_H_FULL, uint32_t(c & 1))) break;
         if (c >= 1 && !ctl.wait(BAR_Y_FREE, uint32_t((c - 1) & 1))) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(dY, kdesc(cb, kk, 16384), mndesc(hb, kk), kIdYo, kk);
-#pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(dY, kdesc(cb, kk, 16384), mndesc(hb + 32768, kk), kIdYo, 1);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(dY, dC + kstep(kk, 16384), dHh + mnstep(kk), kIdYo, kk);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) mma_ss(dY, dC + kstep(kk, 16384), dHl + mnstep(kk), kIdYo, 1);
         mma_commit(ctl.bar(BAR_H_FREE));
         mma_commit(ctl.bar(BAR_C_FREE));
         // Y_ab += hi(G o c) x'hi + hi(G o c) x'lo + lo(G o c) x'hi; K step kk
         // (tokens 16 kk ..) reads 32-column block kk / 2, half kk % 2
         if (!ctl.wait(BAR_GM_FULL, uint32_t(c & 1))) break;
         tc_fence_after();
-#pragma unroll 1
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(dY, tm + kColG + 32u * (kk >> 1) + 8u * (kk & 1), mndesc(xb, kk), kIdYd, 1);
-#pragma unroll 1
+          mma_ts(dY, tG + 32u * (kk >> 1) + 8u * (kk & 1), dXh + mnstep(kk), kIdYd, 1);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(dY, tm + kColG + 32u * (kk >> 1) + 8u * (kk & 1), mndesc(xb + 32768, kk), kIdYd, 1);
-#pragma unroll 1
+          mma_ts(dY, tG + 32u * (kk >> 1) + 8u * (kk & 1), dXl + mnstep(kk), kIdYd, 1);
+#pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          mma_ts(dY, tm + kColG + 32u * (kk >> 1) + 16u + 8u * (kk & 1), mndesc(xb, kk), kIdYd, 1);
+          mma_ts(dY, tG + 32u * (kk >> 1) + 16u + 8u * (kk & 1), dXh + mnstep(kk), kIdYd, 1);
         mma_commit(ctl.bar(BAR_Y_FULL));
         mma_commit(ctl.bar(BAR_X_FREE));
         mma_commit(ctl.bar(BAR_YD_DONE));
