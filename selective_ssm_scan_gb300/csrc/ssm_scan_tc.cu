@@ -565,11 +565,17 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       const bool fac = reinterpret_cast<const float*>(misc + kMiscScal)[4 * st] != 0.0f;
       const uint32_t uh = sb + kOffU + st * 32768;          // x' hi | lo
       const uint32_t xs = fac ? uh : sb + kOffX;             // operand of the state product
+      // base descriptors; each K step adds a compile-time constant
+      const uint64_t dC = sdesc_sw128(sb + kOffC, 16, 1024), dBk = sdesc_sw128(sb + kOffB, 16, 1024);
+      const uint64_t dBm = sdesc_sw128(sb + kOffB, 16384, 1024);
+      const uint64_t dXs = sdesc_sw128(xs, 16384, 1024), dXs2 = sdesc_sw128(xs + 16384, 16384, 1024);
+      const uint64_t dH = sdesc_sw128(sb + kOffH, 16384, 1024), dH2 = sdesc_sw128(sb + kOffH + 16384, 16384, 1024);
+      const uint64_t dU = sdesc_sw128(uh, 16384, 1024);
       tc_fence_after();
       // G = C B^T (mask(c-1) has read G(c-1): Yd(c-1) was issued after it)
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColG, kdesc(sb + kOffC, kk, 16384), kdesc(sb + kOffB, kk, 16384), kIdG, kk);
+        mma_ss(tm + kColG, dC + kstep(kk, 16384), dBk + kstep(kk, 16384), kIdG, kk);
       mma_commit(ctl.bar(BAR_G_FULL));
       // S' = B^T (x'hi + x'lo) into the single S buffer once state(c-1) read it;
       // B^T is the MN-major view of the B chunk
@@ -577,11 +583,10 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(xs, kk), kIdS, kk);
+        mma_ss(tm + kColS, dBm + mnstep(kk), dXs + mnstep(kk), kIdS, kk);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColS, sdesc_sw128(sb + kOffB + kk * 2048, 16384, 1024), mndesc(xs + 16384, kk),
-               kIdS, 1);
+        mma_ss(tm + kColS, dBm + mnstep(kk), dXs2 + mnstep(kk), kIdS, 1);
       mma_commit(ctl.bar(BAR_X_FREE));
       mma_commit(ctl.bar(BAR_S_FULL));
       // Yo = C (h_hi + h_lo)^T once h_{c-1} is in place and the epilogue of
@@ -591,10 +596,10 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColYo, kdesc(sb + kOffC, kk, 16384), mndesc(sb + kOffH, kk), kIdYo, kk);
+        mma_ss(tm + kColYo, dC + kstep(kk, 16384), dH + mnstep(kk), kIdYo, kk);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss(tm + kColYo, kdesc(sb + kOffC, kk, 16384), mndesc(sb + kOffH + 16384, kk), kIdYo, 1);
+        mma_ss(tm + kColYo, dC + kstep(kk, 16384), dH2 + mnstep(kk), kIdYo, 1);
       mma_commit(ctl.bar(BAR_YO_DONE));
       mma_commit(ctl.bar(BAR_CB_FREE));
       // the next chunk's B and C as soon as this chunk's readers are done
@@ -607,9 +612,9 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
       if (!ctl.wait(BAR_GM_FULL, uint32_t(c & 1))) break;
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, mndesc(uh, kk), kIdYd, kk);
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGh + 8u * kk, dU + mnstep(kk), kIdYd, kk);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, mndesc(uh, kk), kIdYdLo, 1);
+      for (int kk = 0; kk < 8; ++kk) mma_ts(tm + kColYd, tm + kColGl + 8u * kk, dU + mnstep(kk), kIdYdLo, 1);
       mma_commit(ctl.bar(BAR_Y_FULL));
       mma_commit(ctl.bar(BAR_U_FREE + st));
     }
