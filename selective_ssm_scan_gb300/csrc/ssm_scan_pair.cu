@@ -123,6 +123,21 @@ constexpr uint32_t kIdS = idesc_bf16(128, 128, 1, 1);   // B^T (MN-major) x [x'_
 constexpr uint32_t kIdYo = idesc_bf16(128, 128, 0, 1);  // C (K-major) x [h'_a | h'_b] (MN-major)
 constexpr uint32_t kIdYd = idesc_bf16(128, 128, 0, 1);  // (G o causal) (TMEM) x [x'_a | x'_b]
 
+// 64 consecutive TMEM columns of this warp's lanes: four loads in flight,
+// one wait (each load with its own wait costs a full TMEM round trip)
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&a)[16], uint32_t (&b)[16],
+                                          uint32_t (&c)[16], uint32_t (&d)[16]) {
+  tmem_ld_x16_nowait(taddr, a);
+  tmem_ld_x16_nowait(taddr + 16, b);
+  tmem_ld_x16_nowait(taddr + 32, c);
+  tmem_ld_x16_nowait(taddr + 48, d);
+  tmem_ld_wait();
+  reg_fence16(a);
+  reg_fence16(b);
+  reg_fence16(c);
+  reg_fence16(d);
+}
+
 // ---- packed fp32 pairs (two channels at once: f32x2 FMA / MUL / ADD) --------
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
   uint64_t r;
@@ -222,7 +237,8 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       counts[BAR_INFO_FULL + i] = 32;             // the decay warp
       counts[BAR_INFO_FREE + i] = kPT + kCT + 1;  // producers, consumers, issuer
     }
-    counts[BAR_GM_FULL] = counts[BAR_H_FULL] = counts[BAR_S_FREE] = kCT;
+    counts[BAR_H_FULL] = counts[BAR_S_FREE] = kCT;
+    counts[BAR_GM_FULL] = kPT;
     counts[BAR_Y_FREE] = kCT;
     counts[BAR_X_FULL] = kPT;
     for (int i = 0; i < NUM_BARS; ++i) mbar_init(ctl.bar(i), counts[i]);
@@ -253,6 +269,9 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     constexpr int NT = 4;
     constexpr int NR = NT + kMaxK - 1;  // staged rows a thread reads
     const int q = tid & 7, g4 = tid >> 3, tb = 4 * g4;
+    // the mask: warp w covers TMEM lanes 32 (w % 4) .. and blocks of parity w / 4
+    const int qw = warp & 3, half = warp >> 2;
+    const uint32_t tlw = tm + (uint32_t(qw * 32) << 16);
     auto stage_x = [&](int start, int hs) {  // TMA of raw rows [start - 3, start + 128)
       mbar_arrive_expect_tx(ctl.bar(BAR_XS_FULL), kXsBytes);
       tma_load_3d(sb + kOffXs, &tmX, (2 * pair + hs) * kP, start - (kMaxK - 1), b,
@@ -362,19 +381,22 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
               for (int k = 0; k < kMaxK; ++k) z = fma2(wk[k], xv[j + k], z);
               split_pair(silu_scaled2(z, gv[j]), hw[j][e2], lw[j][e2]);
             }
-          }
-          // every staged row was used above, so each load has returned:
-          // release the buffer to the next head's (or piece's) rows, the TMA
-          // write ordered after the generic-proxy reads by the proxy fence
-          role_sync(3, kPT);
-          if (tid == 0 && ok) {
-            fence_proxy_async_smem();
-            if (hs == 0) {
-              stage_x(p, 1);
-              xs_issued = su + 2;
-            } else if (!last) {
-              stage_x(p + n, 0);
-              xs_issued = su + 2;
+            if (e2 == 0) {
+              // the first channel pair used every staged row, so each load
+              // has returned: release the buffer to the next head's (or
+              // piece's) rows while the other pairs compute, the TMA write
+              // ordered after the generic-proxy reads by the proxy fence
+              role_sync(3, kPT);
+              if (tid == 0 && ok) {
+                fence_proxy_async_smem();
+                if (hs == 0) {
+                  stage_x(p, 1);
+                  xs_issued = su + 2;
+                } else if (!last) {
+                  stage_x(p + n, 0);
+                  xs_issued = su + 2;
+                }
+              }
             }
           }
         }
@@ -397,7 +419,55 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         fence_proxy_async_smem();
         mbar_arrive(ctl.bar(BAR_X_FULL));
       }
-      if (last) break;
+      // ---- causal mask of G: the rows of this warp's TMEM lane quarter,
+      // the 32-column blocks j of its parity (two producer warps share a
+      // quarter, so no warp splits more than two blocks) ------------------
+      {
+        bool wok = __all_sync(0xffffffffu, ok);
+        if (wok) wok = __all_sync(0xffffffffu, ctl.wait(BAR_G_FULL, uint32_t(c & 1)));
+        if (wok) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int j = half; j < 4; j += 2) {
+            uint32_t ph[16], pl[16];
+            if (j <= qw) {
+              uint32_t g2[2][16];
+              tmem_ld_x16_nowait(tlw + kColG + uint32_t(32 * j), g2[0]);
+              tmem_ld_x16_nowait(tlw + kColG + uint32_t(32 * j + 16), g2[1]);
+              tmem_ld_wait();
+              reg_fence16(g2[0]);
+              reg_fence16(g2[1]);
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                float m[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(g2[hf][i]);
+                if (j == qw) {  // diagonal block: s = 32 j + 16 hf + i <= t = 32 qw + lane
+#pragma unroll
+                  for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[8 * hf + i], pl[8 * hf + i]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) ph[i] = pl[i] = 0u;
+            }
+            // the block's 32 fp32 columns were read above: its hi pairs go
+            // over the first 16, its lo pairs over the last 16
+            tmem_st_x16(tlw + kColG + uint32_t(32 * j), ph);
+            tmem_st_x16(tlw + kColG + uint32_t(32 * j + 16), pl);
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(ctl.bar(BAR_GM_FULL));
+        }
+        ok = ok && wok;
+      }
+      // every producer leaves the loop at the same piece (they share named
+      // barriers), failed waits included
+      if (role_sync_or(3, kPT, !ok)) ok = false;
+      if (last || !ok) break;
     }
     if (FUSED && tid == 0) {  // staged tiles still in flight
       for (int su = xs_landed; su < xs_issued; ++su)
@@ -436,12 +506,21 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
 #pragma unroll 1
       for (int hs = 0; hs < 2; ++hs) {
         float v[kP];
+        if constexpr (FUSED) {
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t w[16];
-          tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, w);
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t w[16];
+            tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, w);
 #pragma unroll
-          for (int pp = 0; pp < 16; ++pp) v[16 * qq + pp] = __uint_as_float(w[pp]);
+            for (int pp = 0; pp < 16; ++pp) v[16 * qq + pp] = __uint_as_float(w[pp]);
+          }
+        } else {
+          uint32_t w[4][16];
+          tmem_ld64(tl + kColH + 64u * hs, w[0], w[1], w[2], w[3]);
+#pragma unroll
+          for (int qq = 0; qq < 4; ++qq)
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp) v[16 * qq + pp] = __uint_as_float(w[qq][pp]);
         }
         uint8_t* ht = sm + kOffH + 16384u * hs;
         write_split_row(ht, ht + 32768, r, v, hs == 0 ? e0 : e1);
@@ -475,39 +554,6 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       if (!(ok = wait_all(BAR_INFO_FULL + slot, uint32_t((c / kSlots) & 1)))) break;
       const int n = inf->n, start = inf->start;
       const bool last = inf->last != 0;
-      // ---- causal mask of this quarter's rows of G, split in place --------
-      if (!(ok = wait_all(BAR_G_FULL, uint32_t(c & 1)))) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        uint32_t ph[16], pl[16];
-        if (j <= q) {
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            uint32_t graw[16];
-            tmem_ld_x16(tl + kColG + uint32_t(32 * j + 16 * hf), graw);
-            float m[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m[i] = __uint_as_float(graw[i]);
-            if (j == q) {  // diagonal block: s = 32 j + 16 hf + i <= t = 32 q + lane
-#pragma unroll
-              for (int i = 0; i < 16; ++i) m[i] = 16 * hf + i <= lane ? m[i] : 0.0f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) split2(m[2 * i], m[2 * i + 1], ph[8 * hf + i], pl[8 * hf + i]);
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) ph[i] = pl[i] = 0u;
-        }
-        // the block's 32 fp32 columns were read above: write its hi pairs
-        // over the first 16 and its lo pairs over the last 16
-        tmem_st_x16(tl + kColG + uint32_t(32 * j), ph);
-        tmem_st_x16(tl + kColG + uint32_t(32 * j + 16), pl);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(ctl.bar(BAR_GM_FULL));
       // ---- state carry: h_end = e^{Lam_end} h + e^{Lam_end - R} S' ---------
       if (!(ok = wait_all(BAR_S_FULL, uint32_t(c & 1)))) break;
       tc_fence_after();
@@ -516,14 +562,42 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         const float dec_end = expf(inf->lend[hs]);
         const float s_scale = expf(inf->lend[hs] - inf->R[hs]);
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t sv[16], hv[16];
-          tmem_ld_x16(tl + kColS + 64u * hs + 16u * qq, sv);
-          tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, hv);
+        // fused: the producers set the pace, and one load per wait keeps the
+        // consumers' traffic spread out (measured faster); otherwise loads
+        // in flight together
+        if constexpr (FUSED) {
 #pragma unroll
-          for (int pp = 0; pp < 16; ++pp)
-            hv[pp] = __float_as_uint(fmaf(dec_end, __uint_as_float(hv[pp]), s_scale * __uint_as_float(sv[pp])));
-          tmem_st_x16(tl + kColH + 64u * hs + 16u * qq, hv);
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t sv[16], hv[16];
+            tmem_ld_x16(tl + kColS + 64u * hs + 16u * qq, sv);
+            tmem_ld_x16(tl + kColH + 64u * hs + 16u * qq, hv);
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp)
+              hv[pp] = __float_as_uint(fmaf(dec_end, __uint_as_float(hv[pp]), s_scale * __uint_as_float(sv[pp])));
+            tmem_st_x16(tl + kColH + 64u * hs + 16u * qq, hv);
+          }
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {  // 32 columns: S' and h loads in flight together
+            uint32_t sv0[16], sv1[16], hv0[16], hv1[16];
+            const uint32_t col = 64u * hs + 32u * hf;
+            tmem_ld_x16_nowait(tl + kColS + col, sv0);
+            tmem_ld_x16_nowait(tl + kColS + col + 16, sv1);
+            tmem_ld_x16_nowait(tl + kColH + col, hv0);
+            tmem_ld_x16_nowait(tl + kColH + col + 16, hv1);
+            tmem_ld_wait();
+            reg_fence16(sv0);
+            reg_fence16(sv1);
+            reg_fence16(hv0);
+            reg_fence16(hv1);
+  #pragma unroll
+            for (int pp = 0; pp < 16; ++pp) {
+              hv0[pp] = __float_as_uint(fmaf(dec_end, __uint_as_float(hv0[pp]), s_scale * __uint_as_float(sv0[pp])));
+              hv1[pp] = __float_as_uint(fmaf(dec_end, __uint_as_float(hv1[pp]), s_scale * __uint_as_float(sv1[pp])));
+            }
+            tmem_st_x16(tl + kColH + col, hv0);
+            tmem_st_x16(tl + kColH + col + 16, hv1);
+          }
         }
       }
       tmem_st_wait();
@@ -544,18 +618,34 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       for (int hs = 0; hs < 2; ++hs) {
         const float f_t = expf(inf->lam[hs][r] - inf->R[hs]);
         TY* yrow = y + (int64_t(b) * L + start + r) * D + int64_t(2 * pair + hs) * kP;
+        if constexpr (FUSED) {
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t a0[16];
-          tmem_ld_x16(tl + kColY + 64u * hs + 16u * qq, a0);
-          if (hs == 1 && qq == 3) {  // Y is read: the next piece's Yo may start
+          for (int qq = 0; qq < 4; ++qq) {
+            uint32_t a0[16];
+            tmem_ld_x16(tl + kColY + 64u * hs + 16u * qq, a0);
+            if (hs == 1 && qq == 3) {  // Y is read: the next piece's Yo may start
+              tc_fence_before();
+              mbar_arrive(ctl.bar(BAR_Y_FREE));
+            }
+            float yv[16];
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(a0[pp]);
+            if (r < n) store_row16<TY>(yrow + 16 * qq, yv);
+          }
+        } else {
+          uint32_t a[4][16];
+          tmem_ld64(tl + kColY + 64u * hs, a[0], a[1], a[2], a[3]);
+          if (hs == 1) {  // Y is read: the next piece's Yo may start
             tc_fence_before();
             mbar_arrive(ctl.bar(BAR_Y_FREE));
           }
-          float yv[16];
 #pragma unroll
-          for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(a0[pp]);
-          if (r < n) store_row16<TY>(yrow + 16 * qq, yv);
+          for (int qq = 0; qq < 4; ++qq) {
+            float yv[16];
+#pragma unroll
+            for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(a[qq][pp]);
+            if (r < n) store_row16<TY>(yrow + 16 * qq, yv);
+          }
         }
       }
       mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
