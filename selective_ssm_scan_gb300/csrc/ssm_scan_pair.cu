@@ -48,6 +48,8 @@
 // and every hand-over (x', h', Y, S', the mask, the next piece's B and C) has
 // at least one product group of slack.  Every wait is bounded (2 s); a timeout
 // raises SSS_ERR_TIMEOUT and unwinds.
+#include <type_traits>
+
 #include "common.cuh"
 #include "scan_tc_util.cuh"
 #include "tc_ptx.cuh"
@@ -96,7 +98,13 @@ constexpr uint32_t kMiBars = 7552;    // mbarriers
 constexpr uint32_t kMiTmem = 7840;
 constexpr uint32_t kMiAbort = 7844;
 constexpr uint32_t kMiscBytes = 7848;
-constexpr uint32_t kSmemBytes = kOffMisc + kMiscBytes + 1024;
+// per consumer warp, 32 rows x 64 bytes of bf16 y: the warp writes its rows
+// here and reads them back as whole 64-byte row segments, so one global store
+// instruction covers 8 rows instead of 32 partial lines
+constexpr uint32_t kOffYs = (kOffMisc + kMiscBytes + 127u) & ~127u;
+constexpr uint32_t kYsWarpBytes = 32 * 64;
+constexpr uint32_t kSmemBytes = kOffYs + 4 * kYsWarpBytes + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 constexpr int kSlots = 4;
 
 struct PieceInfo {
@@ -338,6 +346,27 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
 #pragma unroll
           for (int i = 0; i < NR; ++i)
             xr[i] = *reinterpret_cast<const uint4*>(sm + kOffXs + sw128(tb + i, q));
+          {
+            // a fold of every loaded word: once it is computed each staged
+            // load has returned, so the buffer can go to the next head's (or
+            // piece's) rows before any arithmetic; the proxy fence orders the
+            // TMA write after these generic-proxy reads
+            uint32_t fold = 0u;
+#pragma unroll
+            for (int i = 0; i < NR; ++i) fold ^= xr[i].x ^ xr[i].y ^ xr[i].z ^ xr[i].w;
+            asm volatile("" ::"r"(fold));
+          }
+          role_sync(3, kPT);
+          if (tid == 0 && ok) {
+            fence_proxy_async_smem();
+            if (hs == 0) {
+              stage_x(p, 1);
+              xs_issued = su + 2;
+            } else if (!last) {
+              stage_x(p + n, 0);
+              xs_issued = su + 2;
+            }
+          }
           if (p == 0 && tb < kMaxK - 1 && nv > 0) {
             // positions < 0: the conv state S (zeros without one)
 #pragma unroll
@@ -380,23 +409,6 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
 #pragma unroll
               for (int k = 0; k < kMaxK; ++k) z = fma2(wk[k], xv[j + k], z);
               split_pair(silu_scaled2(z, gv[j]), hw[j][e2], lw[j][e2]);
-            }
-            if (e2 == 0) {
-              // the first channel pair used every staged row, so each load
-              // has returned: release the buffer to the next head's (or
-              // piece's) rows while the other pairs compute, the TMA write
-              // ordered after the generic-proxy reads by the proxy fence
-              role_sync(3, kPT);
-              if (tid == 0 && ok) {
-                fence_proxy_async_smem();
-                if (hs == 0) {
-                  stage_x(p, 1);
-                  xs_issued = su + 2;
-                } else if (!last) {
-                  stage_x(p + n, 0);
-                  xs_issued = su + 2;
-                }
-              }
             }
           }
         }
@@ -614,23 +626,63 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       // ---- y rows of both heads: y_t = f_t Y_t --------------------------------
       if (!(ok = wait_all(BAR_Y_FULL, uint32_t(c & 1)))) break;
       tc_fence_after();
+      // 32 columns [32 hf, 32 hf + 32) of head hs, scaled by f_t, to y
+      auto emit_half = [&](int hs, int hf, float f_t, const uint32_t (&u0)[16],
+                           const uint32_t (&u1)[16]) {
+        // fused, bf16 y: through the warp's buffer (measured faster there;
+        // the scan from fp32 u keeps the direct row stores, faster for it)
+        if constexpr (FUSED && std::is_same<TY, __nv_bfloat16>::value) {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            w[i] = pack2(bf16_bits(f_t * __uint_as_float(u0[2 * i])),
+                         bf16_bits(f_t * __uint_as_float(u0[2 * i + 1])));
+            w[8 + i] = pack2(bf16_bits(f_t * __uint_as_float(u1[2 * i])),
+                             bf16_bits(f_t * __uint_as_float(u1[2 * i + 1])));
+          }
+          // row `lane` of the warp's buffer, 16-byte chunks XOR-swizzled by
+          // (row / 2) % 4: both the row writes and the segment reads below
+          // touch 8 distinct bank groups per 8 lanes
+          uint8_t* yb = sm + kOffYs + uint32_t(q) * kYsWarpBytes;
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            *reinterpret_cast<uint4*>(yb + lane * 64 + ((cc ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(w[4 * cc], w[4 * cc + 1], w[4 * cc + 2], w[4 * cc + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int row = 8 * j + (lane >> 2), ch = lane & 3;
+            const uint4 v = *reinterpret_cast<const uint4*>(yb + row * 64 + ((ch ^ ((row >> 1) & 3)) << 4));
+            if (32 * q + row < n)
+              *reinterpret_cast<uint4*>(y + (int64_t(b) * L + start + 32 * q + row) * D +
+                                        int64_t(2 * pair + hs) * kP + 32 * hf + 8 * ch) = v;
+          }
+          __syncwarp();
+        } else {
+          TY* yrow = y + (int64_t(b) * L + start + r) * D + int64_t(2 * pair + hs) * kP + 32 * hf;
+          float yv[16];
+#pragma unroll
+          for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(u0[pp]);
+          if (r < n) store_row16<TY>(yrow, yv);
+#pragma unroll
+          for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(u1[pp]);
+          if (r < n) store_row16<TY>(yrow + 16, yv);
+        }
+      };
 #pragma unroll 1
       for (int hs = 0; hs < 2; ++hs) {
         const float f_t = expf(inf->lam[hs][r] - inf->R[hs]);
-        TY* yrow = y + (int64_t(b) * L + start + r) * D + int64_t(2 * pair + hs) * kP;
         if constexpr (FUSED) {
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            uint32_t a0[16];
-            tmem_ld_x16(tl + kColY + 64u * hs + 16u * qq, a0);
-            if (hs == 1 && qq == 3) {  // Y is read: the next piece's Yo may start
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t a0[16], a1[16];
+            tmem_ld_x16(tl + kColY + 64u * hs + 32u * hf, a0);
+            tmem_ld_x16(tl + kColY + 64u * hs + 32u * hf + 16u, a1);
+            if (hs == 1 && hf == 1) {  // Y is read: the next piece's Yo may start
               tc_fence_before();
               mbar_arrive(ctl.bar(BAR_Y_FREE));
             }
-            float yv[16];
-#pragma unroll
-            for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(a0[pp]);
-            if (r < n) store_row16<TY>(yrow + 16 * qq, yv);
+            emit_half(hs, hf, f_t, a0, a1);
           }
         } else {
           uint32_t a[4][16];
@@ -639,13 +691,8 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
             tc_fence_before();
             mbar_arrive(ctl.bar(BAR_Y_FREE));
           }
-#pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            float yv[16];
-#pragma unroll
-            for (int pp = 0; pp < 16; ++pp) yv[pp] = f_t * __uint_as_float(a[qq][pp]);
-            if (r < n) store_row16<TY>(yrow + 16 * qq, yv);
-          }
+          emit_half(hs, 0, f_t, a[0], a[1]);
+          emit_half(hs, 1, f_t, a[2], a[3]);
         }
       }
       mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
