@@ -756,13 +756,6 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         for (int kk = 0; kk < 8; ++kk)
           mma_ss(tG, dC + kstep(kk, 16384), dBk + kstep(kk, 16384), kIdG, kk);
         mma_commit(ctl.bar(BAR_G_FULL));
-        if (!last) {  // warm L2 with the next piece's B and C
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            tma_prefetch_3d(&tmC, g * kN + 64 * hh, start + n, b);
-            tma_prefetch_3d(&tmB, g * kN + 64 * hh, start + n, b);
-          }
-        }
         // S' = B^T [x'_a | x'_b] (hi + lo), once the x' tiles are in and the
         // previous carry has read S'
         if (!ctl.wait(BAR_X_FULL, uint32_t(c & 1))) break;
