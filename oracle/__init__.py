@@ -74,11 +74,14 @@ def lib():
                                              _L, _L, _L, ctypes.c_int, ctypes.c_int, ctypes.c_int]
             l.orc_ssm_scan.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _L, _L, _L,
                                        _L, _L, _L, ctypes.c_int]
+            l.orc_ssm_scan_bwd.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp,
+                                           _dp, _dp, _dp, _dp, _L, _L, _L, _L, _L, _L,
+                                           ctypes.c_int]
             l.orc_mixer_update.argtypes = [_dp, _dp, _dp, _dp, _L, _L, _ip, _ip, _dp, _dp,
                                            _dp, _dp, _dp, _dp, _L, _L, _L, _L, _L, _L,
                                            ctypes.c_int, ctypes.c_int]
             l.orc_num_threads.argtypes = [ctypes.c_int]
-            for f in (l.orc_conv_state_fwd, l.orc_conv_state_bwd, l.orc_ssm_scan,
+            for f in (l.orc_conv_state_fwd, l.orc_conv_state_bwd, l.orc_ssm_scan, l.orc_ssm_scan_bwd,
                       l.orc_mixer_update, l.orc_num_threads):
                 f.restype = ctypes.c_int
             _lib = l
@@ -155,6 +158,32 @@ def ssm_scan(u, dt, A, B, C, h0=None, nthreads: int = 0):
     if rc != 0:
         raise ValueError("orc_ssm_scan: bad sizes")
     return y, hT
+
+
+def ssm_scan_bwd(u, dt, A, B, C, h0, dy, dhT=None, nthreads: int = 0):
+    """Gradient of ssm_scan: dy = dL/dy [Bz, L, H, P], dhT = dL/dhT [Bz, H, P, N] | None.
+
+    Returns du [Bz, L, H, P], ddt [Bz, L, H], dA [H], dB [Bz, L, G, N],
+    dC [Bz, L, G, N] and dh0 [Bz, H, P, N] (float64)."""
+    dt, A, B, C, h0, dhT = _f64(dt), _f64(A), _f64(B), _f64(C), _f64(h0), _f64(dhT)
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    u = _f64(u)
+    P = u.shape[3] if u.ndim == 4 else u.shape[2] // H
+    u = u.reshape(Bz, L, H, P)
+    dy = _f64(dy).reshape(Bz, L, H, P)
+    du = np.empty((Bz, L, H, P))
+    ddt = np.empty((Bz, L, H))
+    dA = np.empty((H,))
+    dB = np.empty((Bz, L, G, N))
+    dC = np.empty((Bz, L, G, N))
+    dh0 = np.empty((Bz, H, P, N))
+    rc = lib().orc_ssm_scan_bwd(_ptr(u), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(h0),
+                                _ptr(dy), _ptr(dhT), _ptr(du), _ptr(ddt), _ptr(dA), _ptr(dB),
+                                _ptr(dC), _ptr(dh0), Bz, L, H, P, N, G, nthreads)
+    if rc != 0:
+        raise ValueError("orc_ssm_scan_bwd: bad sizes")
+    return du, ddt, dA, dB, dC, dh0
 
 
 def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, nthreads: int = 0):

@@ -30,6 +30,21 @@
  *                       A_t = exp(dt_t * A_h), run from the initial state
  *                       h_{-1} (Eq. (4)'s non-zero initial state), one token
  *                       at a time.
+ *   orc_ssm_scan_bwd    the gradient of orc_ssm_scan with state, for
+ *                       state-passing and truncated-backpropagation training
+ *                       ("Understanding and Improving Length Generalization
+ *                       in Recurrent Models" sections 4.4-4.5; the causal-conv
+ *                       chapter's "chunked training and truncated backward"
+ *                       section on passing the state gradient across
+ *                       chunks): with g_t = dL/dh_t (every later use
+ *                       included) and a_t = exp(dt_t A_h), token by token
+ *                       in reverse, g_t = a_{t+1} g_{t+1} + dy_t C_t^T (the
+ *                       gradient of the final state dhT entering at t = L-1),
+ *                       dC_t = h_t^T dy_t, dx_t = g_t B_t, dB_t = g_t^T x_t,
+ *                       dl_t = a_t <g_t, h_{t-1}> for l_t = dt_t A_h, so
+ *                       ddt_t = dl_t A_h and dA_h = sum dl_t dt_t, and
+ *                       dh0 = a_0 g_0; dB and dC sum over the heads of a
+ *                       group, dA over the batch.
  *   orc_mixer_update    the single- and multi-token update of the same
  *                       chapter (sections "single-token update", "the
  *                       physical cache can be longer", "circular mode",
@@ -260,6 +275,105 @@ int orc_ssm_scan(const double* u, const double* dt, const double* A,
   if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return -1;
   scan_ctx c = {u, dt, A, B, C, h0, y, hT, Bz, L, H, P, N, G};
   parallel_for(Bz * H, nthreads, scan_item, &c);
+  return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* gradient of the scan, with the initial and final states                  */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+  const double *u, *dt, *A, *B, *C, *h0, *dy, *dhT;
+  double *du, *ddt, *dA_part, *dB, *dC, *dh0;
+  long Bz, L, H, P, N, G;
+} scanb_ctx;
+
+/* one (batch row, group): its heads in order, so the group sums of dB and dC
+ * have one writer and a fixed order */
+static void scanb_item(void* p, long item) {
+  scanb_ctx* c = (scanb_ctx*)p;
+  const long H = c->H, P = c->P, N = c->N, G = c->G, L = c->L, PN = c->P * c->N;
+  const long b = item / G, g = item % G, hpg = H / G;
+  for (long t = 0; t < L; ++t)
+    for (long n = 0; n < N; ++n) {
+      c->dB[((b * L + t) * G + g) * N + n] = 0.0;
+      c->dC[((b * L + t) * G + g) * N + n] = 0.0;
+    }
+  /* hs[t + 1] = h_t, hs[0] = h_{-1} */
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * PN > 0 ? (L + 1) * PN : 1));
+  double* gr = (double*)malloc(sizeof(double) * (size_t)(PN > 0 ? PN : 1));
+  for (long hd = g * hpg; hd < (g + 1) * hpg; ++hd) {
+    for (long i = 0; i < PN; ++i) hs[i] = c->h0 ? c->h0[(b * H + hd) * PN + i] : 0.0;
+    for (long t = 0; t < L; ++t) {
+      const double a = exp(c->dt[(b * L + t) * H + hd] * c->A[hd]);
+      const double* Bt = c->B + ((b * L + t) * G + g) * N;
+      const double* xt = c->u + ((b * L + t) * H + hd) * P;
+      for (long pp = 0; pp < P; ++pp)
+        for (long n = 0; n < N; ++n)
+          hs[(t + 1) * PN + pp * N + n] = a * hs[t * PN + pp * N + n] + xt[pp] * Bt[n];
+    }
+    for (long i = 0; i < PN; ++i) gr[i] = c->dhT ? c->dhT[(b * H + hd) * PN + i] : 0.0;
+    double dA_acc = 0.0;
+    for (long t = L - 1; t >= 0; --t) {
+      const double dtt = c->dt[(b * L + t) * H + hd];
+      const double a = exp(dtt * c->A[hd]);
+      const double* Bt = c->B + ((b * L + t) * G + g) * N;
+      const double* Ct = c->C + ((b * L + t) * G + g) * N;
+      const double* xt = c->u + ((b * L + t) * H + hd) * P;
+      const double* dyt = c->dy + ((b * L + t) * H + hd) * P;
+      const double* ht = hs + (t + 1) * PN;
+      const double* hp = hs + t * PN;
+      double* dBt = c->dB + ((b * L + t) * G + g) * N;
+      double* dCt = c->dC + ((b * L + t) * G + g) * N;
+      /* g = dL/dh_t: the later tokens' part already in gr, plus y_t's */
+      for (long pp = 0; pp < P; ++pp)
+        for (long n = 0; n < N; ++n) gr[pp * N + n] += dyt[pp] * Ct[n];
+      for (long n = 0; n < N; ++n) {
+        double sc = 0.0, sb = 0.0;
+        for (long pp = 0; pp < P; ++pp) {
+          sc += dyt[pp] * ht[pp * N + n];
+          sb += gr[pp * N + n] * xt[pp];
+        }
+        dCt[n] += sc;
+        dBt[n] += sb;
+      }
+      double da = 0.0;
+      for (long pp = 0; pp < P; ++pp) {
+        double sx = 0.0;
+        for (long n = 0; n < N; ++n) {
+          sx += gr[pp * N + n] * Bt[n];
+          da += gr[pp * N + n] * hp[pp * N + n];
+        }
+        c->du[((b * L + t) * H + hd) * P + pp] = sx;
+      }
+      const double dl = a * da;
+      c->ddt[(b * L + t) * H + hd] = dl * c->A[hd];
+      dA_acc += dl * dtt;
+      for (long i = 0; i < PN; ++i) gr[i] *= a; /* now dL/dh_{t-1} */
+    }
+    if (c->dh0)
+      for (long i = 0; i < PN; ++i) c->dh0[(b * H + hd) * PN + i] = gr[i];
+    c->dA_part[b * H + hd] = dA_acc;
+  }
+  free(gr);
+  free(hs);
+}
+
+int orc_ssm_scan_bwd(const double* u, const double* dt, const double* A,
+                     const double* B, const double* C, const double* h0,
+                     const double* dy, const double* dhT, double* du, double* ddt,
+                     double* dA, double* dB, double* dC, double* dh0, long Bz,
+                     long L, long H, long P, long N, long G, int nthreads) {
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return -1;
+  double* part = (double*)malloc(sizeof(double) * (size_t)(Bz * H > 0 ? Bz * H : 1));
+  scanb_ctx c = {u, dt, A, B, C, h0, dy, dhT, du, ddt, part, dB, dC, dh0, Bz, L, H, P, N, G};
+  parallel_for(Bz * G, nthreads, scanb_item, &c);
+  for (long hd = 0; hd < H; ++hd) {
+    double s = 0.0;
+    for (long b = 0; b < Bz; ++b) s += part[b * H + hd];
+    dA[hd] = s;
+  }
+  free(part);
   return 0;
 }
 

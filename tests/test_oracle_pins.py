@@ -450,3 +450,109 @@ def test_conv_bwd_empty_sequence_passes_the_state_gradient():
                                            np.zeros(3), S, np.zeros((2, 0, 3)), q)
     np.testing.assert_array_equal(dS, q)
     assert not dw.any() and not db.any() and dx.shape == (2, 0, 3)
+
+
+# ---------------------------------------------------------------------------
+# scan backward with state
+# ---------------------------------------------------------------------------
+
+def _scan_problem(seed, Bz=2, L=7, H=4, P=3, N=5, G=2):
+    r = np.random.default_rng(seed)
+    u = r.standard_normal((Bz, L, H, P))
+    dt = np.log1p(np.exp(r.standard_normal((Bz, L, H)) - 1.0))
+    A = -r.uniform(0.1, 1.0, H)
+    B = r.standard_normal((Bz, L, G, N))
+    C = r.standard_normal((Bz, L, G, N))
+    h0 = r.standard_normal((Bz, H, P, N))
+    dy = r.standard_normal((Bz, L, H, P))
+    dhT = r.standard_normal((Bz, H, P, N))
+    return u, dt, A, B, C, h0, dy, dhT
+
+
+def _scan_loss(u, dt, A, B, C, h0, dy, dhT):
+    y, hT = oracle.ssm_scan(u, dt, A, B, C, h0)
+    return float((y * dy).sum() + (hT * dhT).sum())
+
+
+@pytest.mark.parametrize("name", ["u", "dt", "A", "B", "C", "h0"])
+def test_scan_bwd_matches_finite_differences(name):
+    """Every gradient against central differences of the (separately pinned)
+    forward, for the linear loss <dy, y> + <dhT, hT>."""
+    args = list(_scan_problem(11))
+    names = ["u", "dt", "A", "B", "C", "h0"]
+    du, ddt, dA, dB, dC, dh0 = oracle.ssm_scan_bwd(*args)
+    grad = dict(zip(names, (du, ddt, dA, dB, dC, dh0)))[name]
+    i = names.index(name)
+    x0 = args[i]
+    fd = np.zeros_like(x0)
+    eps = 1e-6
+    for idx in np.ndindex(x0.shape):
+        xp = x0.copy(); xp[idx] += eps
+        xm = x0.copy(); xm[idx] -= eps
+        args[i] = xp; lp = _scan_loss(*args)
+        args[i] = xm; lm = _scan_loss(*args)
+        fd[idx] = (lp - lm) / (2 * eps)
+    args[i] = x0
+    np.testing.assert_allclose(grad, fd, rtol=1e-6, atol=1e-6)
+
+
+def test_scan_bwd_initial_state_closed_form():
+    """Eq. (4): the h0 term of y_t is exp(Lam_t) C_t^T h0 and that of hT is
+    exp(Lam_{L-1}) h0, so dh0 = exp(Lam_{L-1}) dhT + sum_t exp(Lam_t) dy_t C_t^T,
+    Lam_t the inclusive sum of dt_s A_h."""
+    u, dt, A, B, C, h0, dy, dhT = _scan_problem(12)
+    Bz, L, H, P = u.shape
+    G = B.shape[2]
+    *_, dh0 = oracle.ssm_scan_bwd(u, dt, A, B, C, h0, dy, dhT)
+    lam = np.cumsum(dt * A[None, None, :], axis=1)           # [Bz, L, H]
+    g_of_h = np.arange(H) // (H // G)
+    Ch = C[:, :, g_of_h, :]                                  # [Bz, L, H, N]
+    ref = (np.exp(lam[:, -1])[:, :, None, None] * dhT
+           + np.einsum("blh,blhp,blhn->bhpn", np.exp(lam), dy, Ch))
+    np.testing.assert_allclose(dh0, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_scan_bwd_no_decay_closed_forms():
+    """A = 0 (a_t = 1): h_t = h0 + sum_{s<=t} x_s B_s^T, so
+    dx_s = sum_{t>=s} (C_t . B_s) dy_t + dhT B_s and
+    dC_t = (h0 + sum_{s<=t} x_s B_s^T)^T dy_t."""
+    u, dt, A, B, C, h0, dy, dhT = _scan_problem(13, G=1)
+    A = np.zeros_like(A)
+    du, ddt, dA, dB, dC, dh0 = oracle.ssm_scan_bwd(u, dt, A, B, C, h0, dy, dhT)
+    Bz, L, H, P = u.shape
+    B1, C1 = B[:, :, 0], C[:, :, 0]                          # [Bz, L, N]
+    later = np.triu(np.ones((L, L)))                         # [s, t]: t >= s
+    GCB = np.einsum("btn,bsn->bst", C1, B1) * later          # (C_t . B_s), t >= s
+    ref_dx = np.einsum("bst,bthp->bshp", GCB, dy) + np.einsum("bhpn,bsn->bshp", dhT, B1)
+    np.testing.assert_allclose(du, ref_dx, rtol=1e-11, atol=1e-11)
+    upto = np.tril(np.ones((L, L)))                          # [t, s]: s <= t
+    hs = h0[:, None] + np.einsum("ts,bshp,bsn->bthpn", upto, u, B1)
+    ref_dC = np.einsum("bthpn,bthp->btn", hs, dy)[:, :, None, :]
+    np.testing.assert_allclose(dC, ref_dC, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(ddt, 0.0, atol=1e-12)        # dl_t times A_h = 0
+
+
+@pytest.mark.parametrize("split", [1, 3, 6])
+def test_scan_bwd_segments_equal_whole(split):
+    """Truncated backpropagation made exact: segment B's dh0, fed to segment A
+    as its dhT (A's final state is B's initial state), gives the whole
+    sequence's gradients."""
+    u, dt, A, B, C, h0, dy, dhT = _scan_problem(14)
+    whole = oracle.ssm_scan_bwd(u, dt, A, B, C, h0, dy, dhT)
+    sl_a, sl_b = slice(0, split), slice(split, None)
+    _, hA = oracle.ssm_scan(u[:, sl_a], dt[:, sl_a], A, B[:, sl_a], C[:, sl_a], h0)
+    gb = oracle.ssm_scan_bwd(u[:, sl_b], dt[:, sl_b], A, B[:, sl_b], C[:, sl_b], hA, dy[:, sl_b], dhT)
+    ga = oracle.ssm_scan_bwd(u[:, sl_a], dt[:, sl_a], A, B[:, sl_a], C[:, sl_a], h0, dy[:, sl_a], gb[5])
+    for k in (0, 1, 3, 4):  # du, ddt, dB, dC: per token
+        np.testing.assert_allclose(np.concatenate([ga[k], gb[k]], axis=1), whole[k],
+                                   rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(ga[2] + gb[2], whole[2], rtol=1e-11, atol=1e-11)  # dA
+    np.testing.assert_allclose(ga[5], whole[5], rtol=1e-11, atol=1e-11)          # dh0
+
+
+def test_scan_bwd_empty_sequence():
+    """L = 0: hT = h0, so dh0 = dhT and dA = 0."""
+    u, dt, A, B, C, h0, dy, dhT = _scan_problem(15, L=0)
+    du, ddt, dA, dB, dC, dh0 = oracle.ssm_scan_bwd(u, dt, A, B, C, h0, dy, dhT)
+    np.testing.assert_array_equal(dh0, dhT)
+    assert not dA.any() and du.shape[1] == 0
