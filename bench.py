@@ -438,6 +438,8 @@ def main():
 
     # ---- conv backward with state on one segment, same rules ---------------
     conv_bwd = bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
+    # ---- scan backward with state on one segment, same rules ---------------
+    scan_bwd = bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
 
     # ---- decode update (continuous batching), same rules -------------------
     decode = None
@@ -456,7 +458,7 @@ def main():
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
-        "conv_bwd": conv_bwd,
+        "conv_bwd": conv_bwd, "scan_bwd": scan_bwd,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -530,6 +532,58 @@ def bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
             "avg_call_ms": ms, "launches_per_call": 2, "algorithmic_bytes_per_call": byts,
             "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
             "tokens_per_s": Bz * Lseg / (ms * 1e-3)}
+
+
+def bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
+    """sss_ssm_scan_bwd on one segment of the workload: bf16 x, dt, B, C, fp32
+    h0, dy and dhT in; fp32 dx, ddt, dA, dB, dC and dh0 out (four kernels:
+    chunk-entry states, chunk-end state gradients, the chunk gradients, the
+    fixed-order group and batch sums)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(6)
+    bf = torch.bfloat16
+    Bz, H, P, N, G = s.Bz, s.H, s.P, s.N, 1
+    x = torch.randn((Bz, Lseg, H, P), generator=g, device=dev).to(bf)
+    dt = torch.nn.functional.softplus(torch.randn((Bz, Lseg, H), generator=g, device=dev) - 2).to(bf)
+    A = -torch.rand((H,), generator=g, device=dev) * 0.99 - 0.01
+    B = torch.randn((Bz, Lseg, G, N), generator=g, device=dev).to(bf)
+    C = torch.randn((Bz, Lseg, G, N), generator=g, device=dev).to(bf)
+    h0 = torch.randn((Bz, H, P, N), generator=g, device=dev) * 0.1
+    dy = torch.randn((Bz, Lseg, H, P), generator=g, device=dev)
+    dhT = torch.randn((Bz, H, P, N), generator=g, device=dev)
+    ws = torch.empty(sss.ssm_scan_bwd_workspace_size(Bz, Lseg, H, P, N, G), dtype=torch.uint8,
+                     device=dev)
+
+    def call():
+        sss.ssm_scan_bwd(x, dt, A, B, C, h0, dy, dhT, workspace=ws)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(max(3, args.steps // 50)):
+        flush.zero_()
+        torch.cuda._sleep(200_000)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        call()
+        e1.record(stream)
+        evs.append((e0, e1))
+    stream.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    tok = Bz * Lseg
+    D = H * P
+    byts = (tok * (D * (2 + 4 + 4)                   # x bf16, dy fp32 in; dx fp32 out
+                   + H * (2 + 4)                     # dt in, ddt out
+                   + G * N * (2 * 2 + 2 * 4))        # B, C in; dB, dC out
+            + Bz * H * P * N * 4 * 3                 # h0, dhT in; dh0 out
+            + H * 4 * 2)                             # A in, dA out
+    return {"workload": f"one {Lseg}-token segment, Bz={Bz}, H={H}, P={P}, N={N}, bf16 inputs",
+            "avg_call_ms": ms, "launches_per_call": 4, "algorithmic_bytes_per_call": byts,
+            "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
+            "tokens_per_s": tok / (ms * 1e-3),
+            "kernel": "fp32 CUDA-core chunked backward (chunks of 64)"}
 
 
 def bench_decode(torch, sss, dev, stream, flush, args, hbm):

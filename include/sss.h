@@ -220,6 +220,49 @@ sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt,
                             sss_stream_t stream);
 
 /*
+ * sss_ssm_scan_bwd -- gradient of sss_ssm_scan_fwd with state, for
+ * state-passing and truncated-backpropagation training.  Sources:
+ * "Understanding and Improving Length Generalization in Recurrent Models",
+ * sections 4.4-4.5 (a segment starts from the previous segment's final
+ * state; the gradient of that state is what flows back into the previous
+ * segment), with the recurrence of section 2 Eq. (1) and the initial-state
+ * form Eq. (4); "Chapter 7: state, chunking and incremental inference",
+ * section "chunked training and truncated backpropagation" (the state
+ * gradient of chunk B must be passed to chunk A for the chunked gradient
+ * to equal the whole one).  With g_t = dL/dh_t and a_t = exp(dt_t A_h):
+ *     g_{L-1} = dhT + dy_{L-1} C_{L-1}^T,  g_t = a_{t+1} g_{t+1} + dy_t C_t^T
+ *     dx_t = g_t B_t,  dB_t = g_t^T x_t,  dC_t = h_t^T dy_t,
+ *     ddt_t = A_h a_t <g_t, h_{t-1}>,  dA_h = sum_t dt_t a_t <g_t, h_{t-1}>,
+ *     dh0 = a_0 g_0
+ * (dB and dC summed over the heads of a group, dA over the batch).
+ *
+ *  x, dt, A, B, C, h0_in   as for sss_ssm_scan_fwd (h0_in NULL = zeros)
+ *  dy      [Bz, L, H, P]  float32, dL/dy
+ *  dhT     [Bz, H, P, N]  float32, dL/d(final state); NULL = zeros
+ *  dx      [Bz, L, H, P]  float32 (written)
+ *  ddt     [Bz, L, H]     float32 (written)
+ *  dA      [H]            float32 (written, not accumulated)
+ *  dB, dC  [Bz, L, G, N]  float32 (written)
+ *  dh0     [Bz, H, P, N]  float32, dL/dh0; NULL = not written; may be the
+ *                         same buffer as dhT (any other overlap is invalid)
+ *  workspace: at least sss_ssm_scan_bwd_workspace_size() bytes, 256-byte
+ *          aligned, owned by the caller (chunk-boundary states and gradients
+ *          and per-head partial sums; contents need not be initialised).
+ * Deterministic: every sum has a fixed order.  P <= 64 and N <= 128
+ * (SSS_ERR_UNSUPPORTED otherwise); any dtype mix of x and activations.
+ * The arithmetic is fp32 from the exact input values.
+ */
+size_t sss_ssm_scan_bwd_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G);
+
+sss_status sss_ssm_scan_bwd(const void* x, sss_dtype x_dtype, const void* dt,
+                            const float* A, const void* B, const void* C,
+                            sss_dtype act_dtype, const float* h0_in, const float* dy,
+                            const float* dhT, float* dx, float* ddt, float* dA, float* dB,
+                            float* dC, float* dh0, int64_t Bz, int64_t L, int H, int P,
+                            int N, int G, void* workspace, size_t workspace_bytes,
+                            sss_stream_t stream);
+
+/*
  * sss_mixer_fwd -- one segment of the streaming forward in a single kernel:
  * the conv with state of sss_conv_state_fwd (SiLU applied) feeding the scan
  * of sss_ssm_scan_fwd, so the conv output never goes to memory.  Sources:

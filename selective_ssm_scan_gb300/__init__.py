@@ -68,6 +68,11 @@ _lib.sss_ssm_scan_path.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
 _lib.sss_ssm_scan_fwd.restype = _i
 _lib.sss_ssm_scan_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i64, _i64, _i, _i,
                                   _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_ssm_scan_bwd_workspace_size.restype = ctypes.c_size_t
+_lib.sss_ssm_scan_bwd_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i]
+_lib.sss_ssm_scan_bwd.restype = _i
+_lib.sss_ssm_scan_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
+                                  _i64, _i64, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
 _lib.sss_mixer_update.restype = _i
 _lib.sss_mixer_update.argtypes = [_p, _i, _p, _p, _p, _i64, _i, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i, _i, _i, _i, _i, _i, _p]
@@ -245,6 +250,41 @@ def ssm_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
                                _ptr(workspace), wsb, _stream(stream))
     _check("sss_ssm_scan_fwd", rc)
     return y, hT
+
+
+def ssm_scan_bwd_workspace_size(Bz, L, H, P, N, G) -> int:
+    return int(_lib.sss_ssm_scan_bwd_workspace_size(Bz, L, H, P, N, G))
+
+
+def ssm_scan_bwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                 C: torch.Tensor, h0: Optional[torch.Tensor], dy: torch.Tensor,
+                 dhT: Optional[torch.Tensor] = None, dh0: Optional[torch.Tensor] = None,
+                 want_dh0: bool = True, workspace: Optional[torch.Tensor] = None, stream=None):
+    """Gradient of ssm_scan_fwd.  dy [Bz, L, H, P] fp32, dhT [Bz, H, P, N] fp32
+    or None.  Returns (dx [Bz, L, H, P], ddt [Bz, L, H], dA [H], dB and dC
+    [Bz, L, G, N], dh0 [Bz, H, P, N] or None), all fp32."""
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    P = x.shape[-1] if x.dim() == 4 else x.shape[-1] // H
+    dev = x.device
+    f32 = torch.float32
+    dx = torch.empty((Bz, L, H, P), dtype=f32, device=dev)
+    ddt = torch.empty((Bz, L, H), dtype=f32, device=dev)
+    dA = torch.empty((H,), dtype=f32, device=dev)
+    dB = torch.empty((Bz, L, G, N), dtype=f32, device=dev)
+    dC = torch.empty((Bz, L, G, N), dtype=f32, device=dev)
+    if dh0 is None and want_dh0:
+        dh0 = torch.empty((Bz, H, P, N), dtype=f32, device=dev)
+    need = ssm_scan_bwd_workspace_size(Bz, L, H, P, N, G)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    wsb = workspace.numel() * workspace.element_size()
+    rc = _lib.sss_ssm_scan_bwd(_ptr(x), _dt(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _dt(dt),
+                               _ptr(h0), _ptr(dy), _ptr(dhT), _ptr(dx), _ptr(ddt), _ptr(dA),
+                               _ptr(dB), _ptr(dC), _ptr(dh0), Bz, L, H, P, N, G,
+                               _ptr(workspace), wsb, _stream(stream))
+    _check("sss_ssm_scan_bwd", rc)
+    return dx, ddt, dA, dB, dC, dh0
 
 
 def mixer_fwd_supported(Bz, L, H, P, N, G, K, x_dtype, y_dtype) -> bool:

@@ -50,6 +50,13 @@ cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, c
                                   void* ws, cudaStream_t st);
 size_t conv_state_bwd_workspace(int64_t Bz, int64_t L, int64_t D, int K);
 bool conv_state_bwd_supports(int K);
+size_t ssm_scan_bwd_workspace(int64_t Bz, int64_t L, int H, int P, int N);
+bool ssm_scan_bwd_supports(int P, int N);
+cudaError_t ssm_scan_bwd_launch(const void* x, sss_dtype x_t, const void* dt, const float* A,
+                                const void* B, const void* C, sss_dtype act_t, const float* h0,
+                                const float* dy, const float* dhT, float* dx, float* ddt,
+                                float* dA, float* dB, float* dC, float* dh0, int64_t Bz, int64_t L,
+                                int H, int P, int N, int G, void* ws, cudaStream_t st);
 bool mixer_update_supports(int P, int N, int K, int L_new);
 int mixer_update_path(sss_dtype at, int S_len, int L_new, int P, int N, int K);
 cudaError_t mixer_update_launch(const void* x, sss_dtype at, const float* w, const float* bias,
@@ -238,6 +245,39 @@ sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, co
   if (!ssm_scan_simt_supports(P, N)) return SSS_ERR_UNSUPPORTED;
   return from_cuda(ssm_scan_simt_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y,
                                         y_dtype, Bz, L, H, P, N, G, st));
+}
+
+size_t sss_ssm_scan_bwd_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G) {
+  (void)G;
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1) return 0;
+  return sss::ssm_scan_bwd_workspace(Bz, L, H, P, N);
+}
+
+sss_status sss_ssm_scan_bwd(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
+                            const void* B, const void* C, sss_dtype act_dtype, const float* h0_in,
+                            const float* dy, const float* dhT, float* dx, float* ddt, float* dA,
+                            float* dB, float* dC, float* dh0, int64_t Bz, int64_t L, int H, int P,
+                            int N, int G, void* workspace, size_t workspace_bytes,
+                            sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(act_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return SSS_ERR_INVALID_ARG;
+  if (!sss::ssm_scan_bwd_supports(P, N)) return SSS_ERR_UNSUPPORTED;
+  const size_t xs = dtype_size(x_dtype), as = dtype_size(act_dtype);
+  if (!A || !dA || !aligned(A, 4) || !aligned(dA, 4)) return SSS_ERR_INVALID_ARG;
+  if (Bz > 0 && L > 0 &&
+      (!x || !dt || !B || !C || !dy || !dx || !ddt || !dB || !dC || !aligned(x, xs) ||
+       !aligned(dt, as) || !aligned(B, as) || !aligned(C, as) || !aligned(dy, 4) ||
+       !aligned(dx, 4) || !aligned(ddt, 4) || !aligned(dB, 4) || !aligned(dC, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if ((h0_in && !aligned(h0_in, 4)) || (dhT && !aligned(dhT, 4)) || (dh0 && !aligned(dh0, 4)))
+    return SSS_ERR_INVALID_ARG;
+  const size_t state_bytes = size_t(Bz) * size_t(H) * size_t(P) * size_t(N) * 4;
+  if (dh0 != dhT && ranges_overlap(dh0, dhT, state_bytes)) return SSS_ERR_INVALID_ARG;
+  const size_t need = sss::ssm_scan_bwd_workspace(Bz, L, H, P, N);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::ssm_scan_bwd_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, dy, dhT, dx,
+                                            ddt, dA, dB, dC, dh0, Bz, L, H, P, N, G, workspace,
+                                            reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int sss_mixer_fwd_supported(int64_t Bz, int64_t L, int H, int P, int N, int G, int K,

@@ -1,0 +1,508 @@
+// Gradient of the scalar-decay selective scan with state (dx, ddt, dA, dB,
+// dC and dh0 from dy and the final state's gradient dhT), for state-passing
+// and truncated-backpropagation training: "Understanding and Improving
+// Length Generalization in Recurrent Models" sections 4.4-4.5 (the final
+// state of one segment starts the next; the gradient of that state is the
+// next segment's dh0), with the recurrence of section 2 Eq. (1) and its
+// initial-state form Eq. (4), and the causal-conv chapter's section on
+// chunked training ("the state gradient of chunk B must flow into chunk A").
+//
+// Chunked form.  Cut the sequence into chunks of Q = 64 tokens; inside a
+// chunk let Lam_t be the inclusive sum of l_s = dt_s A_h, M_ts = exp(Lam_t -
+// Lam_s) [s <= t], G = C B^T and W = dY X^T (t x s), h_in the state entering
+// the chunk and g_out = dL/dh at its end.  Then
+//   y     = diag(e^Lam) C h_in^T + (G o M) X
+//   h_out = e^{Lam_e} h_in + X^T diag(e^{Lam_e - Lam}) B
+// and the chunk's gradients are
+//   dX    = (G o M)^T dY + diag(e^{Lam_e - Lam}) B g_out^T
+//   dB    = (W o M)^T C  + diag(e^{Lam_e - Lam}) X g_out
+//   dC    = diag(e^Lam) dY h_in + (W o M) B
+//   dh_in = e^{Lam_e} g_out + dY^T diag(e^Lam) C
+//   dLam_t = dy_t . y_t - sum_t' (G o M o W)_{t' t}
+//            - e^{Lam_e - Lam_t} x_t . (g_out B_t) + [t = e] <g_out, h_out>
+//   dl_t  = sum_{t' >= t in the chunk} dLam_t',  ddt = dl A_h,  dA_h = sum dl dt.
+// Every exponent above is <= 0, so no factor leaves the fp32 range.
+//
+// Kernels (fp32 CUDA-core arithmetic throughout):
+//  1. chunk_states: per (batch, head, 16 state rows) the states entering
+//     every chunk, walking the chunks forward (workspace Hin, with the final
+//     state after the last chunk);
+//  2. chunk_grads:  the same rows walking backward, g_out of every chunk
+//     (workspace Gout) and dh0;
+//  3. chunk_bwd:    per (batch, head, chunk) everything else from the
+//     formulas above, chunk tiles in shared memory; dB and dC per head to
+//     the workspace;
+//  4. reduce:       dB, dC summed over each group's heads, dA over batch and
+//     chunks, in a fixed order (deterministic).
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace sss {
+
+namespace {
+constexpr int kQ = 64;          // chunk length
+constexpr int kMaxP = 64;
+constexpr int kMaxN = 128;
+constexpr int kRows = 16;       // state rows per CTA in kernels 1 and 2
+constexpr int kThreadsB = 256;
+// padded leading dimensions of the shared tiles (odd: column walks spread
+// over the banks)
+constexpr int kLdP = kMaxP + 1;
+constexpr int kLdN = kMaxN + 1;
+
+template <typename T>
+__device__ __forceinline__ float ldf(const T* p) {
+  return to_f32<T>(*p);
+}
+
+// inclusive prefix of l_s = dt_s A_h over the chunk's tokens (zeros past
+// the chunk's end); warp 0, two tokens per lane
+template <typename TA>
+__device__ void chunk_lambda(const TA* __restrict__ dt, int64_t row0, int64_t stride, int Qc,
+                             float Ah, float* lam, float* dts) {
+  if (threadIdx.x < 32) {
+    const int l = threadIdx.x;
+    float v0 = 0.0f, v1 = 0.0f, d0 = 0.0f, d1 = 0.0f;
+    if (2 * l < Qc) d0 = ldf(dt + (row0 + 2 * l) * stride);
+    if (2 * l + 1 < Qc) d1 = ldf(dt + (row0 + 2 * l + 1) * stride);
+    v0 = d0 * Ah;
+    v1 = v0 + d1 * Ah;
+    float s = v1;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, s, o);
+      if (l >= o) s += u;
+    }
+    const float before = s - v1;
+    lam[2 * l] = before + v0;
+    lam[2 * l + 1] = before + v1;
+    dts[2 * l] = d0;
+    dts[2 * l + 1] = d1;
+  }
+}
+
+// ---- kernels 1 and 2: chunk-boundary states and state gradients -----------
+// REV = false: h_in of every chunk (and h after the last) from h0, with
+//   h <- e^{Lam_e} h + sum_s e^{Lam_e - Lam_s} x_s B_s^T.
+// REV = true: g_out of every chunk from dhT, with
+//   g <- e^{Lam_e} g + sum_t e^{Lam_t} dy_t C_t^T, and dh0 = g at the start.
+template <bool REV, typename TX, typename TA>
+__global__ void __launch_bounds__(kThreadsB)
+chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const TA* __restrict__ dt,
+                   const float* __restrict__ A, const TA* __restrict__ BC,
+                   const float* __restrict__ init, float* __restrict__ bound,
+                   float* __restrict__ final_out, int64_t L, int H, int P, int N, int G, int nC) {
+  __shared__ float xs[kQ][kRows];
+  __shared__ float bs[kQ][kMaxN];
+  __shared__ float lam[kQ], dts[kQ], wgt[kQ];
+  const int tid = threadIdx.x;
+  const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (H / G);
+  const int pr = tid >> 4, p = pb * kRows + pr;
+  const bool prow = p < P;
+  const float Ah = A[h];
+  float st[kMaxN / 16];
+  const int64_t soff = (int64_t(b) * H + h) * P * N;
+#pragma unroll
+  for (int j = 0; j < kMaxN / 16; ++j) {
+    const int n = (tid & 15) + 16 * j;
+    st[j] = (prow && n < N && init) ? init[soff + int64_t(p) * N + n] : 0.0f;
+  }
+  for (int k = 0; k < nC; ++k) {
+    const int c = REV ? nC - 1 - k : k;
+    const int64_t t0 = int64_t(c) * kQ;
+    const int Qc = L - t0 < kQ ? int(L - t0) : kQ;
+    // the bound of chunk c before its update: h_in(c), or g_out(c)
+    float* bc = bound + ((int64_t(b) * H + h) * (REV ? nC : nC + 1) + c) * P * N;
+#pragma unroll
+    for (int j = 0; j < kMaxN / 16; ++j) {
+      const int n = (tid & 15) + 16 * j;
+      if (prow && n < N) bc[int64_t(p) * N + n] = st[j];
+    }
+    __syncthreads();  // the previous chunk's tiles are no longer read
+    chunk_lambda(dt + h, int64_t(b) * L + t0, H, Qc, Ah, lam, dts);
+    // x (or dy) of this CTA's rows, and B (or C) of the chunk
+    for (int i = tid; i < kQ * kRows; i += kThreadsB) {
+      const int t = i / kRows, r = i % kRows, pp = pb * kRows + r;
+      float v = 0.0f;
+      if (t < Qc && pp < P) {
+        const int64_t off = ((int64_t(b) * L + t0 + t) * H + h) * P + pp;
+        v = REV ? dy[off] : ldf(x + off);
+      }
+      xs[t][r] = v;
+    }
+    for (int i = tid; i < kQ * kMaxN; i += kThreadsB) {
+      const int t = i / kMaxN, n = i % kMaxN;
+      bs[t][n] = (t < Qc && n < N) ? ldf(BC + ((int64_t(b) * L + t0 + t) * G + g) * N + n) : 0.0f;
+    }
+    __syncthreads();
+    const float lam_e = lam[Qc - 1];
+    if (tid < kQ) wgt[tid] = tid < Qc ? (REV ? expf(lam[tid]) : expf(lam_e - lam[tid])) : 0.0f;
+    __syncthreads();
+    const float dec = expf(lam_e);
+#pragma unroll
+    for (int j = 0; j < kMaxN / 16; ++j) st[j] *= dec;
+    for (int t = 0; t < Qc; ++t) {
+      const float wx = wgt[t] * xs[t][pr];
+#pragma unroll
+      for (int j = 0; j < kMaxN / 16; ++j) st[j] = fmaf(wx, bs[t][(tid & 15) + 16 * j], st[j]);
+    }
+  }
+  if (!REV) {  // the state after the last chunk
+    float* bc = bound + ((int64_t(b) * H + h) * (nC + 1) + nC) * P * N;
+#pragma unroll
+    for (int j = 0; j < kMaxN / 16; ++j) {
+      const int n = (tid & 15) + 16 * j;
+      if (prow && n < N) bc[int64_t(p) * N + n] = st[j];
+    }
+  } else if (final_out) {  // dh0
+#pragma unroll
+    for (int j = 0; j < kMaxN / 16; ++j) {
+      const int n = (tid & 15) + 16 * j;
+      if (prow && n < N) final_out[soff + int64_t(p) * N + n] = st[j];
+    }
+  }
+}
+
+// ---- kernel 3: the chunk's gradients ----------------------------------------
+// out(i, j) = rs(i) * sum_k a1(i,k) b1(k,j) + sum_k a2(i,k) b2(k,j) for
+// i < M, j < Nn, register tiles of 4 x TN per thread; epi(i, j, value).
+struct Op {
+  const float* a;
+  int ai, ak;  // a(i,k) = a[i * ai + k * ak]
+  const float* b;
+  int bk, bj;  // b(k,j) = b[k * bk + j * bj]
+  int K;
+};
+template <int TN, typename RS, typename Epi>
+__device__ __forceinline__ void smem_mm(int M, int Nn, const Op& o1, RS rs, const Op& o2, Epi epi) {
+  const int tn = (Nn + TN - 1) / TN, tm = (M + 3) / 4;
+  for (int tile = threadIdx.x; tile < tm * tn; tile += kThreadsB) {
+    const int i0 = 4 * (tile / tn), j0 = TN * (tile % tn);
+    float acc[4][TN];
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < TN; ++q) acc[r][q] = 0.0f;
+    for (int k = 0; k < o1.K; ++k) {
+      float av[4], bv[TN];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) av[r] = o1.a[(i0 + r) * o1.ai + k * o1.ak];
+#pragma unroll
+      for (int q = 0; q < TN; ++q) bv[q] = o1.b[k * o1.bk + (j0 + q) * o1.bj];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < TN; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const float s = rs(i0 + r);
+#pragma unroll
+      for (int q = 0; q < TN; ++q) acc[r][q] *= s;
+    }
+    for (int k = 0; k < o2.K; ++k) {
+      float av[4], bv[TN];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) av[r] = o2.a[(i0 + r) * o2.ai + k * o2.ak];
+#pragma unroll
+      for (int q = 0; q < TN; ++q) bv[q] = o2.b[k * o2.bk + (j0 + q) * o2.bj];
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int q = 0; q < TN; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int q = 0; q < TN; ++q)
+        if (i0 + r < M && j0 + q < Nn) epi(i0 + r, j0 + q, acc[r][q]);
+  }
+}
+
+struct ChunkSmem {
+  float X[kQ][kLdP], DY[kQ][kLdP];
+  float Bm[kQ][kLdN], Cm[kQ][kLdN];
+  float Hin[kMaxP][kLdN], Go[kMaxP][kLdN];
+  float Gm[kQ][kLdP], Wm[kQ][kLdP];  // [t][s]
+  float S[kQ][kLdP];                  // scratch: y, then B g_out^T
+  float lam[kQ], dts[kQ], el[kQ], ee[kQ];  // Lam, dt, e^Lam, e^{Lam_e - Lam}
+  float At[kQ], Dt[kQ], Et[kQ], red[kThreadsB / 32];
+};
+
+template <typename TX, typename TA>
+__global__ void __launch_bounds__(kThreadsB, 1)
+chunk_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const TA* __restrict__ dt,
+                 const float* __restrict__ A, const TA* __restrict__ B, const TA* __restrict__ C,
+                 const float* __restrict__ Hin_ws, const float* __restrict__ Gout_ws,
+                 float* __restrict__ dx, float* __restrict__ ddt, float* __restrict__ dBp,
+                 float* __restrict__ dCp, float* __restrict__ dAp, int64_t L, int H, int P,
+                 int N, int G, int nC) {
+  extern __shared__ __align__(16) unsigned char smraw[];
+  ChunkSmem& s = *reinterpret_cast<ChunkSmem*>(smraw);
+  const int tid = threadIdx.x;
+  const int c = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int g = h / (H / G);
+  const int64_t t0 = int64_t(c) * kQ;
+  const int Qc = L - t0 < kQ ? int(L - t0) : kQ;
+  const float Ah = A[h];
+  const int64_t hrow = (int64_t(b) * H + h);
+  chunk_lambda(dt + h, int64_t(b) * L + t0, H, Qc, Ah, s.lam, s.dts);
+  // chunk tiles (zero past the chunk's end and past P / N)
+  for (int i = tid; i < kQ * kMaxP; i += kThreadsB) {
+    const int t = i / kMaxP, p = i % kMaxP;
+    float xv = 0.0f, dv = 0.0f;
+    if (t < Qc && p < P) {
+      const int64_t off = ((int64_t(b) * L + t0 + t) * H + h) * P + p;
+      xv = ldf(x + off);
+      dv = dy[off];
+    }
+    s.X[t][p] = xv;
+    s.DY[t][p] = dv;
+  }
+  for (int i = tid; i < kQ * kMaxN; i += kThreadsB) {
+    const int t = i / kMaxN, n = i % kMaxN;
+    float bv = 0.0f, cv = 0.0f;
+    if (t < Qc && n < N) {
+      const int64_t off = ((int64_t(b) * L + t0 + t) * G + g) * N + n;
+      bv = ldf(B + off);
+      cv = ldf(C + off);
+    }
+    s.Bm[t][n] = bv;
+    s.Cm[t][n] = cv;
+  }
+  const float* hin = Hin_ws + (hrow * (nC + 1) + c) * P * N;
+  const float* go = Gout_ws + (hrow * nC + c) * P * N;
+  for (int i = tid; i < kMaxP * kMaxN; i += kThreadsB) {
+    const int p = i / kMaxN, n = i % kMaxN;
+    const bool in = p < P && n < N;
+    s.Hin[p][n] = in ? hin[int64_t(p) * N + n] : 0.0f;
+    s.Go[p][n] = in ? go[int64_t(p) * N + n] : 0.0f;
+  }
+  __syncthreads();
+  const float lam_e = s.lam[Qc - 1];
+  if (tid < kQ) {
+    s.el[tid] = tid < Qc ? expf(s.lam[tid]) : 0.0f;
+    s.ee[tid] = tid < Qc ? expf(lam_e - s.lam[tid]) : 0.0f;
+  }
+  __syncthreads();
+  auto one = [](int) { return 1.0f; };
+  const Op none{nullptr, 0, 0, nullptr, 0, 0, 0};
+  // G o M and W (raw) ------------------------------------------------------
+  smem_mm<4>(Qc, Qc, Op{&s.Cm[0][0], kLdN, 1, &s.Bm[0][0], 1, kLdN, N}, one, none,
+             [&](int t, int sI, float v) {
+               s.Gm[t][sI] = sI <= t ? v * expf(s.lam[t] - s.lam[sI]) : 0.0f;
+             });
+  smem_mm<4>(Qc, Qc, Op{&s.DY[0][0], kLdP, 1, &s.X[0][0], 1, kLdP, P}, one, none,
+             [&](int t, int sI, float v) { s.Wm[t][sI] = v; });
+  __syncthreads();
+  // D_s = sum_t (G o M)_{ts} W_{ts}, then W <- W o M
+  if (tid < Qc) {
+    float d = 0.0f;
+    for (int t = tid; t < Qc; ++t) d = fmaf(s.Gm[t][tid], s.Wm[t][tid], d);
+    s.Dt[tid] = d;
+  }
+  __syncthreads();
+  for (int i = tid; i < kQ * kQ; i += kThreadsB) {
+    const int t = i / kQ, sI = i % kQ;
+    s.Wm[t][sI] = (sI <= t && t < Qc) ? s.Wm[t][sI] * expf(s.lam[t] - s.lam[sI]) : 0.0f;
+  }
+  // y = diag(e^Lam) C h_in^T + (G o M) X, then A_t = dy_t . y_t
+  smem_mm<4>(Qc, P, Op{&s.Cm[0][0], kLdN, 1, &s.Hin[0][0], 1, kLdN, N},
+             [&](int t) { return s.el[t]; },
+             Op{&s.Gm[0][0], kLdP, 1, &s.X[0][0], kLdP, 1, Qc},
+             [&](int t, int p, float v) { s.S[t][p] = v; });
+  __syncthreads();
+  if (tid < Qc) {
+    float a = 0.0f;
+    for (int p = 0; p < P; ++p) a = fmaf(s.DY[tid][p], s.S[tid][p], a);
+    s.At[tid] = a;
+  }
+  __syncthreads();
+  // dC = diag(e^Lam) dY h_in + (W o M) B  (this head's share)
+  float* dCrow = dCp + ((int64_t(b) * L + t0) * H + h) * N;
+  smem_mm<8>(Qc, N, Op{&s.DY[0][0], kLdP, 1, &s.Hin[0][0], kLdN, 1, P},
+             [&](int t) { return s.el[t]; },
+             Op{&s.Wm[0][0], kLdP, 1, &s.Bm[0][0], kLdN, 1, Qc},
+             [&](int t, int n, float v) { dCrow[int64_t(t) * H * N + n] = v; });
+  // B g_out^T into the scratch, then E_s and dX
+  smem_mm<4>(Qc, P, Op{&s.Bm[0][0], kLdN, 1, &s.Go[0][0], 1, kLdN, N}, one, none,
+             [&](int sI, int p, float v) { s.S[sI][p] = v; });
+  __syncthreads();
+  if (tid < Qc) {
+    float e = 0.0f;
+    for (int p = 0; p < P; ++p) e = fmaf(s.X[tid][p], s.S[tid][p], e);
+    s.Et[tid] = s.ee[tid] * e;
+  }
+  float* dxrow = dx + ((int64_t(b) * L + t0) * H + h) * P;
+  smem_mm<4>(Qc, P, Op{&s.Gm[0][0], 1, kLdP, &s.DY[0][0], kLdP, 1, Qc}, one, none,
+             [&](int sI, int p, float v) {
+               dxrow[int64_t(sI) * H * P + p] = fmaf(s.ee[sI], s.S[sI][p], v);
+             });
+  // dB = diag(e^{Lam_e - Lam}) X g_out + (W o M)^T C  (this head's share)
+  float* dBrow = dBp + ((int64_t(b) * L + t0) * H + h) * N;
+  smem_mm<8>(Qc, N, Op{&s.X[0][0], kLdP, 1, &s.Go[0][0], kLdN, 1, P},
+             [&](int sI) { return s.ee[sI]; },
+             Op{&s.Wm[0][0], 1, kLdP, &s.Cm[0][0], kLdN, 1, Qc},
+             [&](int sI, int n, float v) { dBrow[int64_t(sI) * H * N + n] = v; });
+  // <g_out, h_out>, h_out = the next chunk's h_in (or the final state)
+  const float* hout = Hin_ws + (hrow * (nC + 1) + c + 1) * P * N;
+  float part = 0.0f;
+  for (int i = tid; i < P * N; i += kThreadsB) part = fmaf(go[i], hout[i], part);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((tid & 31) == 0) s.red[tid >> 5] = part;
+  __syncthreads();
+  // dLam, its reverse sum over the chunk (dl), ddt and the chunk's dA share
+  if (tid < 32) {
+    float gh = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kThreadsB / 32; ++w) gh += s.red[w];
+    const int l = tid;
+    float v[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = kQ - 1 - (2 * l + e);  // lane 0 holds the chunk's last tokens
+      float d = 0.0f;
+      if (t < Qc) d = s.At[t] - s.Dt[t] - s.Et[t] + (t == Qc - 1 ? gh : 0.0f);
+      v[e] = d;
+    }
+    // inclusive scan over the reversed order = sum over t' >= t
+    const float pair = v[0] + v[1];
+    float sc = pair;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float u = __shfl_up_sync(0xffffffffu, sc, o);
+      if (l >= o) sc += u;
+    }
+    const float before = sc - pair;
+    float dA_acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int t = kQ - 1 - (2 * l + e);
+      const float dl = before + (e == 0 ? v[0] : v[0] + v[1]);
+      if (t < Qc) {
+        ddt[(int64_t(b) * L + t0 + t) * H + h] = dl * Ah;
+        dA_acc = fmaf(dl, s.dts[t], dA_acc);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dA_acc += __shfl_xor_sync(0xffffffffu, dA_acc, o);
+    if (l == 0) dAp[hrow * nC + c] = dA_acc;
+  }
+}
+
+// ---- kernel 4: group sums of dB and dC, dA over batch and chunks -----------
+__global__ void __launch_bounds__(kThreadsB)
+scan_bwd_reduce_kernel(const float* __restrict__ dBp, const float* __restrict__ dCp,
+                       const float* __restrict__ dAp, float* __restrict__ dB,
+                       float* __restrict__ dC, float* __restrict__ dA, int64_t rows, int H,
+                       int N, int G, int64_t Bz, int nC) {
+  const int hpg = H / G;
+  const int64_t total = rows * G * N;
+  for (int64_t i = blockIdx.x * int64_t(kThreadsB) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * kThreadsB) {
+    const int n = int(i % N);
+    const int g = int((i / N) % G);
+    const int64_t r = i / (int64_t(N) * G);
+    float sb = 0.0f, sc = 0.0f;
+    for (int k = 0; k < hpg; ++k) {
+      const int64_t off = (r * H + g * hpg + k) * N + n;
+      sb += dBp[off];
+      sc += dCp[off];
+    }
+    dB[i] = sb;
+    dC[i] = sc;
+  }
+  if (blockIdx.x == 0) {
+    for (int h = threadIdx.x; h < H; h += kThreadsB) {
+      float a = 0.0f;
+      for (int64_t b = 0; b < Bz; ++b)
+        for (int c = 0; c < nC; ++c) a += dAp[(b * H + h) * nC + c];
+      dA[h] = a;
+    }
+  }
+}
+
+struct WsLayout {
+  size_t hin, gout, dbp, dcp, dap, total;
+};
+WsLayout ws_layout(int64_t Bz, int64_t L, int H, int P, int N) {
+  const int64_t nC = (L + kQ - 1) / kQ;
+  auto al = [](size_t v) { return (v + 255) & ~size_t(255); };
+  WsLayout w;
+  w.hin = 0;
+  w.gout = w.hin + al(sizeof(float) * size_t(Bz * H * (nC + 1) * P * N));
+  w.dbp = w.gout + al(sizeof(float) * size_t(Bz * H * nC * P * N));
+  w.dcp = w.dbp + al(sizeof(float) * size_t(Bz * L * H * N));
+  w.dap = w.dcp + al(sizeof(float) * size_t(Bz * L * H * N));
+  w.total = w.dap + al(sizeof(float) * size_t(Bz * H * (nC > 0 ? nC : 1)));
+  return w;
+}
+
+template <typename TX, typename TA>
+cudaError_t launch_bwd(const void* x, const void* dt, const float* A, const void* B, const void* C,
+                       const float* h0, const float* dy, const float* dhT, float* dx, float* ddt,
+                       float* dA, float* dB, float* dC, float* dh0, int64_t Bz, int64_t L, int H,
+                       int P, int N, int G, void* ws, cudaStream_t st) {
+  const int nC = int((L + kQ - 1) / kQ);
+  const WsLayout w = ws_layout(Bz, L, H, P, N);
+  unsigned char* base = static_cast<unsigned char*>(ws);
+  float* hin = reinterpret_cast<float*>(base + w.hin);
+  float* gout = reinterpret_cast<float*>(base + w.gout);
+  float* dbp = reinterpret_cast<float*>(base + w.dbp);
+  float* dcp = reinterpret_cast<float*>(base + w.dcp);
+  float* dap = reinterpret_cast<float*>(base + w.dap);
+  const TX* xx = static_cast<const TX*>(x);
+  const TA* dtt = static_cast<const TA*>(dt);
+  const TA* Bb = static_cast<const TA*>(B);
+  const TA* Cc = static_cast<const TA*>(C);
+  const dim3 gb((P + kRows - 1) / kRows, H, unsigned(Bz));
+  if (Bz > 0) {
+    chunk_bound_kernel<false, TX, TA><<<gb, kThreadsB, 0, st>>>(xx, dy, dtt, A, Bb, h0, hin, nullptr,
+                                                                L, H, P, N, G, nC);
+    chunk_bound_kernel<true, TX, TA><<<gb, kThreadsB, 0, st>>>(xx, dy, dtt, A, Cc, dhT, gout, dh0,
+                                                               L, H, P, N, G, nC);
+  }
+  if (nC > 0 && Bz > 0) {
+    auto k3 = chunk_bwd_kernel<TX, TA>;
+    const int smem = int(sizeof(ChunkSmem));
+    cudaFuncSetAttribute(k3, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    k3<<<dim3(nC, H, unsigned(Bz)), kThreadsB, smem, st>>>(xx, dy, dtt, A, Bb, Cc, hin, gout, dx,
+                                                           ddt, dbp, dcp, dap, L, H, P, N, G, nC);
+  }
+  const int64_t rows = Bz * L;
+  const int64_t total = rows * G * N;
+  const int blocks = int(std::max<int64_t>(1, std::min<int64_t>((total + kThreadsB - 1) / kThreadsB, 4096)));
+  scan_bwd_reduce_kernel<<<blocks, kThreadsB, 0, st>>>(dbp, dcp, dap, dB, dC, dA, rows, H, N, G,
+                                                       Bz, nC);
+  return cudaGetLastError();
+}
+}  // namespace
+
+size_t ssm_scan_bwd_workspace(int64_t Bz, int64_t L, int H, int P, int N) {
+  return ws_layout(Bz, L, H, P, N).total;
+}
+
+cudaError_t ssm_scan_bwd_launch(const void* x, sss_dtype x_t, const void* dt, const float* A,
+                                const void* B, const void* C, sss_dtype act_t, const float* h0,
+                                const float* dy, const float* dhT, float* dx, float* ddt,
+                                float* dA, float* dB, float* dC, float* dh0, int64_t Bz, int64_t L,
+                                int H, int P, int N, int G, void* ws, cudaStream_t st) {
+  if (x_t == SSS_BF16 && act_t == SSS_BF16)
+    return launch_bwd<__nv_bfloat16, __nv_bfloat16>(x, dt, A, B, C, h0, dy, dhT, dx, ddt, dA, dB,
+                                                    dC, dh0, Bz, L, H, P, N, G, ws, st);
+  if (x_t == SSS_F32 && act_t == SSS_BF16)
+    return launch_bwd<float, __nv_bfloat16>(x, dt, A, B, C, h0, dy, dhT, dx, ddt, dA, dB, dC, dh0,
+                                            Bz, L, H, P, N, G, ws, st);
+  if (x_t == SSS_BF16 && act_t == SSS_F32)
+    return launch_bwd<__nv_bfloat16, float>(x, dt, A, B, C, h0, dy, dhT, dx, ddt, dA, dB, dC, dh0,
+                                            Bz, L, H, P, N, G, ws, st);
+  return launch_bwd<float, float>(x, dt, A, B, C, h0, dy, dhT, dx, ddt, dA, dB, dC, dh0, Bz, L, H,
+                                  P, N, G, ws, st);
+}
+
+bool ssm_scan_bwd_supports(int P, int N) { return P >= 1 && P <= kMaxP && N >= 1 && N <= kMaxN; }
+
+}  // namespace sss

@@ -117,3 +117,40 @@ def test_conv_backward_host_checks(lib):
     assert call(args(ds=a(6))) == 1                  # dS would overwrite dF
     assert call(args(dw=None)) == 1                  # no weight gradient buffer
     assert call(args(Bz=0)) == 0                     # empty batch: nothing to do
+
+
+def test_scan_backward_host_checks(lib):
+    """Workspace size and argument checks of the scan backward (each case
+    returns before any launch)."""
+    i64, ci = ctypes.c_int64, ctypes.c_int
+    ws = lib.sss_ssm_scan_bwd_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i64, i64, ci, ci, ci, ci]
+    al = lambda v: (v + 255) // 256 * 256
+    # chunk-entry states (one more than the 64-token chunks), chunk-end state
+    # gradients, per-head dB and dC shares and per-chunk dA shares, fp32
+    Bz, L, H, P, N = 2, 130, 4, 64, 128
+    nC = 3
+    expect = (al(4 * Bz * H * (nC + 1) * P * N) + al(4 * Bz * H * nC * P * N)
+              + 2 * al(4 * Bz * L * H * N) + al(4 * Bz * H * nC))
+    assert ws(Bz, L, H, P, N, 1) == expect
+    f = lib.sss_ssm_scan_bwd
+    f.restype = ci
+    Pp = ctypes.c_void_p
+    f.argtypes = [Pp, ci, Pp, Pp, Pp, Pp, ci, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp,
+                  i64, i64, ci, ci, ci, ci, Pp, ctypes.c_size_t, Pp]
+    a = lambda k: ctypes.c_void_p(0x10000000 * k)  # aligned stand-ins, never dereferenced
+    args = lambda **kw: dict(dict(x=a(1), xt=1, dt=a(2), A=a(3), B=a(4), C=a(5), at=1, h0=a(6),
+                                  dy=a(7), dhT=a(8), dx=a(9), ddt=a(10), dA=a(11), dB=a(12),
+                                  dC=a(13), dh0=a(14), Bz=Bz, L=L, H=H, P=P, N=N, G=1,
+                                  ws=a(15), wsb=expect, st=None), **kw)
+    call = lambda d: f(*d.values())
+    assert call(args(P=65)) == 2                     # P > 64
+    assert call(args(N=129)) == 2                    # N > 128
+    assert call(args(G=3)) == 1                      # H not a multiple of G
+    assert call(args(xt=7)) == 1                     # unknown dtype
+    assert call(args(wsb=expect - 1)) == 1           # workspace too small
+    assert call(args(ws=None)) == 1                  # no workspace
+    assert call(args(dB=None)) == 1                  # no dB buffer
+    assert call(args(dh0=ctypes.c_void_p(0x80000000 + 64))) == 1  # dh0 half over dhT
+    assert call(args(dy=ctypes.c_void_p(0x70000002))) == 1        # misaligned dy
