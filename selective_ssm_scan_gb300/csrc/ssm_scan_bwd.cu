@@ -24,7 +24,7 @@
 // Every exponent above is <= 0, so no factor leaves the fp32 range.
 //
 // Kernels (fp32 CUDA-core arithmetic throughout):
-//  1. chunk_states: per (batch, head, 16 state rows) the states entering
+//  1. chunk_states: per (batch, head) the states entering
 //     every chunk, walking the chunks forward (workspace Hin, with the final
 //     state after the last chunk);
 //  2. chunk_grads:  the same rows walking backward, g_out of every chunk
@@ -44,7 +44,6 @@ namespace {
 constexpr int kQ = 64;          // chunk length
 constexpr int kMaxP = 64;
 constexpr int kMaxN = 128;
-constexpr int kRows = 16;       // state rows per CTA in kernels 1 and 2
 constexpr int kThreadsB = 256;
 // padded leading dimensions of the shared tiles (odd: column walks spread
 // over the banks)
@@ -54,6 +53,26 @@ constexpr int kLdN = kMaxN + 1;
 template <typename T>
 __device__ __forceinline__ float ldf(const T* p) {
   return to_f32<T>(*p);
+}
+
+// for i < total: put(i, get(i)), eight independent loads in flight per
+// thread before any store (a rolled loop of single loads waits one memory
+// round trip per element)
+template <typename Get, typename Put>
+__device__ __forceinline__ void batched_copy(int total, Get get, Put put) {
+  for (int base = threadIdx.x; base < total; base += kThreadsB * 8) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * kThreadsB;
+      v[u] = i < total ? get(i) : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * kThreadsB;
+      if (i < total) put(i, v[u]);
+    }
+  }
 }
 
 // inclusive prefix of l_s = dt_s A_h over the chunk's tokens (zeros past
@@ -87,28 +106,36 @@ __device__ void chunk_lambda(const TA* __restrict__ dt, int64_t row0, int64_t st
 //   h <- e^{Lam_e} h + sum_s e^{Lam_e - Lam_s} x_s B_s^T.
 // REV = true: g_out of every chunk from dhT, with
 //   g <- e^{Lam_e} g + sum_t e^{Lam_t} dy_t C_t^T, and dh0 = g at the start.
+// One CTA per (batch, head); thread (pq, nq) holds state rows 4 pq .. 4 pq + 3
+// and columns nq + 16 j (j < 8), so one float4 of x and eight B values feed
+// 32 FMAs per token.
+struct BoundSmem {
+  float xs[kQ][kMaxP];
+  float bs[kQ][kMaxN];
+  float lam[kQ], dts[kQ], wgt[kQ];
+};
+
 template <bool REV, typename TX, typename TA>
 __global__ void __launch_bounds__(kThreadsB)
 chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const TA* __restrict__ dt,
                    const float* __restrict__ A, const TA* __restrict__ BC,
                    const float* __restrict__ init, float* __restrict__ bound,
                    float* __restrict__ final_out, int64_t L, int H, int P, int N, int G, int nC) {
-  __shared__ float xs[kQ][kRows];
-  __shared__ float bs[kQ][kMaxN];
-  __shared__ float lam[kQ], dts[kQ], wgt[kQ];
+  extern __shared__ __align__(16) unsigned char smraw[];
+  BoundSmem& sm = *reinterpret_cast<BoundSmem*>(smraw);
   const int tid = threadIdx.x;
-  const int pb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int h = blockIdx.x, b = blockIdx.y;
   const int g = h / (H / G);
-  const int pr = tid >> 4, p = pb * kRows + pr;
-  const bool prow = p < P;
+  const int pq = tid >> 4, nq = tid & 15;
   const float Ah = A[h];
-  float st[kMaxN / 16];
+  float st[4][kMaxN / 16];
   const int64_t soff = (int64_t(b) * H + h) * P * N;
+  auto in = [&](int r, int j) { return 4 * pq + r < P && nq + 16 * j < N; };
+  auto sidx = [&](int r, int j) { return int64_t(4 * pq + r) * N + nq + 16 * j; };
 #pragma unroll
-  for (int j = 0; j < kMaxN / 16; ++j) {
-    const int n = (tid & 15) + 16 * j;
-    st[j] = (prow && n < N && init) ? init[soff + int64_t(p) * N + n] : 0.0f;
-  }
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int j = 0; j < kMaxN / 16; ++j) st[r][j] = (init && in(r, j)) ? init[soff + sidx(r, j)] : 0.0f;
   for (int k = 0; k < nC; ++k) {
     const int c = REV ? nC - 1 - k : k;
     const int64_t t0 = int64_t(c) * kQ;
@@ -116,52 +143,59 @@ chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const
     // the bound of chunk c before its update: h_in(c), or g_out(c)
     float* bc = bound + ((int64_t(b) * H + h) * (REV ? nC : nC + 1) + c) * P * N;
 #pragma unroll
-    for (int j = 0; j < kMaxN / 16; ++j) {
-      const int n = (tid & 15) + 16 * j;
-      if (prow && n < N) bc[int64_t(p) * N + n] = st[j];
-    }
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < kMaxN / 16; ++j)
+        if (in(r, j)) bc[sidx(r, j)] = st[r][j];
     __syncthreads();  // the previous chunk's tiles are no longer read
-    chunk_lambda(dt + h, int64_t(b) * L + t0, H, Qc, Ah, lam, dts);
-    // x (or dy) of this CTA's rows, and B (or C) of the chunk
-    for (int i = tid; i < kQ * kRows; i += kThreadsB) {
-      const int t = i / kRows, r = i % kRows, pp = pb * kRows + r;
-      float v = 0.0f;
-      if (t < Qc && pp < P) {
-        const int64_t off = ((int64_t(b) * L + t0 + t) * H + h) * P + pp;
-        v = REV ? dy[off] : ldf(x + off);
-      }
-      xs[t][r] = v;
-    }
-    for (int i = tid; i < kQ * kMaxN; i += kThreadsB) {
-      const int t = i / kMaxN, n = i % kMaxN;
-      bs[t][n] = (t < Qc && n < N) ? ldf(BC + ((int64_t(b) * L + t0 + t) * G + g) * N + n) : 0.0f;
-    }
+    chunk_lambda(dt + h, int64_t(b) * L + t0, H, Qc, Ah, sm.lam, sm.dts);
+    batched_copy(
+        kQ * kMaxP,
+        [&](int i) {
+          const int t = i / kMaxP, pp = i % kMaxP;
+          if (t >= Qc || pp >= P) return 0.0f;
+          const int64_t off = ((int64_t(b) * L + t0 + t) * H + h) * P + pp;
+          return REV ? dy[off] : ldf(x + off);
+        },
+        [&](int i, float v) { sm.xs[i / kMaxP][i % kMaxP] = v; });
+    batched_copy(
+        kQ * kMaxN,
+        [&](int i) {
+          const int t = i / kMaxN, n = i % kMaxN;
+          return (t < Qc && n < N) ? ldf(BC + ((int64_t(b) * L + t0 + t) * G + g) * N + n) : 0.0f;
+        },
+        [&](int i, float v) { sm.bs[i / kMaxN][i % kMaxN] = v; });
     __syncthreads();
-    const float lam_e = lam[Qc - 1];
-    if (tid < kQ) wgt[tid] = tid < Qc ? (REV ? expf(lam[tid]) : expf(lam_e - lam[tid])) : 0.0f;
+    const float lam_e = sm.lam[Qc - 1];
+    if (tid < kQ)
+      sm.wgt[tid] = tid < Qc ? (REV ? expf(sm.lam[tid]) : expf(lam_e - sm.lam[tid])) : 0.0f;
     __syncthreads();
     const float dec = expf(lam_e);
 #pragma unroll
-    for (int j = 0; j < kMaxN / 16; ++j) st[j] *= dec;
-    for (int t = 0; t < Qc; ++t) {
-      const float wx = wgt[t] * xs[t][pr];
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int j = 0; j < kMaxN / 16; ++j) st[j] = fmaf(wx, bs[t][(tid & 15) + 16 * j], st[j]);
+      for (int j = 0; j < kMaxN / 16; ++j) st[r][j] *= dec;
+    for (int t = 0; t < Qc; ++t) {
+      const float w = sm.wgt[t];
+      const float4 xv = *reinterpret_cast<const float4*>(&sm.xs[t][4 * pq]);
+      const float wx[4] = {w * xv.x, w * xv.y, w * xv.z, w * xv.w};
+#pragma unroll
+      for (int j = 0; j < kMaxN / 16; ++j) {
+        const float bv = sm.bs[t][nq + 16 * j];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) st[r][j] = fmaf(wx[r], bv, st[r][j]);
+      }
     }
   }
-  if (!REV) {  // the state after the last chunk
-    float* bc = bound + ((int64_t(b) * H + h) * (nC + 1) + nC) * P * N;
+  // the state after the last chunk, or dh0
+  float* out = REV ? (final_out ? final_out + soff : nullptr)
+                   : bound + ((int64_t(b) * H + h) * (nC + 1) + nC) * P * N;
+  if (out) {
 #pragma unroll
-    for (int j = 0; j < kMaxN / 16; ++j) {
-      const int n = (tid & 15) + 16 * j;
-      if (prow && n < N) bc[int64_t(p) * N + n] = st[j];
-    }
-  } else if (final_out) {  // dh0
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int j = 0; j < kMaxN / 16; ++j) {
-      const int n = (tid & 15) + 16 * j;
-      if (prow && n < N) final_out[soff + int64_t(p) * N + n] = st[j];
-    }
+      for (int j = 0; j < kMaxN / 16; ++j)
+        if (in(r, j)) out[sidx(r, j)] = st[r][j];
   }
 }
 
@@ -250,36 +284,26 @@ chunk_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const T
   const int64_t hrow = (int64_t(b) * H + h);
   chunk_lambda(dt + h, int64_t(b) * L + t0, H, Qc, Ah, s.lam, s.dts);
   // chunk tiles (zero past the chunk's end and past P / N)
-  for (int i = tid; i < kQ * kMaxP; i += kThreadsB) {
-    const int t = i / kMaxP, p = i % kMaxP;
-    float xv = 0.0f, dv = 0.0f;
-    if (t < Qc && p < P) {
-      const int64_t off = ((int64_t(b) * L + t0 + t) * H + h) * P + p;
-      xv = ldf(x + off);
-      dv = dy[off];
-    }
-    s.X[t][p] = xv;
-    s.DY[t][p] = dv;
-  }
-  for (int i = tid; i < kQ * kMaxN; i += kThreadsB) {
-    const int t = i / kMaxN, n = i % kMaxN;
-    float bv = 0.0f, cv = 0.0f;
-    if (t < Qc && n < N) {
-      const int64_t off = ((int64_t(b) * L + t0 + t) * G + g) * N + n;
-      bv = ldf(B + off);
-      cv = ldf(C + off);
-    }
-    s.Bm[t][n] = bv;
-    s.Cm[t][n] = cv;
-  }
+  auto xoff = [&](int i) { return ((int64_t(b) * L + t0 + i / kMaxP) * H + h) * P + i % kMaxP; };
+  auto xin = [&](int i) { return i / kMaxP < Qc && i % kMaxP < P; };
+  batched_copy(kQ * kMaxP, [&](int i) { return xin(i) ? ldf(x + xoff(i)) : 0.0f; },
+               [&](int i, float v) { s.X[i / kMaxP][i % kMaxP] = v; });
+  batched_copy(kQ * kMaxP, [&](int i) { return xin(i) ? dy[xoff(i)] : 0.0f; },
+               [&](int i, float v) { s.DY[i / kMaxP][i % kMaxP] = v; });
+  auto boff = [&](int i) { return ((int64_t(b) * L + t0 + i / kMaxN) * G + g) * N + i % kMaxN; };
+  auto bin = [&](int i) { return i / kMaxN < Qc && i % kMaxN < N; };
+  batched_copy(kQ * kMaxN, [&](int i) { return bin(i) ? ldf(B + boff(i)) : 0.0f; },
+               [&](int i, float v) { s.Bm[i / kMaxN][i % kMaxN] = v; });
+  batched_copy(kQ * kMaxN, [&](int i) { return bin(i) ? ldf(C + boff(i)) : 0.0f; },
+               [&](int i, float v) { s.Cm[i / kMaxN][i % kMaxN] = v; });
   const float* hin = Hin_ws + (hrow * (nC + 1) + c) * P * N;
   const float* go = Gout_ws + (hrow * nC + c) * P * N;
-  for (int i = tid; i < kMaxP * kMaxN; i += kThreadsB) {
-    const int p = i / kMaxN, n = i % kMaxN;
-    const bool in = p < P && n < N;
-    s.Hin[p][n] = in ? hin[int64_t(p) * N + n] : 0.0f;
-    s.Go[p][n] = in ? go[int64_t(p) * N + n] : 0.0f;
-  }
+  auto sin_ = [&](int i) { return i / kMaxN < P && i % kMaxN < N; };
+  auto soff = [&](int i) { return int64_t(i / kMaxN) * N + i % kMaxN; };
+  batched_copy(kMaxP * kMaxN, [&](int i) { return sin_(i) ? hin[soff(i)] : 0.0f; },
+               [&](int i, float v) { s.Hin[i / kMaxN][i % kMaxN] = v; });
+  batched_copy(kMaxP * kMaxN, [&](int i) { return sin_(i) ? go[soff(i)] : 0.0f; },
+               [&](int i, float v) { s.Go[i / kMaxN][i % kMaxN] = v; });
   __syncthreads();
   const float lam_e = s.lam[Qc - 1];
   if (tid < kQ) {
@@ -458,12 +482,15 @@ cudaError_t launch_bwd(const void* x, const void* dt, const float* A, const void
   const TA* dtt = static_cast<const TA*>(dt);
   const TA* Bb = static_cast<const TA*>(B);
   const TA* Cc = static_cast<const TA*>(C);
-  const dim3 gb((P + kRows - 1) / kRows, H, unsigned(Bz));
+  const dim3 gb(H, unsigned(Bz));
   if (Bz > 0) {
-    chunk_bound_kernel<false, TX, TA><<<gb, kThreadsB, 0, st>>>(xx, dy, dtt, A, Bb, h0, hin, nullptr,
-                                                                L, H, P, N, G, nC);
-    chunk_bound_kernel<true, TX, TA><<<gb, kThreadsB, 0, st>>>(xx, dy, dtt, A, Cc, dhT, gout, dh0,
-                                                               L, H, P, N, G, nC);
+    const int bsm = int(sizeof(BoundSmem));
+    auto k1 = chunk_bound_kernel<false, TX, TA>;
+    auto k2 = chunk_bound_kernel<true, TX, TA>;
+    cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, bsm);
+    cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, bsm);
+    k1<<<gb, kThreadsB, bsm, st>>>(xx, dy, dtt, A, Bb, h0, hin, nullptr, L, H, P, N, G, nC);
+    k2<<<gb, kThreadsB, bsm, st>>>(xx, dy, dtt, A, Cc, dhT, gout, dh0, L, H, P, N, G, nC);
   }
   if (nC > 0 && Bz > 0) {
     auto k3 = chunk_bwd_kernel<TX, TA>;
