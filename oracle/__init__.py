@@ -196,7 +196,9 @@ def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, nthreads: int =
 
 def mixer_update(x, w, bias, conv_pool, cache_seqlens, conv_state_indices, dt, A, B, C,
                  ssm_pool, nthreads: int = 0):
-    """x [Bz, L_new, D]; conv_pool [pool, D, S_len]; cache_seqlens [Bz] int;
+    """x [Bz, L_new, D]; conv_pool [pool, D, S_len]; cache_seqlens [Bz] int, or
+    None for the non-circular mode (each row holds its newest S_len inputs,
+    oldest first, and is shifted by L_new);
     conv_state_indices [Bz] int | None (identity); dt [Bz, L_new, H]; A [H];
     B/C [Bz, L_new, G, N]; ssm_pool [pool, H, P, N].
 
@@ -212,14 +214,16 @@ def mixer_update(x, w, bias, conv_pool, cache_seqlens, conv_state_indices, dt, A
     P = D // H
     G, N = B.shape[2], B.shape[3]
     K = w.shape[1]
-    sl = np.ascontiguousarray(getattr(cache_seqlens, "data", cache_seqlens), dtype=np.int32)
+    sl = None
+    if cache_seqlens is not None:
+        sl = np.ascontiguousarray(getattr(cache_seqlens, "data", cache_seqlens), dtype=np.int32)
     ix = None
     if conv_state_indices is not None:
         ix = np.ascontiguousarray(getattr(conv_state_indices, "data", conv_state_indices),
                                   dtype=np.int32)
     y = np.empty((Bz, Lnew, H, P))
     rc = lib().orc_mixer_update(_ptr(x), _ptr(w), _ptr(bias), _ptr(cp), pool, S_len,
-                                sl.ctypes.data_as(_ip),
+                                sl.ctypes.data_as(_ip) if sl is not None else ctypes.cast(None, _ip),
                                 ix.ctypes.data_as(_ip) if ix is not None else ctypes.cast(None, _ip),
                                 _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(sp), _ptr(y),
                                 Bz, Lnew, H, P, N, G, K, nthreads)

@@ -54,6 +54,11 @@
  *                       read, the stored value is the input x (not the
  *                       output), rows are addressed through
  *                       conv_state_indices, cache_seqlens is not advanced;
+ *                       without cache_seqlens, the non-circular mode of
+ *                       "the physical cache can be longer": a row keeps its
+ *                       newest S_len >= K-1 inputs oldest first, the conv
+ *                       reads the last K-1 of them, and the row drops its
+ *                       oldest L_new inputs and appends the new ones;
  *                       then the same recurrence on the pool's SSM state.
  *
  * Threads split only independent (batch, channel) / (batch, head) / request
@@ -401,7 +406,10 @@ static void upd_item(void* p, long b) {
   const long Lnew = c->Lnew, S_len = c->S_len;
   const int K = c->K;
   const long r = c->idx ? (long)c->idx[b] : b;
-  const long pl = (long)c->seqlens[b];
+  /* no lengths: the non-circular mode, the row holds the newest S_len
+     inputs oldest first (as if its write pointer were always at S_len) */
+  const int circular = c->seqlens != NULL;
+  const long pl = circular ? (long)c->seqlens[b] : S_len;
   if (r < 0 || r >= c->pool || pl < 0) {
     c->bad[b] = 1;
     for (long i = 0; i < Lnew * D; ++i) c->y[b * Lnew * D + i] = 0.0;
@@ -422,9 +430,19 @@ static void upd_item(void* p, long b) {
       for (int k = 0; k < K; ++k) z += c->w[d * K + k] * ext[i + k];
       u[i * D + d] = silu(z);
     }
-    /* store the inputs (not the outputs) at the write pointer */
-    for (long i = 0; i < Lnew; ++i)
-      row[d * S_len + pos_mod(pl + i, S_len)] = c->x[(b * Lnew + i) * D + d];
+    if (circular) {
+      /* store the inputs (not the outputs) at the write pointer */
+      for (long i = 0; i < Lnew; ++i)
+        row[d * S_len + pos_mod(pl + i, S_len)] = c->x[(b * Lnew + i) * D + d];
+    } else {
+      /* drop the oldest L_new inputs, append the new ones: the row becomes
+         the last S_len entries of [row, x_0 .. x_{L_new-1}] */
+      double* seq = (double*)malloc(sizeof(double) * (size_t)(S_len + Lnew));
+      for (long j = 0; j < S_len; ++j) seq[j] = row[d * S_len + j];
+      for (long i = 0; i < Lnew; ++i) seq[S_len + i] = c->x[(b * Lnew + i) * D + d];
+      for (long j = 0; j < S_len; ++j) row[d * S_len + j] = seq[Lnew + j];
+      free(seq);
+    }
   }
   for (long hd = 0; hd < H; ++hd) {
     const long g = hd / (H / G);

@@ -346,6 +346,57 @@ def test_update_equals_forward_from_gathered_state(Lnew, S_len, K):
     np.testing.assert_array_equal(sp[untouched], c["ssm_pool"][untouched])
 
 
+@pytest.mark.parametrize("S_len", [2, 4])
+def test_noncircular_single_token_example(S_len):
+    """Non-circular mode, K = 3 (the single-token update: the window is the
+    newest K-1 stored inputs then x_t; the oldest input is dropped and x_t
+    appended; the physical row may be longer than K-1).  Row [.., a, b],
+    x = c: one-hot weights pick a, b, c in tap order and the row becomes
+    [.., b, c]."""
+    K = 3
+    row = np.array([1.0, 10.0, 100.0, 1000.0])[-S_len:]
+    pool = row.reshape(1, 1, S_len)
+    xnew = np.array([7.0]).reshape(1, 1, 1)
+    one = np.ones((1, 1, 1, 1))
+    picked = []
+    for k in range(K):
+        w = np.zeros((1, K))
+        w[0, k] = 1.0
+        # a = exp(-1e5) = 0 and B = C = 1: y equals the conv output
+        y, cp, sp, nbad = oracle.mixer_update(xnew, w, np.zeros(1), pool, None, None,
+                                              np.ones((1, 1, 1)), np.array([-1e5]), one, one,
+                                              np.zeros((1, 1, 1, 1)))
+        assert nbad == 0
+        picked.append(y[0, 0, 0, 0])
+        np.testing.assert_array_equal(cp.reshape(-1), np.concatenate([row[1:], [7.0]]))
+    np.testing.assert_allclose(picked, silu(np.array([row[-2], row[-1], 7.0])), rtol=1e-15)
+
+
+@pytest.mark.parametrize("Lnew,S_len,K", [(1, 3, 4), (2, 4, 4), (4, 4, 4), (6, 4, 4), (3, 7, 4),
+                                          (5, 2, 3)])
+def test_noncircular_update_equals_forward_from_newest_inputs(Lnew, S_len, K):
+    """Non-circular mode on L_new tokens equals the conv-with-state forward
+    plus the scan started from the row's newest K-1 inputs; the row then holds
+    the last S_len entries of [row, x_0 .. x_{L_new-1}] (x, not y)."""
+    g = np.random.default_rng(70 + Lnew * 10 + S_len)
+    c = _decode_case(g, Lnew=Lnew, S_len=S_len, K=K)
+    c["cache_seqlens"] = None
+    y, cp, sp, nbad = oracle.mixer_update(**c)
+    assert nbad == 0
+    pool = c["conv_pool"]
+    for b, r in enumerate(c["conv_state_indices"]):
+        hist = pool[r, :, S_len - (K - 1):]
+        yb, Fb, hb = oracle.mixer_fwd(c["x"][b:b + 1], c["dt"][b:b + 1], c["A"],
+                                      c["B"][b:b + 1], c["C"][b:b + 1], c["w"], c["bias"],
+                                      hist[None], c["ssm_pool"][r:r + 1])
+        np.testing.assert_allclose(y[b], yb[0], rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(sp[r], hb[0], rtol=1e-12, atol=1e-12)
+        seq = np.concatenate([pool[r], c["x"][b].T], axis=1)
+        np.testing.assert_array_equal(cp[r], seq[:, Lnew:Lnew + S_len])
+    untouched = np.setdiff1d(np.arange(pool.shape[0]), c["conv_state_indices"])
+    np.testing.assert_array_equal(cp[untouched], pool[untouched])
+
+
 def test_update_skips_bad_rows():
     g = np.random.default_rng(40)
     c = _decode_case(g)
