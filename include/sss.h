@@ -311,6 +311,12 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w,
  * head the recurrence above runs over the L_new tokens on
  * ssm_pool[r, h] (fp32, updated in place) and writes y.
  * cache_seqlens is NOT advanced: the caller adds L_new after the call.
+ * cache_seqlens NULL selects the non-circular mode of the same chapter
+ * ("the physical cache may be longer than the minimum history"): each row
+ * holds its newest S_len >= K-1 inputs, oldest at slot 0; the history of the
+ * first new token is slots S_len-K+1 .. S_len-1, and after the call the row
+ * holds the last S_len entries of [row, x_0 .. x_{L_new-1}] (the oldest L_new
+ * dropped, the new inputs appended).
  * A slot reused for a new request must be cleared by the caller (p < K-1
  * reads the wrapped slots as they are).  Two rows naming the same pool row
  * is a contract violation (undefined result).  A row with r outside
@@ -320,7 +326,7 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w,
  *  x_new              [Bz, L_new, D]      act_dtype
  *  w, bias            [D, K], [D]         float32 (bias NULL = 0)
  *  conv_pool          [pool, D, S_len]    act_dtype, S_len >= K-1, in/out
- *  cache_seqlens      [Bz]                int32 (device)
+ *  cache_seqlens      [Bz]                int32 (device); NULL = non-circular
  *  conv_state_indices [Bz]                int32 (device), NULL = identity
  *  dt                 [Bz, L_new, H]      act_dtype
  *  A                  [H]                 float32

@@ -327,22 +327,24 @@ def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, conv_state_out=
 
 
 def mixer_update(x_new: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
-                 conv_pool: torch.Tensor, cache_seqlens: torch.Tensor,
+                 conv_pool: torch.Tensor, cache_seqlens: Optional[torch.Tensor],
                  conv_state_indices: Optional[torch.Tensor], dt: torch.Tensor, A: torch.Tensor,
                  B: torch.Tensor, C: torch.Tensor, ssm_pool: torch.Tensor,
                  y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """x_new [Bz, L_new, D]; conv_pool [pool, D, S_len] (updated in place);
     cache_seqlens, conv_state_indices [Bz] int32; dt [Bz, L_new, H]; A [H];
     B, C [Bz, L_new, G, N]; ssm_pool [pool, H, P, N] fp32 (updated in place).
-    Returns y [Bz, L_new, H, P].  cache_seqlens is not advanced."""
+    Returns y [Bz, L_new, H, P].  cache_seqlens is not advanced; None selects
+    the non-circular mode (each row keeps its newest S_len inputs, oldest
+    first, and is shifted by L_new)."""
     Bz, L_new, D = x_new.shape
     H = dt.shape[2]
     P = D // H
     pool, _, S_len = conv_pool.shape
     G, N = B.shape[2], B.shape[3]
     K = w.shape[1]
-    if cache_seqlens.dtype != torch.int32 or (conv_state_indices is not None and
-                                              conv_state_indices.dtype != torch.int32):
+    if (cache_seqlens is not None and cache_seqlens.dtype != torch.int32) or (
+            conv_state_indices is not None and conv_state_indices.dtype != torch.int32):
         raise TypeError("cache_seqlens and conv_state_indices must be int32")
     if y is None:
         y = torch.empty((Bz, L_new, H, P), dtype=x_new.dtype, device=x_new.device)

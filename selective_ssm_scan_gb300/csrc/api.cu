@@ -342,11 +342,12 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype, const float*
   if (!mixer_update_supports(P, N, K, L_new)) return SSS_ERR_UNSUPPORTED;
   if (Bz == 0 || L_new == 0) return SSS_OK;
   const size_t as = dtype_size(act_dtype);
-  if (!x_new || !w || !conv_pool || !cache_seqlens || !dt || !A || !B || !C || !ssm_pool || !y)
+  if (!x_new || !w || !conv_pool || !dt || !A || !B || !C || !ssm_pool || !y)
     return SSS_ERR_INVALID_ARG;
   if (!aligned(x_new, as) || !aligned(conv_pool, as) || !aligned(dt, as) || !aligned(B, as) ||
       !aligned(C, as) || !aligned(y, as) || !aligned(w, 4) || (bias && !aligned(bias, 4)) ||
-      !aligned(A, 4) || !aligned(ssm_pool, 16) || !aligned(cache_seqlens, 4) ||
+      !aligned(A, 4) || !aligned(ssm_pool, 16) ||
+      (cache_seqlens && !aligned(cache_seqlens, 4)) ||
       (conv_state_indices && !aligned(conv_state_indices, 4)))
     return SSS_ERR_INVALID_ARG;
   return from_cuda(mixer_update_launch(x_new, act_dtype, w, bias, conv_pool, pool, S_len,

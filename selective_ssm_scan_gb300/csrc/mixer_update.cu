@@ -82,7 +82,9 @@ mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int D = H * P;
   const int64_t r = idx ? int64_t(idx[b]) : int64_t(b);
-  const int64_t p0 = int64_t(seqlens[b]);
+  // no lengths: the non-circular mode, whose newest S_len inputs sit in
+  // slots 0 .. S_len-1 oldest first (the history reads as if p = S_len)
+  const int64_t p0 = seqlens ? int64_t(seqlens[b]) : int64_t(S_len);
 
   if (r < 0 || r >= pool || p0 < 0) {
     for (int i = tid; i < L_new * P; i += blockDim.x) {
@@ -138,10 +140,18 @@ mixer_update_kernel(const T* __restrict__ x, const float* __restrict__ w,
       for (int k = 0; k < KT - 1; ++k)
         if (k == K - 2) win[k] = xv;
     }
-    // store the inputs (not the outputs) at the write pointer, in token
-    // order, after all reads of this channel's row
-    for (int i = 0; i < L_new; ++i)
-      row[pos_mod(p0 + i, S_len)] = x[(int64_t(b) * L_new + i) * D + d];
+    // store the inputs (not the outputs), after all reads of this channel's
+    // row: at the write pointer in token order, or (non-circular) by dropping
+    // the oldest L_new entries and appending the new inputs (ascending j
+    // reads slot j + L_new before it is written)
+    if (seqlens) {
+      for (int i = 0; i < L_new; ++i)
+        row[pos_mod(p0 + i, S_len)] = x[(int64_t(b) * L_new + i) * D + d];
+    } else {
+      for (int j = 0; j < S_len; ++j)
+        row[j] = j + L_new < S_len ? row[j + L_new]
+                                   : x[(int64_t(b) * L_new + j + L_new - S_len) * D + d];
+    }
   }
   for (int i = tid; i < L_new * N; i += blockDim.x) {
     const int tt = i / N, n = i % N;
@@ -399,7 +409,7 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
         const int64_t bl = b_first + lin / H;
         const int hl = lin % H;
         nx_r = idx ? idx[bl] : int(bl);
-        nx_p0 = seqlens[bl];
+        nx_p0 = seqlens ? seqlens[bl] : S_len;  // no lengths: non-circular
         nx_A = A[hl];
 #pragma unroll
         for (int i = 0; i < LT; ++i)
@@ -577,12 +587,18 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
           }
         }
         // the new inputs go to the pool row directly (the tile in shared
-        // memory is only read)
+        // memory is only read): at the write pointer, or (non-circular) the
+        // row shifted by L_new with the new inputs appended
         T* grow = conv_pool + (int64_t(ms->row[s]) * D + int64_t(h) * P + tid) * S_len;
-        int sl = base;
-        for (int i = 0; i < L_new; ++i) {
-          grow[sl] = xs[i * P + tid];
-          sl = sl + 1 == S_len ? 0 : sl + 1;
+        if (seqlens) {
+          int sl = base;
+          for (int i = 0; i < L_new; ++i) {
+            grow[sl] = xs[i * P + tid];
+            sl = sl + 1 == S_len ? 0 : sl + 1;
+          }
+        } else {
+          for (int j = 0; j < S_len; ++j)
+            grow[j] = j + L_new < S_len ? row[j + L_new] : xs[(j + L_new - S_len) * P + tid];
         }
       }
       tc::role_sync(1, kPipeWarps * 32);

@@ -300,6 +300,31 @@ def test_decode_parity(L_new, S_len, K, H, P, N):
                                   inp["conv_pool"].data.view(np.int16)[untouched])
 
 
+@pytest.mark.parametrize("L_new,S_len,K", [(1, 3, 4), (1, 4, 4), (4, 4, 4), (6, 4, 4),
+                                           (3, 9, 4), (2, 1, 2), (10, 4, 4)])
+@pytest.mark.parametrize("H,P,N", [(2, 64, 128), (3, 4, 8)])
+def test_decode_noncircular_parity(L_new, S_len, K, H, P, N):
+    """No cache_seqlens: each row keeps its newest S_len inputs and is
+    shifted by L_new; both update kernels, slots bit-exact."""
+    d = synth.DECODE["decode_256x1"].with_(Bz=5, pool=9, L_new=L_new, S_len=S_len, K=K, H=H,
+                                           P=P, N=N, max_seqlen=30)
+    inp = synth.decode_inputs(d)
+    g = {k: T(v) for k, v in inp.items()}
+    y = sss.mixer_update(g["x"], g["w"], g["bias"], g["conv_pool"], None,
+                         g["conv_state_indices"], g["dt"], g["A"], g["B"], g["C"], g["ssm_pool"])
+    torch.cuda.synchronize()
+    y_ref, cp_ref, sp_ref, nbad = oracle.mixer_update(
+        inp["x"], inp["w"], inp["bias"], inp["conv_pool"], None,
+        inp["conv_state_indices"], inp["dt"], inp["A"], inp["B"], inp["C"], inp["ssm_pool"])
+    assert nbad == 0 and sss.device_status() == 0
+    assert_y_close(f64(y), y_ref)
+    np.testing.assert_array_equal(f64(g["conv_pool"]), cp_ref)      # slots: bit-exact
+    assert_rel(f64(g["ssm_pool"]), sp_ref, 1e-5, "ssm pool")
+    untouched = np.setdiff1d(np.arange(d.pool), inp["conv_state_indices"].data)
+    np.testing.assert_array_equal(g["conv_pool"].view(torch.int16).cpu().numpy()[untouched],
+                                  inp["conv_pool"].data.view(np.int16)[untouched])
+
+
 @pytest.mark.parametrize("H,P,N", [(2, 4, 8), (2, 64, 128)])
 def test_decode_bad_rows_are_skipped_and_reported(H, P, N):
     d = synth.DECODE["decode_256x1"].with_(Bz=3, pool=5, H=H, P=P, N=N)
