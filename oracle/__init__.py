@@ -230,3 +230,73 @@ def mixer_update(x, w, bias, conv_pool, cache_seqlens, conv_state_indices, dt, A
     if rc < 0:
         raise ValueError("orc_mixer_update: bad sizes")
     return y, cp, sp, rc
+
+
+# ---------------------------------------------------------------------------
+# state-passing training utilities ("Understanding and Improving Length
+# Generalization in Recurrent Models", sections 4.2-4.4 and 3.5)
+# ---------------------------------------------------------------------------
+
+def state_reset(u, p_reset, h, conv_state=None):
+    """State passing with occasional resets (section 4.4): batch row b starts
+    from zero when its uniform draw u[b] < p_reset (the pages use p = 0.1),
+    else from the passed state.  h [Bz, ...] and conv_state [Bz, ...] (or
+    None); returns new copies."""
+    u = _f64(u)
+    keep = (u >= p_reset).astype(np.float64)
+    h = _f64(h)
+    h2 = h * keep.reshape((-1,) + (1,) * (h.ndim - 1))
+    c2 = None
+    if conv_state is not None:
+        c = _f64(conv_state)
+        c2 = c * keep.reshape((-1,) + (1,) * (c.ndim - 1))
+    return h2, c2
+
+
+def fitted_noise_update(hT, mu=None, var=None, beta: float = 0.1):
+    """Fitted noise, Eqs. (5)-(6) (section 4.2): per head, the mean and the
+    variance of the final states over the batch, the channels P and the state
+    size N, mixed into the running values with weight 1 - beta on the new
+    statistic and beta on the history (beta = 0.1: the new statistic weighs
+    0.9).  Without a history (mu, var None) the batch statistics are taken
+    as they are.  hT [Bz, H, P, N]; returns (mu [H], var [H])."""
+    hT = _f64(hT)
+    H = hT.shape[1]
+    flat = np.moveaxis(hT, 1, 0).reshape(H, -1)
+    m = flat.mean(axis=1)
+    v = ((flat - m[:, None]) ** 2).mean(axis=1)          # population variance
+    if mu is None:
+        return m, v
+    return (1.0 - beta) * m + beta * _f64(mu), (1.0 - beta) * v + beta * _f64(var)
+
+
+def fitted_noise_sample(mu, var, eps):
+    """Initial states drawn independently per element from the fitted
+    per-head Gaussian: h0 = mu_h + sqrt(var_h) eps with eps ~ N(0, 1) given,
+    eps [Bz, H, P, N]."""
+    mu, var, eps = _f64(mu), _f64(var), _f64(eps)
+    return mu[None, :, None, None] + np.sqrt(var)[None, :, None, None] * eps
+
+
+def state_std_trace(u, dt, A, B, C, h0, stride: int):
+    """The state-scale diagnostic of section 3.5 (Figs. 4 and 9): the standard
+    deviation, over a head's P x N state elements, of h_t after tokens
+    t = stride - 1, 2 stride - 1, ... and after the last token, for every
+    batch row and head.  Runs the recurrence token by token (small sizes).
+    Returns [Bz, ceil(L / stride), H]."""
+    dt, A, B, C = _f64(dt), _f64(A), _f64(B), _f64(C)
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    u = _f64(u)
+    P = u.shape[3] if u.ndim == 4 else u.shape[2] // H
+    u = u.reshape(Bz, L, H, P)
+    g_of_h = np.arange(H) // (H // G)
+    h = np.zeros((Bz, H, P, N)) if h0 is None else _f64(h0).copy()
+    out = np.zeros((Bz, -(-L // stride), H))
+    for t in range(L):
+        a = np.exp(dt[:, t, :] * A[None, :])                       # [Bz, H]
+        Bt = B[:, t, g_of_h, :]                                     # [Bz, H, N]
+        h = a[:, :, None, None] * h + u[:, t, :, :, None] * Bt[:, :, None, :]
+        if (t + 1) % stride == 0 or t == L - 1:
+            out[:, t // stride, :] = h.reshape(Bz, H, -1).std(axis=2)
+    return out

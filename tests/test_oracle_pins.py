@@ -607,3 +607,66 @@ def test_scan_bwd_empty_sequence():
     du, ddt, dA, dB, dC, dh0 = oracle.ssm_scan_bwd(u, dt, A, B, C, h0, dy, dhT)
     np.testing.assert_array_equal(dh0, dhT)
     assert not dA.any() and du.shape[1] == 0
+
+
+# ---------------------------------------------------------------------------
+# state-passing training utilities
+# ---------------------------------------------------------------------------
+
+def test_state_reset_rows():
+    """A row restarts from zero when its draw is below p (p = 0.1 on the
+    pages); 1000 evenly spaced draws reset exactly 100 rows."""
+    u = (np.arange(1000) + 0.5) / 1000.0
+    h = np.ones((1000, 2, 3, 4))
+    c = np.full((1000, 6, 3), 2.0)
+    h2, c2 = oracle.state_reset(u, 0.1, h, c)
+    zeroed = np.all(h2.reshape(1000, -1) == 0, axis=1)
+    assert zeroed.sum() == 100 and np.all(zeroed[:100]) and not zeroed[100:].any()
+    np.testing.assert_array_equal(np.all(c2.reshape(1000, -1) == 0, axis=1), zeroed)
+    np.testing.assert_array_equal(c2[100:], c[100:])
+
+
+def test_fitted_noise_weights_follow_eqs_5_6():
+    """Eqs. (5)-(6): mu <- 0.9 Mean(hT) + 0.1 mu, var <- 0.9 Var(hT) + 0.1 var
+    (the new statistic weighs 1 - beta = 0.9).  Head 0 holds +-3 in equal
+    numbers (mean 0, population variance 9), head 1 the constant 2."""
+    hT = np.zeros((2, 2, 4, 6))
+    hT[:, 0] = 3.0
+    hT[:, 0, :2] = -3.0
+    hT[:, 1] = 2.0
+    m, v = oracle.fitted_noise_update(hT)
+    np.testing.assert_allclose(m, [0.0, 2.0], atol=1e-15)
+    np.testing.assert_allclose(v, [9.0, 0.0], atol=1e-15)
+    m2, v2 = oracle.fitted_noise_update(hT, mu=np.array([10.0, -10.0]), var=np.array([1.0, 5.0]))
+    np.testing.assert_allclose(m2, [0.9 * 0.0 + 0.1 * 10.0, 0.9 * 2.0 - 0.1 * 10.0], rtol=1e-15)
+    np.testing.assert_allclose(v2, [0.9 * 9.0 + 0.1 * 1.0, 0.1 * 5.0], rtol=1e-15)
+
+
+def test_fitted_noise_sample_moments():
+    """h0 = mu_h + sqrt(var_h) eps: eps = +-1 gives mu +- sigma exactly, and a
+    large standard-normal draw reproduces the per-head mean and variance."""
+    mu, var = np.array([0.5, -1.0]), np.array([4.0, 0.25])
+    e = np.ones((1, 2, 1, 1))
+    np.testing.assert_allclose(oracle.fitted_noise_sample(mu, var, e).reshape(2), mu + np.sqrt(var))
+    np.testing.assert_allclose(oracle.fitted_noise_sample(mu, var, -e).reshape(2), mu - np.sqrt(var))
+    eps = np.random.default_rng(50).standard_normal((64, 2, 16, 32))
+    h0 = oracle.fitted_noise_sample(mu, var, eps)
+    n = 64 * 16 * 32
+    for hh in range(2):
+        x = h0[:, hh].ravel()
+        assert abs(x.mean() - mu[hh]) < 5 * np.sqrt(var[hh] / n)
+        assert abs(x.var() / var[hh] - 1.0) < 5 * np.sqrt(2.0 / n)
+
+
+@pytest.mark.parametrize("stride", [1, 4, 7, 50])
+def test_state_std_trace_matches_scan_prefixes(stride):
+    """The diagnostic at each sampled position equals the standard deviation
+    of the (separately pinned) scan's final state over that prefix."""
+    u, dt, A, B, C, h0, _, _ = _scan_problem(21, L=13)
+    tr = oracle.state_std_trace(u, dt, A, B, C, h0, stride)
+    Bz, L, H, P = u.shape
+    ends = [t for t in range(L) if (t + 1) % stride == 0 or t == L - 1]
+    assert tr.shape == (Bz, len(ends), H)
+    for k, t in enumerate(ends):
+        _, hT = oracle.ssm_scan(u[:, :t + 1], dt[:, :t + 1], A, B[:, :t + 1], C[:, :t + 1], h0)
+        np.testing.assert_allclose(tr[:, k], hT.reshape(Bz, H, -1).std(axis=2), rtol=1e-12)
