@@ -263,6 +263,46 @@ sss_status sss_ssm_scan_bwd(const void* x, sss_dtype x_dtype, const void* dt,
                             sss_stream_t stream);
 
 /*
+ * State-passing training utilities.  Source: "Understanding and Improving
+ * Length Generalization in Recurrent Models", section 4.4 (state passing:
+ * the next batch starts from the previous final states, each reset to zero
+ * with probability p = 0.1), section 4.2 Eqs. (5)-(6) (fitted noise:
+ * per-head mean and variance of the final states, mixed into running values
+ * with weight 1 - beta = 0.9 on the new statistic, then Gaussian initial
+ * states), section 3.5 (the state scale as a function of position).  The
+ * random draws are inputs, so results follow the caller's generator.
+ *
+ * sss_state_reset: row b of h [Bz, h_row_elems] fp32 and of conv_state
+ *   [Bz, conv_row_elems] (conv_dtype; either may be NULL, not both) is set to
+ *   zero when u[b] < p_reset (u [Bz] fp32 uniforms in [0, 1)); other rows are
+ *   not touched (not even rewritten).
+ * sss_fitted_noise_update: per head h, over hT [Bz, H, P, N] fp32, the mean
+ *   and the population variance of the Bz * P * N values; with has_history,
+ *   mu[h] = (1 - beta) mean + beta mu[h] and var[h] likewise, else mu[h] =
+ *   mean, var[h] = variance.  mu, var [H] fp32, in/out.  Sums in fp64, in a
+ *   fixed order (deterministic).
+ * sss_fitted_noise_sample: h0[b, h, p, n] = mu[h] + sqrt(var[h]) eps[b, h, p, n]
+ *   with eps [Bz, H, P, N] fp32 standard normal draws.
+ * sss_state_std_trace: runs the scan of sss_ssm_scan_fwd (inputs as there,
+ *   y not produced) and writes out[b, k, h] = the standard deviation over the
+ *   P x N elements of head h's state after token min(stride (k + 1), L) - 1,
+ *   k < ceil(L / stride); 1 <= stride <= 64, P <= 64, N <= 128
+ *   (SSS_ERR_UNSUPPORTED otherwise).
+ */
+sss_status sss_state_reset(const float* u, float p_reset, float* h, int64_t Bz,
+                           int64_t h_row_elems, void* conv_state, sss_dtype conv_dtype,
+                           int64_t conv_row_elems, sss_stream_t stream);
+sss_status sss_fitted_noise_update(const float* hT, int64_t Bz, int H, int P, int N, float beta,
+                                   int has_history, float* mu, float* var, sss_stream_t stream);
+sss_status sss_fitted_noise_sample(const float* mu, const float* var, const float* eps,
+                                   float* h0, int64_t Bz, int H, int P, int N,
+                                   sss_stream_t stream);
+sss_status sss_state_std_trace(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
+                               const void* B, sss_dtype act_dtype, const float* h0, float* out,
+                               int64_t Bz, int64_t L, int H, int P, int N, int G, int stride,
+                               sss_stream_t stream);
+
+/*
  * sss_mixer_fwd -- one segment of the streaming forward in a single kernel:
  * the conv with state of sss_conv_state_fwd (SiLU applied) feeding the scan
  * of sss_ssm_scan_fwd, so the conv output never goes to memory.  Sources:

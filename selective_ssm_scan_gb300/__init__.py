@@ -73,6 +73,15 @@ _lib.sss_ssm_scan_bwd_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i]
 _lib.sss_ssm_scan_bwd.restype = _i
 _lib.sss_ssm_scan_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i64, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_state_reset.restype = _i
+_lib.sss_state_reset.argtypes = [_p, ctypes.c_float, _p, _i64, _i64, _p, _i, _i64, _p]
+_lib.sss_fitted_noise_update.restype = _i
+_lib.sss_fitted_noise_update.argtypes = [_p, _i64, _i, _i, _i, ctypes.c_float, _i, _p, _p, _p]
+_lib.sss_fitted_noise_sample.restype = _i
+_lib.sss_fitted_noise_sample.argtypes = [_p, _p, _p, _p, _i64, _i, _i, _i, _p]
+_lib.sss_state_std_trace.restype = _i
+_lib.sss_state_std_trace.argtypes = [_p, _i, _p, _p, _p, _i, _p, _p, _i64, _i64, _i, _i, _i, _i,
+                                     _i, _p]
 _lib.sss_mixer_update.restype = _i
 _lib.sss_mixer_update.argtypes = [_p, _i, _p, _p, _p, _i64, _i, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i, _i, _i, _i, _i, _i, _p]
@@ -285,6 +294,55 @@ def ssm_scan_bwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
                                _ptr(workspace), wsb, _stream(stream))
     _check("sss_ssm_scan_bwd", rc)
     return dx, ddt, dA, dB, dC, dh0
+
+
+def state_reset(u: torch.Tensor, p_reset: float, h: Optional[torch.Tensor],
+                conv_state: Optional[torch.Tensor] = None, stream=None):
+    """Zero, in place, row b of h and of conv_state where u[b] < p_reset (u [Bz]
+    fp32 uniforms); other rows are not touched."""
+    Bz = u.shape[0]
+    hr = h[0].numel() if h is not None and Bz else 0
+    cr = conv_state[0].numel() if conv_state is not None and Bz else 0
+    cdt = _dt(conv_state) if conv_state is not None else 0
+    _check("sss_state_reset", _lib.sss_state_reset(_ptr(u), float(p_reset), _ptr(h), Bz, hr,
+                                                   _ptr(conv_state), cdt, cr, _stream(stream)))
+    return h, conv_state
+
+
+def fitted_noise_update(hT: torch.Tensor, mu: torch.Tensor, var: torch.Tensor, beta: float = 0.1,
+                        has_history: bool = True, stream=None):
+    """Per-head mean and variance of hT [Bz, H, P, N] mixed into mu, var [H]
+    (in place) with weight 1 - beta on the new statistic."""
+    Bz, H, P, N = hT.shape
+    _check("sss_fitted_noise_update",
+           _lib.sss_fitted_noise_update(_ptr(hT), Bz, H, P, N, float(beta), int(bool(has_history)),
+                                        _ptr(mu), _ptr(var), _stream(stream)))
+    return mu, var
+
+
+def fitted_noise_sample(mu: torch.Tensor, var: torch.Tensor, eps: torch.Tensor,
+                        h0: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """h0 = mu_h + sqrt(var_h) eps, eps [Bz, H, P, N] standard normal draws."""
+    Bz, H, P, N = eps.shape
+    if h0 is None:
+        h0 = torch.empty_like(eps)
+    _check("sss_fitted_noise_sample", _lib.sss_fitted_noise_sample(
+        _ptr(mu), _ptr(var), _ptr(eps), _ptr(h0), Bz, H, P, N, _stream(stream)))
+    return h0
+
+
+def state_std_trace(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                    h0: Optional[torch.Tensor], stride: int = 64, stream=None) -> torch.Tensor:
+    """Per-head standard deviation of the scan state every `stride` tokens (and
+    after the last one): [Bz, ceil(L / stride), H] fp32."""
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    P = x.shape[-1] if x.dim() == 4 else x.shape[-1] // H
+    out = torch.empty((Bz, -(-L // stride), H), dtype=torch.float32, device=x.device)
+    _check("sss_state_std_trace", _lib.sss_state_std_trace(
+        _ptr(x), _dt(x), _ptr(dt), _ptr(A), _ptr(B), _dt(dt), _ptr(h0), _ptr(out), Bz, L, H, P, N,
+        G, int(stride), _stream(stream)))
+    return out
 
 
 def mixer_fwd_supported(Bz, L, H, P, N, G, K, x_dtype, y_dtype) -> bool:

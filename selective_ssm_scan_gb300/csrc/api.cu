@@ -51,6 +51,17 @@ cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, c
 size_t conv_state_bwd_workspace(int64_t Bz, int64_t L, int64_t D, int K);
 bool conv_state_bwd_supports(int K);
 size_t ssm_scan_bwd_workspace(int64_t Bz, int64_t L, int H, int P, int N);
+cudaError_t state_reset_launch(const float* u, float p, float* h, int64_t Bz, int64_t h_elems,
+                               void* conv, sss_dtype conv_t, int64_t conv_elems, cudaStream_t st);
+cudaError_t fitted_noise_update_launch(const float* hT, int64_t Bz, int H, int64_t PN, float beta,
+                                       int has_history, float* mu, float* var, cudaStream_t st);
+cudaError_t fitted_noise_sample_launch(const float* mu, const float* var, const float* eps,
+                                       float* h0, int64_t Bz, int H, int64_t PN, cudaStream_t st);
+int state_trace_max_stride();
+cudaError_t state_std_trace_launch(const void* x, sss_dtype x_t, const void* dt, const float* A,
+                                   const void* B, sss_dtype act_t, const float* h0, float* out,
+                                   int64_t Bz, int64_t L, int H, int P, int N, int G, int stride,
+                                   cudaStream_t st);
 bool ssm_scan_bwd_supports(int P, int N);
 cudaError_t ssm_scan_bwd_launch(const void* x, sss_dtype x_t, const void* dt, const float* A,
                                 const void* B, const void* C, sss_dtype act_t, const float* h0,
@@ -278,6 +289,62 @@ sss_status sss_ssm_scan_bwd(const void* x, sss_dtype x_dtype, const void* dt, co
   return from_cuda(sss::ssm_scan_bwd_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, dy, dhT, dx,
                                             ddt, dA, dB, dC, dh0, Bz, L, H, P, N, G, workspace,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_state_reset(const float* u, float p_reset, float* h, int64_t Bz,
+                           int64_t h_row_elems, void* conv_state, sss_dtype conv_dtype,
+                           int64_t conv_row_elems, sss_stream_t stream) {
+  if (Bz < 0 || h_row_elems < 0 || conv_row_elems < 0 || !dtype_ok(conv_dtype))
+    return SSS_ERR_INVALID_ARG;
+  if (Bz == 0) return SSS_OK;
+  if (!u || !aligned(u, 4) || (h && !aligned(h, 4)) ||
+      (conv_state && !aligned(conv_state, dtype_size(conv_dtype))))
+    return SSS_ERR_INVALID_ARG;
+  if (!h && !conv_state) return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::state_reset_launch(u, p_reset, h, Bz, h ? h_row_elems : 0, conv_state,
+                                           conv_dtype, conv_state ? conv_row_elems : 0,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_fitted_noise_update(const float* hT, int64_t Bz, int H, int P, int N, float beta,
+                                   int has_history, float* mu, float* var, sss_stream_t stream) {
+  if (Bz < 1 || H < 1 || P < 1 || N < 1 || !(beta >= 0.0f && beta <= 1.0f))
+    return SSS_ERR_INVALID_ARG;
+  if (!hT || !mu || !var || !aligned(hT, 4) || !aligned(mu, 4) || !aligned(var, 4))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::fitted_noise_update_launch(hT, Bz, H, int64_t(P) * N, beta, has_history,
+                                                   mu, var, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_fitted_noise_sample(const float* mu, const float* var, const float* eps,
+                                   float* h0, int64_t Bz, int H, int P, int N,
+                                   sss_stream_t stream) {
+  if (Bz < 0 || H < 1 || P < 1 || N < 1) return SSS_ERR_INVALID_ARG;
+  if (Bz == 0) return SSS_OK;
+  if (!mu || !var || !eps || !h0 || !aligned(mu, 4) || !aligned(var, 4) || !aligned(eps, 4) ||
+      !aligned(h0, 4))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::fitted_noise_sample_launch(mu, var, eps, h0, Bz, H, int64_t(P) * N,
+                                                   reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_state_std_trace(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
+                               const void* B, sss_dtype act_dtype, const float* h0, float* out,
+                               int64_t Bz, int64_t L, int H, int P, int N, int G, int stride,
+                               sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(act_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || stride < 1)
+    return SSS_ERR_INVALID_ARG;
+  if (!sss::ssm_scan_bwd_supports(P, N) || stride > sss::state_trace_max_stride())
+    return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0 || L == 0) return SSS_OK;
+  if (!x || !dt || !A || !B || !out || !aligned(x, dtype_size(x_dtype)) ||
+      !aligned(dt, dtype_size(act_dtype)) || !aligned(B, dtype_size(act_dtype)) ||
+      !aligned(A, 4) || !aligned(out, 4) || (h0 && !aligned(h0, 4)))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::state_std_trace_launch(x, x_dtype, dt, A, B, act_dtype, h0, out, Bz, L, H,
+                                               P, N, G, stride,
+                                               reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int sss_mixer_fwd_supported(int64_t Bz, int64_t L, int H, int P, int N, int G, int K,

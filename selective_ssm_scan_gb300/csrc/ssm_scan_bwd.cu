@@ -109,18 +109,36 @@ __device__ void chunk_lambda(const TA* __restrict__ dt, int64_t row0, int64_t st
 // One CTA per (batch, head); thread (pq, nq) holds state rows 4 pq .. 4 pq + 3
 // and columns nq + 16 j (j < 8), so one float4 of x and eight B values feed
 // 32 FMAs per token.
+// TRACE (forward only): chunks of Qlen <= kQ tokens, and instead of the
+// states, the standard deviation over the head's P x N state elements after
+// every chunk, to trace[b, c, h] (the state-scale diagnostic of "Understanding
+// and Improving Length Generalization in Recurrent Models" section 3.5).
 struct BoundSmem {
   float xs[kQ][kMaxP];
   float bs[kQ][kMaxN];
   float lam[kQ], dts[kQ], wgt[kQ];
+  float red[kThreadsB / 32];
 };
 
-template <bool REV, typename TX, typename TA>
+__device__ float block_sum_f(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kThreadsB / 32; ++i) t += red[i];
+  return t;
+}
+
+template <bool REV, bool TRACE, typename TX, typename TA>
 __global__ void __launch_bounds__(kThreadsB)
 chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const TA* __restrict__ dt,
                    const float* __restrict__ A, const TA* __restrict__ BC,
                    const float* __restrict__ init, float* __restrict__ bound,
-                   float* __restrict__ final_out, int64_t L, int H, int P, int N, int G, int nC) {
+                   float* __restrict__ final_out, int64_t L, int H, int P, int N, int G, int nC,
+                   int Qlen) {
   extern __shared__ __align__(16) unsigned char smraw[];
   BoundSmem& sm = *reinterpret_cast<BoundSmem*>(smraw);
   const int tid = threadIdx.x;
@@ -138,15 +156,16 @@ chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const
     for (int j = 0; j < kMaxN / 16; ++j) st[r][j] = (init && in(r, j)) ? init[soff + sidx(r, j)] : 0.0f;
   for (int k = 0; k < nC; ++k) {
     const int c = REV ? nC - 1 - k : k;
-    const int64_t t0 = int64_t(c) * kQ;
-    const int Qc = L - t0 < kQ ? int(L - t0) : kQ;
-    // the bound of chunk c before its update: h_in(c), or g_out(c)
-    float* bc = bound + ((int64_t(b) * H + h) * (REV ? nC : nC + 1) + c) * P * N;
+    const int64_t t0 = int64_t(c) * Qlen;
+    const int Qc = L - t0 < Qlen ? int(L - t0) : Qlen;
+    if (!TRACE) {  // the bound of chunk c before its update: h_in(c), or g_out(c)
+      float* bc = bound + ((int64_t(b) * H + h) * (REV ? nC : nC + 1) + c) * P * N;
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int j = 0; j < kMaxN / 16; ++j)
-        if (in(r, j)) bc[sidx(r, j)] = st[r][j];
+        for (int j = 0; j < kMaxN / 16; ++j)
+          if (in(r, j)) bc[sidx(r, j)] = st[r][j];
+    }
     __syncthreads();  // the previous chunk's tiles are no longer read
     chunk_lambda(dt + h, int64_t(b) * L + t0, H, Qc, Ah, sm.lam, sm.dts);
     batched_copy(
@@ -186,7 +205,26 @@ chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const
         for (int r = 0; r < 4; ++r) st[r][j] = fmaf(wx[r], bv, st[r][j]);
       }
     }
+    if (TRACE) {  // std of the state after this chunk: mean, then centred squares
+      float s1 = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < kMaxN / 16; ++j) s1 += in(r, j) ? st[r][j] : 0.0f;
+      const float mean = block_sum_f(s1, sm.red) / float(P * N);
+      float s2 = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < kMaxN / 16; ++j) {
+          const float d = in(r, j) ? st[r][j] - mean : 0.0f;
+          s2 = fmaf(d, d, s2);
+        }
+      const float var = block_sum_f(s2, sm.red) / float(P * N);
+      if (tid == 0) bound[(int64_t(b) * nC + c) * H + h] = sqrtf(var);
+    }
   }
+  if (TRACE) return;
   // the state after the last chunk, or dh0
   float* out = REV ? (final_out ? final_out + soff : nullptr)
                    : bound + ((int64_t(b) * H + h) * (nC + 1) + nC) * P * N;
@@ -485,12 +523,12 @@ cudaError_t launch_bwd(const void* x, const void* dt, const float* A, const void
   const dim3 gb(H, unsigned(Bz));
   if (Bz > 0) {
     const int bsm = int(sizeof(BoundSmem));
-    auto k1 = chunk_bound_kernel<false, TX, TA>;
-    auto k2 = chunk_bound_kernel<true, TX, TA>;
+    auto k1 = chunk_bound_kernel<false, false, TX, TA>;
+    auto k2 = chunk_bound_kernel<true, false, TX, TA>;
     cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, bsm);
     cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, bsm);
-    k1<<<gb, kThreadsB, bsm, st>>>(xx, dy, dtt, A, Bb, h0, hin, nullptr, L, H, P, N, G, nC);
-    k2<<<gb, kThreadsB, bsm, st>>>(xx, dy, dtt, A, Cc, dhT, gout, dh0, L, H, P, N, G, nC);
+    k1<<<gb, kThreadsB, bsm, st>>>(xx, dy, dtt, A, Bb, h0, hin, nullptr, L, H, P, N, G, nC, kQ);
+    k2<<<gb, kThreadsB, bsm, st>>>(xx, dy, dtt, A, Cc, dhT, gout, dh0, L, H, P, N, G, nC, kQ);
   }
   if (nC > 0 && Bz > 0) {
     auto k3 = chunk_bwd_kernel<TX, TA>;
@@ -531,5 +569,38 @@ cudaError_t ssm_scan_bwd_launch(const void* x, sss_dtype x_t, const void* dt, co
 }
 
 bool ssm_scan_bwd_supports(int P, int N) { return P >= 1 && P <= kMaxP && N >= 1 && N <= kMaxN; }
+
+namespace {
+template <typename TX, typename TA>
+cudaError_t launch_trace(const void* x, const void* dt, const float* A, const void* B,
+                         const float* h0, float* out, int64_t Bz, int64_t L, int H, int P, int N,
+                         int G, int stride, cudaStream_t st) {
+  const int nC = int((L + stride - 1) / stride);
+  if (Bz == 0 || nC == 0) return cudaSuccess;
+  const int bsm = int(sizeof(BoundSmem));
+  auto k = chunk_bound_kernel<false, true, TX, TA>;
+  cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, bsm);
+  k<<<dim3(H, unsigned(Bz)), kThreadsB, bsm, st>>>(
+      static_cast<const TX*>(x), nullptr, static_cast<const TA*>(dt), A, static_cast<const TA*>(B),
+      h0, out, nullptr, L, H, P, N, G, nC, stride);
+  return cudaGetLastError();
+}
+}  // namespace
+
+int state_trace_max_stride() { return kQ; }
+
+cudaError_t state_std_trace_launch(const void* x, sss_dtype x_t, const void* dt, const float* A,
+                                   const void* B, sss_dtype act_t, const float* h0, float* out,
+                                   int64_t Bz, int64_t L, int H, int P, int N, int G, int stride,
+                                   cudaStream_t st) {
+  if (x_t == SSS_BF16 && act_t == SSS_BF16)
+    return launch_trace<__nv_bfloat16, __nv_bfloat16>(x, dt, A, B, h0, out, Bz, L, H, P, N, G,
+                                                      stride, st);
+  if (x_t == SSS_F32 && act_t == SSS_BF16)
+    return launch_trace<float, __nv_bfloat16>(x, dt, A, B, h0, out, Bz, L, H, P, N, G, stride, st);
+  if (x_t == SSS_BF16 && act_t == SSS_F32)
+    return launch_trace<__nv_bfloat16, float>(x, dt, A, B, h0, out, Bz, L, H, P, N, G, stride, st);
+  return launch_trace<float, float>(x, dt, A, B, h0, out, Bz, L, H, P, N, G, stride, st);
+}
 
 }  // namespace sss
