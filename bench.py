@@ -440,6 +440,7 @@ def main():
     conv_bwd = bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
     # ---- scan backward with state on one segment, same rules ---------------
     scan_bwd = bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
+    train_utils = bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
 
     # ---- decode update (continuous batching), same rules -------------------
     decode = None
@@ -458,7 +459,7 @@ def main():
                    "l2": "flushed before every timed step (256 MiB write, outside the events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
-        "conv_bwd": conv_bwd, "scan_bwd": scan_bwd,
+        "conv_bwd": conv_bwd, "scan_bwd": scan_bwd, "train_utils": train_utils,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -584,6 +585,56 @@ def bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
             "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
             "tokens_per_s": tok / (ms * 1e-3),
             "kernel": "fp32 CUDA-core chunked backward (chunks of 64)"}
+
+
+def bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
+    """The state-passing utilities at the workload's state size: the zero
+    reset (10% of rows), the fitted-noise statistics and sampling, and the
+    per-head state-std trace (stride 64) over one segment."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    Bz, H, P, N = s.Bz, s.H, s.P, s.N
+    hT = torch.randn((Bz, H, P, N), generator=g, device=dev)
+    conv = torch.randn((Bz, s.D, s.K - 1), generator=g, device=dev).to(torch.bfloat16)
+    u = torch.rand((Bz,), generator=g, device=dev)
+    mu = torch.zeros((H,), device=dev)
+    var = torch.ones((H,), device=dev)
+    eps = torch.randn((Bz, H, P, N), generator=g, device=dev)
+    h0 = torch.empty_like(eps)
+    x = torch.randn((Bz, Lseg, H, P), generator=g, device=dev).to(torch.bfloat16)
+    dt = torch.nn.functional.softplus(torch.randn((Bz, Lseg, H), generator=g, device=dev) - 2).to(torch.bfloat16)
+    A = -torch.rand((H,), generator=g, device=dev) * 0.99 - 0.01
+    B = torch.randn((Bz, Lseg, 1, N), generator=g, device=dev).to(torch.bfloat16)
+    state = Bz * H * P * N * 4
+    calls = {
+        "fitted_noise_update": (lambda: sss.fitted_noise_update(hT, mu, var, 0.1, True), state),
+        "fitted_noise_sample": (lambda: sss.fitted_noise_sample(mu, var, eps, h0), 2 * state),
+        "state_std_trace": (lambda: sss.state_std_trace(x, dt, A, B, hT, 64),
+                            Bz * Lseg * (H * P * 2 + H * 2 + N * 2) + state),
+    }
+    out = {"workload": f"Bz={Bz}, H={H}, P={P}, N={N} fp32 states; trace over one {Lseg}-token "
+                       f"segment, bf16 inputs"}
+    for name, (fn, byts) in calls.items():
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        evs = []
+        for _ in range(max(3, args.steps // 50)):
+            flush.zero_()
+            torch.cuda._sleep(100_000)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            evs.append((e0, e1))
+        stream.synchronize()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        out[name] = {"avg_call_ms": ms, "algorithmic_bytes_per_call": byts,
+                     "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm}
+    # the reset writes zeros to the rows it resets and touches nothing else
+    sss.state_reset(u, 0.1, hT, conv)
+    return out
 
 
 def bench_decode(torch, sss, dev, stream, flush, args, hbm):

@@ -11,6 +11,8 @@
 // The random draws are inputs, so results are reproducible from the caller's
 // generator.  The per-head state-std trace (section 3.5) lives with the
 // chunk walk in ssm_scan_bwd.cu.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace sss {
@@ -38,40 +40,88 @@ state_reset_kernel(const float* __restrict__ u, float p, T* __restrict__ rows, i
     row[i] = from_f32<T>(0.0f);
 }
 
-// fixed-order block sum (deterministic)
-__device__ double block_sum(double v, double* red) {
+// Fixed-order sum over the CTAs of a cluster of kStatCtas (deterministic):
+// warp shuffles, the CTA's warps in order, then every CTA reads the partials
+// of all cluster ranks in rank order through distributed shared memory.
+constexpr int kStatCtas = 8;
+__device__ double cluster_sum(double v, double* red, double* part) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cl = cg::this_cluster();
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
   __syncthreads();
-  if ((threadIdx.x & 31) == 0) red[w] = v;
-  __syncthreads();
-  double s = 0.0;
-  for (int i = 0; i < kStatThreads / 32; ++i) s += red[i];
-  return s;
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int i = 0; i < kStatThreads / 32; ++i) s += red[i];
+    *part = s;
+  }
+  cl.sync();  // every rank's partial is written
+  double t = 0.0;
+  for (int r = 0; r < kStatCtas; ++r) t += *cl.map_shared_rank(part, r);
+  cl.sync();  // no rank rewrites its partial while another still reads it
+  return t;
 }
 
-// one CTA per head: mean, then the centred sum of squares, then the EMA
+// a cluster of kStatCtas CTAs per head: each sums a contiguous share of the
+// head's Bz x P x N values (fp32 over four interleaved float4 streams, fp64
+// across threads and CTAs), the mean, then the centred squares, then the EMA
 __global__ void __launch_bounds__(kStatThreads)
 fitted_noise_update_kernel(const float* __restrict__ hT, int64_t Bz, int H, int64_t PN, float beta,
                            int has_history, float* __restrict__ mu, float* __restrict__ var) {
   __shared__ double red[kStatThreads / 32];
-  const int h = blockIdx.x;
+  __shared__ double part;
+  const int h = blockIdx.x / kStatCtas, rank = blockIdx.x % kStatCtas;
   const int64_t n = Bz * PN;
-  double s = 0.0;
-  for (int64_t i = threadIdx.x; i < n; i += kStatThreads) {
-    const int64_t b = i / PN, e = i % PN;
-    s += double(hT[(b * H + h) * PN + e]);
+  const bool vec = (PN & 3) == 0 && (reinterpret_cast<uintptr_t>(hT) & 15) == 0;
+  // this CTA's rows: batch rows b with b % kStatCtas == rank, each a
+  // contiguous block of PN values of head h
+  // first pass: the sum
+  double s1 = 0.0, s2 = 0.0;
+  for (int64_t b = rank; b < Bz; b += kStatCtas) {
+    const float* row = hT + (b * H + h) * PN;
+    float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (vec) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      for (int64_t i = threadIdx.x; i < PN / 4; i += kStatThreads) {
+        const float4 q = r4[i];
+        a4[0] += q.x;
+        a4[1] += q.y;
+        a4[2] += q.z;
+        a4[3] += q.w;
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < PN; i += kStatThreads) a4[i & 3] += row[i];
+    }
+    s1 += double(a4[0]) + double(a4[1]) + double(a4[2]) + double(a4[3]);
   }
-  const double mean = n > 0 ? block_sum(s, red) / double(n) : 0.0;
-  double q = 0.0;
-  for (int64_t i = threadIdx.x; i < n; i += kStatThreads) {
-    const int64_t b = i / PN, e = i % PN;
-    const double d = double(hT[(b * H + h) * PN + e]) - mean;
-    q += d * d;
+  const double mean = n > 0 ? cluster_sum(s1, red, &part) / double(n) : 0.0;
+  const float mf = float(mean);
+  for (int64_t b = rank; b < Bz; b += kStatCtas) {
+    const float* row = hT + (b * H + h) * PN;
+    float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    if (vec) {
+      const float4* r4 = reinterpret_cast<const float4*>(row);
+      for (int64_t i = threadIdx.x; i < PN / 4; i += kStatThreads) {
+        const float4 q = r4[i];
+        const float d0 = q.x - mf, d1 = q.y - mf, d2 = q.z - mf, d3 = q.w - mf;
+        a4[0] = fmaf(d0, d0, a4[0]);
+        a4[1] = fmaf(d1, d1, a4[1]);
+        a4[2] = fmaf(d2, d2, a4[2]);
+        a4[3] = fmaf(d3, d3, a4[3]);
+      }
+    } else {
+      for (int64_t i = threadIdx.x; i < PN; i += kStatThreads) {
+        const float d = row[i] - mf;
+        a4[i & 3] = fmaf(d, d, a4[i & 3]);
+      }
+    }
+    s2 += double(a4[0]) + double(a4[1]) + double(a4[2]) + double(a4[3]);
   }
-  const double v = n > 0 ? block_sum(q, red) / double(n) : 0.0;
-  if (threadIdx.x == 0) {
+  // centred on the fp32-rounded mean: sum (x - m)^2 = sum (x - mf)^2 - n (m - mf)^2
+  const double dm = mean - double(mf);
+  const double v = n > 0 ? cluster_sum(s2, red, &part) / double(n) - dm * dm : 0.0;
+  if (rank == 0 && threadIdx.x == 0) {
     if (has_history) {
       mu[h] = float((1.0 - double(beta)) * mean + double(beta) * double(mu[h]));
       var[h] = float((1.0 - double(beta)) * v + double(beta) * double(var[h]));
@@ -120,8 +170,20 @@ cudaError_t state_reset_launch(const float* u, float p, float* h, int64_t Bz, in
 
 cudaError_t fitted_noise_update_launch(const float* hT, int64_t Bz, int H, int64_t PN, float beta,
                                        int has_history, float* mu, float* var, cudaStream_t st) {
-  fitted_noise_update_kernel<<<H, kStatThreads, 0, st>>>(hT, Bz, H, PN, beta, has_history, mu, var);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(H) * kStatCtas);
+  cfg.blockDim = dim3(kStatThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kStatCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fitted_noise_update_kernel, hT, Bz, H, PN, beta, has_history, mu,
+                            var);
 }
 
 cudaError_t fitted_noise_sample_launch(const float* mu, const float* var, const float* eps,
