@@ -300,3 +300,44 @@ def state_std_trace(u, dt, A, B, C, h0, stride: int):
         if (t + 1) % stride == 0 or t == L - 1:
             out[:, t // stride, :] = h.reshape(Bz, H, -1).std(axis=2)
     return out
+
+
+def prefill_to_pool(x, state_in, K, hT, conv_pool, ssm_pool, cache_seqlens, conv_state_indices):
+    """The state a prompt leaves, written into pool rows (the causal-conv
+    chapter's "continuous batching" and "circular mode" sections): for
+    request b, pool row r = conv_state_indices[b] (b when None) receives the
+    newest S_len entries of the extended sequence u = [state_in, x] (zeros
+    where u has none), laid out as the decode update reads them - circular
+    mode (cache_seqlens given, p = cache_seqlens[b] the length after the
+    prompt, the prompt at logical positions p - L .. p - 1): position q in
+    slot q mod S_len; non-circular (cache_seqlens None): oldest first - and
+    ssm_pool[r] = hT[b].  Rows with r outside [0, pool) or p < 0 are skipped.
+    x [Bz, L, D], state_in [Bz, D, K-1] | None, hT [Bz, H, P, N] | None.
+    Returns new copies of the two pools and the number of skipped rows."""
+    x = _f64(x)
+    Bz, L, D = x.shape
+    cp = _f64(conv_pool).copy()
+    sp = _f64(ssm_pool).copy() if ssm_pool is not None else None
+    pool, _, S_len = cp.shape
+    S = np.zeros((Bz, D, K - 1)) if state_in is None else _f64(state_in)
+    sl = None if cache_seqlens is None else np.asarray(getattr(cache_seqlens, "data", cache_seqlens))
+    ix = None if conv_state_indices is None else np.asarray(
+        getattr(conv_state_indices, "data", conv_state_indices))
+    bad = 0
+    for b in range(Bz):
+        r = int(ix[b]) if ix is not None else b
+        p = int(sl[b]) if sl is not None else L
+        if r < 0 or r >= pool or p < 0:
+            bad += 1
+            continue
+        u = np.concatenate([S[b], x[b].T], axis=1)           # [D, K-1+L], u[:, i] at position p-L-(K-1)+i
+        first = p - L - (K - 1)
+        for j in range(S_len):
+            q = p - S_len + j                                 # the j-th oldest of the newest S_len positions
+            i = q - first
+            v = u[:, i] if 0 <= i < u.shape[1] else np.zeros(D)
+            slot = (q % S_len) if sl is not None else j
+            cp[r, :, slot] = v
+        if sp is not None and hT is not None:
+            sp[r] = _f64(hT)[b]
+    return cp, sp, bad

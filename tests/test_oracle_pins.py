@@ -670,3 +670,52 @@ def test_state_std_trace_matches_scan_prefixes(stride):
     for k, t in enumerate(ends):
         _, hT = oracle.ssm_scan(u[:, :t + 1], dt[:, :t + 1], A, B[:, :t + 1], C[:, :t + 1], h0)
         np.testing.assert_allclose(tr[:, k], hT.reshape(Bz, H, -1).std(axis=2), rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# prefill into the pool
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("circular", [True, False])
+def test_prefill_to_pool_example(circular):
+    """K = 3, S_len = 4, prompt x = [a, b, c, d, e] after a zero state: the
+    newest four inputs b, c, d, e; circular at length 5 they sit at slots
+    1, 2, 3, 0 (row [e, b, c, d]), non-circular oldest first ([b, c, d, e])."""
+    x = np.array([1.0, 10.0, 100.0, 1000.0, 10000.0]).reshape(1, 5, 1)
+    cp, _, bad = oracle.prefill_to_pool(x, None, 3, None, np.zeros((1, 1, 4)), None,
+                                        np.array([5]) if circular else None, None)
+    assert bad == 0
+    expect = [10000.0, 10.0, 100.0, 1000.0] if circular else [10.0, 100.0, 1000.0, 10000.0]
+    np.testing.assert_array_equal(cp.reshape(-1), expect)
+
+
+@pytest.mark.parametrize("circular", [True, False])
+@pytest.mark.parametrize("L,Lnew,S_len,K", [(9, 3, 4, 4), (2, 4, 6, 4), (1, 1, 3, 4), (7, 6, 4, 3)])
+def test_prefill_then_update_equals_whole_forward(circular, L, Lnew, S_len, K):
+    """A prompt's forward, its state written into the pool, then a decode
+    update on the next tokens, equals the forward over the whole sequence
+    (the prompt's initial conv and SSM states included)."""
+    g = np.random.default_rng(80 + L + 10 * Lnew)
+    Bz, pool, H, P, N, G = 3, 5, 2, 3, 4, 1
+    D = H * P
+    x = g.standard_normal((Bz, L + Lnew, D))
+    w, bias = g.standard_normal((D, K)), g.standard_normal(D)
+    S0 = g.standard_normal((Bz, D, K - 1))
+    h0 = g.standard_normal((Bz, H, P, N))
+    dt = np.log1p(np.exp(g.standard_normal((Bz, L + Lnew, H))))
+    A = -g.uniform(0.01, 1, H)
+    B = g.standard_normal((Bz, L + Lnew, G, N))
+    C = g.standard_normal((Bz, L + Lnew, G, N))
+    idx = g.permutation(pool)[:Bz].astype(np.int32)
+    y_all, _, _ = oracle.mixer_fwd(x, dt, A, B, C, w, bias, S0, h0)
+    pre = slice(0, L)
+    _, _, hT = oracle.mixer_fwd(x[:, pre], dt[:, pre], A, B[:, pre], C[:, pre], w, bias, S0, h0)
+    lens = np.full(Bz, L + 7, np.int32) if circular else None   # any length >= L works
+    cp, sp, bad = oracle.prefill_to_pool(x[:, pre], S0, K, hT, g.standard_normal((pool, D, S_len)),
+                                         g.standard_normal((pool, H, P, N)), lens, idx)
+    assert bad == 0
+    post = slice(L, None)
+    y, _, _, nbad = oracle.mixer_update(x[:, post], w, bias, cp, lens, idx, dt[:, post], A,
+                                        B[:, post], C[:, post], sp)
+    assert nbad == 0
+    np.testing.assert_allclose(y, y_all[:, post], rtol=1e-10, atol=1e-10)
