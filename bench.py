@@ -588,9 +588,10 @@ def bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
 
 
 def bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
-    """The state-passing utilities at the workload's state size: the zero
-    reset (10% of rows), the fitted-noise statistics and sampling, and the
-    per-head state-std trace (stride 64) over one segment."""
+    """The state utilities at the workload's state size: a prompt's state
+    written into pool rows (circular layout, S_len 4), the zero reset (10% of
+    rows), the fitted-noise statistics and sampling, and the per-head
+    state-std trace (stride 64) over one segment."""
     g = torch.Generator(device=dev)
     g.manual_seed(7)
     Bz, H, P, N = s.Bz, s.H, s.P, s.N
@@ -606,7 +607,14 @@ def bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
     A = -torch.rand((H,), generator=g, device=dev) * 0.99 - 0.01
     B = torch.randn((Bz, Lseg, 1, N), generator=g, device=dev).to(torch.bfloat16)
     state = Bz * H * P * N * 4
+    xp = torch.randn((Bz, Lseg, s.D), generator=g, device=dev).to(torch.bfloat16)
+    cpool = torch.zeros((2 * Bz, s.D, 4), dtype=torch.bfloat16, device=dev)
+    spool = torch.zeros((2 * Bz, H, P, N), device=dev)
+    pidx = torch.arange(Bz, dtype=torch.int32, device=dev) * 2
+    plen = torch.full((Bz,), Lseg, dtype=torch.int32, device=dev)
     calls = {
+        "prefill_to_pool": (lambda: sss.prefill_to_pool(xp, conv, s.K, hT, cpool, spool, plen, pidx, H),
+                            2 * state + Bz * s.D * 4 * 2 * 2),
         "fitted_noise_update": (lambda: sss.fitted_noise_update(hT, mu, var, 0.1, True), state),
         "fitted_noise_sample": (lambda: sss.fitted_noise_sample(mu, var, eps, h0), 2 * state),
         "state_std_trace": (lambda: sss.state_std_trace(x, dt, A, B, hT, 64),

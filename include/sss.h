@@ -263,6 +263,36 @@ sss_status sss_ssm_scan_bwd(const void* x, sss_dtype x_dtype, const void* dt,
                             sss_stream_t stream);
 
 /*
+ * sss_prefill_to_pool -- write the state a prompt leaves into the pool rows
+ * the decode update reads.  Source: "Chapter 7: state, chunking and
+ * incremental inference", sections "continuous batching" (rows addressed by
+ * conv_state_indices), "circular mode" (logical position q in slot
+ * q mod S_len) and "the physical cache can be longer" (non-circular rows,
+ * oldest first).  For request b, r = conv_state_indices[b] (b when NULL):
+ * conv_pool row r gets the newest S_len entries of the extended sequence
+ * u = [conv_state_in (K-1 values), x (L values)], zeros where u has none;
+ * with cache_seqlens (p = cache_seqlens[b], the length after the prompt,
+ * the prompt at logical positions p - L .. p - 1) position q goes to slot
+ * q mod S_len, without it (non-circular) the S_len values go oldest first.
+ * ssm_pool row r gets hT[b] (hT and ssm_pool both given or both NULL).
+ * The decode update on the next tokens then continues the request exactly.
+ * A row with r outside [0, pool) or p < 0 is skipped and SSS_ERR_INDEX is
+ * raised in the device status; two requests naming one row is a contract
+ * violation.
+ *
+ *  x              [Bz, L, H*P]     x_dtype (the prompt's conv inputs)
+ *  conv_state_in  [Bz, H*P, K-1]   x_dtype, the conv state before the prompt; NULL = zeros
+ *  hT             [Bz, H, P, N]    float32, 16-byte aligned (P*N a multiple of 4)
+ *  conv_pool      [pool, H*P, S_len] x_dtype, S_len >= K-1
+ *  ssm_pool       [pool, H, P, N]  float32
+ */
+sss_status sss_prefill_to_pool(const void* x, sss_dtype x_dtype, const void* conv_state_in, int K,
+                               const float* hT, void* conv_pool, int64_t pool, int S_len,
+                               float* ssm_pool, const int32_t* cache_seqlens,
+                               const int32_t* conv_state_indices, int64_t Bz, int64_t L,
+                               int64_t D, int H, int P, int N, sss_stream_t stream);
+
+/*
  * State-passing training utilities.  Source: "Understanding and Improving
  * Length Generalization in Recurrent Models", section 4.4 (state passing:
  * the next batch starts from the previous final states, each reset to zero

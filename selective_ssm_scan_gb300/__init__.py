@@ -73,6 +73,9 @@ _lib.sss_ssm_scan_bwd_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i]
 _lib.sss_ssm_scan_bwd.restype = _i
 _lib.sss_ssm_scan_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i64, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_prefill_to_pool.restype = _i
+_lib.sss_prefill_to_pool.argtypes = [_p, _i, _p, _i, _p, _p, _i64, _i, _p, _p, _p, _i64, _i64,
+                                     _i64, _i, _i, _i, _p]
 _lib.sss_state_reset.restype = _i
 _lib.sss_state_reset.argtypes = [_p, ctypes.c_float, _p, _i64, _i64, _p, _i, _i64, _p]
 _lib.sss_fitted_noise_update.restype = _i
@@ -294,6 +297,25 @@ def ssm_scan_bwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
                                _ptr(workspace), wsb, _stream(stream))
     _check("sss_ssm_scan_bwd", rc)
     return dx, ddt, dA, dB, dC, dh0
+
+
+def prefill_to_pool(x: torch.Tensor, conv_state_in: Optional[torch.Tensor], K: int,
+                    hT: Optional[torch.Tensor], conv_pool: torch.Tensor,
+                    ssm_pool: Optional[torch.Tensor], cache_seqlens: Optional[torch.Tensor],
+                    conv_state_indices: Optional[torch.Tensor], H: int, stream=None):
+    """Write a prompt's conv history (the newest S_len inputs of [conv_state_in,
+    x]) and its final SSM state hT into the pool rows conv_state_indices, in
+    place: circular layout when cache_seqlens (the lengths after the prompt)
+    is given, oldest first otherwise."""
+    Bz, L, D = x.shape
+    pool, _, S_len = conv_pool.shape
+    P = D // H
+    N = hT.shape[-1] if hT is not None else (ssm_pool.shape[-1] if ssm_pool is not None else 1)
+    _check("sss_prefill_to_pool", _lib.sss_prefill_to_pool(
+        _ptr(x), _dt(x), _ptr(conv_state_in), int(K), _ptr(hT), _ptr(conv_pool), pool, S_len,
+        _ptr(ssm_pool), _ptr(cache_seqlens), _ptr(conv_state_indices), Bz, L, D, H, P, N,
+        _stream(stream)))
+    return conv_pool, ssm_pool
 
 
 def state_reset(u: torch.Tensor, p_reset: float, h: Optional[torch.Tensor],

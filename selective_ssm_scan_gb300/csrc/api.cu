@@ -58,6 +58,11 @@ cudaError_t fitted_noise_update_launch(const float* hT, int64_t Bz, int H, int64
 cudaError_t fitted_noise_sample_launch(const float* mu, const float* var, const float* eps,
                                        float* h0, int64_t Bz, int H, int64_t PN, cudaStream_t st);
 int state_trace_max_stride();
+cudaError_t prefill_to_pool_launch(const void* x, sss_dtype dt, const void* state_in, int K,
+                                   const float* hT, void* conv_pool, int64_t pool, int S_len,
+                                   float* ssm_pool, const int32_t* seqlens, const int32_t* idx,
+                                   int64_t Bz, int64_t L, int64_t D, int64_t ssm_row_elems,
+                                   int* status, cudaStream_t st);
 cudaError_t state_std_trace_launch(const void* x, sss_dtype x_t, const void* dt, const float* A,
                                    const void* B, sss_dtype act_t, const float* h0, float* out,
                                    int64_t Bz, int64_t L, int H, int P, int N, int G, int stride,
@@ -289,6 +294,30 @@ sss_status sss_ssm_scan_bwd(const void* x, sss_dtype x_dtype, const void* dt, co
   return from_cuda(sss::ssm_scan_bwd_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, dy, dhT, dx,
                                             ddt, dA, dB, dC, dh0, Bz, L, H, P, N, G, workspace,
                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_prefill_to_pool(const void* x, sss_dtype x_dtype, const void* conv_state_in, int K,
+                               const float* hT, void* conv_pool, int64_t pool, int S_len,
+                               float* ssm_pool, const int32_t* cache_seqlens,
+                               const int32_t* conv_state_indices, int64_t Bz, int64_t L,
+                               int64_t D, int H, int P, int N, sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || Bz < 0 || L < 0 || D < 1 || K < 1 || S_len < 1 || S_len < K - 1 ||
+      pool < 0 || H < 1 || P < 1 || N < 1 || int64_t(H) * P != D)
+    return SSS_ERR_INVALID_ARG;
+  if (Bz == 0) return SSS_OK;
+  const size_t xs = dtype_size(x_dtype);
+  if (!conv_pool || !aligned(conv_pool, xs) || (L > 0 && (!x || !aligned(x, xs))) ||
+      (conv_state_in && !aligned(conv_state_in, xs)) ||
+      (cache_seqlens && !aligned(cache_seqlens, 4)) ||
+      (conv_state_indices && !aligned(conv_state_indices, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if ((hT != nullptr) != (ssm_pool != nullptr)) return SSS_ERR_INVALID_ARG;
+  if (hT && (!aligned(hT, 16) || !aligned(ssm_pool, 16) || (int64_t(P) * N) % 4))
+    return SSS_ERR_INVALID_ARG;
+  return from_cuda(sss::prefill_to_pool_launch(
+      x, x_dtype, conv_state_in, K, hT, conv_pool, pool, S_len, ssm_pool, cache_seqlens,
+      conv_state_indices, Bz, L, D, int64_t(H) * P * N, status_word(),
+      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sss_status sss_state_reset(const float* u, float p_reset, float* h, int64_t Bz,

@@ -195,4 +195,84 @@ cudaError_t fitted_noise_sample_launch(const float* mu, const float* var, const 
   return cudaGetLastError();
 }
 
+
+// ---- prefill into the pool ---------------------------------------------------
+// A prompt's state written into the pool rows the decode update reads ("Chapter
+// 7: state, chunking and incremental inference", sections "continuous
+// batching" and "circular mode"): row r = idx[b] of the conv pool gets the
+// newest S_len entries of u = [state_in, x] (zeros where u has none) - at slot
+// q mod S_len for logical position q in circular mode (the prompt at positions
+// p - L .. p - 1, p = seqlens[b]), oldest first without lengths - and row r of
+// the SSM pool gets hT[b].  Bad rows are skipped and reported.
+namespace {
+template <typename T>
+__global__ void __launch_bounds__(kResetThreads)
+prefill_conv_kernel(const T* __restrict__ x, const T* __restrict__ state_in, int K,
+                    T* __restrict__ conv_pool, int64_t pool, int S_len,
+                    const int32_t* __restrict__ seqlens, const int32_t* __restrict__ idx,
+                    int64_t L, int64_t D, int* status) {
+  const int64_t b = blockIdx.y;
+  const int64_t r = idx ? int64_t(idx[b]) : b;
+  const int64_t p = seqlens ? int64_t(seqlens[b]) : L;
+  if (r < 0 || r >= pool || p < 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) raise_status(status, SSS_ERR_INDEX);
+    return;
+  }
+  const int64_t first = p - L - (K - 1);  // logical position of u[0]
+  for (int64_t d = blockIdx.x * int64_t(kResetThreads) + threadIdx.x; d < D;
+       d += int64_t(gridDim.x) * kResetThreads) {
+    T* row = conv_pool + (r * D + d) * S_len;
+    for (int j = 0; j < S_len; ++j) {
+      const int64_t q = p - S_len + j;
+      const int64_t i = q - first;
+      T v = from_f32<T>(0.0f);
+      if (i >= 0 && i < K - 1) {
+        if (state_in) v = state_in[(b * D + d) * (K - 1) + i];
+      } else if (i >= K - 1 && i < K - 1 + L) {
+        v = x[(b * L + (i - (K - 1))) * D + d];
+      }
+      const int64_t slot = seqlens ? ((q % S_len) + S_len) % S_len : j;
+      row[slot] = v;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kResetThreads)
+prefill_ssm_kernel(const float* __restrict__ hT, float* __restrict__ ssm_pool, int64_t pool,
+                   const int32_t* __restrict__ seqlens, const int32_t* __restrict__ idx,
+                   int64_t row_elems) {
+  const int64_t b = blockIdx.y;
+  const int64_t r = idx ? int64_t(idx[b]) : b;
+  if (r < 0 || r >= pool || (seqlens && seqlens[b] < 0)) return;  // reported by the conv kernel
+  const float4* src = reinterpret_cast<const float4*>(hT + b * row_elems);
+  float4* dst = reinterpret_cast<float4*>(ssm_pool + r * row_elems);
+  for (int64_t i = blockIdx.x * int64_t(kResetThreads) + threadIdx.x; i < row_elems / 4;
+       i += int64_t(gridDim.x) * kResetThreads)
+    dst[i] = src[i];
+}
+}  // namespace
+
+cudaError_t prefill_to_pool_launch(const void* x, sss_dtype dt, const void* state_in, int K,
+                                   const float* hT, void* conv_pool, int64_t pool, int S_len,
+                                   float* ssm_pool, const int32_t* seqlens, const int32_t* idx,
+                                   int64_t Bz, int64_t L, int64_t D, int64_t ssm_row_elems,
+                                   int* status, cudaStream_t st) {
+  if (Bz == 0) return cudaSuccess;
+  const dim3 gc(grid_for(D, kResetThreads, 64), unsigned(Bz));
+  if (dt == SSS_BF16)
+    prefill_conv_kernel<__nv_bfloat16><<<gc, kResetThreads, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const __nv_bfloat16*>(state_in), K,
+        static_cast<__nv_bfloat16*>(conv_pool), pool, S_len, seqlens, idx, L, D, status);
+  else
+    prefill_conv_kernel<float><<<gc, kResetThreads, 0, st>>>(
+        static_cast<const float*>(x), static_cast<const float*>(state_in), K,
+        static_cast<float*>(conv_pool), pool, S_len, seqlens, idx, L, D, status);
+  if (hT && ssm_pool && ssm_row_elems > 0) {
+    const dim3 gs(grid_for(ssm_row_elems / 4, kResetThreads, 64), unsigned(Bz));
+    prefill_ssm_kernel<<<gs, kResetThreads, 0, st>>>(hT, ssm_pool, pool, seqlens, idx,
+                                                     ssm_row_elems);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace sss
