@@ -341,3 +341,34 @@ def prefill_to_pool(x, state_in, K, hT, conv_pool, ssm_pool, cache_seqlens, conv
         if sp is not None and hT is not None:
             sp[r] = _f64(hT)[b]
     return cp, sp, bad
+
+
+def conv_state_fwd_packed(x, w, bias, S, seq_idx, apply_silu: bool = True):
+    """The conv with state over rows that pack several samples ("Chapter 7:
+    state, chunking and incremental inference", section "packed sequence
+    boundaries"): tap k of token t reads extended-sequence entry u_{t+k} only
+    when that entry's sequence id equals token t's (identity equality, as
+    the page states: a reused id is not recognised as a reset).  The state
+    entries (positions < 0) carry token 0's id: a call continues the sample
+    its first token belongs to.  F = u[L : L+K-1] as without ids.
+    x [Bz, L, D], w [D, K], bias [D] | None, S [Bz, D, K-1] | None,
+    seq_idx [Bz, L] int.  Returns (out [Bz, L, D], F [Bz, D, K-1])."""
+    x, w = _f64(x), _f64(w)
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    bias = np.zeros(D) if bias is None else _f64(bias)
+    S = np.zeros((Bz, D, K - 1)) if S is None else _f64(S)
+    ids = np.asarray(getattr(seq_idx, "data", seq_idx)).astype(np.int64)
+    out = np.empty((Bz, L, D))
+    F = np.empty((Bz, D, K - 1))
+    for b in range(Bz):
+        u = np.concatenate([S[b], x[b].T], axis=1)              # [D, K-1+L]
+        uid = np.concatenate([np.full(K - 1, ids[b, 0] if L else 0), ids[b]])
+        for t in range(L):
+            z = bias.copy()
+            for k in range(K):
+                if uid[t + k] == ids[b, t]:
+                    z += w[:, k] * u[:, t + k]
+            out[b, t] = z / (1.0 + np.exp(-z)) if apply_silu else z
+        F[b] = u[:, L:L + K - 1]
+    return out, F

@@ -719,3 +719,55 @@ def test_prefill_then_update_equals_whole_forward(circular, L, Lnew, S_len, K):
                                         B[:, post], C[:, post], sp)
     assert nbad == 0
     np.testing.assert_allclose(y, y_all[:, post], rtol=1e-10, atol=1e-10)
+
+
+# ---------------------------------------------------------------------------
+# packed sequences in the conv
+# ---------------------------------------------------------------------------
+
+def test_packed_conv_does_not_read_across_samples():
+    """Samples A = [a1, a2] and B = [b1, b2] packed in one row, K = 3: B's
+    first token must not read A's end; one-hot weights pick each tap."""
+    x = np.array([1.0, 10.0, 100.0, 1000.0]).reshape(1, 4, 1)
+    ids = np.array([[0, 0, 1, 1]])
+    got = []
+    for k in range(3):
+        w = np.zeros((1, 3)); w[0, k] = 1.0
+        out, _ = oracle.conv_state_fwd_packed(x, w, None, None, ids, apply_silu=False)
+        got.append(out[0, :, 0])
+    got = np.array(got)                           # [tap k, token t]
+    # token t, tap k reads position t + k - 2 (0 before the row start)
+    np.testing.assert_array_equal(got[:, 2], [0.0, 0.0, 100.0])      # b1 alone
+    np.testing.assert_array_equal(got[:, 3], [0.0, 100.0, 1000.0])   # b2 reads b1 only
+    np.testing.assert_array_equal(got[:, 1], [0.0, 1.0, 10.0])       # a2 reads a1
+
+
+def test_packed_conv_reused_id_is_not_a_reset():
+    """Ids A, B, A: equality alone lets the second A read the first A's input
+    (the page's caveat about reused ids)."""
+    x = np.array([1.0, 10.0, 100.0]).reshape(1, 3, 1)
+    w = np.array([[1.0, 0.0, 0.0]])               # tap 0: position t - 2
+    out, _ = oracle.conv_state_fwd_packed(x, w, None, None, np.array([[0, 1, 0]]), apply_silu=False)
+    assert out[0, 2, 0] == 1.0
+
+
+@pytest.mark.parametrize("bounds", [[5], [2, 9], [1, 2, 3], []])
+def test_packed_conv_equals_separate_samples(bounds):
+    """A packed row equals the samples run one by one: the first continues
+    from the state S, every later one starts from a zero state; F is the
+    row's last K-1 inputs."""
+    g = np.random.default_rng(90 + len(bounds))
+    Bz, L, D, K = 2, 12, 5, 4
+    x = g.standard_normal((Bz, L, D))
+    w, bias, S = g.standard_normal((D, K)), g.standard_normal(D), g.standard_normal((Bz, D, K - 1))
+    ids = np.zeros((Bz, L), np.int64)
+    for i, s in enumerate(bounds):
+        ids[:, s:] = i + 1
+    out, F = oracle.conv_state_fwd_packed(x, w, bias, S, ids)
+    edges = [0] + bounds + [L]
+    for i in range(len(edges) - 1):
+        sl = slice(edges[i], edges[i + 1])
+        ref, _ = oracle.conv_state_fwd(x[:, sl], w, bias, S if i == 0 else None)
+        np.testing.assert_allclose(out[:, sl], ref, rtol=1e-13, atol=1e-13)
+    _, F_plain = oracle.conv_state_fwd(x, w, bias, S)
+    np.testing.assert_array_equal(F, F_plain)
