@@ -176,6 +176,25 @@ sss_status sss_conv_state_bwd_noalloc(const void* x, sss_dtype x_dtype, const fl
                                       int K, int apply_silu, sss_stream_t stream);
 
 /*
+ * sss_conv_state_fwd_packed -- sss_conv_state_fwd over rows that pack several
+ * samples.  Source: "Chapter 7: state, chunking and incremental inference",
+ * section "packed sequence boundaries": with samples A and B concatenated in
+ * one row, B's first tokens must not read A's end; tap k of token t reads
+ * the extended-sequence entry u_{t+k} only when that entry's sequence id
+ * equals token t's (identity equality: a reused id, as in A, B, A, is not
+ * recognised as a reset - the caller gives distinct ids within a window).
+ * The state entries (positions < 0) carry token 0's id: the call continues
+ * the sample its first token belongs to.  F = u[L : L+K-1] as without ids.
+ *  seq_idx  [Bz, L] int32 (device); every other argument as for
+ *           sss_conv_state_fwd (state_out may equal state_in).
+ */
+sss_status sss_conv_state_fwd_packed(const void* x, sss_dtype x_dtype, const float* w,
+                                     const float* bias, const void* state_in, void* state_out,
+                                     const int32_t* seq_idx, void* u, sss_dtype u_dtype,
+                                     int64_t Bz, int64_t L, int64_t D, int K, int apply_silu,
+                                     sss_stream_t stream);
+
+/*
  * sss_ssm_scan_fwd -- scalar-decay selective scan from an initial state.
  *
  * Source: "Understanding and Improving Length Generalization in Recurrent

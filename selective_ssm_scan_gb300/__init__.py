@@ -73,6 +73,9 @@ _lib.sss_ssm_scan_bwd_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i]
 _lib.sss_ssm_scan_bwd.restype = _i
 _lib.sss_ssm_scan_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i64, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_conv_state_fwd_packed.restype = _i
+_lib.sss_conv_state_fwd_packed.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _i64,
+                                           _i, _i, _p]
 _lib.sss_prefill_to_pool.restype = _i
 _lib.sss_prefill_to_pool.argtypes = [_p, _i, _p, _i, _p, _p, _i64, _i, _p, _p, _p, _i64, _i64,
                                      _i64, _i, _i, _i, _p]
@@ -297,6 +300,26 @@ def ssm_scan_bwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
                                _ptr(workspace), wsb, _stream(stream))
     _check("sss_ssm_scan_bwd", rc)
     return dx, ddt, dA, dB, dC, dh0
+
+
+def conv_state_fwd_packed(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                          state_in: Optional[torch.Tensor], seq_idx: torch.Tensor,
+                          state_out: Optional[torch.Tensor] = None, u: Optional[torch.Tensor] = None,
+                          u_dtype=torch.float32, apply_silu: bool = True, stream=None):
+    """conv_state_fwd over rows packing several samples: tap k of token t reads
+    u_{t+k} only when seq_idx agrees (seq_idx [Bz, L] int32).  Returns (u, F)."""
+    Bz, L, D = x.shape
+    K = w.shape[1]
+    if seq_idx.dtype != torch.int32:
+        raise TypeError("seq_idx must be int32")
+    if u is None:
+        u = torch.empty((Bz, L, D), dtype=u_dtype, device=x.device)
+    if state_out is None:
+        state_out = torch.empty((Bz, D, K - 1), dtype=x.dtype, device=x.device)
+    _check("sss_conv_state_fwd_packed", _lib.sss_conv_state_fwd_packed(
+        _ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(state_in), _ptr(state_out), _ptr(seq_idx),
+        _ptr(u), _dt(u), Bz, L, D, K, int(bool(apply_silu)), _stream(stream)))
+    return u, state_out
 
 
 def prefill_to_pool(x: torch.Tensor, conv_state_in: Optional[torch.Tensor], K: int,

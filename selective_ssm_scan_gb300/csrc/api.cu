@@ -49,6 +49,10 @@ cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, c
                                   int64_t Bz, int64_t L, int64_t D, int K, int silu_on,
                                   void* ws, cudaStream_t st);
 size_t conv_state_bwd_workspace(int64_t Bz, int64_t L, int64_t D, int K);
+cudaError_t conv_packed_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
+                               const void* s_in, void* s_out, const int32_t* seq_idx, void* u,
+                               sss_dtype ut, int64_t Bz, int64_t L, int64_t D, int K, int silu_on,
+                               cudaStream_t st);
 bool conv_state_bwd_supports(int K);
 size_t ssm_scan_bwd_workspace(int64_t Bz, int64_t L, int H, int P, int N);
 cudaError_t state_reset_launch(const float* u, float p, float* h, int64_t Bz, int64_t h_elems,
@@ -174,6 +178,29 @@ sss_status sss_conv_state_fwd(const void* x, sss_dtype x_dtype, const float* w,
   return from_cuda(conv_state_fwd_launch(x, x_dtype, w, bias, state_in, state_out, u, u_dtype,
                                          Bz, L, D, K, apply_silu != 0,
                                          reinterpret_cast<cudaStream_t>(stream)));
+}
+
+sss_status sss_conv_state_fwd_packed(const void* x, sss_dtype x_dtype, const float* w,
+                                     const float* bias, const void* state_in, void* state_out,
+                                     const int32_t* seq_idx, void* u, sss_dtype u_dtype,
+                                     int64_t Bz, int64_t L, int64_t D, int K, int apply_silu,
+                                     sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(u_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || D < 0 || K < 1) return SSS_ERR_INVALID_ARG;
+  if (K > 8) return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0 || D == 0) return SSS_OK;
+  if (Bz > 65535 || (L + 15) / 16 > 65535) return SSS_ERR_UNSUPPORTED;
+  const size_t xs = dtype_size(x_dtype), us = dtype_size(u_dtype);
+  if (!w || !aligned(w, 4) || (bias && !aligned(bias, 4))) return SSS_ERR_INVALID_ARG;
+  if (L > 0 && (!x || !u || !seq_idx || !aligned(x, xs) || !aligned(u, us) ||
+                !aligned(seq_idx, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if ((state_in && !aligned(state_in, xs)) || (state_out && !aligned(state_out, xs)))
+    return SSS_ERR_INVALID_ARG;
+  if (L == 0 && !state_out) return SSS_OK;
+  return from_cuda(conv_packed_launch(x, x_dtype, w, bias, state_in, state_out, seq_idx, u,
+                                      u_dtype, Bz, L, D, K, apply_silu != 0,
+                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 size_t sss_ssm_scan_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G,

@@ -237,4 +237,103 @@ cudaError_t conv_state_fwd_launch(const void* x, sss_dtype xt, const float* w,
   return conv_dispatch_u<float, __nv_bfloat16>(x, w, bias, s_in, s_out, u, Bz, L, D, K, silu_on, st);
 }
 
+
+// ---- packed samples -----------------------------------------------------------
+// The conv over rows that pack several samples ("Chapter 7: state, chunking
+// and incremental inference", section "packed sequence boundaries"): tap k of
+// token t reads u_{t+k} only when its sequence id equals token t's (identity
+// equality); state entries (positions < 0) carry token 0's id.  F is the
+// row's last K-1 inputs, as without ids.  One thread per (sequence, channel,
+// tile of kPackTile tokens) walks its tile with a register window of inputs
+// and ids; the thread of tile 0 writes F (state_out may alias state_in).
+namespace {
+constexpr int kPackTile = 16;
+
+template <typename TX, typename TU, bool SILU>
+__global__ void __launch_bounds__(kConvThreads)
+conv_packed_kernel(const TX* __restrict__ x, const float* __restrict__ w,
+                   const float* __restrict__ bias, const TX* s_in, TX* s_out,
+                   const int32_t* __restrict__ seq_idx, TU* __restrict__ u, int64_t L, int64_t D,
+                   int K) {
+  const int64_t d = blockIdx.x * int64_t(kConvThreads) + threadIdx.x;
+  if (d >= D) return;
+  const int64_t b = blockIdx.z;
+  const int64_t t0 = int64_t(blockIdx.y) * kPackTile;
+  const int32_t* ids = seq_idx + b * L;
+  const int32_t id0 = L > 0 ? ids[0] : 0;
+  float win[kConvMaxK];   // u_{t-K+1} .. u_{t-1}, oldest first
+  int32_t wid[kConvMaxK];
+  float wk[kConvMaxK];
+  for (int k = 0; k < K; ++k) wk[k] = w[d * K + k];
+  const float bsd = bias ? bias[d] : 0.0f;
+  for (int j = 0; j < K - 1; ++j) {
+    const int64_t pos = t0 - (K - 1) + j;
+    if (pos < 0) {
+      const int64_t e = K - 1 + pos;  // extended index into S
+      win[j] = s_in ? to_f32(s_in[(b * D + d) * (K - 1) + e]) : 0.0f;
+      wid[j] = id0;
+    } else {
+      win[j] = to_f32(x[(b * L + pos) * D + d]);
+      wid[j] = ids[pos];
+    }
+  }
+  for (int64_t t = t0; t < t0 + kPackTile && t < L; ++t) {
+    const float xv = to_f32(x[(b * L + t) * D + d]);
+    const int32_t it = ids[t];
+    float z = fmaf(wk[K - 1], xv, bsd);
+    for (int j = 0; j < K - 1; ++j)
+      if (wid[j] == it) z = fmaf(wk[j], win[j], z);
+    u[(b * L + t) * D + d] = from_f32<TU>(SILU ? silu(z) : z);
+    for (int j = 0; j + 1 < K - 1; ++j) {
+      win[j] = win[j + 1];
+      wid[j] = wid[j + 1];
+    }
+    if (K > 1) {
+      win[K - 2] = xv;
+      wid[K - 2] = it;
+    }
+  }
+  if (blockIdx.y == 0 && s_out) {  // F_j = u[L + j], read in increasing j before it is written
+    const int64_t sb = (b * D + d) * (K - 1);
+    for (int j = 0; j < K - 1; ++j) {
+      const int64_t e = L + j;
+      s_out[sb + j] = e < K - 1 ? (s_in ? s_in[sb + e] : from_f32<TX>(0.0f))
+                                : x[(b * L + (e - (K - 1))) * D + d];
+    }
+  }
+}
+
+template <typename TX, typename TU>
+cudaError_t launch_packed(const void* x, const float* w, const float* bias, const void* s_in,
+                          void* s_out, const int32_t* seq_idx, void* u, int64_t Bz, int64_t L,
+                          int64_t D, int K, int silu_on, cudaStream_t st) {
+  const int64_t tiles = L > 0 ? (L + kPackTile - 1) / kPackTile : 1;
+  if (Bz == 0 || D == 0) return cudaSuccess;
+  if (Bz > 65535 || tiles > 65535) return cudaErrorInvalidValue;
+  const dim3 g(unsigned((D + kConvThreads - 1) / kConvThreads), unsigned(tiles), unsigned(Bz));
+  if (silu_on)
+    conv_packed_kernel<TX, TU, true><<<g, kConvThreads, 0, st>>>(
+        static_cast<const TX*>(x), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out),
+        seq_idx, static_cast<TU*>(u), L, D, K);
+  else
+    conv_packed_kernel<TX, TU, false><<<g, kConvThreads, 0, st>>>(
+        static_cast<const TX*>(x), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out),
+        seq_idx, static_cast<TU*>(u), L, D, K);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t conv_packed_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
+                               const void* s_in, void* s_out, const int32_t* seq_idx, void* u,
+                               sss_dtype ut, int64_t Bz, int64_t L, int64_t D, int K, int silu_on,
+                               cudaStream_t st) {
+  if (xt == SSS_BF16 && ut == SSS_F32)
+    return launch_packed<__nv_bfloat16, float>(x, w, bias, s_in, s_out, seq_idx, u, Bz, L, D, K, silu_on, st);
+  if (xt == SSS_BF16 && ut == SSS_BF16)
+    return launch_packed<__nv_bfloat16, __nv_bfloat16>(x, w, bias, s_in, s_out, seq_idx, u, Bz, L, D, K, silu_on, st);
+  if (xt == SSS_F32 && ut == SSS_F32)
+    return launch_packed<float, float>(x, w, bias, s_in, s_out, seq_idx, u, Bz, L, D, K, silu_on, st);
+  return launch_packed<float, __nv_bfloat16>(x, w, bias, s_in, s_out, seq_idx, u, Bz, L, D, K, silu_on, st);
+}
+
 }  // namespace sss

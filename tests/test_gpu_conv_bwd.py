@@ -141,3 +141,35 @@ def test_conv_bwd_full_size_sampled():
     assert_y_close(f64(dS[:, ch]), dS_r, "dS")
     assert_rel(f64(dw[ch]), dw_r, F32_REL, "dw")
     assert_rel(f64(db[ch]), db_r, F32_REL, "dbias")
+
+
+# ---------------------------------------------------------------------------
+# packed samples (seq_idx) in the conv forward
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("L,D,K,xdt,udt,bounds", [
+    (40, 256, 4, "bf16", "f32", [5, 17, 18]),
+    (33, 70, 3, "f32", "f32", [1]),
+    (100, 64, 8, "bf16", "bf16", [50, 51, 52, 99]),
+    (7, 32, 4, "f32", "bf16", []),
+])
+def test_packed_conv_matches_oracle(L, D, K, xdt, udt, bounds):
+    g = np.random.default_rng(200 + L)
+    Bz = 3
+    x = synth.store(g.standard_normal((Bz, L, D)), xdt)
+    w = synth.f32(g.normal(0, np.sqrt(0.5), (D, K)))
+    bias = synth.f32(np.full(D, 0.1))
+    S = synth.store(g.standard_normal((Bz, D, K - 1)), xdt)
+    ids = np.zeros((Bz, L), np.int32)
+    for i, s in enumerate(bounds):
+        ids[:, s:] = i + 1
+    ids[1] += 7                                         # other ids on another row
+    u, F = sss.conv_state_fwd_packed(T(x), T(w), T(bias), T(S),
+                                     torch.from_numpy(ids).to(DEV), u_dtype=TD[udt])
+    torch.cuda.synchronize()
+    ref, F_ref = oracle.conv_state_fwd_packed(x, w, bias, S, ids)
+    if udt == "f32":
+        assert_rel(f64(u), ref, F32_REL if xdt == "f32" else 1e-6, "u")
+    else:
+        assert_y_close(f64(u), ref, "u")
+    np.testing.assert_array_equal(f64(F), F_ref)         # the state: copied inputs, bit-exact
