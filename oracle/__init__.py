@@ -372,3 +372,38 @@ def conv_state_fwd_packed(x, w, bias, S, seq_idx, apply_silu: bool = True):
             out[b, t] = z / (1.0 + np.exp(-z)) if apply_silu else z
         F[b] = u[:, L:L + K - 1]
     return out, F
+
+
+def ssm_scan_packed(u, dt, A, B, C, h0, seq_idx):
+    """The scan over rows packing several samples: at a token whose sequence
+    id differs from the previous token's the state restarts from zero (no
+    history crosses a sample boundary, the state counterpart of the conv's
+    packed-boundary rule); the first token continues from h0.  Token by token.
+    Returns (y [Bz, L, H, P], hT)."""
+    dt, A, B, C = _f64(dt), _f64(A), _f64(B), _f64(C)
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    u = _f64(u)
+    P = u.shape[3] if u.ndim == 4 else u.shape[2] // H
+    u = u.reshape(Bz, L, H, P)
+    ids = np.asarray(getattr(seq_idx, "data", seq_idx)).astype(np.int64)
+    g_of_h = np.arange(H) // (H // G)
+    h = np.zeros((Bz, H, P, N)) if h0 is None else _f64(h0).copy()
+    y = np.zeros((Bz, L, H, P))
+    for t in range(L):
+        a = np.exp(dt[:, t, :] * A[None, :])
+        if t > 0:
+            a = np.where((ids[:, t] != ids[:, t - 1])[:, None], 0.0, a)
+        Bt = B[:, t, g_of_h, :]
+        Ct = C[:, t, g_of_h, :]
+        h = a[:, :, None, None] * h + u[:, t, :, :, None] * Bt[:, :, None, :]
+        y[:, t] = np.einsum("bhpn,bhn->bhp", h, Ct)
+    return y, h
+
+
+def mixer_fwd_packed(x, dt, A, B, C, w, bias, conv_state, h0, seq_idx):
+    """One segment of the forward over packed rows: the packed conv, then the
+    packed scan."""
+    u, F = conv_state_fwd_packed(x, w, bias, conv_state, seq_idx, True)
+    y, hT = ssm_scan_packed(u, dt, A, B, C, h0, seq_idx)
+    return y, F, hT

@@ -771,3 +771,22 @@ def test_packed_conv_equals_separate_samples(bounds):
         np.testing.assert_allclose(out[:, sl], ref, rtol=1e-13, atol=1e-13)
     _, F_plain = oracle.conv_state_fwd(x, w, bias, S)
     np.testing.assert_array_equal(F, F_plain)
+
+
+@pytest.mark.parametrize("bounds", [[3], [1, 2, 9], []])
+def test_packed_scan_equals_separate_samples(bounds):
+    """A packed row equals its samples scanned one by one (the first from h0,
+    the others from zero), and agrees with the unpacked scan without
+    boundaries."""
+    u, dt, A, B, C, h0, _, _ = _scan_problem(95 + len(bounds), L=12)
+    Bz, L = dt.shape[:2]
+    ids = np.zeros((Bz, L), np.int64)
+    for i, s in enumerate(bounds):
+        ids[:, s:] = 5 * (i + 1)
+    y, hT = oracle.ssm_scan_packed(u, dt, A, B, C, h0, ids)
+    edges = [0] + bounds + [L]
+    for i in range(len(edges) - 1):
+        sl = slice(edges[i], edges[i + 1])
+        yr, hr = oracle.ssm_scan(u[:, sl], dt[:, sl], A, B[:, sl], C[:, sl], h0 if i == 0 else None)
+        np.testing.assert_allclose(y[:, sl], yr, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hT, hr, rtol=1e-12, atol=1e-12)
