@@ -352,6 +352,33 @@ sss_status sss_state_std_trace(const void* x, sss_dtype x_dtype, const void* dt,
                                sss_stream_t stream);
 
 /*
+ * sss_ssm_scan_fwd_packed / sss_mixer_fwd_packed -- the forward over rows
+ * that pack several samples (seq_idx [Bz, L] int32, device).  Source:
+ * "Chapter 7: state, chunking and incremental inference", section "packed
+ * sequence boundaries" (no history crosses a sample boundary).  The conv of
+ * sss_mixer_fwd_packed follows sss_conv_state_fwd_packed; in the scan a
+ * token whose id differs from the previous token's restarts the state from
+ * zero (its decay is exactly zero: the kernels give it log-decay -200, which
+ * underflows to 0 in fp32); the first token continues from h0_in.  Arguments
+ * otherwise as for sss_ssm_scan_fwd and sss_mixer_fwd; the fused packed
+ * forward needs the two-heads-per-CTA kernel (H / G even), else
+ * SSS_ERR_UNSUPPORTED (compose sss_conv_state_fwd_packed and
+ * sss_ssm_scan_fwd_packed instead).
+ */
+sss_status sss_ssm_scan_fwd_packed(const void* x, sss_dtype x_dtype, const void* dt,
+                                   const float* A, const void* B, const void* C,
+                                   sss_dtype act_dtype, const float* h0_in, float* hT_out,
+                                   const int32_t* seq_idx, void* y, sss_dtype y_dtype, int64_t Bz,
+                                   int64_t L, int H, int P, int N, int G, sss_stream_t stream);
+sss_status sss_mixer_fwd_packed(const void* x, sss_dtype x_dtype, const float* w,
+                                const float* bias, const void* conv_state_in,
+                                void* conv_state_out, const void* dt, const float* A,
+                                const void* B, const void* C, const float* h0_in, float* hT_out,
+                                const int32_t* seq_idx, void* y, sss_dtype y_dtype, int64_t Bz,
+                                int64_t L, int H, int P, int N, int G, int K,
+                                sss_stream_t stream);
+
+/*
  * sss_mixer_fwd -- one segment of the streaming forward in a single kernel:
  * the conv with state of sss_conv_state_fwd (SiLU applied) feeding the scan
  * of sss_ssm_scan_fwd, so the conv output never goes to memory.  Sources:

@@ -73,6 +73,12 @@ _lib.sss_ssm_scan_bwd_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i]
 _lib.sss_ssm_scan_bwd.restype = _i
 _lib.sss_ssm_scan_bwd.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
                                   _i64, _i64, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_ssm_scan_fwd_packed.restype = _i
+_lib.sss_ssm_scan_fwd_packed.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _p, _i, _i64, _i64,
+                                         _i, _i, _i, _i, _p]
+_lib.sss_mixer_fwd_packed.restype = _i
+_lib.sss_mixer_fwd_packed.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i,
+                                      _i64, _i64, _i, _i, _i, _i, _i, _p]
 _lib.sss_conv_state_fwd_packed.restype = _i
 _lib.sss_conv_state_fwd_packed.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _i, _i64, _i64, _i64,
                                            _i, _i, _p]
@@ -300,6 +306,45 @@ def ssm_scan_bwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
                                _ptr(workspace), wsb, _stream(stream))
     _check("sss_ssm_scan_bwd", rc)
     return dx, ddt, dA, dB, dC, dh0
+
+
+def ssm_scan_fwd_packed(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                        C: torch.Tensor, h0: Optional[torch.Tensor], seq_idx: torch.Tensor,
+                        hT: Optional[torch.Tensor] = None, y_dtype=None, stream=None):
+    """ssm_scan_fwd over rows packing several samples: the state restarts at
+    every change of seq_idx [Bz, L] int32.  Returns (y, hT)."""
+    Bz, L, H = dt.shape
+    G, N = B.shape[2], B.shape[3]
+    P = x.shape[-1] if x.dim() == 4 else x.shape[-1] // H
+    y = torch.empty((Bz, L, H, P), dtype=y_dtype or dt.dtype, device=x.device)
+    if hT is None:
+        hT = torch.empty((Bz, H, P, N), dtype=torch.float32, device=x.device)
+    _check("sss_ssm_scan_fwd_packed", _lib.sss_ssm_scan_fwd_packed(
+        _ptr(x), _dt(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _dt(dt), _ptr(h0), _ptr(hT),
+        _ptr(seq_idx), _ptr(y), _dt(y), Bz, L, H, P, N, G, _stream(stream)))
+    return y, hT
+
+
+def mixer_fwd_packed(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                     C: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
+                     conv_state: Optional[torch.Tensor], h0: Optional[torch.Tensor],
+                     seq_idx: torch.Tensor, y_dtype=None, stream=None):
+    """mixer_fwd over rows packing several samples (seq_idx [Bz, L] int32):
+    the conv's taps and the scan's state stop at sample boundaries.  Returns
+    (y, F, hT)."""
+    Bz, L, D = x.shape
+    H = dt.shape[2]
+    P = D // H
+    G, N = B.shape[2], B.shape[3]
+    K = w.shape[1]
+    y = torch.empty((Bz, L, H, P), dtype=y_dtype or x.dtype, device=x.device)
+    F = torch.empty((Bz, D, K - 1), dtype=x.dtype, device=x.device)
+    hT = torch.empty((Bz, H, P, N), dtype=torch.float32, device=x.device)
+    _check("sss_mixer_fwd_packed", _lib.sss_mixer_fwd_packed(
+        _ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(conv_state), _ptr(F), _ptr(dt), _ptr(A),
+        _ptr(B), _ptr(C), _ptr(h0), _ptr(hT), _ptr(seq_idx), _ptr(y), _dt(y), Bz, L, H, P, N, G,
+        K, _stream(stream)))
+    return y, F, hT
 
 
 def conv_state_fwd_packed(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],

@@ -17,30 +17,31 @@ cudaError_t ssm_scan_simt_launch(const void* x, sss_dtype xt, const void* dt, co
                                  const void* B, const void* C, sss_dtype at,
                                  const float* h0, float* hT, void* y, sss_dtype yt,
                                  int64_t Bz, int64_t L, int H, int P, int N, int G,
-                                 cudaStream_t st);
+                                 const int32_t* seq_idx, cudaStream_t st);
 bool ssm_scan_tc_supports(sss_dtype xt, sss_dtype at, sss_dtype yt, int64_t L, int H, int P,
                           int N, int G);
 cudaError_t ssm_scan_tc_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                const void* B, const void* C, const float* h0, float* hT,
                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int P,
-                               int N, int G, int* status, cudaStream_t st);
+                               int N, int G, int* status, const int32_t* seq_idx,
+                               cudaStream_t st);
 bool mixer_fwd_tc_supports(sss_dtype xt, sss_dtype at, int K, int64_t L, int H, int P, int N,
                            int G);
 cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias,
                                 const void* s_in, void* s_out, const void* dt, const float* A,
                                 const void* B, const void* C, const float* h0, float* hT,
                                 void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G, int K,
-                                int* status, cudaStream_t st);
+                                int* status, const int32_t* seq_idx, cudaStream_t st);
 bool ssm_scan_pair_supports(sss_dtype at, int64_t L, int H, int P, int N, int G);
 cudaError_t ssm_scan_pair_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                  const void* B, const void* C, const float* h0, float* hT,
                                  void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                 int* status, cudaStream_t st);
+                                 int* status, const int32_t* seq_idx, cudaStream_t st);
 cudaError_t mixer_fwd_pair_launch(const void* x, const float* w, const float* bias,
                                   const void* s_in, void* s_out, const void* dt, const float* A,
                                   const void* B, const void* C, const float* h0, float* hT,
                                   void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                  int K, int* status, cudaStream_t st);
+                                  int K, int* status, const int32_t* seq_idx, cudaStream_t st);
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
                                cudaStream_t st);
 cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
@@ -259,12 +260,11 @@ sss_status sss_conv_state_bwd(const void* x, sss_dtype x_dtype, const float* w,
       dbias, Bz, L, D, K, apply_silu != 0, workspace, reinterpret_cast<cudaStream_t>(stream)));
 }
 
-sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
-                            const void* B, const void* C, sss_dtype act_dtype,
-                            const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
-                            int64_t Bz, int64_t L, int H, int P, int N, int G, void* workspace,
-                            size_t workspace_bytes, sss_stream_t stream) {
-  (void)workspace; (void)workspace_bytes;
+static sss_status scan_fwd_impl(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
+                                const void* B, const void* C, sss_dtype act_dtype,
+                                const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
+                                int64_t Bz, int64_t L, int H, int P, int N, int G,
+                                const int32_t* seq_idx, sss_stream_t stream) {
   if (!dtype_ok(x_dtype) || !dtype_ok(act_dtype) || !dtype_ok(y_dtype)) return SSS_ERR_INVALID_ARG;
   if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return SSS_ERR_INVALID_ARG;
   if (Bz == 0) return SSS_OK;
@@ -281,13 +281,33 @@ sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, co
       (!h0_in || aligned(h0_in, 16)) && (!hT_out || aligned(hT_out, 16))) {
     if (ssm_scan_pair_supports(act_dtype, L, H, P, N, G))
       return from_cuda(ssm_scan_pair_launch(x, x_dtype, dt, A, B, C, h0_in, hT_out, y, y_dtype,
-                                            Bz, L, H, G, status_word(), st));
+                                            Bz, L, H, G, status_word(), seq_idx, st));
     return from_cuda(ssm_scan_tc_launch(x, x_dtype, dt, A, B, C, h0_in, hT_out, y, y_dtype, Bz,
-                                        L, H, P, N, G, status_word(), st));
+                                        L, H, P, N, G, status_word(), seq_idx, st));
   }
   if (!ssm_scan_simt_supports(P, N)) return SSS_ERR_UNSUPPORTED;
   return from_cuda(ssm_scan_simt_launch(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y,
-                                        y_dtype, Bz, L, H, P, N, G, st));
+                                        y_dtype, Bz, L, H, P, N, G, seq_idx, st));
+}
+
+sss_status sss_ssm_scan_fwd(const void* x, sss_dtype x_dtype, const void* dt, const float* A,
+                            const void* B, const void* C, sss_dtype act_dtype,
+                            const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
+                            int64_t Bz, int64_t L, int H, int P, int N, int G, void* workspace,
+                            size_t workspace_bytes, sss_stream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  return scan_fwd_impl(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y, y_dtype, Bz, L, H,
+                       P, N, G, nullptr, stream);
+}
+
+sss_status sss_ssm_scan_fwd_packed(const void* x, sss_dtype x_dtype, const void* dt,
+                                   const float* A, const void* B, const void* C,
+                                   sss_dtype act_dtype, const float* h0_in, float* hT_out,
+                                   const int32_t* seq_idx, void* y, sss_dtype y_dtype, int64_t Bz,
+                                   int64_t L, int H, int P, int N, int G, sss_stream_t stream) {
+  if (Bz > 0 && L > 0 && (!seq_idx || !aligned(seq_idx, 4))) return SSS_ERR_INVALID_ARG;
+  return scan_fwd_impl(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y, y_dtype, Bz, L, H,
+                       P, N, G, seq_idx, stream);
 }
 
 size_t sss_ssm_scan_bwd_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G) {
@@ -409,11 +429,11 @@ int sss_mixer_fwd_supported(int64_t Bz, int64_t L, int H, int P, int N, int G, i
   return (L == 0 || mixer_fwd_tc_supports(x_dtype, x_dtype, K, L > 0 ? L : 1, H, P, N, G)) ? 1 : 0;
 }
 
-sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const float* bias,
+static sss_status mixer_fwd_impl(const void* x, sss_dtype x_dtype, const float* w, const float* bias,
                          const void* conv_state_in, void* conv_state_out, const void* dt,
                          const float* A, const void* B, const void* C, const float* h0_in,
                          float* hT_out, void* y, sss_dtype y_dtype, int64_t Bz, int64_t L, int H,
-                         int P, int N, int G, int K, sss_stream_t stream) {
+                         int P, int N, int G, int K, const int32_t* seq_idx, sss_stream_t stream) {
   if (!dtype_ok(x_dtype) || !dtype_ok(y_dtype)) return SSS_ERR_INVALID_ARG;
   if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || K < 1)
     return SSS_ERR_INVALID_ARG;
@@ -431,7 +451,7 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const
     if (r != SSS_OK) return r;
     return from_cuda(ssm_scan_simt_launch(nullptr, SSS_F32, nullptr, A, nullptr, nullptr,
                                           x_dtype, h0_in, hT_out, nullptr, y_dtype, Bz, 0, H, P,
-                                          N, G, st));
+                                          N, G, nullptr, st));
   }
   if (!x || !dt || !B || !C || !y || !aligned(x, 16) || !aligned(dt, 2) || !aligned(B, 16) ||
       !aligned(C, 16) || !aligned(y, 16))
@@ -439,10 +459,33 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const
   if (ssm_scan_pair_supports(x_dtype, L, H, P, N, G))
     return from_cuda(mixer_fwd_pair_launch(x, w, bias, conv_state_in, conv_state_out, dt, A, B,
                                            C, h0_in, hT_out, y, y_dtype, Bz, L, H, G, K,
-                                           status_word(), st));
+                                           status_word(), seq_idx, st));
+  // packed rows need the pair kernel's per-piece halo mask
+  if (seq_idx) return SSS_ERR_UNSUPPORTED;
   return from_cuda(mixer_fwd_tc_launch(x, w, bias, conv_state_in, conv_state_out, dt, A, B, C,
                                        h0_in, hT_out, y, y_dtype, Bz, L, H, G, K, status_word(),
-                                       st));
+                                       nullptr, st));
+}
+
+sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w, const float* bias,
+                         const void* conv_state_in, void* conv_state_out, const void* dt,
+                         const float* A, const void* B, const void* C, const float* h0_in,
+                         float* hT_out, void* y, sss_dtype y_dtype, int64_t Bz, int64_t L, int H,
+                         int P, int N, int G, int K, sss_stream_t stream) {
+  return mixer_fwd_impl(x, x_dtype, w, bias, conv_state_in, conv_state_out, dt, A, B, C, h0_in,
+                        hT_out, y, y_dtype, Bz, L, H, P, N, G, K, nullptr, stream);
+}
+
+sss_status sss_mixer_fwd_packed(const void* x, sss_dtype x_dtype, const float* w,
+                                const float* bias, const void* conv_state_in,
+                                void* conv_state_out, const void* dt, const float* A,
+                                const void* B, const void* C, const float* h0_in, float* hT_out,
+                                const int32_t* seq_idx, void* y, sss_dtype y_dtype, int64_t Bz,
+                                int64_t L, int H, int P, int N, int G, int K,
+                                sss_stream_t stream) {
+  if (Bz > 0 && L > 0 && (!seq_idx || !aligned(seq_idx, 4))) return SSS_ERR_INVALID_ARG;
+  return mixer_fwd_impl(x, x_dtype, w, bias, conv_state_in, conv_state_out, dt, A, B, C, h0_in,
+                        hT_out, y, y_dtype, Bz, L, H, P, N, G, K, seq_idx, stream);
 }
 
 int sss_mixer_update_path(int L_new, int P, int N, int K, int S_len, sss_dtype act_dtype) {

@@ -10,6 +10,16 @@
 
 namespace sss {
 
+// log-decay given to a token that starts a new packed sample: exp(-200) is
+// 0 in fp32, so the state carried into it (and every product that weighs
+// earlier tokens through the decay) is exactly zero
+constexpr float kSampleStartLog = -200.0f;
+// whether token t of row b starts a new sample (seq_idx [Bz, L], NULL: never)
+__device__ __forceinline__ bool sample_start(const int32_t* seq_idx, int64_t b, int64_t L,
+                                             int64_t t) {
+  return seq_idx && t > 0 && seq_idx[b * L + t] != seq_idx[b * L + t - 1];
+}
+
 // Kernels OR status bits into a device status word (they never trap).  The
 // word lives in api.cu; its device address is passed to every kernel.
 __device__ __forceinline__ void raise_status(int* status, int bits) {

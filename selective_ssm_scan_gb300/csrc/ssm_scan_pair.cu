@@ -210,7 +210,7 @@ __device__ __forceinline__ void split_pair(uint64_t v, uint32_t& hi, uint32_t& l
 // x: the scan input u [Bz, L, H, 64] (TX = float or bf16), or with FUSED the
 // raw input [Bz, L, H*64] (bf16) that the producers convolve (K <= 4, SiLU).
 // Requires (H / G) even: both heads of a pair read the same B and C group.
-template <typename TX, typename TY, bool FUSED>
+template <typename TX, typename TY, bool FUSED, bool PACKED>
 __global__ void __launch_bounds__(pr::kThreads, 1)
 ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                      const __grid_constant__ CUtensorMap tmX, const TX* __restrict__ x,
@@ -218,7 +218,7 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
                      const float* h0, float* hT, TY* __restrict__ y,
                      const float* __restrict__ conv_w, const float* __restrict__ conv_b,
                      const TX* conv_s_in, TX* conv_s_out, int K, int L, int H, int G,
-                     int* status) {
+                     int* status, const int32_t* __restrict__ seq_idx) {
   using namespace pr;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -366,6 +366,12 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
               stage_x(p + n, 0);
               xs_issued = su + 2;
             }
+          }
+          if (PACKED && tb == 0 && inf->pad != 7) {
+            // packed rows: halo positions of another sample read as zero
+#pragma unroll
+            for (int i = 0; i < kMaxK - 1; ++i)
+              if (!((inf->pad >> i) & 1)) xr[i] = make_uint4(0u, 0u, 0u, 0u);
           }
           if (p == 0 && tb < kMaxK - 1 && nv > 0) {
             // positions < 0: the conv state S (zeros without one)
@@ -820,14 +826,21 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     // (tokens while both heads' Lam range stays <= kFactorRange), and per head
     // R = the middle of the range and Lam_end, published in the descriptor ring
     const float Ah[2] = {A[2 * pair], A[2 * pair + 1]};
+    // the log-decay l_t = dt_t A_h of the piece's tokens; a token that starts
+    // a new packed sample gets kSampleStartLog, which ends the piece before
+    // it (its range would pass kFactorRange) and zeroes the state it inherits
     auto load_dt = [&](int start, float (&v)[2][4]) {
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
+      for (int i = 0; i < 4; ++i) {
+        const int t = start + 4 * lane + i;
+        const bool reset = PACKED && t < L && sample_start(seq_idx, b, L, t);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int t = start + 4 * lane + i;
-          v[hh][i] = t < L ? __bfloat162float(dt[(int64_t(b) * L + t) * H + 2 * pair + hh]) : 0.0f;
-        }
+        for (int hh = 0; hh < 2; ++hh)
+          v[hh][i] = t < L ? (reset ? kSampleStartLog
+                                    : __bfloat162float(dt[(int64_t(b) * L + t) * H + 2 * pair + hh]) *
+                                          Ah[hh])
+                           : 0.0f;
+      }
     };
     float dtv[2][4];
     load_dt(0, dtv);
@@ -843,7 +856,7 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         float run = 0.0f;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          run += dtv[hh][i] * Ah[hh];
+          run += dtv[hh][i];
           lam[hh][i] = run;
         }
         float incl = run;  // inclusive scan of the lanes' sums
@@ -920,6 +933,21 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         inf->start = p;
         inf->n = n;
         inf->last = last ? 1 : 0;
+        // halo mask: bit j set when the conv of this piece may read position
+        // p - (K-1) + j (the same packed sample as token p; positions before
+        // the row carry token 0's id).  A piece never contains a sample start
+        // after its first token, so only the halo can belong to another sample.
+        int halo = 7;
+        if (PACKED && seq_idx) {
+          halo = 0;
+          const int32_t me = seq_idx[int64_t(b) * L + p];
+          for (int j = 0; j < kMaxK - 1; ++j) {
+            const int pos = p - (kMaxK - 1) + j;
+            const int32_t id = seq_idx[int64_t(b) * L + (pos < 0 ? 0 : pos)];
+            if (id == me) halo |= 1 << j;
+          }
+        }
+        inf->pad = halo;
       }
       __syncwarp();
       mbar_arrive(ctl.bar(BAR_INFO_FULL + slot));
@@ -945,7 +973,7 @@ template <typename TX, typename TY, bool FUSED>
 cudaError_t launch_pair(const void* x, const void* dt, const float* A, const void* B,
                         const void* C, const float* h0, float* hT, void* y, const float* w,
                         const float* bias, const void* s_in, void* s_out, int K, int64_t Bz,
-                        int64_t L, int H, int G, int* status, cudaStream_t st) {
+                        int64_t L, int H, int G, int* status, const int32_t* seq_idx, cudaStream_t st) {
   using namespace pr;
   CUtensorMap mB, mC, mX;
   if (!make_bc_map(&mB, B, Bz, L, G, kN) || !make_bc_map(&mC, C, Bz, L, G, kN))
@@ -955,14 +983,17 @@ cudaError_t launch_pair(const void* x, const void* dt, const float* A, const voi
   } else {
     mX = mB;  // unused
   }
-  auto kern = ssm_scan_pair_kernel<TX, TY, FUSED>;
+  // packed rows get their own instantiation: the ordinary one carries none of
+  // their checks
+  auto kern = seq_idx ? ssm_scan_pair_kernel<TX, TY, FUSED, true>
+                      : ssm_scan_pair_kernel<TX, TY, FUSED, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
   if (e != cudaSuccess) return e;
   kern<<<unsigned(Bz * (H / 2)), kThreads, kSmemBytes, st>>>(
       mB, mC, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, h0, hT,
       static_cast<TY*>(y), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out), K,
-      int(L), H, G, status);
+      int(L), H, G, status, seq_idx);
   return cudaGetLastError();
 }
 }  // namespace
@@ -977,11 +1008,11 @@ bool ssm_scan_pair_supports(sss_dtype at, int64_t L, int H, int P, int N, int G)
 cudaError_t ssm_scan_pair_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                  const void* B, const void* C, const float* h0, float* hT,
                                  void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                 int* status, cudaStream_t st) {
+                                 int* status, const int32_t* seq_idx, cudaStream_t st) {
   if (Bz * (H / 2) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
 #define SSS_PAIR(TXT, TYT)                                                                    \
   return launch_pair<TXT, TYT, false>(x, dt, A, B, C, h0, hT, y, nullptr, nullptr, nullptr,  \
-                                      nullptr, 1, Bz, L, H, G, status, st);
+                                      nullptr, 1, Bz, L, H, G, status, seq_idx, st);
   if (xt == SSS_F32 && yt == SSS_BF16) SSS_PAIR(float, __nv_bfloat16)
   if (xt == SSS_F32) SSS_PAIR(float, float)
   if (yt == SSS_BF16) SSS_PAIR(__nv_bfloat16, __nv_bfloat16)
@@ -993,13 +1024,13 @@ cudaError_t mixer_fwd_pair_launch(const void* x, const float* w, const float* bi
                                   const void* s_in, void* s_out, const void* dt, const float* A,
                                   const void* B, const void* C, const float* h0, float* hT,
                                   void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                  int K, int* status, cudaStream_t st) {
+                                  int K, int* status, const int32_t* seq_idx, cudaStream_t st) {
   if (Bz * (H / 2) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (yt == SSS_BF16)
     return launch_pair<__nv_bfloat16, __nv_bfloat16, true>(x, dt, A, B, C, h0, hT, y, w, bias,
-                                                           s_in, s_out, K, Bz, L, H, G, status, st);
+                                                           s_in, s_out, K, Bz, L, H, G, status, seq_idx, st);
   return launch_pair<__nv_bfloat16, float, true>(x, dt, A, B, C, h0, hT, y, w, bias, s_in, s_out,
-                                                 K, Bz, L, H, G, status, st);
+                                                 K, Bz, L, H, G, status, seq_idx, st);
 }
 
 }  // namespace sss

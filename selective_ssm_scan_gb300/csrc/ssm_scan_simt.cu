@@ -53,7 +53,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32)
 ssm_scan_simt_kernel(const TX* __restrict__ x, const TA* __restrict__ dt,
                      const float* __restrict__ A, const TA* __restrict__ Bm,
                      const TA* __restrict__ Cm, const float* h0, float* hT,
-                     TY* __restrict__ y, int64_t L, int H, int P, int N, int G, int TCH) {
+                     TY* __restrict__ y, int64_t L, int H, int P, int N, int G, int TCH,
+                     const int32_t* __restrict__ seq_idx) {
   extern __shared__ float smem[];
   float* xs = smem;               // [TCH][P]
   float* bs = xs + TCH * P;       // [TCH][N]
@@ -88,7 +89,9 @@ ssm_scan_simt_kernel(const TX* __restrict__ x, const TA* __restrict__ dt,
       cs[tt * N + n] = to_f32(Cm[o]);
     }
     for (int i = tid; i < nt; i += blockDim.x)
-      as[i] = expf(to_f32(dt[(int64_t(b) * L + t0 + i) * H + h]) * Ah);
+      as[i] = expf(sample_start(seq_idx, b, L, t0 + i)
+                       ? kSampleStartLog
+                       : to_f32(dt[(int64_t(b) * L + t0 + i) * H + h]) * Ah);
     __syncthreads();
 
     for (int tt = 0; tt < nt; ++tt) {
@@ -136,7 +139,7 @@ template <typename TX, typename TA, typename TY, int RP, int CN>
 static cudaError_t launch_simt(const void* x, const void* dt, const float* A,
                                const void* B, const void* C, const float* h0,
                                float* hT, void* y, int64_t Bz, int64_t L, int H,
-                               int P, int N, int G, cudaStream_t st) {
+                               int P, int N, int G, const int32_t* seq_idx, cudaStream_t st) {
   const int per_tok = (P + 2 * N + 1) * int(sizeof(float));
   int TCH = (40 * 1024) / per_tok;
   if (TCH > 32) TCH = 32;
@@ -148,17 +151,17 @@ static cudaError_t launch_simt(const void* x, const void* dt, const float* A,
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   kern<<<unsigned(grid), kSimtWarps * 32, smem, st>>>(
       static_cast<const TX*>(x), static_cast<const TA*>(dt), A, static_cast<const TA*>(B),
-      static_cast<const TA*>(C), h0, hT, static_cast<TY*>(y), L, H, P, N, G, TCH);
+      static_cast<const TA*>(C), h0, hT, static_cast<TY*>(y), L, H, P, N, G, TCH, seq_idx);
   return cudaGetLastError();
 }
 
 template <typename TX, typename TA, typename TY>
 static cudaError_t simt_shape(const void* x, const void* dt, const float* A, const void* B,
                               const void* C, const float* h0, float* hT, void* y, int64_t Bz,
-                              int64_t L, int H, int P, int N, int G, cudaStream_t st) {
+                              int64_t L, int H, int P, int N, int G, const int32_t* seq_idx, cudaStream_t st) {
 #define SSS_SIMT(RP, CN)                                                                  \
   if (P <= kSimtWarps * RP && N <= 32 * CN)                                               \
-    return launch_simt<TX, TA, TY, RP, CN>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
+    return launch_simt<TX, TA, TY, RP, CN>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
   SSS_SIMT(1, 1)
   SSS_SIMT(2, 2)
   SSS_SIMT(4, 4)
@@ -172,14 +175,14 @@ template <typename TX>
 static cudaError_t simt_act(const void* x, sss_dtype at, sss_dtype yt, const void* dt,
                             const float* A, const void* B, const void* C, const float* h0,
                             float* hT, void* y, int64_t Bz, int64_t L, int H, int P, int N,
-                            int G, cudaStream_t st) {
+                            int G, const int32_t* seq_idx, cudaStream_t st) {
   if (at == SSS_F32 && yt == SSS_F32)
-    return simt_shape<TX, float, float>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
+    return simt_shape<TX, float, float>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
   if (at == SSS_F32)
-    return simt_shape<TX, float, __nv_bfloat16>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
+    return simt_shape<TX, float, __nv_bfloat16>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
   if (yt == SSS_F32)
-    return simt_shape<TX, __nv_bfloat16, float>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
-  return simt_shape<TX, __nv_bfloat16, __nv_bfloat16>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
+    return simt_shape<TX, __nv_bfloat16, float>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
+  return simt_shape<TX, __nv_bfloat16, __nv_bfloat16>(x, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
 }
 
 bool ssm_scan_simt_supports(int P, int N) { return P <= kSimtWarps * 16 && N <= 256; }
@@ -188,10 +191,10 @@ cudaError_t ssm_scan_simt_launch(const void* x, sss_dtype xt, const void* dt, co
                                  const void* B, const void* C, sss_dtype at,
                                  const float* h0, float* hT, void* y, sss_dtype yt,
                                  int64_t Bz, int64_t L, int H, int P, int N, int G,
-                                 cudaStream_t st) {
+                                 const int32_t* seq_idx, cudaStream_t st) {
   if (xt == SSS_F32)
-    return simt_act<float>(x, at, yt, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
-  return simt_act<__nv_bfloat16>(x, at, yt, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, st);
+    return simt_act<float>(x, at, yt, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
+  return simt_act<__nv_bfloat16>(x, at, yt, dt, A, B, C, h0, hT, y, Bz, L, H, P, N, G, seq_idx, st);
 }
 
 }  // namespace sss

@@ -162,7 +162,8 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
                    const __nv_bfloat16* __restrict__ dt, const float* __restrict__ A,
                    const float* h0, float* hT, TY* __restrict__ y, const float* __restrict__ conv_w,
                    const float* __restrict__ conv_b, const TX* conv_s_in, TX* conv_s_out,
-                   int K, int L, int H, int G, int* status) {
+                   int K, int L, int H, int G, int* status,
+                     const int32_t* __restrict__ seq_idx) {
   extern __shared__ uint8_t smem_raw[];
   // 1024-byte aligned base, derived from the shared array itself so that the
   // compiler keeps every access in the shared address space
@@ -233,8 +234,13 @@ ssm_scan_tc_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constan
     for (int c = 0; c < nC; ++c) {
       const int t0 = c * kQ;
       const int valid = min(kQ, L - t0);
+      // a token that starts a new packed sample gets kSampleStartLog: the
+      // chunk's range passes kFactorRange, so it takes the plain weights
+      // exp(Lam_t - Lam_s), which are 0 across the start, as is the carry
       const float ell = ok && s < valid && warp < 4
-                            ? __bfloat162float(dt[(int64_t(b) * L + t0 + s) * H + h]) * Ah
+                            ? (sample_start(seq_idx, b, L, t0 + s)
+                                   ? kSampleStartLog
+                                   : __bfloat162float(dt[(int64_t(b) * L + t0 + s) * H + h]) * Ah)
                             : 0.0f;
       float u[NT][8];  // [token j][channel e]
       const int tb = t0 + NT * g4;  // first token of the group
@@ -854,7 +860,7 @@ template <typename TX, typename TY, bool FUSED>
 cudaError_t launch_tc(const void* x, const void* dt, const float* A, const void* B, const void* C,
                       const float* h0, float* hT, void* y, const float* w, const float* bias,
                       const void* s_in, void* s_out, int K, int64_t Bz, int64_t L, int H, int G,
-                      int* status, cudaStream_t st) {
+                      int* status, const int32_t* seq_idx, cudaStream_t st) {
   CUtensorMap mB, mC, mX;
   if (!make_bc_map(&mB, B, Bz, L, G, kN) || !make_bc_map(&mC, C, Bz, L, G, kN))
     return cudaErrorInvalidValue;
@@ -870,7 +876,7 @@ cudaError_t launch_tc(const void* x, const void* dt, const float* A, const void*
   kern<<<unsigned(Bz * H), kThreads, kSmemBytes, st>>>(
       mB, mC, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, h0, hT,
       static_cast<TY*>(y), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out), K,
-      int(L), H, G, status);
+      int(L), H, G, status, seq_idx);
   return cudaGetLastError();
 }
 }  // namespace
@@ -890,12 +896,12 @@ bool mixer_fwd_tc_supports(sss_dtype xt, sss_dtype at, int K, int64_t L, int H, 
 cudaError_t ssm_scan_tc_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                const void* B, const void* C, const float* h0, float* hT,
                                void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int P,
-                               int N, int G, int* status, cudaStream_t st) {
+                               int N, int G, int* status, const int32_t* seq_idx, cudaStream_t st) {
   (void)P; (void)N;
   if (Bz * H > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
 #define SSS_TC(TXT, TYT)                                                                    \
   return launch_tc<TXT, TYT, false>(x, dt, A, B, C, h0, hT, y, nullptr, nullptr, nullptr,  \
-                                    nullptr, 1, Bz, L, H, G, status, st);
+                                    nullptr, 1, Bz, L, H, G, status, seq_idx, st);
   if (xt == SSS_F32 && yt == SSS_BF16) SSS_TC(float, __nv_bfloat16)
   if (xt == SSS_F32) SSS_TC(float, float)
   if (yt == SSS_BF16) SSS_TC(__nv_bfloat16, __nv_bfloat16)
@@ -907,13 +913,13 @@ cudaError_t mixer_fwd_tc_launch(const void* x, const float* w, const float* bias
                                 const void* s_in, void* s_out, const void* dt, const float* A,
                                 const void* B, const void* C, const float* h0, float* hT,
                                 void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G, int K,
-                                int* status, cudaStream_t st) {
+                                int* status, const int32_t* seq_idx, cudaStream_t st) {
   if (Bz * H > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (yt == SSS_BF16)
     return launch_tc<__nv_bfloat16, __nv_bfloat16, true>(x, dt, A, B, C, h0, hT, y, w, bias, s_in,
-                                                         s_out, K, Bz, L, H, G, status, st);
+                                                         s_out, K, Bz, L, H, G, status, seq_idx, st);
   return launch_tc<__nv_bfloat16, float, true>(x, dt, A, B, C, h0, hT, y, w, bias, s_in, s_out, K,
-                                               Bz, L, H, G, status, st);
+                                               Bz, L, H, G, status, seq_idx, st);
 }
 
 cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,

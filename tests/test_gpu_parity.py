@@ -420,3 +420,69 @@ def test_strong_and_no_decay(fused, A_scale):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(f64(S), S_ref)
     assert_rel(f64(h), h_ref, STATE_REL, "hT")
+
+
+# ---------------------------------------------------------------------------
+# packed samples (seq_idx): the scan restarts, the conv stops at boundaries
+# ---------------------------------------------------------------------------
+
+def _packed_ids(Bz, L, starts):
+    ids = np.zeros((Bz, L), np.int32)
+    for i, s in enumerate(starts):
+        ids[:, s:] = i + 1
+    ids[-1] += 3  # a different id pattern base on the last row
+    return ids
+
+
+@pytest.mark.parametrize("H,G,act,path", [(4, 1, "bf16", 2), (3, 1, "bf16", 1), (2, 1, "f32", 0)])
+def test_packed_scan_matches_oracle(H, G, act, path):
+    """Pair kernel, single-head kernel and CUDA-core scan, one path each."""
+    g = np.random.default_rng(300 + H)
+    Bz, L, P, N = 2, 300, 64, 128
+    tdt = torch.bfloat16 if act == "bf16" else torch.float32
+    assert sss.ssm_scan_path(Bz, L, H, P, N, G, tdt, tdt, tdt) == path
+    starts = [1, 2, 3, 127, 128, 129, 250]
+    x = synth.store(g.standard_normal((Bz, L, H, P)), act)
+    dt = synth.store(np.log1p(np.exp(g.standard_normal((Bz, L, H)) - 2.0)), act)
+    A = synth.f32(-g.uniform(0.01, 1.0, H))
+    B = synth.store(g.standard_normal((Bz, L, G, N)), act)
+    C = synth.store(g.standard_normal((Bz, L, G, N)), act)
+    h0 = synth.f32(g.normal(0.0, 0.1, (Bz, H, P, N)))
+    ids = _packed_ids(Bz, L, starts)
+    y, hT = sss.ssm_scan_fwd_packed(T(x), T(dt), T(A), T(B), T(C), T(h0),
+                                    torch.from_numpy(ids).to(DEV))
+    torch.cuda.synchronize()
+    y_ref, hT_ref = oracle.ssm_scan_packed(x, dt, A, B, C, h0, ids)
+    assert sss.device_status() == 0
+    if act == "f32":
+        assert_rel(f64(y), y_ref, F32_REL, "y")
+        assert_rel(f64(hT), hT_ref, F32_REL, "hT")
+    else:
+        assert_y_close(f64(y), y_ref)
+        assert_rel(f64(hT), hT_ref, STATE_REL, "hT")
+
+
+@pytest.mark.parametrize("starts", [[1, 2, 3, 127, 128, 129, 250], [130], []])
+def test_packed_mixer_matches_oracle(starts):
+    """The fused conv + scan over packed rows (two heads per CTA)."""
+    s = synth.WORKLOADS["m370m_2k"].with_(Bz=2, segments=(300,), H=4)
+    p = synth.mixer_params(s)
+    seg = synth.mixer_segment(s, 0)
+    st_h0 = synth.f32(np.random.default_rng(5).normal(0, 0.1, (s.Bz, s.H, s.P, s.N)))
+    S0 = synth.bf16(np.random.default_rng(6).standard_normal((s.Bz, s.D, s.K - 1)))
+    ids = _packed_ids(s.Bz, 300, starts)
+    y, F, hT = sss.mixer_fwd_packed(T(seg["x"]), T(seg["dt"]), T(p["A"]), T(seg["B"]),
+                                    T(seg["C"]), T(p["w"]), T(p["bias"]), T(S0), T(st_h0),
+                                    torch.from_numpy(ids).to(DEV))
+    torch.cuda.synchronize()
+    y_ref, F_ref, hT_ref = oracle.mixer_fwd_packed(seg["x"], seg["dt"], p["A"], seg["B"],
+                                                   seg["C"], p["w"], p["bias"], S0, st_h0, ids)
+    assert sss.device_status() == 0
+    assert_y_close(f64(y), y_ref)
+    np.testing.assert_array_equal(f64(F), F_ref)
+    assert_rel(f64(hT), hT_ref, STATE_REL, "hT")
+    if not starts:  # one sample per row: the same bits as the unpacked call
+        y2, F2, h2 = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), T(p["A"]), T(seg["B"]), T(seg["C"]),
+                                   T(p["w"]), T(p["bias"]), T(S0), T(st_h0))
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2) and torch.equal(hT, h2)
