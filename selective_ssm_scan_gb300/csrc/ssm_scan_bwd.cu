@@ -55,6 +55,21 @@ __device__ __forceinline__ float ldf(const T* p) {
   return to_f32<T>(*p);
 }
 
+// two fp32 FMAs in one instruction: d = a * b + c on packed pairs
+__device__ __forceinline__ uint64_t pk2f(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void upk2f(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2f(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // for i < total: put(i, get(i)), eight independent loads in flight per
 // thread before any store (a rolled loop of single loads waits one memory
 // round trip per element)
@@ -194,16 +209,29 @@ chunk_bound_kernel(const TX* __restrict__ x, const float* __restrict__ dy, const
     for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int j = 0; j < kMaxN / 16; ++j) st[r][j] *= dec;
-    for (int t = 0; t < Qc; ++t) {
-      const float w = sm.wgt[t];
-      const float4 xv = *reinterpret_cast<const float4*>(&sm.xs[t][4 * pq]);
-      const float wx[4] = {w * xv.x, w * xv.y, w * xv.z, w * xv.w};
+    {
+      // columns j and j + 1 of a row as one packed pair: two FMAs per instruction
+      uint64_t st2[4][kMaxN / 32];
 #pragma unroll
-      for (int j = 0; j < kMaxN / 16; ++j) {
-        const float bv = sm.bs[t][nq + 16 * j];
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int r = 0; r < 4; ++r) st[r][j] = fmaf(wx[r], bv, st[r][j]);
+        for (int j = 0; j < kMaxN / 32; ++j) st2[r][j] = pk2f(st[r][2 * j], st[r][2 * j + 1]);
+      for (int t = 0; t < Qc; ++t) {
+        const float w = sm.wgt[t];
+        const float4 xv = *reinterpret_cast<const float4*>(&sm.xs[t][4 * pq]);
+        const uint64_t wx[4] = {pk2f(w * xv.x, w * xv.x), pk2f(w * xv.y, w * xv.y),
+                                pk2f(w * xv.z, w * xv.z), pk2f(w * xv.w, w * xv.w)};
+#pragma unroll
+        for (int j = 0; j < kMaxN / 32; ++j) {
+          const uint64_t bv = pk2f(sm.bs[t][nq + 32 * j], sm.bs[t][nq + 32 * j + 16]);
+#pragma unroll
+          for (int r = 0; r < 4; ++r) st2[r][j] = fma2f(wx[r], bv, st2[r][j]);
+        }
       }
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < kMaxN / 32; ++j) upk2f(st2[r][j], st[r][2 * j], st[r][2 * j + 1]);
     }
     if (TRACE) {  // std of the state after this chunk: mean, then centred squares
       float s1 = 0.0f;
@@ -249,47 +277,55 @@ struct Op {
 };
 template <int TN, typename RS, typename Epi>
 __device__ __forceinline__ void smem_mm(int M, int Nn, const Op& o1, RS rs, const Op& o2, Epi epi) {
+  static_assert(TN % 2 == 0, "columns go in packed pairs");
   const int tn = (Nn + TN - 1) / TN, tm = (M + 3) / 4;
   for (int tile = threadIdx.x; tile < tm * tn; tile += kThreadsB) {
     const int i0 = 4 * (tile / tn), j0 = TN * (tile % tn);
-    float acc[4][TN];
+    // columns q, q + 1 of a row as one packed pair: two FMAs per instruction
+    uint64_t acc[4][TN / 2];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int q = 0; q < TN; ++q) acc[r][q] = 0.0f;
-    for (int k = 0; k < o1.K; ++k) {
-      float av[4], bv[TN];
+      for (int q = 0; q < TN / 2; ++q) acc[r][q] = 0ull;
+    auto run = [&](const Op& o) {
+      for (int k = 0; k < o.K; ++k) {
+        uint64_t av[4], bv[TN / 2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) av[r] = o1.a[(i0 + r) * o1.ai + k * o1.ak];
+        for (int r = 0; r < 4; ++r) {
+          const float a = o.a[(i0 + r) * o.ai + k * o.ak];
+          av[r] = pk2f(a, a);
+        }
 #pragma unroll
-      for (int q = 0; q < TN; ++q) bv[q] = o1.b[k * o1.bk + (j0 + q) * o1.bj];
+        for (int q = 0; q < TN / 2; ++q)
+          bv[q] = pk2f(o.b[k * o.bk + (j0 + 2 * q) * o.bj], o.b[k * o.bk + (j0 + 2 * q + 1) * o.bj]);
 #pragma unroll
-      for (int r = 0; r < 4; ++r)
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int q = 0; q < TN; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
-    }
+          for (int q = 0; q < TN / 2; ++q) acc[r][q] = fma2f(av[r], bv[q], acc[r][q]);
+      }
+    };
+    run(o1);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
-      const float s = rs(i0 + r);
+      const float sc = rs(i0 + r);
+      const uint64_t s2 = pk2f(sc, sc);
 #pragma unroll
-      for (int q = 0; q < TN; ++q) acc[r][q] *= s;
+      for (int q = 0; q < TN / 2; ++q) {
+        uint64_t d;
+        asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(acc[r][q]), "l"(s2));
+        acc[r][q] = d;
+      }
     }
-    for (int k = 0; k < o2.K; ++k) {
-      float av[4], bv[TN];
-#pragma unroll
-      for (int r = 0; r < 4; ++r) av[r] = o2.a[(i0 + r) * o2.ai + k * o2.ak];
-#pragma unroll
-      for (int q = 0; q < TN; ++q) bv[q] = o2.b[k * o2.bk + (j0 + q) * o2.bj];
-#pragma unroll
-      for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int q = 0; q < TN; ++q) acc[r][q] = fmaf(av[r], bv[q], acc[r][q]);
-    }
+    run(o2);
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int q = 0; q < TN; ++q)
-        if (i0 + r < M && j0 + q < Nn) epi(i0 + r, j0 + q, acc[r][q]);
+      for (int q = 0; q < TN / 2; ++q) {
+        float lo, hi;
+        upk2f(acc[r][q], lo, hi);
+        if (i0 + r < M && j0 + 2 * q < Nn) epi(i0 + r, j0 + 2 * q, lo);
+        if (i0 + r < M && j0 + 2 * q + 1 < Nn) epi(i0 + r, j0 + 2 * q + 1, hi);
+      }
   }
 }
 
