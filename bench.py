@@ -153,6 +153,23 @@ class Clocks:
                 "samples": len(rows)}
 
 
+def max_over_ranks(dist, value: float, device) -> float:
+    """The slowest rank's value (the job finishes when its last rank does);
+    the value itself on one process."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, tokens_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own tokens_per_step each
+    step (weak scaling), the job takes the slowest rank's time."""
+    return world * tokens_per_step * steps / (total_ms * 1e-3)
+
+
 def cpu_step_sample(s, nthreads: int = 0, rows: int = 0):
     """The oracle on one step of the workload (or its first ``rows`` batch
     rows): conv + scan over both segments with the states passed."""
@@ -313,13 +330,9 @@ def main():
         dist.barrier()
     step_ms = [e[0].elapsed_time(e[-1]) for e in evs_all]
     seg_ms = [e[i].elapsed_time(e[i + 1]) for e in evs_all for i in range(n_seg)]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(dist, sum(step_ms), dev)
     tokens_per_step = s.Bz * s.L
-    value = world * tokens_per_step * args.steps / (total_ms * 1e-3)
+    value = job_rate(world, tokens_per_step, args.steps, total_ms)
 
     # the two-call composition, same rules (reported beside the default path)
     evs2 = timed(step_two_calls, 2 * n_seg + 1, max(3, args.steps // 4))
@@ -429,12 +442,8 @@ def main():
         e1.record(stream)
         stream.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = sum(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_total = float(t.item())
-    e2e_value = world * tokens_per_step * e2e_steps / (e2e_total * 1e-3)
+    e2e_total = max_over_ranks(dist, sum(e2e_ms), dev)
+    e2e_value = job_rate(world, tokens_per_step, e2e_steps, e2e_total)
 
     # ---- conv backward with state on one segment, same rules ---------------
     conv_bwd = bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
