@@ -413,6 +413,55 @@ sss_status sss_mixer_fwd(const void* x, sss_dtype x_dtype, const float* w,
                          sss_stream_t stream);
 
 /*
+ * Span-parallel forward -- the same results as sss_mixer_fwd /
+ * sss_ssm_scan_fwd, for long sequences in small batches that give the
+ * chunked scan too few (batch row, head pair) work items to fill the GPU.
+ * Source: "Understanding and Improving Length Generalization in Recurrent
+ * Models", section 2.5 Eq. (4): the state at the end of a stretch of tokens
+ * is the state reached from a zero start plus the inherited state decayed by
+ * the stretch's total decay, so stretches compose associatively.  Each
+ * sequence is cut into ns equal spans of L / ns tokens that run as separate
+ * rows: a first pass from zero states gives every span's own final state, a
+ * warp-shuffle scan over the spans (fp32) gives every span its true initial
+ * state and the call its final state, and a second pass from those states
+ * writes y.  The conv state of span k > 0 is the K-1 inputs before it.
+ *
+ * sss_mixer_fwd_span_count / sss_ssm_scan_fwd_span_count: the ns the library
+ * would pick for these sizes on the current device (1 = no split pays, or
+ * the sizes are not supported by the span path).
+ * sss_fwd_spans_workspace_size: bytes of scratch for ns spans (0 for ns < 2);
+ * K = 1 for the scan alone.
+ * sss_mixer_fwd_spans / sss_ssm_scan_fwd_spans: arguments as in
+ * sss_mixer_fwd / sss_ssm_scan_fwd, plus ns (1..32; 1 = the one-pass call)
+ * and the workspace (256-byte aligned, at least
+ * sss_fwd_spans_workspace_size() bytes, not overlapping any argument).
+ * h0_in / hT_out must be 16-byte aligned here.
+ * Requires L % ns == 0, L / ns >= K - 1 (else SSS_ERR_INVALID_ARG) and the
+ * head-pair tcgen05 scan (bf16 dt/B/C, P == 64, N == 128, H / G even; else
+ * SSS_ERR_UNSUPPORTED).  h0_in / hT_out and conv_state_in / conv_state_out
+ * may be the same buffers.  Numerics: y and hT come from fp32 states as in
+ * the one-pass call; rounding differs by the order of the carry.
+ */
+int sss_mixer_fwd_span_count(int64_t Bz, int64_t L, int H, int P, int N, int G, int K,
+                             sss_dtype x_dtype, sss_dtype y_dtype);
+int sss_ssm_scan_fwd_span_count(int64_t Bz, int64_t L, int H, int P, int N, int G,
+                                sss_dtype x_dtype, sss_dtype act_dtype, sss_dtype y_dtype);
+size_t sss_fwd_spans_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int K, int ns);
+sss_status sss_mixer_fwd_spans(const void* x, sss_dtype x_dtype, const float* w,
+                               const float* bias, const void* conv_state_in,
+                               void* conv_state_out, const void* dt, const float* A,
+                               const void* B, const void* C, const float* h0_in, float* hT_out,
+                               void* y, sss_dtype y_dtype, int64_t Bz, int64_t L, int H, int P,
+                               int N, int G, int K, int ns, void* workspace,
+                               size_t workspace_bytes, sss_stream_t stream);
+sss_status sss_ssm_scan_fwd_spans(const void* x, sss_dtype x_dtype, const void* dt,
+                                  const float* A, const void* B, const void* C,
+                                  sss_dtype act_dtype, const float* h0_in, float* hT_out, void* y,
+                                  sss_dtype y_dtype, int64_t Bz, int64_t L, int H, int P, int N,
+                                  int G, int ns, void* workspace, size_t workspace_bytes,
+                                  sss_stream_t stream);
+
+/*
  * sss_mixer_update -- single/multi-token decode update over a circular
  * conv-state pool, then the same scan on the pool's SSM state.
  *

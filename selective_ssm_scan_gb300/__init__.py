@@ -102,6 +102,18 @@ _lib.sss_mixer_fwd_supported.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
 _lib.sss_mixer_fwd.restype = _i
 _lib.sss_mixer_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i64, _i64,
                                _i, _i, _i, _i, _i, _p]
+_lib.sss_mixer_fwd_span_count.restype = _i
+_lib.sss_mixer_fwd_span_count.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
+_lib.sss_ssm_scan_fwd_span_count.restype = _i
+_lib.sss_ssm_scan_fwd_span_count.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
+_lib.sss_fwd_spans_workspace_size.restype = ctypes.c_size_t
+_lib.sss_fwd_spans_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i, _i]
+_lib.sss_mixer_fwd_spans.restype = _i
+_lib.sss_mixer_fwd_spans.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i64,
+                                     _i64, _i, _i, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
+_lib.sss_ssm_scan_fwd_spans.restype = _i
+_lib.sss_ssm_scan_fwd_spans.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i64, _i64,
+                                        _i, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
 _lib.sss_tcgen05_selftest.restype = _i
 _lib.sss_tcgen05_selftest.argtypes = [_p, _p, _p, _p]
 _lib.sss_device_status.restype = _i
@@ -241,6 +253,33 @@ def ssm_scan_workspace_size(Bz, L, H, P, N, G, x_dtype, act_dtype) -> int:
                                                 _dtype_code(act_dtype)))
 
 
+def _nbytes(t: Optional[torch.Tensor]) -> int:
+    return t.numel() * t.element_size() if t is not None else 0
+
+
+def fwd_spans_workspace_size(Bz, L, H, P, N, K, spans) -> int:
+    return int(_lib.sss_fwd_spans_workspace_size(Bz, L, H, P, N, K, spans))
+
+
+def _span_workspace(Bz, L, H, P, N, K, spans, workspace, dev):
+    """The caller's workspace as given (the library checks its size and
+    alignment), else a fresh one of the size the library asks for."""
+    if workspace is None:
+        need = fwd_spans_workspace_size(Bz, L, H, P, N, K, spans)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    return workspace
+
+
+def mixer_fwd_span_count(Bz, L, H, P, N, G, K, x_dtype, y_dtype) -> int:
+    return int(_lib.sss_mixer_fwd_span_count(Bz, L, H, P, N, G, K, _dtype_code(x_dtype),
+                                             _dtype_code(y_dtype)))
+
+
+def ssm_scan_fwd_span_count(Bz, L, H, P, N, G, x_dtype, act_dtype, y_dtype) -> int:
+    return int(_lib.sss_ssm_scan_fwd_span_count(Bz, L, H, P, N, G, _dtype_code(x_dtype),
+                                                _dtype_code(act_dtype), _dtype_code(y_dtype)))
+
+
 def ssm_scan_path(Bz, L, H, P, N, G, x_dtype, act_dtype, y_dtype) -> int:
     """1 = tcgen05 chunked scan, 0 = fp32 CUDA-core scan, -1 = unsupported."""
     return int(_lib.sss_ssm_scan_path(Bz, L, H, P, N, G, _dtype_code(x_dtype),
@@ -250,10 +289,15 @@ def ssm_scan_path(Bz, L, H, P, N, G, x_dtype, act_dtype, y_dtype) -> int:
 def ssm_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                  C: torch.Tensor, h0: Optional[torch.Tensor] = None,
                  hT: Optional[torch.Tensor] = None, y: Optional[torch.Tensor] = None,
-                 y_dtype=None, workspace: Optional[torch.Tensor] = None, stream=None):
+                 y_dtype=None, workspace: Optional[torch.Tensor] = None, stream=None,
+                 spans: Optional[int] = None):
     """x [Bz, L, H, P] (or [Bz, L, D] with H taken from dt); dt [Bz, L, H];
     A [H] fp32; B, C [Bz, L, G, N]; h0/hT [Bz, H, P, N] fp32 (may be the same
-    tensor).  Returns (y, hT)."""
+    tensor).  Returns (y, hT).
+
+    spans: the number of equal spans the sequence is cut into and run in
+    parallel (sss_ssm_scan_fwd_spans); None = the library's choice for these
+    sizes on this device, 1 = one pass."""
     Bz, L, H = dt.shape
     G, N = B.shape[2], B.shape[3]
     P = x.shape[-1] if x.dim() == 4 else x.shape[-1] // H
@@ -262,6 +306,16 @@ def ssm_scan_fwd(x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor, B: torch.Te
         y = torch.empty((Bz, L, H, P), dtype=y_dtype or dt.dtype, device=dev)
     if hT is None:
         hT = torch.empty((Bz, H, P, N), dtype=torch.float32, device=dev)
+    if spans is None:
+        spans = int(_lib.sss_ssm_scan_fwd_span_count(Bz, L, H, P, N, G, _dt(x), _dt(dt), _dt(y)))
+    if spans > 1:
+        workspace = _span_workspace(Bz, L, H, P, N, 1, spans, workspace, dev)
+        rc = _lib.sss_ssm_scan_fwd_spans(_ptr(x), _dt(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                         _dt(dt), _ptr(h0), _ptr(hT), _ptr(y), _dt(y), Bz, L, H,
+                                         P, N, G, spans, _ptr(workspace), _nbytes(workspace),
+                                         _stream(stream))
+        _check("sss_ssm_scan_fwd_spans", rc)
+        return y, hT
     ws = ssm_scan_workspace_size(Bz, L, H, P, N, G, x.dtype, dt.dtype)
     if ws and (workspace is None or workspace.numel() * workspace.element_size() < ws):
         workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
@@ -441,13 +495,17 @@ def mixer_fwd_supported(Bz, L, H, P, N, G, K, x_dtype, y_dtype) -> bool:
 
 
 def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, conv_state_out=None,
-              hT=None, y=None, u_dtype=torch.float32, y_dtype=None, fused=None, stream=None):
+              hT=None, y=None, u_dtype=torch.float32, y_dtype=None, fused=None, stream=None,
+              spans=None, workspace=None):
     """One segment of the streaming forward: conv (with state) + SiLU, then the
     scan from h0.  Returns (y, conv_state_out, hT).
 
     fused=None picks the single-kernel sss_mixer_fwd when the library supports
     the shapes, else the two calls conv_state_fwd + ssm_scan_fwd (u kept in
-    u_dtype between them); fused=True / False forces one or the other."""
+    u_dtype between them); fused=True / False forces one or the other.
+    spans: for the fused call, the number of equal spans the sequence is cut
+    into and run in parallel (sss_mixer_fwd_spans); None = the library's
+    choice for these sizes on this device, 1 = one pass."""
     Bz, L, D = x.shape
     H = dt.shape[2]
     P = D // H
@@ -462,6 +520,16 @@ def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, conv_state_out=
         y = torch.empty((Bz, L, H, P), dtype=y_dtype, device=x.device)
     if fused is None:
         fused = mixer_fwd_supported(Bz, L, H, P, N, G, K, x.dtype, y.dtype)
+    if fused and spans is None:
+        spans = mixer_fwd_span_count(Bz, L, H, P, N, G, K, x.dtype, y.dtype)
+    if fused and spans > 1:
+        workspace = _span_workspace(Bz, L, H, P, N, K, spans, workspace, x.device)
+        rc = _lib.sss_mixer_fwd_spans(_ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(conv_state),
+                                      _ptr(conv_state_out), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
+                                      _ptr(h0), _ptr(hT), _ptr(y), _dt(y), Bz, L, H, P, N, G, K,
+                                      spans, _ptr(workspace), _nbytes(workspace), _stream(stream))
+        _check("sss_mixer_fwd_spans", rc)
+        return y, conv_state_out, hT
     if fused:
         rc = _lib.sss_mixer_fwd(_ptr(x), _dt(x), _ptr(w), _ptr(bias), _ptr(conv_state),
                                 _ptr(conv_state_out), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),

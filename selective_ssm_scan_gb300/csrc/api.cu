@@ -58,6 +58,15 @@ bool conv_state_bwd_supports(int K);
 size_t ssm_scan_bwd_workspace(int64_t Bz, int64_t L, int H, int P, int N);
 cudaError_t state_reset_launch(const float* u, float p, float* h, int64_t Bz, int64_t h_elems,
                                void* conv, sss_dtype conv_t, int64_t conv_elems, cudaStream_t st);
+cudaError_t span_prepare_launch(const void* x, const void* s_in, void* s_out, void* s_span,
+                                const void* dt, const float* A, float* part, int64_t Bz,
+                                int64_t L, int64_t D, int H, int K, int ns, cudaStream_t st);
+cudaError_t span_combine_launch(const float* part, const float* hloc, const float* h0,
+                                float* h0_span, float* hT, int64_t Bz, int64_t L, int H,
+                                int64_t PN, int ns, cudaStream_t st);
+size_t span_part_floats(int64_t Bz, int64_t L, int H, int ns);
+bool span_sizes_ok(int64_t Bz, int64_t L, int64_t D, int H, int P, int N, int K, int ns);
+
 cudaError_t fitted_noise_update_launch(const float* hT, int64_t Bz, int H, int64_t PN, float beta,
                                        int has_history, float* mu, float* var, cudaStream_t st);
 cudaError_t fitted_noise_sample_launch(const float* mu, const float* var, const float* eps,
@@ -486,6 +495,179 @@ sss_status sss_mixer_fwd_packed(const void* x, sss_dtype x_dtype, const float* w
   if (Bz > 0 && L > 0 && (!seq_idx || !aligned(seq_idx, 4))) return SSS_ERR_INVALID_ARG;
   return mixer_fwd_impl(x, x_dtype, w, bias, conv_state_in, conv_state_out, dt, A, B, C, h0_in,
                         hT_out, y, y_dtype, Bz, L, H, P, N, G, K, seq_idx, stream);
+}
+
+// ---- span-parallel forward --------------------------------------------------
+
+// Scratch of the span path, in order, each 256-byte aligned: partial sums of
+// the log-decay over 64-token pieces of every span [Bz*ns][ceil(Ls/64)][H],
+// the spans' zero-start final states and their initial states
+// [Bz*ns][H][P][N] fp32, and (conv only) their conv states [Bz*ns][H*P][K-1]
+// bf16.
+struct SpanWs {
+  float* part;
+  float* hloc;
+  float* h0s;
+  void* s_span;
+  size_t bytes;
+};
+
+static size_t round256(size_t v) { return (v + 255) & ~size_t(255); }
+
+static SpanWs span_ws(void* base, int64_t Bz, int64_t L, int H, int P, int N, int K, int ns) {
+  const size_t rows = size_t(Bz) * size_t(ns);
+  const size_t lam = round256(span_part_floats(Bz, L, H, ns) * sizeof(float));
+  const size_t st = round256(rows * H * P * N * sizeof(float));
+  const size_t cs = K > 1 ? round256(rows * H * P * (K - 1) * 2) : 0;
+  char* b = static_cast<char*>(base);
+  if (!b) return {nullptr, nullptr, nullptr, nullptr, lam + 2 * st + cs};
+  return {reinterpret_cast<float*>(b), reinterpret_cast<float*>(b + lam),
+          reinterpret_cast<float*>(b + lam + st), K > 1 ? b + lam + 2 * st : nullptr,
+          lam + 2 * st + cs};
+}
+
+// The split that minimises the estimated time: CTAs of the head-pair kernel
+// (one per SM) run in waves; a launch of it costs about its span length plus
+// a fixed pipeline fill and drain worth ~450 tokens (measured: 81 us for
+// 2048 tokens and 275 us for 8192 at 24 CTAs, 32 us for 512 at 96 CTAs); the
+// span path adds two passes and its two small kernels (~150 tokens).  A split
+// is taken when it is estimated to save a tenth of the one-pass time.
+static int span_count_for(int64_t Bz, int64_t L, int H, int K) {
+  constexpr int64_t kMinSpan = 256, kStartup = 450, kSmall = 150;
+  const int64_t ctas = Bz * (H / 2);
+  if (ctas < 1 || L < 2 * kMinSpan) return 1;
+  const int64_t sms = sm_count();
+  const double one = double((ctas + sms - 1) / sms) * double(L + kStartup);
+  int best = 1;
+  double best_t = 0.9 * one;
+  for (int ns = 2; ns <= 32; ++ns) {
+    if (L % ns) continue;
+    const int64_t Ls = L / ns;
+    if (Ls < kMinSpan || Ls < K - 1) continue;
+    const double t =
+        double((ctas * ns + sms - 1) / sms) * 2.0 * double(Ls + kStartup) + double(kSmall);
+    if (t < best_t) {
+      best = ns;
+      best_t = t;
+    }
+  }
+  return best;
+}
+
+static bool spans_supported(bool fused, sss_dtype x_dtype, sss_dtype act_dtype, sss_dtype y_dtype,
+                            int64_t Bz, int64_t Ls, int H, int P, int N, int G, int K,
+                            int ns) {
+  if (!span_sizes_ok(Bz, Ls * ns, int64_t(H) * P, H, P, N, K, ns)) return false;
+  if (!ssm_scan_pair_supports(act_dtype, Ls, H, P, N, G)) return false;
+  if (fused)
+    return x_dtype == SSS_BF16 && sss_mixer_fwd_supported(Bz, Ls, H, P, N, G, K, x_dtype, y_dtype);
+  return ssm_scan_tc_supports(x_dtype, act_dtype, y_dtype, Ls, H, P, N, G);
+}
+
+static sss_status fwd_spans_impl(bool fused, const void* x, sss_dtype x_dtype, const float* w,
+                                 const float* bias, const void* s_in, void* s_out, const void* dt,
+                                 const float* A, const void* B, const void* C, sss_dtype act_dtype,
+                                 const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
+                                 int64_t Bz, int64_t L, int H, int P, int N, int G, int K, int ns,
+                                 void* workspace, size_t workspace_bytes, sss_stream_t stream) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(act_dtype) || !dtype_ok(y_dtype)) return SSS_ERR_INVALID_ARG;
+  if (ns < 1 || ns > 32 || Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || K < 1)
+    return SSS_ERR_INVALID_ARG;
+  if (ns == 1 || Bz == 0 || L == 0) {
+    if (fused)
+      return mixer_fwd_impl(x, x_dtype, w, bias, s_in, s_out, dt, A, B, C, h0_in, hT_out, y,
+                            y_dtype, Bz, L, H, P, N, G, K, nullptr, stream);
+    return scan_fwd_impl(x, x_dtype, dt, A, B, C, act_dtype, h0_in, hT_out, y, y_dtype, Bz, L, H,
+                         P, N, G, nullptr, stream);
+  }
+  if (L % ns || L / ns < K - 1) return SSS_ERR_INVALID_ARG;
+  const int64_t Ls = L / ns;
+  if (!fused) K = 1;
+  if (!spans_supported(fused, x_dtype, act_dtype, y_dtype, Bz, Ls, H, P, N, G, K, ns))
+    return SSS_ERR_UNSUPPORTED;
+  if (!x || !dt || !A || !B || !C || !y || !aligned(x, 16) || !aligned(dt, 2) || !aligned(A, 4) ||
+      !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16))
+    return SSS_ERR_INVALID_ARG;
+  if ((h0_in && !aligned(h0_in, 16)) || (hT_out && !aligned(hT_out, 16)))
+    return SSS_ERR_INVALID_ARG;
+  if (fused && (!w || !aligned(w, 4) || (bias && !aligned(bias, 4)) ||
+                (s_in && !aligned(s_in, 2)) || (s_out && !aligned(s_out, 2))))
+    return SSS_ERR_INVALID_ARG;
+  const SpanWs need = span_ws(nullptr, Bz, L, H, P, N, K, ns);
+  if (!workspace || workspace_bytes < need.bytes || !aligned(workspace, 256))
+    return SSS_ERR_INVALID_ARG;
+  const SpanWs ws = span_ws(workspace, Bz, L, H, P, N, K, ns);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int64_t rows = Bz * ns;
+  int* status = status_word();
+  cudaError_t e = span_prepare_launch(x, fused ? s_in : nullptr, fused ? s_out : nullptr,
+                                      ws.s_span, dt, A, ws.part, Bz, L, int64_t(H) * P, H, K,
+                                      ns, st);
+  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
+    // pass 0: every span from a zero state, keeping its final state; pass 1:
+    // every span from its true initial state, writing y (pass 0's y is
+    // overwritten)
+    const float* h0 = pass ? ws.h0s : nullptr;
+    float* hT = pass ? nullptr : ws.hloc;
+    if (pass) {
+      e = span_combine_launch(ws.part, ws.hloc, h0_in, ws.h0s, hT_out, Bz, L, H, int64_t(P) * N,
+                              ns, st);
+      if (e != cudaSuccess) break;
+    }
+    e = fused ? mixer_fwd_pair_launch(x, w, bias, ws.s_span, nullptr, dt, A, B, C, h0, hT, y,
+                                      y_dtype, rows, Ls, H, G, K, status, nullptr, st)
+              : ssm_scan_pair_launch(x, x_dtype, dt, A, B, C, h0, hT, y, y_dtype, rows, Ls, H, G,
+                                     status, nullptr, st);
+  }
+  return from_cuda(e);
+}
+
+int sss_mixer_fwd_span_count(int64_t Bz, int64_t L, int H, int P, int N, int G, int K,
+                             sss_dtype x_dtype, sss_dtype y_dtype) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(y_dtype)) return 1;
+  if (Bz < 1 || L < 1 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || K < 1) return 1;
+  const int ns = span_count_for(Bz, L, H, K);
+  if (ns > 1 && !spans_supported(true, x_dtype, x_dtype, y_dtype, Bz, L / ns, H, P, N, G, K, ns))
+    return 1;
+  return ns;
+}
+
+int sss_ssm_scan_fwd_span_count(int64_t Bz, int64_t L, int H, int P, int N, int G,
+                                sss_dtype x_dtype, sss_dtype act_dtype, sss_dtype y_dtype) {
+  if (!dtype_ok(x_dtype) || !dtype_ok(act_dtype) || !dtype_ok(y_dtype)) return 1;
+  if (Bz < 1 || L < 1 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return 1;
+  const int ns = span_count_for(Bz, L, H, 1);
+  if (ns > 1 && !spans_supported(false, x_dtype, act_dtype, y_dtype, Bz, L / ns, H, P, N, G, 1, ns))
+    return 1;
+  return ns;
+}
+
+size_t sss_fwd_spans_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int K, int ns) {
+  if (Bz < 1 || L < 1 || H < 1 || P < 1 || N < 1 || K < 1 || ns < 2 || ns > 32) return 0;
+  return span_ws(nullptr, Bz, L, H, P, N, K, ns).bytes;
+}
+
+sss_status sss_mixer_fwd_spans(const void* x, sss_dtype x_dtype, const float* w,
+                               const float* bias, const void* conv_state_in,
+                               void* conv_state_out, const void* dt, const float* A,
+                               const void* B, const void* C, const float* h0_in, float* hT_out,
+                               void* y, sss_dtype y_dtype, int64_t Bz, int64_t L, int H, int P,
+                               int N, int G, int K, int ns, void* workspace,
+                               size_t workspace_bytes, sss_stream_t stream) {
+  return fwd_spans_impl(true, x, x_dtype, w, bias, conv_state_in, conv_state_out, dt, A, B, C,
+                        x_dtype, h0_in, hT_out, y, y_dtype, Bz, L, H, P, N, G, K, ns, workspace,
+                        workspace_bytes, stream);
+}
+
+sss_status sss_ssm_scan_fwd_spans(const void* x, sss_dtype x_dtype, const void* dt,
+                                  const float* A, const void* B, const void* C,
+                                  sss_dtype act_dtype, const float* h0_in, float* hT_out, void* y,
+                                  sss_dtype y_dtype, int64_t Bz, int64_t L, int H, int P, int N,
+                                  int G, int ns, void* workspace, size_t workspace_bytes,
+                                  sss_stream_t stream) {
+  return fwd_spans_impl(false, x, x_dtype, nullptr, nullptr, nullptr, nullptr, dt, A, B, C,
+                        act_dtype, h0_in, hT_out, y, y_dtype, Bz, L, H, P, N, G, 1, ns, workspace,
+                        workspace_bytes, stream);
 }
 
 int sss_mixer_update_path(int L_new, int P, int N, int K, int S_len, sss_dtype act_dtype) {
