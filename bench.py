@@ -228,6 +228,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the long-context streaming line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     s = synth.WORKLOADS[WORKLOAD]
@@ -451,6 +453,11 @@ def main():
     scan_bwd = bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
     train_utils = bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
 
+    # ---- long-context streaming (780M-like, batch 1), same rules ----------
+    long_ctx = None
+    if not args.no_long:
+        long_ctx = bench_long_context(torch, sss, dev, stream, flush, args, hbm)
+
     # ---- decode update (continuous batching), same rules -------------------
     decode = None
     if not args.no_decode:
@@ -476,6 +483,8 @@ def main():
     }
     if decode is not None:
         out["decode"] = decode
+    if long_ctx is not None:
+        out["long_context"] = long_ctx
     if rank == 0 and not args.no_cpu_baseline:
         # repeat whole steps until about 10 s of oracle time has run
         total_t, total_tok, reps, cores = 0.0, 0, 0, None
@@ -594,6 +603,77 @@ def bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
             "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
             "tokens_per_s": tok / (ms * 1e-3),
             "kernel": "fp32 CUDA-core chunked backward (chunks of 64)"}
+
+
+def bench_long_context(torch, sss, dev, stream, flush, args, hbm):
+    """The long-context streaming workload: batch 1, 64 consecutive
+    2048-token segments of a 780M-like layer (H 48, P 64, N 128, K 4, bf16),
+    each sss_mixer_fwd call starting from the previous call's conv and SSM
+    states (in place).  Its 24 head pairs fill a sixth of the GPU, so the
+    library splits each segment into spans (section 2.5 Eq. (4) of "Understanding
+    and Improving Length Generalization in Recurrent Models"); the same stream
+    is also timed in one pass per segment.  Inputs of all 64 segments are
+    resident (about 0.9 GB, larger than L2); L2 is flushed before each timed
+    stream."""
+    s = synth.WORKLOADS["m780m_128k"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    bf = torch.bfloat16
+    Bz, H, P, N, K, G = s.Bz, s.H, s.P, s.N, s.K, s.G
+    D, Lseg, nseg = H * P, s.segments[0], len(s.segments)
+    L = Lseg * nseg
+    x = torch.randn((nseg, Bz, Lseg, D), generator=g, device=dev).to(bf)
+    dt = torch.nn.functional.softplus(
+        torch.randn((nseg, Bz, Lseg, H), generator=g, device=dev) - 2).to(bf)
+    B = torch.randn((nseg, Bz, Lseg, G, N), generator=g, device=dev).to(bf)
+    C = torch.randn((nseg, Bz, Lseg, G, N), generator=g, device=dev).to(bf)
+    A = -torch.rand((H,), generator=g, device=dev) * 0.99 - 0.01
+    w = torch.randn((D, K), generator=g, device=dev) * 0.7
+    bias = torch.full((D,), 0.1, device=dev)
+    S = torch.zeros((Bz, D, K - 1), dtype=bf, device=dev)
+    h = torch.zeros((Bz, H, P, N), device=dev)
+    y = torch.empty((Bz, Lseg, H, P), dtype=bf, device=dev)
+    ns_auto = sss.mixer_fwd_span_count(Bz, Lseg, H, P, N, G, K, bf, bf)
+
+    def timed(ns):
+        ws = (torch.empty(sss.fwd_spans_workspace_size(Bz, Lseg, H, P, N, K, ns),
+                          dtype=torch.uint8, device=dev) if ns > 1 else None)
+
+        def stream_once():
+            for i in range(nseg):
+                sss.mixer_fwd(x[i], dt[i], A, B[i], C[i], w, bias, S, h, conv_state_out=S, hT=h,
+                              y=y, fused=True, spans=ns, workspace=ws, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, min(args.warmup, 3))):
+                stream_once()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(3):
+            flush.zero_()
+            torch.cuda._sleep(200_000)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                stream_once()
+            e1.record(stream)
+            stream.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.median(ms)
+
+    ms_span = timed(ns_auto)
+    ms_one = timed(1)
+    assert sss.device_status() == 0
+    tok = Bz * L
+    return {"workload": workload_desc(s), "spans_per_segment": ns_auto,
+            "ms_per_stream": ms_span, "tokens_per_s": tok / (ms_span * 1e-3),
+            "us_per_segment": ms_span * 1e3 / nseg,
+            "one_pass": {"ms_per_stream": ms_one, "tokens_per_s": tok / (ms_one * 1e-3),
+                         "us_per_segment": ms_one * 1e3 / nseg},
+            "path": "sss_mixer_fwd_spans: conv-state gather + decay sums, pass from zero "
+                    "states, warp-shuffle carry, pass from carried states (5 launches per "
+                    "segment)" if ns_auto > 1 else "sss_mixer_fwd (one launch per segment)"}
 
 
 def bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
