@@ -41,8 +41,12 @@ UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 
 
+MODEL_LIKE = {"m370m_2k": "370M", "m1p3b_8k": "1.3B", "m780m_128k": "780M"}
+
+
 def workload_desc(s) -> str:
-    return (f"{s.name}: Mamba-2 370M-like mixer layer, batch {s.Bz}, L={s.L} as "
+    like = MODEL_LIKE.get(s.name, "")
+    return (f"{s.name}: Mamba-2 {like}-like mixer layer, batch {s.Bz}, L={s.L} as "
             f"{len(s.segments)}x{s.segments[0]}-token segments with conv and SSM state passed, "
             f"H={s.H}, P={s.P}, N={s.N}, K={s.K}, bf16 x/dt/B/C, fp32 state")
 
