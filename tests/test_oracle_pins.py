@@ -254,6 +254,39 @@ def test_segment_equivalence(split):
     np.testing.assert_allclose(hb, hT, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("ns", [2, 3, 4, 8])
+def test_span_composition_equals_whole(ns):
+    """The reading behind the span-parallel forward (Eq. (4): the inherited
+    state enters decayed by the total decay of the tokens since): spans run
+    from ZERO states, each one's initial state rebuilt afterwards by the
+    composition (a1, s1) o (a2, s2) = (a1 a2, a2 s1 + s2) of the earlier spans'
+    (exp(sum of l_t), zero-start final state) pairs applied to h0, and each
+    span's y rebuilt by running it again from that state, equal the whole
+    sequence's y and final state."""
+    g = np.random.default_rng(40 + ns)
+    Bz, H, P, N = 2, 2, 4, 8
+    L = 6 * ns
+    Ls = L // ns
+    u = g.standard_normal((Bz, L, H, P))
+    dt = np.log1p(np.exp(g.standard_normal((Bz, L, H)) - 2.0))
+    A = -g.uniform(0.01, 1, H)
+    B = g.standard_normal((Bz, L, 1, N))
+    C = g.standard_normal((Bz, L, 1, N))
+    h0 = g.normal(0, 0.1, (Bz, H, P, N))
+    y, hT = oracle.ssm_scan(u, dt, A, B, C, h0)
+    h_in = h0.copy()
+    ys = []
+    for k in range(ns):
+        sl = slice(k * Ls, (k + 1) * Ls)
+        _, s_k = oracle.ssm_scan(u[:, sl], dt[:, sl], A, B[:, sl], C[:, sl], None)
+        a_k = np.exp((dt[:, sl] * A).sum(axis=1))           # [Bz, H]
+        y_k, _ = oracle.ssm_scan(u[:, sl], dt[:, sl], A, B[:, sl], C[:, sl], h_in)
+        ys.append(y_k)
+        h_in = a_k[:, :, None, None] * h_in + s_k
+    np.testing.assert_allclose(np.concatenate(ys, axis=1), y, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(h_in, hT, rtol=1e-12, atol=1e-12)
+
+
 def test_tiny_workload_split_equals_unsplit():
     """The tiny fp32 workload: 64 tokens as two 32-token segments == unsplit."""
     s = synth.WORKLOADS["tiny_f32"]
