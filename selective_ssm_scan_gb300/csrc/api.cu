@@ -65,6 +65,13 @@ cudaError_t span_combine_launch(const float* part, const float* hloc, const floa
                                 float* h0_span, float* hT, int64_t Bz, int64_t L, int H,
                                 int64_t PN, int ns, cudaStream_t st);
 size_t span_part_floats(int64_t Bz, int64_t L, int H, int ns);
+cudaError_t ssm_scan_pair_state_launch(const void* x, sss_dtype xt, const void* dt,
+                                       const float* A, const void* B, float* hT, int64_t Bz,
+                                       int64_t L, int H, int G, int* status, cudaStream_t st);
+cudaError_t mixer_fwd_pair_state_launch(const void* x, const float* w, const float* bias,
+                                        const void* s_in, const void* dt, const float* A,
+                                        const void* B, float* hT, int64_t Bz, int64_t L, int H,
+                                        int G, int K, int* status, cudaStream_t st);
 bool span_sizes_ok(int64_t Bz, int64_t L, int64_t D, int H, int P, int N, int K, int ns);
 
 cudaError_t fitted_noise_update_launch(const float* hT, int64_t Bz, int H, int64_t PN, float beta,
@@ -603,22 +610,23 @@ static sss_status fwd_spans_impl(bool fused, const void* x, sss_dtype x_dtype, c
   cudaError_t e = span_prepare_launch(x, fused ? s_in : nullptr, fused ? s_out : nullptr,
                                       ws.s_span, dt, A, ws.part, Bz, L, int64_t(H) * P, H, K,
                                       ns, st);
-  for (int pass = 0; pass < 2 && e == cudaSuccess; ++pass) {
-    // pass 0: every span from a zero state, keeping its final state; pass 1:
-    // every span from its true initial state, writing y (pass 0's y is
-    // overwritten)
-    const float* h0 = pass ? ws.h0s : nullptr;
-    float* hT = pass ? nullptr : ws.hloc;
-    if (pass) {
-      e = span_combine_launch(ws.part, ws.hloc, h0_in, ws.h0s, hT_out, Bz, L, H, int64_t(P) * N,
-                              ns, st);
-      if (e != cudaSuccess) break;
-    }
-    e = fused ? mixer_fwd_pair_launch(x, w, bias, ws.s_span, nullptr, dt, A, B, C, h0, hT, y,
-                                      y_dtype, rows, Ls, H, G, K, status, nullptr, st)
-              : ssm_scan_pair_launch(x, x_dtype, dt, A, B, C, h0, hT, y, y_dtype, rows, Ls, H, G,
-                                     status, nullptr, st);
-  }
+  // pass 1: every span from a zero state, only its final state kept (the
+  // state-only kernel: no y)
+  if (e == cudaSuccess)
+    e = fused ? mixer_fwd_pair_state_launch(x, w, bias, ws.s_span, dt, A, B, ws.hloc, rows, Ls, H,
+                                            G, K, status, st)
+              : ssm_scan_pair_state_launch(x, x_dtype, dt, A, B, ws.hloc, rows, Ls, H, G, status,
+                                           st);
+  // the carry over the spans, then pass 2: every span from its true initial
+  // state, writing y
+  if (e == cudaSuccess)
+    e = span_combine_launch(ws.part, ws.hloc, h0_in, ws.h0s, hT_out, Bz, L, H, int64_t(P) * N, ns,
+                            st);
+  if (e == cudaSuccess)
+    e = fused ? mixer_fwd_pair_launch(x, w, bias, ws.s_span, nullptr, dt, A, B, C, ws.h0s,
+                                      nullptr, y, y_dtype, rows, Ls, H, G, K, status, nullptr, st)
+              : ssm_scan_pair_launch(x, x_dtype, dt, A, B, C, ws.h0s, nullptr, y, y_dtype, rows,
+                                     Ls, H, G, status, nullptr, st);
   return from_cuda(e);
 }
 

@@ -210,7 +210,10 @@ __device__ __forceinline__ void split_pair(uint64_t v, uint32_t& hi, uint32_t& l
 // x: the scan input u [Bz, L, H, 64] (TX = float or bf16), or with FUSED the
 // raw input [Bz, L, H*64] (bf16) that the producers convolve (K <= 4, SiLU).
 // Requires (H / G) even: both heads of a pair read the same B and C group.
-template <typename TX, typename TY, bool FUSED, bool PACKED>
+// STATE: only the final state is wanted (the first pass of the span split):
+// no G, mask, Yo, Yd, h' tiles or y rows; per piece the producers' x' tiles,
+// the S' MMAs and the carry.
+template <typename TX, typename TY, bool FUSED, bool PACKED, bool STATE>
 __global__ void __launch_bounds__(pr::kThreads, 1)
 ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC,
                      const __grid_constant__ CUtensorMap tmX, const TX* __restrict__ x,
@@ -440,7 +443,7 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       // ---- causal mask of G: the rows of this warp's TMEM lane quarter,
       // the 32-column blocks j of its parity (two producer warps share a
       // quarter, so no warp splits more than two blocks) ------------------
-      {
+      if constexpr (!STATE) {
         bool wok = __all_sync(0xffffffffu, ok);
         if (wok) wok = __all_sync(0xffffffffu, ctl.wait(BAR_G_FULL, uint32_t(c & 1)));
         if (wok) {
@@ -547,7 +550,7 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     // the initial state h0 into the state columns, e^{R_0} h0 into the h'
     // tiles (the operand of Yo for piece 0)
     bool ok = wait_all(BAR_INFO_FULL, 0u);
-    if (ok) {
+    if (ok) {  // (the h0 loads below, then the h' tiles unless STATE)
 #pragma unroll 1
       for (int hs = 0; hs < 2; ++hs) {
 #pragma unroll
@@ -562,9 +565,11 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         }
       }
       tmem_st_wait();
-      write_h(expf(info[0].R[0]), expf(info[0].R[1]));
-      fence_proxy_async_smem();
-      mbar_arrive(ctl.bar(BAR_H_FULL));
+      if constexpr (!STATE) {
+        write_h(expf(info[0].R[0]), expf(info[0].R[1]));
+        fence_proxy_async_smem();
+        mbar_arrive(ctl.bar(BAR_H_FULL));
+      }
     }
     for (int c = 0; ok; ++c) {
       const int slot = c & (kSlots - 1);
@@ -621,6 +626,11 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(ctl.bar(BAR_S_FREE));
+      if constexpr (STATE) {
+        mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
+        if (last) break;
+        continue;
+      }
       if (!last) {  // h' tiles of the next piece, once Yo(c) has read these
         const int slot1 = (c + 1) & (kSlots - 1);
         if (!(ok = wait_all(BAR_INFO_FULL + slot1, uint32_t(((c + 1) / kSlots) & 1)))) break;
@@ -740,10 +750,12 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         tma_load_3d(bb + 16384, &tmB, g * kN + 64, start, b, bar);
       };
       prefetch_tmap(&tmB);
-      prefetch_tmap(&tmC);
-      tma_c(0);
+      if constexpr (!STATE) {
+        prefetch_tmap(&tmC);
+        tma_c(0);
+      }
       tma_b(0);
-      int c_issued = 1, c_landed = 0, b_issued = 1, b_landed = 0;
+      int c_issued = STATE ? 0 : 1, c_landed = 0, b_issued = 1, b_landed = 0;
       for (int c = 0;; ++c) {
         const int slot = c & (kSlots - 1);
         if (!ctl.wait(BAR_INFO_FULL + slot, uint32_t((c / kSlots) & 1))) break;
@@ -752,16 +764,20 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
         // G = C B^T once this piece's B and C are in and Yd(c-1) has read the
         // masked split that G overwrites
-        if (!ctl.wait(BAR_C_FULL, uint32_t(c & 1))) break;
-        c_landed = c + 1;
+        if constexpr (!STATE) {
+          if (!ctl.wait(BAR_C_FULL, uint32_t(c & 1))) break;
+          c_landed = c + 1;
+        }
         if (!ctl.wait(BAR_B_FULL, uint32_t(c & 1))) break;
         b_landed = c + 1;
-        if (c >= 1 && !ctl.wait(BAR_YD_DONE, uint32_t((c - 1) & 1))) break;
-        tc_fence_after();
+        if constexpr (!STATE) {
+          if (c >= 1 && !ctl.wait(BAR_YD_DONE, uint32_t((c - 1) & 1))) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_ss(tG, dC + kstep(kk, 16384), dBk + kstep(kk, 16384), kIdG, kk);
-        mma_commit(ctl.bar(BAR_G_FULL));
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tG, dC + kstep(kk, 16384), dBk + kstep(kk, 16384), kIdG, kk);
+          mma_commit(ctl.bar(BAR_G_FULL));
+        }
         // S' = B^T [x'_a | x'_b] (hi + lo), once the x' tiles are in and the
         // previous carry has read S'
         if (!ctl.wait(BAR_X_FULL, uint32_t(c & 1))) break;
@@ -773,6 +789,14 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         for (int kk = 0; kk < 8; ++kk) mma_ss(tS, dBm + mnstep(kk), dXl + mnstep(kk), kIdS, 1);
         mma_commit(ctl.bar(BAR_S_FULL));
         mma_commit(ctl.bar(BAR_B_FREE));
+        if constexpr (STATE) {  // the x' tiles are free once S' has read them
+          mma_commit(ctl.bar(BAR_X_FREE));
+          if (last) break;
+          if (!ctl.wait(BAR_B_FREE, uint32_t(c & 1))) break;
+          tma_b(start + n);
+          b_issued = c + 2;
+          continue;
+        }
         // Y_ab = C [e^R h_a | e^R h_b]^T (hi + lo) starts Y, once the h' tiles
         // are written and the previous piece's y rows are read
         if (!ctl.wait(BAR_H_FULL, uint32_t(c & 1))) break;
@@ -985,8 +1009,8 @@ cudaError_t launch_pair(const void* x, const void* dt, const float* A, const voi
   }
   // packed rows get their own instantiation: the ordinary one carries none of
   // their checks
-  auto kern = seq_idx ? ssm_scan_pair_kernel<TX, TY, FUSED, true>
-                      : ssm_scan_pair_kernel<TX, TY, FUSED, false>;
+  auto kern = seq_idx ? ssm_scan_pair_kernel<TX, TY, FUSED, true, false>
+                      : ssm_scan_pair_kernel<TX, TY, FUSED, false, false>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
   if (e != cudaSuccess) return e;
@@ -1003,6 +1027,51 @@ cudaError_t launch_pair(const void* x, const void* dt, const float* A, const voi
 bool ssm_scan_pair_supports(sss_dtype at, int64_t L, int H, int P, int N, int G) {
   return at == SSS_BF16 && P == pr::kP && N == pr::kN && L >= 1 && L < (int64_t(1) << 31) &&
          H >= 2 && G >= 1 && H % G == 0 && (H / G) % 2 == 0 && encode_fn() != nullptr;
+}
+
+// The state-only kernel (first pass of the span split): zero initial state,
+// hT written, no y.  C is not read, so its tensor map is not encoded.
+template <typename TX, bool FUSED>
+cudaError_t launch_pair_state(const void* x, const void* dt, const float* A, const void* B,
+                              float* hT, const float* w, const float* bias, const void* s_in,
+                              int K, int64_t Bz, int64_t L, int H, int G, int* status,
+                              cudaStream_t st) {
+  using namespace pr;
+  if (Bz * (H / 2) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  CUtensorMap mB, mX;
+  if (!make_bc_map(&mB, B, Bz, L, G, kN)) return cudaErrorInvalidValue;
+  if (FUSED) {
+    if (!make_x_map(&mX, x, Bz, L, int64_t(H) * kP, kXsRows)) return cudaErrorInvalidValue;
+  } else {
+    mX = mB;  // unused
+  }
+  auto kern = ssm_scan_pair_kernel<TX, __nv_bfloat16, FUSED, false, true>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+  if (e != cudaSuccess) return e;
+  kern<<<unsigned(Bz * (H / 2)), kThreads, kSmemBytes, st>>>(
+      mB, mB, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, nullptr,
+      hT, nullptr, w, bias, static_cast<const TX*>(s_in), nullptr, K, int(L), H, G, status,
+      nullptr);
+  return cudaGetLastError();
+}
+
+cudaError_t ssm_scan_pair_state_launch(const void* x, sss_dtype xt, const void* dt,
+                                       const float* A, const void* B, float* hT, int64_t Bz,
+                                       int64_t L, int H, int G, int* status, cudaStream_t st) {
+  if (xt == SSS_F32)
+    return launch_pair_state<float, false>(x, dt, A, B, hT, nullptr, nullptr, nullptr, 1, Bz, L,
+                                           H, G, status, st);
+  return launch_pair_state<__nv_bfloat16, false>(x, dt, A, B, hT, nullptr, nullptr, nullptr, 1,
+                                                 Bz, L, H, G, status, st);
+}
+
+cudaError_t mixer_fwd_pair_state_launch(const void* x, const float* w, const float* bias,
+                                        const void* s_in, const void* dt, const float* A,
+                                        const void* B, float* hT, int64_t Bz, int64_t L, int H,
+                                        int G, int K, int* status, cudaStream_t st) {
+  return launch_pair_state<__nv_bfloat16, true>(x, dt, A, B, hT, w, bias, s_in, K, Bz, L, H, G,
+                                                status, st);
 }
 
 cudaError_t ssm_scan_pair_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
