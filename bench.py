@@ -675,9 +675,9 @@ def bench_long_context(torch, sss, dev, stream, flush, args, hbm):
             "us_per_segment": ms_span * 1e3 / nseg,
             "one_pass": {"ms_per_stream": ms_one, "tokens_per_s": tok / (ms_one * 1e-3),
                          "us_per_segment": ms_one * 1e3 / nseg},
-            "path": "sss_mixer_fwd_spans: conv-state gather + decay sums, pass from zero "
-                    "states, warp-shuffle carry, pass from carried states (5 launches per "
-                    "segment)" if ns_auto > 1 else "sss_mixer_fwd (one launch per segment)"}
+            "path": "sss_mixer_fwd_spans: conv-state gather + decay sums, state-only pass "
+                    "from zero states, warp-shuffle carry, pass from carried states (4 launches "
+                    "per segment)" if ns_auto > 1 else "sss_mixer_fwd (one launch per segment)"}
 
 
 def bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
