@@ -154,3 +154,42 @@ def test_scan_backward_host_checks(lib):
     assert call(args(dB=None)) == 1                  # no dB buffer
     assert call(args(dh0=ctypes.c_void_p(0x80000000 + 64))) == 1  # dh0 half over dhT
     assert call(args(dy=ctypes.c_void_p(0x70000002))) == 1        # misaligned dy
+
+
+def test_span_forward_host_checks(lib):
+    """Workspace size and the argument checks of the span-parallel forward that
+    return before any launch or device query."""
+    i64, ci = ctypes.c_int64, ctypes.c_int
+    ws = lib.sss_fwd_spans_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i64, i64, ci, ci, ci, ci, ci]
+    al = lambda v: (v + 255) // 256 * 256
+    # partial decay sums per 64-token piece of each span, the spans'
+    # zero-start final states and initial states (fp32), their conv states
+    # (bf16, K - 1 per channel)
+    Bz, L, H, P, N, K, ns = 2, 1024, 48, 64, 128, 4, 4
+    Ls = L // ns
+    expect = (al(4 * Bz * ns * (Ls // 64) * H) + 2 * al(4 * Bz * ns * H * P * N)
+              + al(2 * Bz * ns * H * P * (K - 1)))
+    assert ws(Bz, L, H, P, N, K, ns) == expect
+    assert ws(Bz, L, H, P, N, 1, ns) == expect - al(2 * Bz * ns * H * P * (K - 1))  # scan alone
+    assert ws(Bz, 1000, H, P, N, K, 5) == (al(4 * Bz * 5 * 4 * H) + 2 * al(4 * Bz * 5 * H * P * N)
+                                           + al(2 * Bz * 5 * H * P * (K - 1)))  # 200-token spans: 4 pieces
+    assert ws(Bz, L, H, P, N, K, 1) == 0 and ws(Bz, L, H, P, N, K, 33) == 0
+    f = lib.sss_mixer_fwd_spans
+    f.restype = ci
+    Pp = ctypes.c_void_p
+    f.argtypes = [Pp, ci, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, ci, i64, i64, ci, ci, ci,
+                  ci, ci, ci, Pp, ctypes.c_size_t, Pp]
+    a = lambda k: ctypes.c_void_p(0x10000000 * k)  # aligned stand-ins, never dereferenced
+    args = lambda **kw: dict(dict(x=a(1), xt=1, w=a(2), bias=a(3), s_in=a(4), s_out=a(4), dt=a(5),
+                                  A=a(6), B=a(7), C=a(8), h0=a(9), hT=a(9), y=a(10), yt=1, Bz=Bz,
+                                  L=L, H=H, P=P, N=N, G=1, K=K, ns=ns, ws=a(11), wsb=expect,
+                                  st=None), **kw)
+    call = lambda d: f(*d.values())
+    assert call(args(ns=0)) == 1                     # no spans
+    assert call(args(ns=33)) == 1                    # more spans than warp lanes
+    assert call(args(L=1023)) == 1                   # L not a multiple of ns
+    assert call(args(L=8, ns=4)) == 1                # 2-token spans < K - 1
+    assert call(args(xt=7)) == 1                     # unknown dtype
+    assert call(args(G=5)) == 1                      # H not a multiple of G
