@@ -1,15 +1,19 @@
 #!/usr/bin/env python3
-"""Benchmark: state-passing conv + scan forward of a Mamba-2 370M-like mixer
-layer on GB300, tokens/s, with the roofline of the dominant kernel.
+"""Benchmark: state-passing conv + scan forward of Mamba-2-like mixer layers on
+GB300, tokens/s, with the roofline of the dominant kernel.
 
-A step is one pass of the hot path over one batch: batch 8, L = 2048 tokens
-run as two 1024-token segments, each segment = conv with state (+SiLU) then
-the scan from the previous segment's final SSM state (H=32, P=64, N=128, K=4,
-bf16 activations, fp32 state).  Inputs are resident in HBM when the timed
-region starts; L2 is flushed (a 256 MiB write) before every timed step,
-outside the events.  The same line also reports the decode update of a
-continuous-batching call (256 of 512 pool rows, L_new = 1) measured the same
-way.
+A step (the headline) is one forward of the 1.3B-like layer with a random
+Gaussian initial state: batch 4, L = 8192, d_inner 4096 (H = 64, P = 64),
+N = 128, K = 4, bf16 x / dt / B / C, fp32 h0 ~ N(0, 0.1^2) and a conv state
+~ N(0, 1); outputs y and the final conv and SSM states.  It is one
+sss_mixer_fwd call (conv + SiLU + chunked scan in one tcgen05 kernel).  Inputs
+are resident in HBM when the timed region starts; L2 is flushed (a 256 MiB
+write) before every timed step, outside the events.  The same JSON line
+carries every other workload as an extra key, each with its own roofline: the
+370M-like layer as two 1024-token segments with state passing (and the same
+forward as two calls), the 780M-like layer streamed over 64 x 2048-token
+segments, the continuous-batching decode update at L_new = 1 and 4, the tiny
+fp32 check, and the backward and state-utility kernels.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,7 +39,7 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
-WORKLOAD = "m370m_2k"
+WORKLOAD = "m1p3b_8k"
 METRIC = "tokens/s per GB300 (conv+scan fwd w/ state passing) and % of HBM/tensor roofline"
 UNIT = "tokens/s"
 FALLBACK_HBM_GBS = 6800.0
@@ -45,10 +49,16 @@ MODEL_LIKE = {"m370m_2k": "370M", "m1p3b_8k": "1.3B", "m780m_128k": "780M"}
 
 
 def workload_desc(s) -> str:
+    if s.name == "tiny_f32":
+        return (f"{s.name}: batch {s.Bz}, L={s.L} as {len(s.segments)}x{s.segments[0]}-token "
+                f"segments with state passed, H={s.H}, P={s.P}, N={s.N}, K={s.K}, fp32")
     like = MODEL_LIKE.get(s.name, "")
-    return (f"{s.name}: Mamba-2 {like}-like mixer layer, batch {s.Bz}, L={s.L} as "
-            f"{len(s.segments)}x{s.segments[0]}-token segments with conv and SSM state passed, "
-            f"H={s.H}, P={s.P}, N={s.N}, K={s.K}, bf16 x/dt/B/C, fp32 state")
+    init = ("Gaussian initial states (h0 ~ N(0,0.1^2), conv state ~ N(0,1))" if s.gaussian_init
+            else "zero initial states")
+    segs = (f"one {s.L}-token call" if len(s.segments) == 1 else
+            f"{len(s.segments)}x{s.segments[0]}-token segments with conv and SSM state passed")
+    return (f"{s.name}: Mamba-2 {like}-like mixer layer, batch {s.Bz}, L={s.L} as {segs}, "
+            f"H={s.H}, P={s.P}, N={s.N}, K={s.K}, bf16 x/dt/B/C, fp32 state, {init}")
 
 
 def peaks():
@@ -176,7 +186,8 @@ def job_rate(world: int, tokens_per_step: int, steps: int, total_ms: float) -> f
 
 def cpu_step_sample(s, nthreads: int = 0, rows: int = 0):
     """The oracle on one step of the workload (or its first ``rows`` batch
-    rows): conv + scan over both segments with the states passed."""
+    rows, all tokens and heads): conv + scan over every segment with the
+    states passed."""
     import oracle
     p = synth.mixer_params(s)
     st = synth.mixer_initial_states(s)
@@ -193,6 +204,10 @@ def cpu_step_sample(s, nthreads: int = 0, rows: int = 0):
     return tokens / dt, dt, tokens, oracle.num_threads(nthreads)
 
 
+# the oracle's sample of a step: one batch row, all its tokens and heads
+CPU_SAMPLE_ROWS = 1
+
+
 def run_reference(args, s):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -200,17 +215,17 @@ def run_reference(args, s):
     import oracle
     oracle.build()
     for _ in range(args.warmup):
-        cpu_step_sample(s)
+        cpu_step_sample(s, rows=CPU_SAMPLE_ROWS)
     times = []
     tokens = 0
     cores = None
     for _ in range(args.steps):
-        _, dt, tokens, cores = cpu_step_sample(s)
+        _, dt, tokens, cores = cpu_step_sample(s, rows=CPU_SAMPLE_ROWS)
         times.append(dt)
     total = sum(times)
     value = tokens * len(times) / total
-    sample = (f"one full step of {s.name} per step ({tokens} tokens: batch {s.Bz}, "
-              f"{len(s.segments)} segments of {s.segments[0]}, all {s.H} heads)")
+    sample = (f"per step, batch row 0 of {s.name} ({tokens} tokens: {len(s.segments)} "
+              f"segment(s) of {s.segments[0]}, all {s.H} heads, states passed)")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -224,16 +239,58 @@ def run_reference(args, s):
     }), flush=True)
 
 
+def algorithmic_bytes(s, Lseg: int, x_bytes: int = 2, y_bytes: int = 2) -> int:
+    """The method's own HBM traffic for one call over an Lseg-token segment of
+    workload s, conv + scan fused (x read once, u never written): x in, y
+    out, dt, B and C in, h0 in and hT out, the conv state in and out."""
+    a_bytes = 2 if s.dtype == "bf16" else 4
+    return (s.Bz * Lseg * s.D * (x_bytes + y_bytes)
+            + s.Bz * Lseg * (s.H + 2 * s.G * s.N) * a_bytes
+            + 2 * s.Bz * s.H * s.P * s.N * 4
+            + 2 * s.Bz * s.D * (s.K - 1) * a_bytes)
+
+
+def events_timed(torch, stream, flush, fn, steps, sleep_ns=200_000):
+    """Per-call device time (ms) of fn() on `stream`, CUDA events on that
+    stream, L2 flushed before every call outside the events; the GPU is kept
+    busy while the host enqueues the call, so no launch waits for the host."""
+    evs = []
+    for _ in range(steps):
+        flush.zero_()
+        torch.cuda._sleep(sleep_ns)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        evs.append((e0, e1))
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def roofline_block(byts, ms, hbm, hbm_kind, kernel, workload, traffic_key=None):
+    achieved = byts / (ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm,
+            "traffic": traffic_from_profile(*traffic_key) if traffic_key else None,
+            "kernel": kernel, "workload": workload,
+            "algorithmic_bytes_per_launch": byts, "avg_launch_ms": ms,
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured"
+            else "fallback 6.8 TB/s"}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-long", action="store_true",
                     help="skip the long-context streaming line")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="only the headline (no other workloads, backward or utilities)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     s = synth.WORKLOADS[WORKLOAD]
@@ -258,254 +315,312 @@ def main():
             return torch.from_numpy(a.data.view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(a.data).to(dev)
 
-    p = synth.mixer_params(s)
-    st = synth.mixer_initial_states(s)
-    segs = [synth.mixer_segment(s, i) for i in range(len(s.segments))]
-    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
-    S0, h00 = T(st["conv_state"]), T(st["h0"])
-    dseg = [{k: T(v) for k, v in sg.items()} for sg in segs]
-    S = torch.empty_like(S0)
-    h = torch.empty_like(h00)
-    us = [torch.empty((s.Bz, L, s.D), dtype=torch.float32, device=dev) for L in s.segments]
-    ys = [torch.empty((s.Bz, L, s.H, s.P), dtype=torch.bfloat16, device=dev)
-          for L in s.segments]
+    hbm, hbm_kind = peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-    n_seg = len(dseg)
-    fused_ok = sss.mixer_fwd_supported(s.Bz, s.segments[0], s.H, s.P, s.N, s.G, s.K,
-                                       torch.bfloat16, torch.bfloat16)
-    if not fused_ok:
+
+    # ---- the headline: one forward of the 1.3B-like layer ------------------
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    sg = {k: T(v) for k, v in synth.mixer_segment(s, 0).items()}
+    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
+    S0, h0 = T(st["conv_state"]), T(st["h0"])
+    L = s.segments[0]
+    y = torch.empty((s.Bz, L, s.H, s.P), dtype=torch.bfloat16, device=dev)
+    F = torch.empty_like(S0)
+    hT = torch.empty_like(h0)
+    if not sss.mixer_fwd_supported(s.Bz, L, s.H, s.P, s.N, s.G, s.K, torch.bfloat16,
+                                   torch.bfloat16):
         raise SystemExit("the fused forward does not support this workload")
+    spans = sss.mixer_fwd_span_count(s.Bz, L, s.H, s.P, s.N, s.G, s.K, torch.bfloat16,
+                                     torch.bfloat16)
 
-    def reset():
-        S.copy_(S0)
-        h.copy_(h00)
+    def step():
+        sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S0, h0,
+                      conv_state_out=F, hT=hT, y=y, fused=True, stream=stream)
 
-    def step(evs=None):
-        """The default path: one kernel per segment (conv + SiLU + scan)."""
-        for i, sg in enumerate(dseg):
-            if evs is not None:
-                evs[i].record(stream)
-            sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
-                          conv_state_out=S, hT=h, y=ys[i], fused=True)
-        if evs is not None:
-            evs[n_seg].record(stream)
-
-    def step_two_calls(evs=None):
-        """The same forward as two calls per segment, u kept in fp32 in HBM."""
-        for i, sg in enumerate(dseg):
-            if evs is not None:
-                evs[2 * i].record(stream)
-            sss.conv_state_fwd(sg["x"], w, bias, S, S, u=us[i])
-            if evs is not None:
-                evs[2 * i + 1].record(stream)
-            sss.ssm_scan_fwd(us[i], sg["dt"], A, sg["B"], sg["C"], h, h, y=ys[i])
-        if evs is not None:
-            evs[2 * n_seg].record(stream)
-
-    def timed(fn, n_events, steps):
-        all_evs = []
-        for _ in range(steps):
-            reset()
-            flush.zero_()
-            # keep the GPU busy ~100 us while the host enqueues the whole step,
-            # so that no launch in the timed region waits for the host
-            torch.cuda._sleep(200_000)
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_events)]
-            fn(evs)
-            all_evs.append(evs)
-        stream.synchronize()
-        return all_evs
-
-    launches_per_step = n_seg
     for _ in range(args.warmup):
-        reset()
         step()
-        reset()
-        step_two_calls()
     torch.cuda.synchronize()
-
-    # ---- timed: device-resident inputs -----------------------------------
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     with Clocks(local) as clk:
-        evs_all = timed(step, n_seg + 1, args.steps)
+        step_ms = events_timed(torch, stream, flush, step, args.steps)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    step_ms = [e[0].elapsed_time(e[-1]) for e in evs_all]
-    seg_ms = [e[i].elapsed_time(e[i + 1]) for e in evs_all for i in range(n_seg)]
+    assert sss.device_status() == 0, "device status after the headline steps"
     total_ms = max_over_ranks(dist, sum(step_ms), dev)
-    tokens_per_step = s.Bz * s.L
+    tokens_per_step = s.Bz * L
     value = job_rate(world, tokens_per_step, args.steps, total_ms)
-
-    # the two-call composition, same rules (reported beside the default path)
-    evs2 = timed(step_two_calls, 2 * n_seg + 1, max(3, args.steps // 4))
-    conv_ms = [e[2 * i].elapsed_time(e[2 * i + 1]) for e in evs2 for i in range(n_seg)]
-    scan_ms = [e[2 * i + 1].elapsed_time(e[2 * i + 2]) for e in evs2 for i in range(n_seg)]
-    two_call_step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in evs2)
-
-    # ---- roofline of the dominant kernel -----------------------------------
-    hbm, hbm_kind = peaks()
-    Lseg = s.segments[0]
-    state_bytes = 2 * s.Bz * s.H * s.P * s.N * 4                 # h0 read + hT write
-    cstate_bytes = 2 * s.Bz * s.D * (s.K - 1) * 2                # conv state read + write
-    io_bytes = (s.Bz * Lseg * s.H * 2 + 2 * s.Bz * Lseg * s.G * s.N * 2   # dt, B, C
-                + s.Bz * Lseg * s.D * 2)                          # y (bf16) write
-    fused_bytes = s.Bz * Lseg * s.D * 2 + io_bytes + state_bytes + cstate_bytes
-    scan_bytes = s.Bz * Lseg * s.D * 4 + io_bytes + state_bytes   # u (fp32) read
-    conv_bytes = s.Bz * Lseg * s.D * (2 + 4) + cstate_bytes
-    fused_avg = statistics.mean(seg_ms)
-    scan_avg = statistics.mean(scan_ms)
-    conv_avg = statistics.mean(conv_ms)
-    achieved = fused_bytes / (fused_avg * 1e-3) / 1e9
-    # useful (unsplit) contraction flops of the chunked form, for the tensor pipe
+    launch_ms = statistics.mean(step_ms)
+    fused_bytes = algorithmic_bytes(s, L)
+    roofline = roofline_block(
+        fused_bytes, launch_ms, hbm, hbm_kind,
+        "ssm_scan_pair_kernel<bf16,bf16,fused> (conv+SiLU+chunked scan, two heads per CTA, "
+        "one launch per call)", s.name, ("ssm_scan_pair", s.name))
+    roofline["traffic_note"] = ("DRAM read + write bytes per launch from the committed ncu "
+                                "summary when its source hash matches the current kernel")
     Q = 128
-    chunks = -(-Lseg // Q)
-    tc_flops = s.Bz * s.H * chunks * 2 * Q * (Q * s.N + Q * s.P + 2 * s.P * s.N)
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm,
-                "traffic": traffic_from_profile("ssm_scan_pair", WORKLOAD),
-                "kernel": "ssm_scan_pair_kernel<bf16,bf16,fused> (conv+SiLU+scan, two heads "
-                          "per CTA, one launch per segment)",
-                "algorithmic_bytes_per_launch": fused_bytes, "avg_launch_ms": fused_avg,
-                "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs)" if hbm_kind == "measured"
-                else "fallback 6.8 TB/s",
-                "tensor_useful_tflops": tc_flops / (fused_avg * 1e-3) / 1e12,
-                "two_call_path": {
-                    "ms_per_step": two_call_step_ms,
-                    "conv_state_fwd": {"avg_launch_ms": conv_avg,
-                                       "algorithmic_bytes_per_launch": conv_bytes,
-                                       "achieved_gbs": conv_bytes / conv_avg / 1e6,
-                                       "frac": conv_bytes / conv_avg / 1e6 / hbm},
-                    "ssm_scan_fwd": {"avg_launch_ms": scan_avg,
-                                     "algorithmic_bytes_per_launch": scan_bytes,
-                                     "achieved_gbs": scan_bytes / scan_avg / 1e6,
-                                     "frac": scan_bytes / scan_avg / 1e6 / hbm}}}
-    path = sss.ssm_scan_path(s.Bz, Lseg, s.H, s.P, s.N, s.G, torch.float32, torch.bfloat16,
-                             torch.bfloat16)
+    tc_flops = s.Bz * s.H * (-(-L // Q)) * 2 * Q * (Q * s.N + Q * s.P + 2 * s.P * s.N)
+    roofline["tensor_useful_tflops"] = tc_flops / (launch_ms * 1e-3) / 1e12
 
     # ---- end to end through the API with host buffers ----------------------
-    host = {}
-    for i, sg in enumerate(dseg):
-        for k, v in sg.items():
-            host[(i, k)] = torch.empty(v.shape, dtype=v.dtype, pin_memory=True).copy_(v)
-    hS0 = torch.empty(S0.shape, dtype=S0.dtype, pin_memory=True).copy_(S0)
-    hh0 = torch.empty(h00.shape, dtype=h00.dtype, pin_memory=True).copy_(h00)
-    hy = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for y in ys]
-    hS = torch.empty(S0.shape, dtype=S0.dtype, pin_memory=True)
-    hh = torch.empty(h00.shape, dtype=h00.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + \
-        hS0.numel() * hS0.element_size() + hh0.numel() * hh0.element_size()
-    d2h = sum(t.numel() * t.element_size() for t in hy) + hS.numel() * hS.element_size() + \
-        hh.numel() * hh.element_size()
-
-    # Copies in on one stream and out on another, compute on the main stream:
-    # segment i+1's inputs go up while segment i computes, and y(i) comes down
-    # while segment i+1 computes.  Events order each step's work after e0 and
-    # before e1, both recorded on the main stream.
-    s_in = torch.cuda.Stream(device=dev)
-    s_out = torch.cuda.Stream(device=dev)
-
-    def e2e_step(e0=None):
-        landed = [torch.cuda.Event() for _ in dseg]
-        done = [torch.cuda.Event() for _ in dseg]
-        if e0 is not None:
-            s_in.wait_event(e0)
-        with torch.cuda.stream(s_in):
-            S.copy_(hS0, non_blocking=True)
-            h.copy_(hh0, non_blocking=True)
-            for i in range(n_seg):
-                for k in dseg[i]:
-                    dseg[i][k].copy_(host[(i, k)], non_blocking=True)
-                landed[i].record(s_in)
-        for i, sg in enumerate(dseg):
-            stream.wait_event(landed[i])
-            sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
-                          conv_state_out=S, hT=h, y=ys[i], fused=True, stream=stream)
-            done[i].record(stream)
-            s_out.wait_event(done[i])
-            with torch.cuda.stream(s_out):
-                hy[i].copy_(ys[i], non_blocking=True)
-        with torch.cuda.stream(s_out):
-            hS.copy_(S, non_blocking=True)
-            hh.copy_(h, non_blocking=True)
-        stream.wait_stream(s_out)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = []
-    e2e_steps = max(3, args.steps // 10)
-    for _ in range(e2e_steps):
-        flush.zero_()
-        torch.cuda._sleep(200_000)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        e2e_step(e0)
-        e1.record(stream)
-        stream.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = max_over_ranks(dist, sum(e2e_ms), dev)
-    e2e_value = job_rate(world, tokens_per_step, e2e_steps, e2e_total)
-
-    # ---- conv backward with state on one segment, same rules ---------------
-    conv_bwd = bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
-    # ---- scan backward with state on one segment, same rules ---------------
-    scan_bwd = bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
-    train_utils = bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg)
-
-    # ---- long-context streaming (780M-like, batch 1), same rules ----------
-    long_ctx = None
-    if not args.no_long:
-        long_ctx = bench_long_context(torch, sss, dev, stream, flush, args, hbm)
-
-    # ---- decode update (continuous batching), same rules -------------------
-    decode = None
-    if not args.no_decode:
-        decode = bench_decode(torch, sss, dev, stream, flush, args, hbm)
+    e2e = bench_e2e(torch, sss, dev, flush, args, s, p, st, dist, world)
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(s), "tokens_per_step": tokens_per_step,
-                   "path": "sss_mixer_fwd: one tcgen05 kernel per segment (conv+SiLU+scan), "
-                           "two heads per CTA",
-                   "scan_path_two_call": {2: "tcgen05, two heads per CTA", 1: "tcgen05",
-                                          0: "cuda-core fp32"}.get(path, "unsupported"),
-                   "l2": "flushed before every timed step (256 MiB write, outside the events)",
+                   "path": f"sss_mixer_fwd: one tcgen05 kernel per call (conv+SiLU+scan), two "
+                           f"heads per CTA, spans per call {spans}",
+                   "l2": "flushed before every timed step (256 MiB write, outside the events); "
+                         "inputs 0.3 GB, larger than L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roofline,
-        "conv_bwd": conv_bwd, "scan_bwd": scan_bwd, "train_utils": train_utils,
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "e2e": e2e,
+        "gpu_launches": args.steps * (1 if spans <= 1 else 4),
         "clocks": clk.summary(),
     }
-    if decode is not None:
-        out["decode"] = decode
-    if long_ctx is not None:
-        out["long_context"] = long_ctx
+    if not args.no_extra:
+        seg2 = bench_segments(torch, sss, dev, stream, flush, args, hbm, hbm_kind, T)
+        out["m370m_2k"] = seg2
+        s2 = synth.WORKLOADS["m370m_2k"]
+        out["conv_bwd"] = bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s2,
+                                         s2.segments[0])
+        out["scan_bwd"] = bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s2,
+                                         s2.segments[0])
+        out["train_utils"] = bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s2,
+                                               s2.segments[0])
+        out["tiny_f32"] = bench_tiny(torch, sss, dev, stream, flush, args, hbm, hbm_kind, T)
+        if not args.no_long:
+            out["long_context"] = bench_long_context(torch, sss, dev, stream, flush, args, hbm,
+                                                     hbm_kind)
+        if not args.no_decode:
+            out["decode_256x1"] = bench_decode(torch, sss, dev, stream, flush, args, hbm,
+                                               "decode_256x1")
+            out["decode_256x4"] = bench_decode(torch, sss, dev, stream, flush, args, hbm,
+                                               "decode_256x4")
     if rank == 0 and not args.no_cpu_baseline:
-        # repeat whole steps until about 10 s of oracle time has run
+        # whole rows of the step repeated until about 10 s of oracle time has run
         total_t, total_tok, reps, cores = 0.0, 0, 0, None
         while total_t < 10.0 and reps < 200:
-            _, dt, tokens, cores = cpu_step_sample(s)
-            total_t += dt
+            _, dt_, tokens, cores = cpu_step_sample(s, rows=CPU_SAMPLE_ROWS)
+            total_t += dt_
             total_tok += tokens
             reps += 1
         out["cpu_baseline"] = {"value": total_tok / total_t, "unit": UNIT, "cores": cores,
                                "kind": "oracle",
-                               "sample": f"{reps} repetitions of one full step ({tokens} tokens "
-                                         f"each: batch {s.Bz}, {len(s.segments)} segments of "
-                                         f"{s.segments[0]}), {total_t:.1f} s wall"}
+                               "sample": f"{reps} repetitions of batch row 0 of {s.name} "
+                                         f"({tokens} tokens each, all {s.H} heads, Gaussian "
+                                         f"initial states), {total_t:.1f} s wall"}
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def bench_e2e(torch, sss, dev, flush, args, s, p, st, dist, world):
+    """The headline step end to end through the public API: every step copies
+    its inputs from pinned host memory to the device and y plus the final
+    states back.  The batch rows run as separate calls on four streams, so one
+    row's copies overlap another row's kernel."""
+    L = s.segments[0]
+    seg = synth.mixer_segment(s, 0)
+    bf = torch.bfloat16
+
+    def pinned(a):
+        if a.dtype == "bf16":
+            t = torch.from_numpy(a.data.view(np.int16)).view(bf)
+        else:
+            t = torch.from_numpy(a.data)
+        return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
+
+    host = {k: pinned(v) for k, v in seg.items()}
+    hS0, hh0 = pinned(st["conv_state"]), pinned(st["h0"])
+    A = torch.from_numpy(p["A"].data).to(dev)
+    w = torch.from_numpy(p["w"].data).to(dev)
+    bias = torch.from_numpy(p["bias"].data).to(dev)
+    hy = torch.empty((s.Bz, L, s.H, s.P), dtype=bf, pin_memory=True)
+    hF = torch.empty(hS0.shape, dtype=hS0.dtype, pin_memory=True)
+    hhT = torch.empty(hh0.shape, dtype=hh0.dtype, pin_memory=True)
+    dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host.items()}
+    dS0 = torch.empty(hS0.shape, dtype=hS0.dtype, device=dev)
+    dh0 = torch.empty(hh0.shape, dtype=hh0.dtype, device=dev)
+    dy = torch.empty(hy.shape, dtype=bf, device=dev)
+    dF = torch.empty(hF.shape, dtype=hF.dtype, device=dev)
+    dhT = torch.empty(hhT.shape, dtype=hhT.dtype, device=dev)
+    nstreams = min(4, s.Bz)
+    streams = [torch.cuda.Stream(device=dev) for _ in range(nstreams)]
+    main = torch.cuda.current_stream()
+    rows = [list(range(i, s.Bz, nstreams)) for i in range(nstreams)]
+
+    def e2e_step(e0):
+        for sti, rr in zip(streams, rows):
+            sti.wait_event(e0)
+            with torch.cuda.stream(sti):
+                for b in rr:
+                    for k in dev_in:
+                        dev_in[k][b].copy_(host[k][b], non_blocking=True)
+                    dS0[b].copy_(hS0[b], non_blocking=True)
+                    dh0[b].copy_(hh0[b], non_blocking=True)
+                    sl = slice(b, b + 1)
+                    sss.mixer_fwd(dev_in["x"][sl], dev_in["dt"][sl], A, dev_in["B"][sl],
+                                  dev_in["C"][sl], w, bias, dS0[sl], dh0[sl],
+                                  conv_state_out=dF[sl], hT=dhT[sl], y=dy[sl], fused=True,
+                                  stream=sti)
+                    hy[b].copy_(dy[b], non_blocking=True)
+                    hF[b].copy_(dF[b], non_blocking=True)
+                    hhT[b].copy_(dhT[b], non_blocking=True)
+        for sti in streams:
+            main.wait_stream(sti)
+
+    for _ in range(3):
+        e0 = torch.cuda.Event()
+        e0.record(main)
+        e2e_step(e0)
+    torch.cuda.synchronize()
+    ms = []
+    e2e_steps = max(3, args.steps // 10)
+    for _ in range(e2e_steps):
+        flush.zero_()
+        torch.cuda._sleep(200_000)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        e2e_step(e0)
+        e1.record(main)
+        main.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    total = max_over_ranks(dist, sum(ms), dev)
+    h2d = (sum(t.numel() * t.element_size() for t in host.values())
+           + hS0.numel() * hS0.element_size() + hh0.numel() * hh0.element_size())
+    d2h = (hy.numel() * hy.element_size() + hF.numel() * hF.element_size()
+           + hhT.numel() * hhT.element_size())
+    return {"value": job_rate(world, s.Bz * L, e2e_steps, total), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": total / e2e_steps,
+            "path": f"sss_mixer_fwd per batch row on {nstreams} streams, pinned host buffers, "
+                    "copies in and out inside the timed region"}
+
+
+def bench_segments(torch, sss, dev, stream, flush, args, hbm, hbm_kind, T):
+    """The 370M-like layer: batch 8, L = 2048 as two 1024-token segments with
+    conv and SSM state passed (one sss_mixer_fwd per segment), and the same
+    forward as two calls per segment (conv with u in fp32, then the scan)."""
+    s = synth.WORKLOADS["m370m_2k"]
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    segs = [{k: T(v) for k, v in synth.mixer_segment(s, i).items()} for i in range(len(s.segments))]
+    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
+    S0, h00 = T(st["conv_state"]), T(st["h0"])
+    S = torch.empty_like(S0)
+    h = torch.empty_like(h00)
+    Lseg = s.segments[0]
+    us = [torch.empty((s.Bz, L, s.D), dtype=torch.float32, device=dev) for L in s.segments]
+    ys = [torch.empty((s.Bz, L, s.H, s.P), dtype=torch.bfloat16, device=dev) for L in s.segments]
+    n_seg = len(segs)
+
+    def run(evs, two_call):
+        for i, sg in enumerate(segs):
+            evs[i].record(stream)
+            if two_call:
+                sss.conv_state_fwd(sg["x"], w, bias, S, S, u=us[i], stream=stream)
+                evs[n_seg + 1 + i].record(stream)
+                sss.ssm_scan_fwd(us[i], sg["dt"], A, sg["B"], sg["C"], h, h, y=ys[i],
+                                 stream=stream)
+            else:
+                sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
+                              conv_state_out=S, hT=h, y=ys[i], fused=True, spans=1,
+                              stream=stream)
+        evs[n_seg].record(stream)
+
+    def timed(two_call, steps):
+        all_evs = []
+        for _ in range(steps):
+            S.copy_(S0)
+            h.copy_(h00)
+            flush.zero_()
+            torch.cuda._sleep(200_000)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n_seg + 1)]
+            run(evs, two_call)
+            all_evs.append(evs)
+        stream.synchronize()
+        return all_evs
+
+    for _ in range(args.warmup):
+        S.copy_(S0)
+        h.copy_(h00)
+        run([torch.cuda.Event() for _ in range(2 * n_seg + 1)], False)
+        S.copy_(S0)
+        h.copy_(h00)
+        run([torch.cuda.Event() for _ in range(2 * n_seg + 1)], True)
+    torch.cuda.synchronize()
+    ev1 = timed(False, max(3, args.steps // 2))
+    seg_ms = [e[i].elapsed_time(e[i + 1]) for e in ev1 for i in range(n_seg)]
+    step_ms = statistics.mean(e[0].elapsed_time(e[n_seg]) for e in ev1)
+    ev2 = timed(True, max(3, args.steps // 4))
+    conv_ms = statistics.mean(e[i].elapsed_time(e[n_seg + 1 + i]) for e in ev2 for i in range(n_seg))
+    scan_ms = statistics.mean(e[n_seg + 1 + i].elapsed_time(e[i + 1] if i + 1 < n_seg else e[n_seg])
+                              for e in ev2 for i in range(n_seg))
+    two_ms = statistics.mean(e[0].elapsed_time(e[n_seg]) for e in ev2)
+    assert sss.device_status() == 0
+    fused_bytes = algorithmic_bytes(s, Lseg)
+    io = (s.Bz * Lseg * s.H * 2 + 2 * s.Bz * Lseg * s.G * s.N * 2 + s.Bz * Lseg * s.D * 2
+          + 2 * s.Bz * s.H * s.P * s.N * 4)
+    scan_bytes = s.Bz * Lseg * s.D * 4 + io
+    conv_bytes = s.Bz * Lseg * s.D * (2 + 4) + 2 * s.Bz * s.D * (s.K - 1) * 2
+    return {"workload": workload_desc(s), "tokens_per_s": s.Bz * s.L / (step_ms * 1e-3),
+            "ms_per_step": step_ms,
+            "roofline": roofline_block(fused_bytes, statistics.mean(seg_ms), hbm, hbm_kind,
+                                       "ssm_scan_pair_kernel<bf16,bf16,fused>", s.name,
+                                       ("ssm_scan_pair", s.name)),
+            "two_call_path": {
+                "ms_per_step": two_ms,
+                "conv_state_fwd": {"avg_launch_ms": conv_ms,
+                                   "algorithmic_bytes_per_launch": conv_bytes,
+                                   "achieved_gbs": conv_bytes / conv_ms / 1e6,
+                                   "frac": conv_bytes / conv_ms / 1e6 / hbm},
+                "ssm_scan_fwd": {"avg_launch_ms": scan_ms,
+                                 "algorithmic_bytes_per_launch": scan_bytes,
+                                 "achieved_gbs": scan_bytes / scan_ms / 1e6,
+                                 "frac": scan_bytes / scan_ms / 1e6 / hbm}}}
+
+
+def bench_tiny(torch, sss, dev, stream, flush, args, hbm, hbm_kind, T):
+    """The tiny fp32 check (batch 1, L = 64 as two 32-token segments, H = 2,
+    P = 4, N = 8): one sss_mixer_fwd per segment on the fp32 path.  Far too
+    small to fill the GPU; its time is launch latency."""
+    s = synth.WORKLOADS["tiny_f32"]
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    segs = [{k: T(v) for k, v in synth.mixer_segment(s, i).items()} for i in range(len(s.segments))]
+    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
+    S = T(st["conv_state"])
+    h = T(st["h0"])
+    ys = [torch.empty((s.Bz, L, s.H, s.P), dtype=torch.float32, device=dev) for L in s.segments]
+
+    def call():
+        for i, sg in enumerate(segs):
+            sss.mixer_fwd(sg["x"], sg["dt"], A, sg["B"], sg["C"], w, bias, S, h,
+                          conv_state_out=S, hT=h, y=ys[i], stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ms = statistics.mean(events_timed(torch, stream, flush, call, max(3, args.steps // 10),
+                                      sleep_ns=50_000))
+    byts = sum(algorithmic_bytes(s, L, 4, 4) for L in s.segments)
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"workload": workload_desc(s), "ms_per_step": ms,
+            "tokens_per_s": s.Bz * s.L / (ms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / hbm, "algorithmic_bytes_per_step": byts,
+                         "avg_step_ms": ms, "traffic": None,
+                         "kernel": "fp32 path (conv, CUDA-core scan) per segment; far too small "
+                                   "to fill the GPU, its time is launch latency"}}
 
 
 def bench_conv_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
@@ -609,7 +724,7 @@ def bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
             "kernel": "fp32 CUDA-core chunked backward (chunks of 64)"}
 
 
-def bench_long_context(torch, sss, dev, stream, flush, args, hbm):
+def bench_long_context(torch, sss, dev, stream, flush, args, hbm, hbm_kind):
     """The long-context streaming workload: batch 1, 64 consecutive
     2048-token segments of a 780M-like layer (H 48, P 64, N 128, K 4, bf16),
     each sss_mixer_fwd call starting from the previous call's conv and SSM
@@ -670,11 +785,19 @@ def bench_long_context(torch, sss, dev, stream, flush, args, hbm):
     ms_one = timed(1)
     assert sss.device_status() == 0
     tok = Bz * L
+    seg_bytes = algorithmic_bytes(s, Lseg)
+    us_seg = ms_span * 1e3 / nseg
     return {"workload": workload_desc(s), "spans_per_segment": ns_auto,
             "ms_per_stream": ms_span, "tokens_per_s": tok / (ms_span * 1e-3),
-            "us_per_segment": ms_span * 1e3 / nseg,
+            "us_per_segment": us_seg,
+            "roofline": roofline_block(seg_bytes, us_seg * 1e-3, hbm, hbm_kind,
+                                       "the segment's launches together (span kernels and the "
+                                       "pair kernel passes)" if ns_auto > 1 else
+                                       "ssm_scan_pair_kernel<bf16,bf16,fused>", s.name)
+                        | {"per": "2048-token segment, averaged over the 64-segment stream"},
             "one_pass": {"ms_per_stream": ms_one, "tokens_per_s": tok / (ms_one * 1e-3),
-                         "us_per_segment": ms_one * 1e3 / nseg},
+                         "us_per_segment": ms_one * 1e3 / nseg,
+                         "frac": seg_bytes / (ms_one * 1e-3 / nseg) / 1e9 / hbm},
             "path": "sss_mixer_fwd_spans: conv-state gather + decay sums, state-only pass "
                     "from zero states, warp-shuffle carry, pass from carried states (4 launches "
                     "per segment)" if ns_auto > 1 else "sss_mixer_fwd (one launch per segment)"}
@@ -738,8 +861,11 @@ def bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
     return out
 
 
-def bench_decode(torch, sss, dev, stream, flush, args, hbm):
-    d = synth.DECODE["decode_256x1"]
+def bench_decode(torch, sss, dev, stream, flush, args, hbm, name):
+    """The continuous-batching decode update (sss_mixer_update): 256 of 512
+    pool rows by a random permutation, circular conv pool, SSM pool in fp32,
+    L_new tokens per call."""
+    d = synth.DECODE[name]
     g = torch.Generator(device=dev)
     g.manual_seed(d.seed)
     bf = torch.bfloat16
@@ -781,9 +907,9 @@ def bench_decode(torch, sss, dev, stream, flush, args, hbm):
             + d.Bz * d.D * (d.K - 1) * 2 + d.Bz * d.L_new * d.D * 2
             + d.Bz * d.L_new * (2 * d.D * 2 + 2 * d.G * d.N * 2 + d.H * 2))
     gbs = byts / (avg * 1e-3) / 1e9
-    return {"workload": "decode_256x1: 256 of 512 pool rows by a random permutation, circular "
-                        "conv pool [512,4096,4], cache_seqlens ~ U[0,10000), SSM pool "
-                        "[512,64,64,128] fp32, L_new=1, H=64, P=64, N=128, K=4, bf16",
+    return {"workload": f"{name}: 256 of 512 pool rows by a random permutation, circular "
+                        f"conv pool [512,4096,4], cache_seqlens ~ U[0,10000), SSM pool "
+                        f"[512,64,64,128] fp32, L_new={d.L_new}, H=64, P=64, N=128, K=4, bf16",
             "tokens_per_s": d.Bz * d.L_new / (avg * 1e-3), "avg_launch_ms": avg,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
                          "frac": gbs / hbm, "algorithmic_bytes_per_launch": byts,

@@ -611,13 +611,20 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
           ssm_pool + (int64_t(ms->row[s]) * H + h) * int64_t(P) * kPipeN);
       // row-invariant operands, read once (the in-place state stores would
       // otherwise make the compiler re-read them for every row)
-      float av[LT];
+      // per token: the decay as a packed pair, this lane's four columns of B
+      // and C as two packed pairs each (the state rows then take packed
+      // f32x2 multiplies and FMAs: half the instructions)
+      uint64_t av2[LT], b01[LT], b23[LT], c01[LT], c23[LT];
 #pragma unroll
-      for (int i = 0; i < LT; ++i) av[i] = i < L_new ? ms->a[s][i] : 0.0f;
-      float4 bv1 = make_float4(0.f, 0.f, 0.f, 0.f), cv1 = bv1;
-      if constexpr (LT == 1) {
-        bv1 = ld4_f32<T>(bsm + lane * 4);
-        cv1 = ld4_f32<T>(csm + lane * 4);
+      for (int i = 0; i < LT; ++i) {
+        const float a = i < L_new ? ms->a[s][i] : 0.0f;
+        const float4 bv = i < L_new ? ld4_f32<T>(bsm + i * kPipeN + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 cv = i < L_new ? ld4_f32<T>(csm + i * kPipeN + lane * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        av2[i] = pk2(a, a);
+        b01[i] = pk2(bv.x, bv.y);
+        b23[i] = pk2(bv.z, bv.w);
+        c01[i] = pk2(cv.x, cv.y);
+        c23[i] = pk2(cv.z, cv.w);
       }
       float part[LT][RP];
 #pragma unroll
@@ -626,26 +633,25 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
 #pragma unroll
         for (int i = 0; i < LT; ++i) part[i][rr] = 0.0f;
         if (p < P) {
-          float4 hv = hst[p * (kPipeN / 4) + lane];
+          const float4 hv = hst[p * (kPipeN / 4) + lane];
+          uint64_t h01 = pk2(hv.x, hv.y), h23 = pk2(hv.z, hv.w);
 #pragma unroll
           for (int i = 0; i < LT; ++i) {
             if (i < L_new) {
-              const float4 bv = LT == 1 ? bv1 : ld4_f32<T>(bsm + i * kPipeN + lane * 4);
-              const float4 cv = LT == 1 ? cv1 : ld4_f32<T>(csm + i * kPipeN + lane * 4);
-              const float a = av[i];
+              // h = a h + u B (columns in pairs), then this lane's part of h C
               const float u = ms->us[i][p];
-              hv.x = fmaf(a, hv.x, u * bv.x);
-              hv.y = fmaf(a, hv.y, u * bv.y);
-              hv.z = fmaf(a, hv.z, u * bv.z);
-              hv.w = fmaf(a, hv.w, u * bv.w);
-              float acc = hv.x * cv.x;
-              acc = fmaf(hv.y, cv.y, acc);
-              acc = fmaf(hv.z, cv.z, acc);
-              acc = fmaf(hv.w, cv.w, acc);
-              part[i][rr] = acc;
+              const uint64_t u2 = pk2(u, u);
+              h01 = fma2(av2[i], h01, mul2(u2, b01[i]));
+              h23 = fma2(av2[i], h23, mul2(u2, b23[i]));
+              float e, o;
+              upk2(fma2(h23, c23[i], mul2(h01, c01[i])), e, o);
+              part[i][rr] = e + o;
             }
           }
-          gst[p * (kPipeN / 4) + lane] = hv;  // coalesced 16-byte stores
+          float4 hn;
+          upk2(h01, hn.x, hn.y);
+          upk2(h23, hn.z, hn.w);
+          gst[p * (kPipeN / 4) + lane] = hn;  // coalesced 16-byte stores
         }
       }
 #pragma unroll
@@ -713,10 +719,20 @@ static cudaError_t pipe_shape(const void* x, const float* w, const float* bias, 
 #define SSS_PIPE(RP, LT, KT)                                                                  \
   return launch_pipe<T, RP, LT, KT>(x, w, bias, cp, pool, S_len, sl, ix, dt, A, B, C, sp, y, \
                                     Bz, L_new, H, P, G, K, geo, stages, status, st)
+  // the token count rounded up to 1, 2, 4 or 8: every loop over the tokens
+  // unrolls and the operands of the new tokens stay in registers
   if (P <= 64) {
     if (L_new == 1) {
       if (K <= 4) SSS_PIPE(8, 1, 4);
       SSS_PIPE(8, 1, 8);
+    }
+    if (L_new == 2) {
+      if (K <= 4) SSS_PIPE(8, 2, 4);
+      SSS_PIPE(8, 2, 8);
+    }
+    if (L_new <= 4) {
+      if (K <= 4) SSS_PIPE(8, 4, 4);
+      SSS_PIPE(8, 4, 8);
     }
     if (K <= 4) SSS_PIPE(8, kPipeMaxLnew, 4);
     SSS_PIPE(8, kPipeMaxLnew, 8);
