@@ -155,9 +155,12 @@ sss_status sss_conv_state_bwd(const void* x, sss_dtype x_dtype, const float* w,
  *  - Memory: every GPU that loads the library holds the 8 MiB array until
  *    the process exits.
  *  - Set-up: the first call on a device, with that device current, looks up
- *    the array's device address (cudaGetSymbolAddress) and caches it; make
- *    that first call before any stream capture begins.  A failed lookup
- *    returns SSS_ERR_CUDA.
+ *    the array's device address (cudaGetSymbolAddress) and caches it for
+ *    that device's current context; a call under another context (after
+ *    cudaDeviceReset, say, when the module is loaded again and the array may
+ *    sit elsewhere) looks it up again.  Make the first call on a device, and
+ *    the first after a reset, before any stream capture begins.  A failed
+ *    lookup returns SSS_ERR_CUDA.
  *  - Sharing: all calls on a device use the same array, and it keeps the
  *    last call's partial sums.  Each call writes every partial it reads
  *    before reading it, so nothing needs clearing between calls; but two
@@ -174,6 +177,11 @@ sss_status sss_conv_state_bwd_noalloc(const void* x, sss_dtype x_dtype, const fl
                                       sss_dtype dx_dtype, void* dstate_in, float* dw,
                                       float* dbias, int64_t Bz, int64_t L, int64_t D,
                                       int K, int apply_silu, sss_stream_t stream);
+
+/* The size in bytes of the static array behind sss_conv_state_bwd_noalloc
+ * (SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES), for bindings that cannot read the
+ * macro. */
+size_t sss_conv_state_bwd_noalloc_scratch_bytes(void);
 
 /*
  * sss_conv_state_fwd_packed -- sss_conv_state_fwd over rows that pack several
@@ -519,20 +527,6 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype,
  * per (request, head), -1 = unsupported. */
 int sss_mixer_update_path(int L_new, int P, int N, int K, int S_len,
                           sss_dtype act_dtype);
-
-/*
- * sss_tcgen05_selftest -- diagnostic of the tensor-core operand layouts the
- * chunked scan uses (no counterpart on the pages).  With A and B two
- * [128][128] bf16 row-major matrices (device), writes nine fp32 [128][128]
- * blocks to `out` (device, 9*128*128 floats), each = A B^T computed through
- * one descriptor form: [0] both operands K-major; [1] A MN-major; [2] B
- * MN-major; [3] A read from tensor memory; [4] A from tensor memory with B
- * MN-major; [5] A and B MN-major ([1]..[5]: N = 64, columns 0..63 valid);
- * [6] K-major A, [7] A from tensor memory, [8] MN-major A, each with an
- * N = 128 MN-major B made of two 64-wide blocks 16 KB apart.
- */
-sss_status sss_tcgen05_selftest(const void* A, const void* B, float* out,
-                                sss_stream_t stream);
 
 /*
  * sss_device_status -- read the device status word (OR of SSS_ERR_INDEX /

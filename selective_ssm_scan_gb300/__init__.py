@@ -114,8 +114,6 @@ _lib.sss_mixer_fwd_spans.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p,
 _lib.sss_ssm_scan_fwd_spans.restype = _i
 _lib.sss_ssm_scan_fwd_spans.argtypes = [_p, _i, _p, _p, _p, _p, _i, _p, _p, _p, _i, _i64, _i64,
                                         _i, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
-_lib.sss_tcgen05_selftest.restype = _i
-_lib.sss_tcgen05_selftest.argtypes = [_p, _p, _p, _p]
 _lib.sss_device_status.restype = _i
 _lib.sss_device_status.argtypes = [ctypes.POINTER(_i), _i, _p]
 
@@ -222,8 +220,10 @@ def conv_state_bwd(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor
 
 
 # Size of the library's static scratch behind conv_state_bwd_noalloc (the
-# SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES of the C header).
-CONV_BWD_NOALLOC_SCRATCH_BYTES = 8 << 20
+# SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES of the C header), read from the library.
+_lib.sss_conv_state_bwd_noalloc_scratch_bytes.restype = ctypes.c_size_t
+_lib.sss_conv_state_bwd_noalloc_scratch_bytes.argtypes = []
+CONV_BWD_NOALLOC_SCRATCH_BYTES = int(_lib.sss_conv_state_bwd_noalloc_scratch_bytes())
 
 
 def conv_state_bwd_noalloc(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor],
@@ -576,16 +576,6 @@ def mixer_update_path(L_new, P, N, K, S_len, act_dtype) -> int:
     """1 = bulk-copy pipelined update kernel, 0 = one CTA per (request, head),
     -1 = unsupported (for 16-byte aligned tensors with a bias)."""
     return int(_lib.sss_mixer_update_path(L_new, P, N, K, S_len, _dtype_code(act_dtype)))
-
-
-def tcgen05_selftest(A: torch.Tensor, B: torch.Tensor, stream=None) -> torch.Tensor:
-    """A, B [128, 128] bf16 (cuda).  Returns [9, 128, 128] fp32: A @ B.T through
-    the tensor-core operand forms of the chunked scan (blocks 1..5 valid in
-    columns 0..63, the others in all columns)."""
-    out = torch.zeros((9, 128, 128), dtype=torch.float32, device=A.device)
-    _check("sss_tcgen05_selftest", _lib.sss_tcgen05_selftest(_ptr(A), _ptr(B), _ptr(out),
-                                                             _stream(stream)))
-    return out
 
 
 def device_status(clear: bool = True, stream=None) -> int:

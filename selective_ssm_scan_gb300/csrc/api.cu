@@ -42,8 +42,6 @@ cudaError_t mixer_fwd_pair_launch(const void* x, const float* w, const float* bi
                                   const void* B, const void* C, const float* h0, float* hT,
                                   void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
                                   int K, int* status, const int32_t* seq_idx, cudaStream_t st);
-cudaError_t tc_selftest_launch(const void* A, const void* B, float* out, int* status,
-                               cudaStream_t st);
 cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
                                   const void* s_in, const void* dy, sss_dtype dyt, const void* q,
                                   void* dx, sss_dtype dxt, void* dS, float* dw, float* dbias,
@@ -592,6 +590,9 @@ static sss_status fwd_spans_impl(bool fused, const void* x, sss_dtype x_dtype, c
   if (!fused) K = 1;
   if (!spans_supported(fused, x_dtype, act_dtype, y_dtype, Bz, Ls, H, P, N, G, K, ns))
     return SSS_ERR_UNSUPPORTED;
+  // the span kernels (gather of the conv state and per-span decay sums) read
+  // dt, B, C and, fused, x and the conv state as bf16
+  if (act_dtype != SSS_BF16 || (fused && x_dtype != SSS_BF16)) return SSS_ERR_UNSUPPORTED;
   if (!x || !dt || !A || !B || !C || !y || !aligned(x, 16) || !aligned(dt, 2) || !aligned(A, 4) ||
       !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16))
     return SSS_ERR_INVALID_ARG;
@@ -710,14 +711,6 @@ sss_status sss_mixer_update(const void* x_new, sss_dtype act_dtype, const float*
                                        cache_seqlens, conv_state_indices, dt, A, B, C,
                                        ssm_pool, y, Bz, L_new, H, P, N, G, K, status_word(),
                                        reinterpret_cast<cudaStream_t>(stream)));
-}
-
-sss_status sss_tcgen05_selftest(const void* A, const void* B, float* out,
-                                sss_stream_t stream) {
-  if (!A || !B || !out || !aligned(A, 16) || !aligned(B, 16) || !aligned(out, 4))
-    return SSS_ERR_INVALID_ARG;
-  return from_cuda(tc_selftest_launch(A, B, out, status_word(),
-                                      reinterpret_cast<cudaStream_t>(stream)));
 }
 
 sss_status sss_device_status(int* status_out, int clear, sss_stream_t stream) {

@@ -25,20 +25,45 @@ static __device__ __align__(256) unsigned char g_conv_bwd_scratch[SSS_CONV_BWD_N
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices];
+void* g_scratch_ctx[kMaxDevices];  // the context the cached address belongs to
 
-// The scratch's device address on the current device, looked up once per
-// device (with that device current) and cached.
+// The calling thread's current context (driver entry point, fetched through
+// the runtime once); null when the entry point is unavailable.
+void* current_context() {
+  using Fn = int (*)(void**);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(f);
+  });
+  void* ctx = nullptr;
+  if (!fn || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
+// The scratch's device address on the current device, looked up with that
+// device current and cached per (device, context): a device reset or any new
+// primary context loads the module again, possibly at another address, so a
+// changed context (or an unknown one) means a fresh lookup.
 cudaError_t scratch_address(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  const void* ctx = current_context();
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || !ctx || g_scratch_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_conv_bwd_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = p;
+    // the lookup makes the device's primary context current if it was not
+    g_scratch_ctx[dev] = current_context();
   }
   *out = g_scratch_addr[dev];
   return cudaSuccess;
@@ -68,4 +93,8 @@ extern "C" sss_status sss_conv_state_bwd_noalloc(
   return sss_conv_state_bwd(x, x_dtype, w, bias, state_in, dy, dy_dtype, dstate_out, dx,
                             dx_dtype, dstate_in, dw, dbias, Bz, L, D, K, apply_silu, scratch,
                             need > 0 ? size_t(SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES) : 0, stream);
+}
+
+extern "C" size_t sss_conv_state_bwd_noalloc_scratch_bytes(void) {
+  return size_t(SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES);
 }

@@ -216,6 +216,7 @@ bool span_sizes_ok(int64_t Bz, int64_t L, int64_t D, int H, int P, int N, int K,
          int64_t(P) * N < (int64_t(1) << 31) && Bz * H <= 65535 && blocks < (int64_t(1) << 31);
 }
 
+// x, s_in, s_out, s_span and dt are bf16 (the caller checks the dtypes).
 cudaError_t span_prepare_launch(const void* x, const void* s_in, void* s_out, void* s_span,
                                 const void* dt, const float* A, float* part, int64_t Bz,
                                 int64_t L, int64_t D, int H, int K, int ns, cudaStream_t st) {

@@ -1,7 +1,7 @@
 """The tensor-core path: operand layouts of tcgen05.mma and path selection.
 
-The layout self-test multiplies two bf16 tiles through the four descriptor
-forms the chunked scan uses and compares with a plain fp32 matmul of the same
+The layout self-test (a test-only library, tests/tc_selftest) multiplies two
+bf16 tiles through the descriptor forms the chunked scan uses and compares with a plain fp32 matmul of the same
 bf16 values (a hardware-layout check; the scan itself is checked against the
 oracle in test_gpu_parity.py)."""
 import numpy as np
@@ -18,14 +18,34 @@ import selective_ssm_scan_gb300 as sss  # noqa: E402
 DEV = torch.device("cuda:0")
 
 
+def _selftest_lib():
+    """The test-only library with the operand-layout kernels (built on demand
+    from tests/tc_selftest/tc_selftest.cu; not part of libsss)."""
+    import ctypes
+    import importlib.util
+    import os
+    here = os.path.join(os.path.dirname(os.path.abspath(__file__)), "tc_selftest", "build.py")
+    spec = importlib.util.spec_from_file_location("tc_selftest_build", here)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    lib = ctypes.CDLL(mod.build())
+    lib.sss_test_tcgen05_layouts.restype = ctypes.c_int
+    lib.sss_test_tcgen05_layouts.argtypes = [ctypes.c_void_p] * 5
+    return lib
+
+
 def test_tcgen05_operand_layouts():
     g = torch.Generator(device="cpu").manual_seed(5)
     A = torch.randn((128, 128), generator=g).to(torch.bfloat16).to(DEV)
     B = torch.randn((128, 128), generator=g).to(torch.bfloat16).to(DEV)
-    sss.device_status(clear=True)
-    out = sss.tcgen05_selftest(A, B)
+    out = torch.empty((9, 128, 128), dtype=torch.float32, device=DEV)
+    status = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    lib = _selftest_lib()
+    rc = lib.sss_test_tcgen05_layouts(A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                                      status.data_ptr(), torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
-    assert sss.device_status() == 0
+    assert rc == 0
+    assert int(status.item()) == 0
     ref = (A.double() @ B.double().T).float()
     names = ["K-major A and B", "MN-major A", "MN-major B", "A from tensor memory",
              "A from tensor memory, MN-major B", "MN-major A and B",
