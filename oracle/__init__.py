@@ -28,6 +28,9 @@ mixer_update(...) -> (y, conv_pool', ssm_pool', n_skipped)
     batching), followed by the recurrence on the pool's SSM state.
 mixer_fwd(...) -> (y, F, hT)
     conv_state_fwd then ssm_scan (a segment of the streaming forward).
+mamba2_mixer_fwd(...) -> (y, F, hT)
+    The full Mamba-2 mixer wiring: the conv over all xBC channels, dt bias
+    and softplus, the dt-scaled input, the D skip and the SiLU(z) gate.
 """
 from __future__ import annotations
 
@@ -80,9 +83,11 @@ def lib():
             l.orc_mixer_update.argtypes = [_dp, _dp, _dp, _dp, _L, _L, _ip, _ip, _dp, _dp,
                                            _dp, _dp, _dp, _dp, _L, _L, _L, _L, _L, _L,
                                            ctypes.c_int, ctypes.c_int]
+            l.orc_mamba2_scan.argtypes = [_dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _dp, _L, _L,
+                                          _L, _L, _L, _L, ctypes.c_int]
             l.orc_num_threads.argtypes = [ctypes.c_int]
             for f in (l.orc_conv_state_fwd, l.orc_conv_state_bwd, l.orc_ssm_scan, l.orc_ssm_scan_bwd,
-                      l.orc_mixer_update, l.orc_num_threads):
+                      l.orc_mixer_update, l.orc_mamba2_scan, l.orc_num_threads):
                 f.restype = ctypes.c_int
             _lib = l
     return _lib
@@ -191,6 +196,37 @@ def mixer_fwd(x, dt, A, B, C, w, bias, conv_state=None, h0=None, nthreads: int =
     the scan from h0.  Returns y [Bz, L, H, P], F [Bz, D, K-1], hT."""
     u, F = conv_state_fwd(x, w, bias, conv_state, True, nthreads)
     y, hT = ssm_scan(u, dt, A, B, C, h0, nthreads)
+    return y, F, hT
+
+
+def mamba2_mixer_fwd(xBC, z, dt_raw, dt_bias, A, D_skip, w, bias, conv_state, h0, H, G, N,
+                     nthreads: int = 0):
+    """The full Mamba-2 mixer wiring over one segment (the Mamba-2 layers of
+    "Understanding and Improving Length Generalization in Recurrent Models";
+    the xBC conv of "Chapter 7: state, chunking and incremental inference").
+
+    xBC [Bz, L, D + 2 G N] (channels [0, D) are x, then B, then C), z [Bz, L,
+    D] | None (no gate), dt_raw [Bz, L, H], dt_bias [H] | None, A [H],
+    D_skip [H] | None, w [D + 2 G N, K], bias [D + 2 G N] | None,
+    conv_state [Bz, D + 2 G N, K-1] | None, h0 [Bz, H, P, N] | None.
+    The conv (+ SiLU) runs over every channel; then per token
+    dt = softplus(dt_raw + dt_bias), a = exp(dt A_h), h = a h + dt x B^T,
+    y = (h C + D_h x) SiLU(z).  Returns y [Bz, L, H, P], F [Bz, D + 2 G N,
+    K-1] and hT [Bz, H, P, N] (float64)."""
+    u, F = conv_state_fwd(xBC, w, bias, conv_state, True, nthreads)
+    dt_raw, dt_bias, A, D_skip, h0 = _f64(dt_raw), _f64(dt_bias), _f64(A), _f64(D_skip), _f64(h0)
+    z = _f64(z)
+    Bz, L, Dt = u.shape
+    P = (Dt - 2 * G * N) // H
+    if H * P + 2 * G * N != Dt or dt_raw.shape != (Bz, L, H):
+        raise ValueError("mamba2_mixer_fwd: channel count is not H P + 2 G N")
+    y = np.empty((Bz, L, H, P))
+    hT = np.empty((Bz, H, P, N))
+    rc = lib().orc_mamba2_scan(_ptr(u), _ptr(z), _ptr(dt_raw), _ptr(dt_bias), _ptr(A),
+                               _ptr(D_skip), _ptr(h0), _ptr(y), _ptr(hT), Bz, L, H, P, N, G,
+                               nthreads)
+    if rc != 0:
+        raise ValueError("orc_mamba2_scan: bad sizes")
     return y, F, hT
 
 

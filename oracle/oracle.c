@@ -45,6 +45,16 @@
  *                       ddt_t = dl_t A_h and dA_h = sum dl_t dt_t, and
  *                       dh0 = a_0 g_0; dB and dC sum over the heads of a
  *                       group, dA over the batch.
+ *   orc_mamba2_scan     the recurrence of the full Mamba-2 mixer wiring
+ *                       (the Mamba-2 layers of "Understanding and Improving
+ *                       Length Generalization in Recurrent Models" sections 1
+ *                       and 4.4, with the causal-conv chapter's xBC conv): on
+ *                       the conv + SiLU output of all D + 2 G N channels of
+ *                       xBC (channels [0, D) are x, then B and C),
+ *                       dt_t = softplus(dt_raw_t + dt_bias_h),
+ *                       a_t = exp(dt_t A_h), h_t = a_t h_{t-1} + dt_t x_t B_t^T,
+ *                       y_t = (h_t C_t + D_h x_t) SiLU(z_t), one token at a
+ *                       time from the initial state.
  *   orc_mixer_update    the single- and multi-token update of the same
  *                       chapter (sections "single-token update", "the
  *                       physical cache can be longer", "circular mode",
@@ -501,4 +511,62 @@ int orc_mixer_update(const double* x, const double* w, const double* bias,
   for (long b = 0; b < Bz; ++b) nbad += bad[b];
   free(bad);
   return nbad;
+}
+
+/* ------------------------------------------------------------------------ */
+/* the full Mamba-2 mixer wiring                                            */
+/* ------------------------------------------------------------------------ */
+
+/* log(1 + e^v), without overflow for large v */
+static double softplus(double v) { return v > 30.0 ? v + log1p(exp(-v)) : log1p(exp(v)); }
+
+typedef struct {
+  const double *u, *z, *dtr, *dtb, *A, *Dsk, *h0;
+  double *y, *hT;
+  long Bz, L, H, P, N, G;
+} m2_ctx;
+
+static void m2_item(void* p, long item) {
+  m2_ctx* c = (m2_ctx*)p;
+  const long H = c->H, P = c->P, N = c->N, G = c->G, L = c->L;
+  const long Dx = H * P, Dt = Dx + 2 * G * N;
+  const long b = item / H, hd = item % H;
+  const long g = hd / (H / G);
+  const double Dh = c->Dsk ? c->Dsk[hd] : 0.0;
+  double* h = (double*)malloc(sizeof(double) * (size_t)(P * N > 0 ? P * N : 1));
+  for (long i = 0; i < P * N; ++i)
+    h[i] = c->h0 ? c->h0[(b * H + hd) * P * N + i] : 0.0;
+  for (long t = 0; t < L; ++t) {
+    /* the conv output of token t: x of this head, B and C of its group */
+    const double* ut = c->u + (b * L + t) * Dt;
+    const double* xt = ut + hd * P;
+    const double* Bt = ut + Dx + g * N;
+    const double* Ct = ut + Dx + G * N + g * N;
+    const double dt = softplus(c->dtr[(b * L + t) * H + hd] + (c->dtb ? c->dtb[hd] : 0.0));
+    const double a = exp(dt * c->A[hd]);
+    double* yt = c->y + ((b * L + t) * H + hd) * P;
+    for (long pp = 0; pp < P; ++pp) {
+      double acc = 0.0;
+      for (long n = 0; n < N; ++n) {
+        double v = a * h[pp * N + n] + dt * xt[pp] * Bt[n];
+        h[pp * N + n] = v;
+        acc += v * Ct[n];
+      }
+      const double gate = c->z ? silu(c->z[(b * L + t) * Dx + hd * P + pp]) : 1.0;
+      yt[pp] = (acc + Dh * xt[pp]) * gate;
+    }
+  }
+  if (c->hT)
+    for (long i = 0; i < P * N; ++i) c->hT[(b * H + hd) * P * N + i] = h[i];
+  free(h);
+}
+
+int orc_mamba2_scan(const double* u, const double* z, const double* dt_raw,
+                    const double* dt_bias, const double* A, const double* D_skip,
+                    const double* h0, double* y, double* hT, long Bz, long L, long H,
+                    long P, long N, long G, int nthreads) {
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G) return -1;
+  m2_ctx c = {u, z, dt_raw, dt_bias, A, D_skip, h0, y, hT, Bz, L, H, P, N, G};
+  parallel_for(Bz * H, nthreads, m2_item, &c);
+  return 0;
 }

@@ -823,3 +823,129 @@ def test_packed_scan_equals_separate_samples(bounds):
         yr, hr = oracle.ssm_scan(u[:, sl], dt[:, sl], A, B[:, sl], C[:, sl], h0 if i == 0 else None)
         np.testing.assert_allclose(y[:, sl], yr, rtol=1e-12, atol=1e-12)
     np.testing.assert_allclose(hT, hr, rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# the full Mamba-2 mixer wiring (xBC conv, dt bias + softplus, dt-scaled input,
+# D skip, SiLU(z) gate)
+# ---------------------------------------------------------------------------
+
+def _m2_inputs(seed, Bz=2, L=13, H=4, P=3, N=5, G=2, K=4, gate=True):
+    r = np.random.default_rng(seed)
+    D = H * P
+    Dt = D + 2 * G * N
+    return dict(
+        xBC=r.standard_normal((Bz, L, Dt)),
+        z=r.standard_normal((Bz, L, D)) if gate else None,
+        dt_raw=r.standard_normal((Bz, L, H)) - 2.0,
+        dt_bias=r.uniform(-1.0, 1.0, H),
+        A=-r.uniform(0.01, 1.0, H),
+        D_skip=r.standard_normal(H),
+        w=r.standard_normal((Dt, K)) * np.sqrt(0.5),
+        bias=np.full(Dt, 0.1),
+        conv_state=r.standard_normal((Bz, Dt, K - 1)),
+        h0=r.normal(0.0, 0.1, (Bz, H, P, N)),
+        H=H, G=G, N=N)
+
+
+def test_mamba2_zero_gate_gives_zero_output():
+    """SiLU(0) = 0: with z = 0 the gated output is exactly zero while the
+    state still advances."""
+    a = _m2_inputs(1)
+    a["z"] = np.zeros_like(a["z"])
+    y, _, hT = oracle.mamba2_mixer_fwd(**a)
+    assert np.all(y == 0.0)
+    _, _, hT_nogate = oracle.mamba2_mixer_fwd(**dict(a, z=None))
+    np.testing.assert_array_equal(hT, hT_nogate)
+
+
+def test_mamba2_equals_plain_scan_of_the_conv_channels():
+    """With the conv output split into x, B and C and dt = softplus(dt_raw +
+    dt_bias) (numpy logaddexp), the wiring equals the plain scan oracle fed
+    x, dt, A, dt-scaled B (one head per group, so dt_t B_t is that head's)
+    and C, plus D_h x, times SiLU(z)."""
+    a = _m2_inputs(2, H=4, G=4)
+    Bz, L, Dt = a["xBC"].shape
+    H, G, N = a["H"], a["G"], a["N"]
+    D = Dt - 2 * G * N
+    P = D // H
+    y, F, hT = oracle.mamba2_mixer_fwd(**a)
+    u, F_ref = oracle.conv_state_fwd(a["xBC"], a["w"], a["bias"], a["conv_state"])
+    x = u[:, :, :D]
+    Bm = u[:, :, D:D + G * N].reshape(Bz, L, G, N)
+    Cm = u[:, :, D + G * N:].reshape(Bz, L, G, N)
+    dt = np.logaddexp(0.0, a["dt_raw"] + a["dt_bias"])          # [Bz, L, H]
+    y_s, h_s = oracle.ssm_scan(x, dt, a["A"], Bm * dt[..., None], Cm, a["h0"])
+    gate = silu(a["z"]).reshape(Bz, L, H, P)
+    y_ref = (y_s + a["D_skip"][None, None, :, None] * x.reshape(Bz, L, H, P)) * gate
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(hT, h_s, rtol=1e-12, atol=1e-14)
+    np.testing.assert_array_equal(F, F_ref)
+
+
+def test_mamba2_dt_bias_shift_invariance():
+    """Only dt_raw + dt_bias enters: shifting one by c and the other by -c
+    changes nothing."""
+    a = _m2_inputs(3)
+    y0, _, h0 = oracle.mamba2_mixer_fwd(**a)
+    c = 0.375
+    y1, _, h1 = oracle.mamba2_mixer_fwd(**dict(a, dt_raw=a["dt_raw"] + c, dt_bias=a["dt_bias"] - c))
+    np.testing.assert_allclose(y1, y0, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(h1, h0, rtol=1e-12, atol=1e-14)
+
+
+def test_mamba2_skip_alone_when_b_channels_are_silent():
+    """Zero conv weights and bias on the B channels make B = SiLU(0) = 0; from
+    h0 = 0 the state stays zero and y = D_h x SiLU(z) (x the conv output)."""
+    a = _m2_inputs(4)
+    Bz, L, Dt = a["xBC"].shape
+    G, N, H = a["G"], a["N"], a["H"]
+    D = Dt - 2 * G * N
+    a["w"][D:D + G * N] = 0.0
+    a["bias"][D:D + G * N] = 0.0
+    a["h0"] = np.zeros_like(a["h0"])
+    y, _, hT = oracle.mamba2_mixer_fwd(**a)
+    assert np.all(hT == 0.0)
+    u, _ = oracle.conv_state_fwd(a["xBC"], a["w"], a["bias"], a["conv_state"])
+    P = D // H
+    y_ref = (a["D_skip"][None, None, :, None] * u[:, :, :D].reshape(Bz, L, H, P)
+             * silu(a["z"]).reshape(Bz, L, H, P))
+    np.testing.assert_allclose(y, y_ref, rtol=1e-13, atol=1e-15)
+
+
+def test_mamba2_large_negative_dt_holds_the_state():
+    """dt_raw -> -inf gives dt = softplus(.) -> 0: a = 1 and no input enters,
+    so h_t = h0 and y_t = (h0 C_t + D_h x_t) SiLU(z_t)."""
+    a = _m2_inputs(5)
+    a["dt_raw"] = np.full_like(a["dt_raw"], -800.0)
+    y, _, hT = oracle.mamba2_mixer_fwd(**a)
+    np.testing.assert_array_equal(hT, a["h0"])
+    Bz, L, Dt = a["xBC"].shape
+    G, N, H = a["G"], a["N"], a["H"]
+    D = Dt - 2 * G * N
+    P = D // H
+    u, _ = oracle.conv_state_fwd(a["xBC"], a["w"], a["bias"], a["conv_state"])
+    Cm = u[:, :, D + G * N:].reshape(Bz, L, G, N)
+    g_of_h = np.arange(H) // (H // G)
+    hC = np.einsum("bhpn,blhn->blhp", a["h0"], Cm[:, :, g_of_h, :])
+    y_ref = (hC + a["D_skip"][None, None, :, None] * u[:, :, :D].reshape(Bz, L, H, P)) \
+        * silu(a["z"]).reshape(Bz, L, H, P)
+    np.testing.assert_allclose(y, y_ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("cut", [1, 5, 12])
+def test_mamba2_segment_equivalence(cut):
+    """Whole sequence = first part then the rest from the passed conv state
+    (over every xBC channel) and SSM state."""
+    a = _m2_inputs(6)
+    y, F, hT = oracle.mamba2_mixer_fwd(**a)
+    sl = lambda v, s: None if v is None else v[:, s]
+    first = dict(a, xBC=a["xBC"][:, :cut], z=sl(a["z"], slice(0, cut)),
+                 dt_raw=a["dt_raw"][:, :cut])
+    y1, F1, h1 = oracle.mamba2_mixer_fwd(**first)
+    second = dict(a, xBC=a["xBC"][:, cut:], z=sl(a["z"], slice(cut, None)),
+                  dt_raw=a["dt_raw"][:, cut:], conv_state=F1, h0=h1)
+    y2, F2, h2 = oracle.mamba2_mixer_fwd(**second)
+    np.testing.assert_allclose(np.concatenate([y1, y2], axis=1), y, rtol=1e-12, atol=1e-13)
+    np.testing.assert_array_equal(F2, F)
+    np.testing.assert_allclose(h2, hT, rtol=1e-12, atol=1e-14)
