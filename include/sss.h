@@ -529,6 +529,47 @@ int sss_mixer_update_path(int L_new, int P, int N, int K, int S_len,
                           sss_dtype act_dtype);
 
 /*
+ * sss_mamba2_mixer_fwd -- one segment of the full Mamba-2 mixer wiring: the
+ * conv with state over every channel of xBC, then the scan with Mamba-2's
+ * discretisation, D skip and gate.  Sources: the Mamba-2 370M-1.3B layers the
+ * length-generalisation study post-trains ("Understanding and Improving
+ * Length Generalization in Recurrent Models", sections 1 and 4.4), whose
+ * mixer convolves x, B and C together before the scan, and "Chapter 7:
+ * state, chunking and incremental inference" for the conv with state.  Per
+ * (batch row b, head h) and token t, with u = SiLU(conv(xBC)) split into
+ * x = u[..., 0:D], B = u[..., D + g N : D + (g+1) N] and
+ * C = u[..., D + G N + g N : D + G N + (g+1) N] (g the head's group):
+ *   dt_t = softplus(dt_raw_t + dt_bias_h),  a_t = exp(dt_t A_h),
+ *   h_t  = a_t h_{t-1} + dt_t x_t B_t^T,
+ *   y_t  = (h_t C_t + D_h x_t) SiLU(z_t).
+ *
+ *  xBC                 [Bz, L, D + 2 G N]  act_dtype, D = H*P
+ *  z                   [Bz, L, D] act_dtype, or NULL (no gate)
+ *  dt_raw              [Bz, L, H] act_dtype (before bias and softplus)
+ *  dt_bias, A, D_skip  [H] float32 (dt_bias / D_skip NULL = 0)
+ *  conv_w, conv_b      [D + 2 G N, K], [D + 2 G N] float32 (conv_b NULL = 0)
+ *  conv_state_in/out   [Bz, D + 2 G N, K-1] act_dtype; may be the same
+ *                      buffer; NULL in = zeros, NULL out = not written
+ *  h0_in / hT_out      [Bz, H, P, N] float32; may be the same buffer
+ *  y                   [Bz, L, H, P] y_dtype
+ *  workspace           caller-owned device buffer of at least
+ *                      sss_mamba2_mixer_fwd_workspace_size() bytes, 16-byte
+ *                      aligned: the fp32 conv output of every channel
+ * The scan runs in fp32 on CUDA cores with the state in registers: B and C
+ * come out of the conv and are not rounded before the scan.  K <= 8,
+ * P <= 128, N <= 256 (else SSS_ERR_UNSUPPORTED).  Asynchronous on `stream`.
+ */
+size_t sss_mamba2_mixer_fwd_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G);
+
+sss_status sss_mamba2_mixer_fwd(const void* xBC, const void* z, sss_dtype act_dtype,
+                                const void* dt_raw, const float* dt_bias, const float* A,
+                                const float* D_skip, const float* conv_w, const float* conv_b,
+                                const void* conv_state_in, void* conv_state_out,
+                                const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
+                                int64_t Bz, int64_t L, int H, int P, int N, int G, int K,
+                                void* workspace, size_t workspace_bytes, sss_stream_t stream);
+
+/*
  * sss_device_status -- read the device status word (OR of SSS_ERR_INDEX /
  * SSS_ERR_TIMEOUT raised by kernels of this library on the current device)
  * after the work on `stream` has finished; clear it when `clear` != 0.

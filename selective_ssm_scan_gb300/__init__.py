@@ -99,6 +99,11 @@ _lib.sss_mixer_update.argtypes = [_p, _i, _p, _p, _p, _i64, _i, _p, _p, _p, _p, 
                                   _i64, _i, _i, _i, _i, _i, _i, _p]
 _lib.sss_mixer_fwd_supported.restype = _i
 _lib.sss_mixer_fwd_supported.argtypes = [_i64, _i64, _i, _i, _i, _i, _i, _i, _i]
+_lib.sss_mamba2_mixer_fwd_workspace_size.restype = ctypes.c_size_t
+_lib.sss_mamba2_mixer_fwd_workspace_size.argtypes = [_i64, _i64, _i, _i, _i, _i]
+_lib.sss_mamba2_mixer_fwd.restype = _i
+_lib.sss_mamba2_mixer_fwd.argtypes = [_p, _p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i,
+                                      _i64, _i64, _i, _i, _i, _i, _i, _p, ctypes.c_size_t, _p]
 _lib.sss_mixer_fwd.restype = _i
 _lib.sss_mixer_fwd.argtypes = [_p, _i, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i64, _i64,
                                _i, _i, _i, _i, _i, _p]
@@ -584,3 +589,38 @@ def device_status(clear: bool = True, stream=None) -> int:
     _check("sss_device_status", _lib.sss_device_status(ctypes.byref(v), int(bool(clear)),
                                                        _stream(stream)))
     return int(v.value)
+
+def mamba2_mixer_fwd_workspace_size(Bz, L, H, P, N, G) -> int:
+    return int(_lib.sss_mamba2_mixer_fwd_workspace_size(Bz, L, H, P, N, G))
+
+
+def mamba2_mixer_fwd(xBC, z, dt_raw, dt_bias, A, D_skip, w, bias, H: int, G: int, N: int,
+                     conv_state=None, h0=None, conv_state_out=None, hT=None, y=None,
+                     y_dtype=None, workspace=None, stream=None):
+    """One segment of the full Mamba-2 mixer wiring (sss_mamba2_mixer_fwd):
+    the conv with state over every channel of xBC [Bz, L, H*P + 2 G N]
+    (x, then B, then C), then per token dt = softplus(dt_raw + dt_bias),
+    h = exp(dt A) h + dt x B^T, y = (h C + D_skip x) SiLU(z).  z, dt_bias,
+    D_skip, bias, conv_state and h0 may be None.  Returns (y, conv_state_out,
+    hT)."""
+    Bz, L, Dt = xBC.shape
+    P = (Dt - 2 * G * N) // H
+    if P < 1 or H * P + 2 * G * N != Dt or w.shape[0] != Dt or dt_raw.shape != (Bz, L, H):
+        raise ValueError("mamba2_mixer_fwd: xBC channels must be H*P + 2*G*N and match w, dt_raw")
+    K = w.shape[1]
+    y_dtype = y_dtype or xBC.dtype
+    if conv_state_out is None:
+        conv_state_out = torch.empty((Bz, Dt, K - 1), dtype=xBC.dtype, device=xBC.device)
+    if hT is None:
+        hT = torch.empty((Bz, H, P, N), dtype=torch.float32, device=xBC.device)
+    if y is None:
+        y = torch.empty((Bz, L, H, P), dtype=y_dtype, device=xBC.device)
+    need = mamba2_mixer_fwd_workspace_size(Bz, L, H, P, N, G)
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=xBC.device)
+    _check("sss_mamba2_mixer_fwd", _lib.sss_mamba2_mixer_fwd(
+        _ptr(xBC), _ptr(z), _dt(xBC), _ptr(dt_raw), _ptr(dt_bias), _ptr(A), _ptr(D_skip),
+        _ptr(w), _ptr(bias), _ptr(conv_state), _ptr(conv_state_out), _ptr(h0), _ptr(hT),
+        _ptr(y), _dt(y), Bz, L, H, P, N, G, K, _ptr(workspace), _nbytes(workspace),
+        _stream(stream)))
+    return y, conv_state_out, hT

@@ -8,6 +8,11 @@ namespace sss {
 
 __device__ int g_status_word;
 
+cudaError_t mamba2_scan_launch(const float* u, const void* z, const void* dt_raw, sss_dtype at,
+                               const float* dt_bias, const float* A, const float* D_skip,
+                               const float* h0, float* hT, void* y, sss_dtype yt, int64_t Bz,
+                               int64_t L, int H, int P, int N, int G, cudaStream_t st);
+bool ssm_scan_simt_supports(int P, int N);
 cudaError_t conv_state_fwd_launch(const void* x, sss_dtype xt, const float* w,
                                   const float* bias, const void* s_in, void* s_out,
                                   void* u, sss_dtype ut, int64_t Bz, int64_t L,
@@ -725,6 +730,65 @@ sss_status sss_device_status(int* status_out, int clear, sss_stream_t stream) {
   if (cudaStreamSynchronize(st) != cudaSuccess) return SSS_ERR_CUDA;
   *status_out = v;
   return SSS_OK;
+}
+
+// ---- the full Mamba-2 mixer wiring ------------------------------------------
+size_t sss_mamba2_mixer_fwd_workspace_size(int64_t Bz, int64_t L, int H, int P, int N, int G) {
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1) return 0;
+  return size_t(Bz) * size_t(L) * size_t(int64_t(H) * P + 2 * int64_t(G) * N) * sizeof(float);
+}
+
+sss_status sss_mamba2_mixer_fwd(const void* xBC, const void* z, sss_dtype act_dtype,
+                                const void* dt_raw, const float* dt_bias, const float* A,
+                                const float* D_skip, const float* conv_w, const float* conv_b,
+                                const void* conv_state_in, void* conv_state_out,
+                                const float* h0_in, float* hT_out, void* y, sss_dtype y_dtype,
+                                int64_t Bz, int64_t L, int H, int P, int N, int G, int K,
+                                void* workspace, size_t workspace_bytes, sss_stream_t stream) {
+  if (!dtype_ok(act_dtype) || !dtype_ok(y_dtype)) return SSS_ERR_INVALID_ARG;
+  if (Bz < 0 || L < 0 || H < 1 || P < 1 || N < 1 || G < 1 || H % G || K < 1)
+    return SSS_ERR_INVALID_ARG;
+  if (K > 8 || !ssm_scan_simt_supports(P, N)) return SSS_ERR_UNSUPPORTED;
+  if (Bz == 0) return SSS_OK;
+  const size_t as = dtype_size(act_dtype), ys = dtype_size(y_dtype);
+  const int64_t Dt = int64_t(H) * P + 2 * int64_t(G) * N;
+  if (!A || !conv_w || !aligned(A, 4) || !aligned(conv_w, 4) || (conv_b && !aligned(conv_b, 4)) ||
+      (dt_bias && !aligned(dt_bias, 4)) || (D_skip && !aligned(D_skip, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if ((conv_state_in && !aligned(conv_state_in, as)) ||
+      (conv_state_out && !aligned(conv_state_out, as)) || (h0_in && !aligned(h0_in, 4)) ||
+      (hT_out && !aligned(hT_out, 4)))
+    return SSS_ERR_INVALID_ARG;
+  if (L > 0) {
+    if (!xBC || !dt_raw || !y || !aligned(xBC, as) || !aligned(dt_raw, as) || !aligned(y, ys) ||
+        (z && !aligned(z, as)))
+      return SSS_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 16) ||
+        workspace_bytes < sss_mamba2_mixer_fwd_workspace_size(Bz, L, H, P, N, G))
+      return SSS_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the conv + SiLU of every xBC channel into the workspace, in fp32 (the
+  // scan reads B and C from it unrounded), and the final conv state
+  if (L > 0 || conv_state_out) {
+    cudaError_t e = conv_state_fwd_launch(xBC, act_dtype, conv_w, conv_b, conv_state_in,
+                                          conv_state_out, L > 0 ? workspace : nullptr, SSS_F32,
+                                          Bz, L, Dt, K, 1, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (L == 0) {
+    // no tokens: the state passes through unchanged
+    if (hT_out && hT_out != h0_in) {
+      const size_t bytes = size_t(Bz) * H * P * N * sizeof(float);
+      const cudaError_t e = h0_in ? cudaMemcpyAsync(hT_out, h0_in, bytes, cudaMemcpyDeviceToDevice, st)
+                                  : cudaMemsetAsync(hT_out, 0, bytes, st);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
+    return SSS_OK;
+  }
+  return from_cuda(mamba2_scan_launch(static_cast<const float*>(workspace), z, dt_raw, act_dtype,
+                                      dt_bias, A, D_skip, h0_in, hT_out, y, y_dtype, Bz, L, H, P,
+                                      N, G, st));
 }
 
 }  // extern "C"

@@ -20,6 +20,9 @@ x ~ N(0,1); B, C ~ N(0,1); dt = softplus(N(0,1) - 2) (already positive);
 A_h ~ -U(0.01, 1) one value per head; conv weight w ~ N(0, 0.5) (variance
 0.5); conv bias = 0.1 for every channel; optional Gaussian initial states
 h0 ~ N(0, 0.1^2) (fp32) and conv state ~ N(0, 1) (activation type).
+Full Mamba-2 wiring: xBC and z ~ N(0,1), dt_raw ~ N(0,1) - 2 (before its bias
+and softplus), dt_bias ~ U(-0.5, 0.5) and D_skip ~ U(0.5, 1.5) per head, conv
+weight ~ N(0, 0.5) and bias 0.1 over every xBC channel.
 Decode pools: conv pool ~ N(0,1), SSM pool ~ N(0, 0.1^2), slot map = the
 first Bz entries of a random permutation of the pool rows, cache_seqlens ~
 integers uniform on [0, 10000).
@@ -42,7 +45,7 @@ import numpy as np
 __all__ = [
     "Arr", "f32", "bf16", "rng", "MixerShape", "DecodeShape", "WORKLOADS",
     "DECODE", "mixer_params", "mixer_segment", "mixer_initial_states",
-    "decode_inputs", "bf16_bits_from_f32", "bf16_bits_to_f64",
+    "decode_inputs", "bf16_bits_from_f32", "bf16_bits_to_f64", "mamba2_inputs",
 ]
 
 
@@ -255,3 +258,37 @@ def decode_inputs(s: DecodeShape) -> Dict[str, Arr]:
 def shrink(s, **kw):
     """Same recipe at other sizes (tests use this for oracle-sized cases)."""
     return s.with_(**kw)
+
+
+def mamba2_inputs(s: MixerShape, seg: int = 0, Bz: Optional[slice] = None) -> Dict[str, Arr]:
+    """Inputs of segment ``seg`` of the full Mamba-2 wiring for the shape of
+    ``s`` (its segment lengths, H, P, N, G, K, dtype): xBC [Bz, Ls, D + 2 G N],
+    z [Bz, Ls, D], dt_raw [Bz, Ls, H]; and, independent of the segment,
+    dt_bias, A, D_skip [H], conv w [D + 2 G N, K], bias [D + 2 G N], conv state
+    [Bz, D + 2 G N, K-1] and h0 [Bz, H, P, N] (zeros unless s.gaussian_init)."""
+    Ls = s.segments[seg]
+    Dt = s.D + 2 * s.G * s.N
+    xBC = rng(s.seed, "m2_xBC", seg).standard_normal((s.Bz, Ls, Dt))
+    z = rng(s.seed, "m2_z", seg).standard_normal((s.Bz, Ls, s.D))
+    dt_raw = rng(s.seed, "m2_dt", seg).standard_normal((s.Bz, Ls, s.H)) - 2.0
+    out = {"xBC": store(xBC, s.dtype), "z": store(z, s.dtype), "dt_raw": store(dt_raw, s.dtype)}
+    if Bz is not None:
+        out = {k: Arr(np.ascontiguousarray(v.data[Bz]), v.dtype) for k, v in out.items()}
+    nb = s.Bz if Bz is None else len(range(*Bz.indices(s.Bz)))
+    rows = slice(0, s.Bz) if Bz is None else Bz
+    if s.gaussian_init:
+        S = rng(s.seed, "m2_conv_state").standard_normal((s.Bz, Dt, s.K - 1))[rows]
+        h0 = rng(s.seed, "m2_h0").normal(0.0, 0.1, size=(s.Bz, s.H, s.P, s.N))[rows]
+    else:
+        S = np.zeros((nb, Dt, s.K - 1))
+        h0 = np.zeros((nb, s.H, s.P, s.N))
+    out.update({
+        "dt_bias": f32(rng(s.seed, "m2_dt_bias").uniform(-0.5, 0.5, s.H)),
+        "A": f32(-rng(s.seed, "A").uniform(0.01, 1.0, size=s.H)),
+        "D_skip": f32(rng(s.seed, "m2_D").uniform(0.5, 1.5, s.H)),
+        "w": f32(rng(s.seed, "m2_w").normal(0.0, np.sqrt(0.5), size=(Dt, s.K))),
+        "bias": f32(np.full(Dt, 0.1)),
+        "conv_state": store(S, s.dtype),
+        "h0": f32(h0),
+    })
+    return out

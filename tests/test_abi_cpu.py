@@ -193,3 +193,36 @@ def test_span_forward_host_checks(lib):
     assert call(args(L=8, ns=4)) == 1                # 2-token spans < K - 1
     assert call(args(xt=7)) == 1                     # unknown dtype
     assert call(args(G=5)) == 1                      # H not a multiple of G
+
+
+def test_mamba2_forward_host_checks(lib):
+    """Workspace size and the argument checks of the full Mamba-2 forward that
+    return before any launch."""
+    i64, ci, Pp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+    ws = lib.sss_mamba2_mixer_fwd_workspace_size
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [i64, i64, ci, ci, ci, ci]
+    Bz, L, H, P, N, G, K = 2, 100, 4, 16, 32, 2, 4
+    # the fp32 conv output of every xBC channel
+    assert ws(Bz, L, H, P, N, G) == 4 * Bz * L * (H * P + 2 * G * N)
+    assert ws(Bz, 0, H, P, N, G) == 0
+    f = lib.sss_mamba2_mixer_fwd
+    f.restype = ci
+    f.argtypes = [Pp, Pp, ci, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, Pp, ci, i64, i64, ci, ci,
+                  ci, ci, ci, Pp, ctypes.c_size_t, Pp]
+    a = lambda k: ctypes.c_void_p(0x10000000 * k)  # aligned stand-ins, never dereferenced
+    need = ws(Bz, L, H, P, N, G)
+    base = dict(xBC=a(1), z=a(2), at=1, dtr=a(3), dtb=a(4), A=a(5), Dsk=a(6), w=a(7), b=a(8),
+                s_in=a(9), s_out=a(9), h0=a(10), hT=a(10), y=a(11), yt=1, Bz=Bz, L=L, H=H, P=P,
+                N=N, G=G, K=K, ws=a(12), wsb=need, st=None)
+    call = lambda **kw: f(*dict(base, **kw).values())
+    INVALID, UNSUPPORTED = 1, 2
+    assert call(xBC=None) == INVALID                 # tokens but no input
+    assert call(A=None) == INVALID
+    assert call(ws=None) == INVALID                  # no workspace
+    assert call(wsb=need - 4) == INVALID             # workspace too small
+    assert call(at=7) == INVALID                     # unknown dtype
+    assert call(H=3) == INVALID                      # H not a multiple of G
+    assert call(K=9) == UNSUPPORTED                  # conv wider than 8
+    assert call(P=200) == UNSUPPORTED                # head dim beyond the scan's
+    assert call(Bz=0) == 0                           # nothing to do
