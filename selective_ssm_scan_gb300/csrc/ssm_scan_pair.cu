@@ -114,9 +114,9 @@ constexpr uint32_t kOffMisc = kOffXs + kXsBytes;  // 213376
 // misc (offsets from kOffMisc)
 constexpr uint32_t kMiInfo = 0;       // 4 piece descriptors
 constexpr uint32_t kMiRed = 4224;     // (unused)
-// conv weights and bias, per (head hs, channel pair e2, channel group q) 12
-// floats: the taps of channels 8q + 2e2 and 8q + 2e2 + 1 interleaved (tap k of
-// the pair = floats 2k, 2k+1), the two biases, 2 pad.  The 48-byte stride puts
+// conv weights and bias times -log2(e), per (head hs, channel pair e2, channel
+// group q) 12 floats: the taps of channels 8q + 2e2 and 8q + 2e2 + 1 interleaved
+// (tap k of the pair = floats 2k, 2k+1), the two biases, 2 pad.  The 48-byte stride puts
 // the 8 groups a warp reads on distinct banks.
 constexpr uint32_t kMiW = 4480;       // [2][4][8][12] floats
 constexpr uint32_t kMiBars = 7552;    // mbarriers
@@ -190,19 +190,18 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) {
   return pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
-// SiLU of a pair, times g: z / (1 + e^-z) * g, with e^-z = 2^(-z log2 e).
-// One reciprocal serves the pair (1 / (d_a d_b), times d_b and d_a): the
-// reciprocal is the slowest multi-function unit operation (half the rate of
-// ex2), and that unit is the producers' busiest pipe.  The exponent is capped
-// at 60 so that d_a d_b <= 2^120 stays finite; beyond it SiLU(z) is below
-// 2^-60 |z| either way.
-__device__ __forceinline__ uint64_t silu_scaled2(uint64_t z, float g) {
+constexpr float kLn2 = 0.6931471805599453f;
+// SiLU of a pair, times g, from z' = -z log2(e) (the conv's weights and bias
+// carry the factor -log2(e), so the conv yields z' directly):
+//   SiLU(z) g = z g / (1 + e^-z) = (z' gn) / (1 + 2^z'),  gn = -ln(2) g.
+// One reciprocal per channel: a large z' gives 2^z' = inf and a zero, which
+// is SiLU's limit there (no cap on the exponent is needed).
+__device__ __forceinline__ uint64_t silu_scaled2(uint64_t zp, float gn) {
   float ta, tb;
-  upk2(mul2(z, pk2(-kLog2e, -kLog2e)), ta, tb);
+  upk2(zp, ta, tb);
   float da, db;
-  upk2(add2(pk2(ex2f(fminf(ta, 60.0f)), ex2f(fminf(tb, 60.0f))), pk2(1.0f, 1.0f)), da, db);
-  const float r = rcpf(da * db) * g;
-  return mul2(z, mul2(pk2(db, da), pk2(r, r)));
+  upk2(add2(pk2(ex2f(ta), ex2f(tb)), pk2(1.0f, 1.0f)), da, db);
+  return mul2(mul2(zp, pk2(gn, gn)), pk2(rcpf(da), rcpf(db)));
 }
 // a packed pair -> one bf16 pair word (round to nearest even, element 0 low)
 __device__ __forceinline__ uint32_t bf2_pack(uint64_t v) {
@@ -330,8 +329,8 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     // taps right-aligned in a window of kMaxK (leading zero weights for K < kMaxK)
 #pragma unroll
     for (int k = 0; k < kMaxK; ++k)
-      sw[2 * k + odd] = k >= kMaxK - K ? conv_w[d * K + k - (kMaxK - K)] : 0.0f;
-    sw[8 + odd] = conv_b ? conv_b[d] : 0.0f;
+      sw[2 * k + odd] = k >= kMaxK - K ? -kLog2e * conv_w[d * K + k - (kMaxK - K)] : 0.0f;
+    sw[8 + odd] = conv_b ? -kLog2e * conv_b[d] : 0.0f;
     sw[10 + odd] = 0.0f;
   }
   tc_fence_before();
@@ -371,11 +370,12 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         const int head = 2 * pair + hs;
         const int nv = ok ? min(NT, max(0, n - tb)) : 0;  // live tokens of this thread
         const float R = inf->R[hs];
-        // x' = g_s x with g_s = exp(R - Lam_s), 0 for dead tokens
+        // x' = g_s x with g_s = exp(R - Lam_s), 0 for dead tokens (fused:
+        // times -ln 2, the factor SiLU takes from z')
         float gv[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j)
-          gv[j] = j < nv ? ex2f((R - inf->lam[hs][tb + j]) * kLog2e) : 0.0f;
+          gv[j] = j < nv ? (FUSED ? -kLn2 : 1.0f) * ex2f((R - inf->lam[hs][tb + j]) * kLog2e) : 0.0f;
         uint32_t(&hw)[NT][4] = hw2[hs];
         uint32_t(&lw)[NT][4] = lw2[hs];
         if constexpr (!FUSED) {
