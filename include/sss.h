@@ -149,7 +149,7 @@ sss_status sss_conv_state_bwd(const void* x, sss_dtype x_dtype, const float* w,
  *
  *  - Size limit: it serves calls whose sss_conv_state_bwd_workspace_size()
  *    is at most SSS_CONV_BWD_NOALLOC_SCRATCH_BYTES (8 MiB: for example
- *    Bz = 64 sequences of 1024 tokens at D = 2048, K = 4 need 5 MiB)
+ *    Bz = 32 sequences of 1024 tokens at D = 2048, K = 4 need 5 MiB)
  *    and returns SSS_ERR_UNSUPPORTED, before anything is launched, for
  *    larger ones.  Other errors are those of sss_conv_state_bwd.
  *  - Memory: every GPU that loads the library holds the 8 MiB array until

@@ -26,6 +26,8 @@
 //    shared memory and writes one row of partials to the workspace; a second
 //    kernel adds the rows in a fixed order, so the result is deterministic.
 #include "common.cuh"
+#include "scan_tc_util.cuh"
+#include "tc_ptx.cuh"
 
 namespace sss {
 
@@ -217,6 +219,269 @@ conv_state_bwd_kernel(const TX* __restrict__ x, const float* __restrict__ w,
   }
 }
 
+// ---- K = 4 fast path -----------------------------------------------------------
+// The same walk for the common width K = 4 with a channel pair per lane (D a
+// multiple of 64, 16-byte aligned rows) in packed f32x2 arithmetic.  The rows
+// reach a warp through shared memory: each warp keeps a ring of kK4Stages
+// groups of 4 tokens (its 64 channels of x and dy per token), filled by
+// cp.async.bulk row copies that one lane issues kK4Stages groups ahead, so
+// ~16 tokens per warp are in flight without holding registers.  A step is
+// then only its arithmetic: the window turns over every 4 steps (the unrolled
+// group), so no register moves; the first group (the state gradient in tile
+// 0), the look-ahead group (three steps past the tile that only finish dx)
+// and the sequence's last tile (masks, the direct path from F) are the only
+// special cases.
+namespace {
+constexpr float kLog2eB = 1.4426950408889634f;
+constexpr int kK4Warps = 4;                       // warps per CTA
+constexpr int kK4Tile = 64;                       // tokens per warp
+constexpr int kK4CtaTokens = kK4Warps * kK4Tile;  // tokens per row of partial sums
+constexpr int kK4Stages = 4;                      // groups of 4 tokens in flight per warp
+
+__device__ __forceinline__ float ex2a(float v) {  // 2^v, approximate
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+__device__ __forceinline__ float rcpa(float v) {  // 1 / v, approximate
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+// SiLU'(z) of a channel pair: s (1 + z (1 - s)) with s = 1 / (1 + 2^(-z log2 e));
+// a very negative z gives 2^(..) = inf and s = 0, the limit.
+__device__ __forceinline__ uint64_t dsilu2(uint64_t z) {
+  float ta, tb;
+  upk2(mul2(z, pk2(-kLog2eB, -kLog2eB)), ta, tb);
+  float da, db;
+  upk2(add2(pk2(ex2a(ta), ex2a(tb)), pk2(1.0f, 1.0f)), da, db);
+  const uint64_t sg = pk2(rcpa(da), rcpa(db));
+  const uint64_t oms = fma2(sg, pk2(-1.0f, -1.0f), pk2(1.0f, 1.0f));
+  return mul2(sg, fma2(z, oms, pk2(1.0f, 1.0f)));
+}
+
+// a channel pair as a packed fp32 pair, and back
+template <typename T> struct Pair;
+template <> struct Pair<float> {
+  using Raw = uint64_t;
+  static __device__ __forceinline__ Raw load(const float* p) {
+    return __ldg(reinterpret_cast<const unsigned long long*>(p));
+  }
+  static __device__ __forceinline__ uint64_t f2(Raw r) { return r; }
+  static __device__ __forceinline__ void store(float* p, uint64_t v) {
+    *reinterpret_cast<uint64_t*>(p) = v;
+  }
+};
+template <> struct Pair<__nv_bfloat16> {
+  using Raw = uint32_t;
+  static __device__ __forceinline__ Raw load(const __nv_bfloat16* p) {
+    return __ldg(reinterpret_cast<const unsigned int*>(p));
+  }
+  static __device__ __forceinline__ uint64_t f2(Raw r) {
+    return pk2(__uint_as_float(r << 16), __uint_as_float(r & 0xFFFF0000u));
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, uint64_t v) {
+    float a, b;
+    upk2(v, a, b);
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    *reinterpret_cast<__nv_bfloat162*>(p) = h;
+  }
+};
+
+template <typename TX, typename TD>
+__host__ __device__ constexpr int k4_ring_bytes() {  // per warp: stages x 4 tokens x (x row + dy row)
+  return kK4Stages * 4 * 64 * int(sizeof(TX) + sizeof(TD));
+}
+}  // namespace
+
+template <typename TX, typename TD, typename TO, bool SILU>
+__global__ void __launch_bounds__(kK4Warps * 32, 7)
+conv_bwd_k4_kernel(const TX* __restrict__ x, const float* __restrict__ w,
+                   const float* __restrict__ bias, const TX* __restrict__ s_in,
+                   const TD* __restrict__ dy, const TD* __restrict__ q, TO* __restrict__ dx,
+                   TO* __restrict__ dS, float* __restrict__ part, int L, int D, int n_groups,
+                   int* status) {
+  using namespace tc;
+  using tcs::kWaitNs;
+  using PX = Pair<TX>;
+  using PD = Pair<TD>;
+  using PO = Pair<TO>;
+  constexpr int K = 4, TT = kK4Tile, NG = TT / 4;   // groups NG: the look-ahead group
+  constexpr uint32_t RX = 64 * sizeof(TX), RD = 64 * sizeof(TD);  // row bytes of a warp
+  constexpr uint32_t GB = 4 * (RX + RD);                          // bytes of a group
+  extern __shared__ __align__(128) uint8_t k4_smem[];
+  __shared__ __align__(8) uint64_t bars[kK4Warps][kK4Stages];
+  __shared__ float red[kK4Warps][K + 1][64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c0 = blockIdx.x * 64;      // the CTA's 64 channels
+  const int d0 = c0 + 2 * lane;        // this lane's channel pair
+  const int tg = blockIdx.y;
+  const int64_t b = blockIdx.z;
+  const int t0 = (tg * kK4Warps + warp) * TT;
+  uint8_t* ring = k4_smem + warp * k4_ring_bytes<TX, TD>();
+  const uint32_t ring_s = smem_u32(ring);
+  uint64_t dw0 = 0, dw1 = 0, dw2 = 0, dw3 = 0, dbs = 0;  // packed zeros
+
+  if (t0 < L) {
+    if (lane == 0) {
+#pragma unroll
+      for (int st = 0; st < kK4Stages; ++st) mbar_init(smem_u32(&bars[warp][st]), 1);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    // group gi (tokens t0 + 4 gi .. + 3) into ring stage gi % kK4Stages; rows
+    // at or past L are not copied (their values are masked at use)
+    auto issue = [&](int gi) {
+      const int st = gi % kK4Stages;
+      const uint32_t bar = smem_u32(&bars[warp][st]);
+      const int j0 = t0 + 4 * gi;
+      const int nrow = min(4, L - j0);
+      if (nrow <= 0) {
+        mbar_arrive(bar);
+        return;
+      }
+      mbar_arrive_expect_tx(bar, uint32_t(nrow) * (RX + RD));
+      const uint32_t gs = ring_s + uint32_t(st) * GB;
+      for (int i = 0; i < nrow; ++i) {
+        bulk_load(gs + uint32_t(i) * RX, x + (b * L + j0 + i) * D + c0, RX, bar);
+        bulk_load(gs + 4 * RX + uint32_t(i) * RD, dy + (b * L + j0 + i) * D + c0, RD, bar);
+      }
+    };
+    if (lane == 0) {
+#pragma unroll
+      for (int gi = 0; gi < kK4Stages; ++gi)
+        if (gi <= NG) issue(gi);
+    }
+    const uint64_t wk0 = pk2(w[d0 * K + 0], w[(d0 + 1) * K + 0]);
+    const uint64_t wk1 = pk2(w[d0 * K + 1], w[(d0 + 1) * K + 1]);
+    const uint64_t wk2 = pk2(w[d0 * K + 2], w[(d0 + 1) * K + 2]);
+    const uint64_t wk3 = pk2(w[d0 * K + 3], w[(d0 + 1) * K + 3]);
+    const uint64_t bs = bias ? pk2(bias[d0], bias[d0 + 1]) : 0ull;
+    // x of tokens t0-3 .. t0-1 (the conv state before token 0, zeros without one)
+    auto x_at = [&](int t) -> uint64_t {
+      if (t >= 0) return PX::f2(PX::load(x + (b * L + t) * D + d0));
+      if (!s_in) return 0ull;
+      return pk2(to_f32(s_in[(b * D + d0) * (K - 1) + (K - 1) + t]),
+                 to_f32(s_in[(b * D + d0 + 1) * (K - 1) + (K - 1) + t]));
+    };
+    uint64_t xm3 = x_at(t0 - 3), xm2 = x_at(t0 - 2), xm1 = x_at(t0 - 1);
+    uint64_t dm3 = 0ull, dm2 = 0ull, dm1 = 0ull;  // delta of the three steps before
+
+    // step j: z_j, delta_j, the tile's dw / dbias terms, and du of token j - 3
+    auto step = [&](uint64_t xj, uint64_t gj, bool acc) -> uint64_t {
+      const uint64_t z = fma2(wk3, xj, fma2(wk2, xm1, fma2(wk1, xm2, fma2(wk0, xm3, bs))));
+      const uint64_t dl = SILU ? mul2(gj, dsilu2(z)) : gj;
+      if (acc) {
+        dbs = add2(dbs, dl);
+        dw0 = fma2(dl, xm3, dw0);
+        dw1 = fma2(dl, xm2, dw1);
+        dw2 = fma2(dl, xm1, dw2);
+        dw3 = fma2(dl, xj, dw3);
+      }
+      const uint64_t o = fma2(wk0, dl, fma2(wk1, dm1, fma2(wk2, dm2, mul2(wk3, dm3))));
+      xm3 = xm2;
+      xm2 = xm1;
+      xm1 = xj;
+      dm3 = dm2;
+      dm2 = dm1;
+      dm1 = dl;
+      return o;
+    };
+    auto store_dx = [&](int t, uint64_t o) { PO::store(dx + (b * L + t) * D + d0, o); };
+    auto store_ds = [&](int j, uint64_t o) {  // u index j < K - 1: the state's gradient
+      float a, c;
+      upk2(o, a, c);
+      dS[(b * D + d0) * (K - 1) + j] = from_f32<TO>(a);
+      dS[(b * D + d0 + 1) * (K - 1) + j] = from_f32<TO>(c);
+    };
+    const bool last_tile = t0 + TT + 3 >= L;  // masks and the direct path from F
+#pragma unroll 1
+    for (int g = 0; g <= NG; ++g) {
+      const int st = g % kK4Stages;
+      if (!mbar_wait(smem_u32(&bars[warp][st]), uint32_t((g / kK4Stages) & 1), kWaitNs)) {
+        raise_status(status, SSS_ERR_TIMEOUT);
+        break;
+      }
+      const uint8_t* gs = ring + st * GB;
+      typename PX::Raw xr[4];
+      typename PD::Raw gr[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xr[i] = *reinterpret_cast<const typename PX::Raw*>(gs + i * RX + lane * sizeof(typename PX::Raw));
+        gr[i] = *reinterpret_cast<const typename PD::Raw*>(gs + 4 * RX + i * RD +
+                                                           lane * sizeof(typename PD::Raw));
+      }
+      // the stage is read: refill it with group g + kK4Stages (the fence
+      // orders the warp's generic reads before the async copy's writes)
+      __syncwarp();
+      if (lane == 0 && g + kK4Stages <= NG) {
+        fence_proxy_async_smem();
+        issue(g + kK4Stages);
+      }
+      if (!last_tile) {
+        if (g == 0) {
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            const uint64_t o = step(PX::f2(xr[i]), PD::f2(gr[i]), true);
+            if (t0 == 0) store_ds(i, o);
+          }
+          store_dx(t0, step(PX::f2(xr[3]), PD::f2(gr[3]), true));
+        } else if (g < NG) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            store_dx(t0 + 4 * g + i - 3, step(PX::f2(xr[i]), PD::f2(gr[i]), true));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 3; ++i)
+            store_dx(t0 + TT + i - 3, step(PX::f2(xr[i]), PD::f2(gr[i]), false));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int sidx = 4 * g + i;
+          if (sidx >= TT + 3) break;
+          const int j = t0 + sidx;
+          const bool in = j < L;
+          const uint64_t xj = in ? PX::f2(xr[i]) : 0ull;
+          const uint64_t gj = in ? PD::f2(gr[i]) : 0ull;
+          uint64_t o = step(xj, gj, sidx < TT);
+          const int t = j - 3;
+          if (t < t0) {
+            if (t0 == 0) store_ds(j, o);
+          } else if (t < L) {
+            if (q && t >= L - (K - 1)) {
+              const int f = t - (L - (K - 1));
+              o = add2(o, pk2(to_f32(q[(b * D + d0) * (K - 1) + f]),
+                              to_f32(q[(b * D + d0 + 1) * (K - 1) + f])));
+            }
+            store_dx(t, o);
+          }
+        }
+      }
+    }
+  }
+
+  // the CTA's tiles summed in shared memory, in warp order: one row of
+  // partial sums per CTA (the same [D][K+1] layout as the general kernel)
+  {
+    float a, c;
+    upk2(dw0, a, c); red[warp][0][2 * lane] = a; red[warp][0][2 * lane + 1] = c;
+    upk2(dw1, a, c); red[warp][1][2 * lane] = a; red[warp][1][2 * lane + 1] = c;
+    upk2(dw2, a, c); red[warp][2][2 * lane] = a; red[warp][2][2 * lane + 1] = c;
+    upk2(dw3, a, c); red[warp][3][2 * lane] = a; red[warp][3][2 * lane + 1] = c;
+    upk2(dbs, a, c); red[warp][4][2 * lane] = a; red[warp][4][2 * lane + 1] = c;
+  }
+  __syncthreads();
+  float* row = part + (b * n_groups + tg) * int64_t(D) * (K + 1);
+  for (int e = threadIdx.x; e < 64 * (K + 1); e += blockDim.x) {
+    const int c = e / (K + 1), k = e % (K + 1);
+    float acc = 0.0f;
+#pragma unroll
+    for (int ww = 0; ww < kK4Warps; ++ww) acc += red[ww][k][c];
+    row[int64_t(c0 + c) * (K + 1) + k] = acc;
+  }
+}
+
 // dw[d][k] = sum over rows of part[row][d][k] (k < K); dbias[d] = part[..][d][K].
 // A CTA takes 32 consecutive entries; warp w adds rows w, w+8, ... in order,
 // then the 8 warp sums are added in warp order (a fixed order for given sizes).
@@ -267,7 +532,10 @@ __global__ void conv_bwd_empty_kernel(const TD* __restrict__ q, TO* __restrict__
 
 size_t conv_state_bwd_workspace(int64_t Bz, int64_t L, int64_t D, int K) {
   if (Bz <= 0 || L <= 0 || D <= 0 || K < 1) return 0;
-  const int64_t groups = (L + kBwdCtaTokens - 1) / kBwdCtaTokens;
+  // one row of partial sums per CTA row of tokens (the K = 4 walk's rows are
+  // shorter; its size covers the general kernel's too)
+  const int64_t rows_tokens = K == 4 ? kK4CtaTokens : kBwdCtaTokens;
+  const int64_t groups = (L + rows_tokens - 1) / rows_tokens;
   return size_t(Bz * groups * D * (K + 1)) * sizeof(float);
 }
 
@@ -305,6 +573,34 @@ static cudaError_t launch_bwd(const void* x, const float* w, const float* bias, 
 }
 
 template <typename TX, typename TD, typename TO>
+static cudaError_t launch_k4(const void* x, const float* w, const float* bias, const void* s_in,
+                             const void* dy, const void* q, void* dx, void* dS, float* dw,
+                             float* dbias, int64_t Bz, int64_t L, int64_t D, int silu_on,
+                             void* ws, cudaStream_t st) {
+  const int64_t groups = (L + kK4CtaTokens - 1) / kK4CtaTokens;
+  if (groups > 65535 || Bz > 65535) return cudaErrorInvalidValue;
+  const dim3 grid(unsigned(D / 64), unsigned(groups), unsigned(Bz));
+  const int smem = kK4Warps * k4_ring_bytes<TX, TD>();
+  float* part = static_cast<float*>(ws);
+  auto args = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kK4Warps * 32, smem, st>>>(
+        static_cast<const TX*>(x), w, bias, static_cast<const TX*>(s_in),
+        static_cast<const TD*>(dy), static_cast<const TD*>(q), static_cast<TO*>(dx),
+        static_cast<TO*>(dS), part, int(L), int(D), int(groups), status_word());
+    return cudaGetLastError();
+  };
+  cudaError_t e = silu_on ? args(conv_bwd_k4_kernel<TX, TD, TO, true>)
+                          : args(conv_bwd_k4_kernel<TX, TD, TO, false>);
+  if (e != cudaSuccess) return e;
+  const int64_t n = D * 5;
+  conv_bwd_reduce_kernel<<<unsigned((n + 31) / 32), 256, 0, st>>>(part, dw, dbias, Bz * groups,
+                                                                  int(D), 4);
+  return cudaGetLastError();
+}
+
+template <typename TX, typename TD, typename TO>
 static cudaError_t bwd_vec(const void* x, const float* w, const float* bias, const void* s_in,
                            const void* dy, const void* q, void* dx, void* dS, float* dw,
                            float* dbias, int64_t Bz, int64_t L, int64_t D, int K, int silu_on,
@@ -322,6 +618,12 @@ static cudaError_t bwd_vec(const void* x, const float* w, const float* bias, con
   auto al2 = [](const void* p, size_t es) {
     return (reinterpret_cast<uintptr_t>(p) % (2 * es)) == 0;
   };
+  // the K = 4 walk copies whole 64-channel rows with cp.async.bulk: 16-byte
+  // aligned x and dy
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; };
+  if (K == 4 && D % 64 == 0 && L >= K - 1 && al16(x) && al16(dy) && al2(dx, sizeof(TO)))
+    return launch_k4<TX, TD, TO>(x, w, bias, s_in, dy, q, dx, dS, dw, dbias, Bz, L, D, silu_on,
+                                 ws, st);
   if (D % 2 == 0 && al2(x, sizeof(TX)) && al2(dy, sizeof(TD)) && al2(dx, sizeof(TO)))
     return launch_bwd<TX, TD, TO, 2>(x, w, bias, s_in, dy, q, dx, dS, dw, dbias, Bz, L, D, K,
                                      silu_on, ws, st);

@@ -65,6 +65,25 @@ def test_conv_bwd_fp32_parity(Bz, L, D, K, silu):
     assert_rel(f64(db), db_r, F32_REL, "dbias")
 
 
+@pytest.mark.parametrize("L", [3, 4, 63, 64, 66, 67, 68, 131, 512, 515, 577, 1091])
+@pytest.mark.parametrize("D,silu,state,dstate", [
+    (64, True, True, True), (128, False, True, True), (64, True, False, False),
+    (192, True, True, False)])
+def test_conv_bwd_k4_tiles_parity(L, D, silu, state, dstate):
+    """K = 4 with D a multiple of 64 (the channel-pair walk): the first tile's
+    state gradient, interior tiles, the look-ahead past a tile's end, the last
+    tile's masks and the direct gradient of F, at lengths around the 64-token
+    tile and the 512-token CTA row."""
+    x, w, bias, S, dy, q = _case(101 * L + D, 2, L, D, 4, "f32", "f32", state=state,
+                                 dstate=dstate)
+    dx_r, dS_r, dw_r, db_r = oracle.conv_state_bwd(x, w, bias, S, dy, q, apply_silu=silu)
+    dx, dS, dw, db = _run(x, w, bias, S, dy, q, "f32", silu)
+    assert_rel(f64(dx), dx_r, F32_REL, "dx")
+    assert_rel(f64(dS), dS_r, F32_REL, "dS")
+    assert_rel(f64(dw), dw_r, F32_REL, "dw")
+    assert_rel(f64(db), db_r, F32_REL, "dbias")
+
+
 @pytest.mark.parametrize("dydt,dxdt", [("f32", "bf16"), ("bf16", "bf16"), ("f32", "f32")])
 @pytest.mark.parametrize("L", [3, 300])
 def test_conv_bwd_bf16_parity(dydt, dxdt, L):

@@ -71,7 +71,7 @@ def _compare(got, ref, bf16_out):
 
 def test_noalloc_matches_workspace_entry_point_on_two_calls_in_a_row():
     # first call: a full 1024-token segment of the Mamba-2 370M-like layer
-    # (0.6 MiB of partial sums); second call: a smaller ragged fp32 case that
+    # (1.3 MiB of partial sums); second call: a smaller ragged fp32 case that
     # reads only part of what the first call left in the scratch
     cases = [((1, 8, 1024, 2048, 4), "bf16", "f32", torch.bfloat16),
              ((2, 3, 301, 96, 4), "f32", "f32", torch.float32)]
