@@ -95,8 +95,10 @@ def test_conv_backward_host_checks(lib):
     ws = lib.sss_conv_state_bwd_workspace_size
     ws.restype = ctypes.c_size_t
     ws.argtypes = [i64, i64, i64, ctypes.c_int]
-    # one row of D * (K+1) fp32 partial sums per sequence and 512-token group
-    assert ws(8, 1024, 2048, 4) == 8 * 2 * 2048 * 5 * 4
+    # one row of D * (K+1) fp32 partial sums per sequence and token group:
+    # 256 tokens for K = 4 (the channel-pair walk's CTA rows), 512 otherwise
+    assert ws(8, 1024, 2048, 4) == 8 * 4 * 2048 * 5 * 4
+    assert ws(2, 257, 64, 4) == 2 * 2 * 64 * 5 * 4
     assert ws(2, 513, 10, 3) == 2 * 2 * 10 * 4 * 4
     assert ws(2, 0, 10, 3) == 0
     f = lib.sss_conv_state_bwd
