@@ -547,58 +547,52 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
       }
       if (tid == 0) raise_status(status, SSS_ERR_INDEX);
     } else {
-      // ---- conv of channel h*P + tid over the slot tile, reads before writes
-      if (tid < P) {
-        const T* row = reinterpret_cast<const T*>(stg + geo.cv) + tid * S_len;
+      // ---- conv over the slot tile: one (token i, channel c) per thread, so
+      // the L_new tokens' convs run side by side.  Every read is of the
+      // shared-memory copy of the pool row (the history) or of the new rows,
+      // and every write goes to the pool in global memory: no read sees a write.
+      {
         const T* xs = reinterpret_cast<const T*>(stg + geo.xs);
-        const float* wr = reinterpret_cast<const float*>(stg + geo.ws) + tid * K;
-        // slot of logical position p0: one 32-bit modulo; history slots are
-        // p0 - (K-1) + j with K-1 <= S_len, so one wrap at most
-        const int base = p0 % S_len;
-        float win[KT - 1];
+        const T* tile = reinterpret_cast<const T*>(stg + geo.cv);
+        const int base = p0 % S_len;  // slot of logical position p0
+        for (int e = tid; e < L_new * P; e += kPipeWarps * 32) {
+          const int i = e / P, c = e - (e / P) * P;
+          const T* row = tile + c * S_len;
+          const float* wr = reinterpret_cast<const float*>(stg + geo.ws) + c * K;
+          float z = geo.n_bi ? reinterpret_cast<const float*>(stg + geo.bi)[c] : 0.0f;
+          // taps 0 .. K-2 read logical positions p0 + i - (K-1) + kk: a new
+          // row when that is >= p0, else a history slot (one wrap at most)
 #pragma unroll
-        for (int j = 0; j < KT - 1; ++j) {
-          int sl = base - (K - 1) + j;
-          sl += sl < 0 ? S_len : 0;
-          win[j] = (j < K - 1) ? to_f32(row[sl]) : 0.0f;
-        }
-        float wk[KT];
-#pragma unroll
-        for (int kk = 0; kk < KT; ++kk) wk[kk] = kk < K ? wr[kk] : 0.0f;
-        const float bsd = geo.n_bi ? reinterpret_cast<const float*>(stg + geo.bi)[tid] : 0.0f;
-#pragma unroll
-        for (int i = 0; i < LT; ++i) {
-          if (i < L_new) {
-            const float xv = to_f32(xs[i * P + tid]);
-            float z = bsd;
-#pragma unroll
-            for (int kk = 0; kk < KT - 1; ++kk)
-              if (kk < K - 1) z = fmaf(wk[kk], win[kk], z);
-#pragma unroll
-            for (int kk = 0; kk < KT; ++kk)
-              if (kk == K - 1) z = fmaf(wk[kk], xv, z);
-            ms->us[i][tid] = silu(z);
-#pragma unroll
-            for (int kk = 0; kk < KT - 2; ++kk)
-              if (kk < K - 2) win[kk] = win[kk + 1];
-#pragma unroll
-            for (int kk = 0; kk < KT - 1; ++kk)
-              if (kk == K - 2) win[kk] = xv;
+          for (int kk = 0; kk < KT - 1; ++kk) {
+            if (kk < K - 1) {
+              const int rel = i - (K - 1) + kk;
+              float v;
+              if (rel >= 0) {
+                v = to_f32(xs[rel * P + c]);
+              } else {
+                int sl = base + rel;
+                sl += sl < 0 ? S_len : 0;
+                v = to_f32(row[sl]);
+              }
+              z = fmaf(wr[kk], v, z);
+            }
           }
+          z = fmaf(wr[K - 1], to_f32(xs[i * P + c]), z);
+          ms->us[i][c] = silu(z);
+          // the new input goes to the pool row: at the write pointer, or
+          // (non-circular) the row shifted by L_new with the inputs appended
+          T* grow = conv_pool + (int64_t(ms->row[s]) * D + int64_t(h) * P + c) * S_len;
+          // (when L_new > S_len two tokens share a slot: the later one's
+          // input is the one that stays, so only the last S_len tokens write)
+          if (seqlens && i + S_len >= L_new) grow[(base + i) % S_len] = xs[i * P + c];
         }
-        // the new inputs go to the pool row directly (the tile in shared
-        // memory is only read): at the write pointer, or (non-circular) the
-        // row shifted by L_new with the new inputs appended
-        T* grow = conv_pool + (int64_t(ms->row[s]) * D + int64_t(h) * P + tid) * S_len;
-        if (seqlens) {
-          int sl = base;
-          for (int i = 0; i < L_new; ++i) {
-            grow[sl] = xs[i * P + tid];
-            sl = sl + 1 == S_len ? 0 : sl + 1;
+        if (!seqlens) {
+          for (int e = tid; e < S_len * P; e += kPipeWarps * 32) {
+            const int j = e / P, c = e - (e / P) * P;
+            const T* row = tile + c * S_len;
+            T* grow = conv_pool + (int64_t(ms->row[s]) * D + int64_t(h) * P + c) * S_len;
+            grow[j] = j + L_new < S_len ? row[j + L_new] : xs[(j + L_new - S_len) * P + c];
           }
-        } else {
-          for (int j = 0; j < S_len; ++j)
-            grow[j] = j + L_new < S_len ? row[j + L_new] : xs[(j + L_new - S_len) * P + tid];
         }
       }
       tc::role_sync(1, kPipeWarps * 32);
