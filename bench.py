@@ -71,6 +71,15 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def tensor_peak() -> float:
+    """Measured dense bf16 TFLOP/s (burst), else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def kernel_source_hash(kernel: str) -> str:
     """sha256 (first 16 hex digits) of the kernel's .cu file followed by every
     local header it includes, directly or through another header, in the
@@ -365,6 +374,18 @@ def main():
     Q = 128
     tc_flops = s.Bz * s.H * (-(-L // Q)) * 2 * Q * (Q * s.N + Q * s.P + 2 * s.P * s.N)
     roofline["tensor_useful_tflops"] = tc_flops / (launch_ms * 1e-3) / 1e12
+    # the same kernel against the tensor roofline: the MMAs it issues (per
+    # 128-token piece and head pair 64 MMAs of 128x128x16 -- G 8, S' 16, Yo 16,
+    # Yd 24, the hi/lo split terms included) over the launch time, against the
+    # measured dense bf16 peak (burst: the kernel is timed alone)
+    issued = (s.Bz * (s.H // 2)) * (-(-L // Q)) * 64 * 2 * 128 * 128 * 16
+    bf16_peak = tensor_peak()
+    roofline["tensor"] = {"issued_tflop_per_launch": issued / 1e12,
+                          "achieved": issued / (launch_ms * 1e-3) / 1e12,
+                          "peak": bf16_peak, "unit": "TFLOP/s",
+                          "frac": issued / (launch_ms * 1e-3) / 1e12 / bf16_peak,
+                          "useful_frac": tc_flops / (launch_ms * 1e-3) / 1e12 / bf16_peak,
+                          "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, burst)"}
 
     # ---- end to end through the API with host buffers ----------------------
     e2e = bench_e2e(torch, sss, dev, flush, args, s, p, st, dist, world)

@@ -9,7 +9,9 @@ span's conv state, its decay or the carry shows up in y, F or hT.  Cases: 2
 to 32 spans, spans shorter than a chunk and spans of several chunks, the
 conv window reaching into the previous span, states passed in place,
 grouped B/C, fp32 x and y on the scan alone, the library's choice of span
-count, a full-size 780M-like segment pair on sampled heads, argument checks.
+count, a full-size 780M-like segment pair on sampled heads, the whole
+64-segment long-context stream at 4, 8 and 16 spans on sampled heads,
+argument checks.
 """
 import numpy as np
 import pytest
@@ -134,6 +136,38 @@ def test_long_context_segments_with_spans_sampled():
         seg = synth.mixer_segment(s, i)
         y, S, h = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), A, T(seg["B"]), T(seg["C"]), w, bias,
                                 S, h, conv_state_out=S, hT=h)
+        y_ref, S_ref, h_ref = oracle.mixer_fwd(seg["x"].f64()[:, :, chan],
+                                               seg["dt"].f64()[:, :, heads], p["A"].f64()[heads],
+                                               seg["B"].f64(), seg["C"].f64(), p["w"].f64()[chan],
+                                               p["bias"].f64()[chan], S_ref, h_ref)
+        assert_y_close(f64(y[:, :, heads]), y_ref, f"segment {i} y")
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(f64(S)[:, chan], S_ref)
+    assert_rel(f64(h)[:, heads], h_ref, STATE_REL, "hT")
+
+
+@pytest.mark.parametrize("ns", [4, 8, 16])
+def test_long_context_stream_with_spans_sampled(ns):
+    """The whole 780M-like long-context stream: 64 segments of 2048 tokens
+    (batch 1, H 48, Gaussian initial states), every call cut into ns spans,
+    conv and SSM states passed in place from call to call.  y of heads 0, 23
+    and 47 in every segment, and the final states, against the oracle run
+    segment by segment on those heads' channels (the conv is depthwise and
+    the heads independent, so the sample is exact)."""
+    s = synth.WORKLOADS["m780m_128k"].with_(gaussian_init=True)
+    assert len(s.segments) == 64
+    heads = [0, 23, 47]
+    p = synth.mixer_params(s)
+    st = synth.mixer_initial_states(s)
+    A, w, bias = T(p["A"]), T(p["w"]), T(p["bias"])
+    S, h = T(st["conv_state"]), T(st["h0"])
+    chan = np.concatenate([np.arange(hh * s.P, (hh + 1) * s.P) for hh in heads])
+    S_ref = st["conv_state"].f64()[:, chan]
+    h_ref = st["h0"].f64()[:, heads]
+    for i in range(len(s.segments)):
+        seg = synth.mixer_segment(s, i)
+        y, S, h = sss.mixer_fwd(T(seg["x"]), T(seg["dt"]), A, T(seg["B"]), T(seg["C"]), w, bias,
+                                S, h, conv_state_out=S, hT=h, spans=ns)
         y_ref, S_ref, h_ref = oracle.mixer_fwd(seg["x"].f64()[:, :, chan],
                                                seg["dt"].f64()[:, :, heads], p["A"].f64()[heads],
                                                seg["B"].f64(), seg["C"].f64(), p["w"].f64()[chan],
