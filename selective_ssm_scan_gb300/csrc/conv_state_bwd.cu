@@ -395,47 +395,65 @@ conv_bwd_k4_kernel(const TX* __restrict__ x, const float* __restrict__ w,
       dS[(b * D + d0 + 1) * (K - 1) + j] = from_f32<TO>(c);
     };
     const bool last_tile = t0 + TT + 3 >= L;  // masks and the direct path from F
-#pragma unroll 1
-    for (int g = 0; g <= NG; ++g) {
+    // the group's rows from the ring (waits for them), then the refill of
+    // the stage with group g + kK4Stages (the fence orders the warp's
+    // generic reads before the async copy's writes)
+    auto take_group = [&](int g, typename PX::Raw (&xr)[4], typename PD::Raw (&gr)[4]) -> bool {
       const int st = g % kK4Stages;
       if (!mbar_wait(smem_u32(&bars[warp][st]), uint32_t((g / kK4Stages) & 1), kWaitNs)) {
         raise_status(status, SSS_ERR_TIMEOUT);
-        break;
+        return false;
       }
       const uint8_t* gs = ring + st * GB;
-      typename PX::Raw xr[4];
-      typename PD::Raw gr[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         xr[i] = *reinterpret_cast<const typename PX::Raw*>(gs + i * RX + lane * sizeof(typename PX::Raw));
         gr[i] = *reinterpret_cast<const typename PD::Raw*>(gs + 4 * RX + i * RD +
                                                            lane * sizeof(typename PD::Raw));
       }
-      // the stage is read: refill it with group g + kK4Stages (the fence
-      // orders the warp's generic reads before the async copy's writes)
       __syncwarp();
       if (lane == 0 && g + kK4Stages <= NG) {
         fence_proxy_async_smem();
         issue(g + kK4Stages);
       }
-      if (!last_tile) {
-        if (g == 0) {
+      return true;
+    };
+    if (!last_tile) {
+      // rows of dx are written through a pointer that steps one row a token
+      TO* dxr = dx + (b * L + t0) * D + d0;  // token t0
+      typename PX::Raw xr[4];
+      typename PD::Raw gr[4];
+      if (take_group(0, xr, gr)) {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          const uint64_t o = step(PX::f2(xr[i]), PD::f2(gr[i]), true);
+          if (t0 == 0) store_ds(i, o);
+        }
+        PO::store(dxr, step(PX::f2(xr[3]), PD::f2(gr[3]), true));
+        dxr += D;
+#pragma unroll 1
+        for (int g = 1; g < NG; ++g) {
+          if (!take_group(g, xr, gr)) break;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            PO::store(dxr, step(PX::f2(xr[i]), PD::f2(gr[i]), true));
+            dxr += D;
+          }
+        }
+        if (take_group(NG, xr, gr)) {
 #pragma unroll
           for (int i = 0; i < 3; ++i) {
-            const uint64_t o = step(PX::f2(xr[i]), PD::f2(gr[i]), true);
-            if (t0 == 0) store_ds(i, o);
+            PO::store(dxr, step(PX::f2(xr[i]), PD::f2(gr[i]), false));
+            dxr += D;
           }
-          store_dx(t0, step(PX::f2(xr[3]), PD::f2(gr[3]), true));
-        } else if (g < NG) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            store_dx(t0 + 4 * g + i - 3, step(PX::f2(xr[i]), PD::f2(gr[i]), true));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 3; ++i)
-            store_dx(t0 + TT + i - 3, step(PX::f2(xr[i]), PD::f2(gr[i]), false));
         }
-      } else {
+      }
+    } else {
+#pragma unroll 1
+      for (int g = 0; g <= NG; ++g) {
+        typename PX::Raw xr[4];
+        typename PD::Raw gr[4];
+        if (!take_group(g, xr, gr)) break;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int sidx = 4 * g + i;
@@ -488,6 +506,10 @@ conv_bwd_k4_kernel(const TX* __restrict__ x, const float* __restrict__ w,
 __global__ void __launch_bounds__(256)
 conv_bwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
                        float* __restrict__ dbias, int64_t rows, int D, int K) {
+  // launched as a programmatic dependent of the walk: its blocks may start
+  // while the walk's last CTAs run, and wait here until the walk's partial
+  // rows are complete and visible (a no-op in an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ float acc_s[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n = int64_t(D) * (K + 1);
@@ -594,10 +616,21 @@ static cudaError_t launch_k4(const void* x, const float* w, const float* bias, c
   cudaError_t e = silu_on ? args(conv_bwd_k4_kernel<TX, TD, TO, true>)
                           : args(conv_bwd_k4_kernel<TX, TD, TO, false>);
   if (e != cudaSuccess) return e;
+  // the fixed-order sum of the partial rows, launched so that its start
+  // overlaps the walk's tail (it waits for the walk's memory itself)
   const int64_t n = D * 5;
-  conv_bwd_reduce_kernel<<<unsigned((n + 31) / 32), 256, 0, st>>>(part, dw, dbias, Bz * groups,
-                                                                  int(D), 4);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((n + 31) / 32));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, conv_bwd_reduce_kernel, static_cast<const float*>(part), dw,
+                            dbias, int64_t(Bz * groups), int(D), 4);
 }
 
 template <typename TX, typename TD, typename TO>
