@@ -41,12 +41,14 @@ bool ssm_scan_pair_supports(sss_dtype at, int64_t L, int H, int P, int N, int G)
 cudaError_t ssm_scan_pair_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                  const void* B, const void* C, const float* h0, float* hT,
                                  void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                 int* status, const int32_t* seq_idx, cudaStream_t st);
+                                 int* status, const int32_t* seq_idx, cudaStream_t st,
+                                 bool dependent = false);
 cudaError_t mixer_fwd_pair_launch(const void* x, const float* w, const float* bias,
                                   const void* s_in, void* s_out, const void* dt, const float* A,
                                   const void* B, const void* C, const float* h0, float* hT,
                                   void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                  int K, int* status, const int32_t* seq_idx, cudaStream_t st);
+                                  int K, int* status, const int32_t* seq_idx, cudaStream_t st,
+                                  bool dependent = false);
 cudaError_t conv_state_bwd_launch(const void* x, sss_dtype xt, const float* w, const float* bias,
                                   const void* s_in, const void* dy, sss_dtype dyt, const void* q,
                                   void* dx, sss_dtype dxt, void* dS, float* dw, float* dbias,
@@ -624,15 +626,18 @@ static sss_status fwd_spans_impl(bool fused, const void* x, sss_dtype x_dtype, c
               : ssm_scan_pair_state_launch(x, x_dtype, dt, A, B, ws.hloc, rows, Ls, H, G, status,
                                            st);
   // the carry over the spans, then pass 2: every span from its true initial
-  // state, writing y
+  // state, writing y.  The three launches after the first are programmatic
+  // dependents: each starts while the one before drains and waits
+  // (griddepcontrol.wait) for its results before it reads them.
   if (e == cudaSuccess)
     e = span_combine_launch(ws.part, ws.hloc, h0_in, ws.h0s, hT_out, Bz, L, H, int64_t(P) * N, ns,
                             st);
   if (e == cudaSuccess)
     e = fused ? mixer_fwd_pair_launch(x, w, bias, ws.s_span, nullptr, dt, A, B, C, ws.h0s,
-                                      nullptr, y, y_dtype, rows, Ls, H, G, K, status, nullptr, st)
+                                      nullptr, y, y_dtype, rows, Ls, H, G, K, status, nullptr, st,
+                                      true)
               : ssm_scan_pair_launch(x, x_dtype, dt, A, B, C, ws.h0s, nullptr, y, y_dtype, rows,
-                                     Ls, H, G, status, nullptr, st);
+                                     Ls, H, G, status, nullptr, st, true);
   return from_cuda(e);
 }
 

@@ -51,6 +51,10 @@ __device__ __forceinline__ float silu(float z) {
   return __fdividef(z, 1.0f + __expf(fminf(-z, 80.0f)));
 }
 
+// Wait until the kernel this one was launched as a programmatic dependent of
+// has finished and its memory is visible (a no-op in an ordinary launch).
+__device__ __forceinline__ void dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---- packed fp32 pairs: one instruction operates on two floats (f32x2) ------
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
   uint64_t r;
@@ -79,6 +83,26 @@ __device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
 // Host helpers implemented in api.cu.
 int sm_count();        // SMs of the current device (cached per device)
 int* status_word();    // device address of the status word (current device)
+
+// Launch `kern` on `st`; with `dependent` as a programmatic dependent of the
+// kernel before it on the stream (its blocks may start while that kernel's
+// last blocks run; the kernel must execute griddepcontrol.wait, dep_wait()
+// below, before it touches memory the earlier kernel writes or reads).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dep(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t st, bool dependent, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = dependent ? attr : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
 
 inline size_t dtype_size(sss_dtype t) { return t == SSS_BF16 ? 2 : 4; }
 inline bool dtype_ok(int t) { return t == SSS_F32 || t == SSS_BF16; }

@@ -509,7 +509,7 @@ conv_bwd_reduce_kernel(const float* __restrict__ part, float* __restrict__ dw,
   // launched as a programmatic dependent of the walk: its blocks may start
   // while the walk's last CTAs run, and wait here until the walk's partial
   // rows are complete and visible (a no-op in an ordinary launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  dep_wait();
   __shared__ float acc_s[8][32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t n = int64_t(D) * (K + 1);

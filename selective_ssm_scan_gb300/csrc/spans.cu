@@ -119,6 +119,7 @@ span_combine_kernel(const float* __restrict__ part, const float* __restrict__ hl
                     const float* h0, float* __restrict__ h0_span, float* hT, int H, int PN,
                     int ns, int dec_c) {
   __shared__ float dec[32];
+  dep_wait();  // the first pass's final states are complete and visible
   const int bh = blockIdx.y, b = bh / H, h = bh % H;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int k = w; k < ns; k += kSpanThreads / 32) {
@@ -237,9 +238,8 @@ cudaError_t span_combine_launch(const float* part, const float* hloc, const floa
   const int dec_c = int((L / ns + kDecayPiece - 1) / kDecayPiece);
   const int nvec = int(PN / 4);
   const dim3 grid(unsigned((nvec + kCombineVec4 - 1) / kCombineVec4), unsigned(Bz * H));
-  span_combine_kernel<<<grid, kSpanThreads, 0, st>>>(part, hloc, h0, h0_span, hT, H, int(PN), ns,
-                                                      dec_c);
-  return cudaGetLastError();
+  return launch_dep(span_combine_kernel, grid, dim3(kSpanThreads), 0, st, true, part, hloc, h0,
+                    h0_span, hT, H, int(PN), ns, dec_c);
 }
 
 }  // namespace sss

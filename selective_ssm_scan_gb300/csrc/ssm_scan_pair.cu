@@ -301,6 +301,9 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
   const int b = blockIdx.x / npair, pair = blockIdx.x % npair;
   const int g = (2 * pair) / (H / G);
   const int64_t D = int64_t(H) * kP;
+  // launched as a dependent of the previous kernel of the span split: its
+  // outputs (conv and SSM states) are complete and visible from here on
+  dep_wait();
 
   if (warp == kIssuerWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -1052,7 +1055,8 @@ template <typename TX, typename TY, bool FUSED>
 cudaError_t launch_pair(const void* x, const void* dt, const float* A, const void* B,
                         const void* C, const float* h0, float* hT, void* y, const float* w,
                         const float* bias, const void* s_in, void* s_out, int K, int64_t Bz,
-                        int64_t L, int H, int G, int* status, const int32_t* seq_idx, cudaStream_t st) {
+                        int64_t L, int H, int G, int* status, const int32_t* seq_idx, cudaStream_t st,
+                        bool dependent = false) {
   using namespace pr;
   CUtensorMap mB, mC, mX;
   if (!make_bc_map(&mB, B, Bz, L, G, kN) || !make_bc_map(&mC, C, Bz, L, G, kN))
@@ -1068,11 +1072,10 @@ cudaError_t launch_pair(const void* x, const void* dt, const float* A, const voi
                       : ssm_scan_pair_kernel<TX, TY, FUSED, false, false>;
   cudaError_t e = prepare_pair(kern);
   if (e != cudaSuccess) return e;
-  kern<<<unsigned(Bz * (H / 2)), kThreads, kSmemBytes, st>>>(
-      mB, mC, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, h0, hT,
-      static_cast<TY*>(y), w, bias, static_cast<const TX*>(s_in), static_cast<TX*>(s_out), K,
-      int(L), H, G, status, seq_idx);
-  return cudaGetLastError();
+  return launch_dep(kern, dim3(unsigned(Bz * (H / 2))), dim3(kThreads), kSmemBytes, st, dependent,
+                    mB, mC, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt),
+                    A, h0, hT, static_cast<TY*>(y), w, bias, static_cast<const TX*>(s_in),
+                    static_cast<TX*>(s_out), K, int(L), H, G, status, seq_idx);
 }
 }  // namespace
 
@@ -1089,7 +1092,7 @@ template <typename TX, bool FUSED>
 cudaError_t launch_pair_state(const void* x, const void* dt, const float* A, const void* B,
                               float* hT, const float* w, const float* bias, const void* s_in,
                               int K, int64_t Bz, int64_t L, int H, int G, int* status,
-                              cudaStream_t st) {
+                              cudaStream_t st, bool dependent) {
   using namespace pr;
   if (Bz * (H / 2) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   CUtensorMap mB, mX;
@@ -1102,11 +1105,10 @@ cudaError_t launch_pair_state(const void* x, const void* dt, const float* A, con
   auto kern = ssm_scan_pair_kernel<TX, __nv_bfloat16, FUSED, false, true>;
   cudaError_t e = prepare_pair(kern);
   if (e != cudaSuccess) return e;
-  kern<<<unsigned(Bz * (H / 2)), kThreads, kSmemBytes, st>>>(
-      mB, mB, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt), A, nullptr,
-      hT, nullptr, w, bias, static_cast<const TX*>(s_in), nullptr, K, int(L), H, G, status,
-      nullptr);
-  return cudaGetLastError();
+  return launch_dep(kern, dim3(unsigned(Bz * (H / 2))), dim3(kThreads), kSmemBytes, st, dependent,
+                    mB, mB, mX, static_cast<const TX*>(x), static_cast<const __nv_bfloat16*>(dt),
+                    A, nullptr, hT, nullptr, w, bias, static_cast<const TX*>(s_in), nullptr, K,
+                    int(L), H, G, status, nullptr);
 }
 
 cudaError_t ssm_scan_pair_state_launch(const void* x, sss_dtype xt, const void* dt,
@@ -1114,9 +1116,9 @@ cudaError_t ssm_scan_pair_state_launch(const void* x, sss_dtype xt, const void* 
                                        int64_t L, int H, int G, int* status, cudaStream_t st) {
   if (xt == SSS_F32)
     return launch_pair_state<float, false>(x, dt, A, B, hT, nullptr, nullptr, nullptr, 1, Bz, L,
-                                           H, G, status, st);
+                                           H, G, status, st, true);
   return launch_pair_state<__nv_bfloat16, false>(x, dt, A, B, hT, nullptr, nullptr, nullptr, 1,
-                                                 Bz, L, H, G, status, st);
+                                                 Bz, L, H, G, status, st, true);
 }
 
 cudaError_t mixer_fwd_pair_state_launch(const void* x, const float* w, const float* bias,
@@ -1124,17 +1126,18 @@ cudaError_t mixer_fwd_pair_state_launch(const void* x, const float* w, const flo
                                         const void* B, float* hT, int64_t Bz, int64_t L, int H,
                                         int G, int K, int* status, cudaStream_t st) {
   return launch_pair_state<__nv_bfloat16, true>(x, dt, A, B, hT, w, bias, s_in, K, Bz, L, H, G,
-                                                status, st);
+                                                status, st, true);
 }
 
 cudaError_t ssm_scan_pair_launch(const void* x, sss_dtype xt, const void* dt, const float* A,
                                  const void* B, const void* C, const float* h0, float* hT,
                                  void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                 int* status, const int32_t* seq_idx, cudaStream_t st) {
+                                 int* status, const int32_t* seq_idx, cudaStream_t st,
+                                 bool dependent) {
   if (Bz * (H / 2) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
 #define SSS_PAIR(TXT, TYT)                                                                    \
   return launch_pair<TXT, TYT, false>(x, dt, A, B, C, h0, hT, y, nullptr, nullptr, nullptr,  \
-                                      nullptr, 1, Bz, L, H, G, status, seq_idx, st);
+                                      nullptr, 1, Bz, L, H, G, status, seq_idx, st, dependent);
   if (xt == SSS_F32 && yt == SSS_BF16) SSS_PAIR(float, __nv_bfloat16)
   if (xt == SSS_F32) SSS_PAIR(float, float)
   if (yt == SSS_BF16) SSS_PAIR(__nv_bfloat16, __nv_bfloat16)
@@ -1146,13 +1149,15 @@ cudaError_t mixer_fwd_pair_launch(const void* x, const float* w, const float* bi
                                   const void* s_in, void* s_out, const void* dt, const float* A,
                                   const void* B, const void* C, const float* h0, float* hT,
                                   void* y, sss_dtype yt, int64_t Bz, int64_t L, int H, int G,
-                                  int K, int* status, const int32_t* seq_idx, cudaStream_t st) {
+                                  int K, int* status, const int32_t* seq_idx, cudaStream_t st,
+                                  bool dependent) {
   if (Bz * (H / 2) > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   if (yt == SSS_BF16)
     return launch_pair<__nv_bfloat16, __nv_bfloat16, true>(x, dt, A, B, C, h0, hT, y, w, bias,
-                                                           s_in, s_out, K, Bz, L, H, G, status, seq_idx, st);
+                                                           s_in, s_out, K, Bz, L, H, G, status,
+                                                           seq_idx, st, dependent);
   return launch_pair<__nv_bfloat16, float, true>(x, dt, A, B, C, h0, hT, y, w, bias, s_in, s_out,
-                                                 K, Bz, L, H, G, status, seq_idx, st);
+                                                 K, Bz, L, H, G, status, seq_idx, st, dependent);
 }
 
 }  // namespace sss
