@@ -416,6 +416,7 @@ def main():
         out["train_utils"] = bench_train_utils(torch, sss, dev, stream, flush, args, hbm, s2,
                                                s2.segments[0])
         out["tiny_f32"] = bench_tiny(torch, sss, dev, stream, flush, args, hbm, hbm_kind, T)
+        out["mamba2_wiring"] = bench_mamba2(torch, sss, dev, stream, flush, args, hbm, s2)
         if not args.no_long:
             out["long_context"] = bench_long_context(torch, sss, dev, stream, flush, args, hbm,
                                                      hbm_kind)
@@ -743,6 +744,57 @@ def bench_scan_bwd(torch, sss, dev, stream, flush, args, hbm, s, Lseg):
             "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
             "tokens_per_s": tok / (ms * 1e-3),
             "kernel": "fp32 CUDA-core chunked backward (chunks of 64)"}
+
+
+def bench_mamba2(torch, sss, dev, stream, flush, args, hbm, s):
+    """sss_mamba2_mixer_fwd (the full Mamba-2 wiring) on one segment of the
+    workload's shape: bf16 xBC over D + 2GN channels, z and dt_raw, fp32
+    dt_bias, A, D_skip, conv weights and bias, Gaussian conv state (bf16) and
+    h0 (fp32); bf16 y and the final conv and SSM states out.  Two launches: the
+    conv over every xBC channel into an fp32 workspace, then the register-tiled
+    fp32 CUDA-core scan with the discretisation, skip and gate."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(7)
+    bf = torch.bfloat16
+    Bz, Ls, H, P, N, G, K = s.Bz, s.segments[0], s.H, s.P, s.N, s.G, s.K
+    D = H * P
+    Dt = D + 2 * G * N
+    xBC = torch.randn((Bz, Ls, Dt), generator=g, device=dev).to(bf)
+    z = torch.randn((Bz, Ls, D), generator=g, device=dev).to(bf)
+    dt_raw = (torch.randn((Bz, Ls, H), generator=g, device=dev) - 2.0).to(bf)
+    dt_bias = torch.rand((H,), generator=g, device=dev) - 0.5
+    A = -torch.rand((H,), generator=g, device=dev) * 0.99 - 0.01
+    D_skip = torch.rand((H,), generator=g, device=dev) + 0.5
+    w = torch.randn((Dt, K), generator=g, device=dev) * (0.5 ** 0.5)
+    bias = torch.full((Dt,), 0.1, device=dev)
+    S = torch.randn((Bz, Dt, K - 1), generator=g, device=dev).to(bf)
+    h0 = torch.randn((Bz, H, P, N), generator=g, device=dev) * 0.1
+    F = torch.empty_like(S)
+    hT = torch.empty_like(h0)
+    y = torch.empty((Bz, Ls, H, P), dtype=bf, device=dev)
+    ws = torch.empty(max(16, sss.mamba2_mixer_fwd_workspace_size(Bz, Ls, H, P, N, G)),
+                     dtype=torch.uint8, device=dev)
+
+    def call():
+        sss.mamba2_mixer_fwd(xBC, z, dt_raw, dt_bias, A, D_skip, w, bias, H, G, N,
+                             conv_state=S, h0=h0, conv_state_out=F, hT=hT, y=y, workspace=ws,
+                             stream=stream)
+
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ms = statistics.mean(events_timed(torch, stream, flush, call, max(3, args.steps // 10)))
+    byts = (Bz * Ls * (Dt * 2 + D * 2 + H * 2 + D * 2)       # xBC, z, dt_raw in; y out
+            + 2 * Bz * Dt * (K - 1) * 2                       # conv state in and out
+            + 2 * Bz * H * P * N * 4                          # h0 in, hT out
+            + Dt * (K + 1) * 4 + 3 * H * 4)                   # weights, bias, dt_bias, A, D
+    return {"workload": f"{s.name} shape, one {Ls}-token segment: Bz={Bz}, H={H}, P={P}, N={N}, "
+                        f"G={G}, K={K}, xBC over {Dt} channels, bf16, Gaussian states",
+            "avg_call_ms": ms, "launches_per_call": 2, "algorithmic_bytes_per_call": byts,
+            "achieved_gbs": byts / ms / 1e6, "frac": byts / ms / 1e6 / hbm,
+            "tokens_per_s": Bz * Ls / (ms * 1e-3),
+            "kernel": "conv_state_fwd_kernel over xBC (fp32 workspace), then "
+                      "mamba2_scan_rt_kernel (register-tiled fp32 CUDA cores)"}
 
 
 def bench_long_context(torch, sss, dev, stream, flush, args, hbm, hbm_kind):

@@ -65,7 +65,7 @@ def _check(gpu, ref, dtype):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("L", [1, 37, 130])
-@pytest.mark.parametrize("H,P,N,G", [(4, 16, 32, 2), (2, 64, 128, 1)])
+@pytest.mark.parametrize("H,P,N,G", [(4, 16, 32, 2), (2, 64, 128, 1), (2, 24, 48, 1)])
 def test_mamba2_small_parity(dtype, L, H, P, N, G):
     s = synth.WORKLOADS["m370m_2k"].with_(dtype=dtype, Bz=2, segments=(L,), H=H, P=P, N=N, G=G,
                                            gaussian_init=True, seed=2101 + L)
@@ -82,6 +82,17 @@ def test_mamba2_optional_terms(gate, skip, dt_bias, states):
     a = synth.mamba2_inputs(s)
     kw = dict(gate=gate, skip=skip, dt_bias=dt_bias, states=states)
     _check(_run_gpu(a, s, **kw), _run_ref(a, s, **kw), "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_mamba2_strong_decay_chunks(dtype):
+    """Heads whose log decay over 32 tokens passes 60 (the kernel's direct
+    form) beside ordinary heads (its scaled form), over a ragged tail."""
+    s = synth.WORKLOADS["m370m_2k"].with_(dtype=dtype, Bz=2, segments=(203,), H=4, P=64, N=128,
+                                           G=2, gaussian_init=True, seed=2151)
+    a = synth.mamba2_inputs(s)
+    a["A"] = synth.f32(np.array([-0.02, -14.0, -60.0, -1.0]))
+    _check(_run_gpu(a, s), _run_ref(a, s), dtype)
 
 
 def test_mamba2_segments_with_state_aliasing_equal_one_call():
