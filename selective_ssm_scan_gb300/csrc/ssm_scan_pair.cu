@@ -356,6 +356,9 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
     if (FUSED && tid == 0) {
       prefetch_tmap(&tmX);
       stage_x(0, 0);
+      // head b's rows of piece 0 are staged once head a's are consumed: have
+      // them in L2 by then (the 3 halo rows before token 0 come from S)
+      tma_prefetch_3d(&tmX, (2 * pair + 1) * kP, 0, b);
     }
     int xs_issued = FUSED ? 1 : 0, xs_landed = 0;
     bool ok = true;
@@ -598,23 +601,27 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
       if constexpr (!STATE) fence_proxy_async_smem();
       tc_fence_before();
     };
-    // sigma = e^{R_0} h0 (zeros without h0), then the h' tiles of piece 0
+    // sigma = h0 (zeros without h0) needs no descriptor: it goes to tensor
+    // memory while the decay warp forms piece 0; then sigma = e^{R_0} h0 and
+    // the h' tiles of piece 0
+#pragma unroll 1
+    for (int hs = 0; hs < 2; ++hs) {
+#pragma unroll 1
+      for (int q2 = 0; q2 < 2; ++q2) {
+        uint32_t w[2][16];
+#pragma unroll
+        for (int pp = 0; pp < 32; ++pp) {
+          const int pc = 32 * q2 + pp;
+          w[pp >> 4][pp & 15] =
+              __float_as_uint(h0 ? h0[hoff0 + int64_t(hs) * kP * kN + int64_t(pc) * kN + r] : 0.0f);
+        }
+        tmem_st_x16(tl + kColH + 64u * hs + 32u * q2, w[0]);
+        tmem_st_x16(tl + kColH + 64u * hs + 32u * q2 + 16u, w[1]);
+      }
+    }
+    tmem_st_wait();
     bool ok = wait_all(BAR_INFO_FULL, 0u);
     if (ok) {
-#pragma unroll 1
-      for (int hs = 0; hs < 2; ++hs) {
-#pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          uint32_t w[16];
-#pragma unroll
-          for (int pp = 0; pp < 16; ++pp) {
-            const int pc = 16 * qq + pp;
-            w[pp] = __float_as_uint(h0 ? h0[hoff0 + int64_t(hs) * kP * kN + int64_t(pc) * kN + r] : 0.0f);
-          }
-          tmem_st_x16(tl + kColH + 64u * hs + 16u * qq, w);
-        }
-      }
-      tmem_st_wait();
       rescale(1.0f, 1.0f, expf(info[0].R[0]), expf(info[0].R[1]));
       mbar_arrive(ctl.bar(BAR_H_FULL));
     }
@@ -856,6 +863,21 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
         prefetch_tmap(&tmB);
         if constexpr (!STATE) prefetch_tmap(&tmC);
         int c_issued = 0, b_issued = 0;
+        auto load_c = [&](int start) {
+          const uint32_t bar = ctl.bar(BAR_C_FULL);
+          mbar_arrive_expect_tx(bar, 32768u);
+          tma_load_3d(cb, &tmC, g * kN, start, b, bar);
+          tma_load_3d(cb + 16384, &tmC, g * kN + 64, start, b, bar);
+        };
+        auto load_b = [&](int start) {
+          const uint32_t bar = ctl.bar(BAR_B_FULL);
+          mbar_arrive_expect_tx(bar, 32768u);
+          tma_load_3d(bb, &tmB, g * kN, start, b, bar);
+          tma_load_3d(bb + 16384, &tmB, g * kN + 64, start, b, bar);
+        };
+        // piece 0 starts at token 0: its C and B go out before its descriptor
+        if constexpr (!STATE) load_c(0);
+        load_b(0);
         for (int c = 0;; ++c) {
           const int slot = c & (kSlots - 1);
           if (!ctl.wait(BAR_INFO_FULL + slot, uint32_t((c / kSlots) & 1))) break;
@@ -863,21 +885,17 @@ ssm_scan_pair_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_const
           const bool last = info[slot].last != 0;
           mbar_arrive(ctl.bar(BAR_INFO_FREE + slot));
           if constexpr (!STATE) {
-            if (c >= 1 && !ctl.wait(BAR_G_DONE, uint32_t((c - 1) & 1))) break;
-            const uint32_t bar = ctl.bar(BAR_C_FULL);
-            mbar_arrive_expect_tx(bar, 32768u);
-            tma_load_3d(cb, &tmC, g * kN, start, b, bar);
-            tma_load_3d(cb + 16384, &tmC, g * kN + 64, start, b, bar);
+            if (c >= 1) {
+              if (!ctl.wait(BAR_G_DONE, uint32_t((c - 1) & 1))) break;
+              load_c(start);
+            }
             c_issued = c + 1;
           }
-          if (c >= 1 && !ctl.wait(BAR_S_DONE, uint32_t((c - 1) & 1))) break;
-          {
-            const uint32_t bar = ctl.bar(BAR_B_FULL);
-            mbar_arrive_expect_tx(bar, 32768u);
-            tma_load_3d(bb, &tmB, g * kN, start, b, bar);
-            tma_load_3d(bb + 16384, &tmB, g * kN + 64, start, b, bar);
-            b_issued = c + 1;
+          if (c >= 1) {
+            if (!ctl.wait(BAR_S_DONE, uint32_t((c - 1) & 1))) break;
+            load_b(start);
           }
+          b_issued = c + 1;
           if (last) break;
         }
         // a load of each buffer is in flight at most: wait for the last one
