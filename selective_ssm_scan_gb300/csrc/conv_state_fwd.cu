@@ -220,7 +220,7 @@ static cudaError_t conv_dispatch_u(const void* x, const float* w, const float* b
                        (reinterpret_cast<uintptr_t>(x) % (sizeof(TX) * VEC) == 0) &&
                        (reinterpret_cast<uintptr_t>(u) % (sizeof(TU) * VEC) == 0);
   if (aligned)
-    return launch_conv<TX, TU, VEC, 8>(x, w, bias, s_in, s_out, u, Bz, L, D, K, silu_on, st);
+    return launch_conv<TX, TU, VEC, 16>(x, w, bias, s_in, s_out, u, Bz, L, D, K, silu_on, st);
   return launch_conv<TX, TU, 1, 16>(x, w, bias, s_in, s_out, u, Bz, L, D, K, silu_on, st);
 }
 
