@@ -288,6 +288,7 @@ __device__ __forceinline__ void smem_mm(int M, int Nn, const Op& o1, RS rs, cons
 #pragma unroll
       for (int q = 0; q < TN / 2; ++q) acc[r][q] = 0ull;
     auto run = [&](const Op& o) {
+#pragma unroll 8
       for (int k = 0; k < o.K; ++k) {
         uint64_t av[4], bv[TN / 2];
 #pragma unroll
