@@ -362,38 +362,49 @@ __device__ __forceinline__ void cp16(void* dst, const void* src, bool full) {
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
+// The row a lane ends the butterfly with: the levels with offsets Q/2 .. 1
+// first halve the R rows (log2 R levels), and bit `off` of the lane's group
+// index picks the upper half at each of them.  Register slot s of a lane holds
+// row s ^ m2rt_row(qi), so that at every level the half a lane keeps is in
+// slots [0, cnt) and the half it hands over in [cnt, 2 cnt).
+template <int Q, int R>
+__device__ __forceinline__ int m2rt_row(int qi) {
+  int row = 0, cnt = R;
+#pragma unroll
+  for (int off = Q / 2; off >= 1; off >>= 1)
+    if (cnt > 1) {
+      cnt >>= 1;
+      if (qi & off) row += cnt;
+    }
+  return row;
+}
+
 template <bool DIRECT, int N, int Q, int R, int PB>
 __device__ __forceinline__ void m2rt_tokens(float (&st)[R][N / Q], const float* bs,
                                             const float* cs, const float* cf, float* ys,
                                             const float* lm, int nt, int pl0, int qi) {
   constexpr int M = N / Q;
-  // the butterfly's row of this lane and whether it writes it: levels with
-  // offsets Q/2 .. 1 first halve the R rows (log2 R levels), then add
-  int row = 0, wmask = 0;
+  const int row = m2rt_row<Q, R>(qi);
+  int wmask = 0;  // the levels past the halving add; their lanes hold copies
   {
     int cnt = R;
 #pragma unroll
     for (int off = Q / 2; off >= 1; off >>= 1) {
-      if (cnt > 1) {
+      if (cnt > 1)
         cnt >>= 1;
-        if (qi & off) row += cnt;
-      } else {
+      else
         wmask |= off;
-      }
     }
   }
 #pragma unroll 2
   for (int tt = 0; tt < nt; ++tt) {
     float cv8[R];
 #pragma unroll
-    for (int r4 = 0; r4 < R / 4; ++r4) {
-      const float4 f = *reinterpret_cast<const float4*>(cf + tt * PB + pl0 + 4 * r4);
-      cv8[4 * r4] = f.x; cv8[4 * r4 + 1] = f.y; cv8[4 * r4 + 2] = f.z; cv8[4 * r4 + 3] = f.w;
-    }
+    for (int r = 0; r < R; ++r) cv8[r] = cf[tt * PB + pl0 + (r ^ row)];
     const float m = DIRECT ? lm[tt] : 1.0f;
-    float a[R][2];
+    float a[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) a[r][0] = a[r][1] = 0.0f;
+    for (int r = 0; r < R; ++r) a[r] = 0.0f;
 #pragma unroll
     for (int k = 0; k < M / 4; ++k) {
       const float4 b4 = *reinterpret_cast<const float4*>(bs + tt * N + 4 * qi + 4 * Q * k);
@@ -406,28 +417,22 @@ __device__ __forceinline__ void m2rt_tokens(float (&st)[R][N / Q], const float* 
         for (int r = 0; r < R; ++r) {
           float& s = st[r][4 * k + e];
           s = DIRECT ? fmaf(cv8[r], bv[e], m * s) : fmaf(cv8[r], bv[e], s);
-          a[r][e & 1] = fmaf(cv[e], s, a[r][e & 1]);
+          a[r] = fmaf(cv[e], s, a[r]);
         }
     }
-    float v[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) v[r] = a[r][0] + a[r][1];
     int cnt = R;
 #pragma unroll
     for (int off = Q / 2; off >= 1; off >>= 1) {
-      const bool hi = (qi & off) != 0;
       if (cnt > 1) {
         cnt >>= 1;
 #pragma unroll
         for (int i = 0; i < R / 2; ++i)
-          if (i < cnt)
-            v[i] = (hi ? v[cnt + i] : v[i]) +
-                   __shfl_xor_sync(0xffffffffu, hi ? v[i] : v[cnt + i], off);
+          if (i < cnt) a[i] += __shfl_xor_sync(0xffffffffu, a[cnt + i], off);
       } else {
-        v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+        a[0] += __shfl_xor_sync(0xffffffffu, a[0], off);
       }
     }
-    if ((qi & wmask) == 0) ys[tt * PB + pl0 + row] = v[0];
+    if ((qi & wmask) == 0) ys[tt * PB + pl0 + row] = a[0];
   }
 }
 }  // namespace
@@ -455,6 +460,7 @@ mamba2_scan_rt_kernel(const float* __restrict__ u, const TA* __restrict__ z,
   const int g = h / (H / G);
   const int p0 = int(blockIdx.y) * PB;
   const int pl0 = (warp * (32 / Q) + lane / Q) * R;  // this group's first row, CTA-local
+  const int prow = m2rt_row<Q, R>(qi);  // register slot r holds row pl0 + (r ^ prow)
   const float Ah = A[h];
   const float bias_h = dt_bias ? dt_bias[h] : 0.0f;
   const float Dh = D_skip ? D_skip[h] : 0.0f;
@@ -497,7 +503,7 @@ mamba2_scan_rt_kernel(const float* __restrict__ u, const TA* __restrict__ z,
 #pragma unroll
     for (int i = 0; i < M; ++i) {
       const int n = 4 * qi + 4 * Q * (i >> 2) + (i & 3);
-      st[r][i] = h0 ? h0[((int64_t(b) * H + h) * P + p0 + pl0 + r) * N + n] : 0.0f;
+      st[r][i] = h0 ? h0[((int64_t(b) * H + h) * P + p0 + pl0 + (r ^ prow)) * N + n] : 0.0f;
     }
 
   stage(0);
@@ -573,7 +579,7 @@ mamba2_scan_rt_kernel(const float* __restrict__ u, const TA* __restrict__ z,
 #pragma unroll
       for (int i = 0; i < M; ++i) {
         const int n = 4 * qi + 4 * Q * (i >> 2) + (i & 3);
-        hT[((int64_t(b) * H + h) * P + p0 + pl0 + r) * N + n] = st[r][i];
+        hT[((int64_t(b) * H + h) * P + p0 + pl0 + (r ^ prow)) * N + n] = st[r][i];
       }
   }
 }
