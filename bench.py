@@ -444,6 +444,24 @@ def main():
         dist.destroy_process_group()
 
 
+def gpu_local_cpus(torch, dev):
+    """The CPUs of the GPU's own NUMA node (the sysfs local_cpulist of its PCI
+    function) that this process may run on, or None when that is unknown."""
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        addr = "%04x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        with open(f"/sys/bus/pci/devices/{addr}/local_cpulist") as f:
+            text = f.read().strip()
+        cpus = set()
+        for part in text.split(","):
+            a, _, b = part.partition("-")
+            cpus.update(range(int(a), int(b or a) + 1))
+        cpus &= os.sched_getaffinity(0)
+        return cpus or None
+    except (OSError, ValueError, AttributeError):
+        return None
+
+
 def bench_e2e(torch, sss, dev, flush, args, s, p, st, dist, world):
     """The headline step end to end through the public API: every step copies
     its inputs from pinned host memory to the device and y plus the final
@@ -460,14 +478,26 @@ def bench_e2e(torch, sss, dev, flush, args, s, p, st, dist, world):
             t = torch.from_numpy(a.data)
         return torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)
 
-    host = {k: pinned(v) for k, v in seg.items()}
-    hS0, hh0 = pinned(st["conv_state"]), pinned(st["h0"])
+    # the pinned buffers are allocated and first touched from the GPU's own
+    # NUMA node, so the copies do not cross between host memory nodes
+    local = gpu_local_cpus(torch, dev)
+    saved = os.sched_getaffinity(0)
+    if local:
+        os.sched_setaffinity(0, local)
+    try:
+        host = {k: pinned(v) for k, v in seg.items()}
+        hS0, hh0 = pinned(st["conv_state"]), pinned(st["h0"])
+        hy = torch.empty((s.Bz, L, s.H, s.P), dtype=bf, pin_memory=True)
+        hF = torch.empty(hS0.shape, dtype=hS0.dtype, pin_memory=True)
+        hhT = torch.empty(hh0.shape, dtype=hh0.dtype, pin_memory=True)
+        hy.zero_()
+        hF.zero_()
+        hhT.zero_()
+    finally:
+        os.sched_setaffinity(0, saved)
     A = torch.from_numpy(p["A"].data).to(dev)
     w = torch.from_numpy(p["w"].data).to(dev)
     bias = torch.from_numpy(p["bias"].data).to(dev)
-    hy = torch.empty((s.Bz, L, s.H, s.P), dtype=bf, pin_memory=True)
-    hF = torch.empty(hS0.shape, dtype=hS0.dtype, pin_memory=True)
-    hhT = torch.empty(hh0.shape, dtype=hh0.dtype, pin_memory=True)
     dev_in = {k: torch.empty(v.shape, dtype=v.dtype, device=dev) for k, v in host.items()}
     dS0 = torch.empty(hS0.shape, dtype=hS0.dtype, device=dev)
     dh0 = torch.empty(hh0.shape, dtype=hh0.dtype, device=dev)
@@ -525,7 +555,9 @@ def bench_e2e(torch, sss, dev, flush, args, s, p, st, dist, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": total / e2e_steps,
             "path": f"sss_mixer_fwd per batch row on {nstreams} streams, pinned host buffers, "
-                    "copies in and out inside the timed region"}
+                    "copies in and out inside the timed region",
+            "host_buffers": ("allocated from the GPU's NUMA node (CPUs %d-%d)" % (min(local), max(local))
+                             if local else "allocated without a NUMA binding (node unknown)")}
 
 
 def bench_segments(torch, sss, dev, stream, flush, args, hbm, hbm_kind, T):
