@@ -311,15 +311,16 @@ __host__ inline PipeGeom pipe_geom(int P, int S_len, int L_new, int K, int esz, 
 }
 
 // shared memory after the ring
+constexpr int kPipeMaxGroups = 2;
 struct PipeMisc {
-  float us[kPipeMaxLnew][kPipeMaxP];  // conv outputs of the current item
+  float us[kPipeMaxGroups][kPipeMaxLnew][kPipeMaxP];  // conv outputs of each group's item
   float a[kPipeMaxStages][kPipeMaxLnew];  // decays exp(dt A_h) of the stage's item
   uint64_t full[kPipeMaxStages];      // stage landed
   uint64_t done[kPipeMaxStages];      // compute finished with the stage
   int valid[kPipeMaxStages];
   int p0[kPipeMaxStages];
   int row[kPipeMaxStages];
-  int go;
+  int go[kPipeMaxGroups];
   int abort;
 };
 
@@ -524,28 +525,31 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
   }
 
   // ------------------------------ compute ------------------------------
-  int64_t b = b_first;
-  int h = h_first - 1;
-  for (int k = 0; k < n; ++k) {
+  // With up to four new tokens the compute warps form two groups of four that
+  // take alternate items, so one item's barriers and shuffle chains overlap
+  // the other's arithmetic; group g syncs on named barrier 1 + g.
+  constexpr int CG = LT <= 4 ? 2 : 1;
+  constexpr int GW = kPipeWarps / CG;  // warps per group
+  constexpr int RPG = RP * CG;         // state rows per warp of a group
+  const int grp = warp / GW, gwarp = warp % GW, gtid = tid % (GW * 32);
+  for (int k = grp; k < n; k += CG) {
     const int s = k % stages;
-    if (++h == H) {
-      h = 0;
-      ++b;
-    }
-    if (tid == 0)
-      ms->go = pipe_wait(tc::smem_u32(&ms->full[s]), uint32_t((k / stages) & 1), abort_flag,
-                         status) ? 1 : 0;
-    tc::role_sync(1, kPipeWarps * 32);
-    if (!ms->go) return;
+    const int64_t b = b_first + (h_first + k) / H;
+    const int h = (h_first + k) % H;
+    if (gtid == 0)
+      ms->go[grp] = pipe_wait(tc::smem_u32(&ms->full[s]), uint32_t((k / stages) & 1), abort_flag,
+                              status) ? 1 : 0;
+    tc::role_sync(1 + grp, GW * 32);
+    if (!ms->go[grp]) return;
     const int valid = ms->valid[s];
     const int p0 = ms->p0[s];
     uint8_t* stg = ring + size_t(s) * geo.stage;
     if (!valid) {
-      for (int i = tid; i < L_new * P; i += kPipeWarps * 32) {
+      for (int i = gtid; i < L_new * P; i += GW * 32) {
         const int tt = i / P, pp = i % P;
         y[((b * L_new + tt) * H + h) * P + pp] = from_f32<T>(0.0f);
       }
-      if (tid == 0) raise_status(status, SSS_ERR_INDEX);
+      if (gtid == 0) raise_status(status, SSS_ERR_INDEX);
     } else {
       // ---- conv over the slot tile: one (token i, channel c) per thread, so
       // the L_new tokens' convs run side by side.  Every read is of the
@@ -555,7 +559,7 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
         const T* xs = reinterpret_cast<const T*>(stg + geo.xs);
         const T* tile = reinterpret_cast<const T*>(stg + geo.cv);
         const int base = p0 % S_len;  // slot of logical position p0
-        for (int e = tid; e < L_new * P; e += kPipeWarps * 32) {
+        for (int e = gtid; e < L_new * P; e += GW * 32) {
           const int i = e / P, c = e - (e / P) * P;
           const T* row = tile + c * S_len;
           const float* wr = reinterpret_cast<const float*>(stg + geo.ws) + c * K;
@@ -578,7 +582,7 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
             }
           }
           z = fmaf(wr[K - 1], to_f32(xs[i * P + c]), z);
-          ms->us[i][c] = silu(z);
+          ms->us[grp][i][c] = silu(z);
           // the new input goes to the pool row: at the write pointer, or
           // (non-circular) the row shifted by L_new with the inputs appended
           T* grow = conv_pool + (int64_t(ms->row[s]) * D + int64_t(h) * P + c) * S_len;
@@ -587,7 +591,7 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
           if (seqlens && i + S_len >= L_new) grow[(base + i) % S_len] = xs[i * P + c];
         }
         if (!seqlens) {
-          for (int e = tid; e < S_len * P; e += kPipeWarps * 32) {
+          for (int e = gtid; e < S_len * P; e += GW * 32) {
             const int j = e / P, c = e - (e / P) * P;
             const T* row = tile + c * S_len;
             T* grow = conv_pool + (int64_t(ms->row[s]) * D + int64_t(h) * P + c) * S_len;
@@ -595,7 +599,7 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
           }
         }
       }
-      tc::role_sync(1, kPipeWarps * 32);
+      tc::role_sync(1 + grp, GW * 32);
 
       // ---- recurrence on the state block, in place
       const T* bsm = reinterpret_cast<const T*>(stg + geo.bs);
@@ -620,10 +624,10 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
         c01[i] = pk2(cv.x, cv.y);
         c23[i] = pk2(cv.z, cv.w);
       }
-      float part[LT][RP];
+      float part[LT][RPG];
 #pragma unroll
-      for (int rr = 0; rr < RP; ++rr) {
-        const int p = warp + kPipeWarps * rr;
+      for (int rr = 0; rr < RPG; ++rr) {
+        const int p = gwarp + GW * rr;
 #pragma unroll
         for (int i = 0; i < LT; ++i) part[i][rr] = 0.0f;
         if (p < P) {
@@ -633,7 +637,7 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
           for (int i = 0; i < LT; ++i) {
             if (i < L_new) {
               // h = a h + u B (columns in pairs), then this lane's part of h C
-              const float u = ms->us[i][p];
+              const float u = ms->us[grp][i][p];
               const uint64_t u2 = pk2(u, u);
               h01 = fma2(av2[i], h01, mul2(u2, b01[i]));
               h23 = fma2(av2[i], h23, mul2(u2, b23[i]));
@@ -652,15 +656,15 @@ mixer_update_pipe_kernel(const T* __restrict__ x, const float* __restrict__ w,
       for (int i = 0; i < LT; ++i) {
         if (i < L_new) {
           int rsel;
-          const float yv = upd_reduce_scatter<RP>(part[i], lane, &rsel);
-          const int p = warp + kPipeWarps * rsel;
-          if ((lane & (32 / RP - 1)) == 0 && p < P)
+          const float yv = upd_reduce_scatter<RPG>(part[i], lane, &rsel);
+          const int p = gwarp + GW * rsel;
+          if ((lane & (32 / RPG - 1)) == 0 && p < P)
             y[((b * L_new + i) * H + h) * P + p] = from_f32<T>(yv);
         }
       }
     }
-    tc::role_sync(1, kPipeWarps * 32);
-    if (tid == 0) tc::mbar_arrive(tc::smem_u32(&ms->done[s]));
+    tc::role_sync(1 + grp, GW * 32);
+    if (gtid == 0) tc::mbar_arrive(tc::smem_u32(&ms->done[s]));
   }
 }
 
